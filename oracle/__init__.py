@@ -1,0 +1,119 @@
+"""fp64 CPU oracle for the attention forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and this
+package imports nothing from the library: the two share no code.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, one score row at a
+time, full-row softmax).  This module builds it with the host C compiler,
+loads it with ctypes and marshals numpy arrays.  See the C file's header for
+the definition and the page sections it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(mutant: int = 0, out_path: str | None = None) -> str:
+    """Compile the oracle (or a variant with a planted mistake) to a shared object.
+
+    ``mutant`` 0 is the oracle itself; 1..8 each plant one known mistake and
+    exist only so the tests can show that the pins catch it.
+    """
+    if out_path is None:
+        out_path = _LIB_PATH if mutant == 0 else os.path.join(
+            tempfile.mkdtemp(prefix="oracle_mut"), f"liboracle_m{mutant}.so")
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def _bind(lib):
+    f = lib.oracle_attention
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int,
+                                   ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int]
+    lib.oracle_mutant_id.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load the oracle shared object (building it first if it is missing or stale)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        if (not os.path.exists(_LIB_PATH)
+                or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+            build()
+        _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float64)
+    return np.ascontiguousarray(a)
+
+
+def attention(q, k, v, scale: float, causal: bool = False, mask=None,
+              mask_kind: int = 0, rows=None, n_threads: int | None = None,
+              lib=None):
+    """O and L of softmax(scale * q k^T + mask) v in fp64.
+
+    q: [B, H_q, qL, D]; k, v: [B, H_kv, kL, D] (any real dtype; widened to
+    fp64 exactly).  mask: None, or [B, H_q, qL, kL] -- bool/uint8 with
+    nonzero = keep (mask_kind 1) or additive real values (mask_kind 2).
+    ``scale`` is used as given (pass the fp32-rounded value the GPU sees).
+    rows: optional iterable of flat row indices (b*H_q + h)*qL + i.
+    Returns (O, L): O [B,H_q,qL,D] and L [B,H_q,qL], or [n,D] and [n] for rows.
+    """
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, qL, D = q.shape
+    Bk, Hkv, kL, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape:
+        raise ValueError("shape mismatch between q, k and v")
+    mptr = None
+    if mask_kind == 1:
+        mask = np.ascontiguousarray(np.broadcast_to(np.asarray(mask) != 0, (B, Hq, qL, kL)).astype(np.uint8))
+        mptr = mask.ctypes.data
+    elif mask_kind == 2:
+        mask = _f64(np.broadcast_to(np.asarray(mask, dtype=np.float64), (B, Hq, qL, kL)))
+        mptr = mask.ctypes.data
+    elif mask_kind != 0:
+        raise ValueError("mask_kind must be 0, 1 or 2")
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(np.asarray(list(rows), dtype=np.int64))
+        n = int(rows_arr.size)
+        o = np.empty((n, D), dtype=np.float64)
+        lse = np.empty((n,), dtype=np.float64)
+        rptr = rows_arr.ctypes.data
+    else:
+        rows_arr = None
+        n = 0
+        o = np.empty((B, Hq, qL, D), dtype=np.float64)
+        lse = np.empty((B, Hq, qL), dtype=np.float64)
+        rptr = None
+    if n_threads is None:
+        n_threads = os.cpu_count() or 1
+    rc = lib.oracle_attention(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr,
+                              int(mask_kind), o.ctypes.data, lse.ctypes.data,
+                              B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)),
+                              rptr, n, int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_attention rejected its arguments")
+    return o, lse

@@ -1,0 +1,120 @@
+"""Seeded synthetic inputs shared by the parity tests, the smoke check and the bench.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic.  Both the fp64 oracle and the CUDA library consume what
+it produces, so it imports neither of them.
+
+Recipe (same for every workload): a CPU ``torch.Generator`` seeded with
+``seed`` draws Q, K, V in that order as fp32 N(0, 1), which are then cast to
+the workload's I/O dtype.  Masks use their own generator (``mask_seed``):
+  additive  -- N(0, 1) cast to the I/O dtype, then Bernoulli(0.1) entries set
+               to -inf, with the diagonal left finite so no row is empty;
+  bool      -- Bernoulli(0.9) keep, with the diagonal forced to keep.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+MASK_NONE, MASK_BOOL, MASK_ADDITIVE = 0, 1, 2
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H_q: int
+    H_kv: int
+    qL: int
+    kL: int
+    D: int
+    dtype: str            # "bf16" or "f32"
+    causal: bool = False
+    mask_kind: int = MASK_NONE
+    layout: str = "bhsd"  # "bhsd", or "dit": O written token-major [seq, H*D]
+    seed: int = 1000
+    mask_seed: int = 2000
+    scale: float = field(default=float("nan"))
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.D) if math.isnan(self.scale) else self.scale
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def flops(self) -> float:
+        """Algorithmic FLOP: 4*B*H_q*qL*kL*D, halved when causal."""
+        f = 4.0 * self.B * self.H_q * self.qL * self.kL * self.D
+        return f / 2.0 if self.causal else f
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# The five workloads of the pages (FA-2 forward on one GPU).
+WORKLOADS = {
+    "fp32_b1_h2_l128_d64": Workload("fp32_b1_h2_l128_d64", 1, 2, 2, 128, 128, 64, "f32", seed=1000),
+    "bf16_causal_b4_h8_l1024_d64": Workload("bf16_causal_b4_h8_l1024_d64", 4, 8, 8, 1024, 1024, 64,
+                                            "bf16", causal=True, seed=1001),
+    "bf16_gqa_causal_b2_hq32_hkv8_l4096_d128": Workload(
+        "bf16_gqa_causal_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "bf16",
+        causal=True, seed=1002),
+    "fp32_dit_h24_l4608_d128_tokenmajor": Workload(
+        "fp32_dit_h24_l4608_d128_tokenmajor", 1, 24, 24, 4608, 4608, 128, "f32",
+        layout="dit", seed=1003),
+    "bf16_additive_mask_h8_l2000_d256": Workload(
+        "bf16_additive_mask_h8_l2000_d256", 1, 8, 8, 2000, 2000, 256, "bf16",
+        mask_kind=MASK_ADDITIVE, seed=1004),
+    "bf16_bool_mask_h8_l2000_d256": Workload(
+        "bf16_bool_mask_h8_l2000_d256", 1, 8, 8, 2000, 2000, 256, "bf16",
+        mask_kind=MASK_BOOL, seed=1004),
+}
+
+BENCH_WORKLOAD = "bf16_gqa_causal_b2_hq32_hkv8_l4096_d128"
+
+
+def make_qkv(w: Workload):
+    """Q [B,H_q,qL,D], K and V [B,H_kv,kL,D] on the CPU in the I/O dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    q = torch.randn(w.B, w.H_q, w.qL, w.D, generator=g, dtype=torch.float32)
+    k = torch.randn(w.B, w.H_kv, w.kL, w.D, generator=g, dtype=torch.float32)
+    v = torch.randn(w.B, w.H_kv, w.kL, w.D, generator=g, dtype=torch.float32)
+    dt = w.torch_dtype
+    return q.to(dt), k.to(dt), v.to(dt)
+
+
+def make_mask(w: Workload):
+    """The workload's mask on the CPU: None, uint8 keep-mask, or additive in the I/O dtype."""
+    if w.mask_kind == MASK_NONE:
+        return None
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.mask_seed)
+    shape = (w.B, w.H_q, w.qL, w.kL)
+    n = min(w.qL, w.kL)
+    idx = torch.arange(n)
+    if w.mask_kind == MASK_ADDITIVE:
+        vals = torch.randn(*shape, generator=g, dtype=torch.float32).to(w.torch_dtype)
+        drop = torch.rand(*shape, generator=g) < 0.1
+        drop[..., idx, idx] = False
+        vals[drop] = float("-inf")
+        return vals
+    keep = torch.rand(*shape, generator=g) < 0.9
+    keep[..., idx, idx] = True
+    return keep.to(torch.uint8)
+
+
+def make_inputs(w: Workload):
+    q, k, v = make_qkv(w)
+    return q, k, v, make_mask(w)
+
+
+def small_case(name, B, H_q, H_kv, qL, kL, D, dtype, causal=False, mask_kind=MASK_NONE,
+               layout="bhsd", seed=7, scale=float("nan")) -> Workload:
+    """A reduced-size workload for element-by-element parity runs."""
+    return Workload(name, B, H_q, H_kv, qL, kL, D, dtype, causal=causal, mask_kind=mask_kind,
+                    layout=layout, seed=seed, mask_seed=seed + 1000, scale=scale)
