@@ -1,0 +1,332 @@
+// fa_api.cu -- the C ABI (include/fa.h): argument validation, instantiation
+// choice, the per-device status word, and error reporting.
+//
+// Validation follows mlx-native "ops/flash_attn_train.rs" (`validate_params`:
+// every size positive, H_q divisible by H_kv; `dispatch_inner`: head_dim
+// checked against the supported set and dtypes checked before dispatch),
+// extended with the TMA alignment rules of this library.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_launch.cuh"
+
+namespace fa {
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+// One status word per device (a static device variable: nothing is allocated).
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
+int g_num_sms[kMaxDevices] = {0};
+long long g_timeout_cycles = 0;  // 0: not yet initialised
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+constexpr long long kDefaultTimeout = 1LL << 31;
+
+long long timeout_cycles() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_timeout_cycles == 0) {
+    g_timeout_cycles = kDefaultTimeout;
+    if (const char* s = std::getenv("FA_TIMEOUT_CYCLES")) {
+      long long v = std::atoll(s);
+      if (v > 0) g_timeout_cycles = v;
+    }
+  }
+  return g_timeout_cycles;
+}
+
+// Per-device set-up with that device current: status word address, SM count.
+int device_setup(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal %d is out of range", dev);
+    return FA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_status_ptr[dev]) return FA_OK;
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_status_word);
+  if (e != cudaSuccess) {
+    set_error("cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    set_error("cudaDeviceGetAttribute(SM count): %s", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+  }
+  g_num_sms[dev] = sms;
+  g_status_ptr[dev] = static_cast<unsigned int*>(ptr);
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bytes of a stride that TMA will use (extent-1 dimensions are never stepped).
+bool stride_ok(long long elems, int extent, int esz) {
+  if (extent <= 1) return true;
+  const long long bytes = elems * esz;
+  return bytes > 0 && (bytes % 16) == 0 && bytes < (1LL << 40);
+}
+
+int validate(const fa_fwd_args* a) {
+  if (!a) {
+    set_error("args is NULL");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (!a->q || !a->k || !a->v || !a->o || !a->lse) {
+    set_error("q, k, v, o and lse must all be non-NULL");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->B <= 0 || a->H_q <= 0 || a->H_kv <= 0 || a->qL <= 0 || a->kL <= 0) {
+    set_error("B (%d), H_q (%d), H_kv (%d), qL (%d) and kL (%d) must be > 0", a->B, a->H_q, a->H_kv, a->qL,
+              a->kL);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->H_q % a->H_kv != 0) {
+    set_error("H_q (%d) must be divisible by H_kv (%d)", a->H_q, a->H_kv);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->dtype != FA_DTYPE_F32 && a->dtype != FA_DTYPE_BF16) {
+    set_error("dtype %d is not FA_DTYPE_F32 (0) or FA_DTYPE_BF16 (1)", a->dtype);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->mask_kind < FA_MASK_NONE || a->mask_kind > FA_MASK_ADDITIVE) {
+    set_error("mask_kind %d is not 0 (none), 1 (bool) or 2 (additive)", a->mask_kind);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if ((a->mask_kind != FA_MASK_NONE) != (a->mask != nullptr)) {
+    set_error("mask must be non-NULL exactly when mask_kind != 0 (mask_kind %d, mask %p)", a->mask_kind, a->mask);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (!std::isfinite(a->scale)) {
+    set_error("scale must be finite");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->D != 64 && a->D != 128 && a->D != 256) {
+    set_error("head dim D = %d is not supported (64, 128 or 256)", a->D);
+    return FA_ERR_UNSUPPORTED;
+  }
+  const int esz = a->dtype == FA_DTYPE_F32 ? 4 : 2;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o)) {
+    set_error("q, k, v and o must be 16-byte aligned");
+    return FA_ERR_MISALIGNED;
+  }
+  if ((reinterpret_cast<uintptr_t>(a->lse) & 3u) != 0) {
+    set_error("lse must be 4-byte aligned");
+    return FA_ERR_MISALIGNED;
+  }
+  struct {
+    const long long* s;
+    int H, L;
+    const char* name;
+  } views[4] = {{a->q_strides, a->H_q, a->qL, "q"},
+                {a->k_strides, a->H_kv, a->kL, "k"},
+                {a->v_strides, a->H_kv, a->kL, "v"},
+                {a->o_strides, a->H_q, a->qL, "o"}};
+  for (auto& w : views) {
+    if (!stride_ok(w.s[0], a->B, esz) || !stride_ok(w.s[1], w.H, esz) || !stride_ok(w.s[2], w.L, esz)) {
+      set_error("%s strides {%lld, %lld, %lld} (elements) must be positive multiples of 16 bytes", w.name,
+                w.s[0], w.s[1], w.s[2]);
+      return FA_ERR_MISALIGNED;
+    }
+    if (w.s[2] < a->D && w.L > 1) {
+      set_error("%s row stride %lld is smaller than D = %d", w.name, w.s[2], a->D);
+      return FA_ERR_INVALID_ARGUMENT;
+    }
+  }
+  if (a->mask_kind != FA_MASK_NONE) {
+    for (int i = 0; i < 3; ++i)
+      if (a->mask_strides[i] < 0) {
+        set_error("mask strides must be >= 0");
+        return FA_ERR_INVALID_ARGUMENT;
+      }
+  }
+  // Work units and flat L indices must fit the kernel's int32 arithmetic.
+  if ((long long)a->B * a->H_q * a->qL > 0x7fffffffLL) {
+    set_error("B * H_q * qL = %lld exceeds 2^31 - 1", (long long)a->B * a->H_q * a->qL);
+    return FA_ERR_UNSUPPORTED;
+  }
+  return FA_OK;
+}
+
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+EncodeTiledFn get_encode_tiled() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd_ex(const fa_fwd_args* a) {
+  using namespace fa;
+  g_err[0] = '\0';
+  int rc = validate(a);
+  if (rc != FA_OK) return rc;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+  }
+  rc = device_setup(dev);
+  if (rc != FA_OK) return rc;
+
+  LaunchArgs la;
+  la.q = a->q;
+  la.k = a->k;
+  la.v = a->v;
+  la.o = a->o;
+  la.lse = a->lse;
+  la.mask = a->mask;
+  la.B = a->B;
+  la.Hq = a->H_q;
+  la.Hkv = a->H_kv;
+  la.qL = a->qL;
+  la.kL = a->kL;
+  la.D = a->D;
+  la.scale = a->scale;
+  la.causal = a->causal ? 1 : 0;
+  la.mask_kind = a->mask_kind;
+  for (int i = 0; i < 3; ++i) {
+    la.qs[i] = a->q_strides[i];
+    la.ks[i] = a->k_strides[i];
+    la.vs[i] = a->v_strides[i];
+    la.os[i] = a->o_strides[i];
+    la.ms[i] = a->mask_kind ? a->mask_strides[i] : 0;
+  }
+  la.mask_vec = 0;
+  if (a->mask_kind != FA_MASK_NONE) {
+    const int mesz = (a->mask_kind == FA_MASK_BOOL) ? 1 : (a->dtype == FA_DTYPE_F32 ? 4 : 2);
+    bool vec = aligned16(a->mask);
+    for (int i = 0; i < 3; ++i) vec = vec && ((la.ms[i] * mesz) % 16 == 0);
+    la.mask_vec = vec ? 1 : 0;
+  }
+  la.stream = static_cast<cudaStream_t>(a->stream);
+  la.status = g_status_ptr[dev];
+  la.timeout_cycles = timeout_cycles();
+  la.num_sms = g_num_sms[dev];
+
+  const bool f32 = a->dtype == FA_DTYPE_F32;
+  switch (a->D) {
+    case 64: rc = f32 ? launch_f32_d64(la) : launch_bf16_d64(la); break;
+    case 128: rc = f32 ? launch_f32_d128(la) : launch_bf16_d128(la); break;
+    default: rc = f32 ? launch_f32_d256(la) : launch_bf16_d256(la); break;
+  }
+  return rc;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q, int H_kv, int qL,
+           int kL, int D, float scale, int causal, const void* mask, int mask_kind, int dtype, void* stream) {
+  fa_fwd_args a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.mask = mask;
+  a.B = B;
+  a.H_q = H_q;
+  a.H_kv = H_kv;
+  a.qL = qL;
+  a.kL = kL;
+  a.D = D;
+  a.scale = scale;
+  a.causal = causal;
+  a.mask_kind = mask_kind;
+  a.dtype = dtype;
+  const long long Dl = D;
+  a.q_strides[0] = (long long)H_q * qL * Dl;
+  a.q_strides[1] = (long long)qL * Dl;
+  a.q_strides[2] = Dl;
+  a.o_strides[0] = a.q_strides[0];
+  a.o_strides[1] = a.q_strides[1];
+  a.o_strides[2] = a.q_strides[2];
+  a.k_strides[0] = (long long)H_kv * kL * Dl;
+  a.k_strides[1] = (long long)kL * Dl;
+  a.k_strides[2] = Dl;
+  a.v_strides[0] = a.k_strides[0];
+  a.v_strides[1] = a.k_strides[1];
+  a.v_strides[2] = a.k_strides[2];
+  a.mask_strides[0] = (long long)H_q * qL * kL;
+  a.mask_strides[1] = (long long)qL * kL;
+  a.mask_strides[2] = kL;
+  a.stream = stream;
+  return fa_fwd_ex(&a);
+}
+
+const char* fa_last_error(void) { return fa::g_err; }
+
+int fa_sync_status(void* stream) {
+  using namespace fa;
+  g_err[0] = '\0';
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_error("stream synchronise: %s", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+  }
+  int rc = device_setup(dev);
+  if (rc != FA_OK) return rc;
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, g_status_ptr[dev], sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpy(g_status_ptr[dev], &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    set_error("status word read: %s", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+  }
+  if (word & kStatusTimeout) {
+    set_error("a forward kernel reached its wait bound and stopped early (status 0x%x)", word);
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+void fa_set_timeout_cycles(long long cycles) {
+  std::lock_guard<std::mutex> lk(fa::g_mu);
+  fa::g_timeout_cycles = cycles > 0 ? cycles : fa::kDefaultTimeout;
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

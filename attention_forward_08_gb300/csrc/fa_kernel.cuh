@@ -1,0 +1,656 @@
+// fa_kernel.cuh -- FlashAttention-2 forward for sm_103a: TMA-fed shared-memory
+// rings, tcgen05 MMAs accumulating in tensor memory (TMEM), and one softmax
+// warpgroup per 128-row query tile (TMEM lane i = query row i).
+//
+// What it computes (per batch b, query head h, query row i):
+//   O_i = softmax_j(scale * q_i . k_j + mask_ij) v_j,  L_i = m_i + ln(l_i)
+// with causal (j <= i) masking, GQA (K/V head = h / (H_q / H_kv)), optional
+// bool (nonzero keeps) or additive masks, and ragged tails.  Sources:
+//  - mlx-native "ops/flash_attn_train.rs", module doc "Algorithm": FA-2
+//    online softmax with the score pre-scaled by scale*log2(e) so the running
+//    max and sum live in base 2, and L = m2 * ln2 + ln(l2) written per row;
+//    "Buffer layout" ([B,H_q,qL,D] Q/O, [B,H_kv,kL,D] K/V, [B,H_q,qL] L).
+//  - forge "flash_attention_mma.metal", header and kernel body: split-Q
+//    (each row owned by one worker for the whole KV sweep), causal KV loop
+//    bounded by the tile's last row, per-row rescale of O by exp(m_old -
+//    m_new), and the epilogue O / l with l == 0 giving O = 0.
+//  - ruDNN "dense_attention.rs", functions `forward` (mask kinds, -inf
+//    exclusion) and `forward_flash` (exp2 domain, bf16 unnormalised P with
+//    fp32 accumulation).
+//  - oxibonsai "dit_attention_flash.rs", module doc: head-major input with
+//    the transpose to token-major output folded into the epilogue.
+//
+// GB300 design (differs from the pages' Apple-GPU kernels):
+//  - warp 0 issues TMA loads: Q once, then K and V tiles through two
+//    mbarrier rings (separate K and V rings);
+//  - warp 1 owns TMEM and issues every tcgen05.mma from one thread:
+//    S = Q K^T (both operands in shared memory, K-major, 128-byte swizzle)
+//    and O += P V (P read from TMEM, V MN-major from shared memory);
+//  - warps 2-3 (fp32 I/O only) round Q and K tiles to tf32 in place;
+//  - one softmax warpgroup per 128-row Q tile: thread r owns row r (TMEM lane
+//    r), reads its S row with tcgen05.ld, applies masks, updates the base-2
+//    running max/sum, writes P back to TMEM and rescales its O row in TMEM
+//    only when the running max grows by more than 2^8 (exact: O and l share
+//    the stale max; the epilogue divides it out);
+//  - two Q tiles per CTA ping-pong on the tensor core where TMEM allows;
+//  - epilogue: O / l -> I/O dtype -> swizzled smem -> TMA store (any
+//    {batch, head, row} strides, e.g. token-major), L in fp32.
+//  - every wait is bounded; on expiry the kernel records kStatusTimeout,
+//    drains its own copies and MMAs, frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "fa_params.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// The running max is only moved (and O rescaled) when it grows by more than
+// this many powers of two; unnormalised p then stays below 2^8.
+constexpr float kRescaleThreshold = 8.0f;
+// Bound on the exit-time drains (copies and MMAs still in flight after an
+// abort); independent of the configurable wait bound so a short bound never
+// lets TMEM or shared memory go while the hardware still writes to them.
+constexpr long long kDrainCycles = 1LL << 33;
+
+template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_>
+struct Cfg {
+  static constexpr bool kTf32 = kTf32_;
+  static constexpr int kD = kD_;
+  static constexpr int kEsz = kTf32 ? 4 : 2;          // bytes per stored element
+  static constexpr int kChunk = 128 / kEsz;           // elements per 128-byte swizzle row
+  static constexpr int kNChunk = kD / kChunk;         // swizzle column blocks per row
+  static constexpr int kBM = 128;                     // rows per Q tile (= TMEM lanes)
+  static constexpr int kNQT = kNQT_;                  // Q tiles per CTA
+  static constexpr int kBN = kBN_;                    // keys per KV tile
+  static constexpr int kKStages = kKStages_;
+  static constexpr int kVStages = kVStages_;
+  static constexpr int kKStep = kTf32 ? 8 : 16;       // MMA K per instruction (32 bytes)
+  static constexpr bool kAliasP = (kNQT == 2);        // P over S; PV issued before the next S
+  static constexpr int kPCols = kTf32 ? kBN : kBN / 2;  // TMEM columns of one P tile
+  static constexpr int kColO = kNQT * kBN;            // first O column
+  static constexpr int kColP = kColO + kNQT * kD;     // P double buffer (non-aliased mode)
+  static constexpr int kTmemUsed = kAliasP ? kNQT * (kBN + kD) : (kBN + kD + 2 * kPCols);
+  static constexpr uint32_t kTmemCols =
+      kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr int kThreads = 128 * (1 + kNQT);
+  static constexpr uint32_t kQTileBytes = kBM * kD * kEsz;
+  static constexpr uint32_t kKVTileBytes = kBN * kD * kEsz;
+  static constexpr uint32_t kOffK = kNQT * kQTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kKVTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kVStages * kKVTileBytes;
+  static constexpr uint32_t kBarBytes = 512;
+  static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
+
+  static_assert(kD % kChunk == 0, "head dim must be a whole number of 128-byte rows");
+  static_assert(kBN % 32 == 0 && kBN >= 32 && kBN <= 256, "KV tile must be 32..256, multiple of 32");
+  static_assert(kD % 16 == 0 && kD <= 256, "PV MMA needs N = D in 16..256");
+  static_assert(kTmemUsed <= 512, "TMEM overflow");
+  static_assert(kSmemBytes <= 232448, "shared memory overflow");
+  static_assert(kKStages >= 1 && kVStages >= 1 && kKStages <= 4 && kVStages <= 4, "ring size");
+};
+
+// Shared-memory control block (after the tiles).
+template <class C>
+struct Ctrl {
+  uint64_t q_full[2];             // TMA -> Q tile t landed
+  uint64_t q_ready[2];            // (tf32) Q tile t rounded in place
+  uint64_t k_full[4], k_empty[4], k_ready[4];
+  uint64_t v_full[4], v_empty[4];
+  uint64_t s_full[2];             // S_t computed (commit)
+  uint64_t p_ready[2];            // softmax t wrote P (and rescaled O)
+  uint64_t o_ready[2];            // PV_t completed (commit)
+  uint64_t drain;                 // MMA drain at exit
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Bounded wait: true once the phase of `parity` completed; false after the
+// CTA-wide abort flag is raised or `timeout` cycles pass (then it raises the
+// flag and records the timeout in the device status word).
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                             unsigned int* status, long long timeout, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64_now();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *abort) return false;
+    if (clock64_now() - t0 > timeout) {
+      *abort = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned int* status,
+                                          long long timeout) {
+  const bool ok = wait_bounded(bar, parity, abort, status, timeout);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Number of KV tiles a 128-row Q tile starting at r0 visits (0 if it has no rows).
+template <class C>
+__device__ __forceinline__ int tile_kv_blocks(const FaParams& p, int r0) {
+  if (r0 >= p.qL) return 0;
+  const int last = min(r0 + C::kBM, p.qL) - 1;
+  const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
+  return (kv_end + C::kBN - 1) / C::kBN;
+}
+
+// Round a tile of fp32 values in shared memory to tf32 (round to nearest).
+__device__ __forceinline__ void round_tf32_inplace(uint8_t* base, uint32_t bytes, int tid, int nthreads) {
+  uint4* p4 = reinterpret_cast<uint4*>(base);
+  const uint32_t n = bytes / 16;
+  for (uint32_t i = tid; i < n; i += nthreads) {
+    uint4 v = p4[i];
+    v.x = to_tf32(__uint_as_float(v.x));
+    v.y = to_tf32(__uint_as_float(v.y));
+    v.z = to_tf32(__uint_as_float(v.z));
+    v.w = to_tf32(__uint_as_float(v.w));
+    p4[i] = v;
+  }
+}
+
+// Load 32 mask entries [k0, k0+32) of one row and fold them into s[off .. off+32):
+// additive: s += mask * log2(e) (s already scaled to base 2); bool: s = -inf
+// where the mask is zero.  Keys >= kL are left alone (cut by the tail limit).
+template <class C, int kMaskKind>
+__device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, int k0, int kL, bool vec) {
+  if constexpr (kMaskKind == 1) {
+    const uint8_t* mrow = static_cast<const uint8_t*>(mrow_v);
+    if (vec && k0 + 32 <= kL) {
+      const uint4* m4 = reinterpret_cast<const uint4*>(mrow + k0);
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const uint4 w = __ldg(m4 + v);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t byte = (ws[e >> 2] >> ((e & 3) * 8)) & 0xFFu;
+          if (byte == 0u) s[v * 16 + e] = -INFINITY;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (k0 + e < kL && __ldg(mrow + k0 + e) == 0) s[e] = -INFINITY;
+    }
+  } else {
+    if constexpr (C::kTf32) {
+      const float* mrow = static_cast<const float*>(mrow_v);
+      if (vec && k0 + 32 <= kL) {
+        const float4* m4 = reinterpret_cast<const float4*>(mrow + k0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 w = __ldg(m4 + v);
+          s[v * 4 + 0] = fmaf(w.x, kLog2e, s[v * 4 + 0]);
+          s[v * 4 + 1] = fmaf(w.y, kLog2e, s[v * 4 + 1]);
+          s[v * 4 + 2] = fmaf(w.z, kLog2e, s[v * 4 + 2]);
+          s[v * 4 + 3] = fmaf(w.w, kLog2e, s[v * 4 + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (k0 + e < kL) s[e] = fmaf(__ldg(mrow + k0 + e), kLog2e, s[e]);
+      }
+    } else {
+      const uint16_t* mrow = static_cast<const uint16_t*>(mrow_v);
+      if (vec && k0 + 32 <= kL) {
+        const uint4* m4 = reinterpret_cast<const uint4*>(mrow + k0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 w = __ldg(m4 + v);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t bits = (e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16);
+            s[v * 8 + e] = fmaf(__uint_as_float(bits), kLog2e, s[v * 8 + e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (k0 + e < kL) s[e] = fmaf(__uint_as_float((uint32_t)__ldg(mrow + k0 + e) << 16), kLog2e, s[e]);
+      }
+    }
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p, int b, int h, int row, int kbase) {
+  // Scores to base 2 first when the mask is additive or the scale is not positive.
+  if (p.pre_scale) {
+#pragma unroll
+    for (int c = 0; c < C::kBN; ++c) s[c] *= p.scale_log2;
+  }
+  if (p.mask_kind != 0 && row < p.qL) {
+    const size_t esz = (p.mask_kind == 1) ? 1 : C::kEsz;
+    const char* mrow = static_cast<const char*>(p.mask) +
+                       ((long long)b * p.mask_sb + (long long)h * p.mask_sh + (long long)row * p.mask_ss) * esz;
+    const bool vec = p.mask_vec != 0;
+#pragma unroll
+    for (int cc = 0; cc < C::kBN / 32; ++cc) {
+      if (p.mask_kind == 1)
+        fold_mask_chunk<C, 1>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec);
+      else
+        fold_mask_chunk<C, 2>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec);
+    }
+  }
+  // Causal and tail limits: key kbase + c is allowed iff c < lim.
+  int lim = p.kL - kbase;
+  if (p.causal) lim = min(lim, row + 1 - kbase);
+#pragma unroll
+  for (int c = 0; c < C::kBN; ++c)
+    if (c >= lim) s[c] = -INFINITY;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FaParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  Ctrl<C>* ctl = reinterpret_cast<Ctrl<C>*>(smem + C::kOffBar);
+  volatile int* abort_flag = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: (query block, batch, head); heavy causal blocks first,
+  //      consecutive CTAs share a K/V head (GQA) so K/V stay hot in L2.
+  const int per_q = p.B * p.Hq;
+  const int qb_rev = blockIdx.x / per_q;
+  const int rem = blockIdx.x - qb_rev * per_q;
+  const int qb = p.causal ? (p.n_qblocks - 1 - qb_rev) : qb_rev;
+  const int b = rem / p.Hq;
+  const int h = rem - b * p.Hq;
+  const int kvh = h / p.group;
+  const int q0 = qb * (C::kBM * C::kNQT);
+  int nblk[2];
+  nblk[0] = tile_kv_blocks<C>(p, q0);
+  nblk[1] = (C::kNQT == 2) ? tile_kv_blocks<C>(p, q0 + C::kBM) : 0;
+  const int N = max(nblk[0], nblk[1]);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&ctl->q_full[t], 1);
+      mbar_init(&ctl->q_ready[t], 64);
+      mbar_init(&ctl->s_full[t], 1);
+      mbar_init(&ctl->p_ready[t], 128);
+      mbar_init(&ctl->o_ready[t], 1);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+      mbar_init(&ctl->k_ready[s], 64);
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      int k_issued = 0, v_issued = 0;
+      bool q_issued[2] = {false, false};
+#pragma unroll
+      for (int t = 0; t < C::kNQT; ++t) {
+        if (nblk[t] == 0) continue;
+        mbar_arrive_expect_tx(&ctl->q_full[t], C::kQTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kNChunk; ++c)
+          tma_load_4d(sQ + t * C::kQTileBytes + c * (C::kBM * 128), &tmQ, &ctl->q_full[t], c * C::kChunk,
+                      q0 + t * C::kBM, h, b);
+        q_issued[t] = true;
+      }
+      for (int j = 0; j < N; ++j) {
+        {  // K_j
+          const int slot = j % C::kKStages, use = j / C::kKStages;
+          if (!wait_bounded(&ctl->k_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles)) break;
+          mbar_arrive_expect_tx(&ctl->k_full[slot], C::kKVTileBytes);
+          uint8_t* dst = sK + slot * C::kKVTileBytes;
+#pragma unroll
+          for (int c = 0; c < C::kNChunk; ++c)
+            tma_load_4d(dst + c * (C::kBN * 128), &tmK, &ctl->k_full[slot], c * C::kChunk, j * C::kBN, kvh, b);
+          ++k_issued;
+        }
+        {  // V_j
+          const int slot = j % C::kVStages, use = j / C::kVStages;
+          if (!wait_bounded(&ctl->v_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles)) break;
+          mbar_arrive_expect_tx(&ctl->v_full[slot], C::kKVTileBytes);
+          uint8_t* dst = sV + slot * C::kKVTileBytes;
+#pragma unroll
+          for (int c = 0; c < C::kNChunk; ++c)
+            tma_load_4d(dst + c * (C::kBN * 128), &tmV, &ctl->v_full[slot], c * C::kChunk, j * C::kBN, kvh, b);
+          ++v_issued;
+        }
+      }
+      if (*abort_flag) {
+        // Let every copy this thread started land before the CTA lets go of its memory.
+        for (int t = 0; t < 2; ++t)
+          if (q_issued[t]) wait_bounded(&ctl->q_full[t], 0, abort_flag, p.status, kDrainCycles, false);
+        for (int it = max(0, k_issued - C::kKStages); it < k_issued; ++it)
+          wait_bounded(&ctl->k_full[it % C::kKStages], (it / C::kKStages) & 1, abort_flag, p.status,
+                       kDrainCycles, false);
+        for (int it = max(0, v_issued - C::kVStages); it < v_issued; ++it)
+          wait_bounded(&ctl->v_full[it % C::kVStages], (it / C::kVStages) & 1, abort_flag, p.status,
+                       kDrainCycles, false);
+      }
+    }
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc(C::kTf32, 128, C::kBN, false, false);
+      constexpr uint32_t idPV = make_idesc(C::kTf32, 128, C::kD, false, true);
+      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+
+      auto issue_S = [&](int t, int kslot) {
+        const uint32_t qa = sQa + t * C::kQTileBytes;
+        const uint32_t ka = sKa + kslot * C::kKVTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kD / C::kKStep; ++kk) {
+          const int c = kk / 4;             // 4 MMA K-steps per 128-byte swizzle row
+          const uint32_t off = (kk % 4) * 32;
+          const uint64_t ad = make_sdesc_sw128(qa + c * (C::kBM * 128) + off, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(ka + c * (C::kBN * 128) + off, 16, 1024);
+          mma_ss<C::kTf32>(tmem + t * C::kBN, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_PV = [&](int t, int j, int vslot) {
+        const uint32_t va = sVa + vslot * C::kKVTileBytes;
+        const uint32_t pcol = C::kAliasP ? (uint32_t)(t * C::kBN) : (uint32_t)(C::kColP + (j & 1) * C::kPCols);
+#pragma unroll
+        for (int kk = 0; kk < C::kBN / C::kKStep; ++kk) {
+          // V tile: rows = keys (the MMA's K), 128 bytes of D per row; D column
+          // blocks are kBN*128 bytes apart (LBO), 8-key groups 1024 apart (SBO).
+          const uint64_t bd = make_sdesc_sw128(va + kk * (C::kKStep * 128), C::kBN * 128, 1024);
+          mma_ts<C::kTf32>(tmem + C::kColO + t * C::kD, tmem + pcol + kk * 8, bd, idPV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = true;
+      for (int t = 0; t < C::kNQT && ok; ++t) {
+        if (nblk[t] == 0) continue;
+        ok = C::kTf32 ? wait_bounded(&ctl->q_ready[t], 0, abort_flag, p.status, p.timeout_cycles)
+                      : wait_bounded(&ctl->q_full[t], 0, abort_flag, p.status, p.timeout_cycles);
+      }
+      // K_0 -> S_t,0 for every tile
+      if (ok) {
+        ok = C::kTf32 ? wait_bounded(&ctl->k_ready[0], 0, abort_flag, p.status, p.timeout_cycles)
+                      : wait_bounded(&ctl->k_full[0], 0, abort_flag, p.status, p.timeout_cycles);
+      }
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < C::kNQT; ++t) {
+          if (nblk[t] == 0) continue;
+          issue_S(t, 0);
+          mma_commit(&ctl->s_full[t]);
+        }
+        mma_commit(&ctl->k_empty[0]);
+      }
+      for (int j = 0; j < N && ok; ++j) {
+        const int vslot = j % C::kVStages;
+        ok = wait_bounded(&ctl->v_full[vslot], (j / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        const bool next = (j + 1 < N);
+        const int kslot = (j + 1) % C::kKStages;
+        bool k_waited = false;
+        auto wait_k = [&]() -> bool {
+          if (k_waited) return true;
+          k_waited = true;
+          const uint32_t par = ((j + 1) / C::kKStages) & 1;
+          return C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
+                          : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
+        };
+#pragma unroll
+        for (int t = 0; t < C::kNQT; ++t) {
+          if (!ok || j >= nblk[t]) continue;
+          ok = wait_bounded(&ctl->p_ready[t], j & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          const bool s_next = (j + 1 < nblk[t]);
+          if (s_next) {
+            ok = wait_k();
+            if (!ok) break;
+          }
+          tc_fence_after();
+          if (C::kAliasP) {
+            issue_PV(t, j, vslot);
+            mma_commit(&ctl->o_ready[t]);
+            if (s_next) {
+              issue_S(t, kslot);
+              mma_commit(&ctl->s_full[t]);
+            }
+          } else {
+            if (s_next) {
+              issue_S(t, kslot);
+              mma_commit(&ctl->s_full[t]);
+            }
+            issue_PV(t, j, vslot);
+            mma_commit(&ctl->o_ready[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&ctl->v_empty[vslot]);
+        if (next) {
+          // Tiles that stop earlier (causal) never waited on K_{j+1}; make sure
+          // it landed before its slot is handed back.
+          ok = wait_k();
+          if (!ok) break;
+          mma_commit(&ctl->k_empty[kslot]);
+        }
+      }
+      // Drain: every MMA this thread issued completes before TMEM is freed.
+      mma_commit(&ctl->drain);
+      wait_bounded(&ctl->drain, 0, abort_flag, p.status, kDrainCycles, false);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ===================================================== tf32 rounding (fp32 I/O only)
+    if constexpr (C::kTf32) {
+      const int ct = threadIdx.x - 64;  // 0..63
+      bool ok = true;
+      for (int t = 0; t < C::kNQT && ok; ++t) {
+        if (nblk[t] == 0) continue;
+        ok = warp_wait(&ctl->q_full[t], 0, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        round_tf32_inplace(sQ + t * C::kQTileBytes, C::kQTileBytes, ct, 64);
+        fence_proxy_async_smem();
+        mbar_arrive(&ctl->q_ready[t]);
+      }
+      for (int j = 0; j < N && ok; ++j) {
+        const int slot = j % C::kKStages;
+        ok = warp_wait(&ctl->k_full[slot], (j / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, 64);
+        fence_proxy_async_smem();
+        mbar_arrive(&ctl->k_ready[slot]);
+      }
+    }
+  } else {
+    // ===================================================== softmax warpgroup t
+    const int t = (warp - 4) >> 2;
+    const int tl = threadIdx.x - 128 * (1 + t);   // 0..127 = TMEM lane = tile row
+    const int r0 = q0 + t * C::kBM;
+    const int row = r0 + tl;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + t * C::kBN;
+    const uint32_t tO = tmem + lane_addr + C::kColO + t * C::kD;
+    const int nb = nblk[t];
+    const float sl = p.pre_scale ? 1.0f : p.scale_log2;
+
+    float m_run = -INFINITY;  // running max, base 2 (scaled)
+    float l_run = 0.0f;       // running sum of 2^(s - m_run)
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      ok = warp_wait(&ctl->s_full[t], j & 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      tc_fence_after();
+
+      float s[C::kBN];
+#pragma unroll
+      for (int cc = 0; cc < C::kBN / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tS + cc * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(r[e]);
+      }
+
+      const int kbase = j * C::kBN;
+      const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + C::kBN > p.kL ||
+                             (p.causal && kbase + C::kBN - 1 > r0);
+      if (need_mask) apply_mask<C>(s, p, b, h, row, kbase);
+
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < C::kBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_blk = mx * sl;  // -inf stays -inf (sl > 0 whenever it is not 1)
+      const float m_new = fmaxf(m_run, m_blk);
+      float corr = 1.0f;
+      const bool resc = m_new > m_run + kRescaleThreshold;
+      if (resc) {
+        corr = ex2(m_run - m_new);  // 0 when m_run = -inf
+        m_run = m_new;
+      }
+      const float msub = (m_run == -INFINITY) ? 0.0f : m_run;
+
+      // P = 2^(s*sl - m): fp32 sum, stored to TMEM as bf16 pairs or tf32.
+      const uint32_t tP = C::kAliasP ? tS : (tmem + lane_addr + C::kColP + (j & 1) * C::kPCols);
+      float sum = 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < C::kBN / 32; ++cc) {
+        if constexpr (C::kTf32) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float pv = ex2(fmaf(s[cc * 32 + e], sl, -msub));
+            sum += pv;
+            pk[e] = to_tf32(pv);
+          }
+          tmem_st32(tP + cc * 32, pk);
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(s[cc * 32 + 2 * e], sl, -msub));
+            const float p1 = ex2(fmaf(s[cc * 32 + 2 * e + 1], sl, -msub));
+            sum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tP + cc * 16, pk);
+        }
+      }
+      l_run = l_run * corr + sum;
+
+      // Rescale this warp's O rows once the previous PV has landed.
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        ok = warp_wait(&ctl->o_ready[t], (j - 1) & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < C::kD / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tO + cc * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+          tmem_st32(tO + cc * 32, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ctl->p_ready[t]);
+    }
+
+    // ---- epilogue: O / l -> I/O dtype -> swizzled smem (the dead Q tile) -> TMA store; L.
+    if (ok && nb > 0) ok = warp_wait(&ctl->o_ready[t], (nb - 1) & 1, abort_flag, p.status, p.timeout_cycles);
+    const bool do_out = ok && nb > 0;
+    uint8_t* stage = sQ + t * C::kQTileBytes;
+    if (do_out) {
+      tc_fence_after();
+      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < C::kD / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tO + cc * 32, r);
+        tmem_wait_ld();
+        if constexpr (C::kTf32) {
+          // 32 fp32 = one 128-byte row of column block cc
+          uint8_t* rowp = stage + cc * (C::kBM * 128) + tl * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 w;
+            w.x = __float_as_uint(__uint_as_float(r[4 * u + 0]) * inv_l);
+            w.y = __float_as_uint(__uint_as_float(r[4 * u + 1]) * inv_l);
+            w.z = __float_as_uint(__uint_as_float(r[4 * u + 2]) * inv_l);
+            w.w = __float_as_uint(__uint_as_float(r[4 * u + 3]) * inv_l);
+            *reinterpret_cast<uint4*>(rowp + ((u ^ (tl & 7)) << 4)) = w;
+          }
+        } else {
+          // 32 bf16 = half of a 128-byte row: column block cc/2, 16-byte units (cc&1)*4 ..
+          uint8_t* rowp = stage + (cc >> 1) * (C::kBM * 128) + tl * 128;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l, __uint_as_float(r[8 * u + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l, __uint_as_float(r[8 * u + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l, __uint_as_float(r[8 * u + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l, __uint_as_float(r[8 * u + 7]) * inv_l);
+            const int unit = (cc & 1) * 4 + u;
+            *reinterpret_cast<uint4*>(rowp + ((unit ^ (tl & 7)) << 4)) = w;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + t, 128);
+    if (do_out && tl == 0 && !*abort_flag) {
+#pragma unroll
+      for (int c = 0; c < C::kNChunk; ++c)
+        tma_store_4d(&tmO, stage + c * (C::kBM * 128), c * C::kChunk, r0, h, b);
+      tma_store_commit();
+      tma_store_wait_read0();
+    }
+    if (do_out && row < p.qL) {
+      const float lse = (l_run > 0.0f) ? (m_run + lg2(l_run)) * kLn2 : -INFINITY;
+      p.lse[((long long)b * p.Hq + h) * p.qL + row] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,137 @@
+// fa_launch.cuh -- host launcher for one (I/O dtype, head dim) instantiation:
+// encodes the four TMA tensor maps, sizes the grid and launches on the
+// caller's stream.  Arguments arrive already validated by the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_kernel.cuh"
+
+namespace fa {
+
+struct LaunchArgs {
+  const void *q, *k, *v;
+  void* o;
+  float* lse;
+  const void* mask;
+  int B, Hq, Hkv, qL, kL, D;
+  float scale;
+  int causal, mask_kind;
+  long long qs[3], ks[3], vs[3], os[3], ms[3];  // element strides: batch, head, row
+  int mask_vec;
+  cudaStream_t stream;
+  unsigned int* status;
+  long long timeout_cycles;
+  int num_sms;
+};
+
+// cuTensorMapEncodeTiled, resolved from the driver at run time (the library
+// does not link libcuda directly).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();  // defined in fa_api.cu
+void set_error(const char* fmt, ...);
+
+// A [B, H, rows, D] view with element strides {sb, sh, sr} and unit inner
+// stride, tiled as {chunk elements (128 bytes), box_rows, 1, 1} with 128-byte
+// swizzle.  Rows past `rows` read as zero and are clipped on store.
+inline bool encode_bhsd(CUtensorMap* map, bool f32, const void* ptr, int B, int H, int rows, int D,
+                        const long long* st, int chunk, int box_rows) {
+  const int esz = f32 ? 4 : 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+  // A stride of an extent-1 dimension is never used; give it a legal value.
+  auto legal = [](long long bytes, int extent) -> cuuint64_t {
+    return (extent <= 1 || bytes <= 0) ? (cuuint64_t)16 : (cuuint64_t)bytes;
+  };
+  cuuint64_t strides[3] = {legal(st[2] * esz, rows), legal(st[1] * esz, H), legal(st[0] * esz, B)};
+  cuuint32_t box[4] = {(cuuint32_t)chunk, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the CUDA driver");
+    return false;
+  }
+  CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
+template <class C>
+int launch_fa_fwd(const LaunchArgs& a) {
+  CUtensorMap tq, tk, tv, to;
+  if (!encode_bhsd(&tq, C::kTf32, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
+  if (!encode_bhsd(&tk, C::kTf32, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
+  if (!encode_bhsd(&tv, C::kTf32, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
+  if (!encode_bhsd(&to, C::kTf32, a.o, a.B, a.Hq, a.qL, a.D, a.os, C::kChunk, C::kBM)) return 4;
+
+  FaParams p;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.qL = a.qL;
+  p.kL = a.kL;
+  p.group = a.Hq / a.Hkv;
+  p.n_qblocks = (a.qL + C::kBM * C::kNQT - 1) / (C::kBM * C::kNQT);
+  p.causal = a.causal;
+  p.mask_kind = a.mask_kind;
+  p.pre_scale = (a.mask_kind == 2 || !(a.scale > 0.0f)) ? 1 : 0;
+  p.mask_vec = a.mask_vec;
+  p.scale_log2 = a.scale * kLog2e;
+  p.mask = a.mask;
+  p.mask_sb = a.ms[0];
+  p.mask_sh = a.ms[1];
+  p.mask_ss = a.ms[2];
+  p.lse = a.lse;
+  p.status = a.status;
+  p.timeout_cycles = a.timeout_cycles;
+
+  auto kern = fa_fwd_kernel<C>;
+  static int configured_device = -1;  // attribute set once per device (per instantiation)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    if (e != cudaSuccess) {
+      set_error("cudaFuncSetAttribute(max dynamic smem = %u): %s", (unsigned)C::kSmemBytes, cudaGetErrorString(e));
+      return 4;
+    }
+    configured_device = dev;
+  }
+  const long long grid = (long long)p.n_qblocks * a.B * a.Hq;
+  if (grid <= 0 || grid > 0x7fffffffLL) {
+    set_error("grid of %lld CTAs is out of range", grid);
+    return 2;
+  }
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, to, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("kernel launch failed: %s", cudaGetErrorString(e));
+    return 4;
+  }
+  return 0;
+}
+
+// Per-instantiation configurations (dtype, D) -> tiles, rings and TMEM plan.
+//                    tf32   D    Q tiles  BN  K ring  V ring
+using CfgBf16D64  = Cfg<false, 64,  2, 128, 4, 4>;  // smem 160 KB, TMEM 384
+using CfgBf16D128 = Cfg<false, 128, 2, 128, 2, 2>;  // smem 192 KB, TMEM 512
+using CfgBf16D256 = Cfg<false, 256, 1, 128, 1, 1>;  // smem 192 KB, TMEM 512 (P double-buffered)
+using CfgF32D64   = Cfg<true, 64,   2, 128, 2, 2>;  // smem 192 KB, TMEM 384
+using CfgF32D128  = Cfg<true, 128,  1, 64, 2, 2>;   // smem 192 KB, TMEM 320
+using CfgF32D256  = Cfg<true, 256,  1, 32, 1, 2>;   // smem 224 KB, TMEM 352
+
+int launch_bf16_d64(const LaunchArgs& a);
+int launch_bf16_d128(const LaunchArgs& a);
+int launch_bf16_d256(const LaunchArgs& a);
+int launch_f32_d64(const LaunchArgs& a);
+int launch_f32_d128(const LaunchArgs& a);
+int launch_f32_d256(const LaunchArgs& a);
+
+}  // namespace fa

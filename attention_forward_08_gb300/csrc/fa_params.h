@@ -1,0 +1,30 @@
+// fa_params.h -- the scalar parameter block the launcher hands to the forward
+// kernel (passed by value as a kernel argument; tensor maps travel beside it).
+#pragma once
+
+#include <stdint.h>
+
+namespace fa {
+
+// Device status word bits (the library keeps one static word per device).
+enum : unsigned int {
+  kStatusTimeout = 1u << 0,  // a bounded wait ran out; the kernel unwound early
+};
+
+struct FaParams {
+  int B, Hq, Hkv, qL, kL;
+  int group;        // Hq / Hkv: query heads per K/V head
+  int n_qblocks;    // query blocks of (tiles per CTA * 128) rows per (b, h)
+  int causal;       // top-left aligned: key j allowed for row i iff j <= i
+  int mask_kind;    // 0 none, 1 bool (uint8, nonzero keeps), 2 additive (I/O dtype)
+  int pre_scale;    // scale scores before masking (additive mask, or scale <= 0)
+  int mask_vec;     // mask rows 16-byte aligned: vector loads allowed
+  float scale_log2; // scale * log2(e)
+  const void* mask;
+  long long mask_sb, mask_sh, mask_ss;  // mask element strides: batch, head, query row
+  float* lse;                           // [B, Hq, qL] fp32, natural log
+  unsigned int* status;                 // device status word (kStatus* bits)
+  long long timeout_cycles;             // bound on every wait, in SM clock cycles
+};
+
+}  // namespace fa

@@ -1,0 +1,202 @@
+"""ctypes binding of the C ABI in ``include/fa.h`` (argument marshalling only).
+
+``fa_fwd``, ``fa_fwd_ex``, ``fa_last_error``, ``fa_sync_status``,
+``fa_set_timeout_cycles`` and ``fa_version`` mirror the C entry points one to
+one and take raw device pointers (ints).  ``attention`` is a convenience
+wrapper for torch CUDA tensors: it checks device, dtype, shape and strides
+(the buffer checks of mlx-native "ops/flash_attn_train.rs",
+`validate_buffer_size`), allocates the outputs if none are given and calls
+``fa_fwd_ex`` on the current torch stream.  Every step of the computation
+runs in the CUDA library; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
+
+FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
+FA_MASK_NONE, FA_MASK_BOOL, FA_MASK_ADDITIVE = 0, 1, 2
+FA_OK, FA_ERR_INVALID_ARGUMENT, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(6)
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
+                4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
+
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_version")
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class FaFwdArgs(ctypes.Structure):
+    """Layout of ``fa_fwd_args`` in include/fa.h."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("mask", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H_q", ctypes.c_int), ("H_kv", ctypes.c_int),
+        ("qL", ctypes.c_int), ("kL", ctypes.c_int), ("D", ctypes.c_int),
+        ("scale", ctypes.c_float), ("causal", ctypes.c_int), ("mask_kind", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("q_strides", ctypes.c_longlong * 3), ("k_strides", ctypes.c_longlong * 3),
+        ("v_strides", ctypes.c_longlong * 3), ("o_strides", ctypes.c_longlong * 3),
+        ("mask_strides", ctypes.c_longlong * 3),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load ``libfa_gb300.so``; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build the CUDA library first "
+                          f"(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_void_p] + [ctypes.c_int] * 6 + \
+        [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_fwd_ex.restype = ctypes.c_int
+    lib.fa_fwd_ex.argtypes = [ctypes.POINTER(FaFwdArgs)]
+    lib.fa_last_error.restype = ctypes.c_char_p
+    lib.fa_last_error.argtypes = []
+    lib.fa_sync_status.restype = ctypes.c_int
+    lib.fa_sync_status.argtypes = [ctypes.c_void_p]
+    lib.fa_set_timeout_cycles.restype = None
+    lib.fa_set_timeout_cycles.argtypes = [ctypes.c_longlong]
+    lib.fa_version.restype = ctypes.c_int
+    lib.fa_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(rc: int) -> int:
+    if rc != FA_OK:
+        raise FaError(rc, fa_last_error())
+    return rc
+
+
+# ----------------------------------------------------------------- raw C entry points
+
+def fa_fwd(q, k, v, o, lse, B, H_q, H_kv, qL, kL, D, scale, causal, mask, mask_kind, dtype, stream):
+    """``fa_fwd`` of include/fa.h; pointers are ints (device addresses). Returns the status."""
+    return load_library().fa_fwd(q, k, v, o, lse, B, H_q, H_kv, qL, kL, D, float(scale), int(causal),
+                                  mask, int(mask_kind), int(dtype), stream)
+
+
+def fa_fwd_ex(args: FaFwdArgs) -> int:
+    return load_library().fa_fwd_ex(ctypes.byref(args))
+
+
+def fa_last_error() -> str:
+    return load_library().fa_last_error().decode(errors="replace")
+
+
+def fa_sync_status(stream=None) -> int:
+    return load_library().fa_sync_status(stream)
+
+
+def fa_set_timeout_cycles(cycles: int) -> None:
+    load_library().fa_set_timeout_cycles(int(cycles))
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+# ----------------------------------------------------------------- torch convenience layer
+
+def _strides_bhs(t, name):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, H, rows, D] (got {tuple(t.shape)})")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    return (t.stride(0), t.stride(1), t.stride(2))
+
+
+def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind=None, stream=None) -> FaFwdArgs:
+    """Fill ``fa_fwd_args`` from torch CUDA tensors (4-D views with unit inner stride).
+
+    q, o: [B, H_q, qL, D]; k, v: [B, H_kv, kL, D]; lse: contiguous [B, H_q, qL]
+    fp32; mask: None, bool/uint8 (keep = nonzero) or an additive tensor of
+    q's dtype, broadcastable to [B, H_q, qL, kL] through its strides.
+    """
+    import torch
+    B, H_q, qL, D = q.shape
+    Bk, H_kv, kL, Dk = k.shape
+    if tuple(v.shape) != (Bk, H_kv, kL, Dk) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if tuple(o.shape) != (B, H_q, qL, D):
+        raise ValueError(f"o must be [B, H_q, qL, D] = {(B, H_q, qL, D)} (got {tuple(o.shape)})")
+    if tuple(lse.shape) != (B, H_q, qL) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous fp32 [B, H_q, qL] = {(B, H_q, qL)} tensor")
+    if q.dtype == torch.bfloat16:
+        dtype = FA_DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dtype = FA_DTYPE_F32
+    else:
+        raise ValueError(f"q dtype {q.dtype} is not bfloat16 or float32")
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        if t.dtype != q.dtype:
+            raise ValueError(f"{name} dtype {t.dtype} differs from q dtype {q.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    a = FaFwdArgs()
+    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr()
+    a.B, a.H_q, a.H_kv, a.qL, a.kL, a.D = B, H_q, H_kv, qL, kL, D
+    a.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
+    a.causal = int(bool(causal))
+    a.dtype = dtype
+    a.q_strides[:] = _strides_bhs(q, "q")
+    a.k_strides[:] = _strides_bhs(k, "k")
+    a.v_strides[:] = _strides_bhs(v, "v")
+    a.o_strides[:] = _strides_bhs(o, "o")
+    if mask is None:
+        a.mask, a.mask_kind = None, FA_MASK_NONE
+        a.mask_strides[:] = (0, 0, 0)
+    else:
+        if mask_kind is None:
+            mask_kind = FA_MASK_BOOL if mask.dtype in (torch.bool, torch.uint8) else FA_MASK_ADDITIVE
+        if mask_kind == FA_MASK_BOOL:
+            if mask.dtype == torch.bool:
+                mask = mask.view(torch.uint8)
+            if mask.dtype != torch.uint8:
+                raise ValueError("a bool mask must be torch.bool or torch.uint8")
+        elif mask.dtype != q.dtype:
+            raise ValueError(f"an additive mask must have q's dtype {q.dtype} (got {mask.dtype})")
+        if not mask.is_cuda:
+            raise ValueError("mask must be a CUDA tensor")
+        mask = mask.expand(B, H_q, qL, kL)
+        if mask.stride(3) != 1:
+            raise ValueError("mask must have unit stride along the key dimension")
+        a.mask, a.mask_kind = mask.data_ptr(), int(mask_kind)
+        a.mask_strides[:] = (mask.stride(0), mask.stride(1), mask.stride(2))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    a.stream = stream
+    return a
+
+
+def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, out=None, lse=None,
+              stream=None):
+    """O and L for torch CUDA tensors (see ``make_args``); returns (o, lse)."""
+    import torch
+    B, H_q, qL, D = q.shape
+    if out is None:
+        out = torch.empty((B, H_q, qL, D), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H_q, qL), dtype=torch.float32, device=q.device)
+    args = make_args(q, k, v, out, lse, scale=scale, causal=causal, mask=mask, mask_kind=mask_kind,
+                     stream=stream)
+    _check(fa_fwd_ex(args))
+    return out, lse

@@ -1,0 +1,414 @@
+"""Benchmark of the GB300 FlashAttention-2 forward (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one forward pass (one kernel launch of the library) over the whole
+workload: by default bf16, causal, GQA, B=2, H_q=32, H_kv=8, qL=kL=4096,
+D=128, inputs resident in HBM.  L2 is flushed (a 512 MiB write) before every
+timed step, outside the timed kernel.  The device time of each launch is taken
+with CUDA events on the stream the kernel runs on; ``value`` is TFLOP/s =
+4*B*H_q*qL*kL*D (halved when causal) / mean launch time, summed over ranks
+(each rank runs its own copy of the workload: weak scaling, no collective on
+the data path).  ``e2e`` repeats the measurement through the C ABI with the
+inputs in pinned host memory: host->device copies of Q, K, V, the forward,
+and device->host copies of O and L are all inside the timed region.
+``cpu_baseline`` times the fp64 oracle (test infrastructure, CPU) on a
+bounded sample of query rows of the same workload.
+``--impl reference`` times that oracle alone (the CPU reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ["attention_forward_08_gb300/csrc/fa_kernel.cuh", "attention_forward_08_gb300/csrc/fa_ptx.cuh",
+                  "attention_forward_08_gb300/csrc/fa_launch.cuh"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_for(w: workloads.Workload, peaks: dict) -> float:
+    """Dense tensor peak for the workload's MMA kind (TF32 = bf16 x 1/2, the nominal ratio)."""
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return bf16 if w.dtype == "bf16" else bf16 * 0.5
+
+
+def algorithmic_bytes(w: workloads.Workload) -> int:
+    esz = 2 if w.dtype == "bf16" else 4
+    qo = 2 * w.B * w.H_q * w.qL * w.D * esz
+    kv = 2 * w.B * w.H_kv * w.kL * w.D * esz
+    lse = 4 * w.B * w.H_q * w.qL
+    mask = 0 if w.mask_kind == 0 else w.B * w.H_q * w.qL * w.kL * (1 if w.mask_kind == 1 else esz)
+    return qo + kv + lse + mask
+
+
+def traffic_from_profiles(w: workloads.Workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_{w.name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+        self.window = [None, None]
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                     timeout=5).stdout.strip()
+                self.samples.append((time.time(), out))
+            except Exception:
+                pass
+            self._stop.wait(0.1)
+
+    def start(self):
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=10)
+
+    def summary(self):
+        t0, t1 = self.window
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for _, p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for _, p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in inside for i in range(4) if p[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(w: workloads.Workload, q, k, v, m, seconds: float):
+    """Time the fp64 oracle on evenly spaced query rows (~`seconds` of CPU work).
+
+    Returns (algorithmic FLOP of the sampled rows, wall seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    qo, ko, vo = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    mo = None if m is None else m.double().numpy()
+    total_rows = w.B * w.H_q * w.qL
+    threads = os.cpu_count() or 1
+    scale = float(np.float32(w.sm_scale))
+
+    def rows_flops(rows):
+        i = np.asarray(rows) % w.qL
+        n = np.minimum(i + 1, w.kL) if w.causal else np.full(len(rows), w.kL)
+        return float(np.sum(4.0 * w.D * n))
+
+    def run(n):
+        rows = np.linspace(0, total_rows - 1, n).astype(np.int64).tolist()
+        t0 = time.perf_counter()
+        oracle.attention(qo, ko, vo, scale, causal=w.causal, mask=mo, mask_kind=w.mask_kind, rows=rows,
+                         n_threads=threads)
+        return rows, time.perf_counter() - t0
+
+    n = max(threads, 16)
+    rows, dt = run(n)
+    while dt < 0.5 and n < total_rows:
+        n = min(total_rows, n * 4)
+        rows, dt = run(n)
+    if dt < seconds and n < total_rows:
+        n = min(total_rows, max(n, int(n * seconds / max(dt, 1e-6))))
+        rows, dt = run(n)
+    return rows_flops(rows), dt, len(rows), threads
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v, m = workloads.make_inputs(w)
+    per_step = max(2.0, min(15.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, m, seconds=per_step / 4)
+    flops = secs = 0.0
+    rows_total = 0
+    threads = 1
+    for _ in range(args.steps):
+        f, dt, nrows, threads = oracle_sample(w, q, k, v, m, seconds=per_step)
+        flops += f
+        secs += dt
+        rows_total += nrows
+    value = flops / secs / 1e12
+    sample = (f"{rows_total} evenly spaced query rows over {args.steps} steps "
+              f"({rows_total / args.steps:.0f} of {w.B * w.H_q * w.qL} per step), fp64 C oracle")
+    line = {
+        "impl": "reference", "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, args):
+    return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "seq_len": w.qL, "kL": w.kL, "D": w.D,
+            "causal": w.causal, "mask": ["none", "bool", "additive"][w.mask_kind],
+            "layout": "token-major O" if w.layout == "dit" else "BHSD",
+            "global_batch": w.B * max(1, args.gpus), "parallelism": f"replicas x{max(1, args.gpus)}",
+            "l2": "flushed (512 MiB write) before every timed step"}
+
+
+def run_ours(args, w):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import attention_forward_08_gb300 as fa
+    fa.load_library()
+
+    q, k, v, m = workloads.make_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if m is None else m.to(dev)
+    B, H, qL, D = q.shape
+    if w.layout == "dit":
+        o_tok = torch.empty((qL, H * D), dtype=q.dtype, device=dev)
+        od = o_tok.view(qL, H, D).permute(1, 0, 2).unsqueeze(0)
+    else:
+        od = torch.empty((B, H, qL, D), dtype=q.dtype, device=dev)
+    lsed = torch.empty((B, H, qL), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fargs = fa.make_args(qd, kd, vd, od, lsed, scale=w.sm_scale, causal=w.causal, mask=md,
+                         mask_kind=None if md is None else w.mask_kind, stream=stream.cuda_stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def launch():
+        rc = fa.fa_fwd_ex(fargs)
+        if rc != 0:
+            raise fa.FaError(rc, fa.fa_last_error())
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        launch()
+    torch.cuda.synchronize(dev)
+    assert fa.fa_sync_status(None) == 0, fa.fa_last_error()
+
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.window[0] = time.time()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    sampler.window[1] = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    rc = fa.fa_sync_status(None)
+    assert rc == 0, fa.fa_last_error()
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = sum(kernel_ms) / len(kernel_ms)
+    mean_ms = max_over_ranks(mean_ms, world, dev)
+    flops = w.flops()
+    value = flops * world / (mean_ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI: pinned host inputs -> device -> forward -> host outputs
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    mh = None if m is None else m.pin_memory()
+    oh = torch.empty(od.shape, dtype=q.dtype).pin_memory() if w.layout != "dit" else \
+        torch.empty((qL, H * D), dtype=q.dtype).pin_memory()
+    lh = torch.empty((B, H, qL), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (0 if mh is None else mh.numel() * mh.element_size())
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    o_dev_src = o_tok if w.layout == "dit" else od
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        if mh is not None:
+            md.copy_(mh, non_blocking=True)
+        launch()
+        oh.copy_(o_dev_src, non_blocking=True)
+        lh.copy_(lsed, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(3, min(args.steps, 50))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = peak_for(w, peaks)
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    traffic = traffic_from_profiles(w)
+    clocks = sampler.summary()
+
+    line = {
+        "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_of(w, argparse.Namespace(gpus=world)),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": (f"{peak_src} bf16 dense (burst)" if w.dtype == "bf16"
+                                     else f"{peak_src} bf16 dense (burst) x 0.5 nominal tf32 ratio"),
+                     "algorithmic_bytes": algorithmic_bytes(w),
+                     "hbm_gbs": algorithmic_bytes(w) / (mean_ms * 1e-3) / 1e9},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+                   "samples": clocks["samples"]},
+        "gpu_launches": args.steps,
+        "timed_region_s": wall,
+        "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        f, dt, nrows, threads = oracle_sample(w, q, k, v, m, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{nrows} evenly spaced query rows of {w.B * w.H_q * w.qL} "
+                                          f"({dt:.1f} s, fp64 C oracle, {threads} threads)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=workloads.BENCH_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,130 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ *
+ * The operation (per batch b, query head h, query row i):
+ *
+ *   kvh  = h / (H_q / H_kv)                                  GQA, no K/V copy
+ *   S_ij = scale * q[b,h,i,:] . k[b,kvh,j,:] (+ mask[b,h,i,j] if additive)
+ *   key j is excluded when causal and j > i (top-left aligned), when a bool
+ *   mask entry is 0, or when an additive mask makes S_ij = -inf
+ *   O[b,h,i,:] = sum_j softmax_j(S_i.) * v[b,kvh,j,:]
+ *   L[b,h,i]   = m_i + ln(l_i)   (natural-log logsumexp of the allowed S_ij)
+ *   a row with no allowed key gets O = 0 and L = -inf.
+ *
+ * Defined by: mlx-native "ops/flash_attn_train.rs" (module doc "Algorithm":
+ * FA-2 forward emitting O and L = m + ln(l), the FA-2 Algorithm 1
+ * logsumexp; "Buffer layout": Q/O [B,H_q,qL,D], K/V [B,H_kv,kL,D], mask
+ * [B,H_q,qL,kL], L [B,H_q,qL] fp32; `FlashAttnTrainParams` and
+ * `validate_params`), forge "flash_attention_mma.metal" (causal bound and
+ * GQA map), ruDNN "dense_attention.rs" (`forward`: mask kind 1 keeps nonzero
+ * entries, kind 2 adds the value, additive -inf excludes the key) and
+ * oxibonsai "dit_attention_flash.rs" (head-major input, token-major output).
+ *
+ * Memory: every pointer is caller-owned DEVICE memory on the current CUDA
+ * device.  The library allocates nothing per call and keeps no reference to
+ * the buffers after the kernel finishes.  o and lse must not overlap any
+ * input.  Calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream).
+ *
+ * Errors: arguments are validated before anything is launched; on error
+ * nothing is written and a non-zero fa_status is returned, with a message
+ * available from fa_last_error() on the calling thread.  A kernel that
+ * hits its internal wait bound stops early and raises a device status bit
+ * that fa_sync_status() reports as FA_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_DTYPE_F32 = 0,  /* fp32 I/O, tensor-core products in TF32 (inputs rounded to nearest) */
+  FA_DTYPE_BF16 = 1  /* bf16 I/O, fp32 accumulation, P rounded to bf16 before P.V */
+} fa_dtype;
+
+typedef enum {
+  FA_MASK_NONE = 0,
+  FA_MASK_BOOL = 1,     /* uint8, nonzero = keep the key */
+  FA_MASK_ADDITIVE = 2  /* same dtype as q; added after scaling; -inf excludes the key */
+} fa_mask_kind;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARGUMENT = 1, /* null pointer, non-positive size, H_q % H_kv != 0, bad enum, non-finite scale */
+  FA_ERR_UNSUPPORTED = 2,      /* head dim not in {64, 128, 256}, or sizes beyond the kernel's index range */
+  FA_ERR_MISALIGNED = 3,       /* q/k/v/o base or row/head/batch stride not a multiple of 16 bytes */
+  FA_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed (message says which) */
+  FA_ERR_DEVICE_TIMEOUT = 5    /* a kernel stopped at its wait bound (reported by fa_sync_status) */
+} fa_status;
+
+/*
+ * fa_fwd -- contiguous layouts:
+ *   q, o   [B, H_q, qL, D]   (dtype)
+ *   k, v   [B, H_kv, kL, D]  (dtype)
+ *   lse    [B, H_q, qL]      fp32, natural-log logsumexp L
+ *   mask   [B, H_q, qL, kL]  mask_kind 1: uint8; mask_kind 2: dtype; NULL when mask_kind 0
+ * D must be 64, 128 or 256.  scale is typically 1/sqrt(D).
+ * Returns an fa_status.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q, int H_kv, int qL,
+           int kL, int D, float scale, int causal, const void* mask, int mask_kind, int dtype, void* stream);
+
+/*
+ * fa_fwd_ex -- the same operation on strided views.  Each *_strides array
+ * holds ELEMENT strides {batch, head, row}; the innermost (D, or key for the
+ * mask) stride is 1.  q/k/v/o strides times the element size must be
+ * multiples of 16 bytes (TMA).  Mask strides are free, and 0 broadcasts that
+ * dimension.  lse stays contiguous [B, H_q, qL].
+ * Example: head-major q/k/v [H, seq, D] with token-major output
+ * o[seq, H*D] is B = 1 with o_strides = {seq*H*D, D, H*D}.
+ */
+typedef struct fa_fwd_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const void* mask;
+  int B, H_q, H_kv, qL, kL, D;
+  float scale;
+  int causal;
+  int mask_kind;
+  int dtype;
+  long long q_strides[3];
+  long long k_strides[3];
+  long long v_strides[3];
+  long long o_strides[3];
+  long long mask_strides[3];
+  void* stream; /* cudaStream_t */
+} fa_fwd_args;
+
+int fa_fwd_ex(const fa_fwd_args* args);
+
+/* Message for the last non-FA_OK return on the calling thread ("" if none). */
+const char* fa_last_error(void);
+
+/*
+ * fa_sync_status -- synchronise `stream`, then read and clear the device
+ * status word of the current device.  FA_OK if no kernel stopped early since
+ * the last call, FA_ERR_DEVICE_TIMEOUT if one did, FA_ERR_CUDA on a CUDA
+ * error (including an earlier asynchronous kernel fault).
+ */
+int fa_sync_status(void* stream);
+
+/*
+ * fa_set_timeout_cycles -- bound (in SM clock cycles) on every wait inside
+ * the kernel; <= 0 restores the default (2^31 cycles, about one second).
+ * The environment variable FA_TIMEOUT_CYCLES sets the initial value.
+ */
+void fa_set_timeout_cycles(long long cycles);
+
+/* ABI version: major * 100 + minor. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,0 +1,151 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point include/fa.h declares, its argument struct matches
+the header's layout, and validation rejects bad arguments before any CUDA
+call, with the documented status codes and a message."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from attention_forward_08_gb300 import _build
+    _build.build()
+    import attention_forward_08_gb300 as fa
+    fa.load_library()
+    return fa
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_abi():
+    assert _declared_functions() == sorted(
+        ["fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_version"])
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = fa.load_library()
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.fa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (fa_\w+)", out))
+    assert set(_declared_functions()) <= exported
+
+
+def test_args_struct_matches_header(tmp_path):
+    """ctypes' FaFwdArgs has the same size and field offsets as the C struct."""
+    from attention_forward_08_gb300.fa import FaFwdArgs
+    fields = [f for f, _ in FaFwdArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "fa.h"\nint main(void){\n'
+                   '  printf("%zu\\n", sizeof(fa_fwd_args));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(fa_fwd_args, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", f"-I{ROOT}/include", str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(FaFwdArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(FaFwdArgs, f).offset == off, f
+
+
+def test_version(fa):
+    assert fa.fa_version() == 100
+
+
+P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
+
+
+def _call(fa, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H_q=2, H_kv=2, qL=128, kL=128, D=128, scale=0.125, causal=0,
+             mask=None, mask_kind=0, dtype=1, stream=None)
+    a.update(kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H_q"], a["H_kv"], a["qL"], a["kL"],
+                     a["D"], a["scale"], a["causal"], a["mask"], a["mask_kind"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(q=None), 1, "non-NULL"),
+    (dict(lse=None), 1, "non-NULL"),
+    (dict(B=0), 1, "> 0"),
+    (dict(qL=-5), 1, "> 0"),
+    (dict(kL=0), 1, "> 0"),
+    (dict(H_q=6, H_kv=4), 1, "divisible"),
+    (dict(dtype=7), 1, "dtype"),
+    (dict(mask_kind=3, mask=P), 1, "mask_kind"),
+    (dict(mask_kind=1, mask=None), 1, "mask must be non-NULL"),
+    (dict(mask_kind=0, mask=P), 1, "mask must be non-NULL"),
+    (dict(scale=float("nan")), 1, "finite"),
+    (dict(scale=float("inf")), 1, "finite"),
+    (dict(D=96), 2, "head dim"),
+    (dict(D=32), 2, "head dim"),
+    (dict(q=P + 8), 3, "16-byte"),
+    (dict(o=P + 2), 3, "16-byte"),
+    (dict(lse=P + 2), 3, "4-byte"),
+])
+def test_validation_rejects(fa, kw, status, needle):
+    rc = _call(fa, **kw)
+    assert rc == status
+    assert needle in fa.fa_last_error()
+
+
+def test_misaligned_strides_rejected(fa):
+    """fa_fwd_ex: a row stride that is not a multiple of 16 bytes cannot feed TMA."""
+    a = fa.FaFwdArgs()
+    a.q = a.k = a.v = a.o = a.lse = P
+    a.B, a.H_q, a.H_kv, a.qL, a.kL, a.D = 1, 2, 2, 64, 64, 64
+    a.scale, a.dtype = 0.125, 1
+    for s in (a.q_strides, a.k_strides, a.v_strides, a.o_strides):
+        s[:] = (2 * 64 * 64, 64 * 64, 64)
+    a.o_strides[:] = (2 * 64 * 68, 64 * 68, 68 + 1)   # 69 bf16 = 138 bytes per row
+    assert fa.fa_fwd_ex(a) == 3
+    assert "strides" in fa.fa_last_error()
+    a.o_strides[:] = (2 * 64 * 64, 64 * 64, 32)        # rows overlap: stride < D
+    assert fa.fa_fwd_ex(a) == 1
+
+
+def test_no_gpu_is_a_cuda_error(fa):
+    """A fully valid call on a machine without a usable GPU reports FA_ERR_CUDA (it never falls back)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = _call(fa)
+    assert rc == 4
+    assert fa.fa_last_error()
+
+
+def test_error_message_cleared_on_success_path(fa):
+    _call(fa, D=96)
+    assert fa.fa_last_error()
+    _call(fa, q=None)
+    assert "non-NULL" in fa.fa_last_error()
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "attention_forward_08_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\b(import|from)\s+oracle\b", text), f
+                assert "attn_oracle" not in text and "liboracle" not in text, f
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from attention_forward_08_gb300 import fa as binding
+    with pytest.raises(ImportError):
+        saved = binding._lib
+        binding._lib = None
+        try:
+            binding.load_library(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = saved

@@ -1,0 +1,122 @@
+"""GPU parity: the CUDA library against the fp64 oracle on the same seeded inputs.
+
+Reduced sizes are compared element by element (several Q and KV tiles,
+ragged tails, every head dim, dtype, mask kind, causal, GQA and the
+token-major output); the five full-size workloads are compared on sampled
+rows computed one by one by the oracle, in the launch configuration the
+benchmark times.  Tolerances (inputs N(0,1)): bf16 max|dO| <= 2e-2 and
+max|dL| <= 1e-2; fp32 via TF32 max|dO| <= 2e-3 and max|dL| <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import compare, fp32_scale, gpu_run, oracle_inputs, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+W = workloads
+S = W.small_case
+
+SMALL = [
+    S("bf16_d128_plain", 1, 2, 2, 384, 384, 128, "bf16"),
+    S("bf16_d128_causal_gqa", 1, 4, 2, 512, 512, 128, "bf16", causal=True),
+    S("bf16_d128_causal_ragged", 2, 2, 1, 333, 333, 128, "bf16", causal=True),
+    S("bf16_d64_causal_ragged", 2, 2, 2, 300, 300, 64, "bf16", causal=True),
+    S("bf16_d64_plain_long_kv", 1, 2, 2, 200, 700, 64, "bf16"),
+    S("bf16_d256_additive_ragged", 1, 2, 2, 200, 200, 256, "bf16", mask_kind=W.MASK_ADDITIVE),
+    S("bf16_d256_bool_ragged", 1, 2, 2, 200, 200, 256, "bf16", mask_kind=W.MASK_BOOL),
+    S("bf16_d256_causal", 1, 2, 1, 260, 260, 256, "bf16", causal=True),
+    S("bf16_d128_bool_causal", 1, 2, 2, 300, 300, 128, "bf16", causal=True, mask_kind=W.MASK_BOOL),
+    S("bf16_d64_additive_causal", 1, 2, 2, 257, 257, 64, "bf16", causal=True, mask_kind=W.MASK_ADDITIVE),
+    S("f32_d64_plain", 1, 2, 2, 128, 128, 64, "f32"),
+    S("f32_d64_causal_ragged", 1, 3, 3, 290, 290, 64, "f32", causal=True),
+    S("f32_d128_tokenmajor", 1, 3, 3, 300, 300, 128, "f32", layout="dit"),
+    S("f32_d128_causal_gqa", 1, 4, 1, 260, 260, 128, "f32", causal=True),
+    S("f32_d256_plain", 1, 2, 2, 150, 150, 256, "f32"),
+    S("f32_d256_additive", 1, 2, 2, 100, 170, 256, "f32", mask_kind=W.MASK_ADDITIVE),
+    S("bf16_d128_q_longer_than_k_causal", 1, 2, 2, 400, 150, 128, "bf16", causal=True),
+    S("bf16_d128_tiny", 1, 1, 1, 1, 1, 128, "bf16"),
+    S("bf16_d64_tiny_ragged", 1, 1, 1, 5, 3, 64, "bf16", causal=True),
+    S("f32_d64_tiny", 1, 1, 1, 3, 7, 64, "f32"),
+    S("bf16_d128_gqa8", 1, 8, 1, 256, 256, 128, "bf16", causal=True),
+]
+
+
+def _run_small(w, scale=None, mask=None, qkv=None):
+    if qkv is None:
+        q, k, v, m = W.make_inputs(w)
+    else:
+        (q, k, v), m = qkv, mask
+    o_g, l_g, _ = gpu_run(w, q, k, v, m, scale=scale)
+    qo, ko, vo, mo = oracle_inputs(q, k, v, m)
+    o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w, scale), causal=w.causal, mask=mo,
+                                mask_kind=w.mask_kind if m is not None else 0)
+    return compare(w, o_g, l_g, o_r, l_r, what=w.name)
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_elementwise(w):
+    _run_small(w)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.3, 2.5])
+def test_unusual_scales(scale):
+    """scale = 0 (uniform weights), a negative scale, and a large one."""
+    _run_small(S("bf16_d128_scale", 1, 2, 2, 200, 300, 128, "bf16", causal=True), scale=scale)
+
+
+def test_fully_masked_rows():
+    """Rows whose bool mask keeps nothing: O = 0 and L = -inf; other rows unaffected."""
+    w = S("bf16_d128_bool_empty_rows", 1, 2, 2, 256, 256, 128, "bf16", mask_kind=W.MASK_BOOL)
+    q, k, v = W.make_qkv(w)
+    g = torch.Generator().manual_seed(5)
+    m = (torch.rand(1, 2, 256, 256, generator=g) < 0.5).to(torch.uint8)
+    m[0, 0, 7] = 0
+    m[0, 1, 130:140] = 0
+    _run_small(w, mask=m, qkv=(q, k, v))
+
+
+def test_broadcast_mask_strides():
+    """An additive mask broadcast over batch and heads through zero strides."""
+    w = S("bf16_d64_bcast_mask", 2, 2, 2, 200, 200, 64, "bf16", mask_kind=W.MASK_ADDITIVE)
+    q, k, v = W.make_qkv(w)
+    g = torch.Generator().manual_seed(9)
+    base = torch.randn(1, 1, 200, 200, generator=g).to(torch.bfloat16)
+    import attention_forward_08_gb300 as fa
+    dev = "cuda:0"
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), scale=w.sm_scale,
+                          mask=base.to(dev).expand(2, 2, 200, 200), mask_kind=2)
+    assert fa.fa_sync_status(None) == 0
+    qo, ko, vo, _ = oracle_inputs(q, k, v, None)
+    o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w), mask=np.broadcast_to(base.double().numpy(),
+                                                                                 (2, 2, 200, 200)), mask_kind=2)
+    compare(w, o.double().cpu().numpy(), lse.double().cpu().numpy(), o_r, l_r, what=w.name)
+
+
+def test_repeat_is_deterministic():
+    """Two launches on identical inputs give bit-identical O and L."""
+    w = S("bf16_d128_repeat", 1, 4, 2, 300, 300, 128, "bf16", causal=True)
+    q, k, v, m = W.make_inputs(w)
+    o1, l1, _ = gpu_run(w, q, k, v, m)
+    o2, l2, _ = gpu_run(w, q, k, v, m)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS), ids=list(W.WORKLOADS))
+def test_full_workload_sampled_rows(name):
+    """Full-size workloads: every output finite where it should be, and sampled rows vs the oracle."""
+    w = W.WORKLOADS[name]
+    q, k, v, m = W.make_inputs(w)
+    o_g, l_g, _ = gpu_run(w, q, k, v, m)
+    # properties over every row
+    assert np.all(np.isfinite(o_g)), "non-finite O"
+    assert np.all(np.isfinite(l_g)), "every row of these workloads has an allowed key"
+    rows = sample_rows(w, n_per_head=3 if w.qL * w.kL > 4e6 else 8)
+    qo, ko, vo, mo = oracle_inputs(q, k, v, m)
+    o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w), causal=w.causal, mask=mo,
+                                mask_kind=w.mask_kind, rows=rows)
+    D = w.D
+    compare(w, o_g.reshape(-1, D)[rows], l_g.reshape(-1)[rows], o_r, l_r, what=name)
