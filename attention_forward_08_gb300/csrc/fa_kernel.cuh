@@ -515,13 +515,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_after();
 
       float s[C::kBN];
+      {
+        uint32_t r[C::kBN];
 #pragma unroll
-      for (int cc = 0; cc < C::kBN / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tS + cc * 32, r);
+        for (int cc = 0; cc < C::kBN / 32; ++cc)
+          tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
         tmem_wait_ld();
+        reg_fence(r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[cc * 32 + e] = __uint_as_float(r[e]);
+        for (int c = 0; c < C::kBN; ++c) s[c] = __uint_as_float(r[c]);
       }
 
       const int kbase = j * C::kBN;
@@ -529,9 +531,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                              (p.causal && kbase + C::kBN - 1 > r0);
       if (need_mask) apply_mask<C>(s, p, b, h, row, kbase);
 
-      float mx = -INFINITY;
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < C::kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int c = 0; c < C::kBN; c += 4) {
+        mx4[0] = fmaxf(mx4[0], s[c + 0]);
+        mx4[1] = fmaxf(mx4[1], s[c + 1]);
+        mx4[2] = fmaxf(mx4[2], s[c + 2]);
+        mx4[3] = fmaxf(mx4[3], s[c + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_blk = mx * sl;  // -inf stays -inf (sl > 0 whenever it is not 1)
       const float m_new = fmaxf(m_run, m_blk);
       float corr = 1.0f;
@@ -544,7 +552,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
       // P = 2^(s*sl - m): fp32 sum, stored to TMEM as bf16 pairs or tf32.
       const uint32_t tP = C::kAliasP ? tS : (tmem + lane_addr + C::kColP + (j & 1) * C::kPCols);
-      float sum = 0.0f;
+      float sum2[2] = {0.0f, 0.0f};
 #pragma unroll
       for (int cc = 0; cc < C::kBN / 32; ++cc) {
         if constexpr (C::kTf32) {
@@ -552,7 +560,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float pv = ex2(fmaf(s[cc * 32 + e], sl, -msub));
-            sum += pv;
+            sum2[e & 1] += pv;
             pk[e] = to_tf32(pv);
           }
           tmem_st32(tP + cc * 32, pk);
@@ -562,13 +570,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             const float p0 = ex2(fmaf(s[cc * 32 + 2 * e], sl, -msub));
             const float p1 = ex2(fmaf(s[cc * 32 + 2 * e + 1], sl, -msub));
-            sum += p0 + p1;
+            sum2[0] += p0;
+            sum2[1] += p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tP + cc * 16, pk);
         }
       }
-      l_run = l_run * corr + sum;
+      l_run = l_run * corr + (sum2[0] + sum2[1]);
 
       // Rescale this warp's O rows once the previous PV has landed.
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -580,6 +589,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           uint32_t r[32];
           tmem_ld32(tO + cc * 32, r);
           tmem_wait_ld();
+          reg_fence(r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
           tmem_st32(tO + cc * 32, r);
@@ -602,6 +612,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         uint32_t r[32];
         tmem_ld32(tO + cc * 32, r);
         tmem_wait_ld();
+        reg_fence(r);
         if constexpr (C::kTf32) {
           // 32 fp32 = one 128-byte row of column block cc
           uint8_t* rowp = stage + cc * (C::kBM * 128) + tl * 128;

@@ -223,6 +223,16 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 #undef FA_R8
 #undef FA_W8
 
+// Registers filled by an asynchronous tcgen05.ld hold their values only after
+// tcgen05.wait::ld.  Passing them through an empty volatile asm placed after
+// the wait makes every later use depend on a point after the wait, so the
+// compiler cannot hoist a use above it.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i])::"memory");
+}
+
 // ------------------------------------------------------------------ scalar helpers
 
 // 2^x on the special-function unit (approximate; ex2(-inf) = +0).
