@@ -57,7 +57,7 @@ constexpr float kRescaleThreshold = 8.0f;
 // lets TMEM or shared memory go while the hardware still writes to them.
 constexpr long long kDrainCycles = 1LL << 33;
 
-template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_>
+template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_, int kVTStages_ = 0>
 struct Cfg {
   static constexpr bool kTf32 = kTf32_;
   static constexpr int kD = kD_;
@@ -69,6 +69,9 @@ struct Cfg {
   static constexpr int kBN = kBN_;                    // keys per KV tile
   static constexpr int kKStages = kKStages_;
   static constexpr int kVStages = kVStages_;
+  // TF32 MMAs take B only K-major, so fp32 I/O transposes each V tile into a
+  // K-major V^T ring ([D rows x kBN keys]); bf16 reads V MN-major directly.
+  static constexpr int kVTStages = kVTStages_;
   static constexpr int kKStep = kTf32 ? 8 : 16;       // MMA K per instruction (32 bytes)
   static constexpr bool kAliasP = (kNQT == 2);        // P over S; PV issued before the next S
   static constexpr int kPCols = kTf32 ? kBN : kBN / 2;  // TMEM columns of one P tile
@@ -78,11 +81,20 @@ struct Cfg {
   static constexpr uint32_t kTmemCols =
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
   static constexpr int kThreads = 128 * (1 + kNQT);
+  // Per-thread registers at launch, and the split after setmaxnreg: the
+  // control warpgroup (TMA, MMA, tf32 helpers) gives registers to the softmax
+  // warpgroups.  Sums stay within the launch total (kThreads * kRegsLaunch).
+  static constexpr int kRegsLaunch = kNQT == 2 ? 168 : 255;
+  static constexpr int kRegsCtrl = 80;
+  static constexpr int kRegsSoftmax = kNQT == 2 ? 208 : 0;  // 0: no reallocation
+  static_assert(kRegsSoftmax == 0 || 128 * kRegsCtrl + 128 * kNQT * kRegsSoftmax <= kThreads * kRegsLaunch,
+                "register split exceeds the launch allocation");
   static constexpr uint32_t kQTileBytes = kBM * kD * kEsz;
   static constexpr uint32_t kKVTileBytes = kBN * kD * kEsz;
   static constexpr uint32_t kOffK = kNQT * kQTileBytes;
   static constexpr uint32_t kOffV = kOffK + kKStages * kKVTileBytes;
-  static constexpr uint32_t kOffBar = kOffV + kVStages * kKVTileBytes;
+  static constexpr uint32_t kOffVT = kOffV + kVStages * kKVTileBytes;
+  static constexpr uint32_t kOffBar = kOffVT + kVTStages * kKVTileBytes;
   static constexpr uint32_t kBarBytes = 512;
   static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 
@@ -92,6 +104,7 @@ struct Cfg {
   static_assert(kTmemUsed <= 512, "TMEM overflow");
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static_assert(kKStages >= 1 && kVStages >= 1 && kKStages <= 4 && kVStages <= 4, "ring size");
+  static_assert(kTf32 ? (kVTStages >= 1 && kVTStages <= 4) : kVTStages == 0, "V^T ring is for TF32 only");
 };
 
 // Shared-memory control block (after the tiles).
@@ -101,6 +114,7 @@ struct Ctrl {
   uint64_t q_ready[2];            // (tf32) Q tile t rounded in place
   uint64_t k_full[4], k_empty[4], k_ready[4];
   uint64_t v_full[4], v_empty[4];
+  uint64_t vt_full[4], vt_empty[4];  // (tf32) transposed V tiles
   uint64_t s_full[2];             // S_t computed (commit)
   uint64_t p_ready[2];            // softmax t wrote P (and rescaled O)
   uint64_t o_ready[2];            // PV_t completed (commit)
@@ -153,6 +167,45 @@ __device__ __forceinline__ void round_tf32_inplace(uint8_t* base, uint32_t bytes
     v.z = to_tf32(__uint_as_float(v.z));
     v.w = to_tf32(__uint_as_float(v.w));
     p4[i] = v;
+  }
+}
+
+// Transpose a landed V tile (rows = kBN keys, 128-byte swizzled rows of 32
+// fp32, D/32 column blocks) into V^T (rows = D, 128-byte swizzled rows of 32
+// keys, kBN/32 column blocks), rounding to tf32: the K-major B operand of
+// O += P V for TF32.
+// Each step moves a 4 keys x 4 d block with four 16-byte loads and stores.
+// Within 8 consecutive threads both the d-group and the key-group run
+// through 8 distinct values (diagonals of 8x8 block super-tiles), so the
+// swizzled 16-byte units they touch are distinct: no bank conflicts.
+template <class C>
+__device__ __forceinline__ void transpose_v_tile(const uint8_t* src, uint8_t* dst, int tid, int nthreads) {
+  constexpr int kKG = C::kBN / 32;  // key super-groups (8 groups of 4 keys each)
+  constexpr int kBlocks = (C::kBN / 4) * (C::kD / 4);
+  for (int blk = tid; blk < kBlocks; blk += nthreads) {
+    const int t8 = blk & 7, diag = (blk >> 3) & 7, st = blk >> 6;
+    const int kg = (st % kKG) * 8 + ((t8 + diag) & 7);  // group of keys 4kg .. 4kg+3
+    const int dg = (st / kKG) * 8 + t8;                 // group of d 4dg .. 4dg+3
+    float4 in[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = 4 * kg + i;
+      in[i] = *reinterpret_cast<const float4*>(src + (dg >> 3) * (C::kBN * 128) + r * 128 +
+                                               (((dg & 7) ^ (r & 7)) << 4));
+    }
+#pragma unroll
+    for (int jd = 0; jd < 4; ++jd) {
+      const int d = 4 * dg + jd;
+      // Rounded to tf32 here: the tensor core would otherwise drop the low
+      // mantissa bits, an error that rows with few allowed keys (O close to
+      // a single V row) would see directly.
+      uint4 o;
+      o.x = to_tf32((&in[0].x)[jd]);
+      o.y = to_tf32((&in[1].x)[jd]);
+      o.z = to_tf32((&in[2].x)[jd]);
+      o.w = to_tf32((&in[3].x)[jd]);
+      *reinterpret_cast<uint4*>(dst + (kg >> 3) * (C::kD * 128) + d * 128 + (((kg & 7) ^ (d & 7)) << 4)) = o;
+    }
   }
 }
 
@@ -259,6 +312,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
+  uint8_t* sVT = smem + C::kOffVT;
   Ctrl<C>* ctl = reinterpret_cast<Ctrl<C>*>(smem + C::kOffBar);
   volatile int* abort_flag = &ctl->abort;
 
@@ -283,17 +337,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl->q_full[t], 1);
-      mbar_init(&ctl->q_ready[t], 64);
+      mbar_init(&ctl->q_ready[t], 2);    // one arrival per tf32 helper warp
       mbar_init(&ctl->s_full[t], 1);
-      mbar_init(&ctl->p_ready[t], 128);
+      mbar_init(&ctl->p_ready[t], 4);    // one arrival per softmax warp
       mbar_init(&ctl->o_ready[t], 1);
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], 1);
-      mbar_init(&ctl->k_ready[s], 64);
+      mbar_init(&ctl->k_ready[s], 2);
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->v_empty[s], 1);
+      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : 1);  // tf32: released by the two transposing warps
+      mbar_init(&ctl->vt_full[s], 2);
+      mbar_init(&ctl->vt_empty[s], 1);
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -314,6 +370,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
+  if (warp < 4) {
+  // Control warpgroup: TMA producer, MMA issuer, tf32 helpers.
+  if constexpr (C::kRegsSoftmax > 0) regs_dec<C::kRegsCtrl>();
   if (warp == 0) {
     // ===================================================== TMA producer
     if (lane == 0) {
@@ -367,30 +426,38 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // ===================================================== MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(C::kTf32, 128, C::kBN, false, false);
-      constexpr uint32_t idPV = make_idesc(C::kTf32, 128, C::kD, false, true);
+      constexpr uint32_t idPV = make_idesc(C::kTf32, 128, C::kD, false, !C::kTf32);
       const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      (void)sVa;
 
+      // Descriptors of the first K-step of each operand tile; later K-steps
+      // only advance the start address (bits 0-13 hold address >> 4, and no
+      // tile address comes near the 256 KB field limit, so a plain add works).
+      const uint64_t dQ0 = make_sdesc_sw128(sQa, 16, 1024);
+      const uint64_t dK0 = make_sdesc_sw128(sKa, 16, 1024);
       auto issue_S = [&](int t, int kslot) {
-        const uint32_t qa = sQa + t * C::kQTileBytes;
-        const uint32_t ka = sKa + kslot * C::kKVTileBytes;
+        const uint64_t qd = dQ0 + ((t * C::kQTileBytes) >> 4);
+        const uint64_t kd = dK0 + ((kslot * C::kKVTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::kD / C::kKStep; ++kk) {
-          const int c = kk / 4;             // 4 MMA K-steps per 128-byte swizzle row
-          const uint32_t off = (kk % 4) * 32;
-          const uint64_t ad = make_sdesc_sw128(qa + c * (C::kBM * 128) + off, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(ka + c * (C::kBN * 128) + off, 16, 1024);
-          mma_ss<C::kTf32>(tmem + t * C::kBN, ad, bd, idS, kk > 0 ? 1u : 0u);
+          // 4 MMA K-steps of 32 bytes per 128-byte swizzle row, then the next column block
+          const uint32_t qoff = (kk / 4) * (C::kBM * 128) + (kk % 4) * 32;
+          const uint32_t koff = (kk / 4) * (C::kBN * 128) + (kk % 4) * 32;
+          mma_ss<C::kTf32>(tmem + t * C::kBN, qd + (qoff >> 4), kd + (koff >> 4), idS, kk > 0 ? 1u : 0u);
         }
       };
+      // tf32: V^T tile, rows = D (the MMA's N), keys along the 128-byte rows (K-major).
+      // bf16: V tile, rows = keys (the MMA's K), 128 bytes of D per row; D column
+      // blocks are kBN*128 bytes apart (LBO), 8-key groups 1024 apart (SBO).
+      const uint64_t dV0 = C::kTf32 ? make_sdesc_sw128(smem_u32(sVT), 16, 1024)
+                                    : make_sdesc_sw128(sVa, C::kBN * 128, 1024);
       auto issue_PV = [&](int t, int j, int vslot) {
-        const uint32_t va = sVa + vslot * C::kKVTileBytes;
         const uint32_t pcol = C::kAliasP ? (uint32_t)(t * C::kBN) : (uint32_t)(C::kColP + (j & 1) * C::kPCols);
+        const uint64_t vd = dV0 + ((vslot * C::kKVTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::kBN / C::kKStep; ++kk) {
-          // V tile: rows = keys (the MMA's K), 128 bytes of D per row; D column
-          // blocks are kBN*128 bytes apart (LBO), 8-key groups 1024 apart (SBO).
-          const uint64_t bd = make_sdesc_sw128(va + kk * (C::kKStep * 128), C::kBN * 128, 1024);
-          mma_ts<C::kTf32>(tmem + C::kColO + t * C::kD, tmem + pcol + kk * 8, bd, idPV,
+          const uint32_t voff = C::kTf32 ? (kk / 4) * (C::kD * 128) + (kk % 4) * 32 : kk * (C::kKStep * 128);
+          mma_ts<C::kTf32>(tmem + C::kColO + t * C::kD, tmem + pcol + kk * 8, vd + (voff >> 4), idPV,
                            (j > 0 || kk > 0) ? 1u : 0u);
         }
       };
@@ -417,8 +484,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mma_commit(&ctl->k_empty[0]);
       }
       for (int j = 0; j < N && ok; ++j) {
-        const int vslot = j % C::kVStages;
-        ok = wait_bounded(&ctl->v_full[vslot], (j / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
+        // bf16: V ring slot; tf32: V^T ring slot
+        const int vslot = C::kTf32 ? j % C::kVTStages : j % C::kVStages;
+        const uint32_t vpar = (C::kTf32 ? j / C::kVTStages : j / C::kVStages) & 1;
+        ok = C::kTf32 ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
+                      : wait_bounded(&ctl->v_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
         const bool next = (j + 1 < N);
         const int kslot = (j + 1) % C::kKStages;
@@ -458,7 +528,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(&ctl->v_empty[vslot]);
+        mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
         if (next) {
           // Tiles that stop earlier (causal) never waited on K_{j+1}; make sure
           // it landed before its slot is handed back.
@@ -472,7 +542,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       wait_bounded(&ctl->drain, 0, abort_flag, p.status, kDrainCycles, false);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else {
     // ===================================================== tf32 rounding (fp32 I/O only)
     if constexpr (C::kTf32) {
       const int ct = threadIdx.x - 64;  // 0..63
@@ -483,7 +553,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!ok) break;
         round_tf32_inplace(sQ + t * C::kQTileBytes, C::kQTileBytes, ct, 64);
         fence_proxy_async_smem();
-        mbar_arrive(&ctl->q_ready[t]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
       }
       for (int j = 0; j < N && ok; ++j) {
         const int slot = j % C::kKStages;
@@ -491,11 +562,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (!ok) break;
         round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, 64);
         fence_proxy_async_smem();
-        mbar_arrive(&ctl->k_ready[slot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
+        // V_j -> V^T_j (K-major), then hand the V slot back to the producer.
+        const int vs = j % C::kVStages, ts = j % C::kVTStages;
+        ok = warp_wait(&ctl->v_full[vs], (j / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        ok = warp_wait(&ctl->vt_empty[ts], ((j / C::kVTStages) & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        transpose_v_tile<C>(sV + vs * C::kKVTileBytes, sVT + ts * C::kKVTileBytes, ct, 64);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ctl->vt_full[ts]);
+          mbar_arrive(&ctl->v_empty[vs]);
+        }
       }
     }
+  }
   } else {
     // ===================================================== softmax warpgroup t
+    if constexpr (C::kRegsSoftmax > 0) regs_inc<C::kRegsSoftmax>();
     const int t = (warp - 4) >> 2;
     const int tl = threadIdx.x - 128 * (1 + t);   // 0..127 = TMEM lane = tile row
     const int r0 = q0 + t * C::kBM;
@@ -597,7 +684,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ctl->p_ready[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_ready[t]);
     }
 
     // ---- epilogue: O / l -> I/O dtype -> swizzled smem (the dead Q tile) -> TMA store; L.

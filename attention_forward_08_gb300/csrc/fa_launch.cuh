@@ -102,6 +102,18 @@ int launch_fa_fwd(const LaunchArgs& a) {
       set_error("cudaFuncSetAttribute(max dynamic smem = %u): %s", (unsigned)C::kSmemBytes, cudaGetErrorString(e));
       return 4;
     }
+    // The setmaxnreg split inside the kernel assumes this launch register
+    // count; a smaller allocation would make the softmax warps' increase wait
+    // forever, so refuse to launch instead.
+    if (C::kRegsSoftmax > 0) {
+      cudaFuncAttributes fattr;
+      e = cudaFuncGetAttributes(&fattr, kern);
+      if (e != cudaSuccess || fattr.numRegs != C::kRegsLaunch) {
+        set_error("kernel register count %d differs from the %d its register split assumes",
+                  e == cudaSuccess ? fattr.numRegs : -1, C::kRegsLaunch);
+        return 4;
+      }
+    }
     configured_device = dev;
   }
   const long long grid = (long long)p.n_qblocks * a.B * a.Hq;
@@ -123,9 +135,10 @@ int launch_fa_fwd(const LaunchArgs& a) {
 using CfgBf16D64  = Cfg<false, 64,  2, 128, 4, 4>;  // smem 160 KB, TMEM 384
 using CfgBf16D128 = Cfg<false, 128, 2, 128, 2, 2>;  // smem 192 KB, TMEM 512
 using CfgBf16D256 = Cfg<false, 256, 1, 128, 1, 1>;  // smem 192 KB, TMEM 512 (P double-buffered)
-using CfgF32D64   = Cfg<true, 64,   2, 128, 2, 2>;  // smem 192 KB, TMEM 384
-using CfgF32D128  = Cfg<true, 128,  1, 64, 2, 2>;   // smem 192 KB, TMEM 320
-using CfgF32D256  = Cfg<true, 256,  1, 32, 1, 2>;   // smem 224 KB, TMEM 352
+//                                                 V^T ring (tf32)
+using CfgF32D64   = Cfg<true, 64,   2, 64, 2, 2, 2>;  // smem 160 KB, TMEM 256
+using CfgF32D128  = Cfg<true, 128,  1, 64, 2, 1, 2>;  // smem 224 KB, TMEM 320
+using CfgF32D256  = Cfg<true, 256,  1, 32, 1, 1, 1>;  // smem 224 KB, TMEM 352
 
 int launch_bf16_d64(const LaunchArgs& a);
 int launch_bf16_d128(const LaunchArgs& a);
