@@ -74,6 +74,11 @@ struct Cfg {
   static constexpr int kVTStages = kVTStages_;
   static constexpr int kKStep = kTf32 ? 8 : 16;       // MMA K per instruction (32 bytes)
   static constexpr bool kAliasP = (kNQT == 2);        // P over S; PV issued before the next S
+  // Threads issuing MMAs (tile t's MMAs come from warp 1 + t when 2).
+  // Measured: with one issuer per tile the two tiles drift into lockstep
+  // (both softmaxes at once, then both tiles' MMAs) and the tensor core idles;
+  // one issuer keeps the ping-pong order.  The code supports 2 for study.
+  static constexpr int kIssuers = 1;
   static constexpr int kPCols = kTf32 ? kBN : kBN / 2;  // TMEM columns of one P tile
   static constexpr int kColO = kNQT * kBN;            // first O column
   static constexpr int kColP = kColO + kNQT * kD;     // P double buffer (non-aliased mode)
@@ -118,7 +123,7 @@ struct Ctrl {
   uint64_t s_full[2];             // S_t computed (commit)
   uint64_t p_ready[2];            // softmax t wrote P (and rescaled O)
   uint64_t o_ready[2];            // PV_t completed (commit)
-  uint64_t drain;                 // MMA drain at exit
+  uint64_t drain[2];              // MMA drain at exit, one per issuing thread
   uint32_t tmem_base;
   int abort;
 };
@@ -344,14 +349,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&ctl->k_full[s], 1);
-      mbar_init(&ctl->k_empty[s], 1);
+      mbar_init(&ctl->k_empty[s], C::kIssuers);  // one commit per issuing thread
       mbar_init(&ctl->k_ready[s], 2);
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : 1);  // tf32: released by the two transposing warps
+      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : C::kIssuers);  // tf32: released by the two transposing warps
       mbar_init(&ctl->vt_full[s], 2);
-      mbar_init(&ctl->vt_empty[s], 1);
+      mbar_init(&ctl->vt_empty[s], C::kIssuers);
     }
-    mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->drain[0], 1);
+    mbar_init(&ctl->drain[1], 1);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -422,61 +428,71 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                        kDrainCycles, false);
       }
     }
-  } else if (warp == 1) {
-    // ===================================================== MMA issuer
+  } else if (warp == 1 || (C::kIssuers == 2 && warp == 2)) {
+    // ===================================================== MMA issuer (warp 1, and warp 2 with two issuers)
+    // Issuer i handles Q tiles [t_begin, t_end).  Every issuer walks all K/V
+    // tiles in order and commits its own arrival on each release barrier, so
+    // each release phase sees exactly kIssuers arrivals even when one tile
+    // stops early (causal).
+    const int issuer = warp - 1;
+    const int t_begin = C::kIssuers == 1 ? 0 : issuer;
+    const int t_end = C::kIssuers == 1 ? C::kNQT : issuer + 1;
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(C::kTf32, 128, C::kBN, false, false);
       constexpr uint32_t idPV = make_idesc(C::kTf32, 128, C::kD, false, !C::kTf32);
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-      (void)sVa;
-
-      // Descriptors of the first K-step of each operand tile; later K-steps
-      // only advance the start address (bits 0-13 hold address >> 4, and no
-      // tile address comes near the 256 KB field limit, so a plain add works).
-      const uint64_t dQ0 = make_sdesc_sw128(sQa, 16, 1024);
-      const uint64_t dK0 = make_sdesc_sw128(sKa, 16, 1024);
-      auto issue_S = [&](int t, int kslot) {
-        const uint64_t qd = dQ0 + ((t * C::kQTileBytes) >> 4);
-        const uint64_t kd = dK0 + ((kslot * C::kKVTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < C::kD / C::kKStep; ++kk) {
-          // 4 MMA K-steps of 32 bytes per 128-byte swizzle row, then the next column block
-          const uint32_t qoff = (kk / 4) * (C::kBM * 128) + (kk % 4) * 32;
-          const uint32_t koff = (kk / 4) * (C::kBN * 128) + (kk % 4) * 32;
-          mma_ss<C::kTf32>(tmem + t * C::kBN, qd + (qoff >> 4), kd + (koff >> 4), idS, kk > 0 ? 1u : 0u);
-        }
-      };
+      // Descriptor halves of the first K-step of each operand ring; later
+      // K-steps and slots only add to the start address in the low half.
+      const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       // tf32: V^T tile, rows = D (the MMA's N), keys along the 128-byte rows (K-major).
       // bf16: V tile, rows = keys (the MMA's K), 128 bytes of D per row; D column
       // blocks are kBN*128 bytes apart (LBO), 8-key groups 1024 apart (SBO).
-      const uint64_t dV0 = C::kTf32 ? make_sdesc_sw128(smem_u32(sVT), 16, 1024)
-                                    : make_sdesc_sw128(sVa, C::kBN * 128, 1024);
+      const uint64_t dV = C::kTf32 ? make_sdesc_sw128(smem_u32(sVT), 16, 1024)
+                                   : make_sdesc_sw128(smem_u32(sV), C::kBN * 128, 1024);
+      const uint32_t q_lo = (uint32_t)dQ, q_hi = (uint32_t)(dQ >> 32);
+      const uint32_t k_lo = (uint32_t)dK, k_hi = (uint32_t)(dK >> 32);
+      const uint32_t v_lo = (uint32_t)dV, v_hi = (uint32_t)(dV >> 32);
+
+      auto issue_S = [&](int t, int kslot) {
+        const uint32_t qa = q_lo + ((t * C::kQTileBytes) >> 4);
+        const uint32_t ka = k_lo + ((kslot * C::kKVTileBytes) >> 4);
+        const uint32_t dst = tmem + t * C::kBN;
+        mma_ss_lh<C::kTf32, 0>(dst, qa, q_hi, ka, k_hi, idS, 0u);
+#pragma unroll
+        for (int kk = 1; kk < C::kD / C::kKStep; ++kk) {
+          // 4 MMA K-steps of 32 bytes per 128-byte swizzle row, then the next column block
+          constexpr int kQCol = (C::kBM * 128) >> 4, kKCol = (C::kBN * 128) >> 4;
+          mma_ss_lh<C::kTf32, 1>(dst, qa + (kk / 4) * kQCol + (kk % 4) * 2, q_hi, ka + (kk / 4) * kKCol + (kk % 4) * 2,
+                                 k_hi, idS, 1u);
+        }
+      };
       auto issue_PV = [&](int t, int j, int vslot) {
         const uint32_t pcol = C::kAliasP ? (uint32_t)(t * C::kBN) : (uint32_t)(C::kColP + (j & 1) * C::kPCols);
-        const uint64_t vd = dV0 + ((vslot * C::kKVTileBytes) >> 4);
+        const uint32_t va = v_lo + ((vslot * C::kKVTileBytes) >> 4);
+        const uint32_t dst = tmem + C::kColO + t * C::kD;
+        const uint32_t src = tmem + pcol;
+        mma_ts_lh<C::kTf32, 0>(dst, src, va, v_hi, idPV, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < C::kBN / C::kKStep; ++kk) {
-          const uint32_t voff = C::kTf32 ? (kk / 4) * (C::kD * 128) + (kk % 4) * 32 : kk * (C::kKStep * 128);
-          mma_ts<C::kTf32>(tmem + C::kColO + t * C::kD, tmem + pcol + kk * 8, vd + (voff >> 4), idPV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 1; kk < C::kBN / C::kKStep; ++kk) {
+          const uint32_t voff = C::kTf32 ? ((kk / 4) * (C::kD * 128) + (kk % 4) * 32) >> 4 : (kk * (C::kKStep * 128)) >> 4;
+          mma_ts_lh<C::kTf32, 1>(dst, src + kk * 8, va + voff, v_hi, idPV, 1u);
         }
       };
 
       bool ok = true;
-      for (int t = 0; t < C::kNQT && ok; ++t) {
+      for (int t = t_begin; t < t_end && ok; ++t) {
         if (nblk[t] == 0) continue;
         ok = C::kTf32 ? wait_bounded(&ctl->q_ready[t], 0, abort_flag, p.status, p.timeout_cycles)
                       : wait_bounded(&ctl->q_full[t], 0, abort_flag, p.status, p.timeout_cycles);
       }
-      // K_0 -> S_t,0 for every tile
+      // K_0 -> S_t,0 for every tile of this issuer
       if (ok) {
         ok = C::kTf32 ? wait_bounded(&ctl->k_ready[0], 0, abort_flag, p.status, p.timeout_cycles)
                       : wait_bounded(&ctl->k_full[0], 0, abort_flag, p.status, p.timeout_cycles);
       }
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < C::kNQT; ++t) {
+        for (int t = t_begin; t < t_end; ++t) {
           if (nblk[t] == 0) continue;
           issue_S(t, 0);
           mma_commit(&ctl->s_full[t]);
@@ -500,8 +516,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           return C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
                           : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
         };
-#pragma unroll
-        for (int t = 0; t < C::kNQT; ++t) {
+        for (int t = t_begin; t < t_end; ++t) {
           if (!ok || j >= nblk[t]) continue;
           ok = wait_bounded(&ctl->p_ready[t], j & 1, abort_flag, p.status, p.timeout_cycles);
           if (!ok) break;
@@ -531,15 +546,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
         if (next) {
           // Tiles that stop earlier (causal) never waited on K_{j+1}; make sure
-          // it landed before its slot is handed back.
+          // it landed before this issuer's release of its slot.
           ok = wait_k();
           if (!ok) break;
           mma_commit(&ctl->k_empty[kslot]);
         }
       }
       // Drain: every MMA this thread issued completes before TMEM is freed.
-      mma_commit(&ctl->drain);
-      wait_bounded(&ctl->drain, 0, abort_flag, p.status, kDrainCycles, false);
+      mma_commit(&ctl->drain[issuer]);
+      wait_bounded(&ctl->drain[issuer], 0, abort_flag, p.status, kDrainCycles, false);
     }
     __syncwarp();
   } else {
@@ -618,15 +633,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                              (p.causal && kbase + C::kBN - 1 > r0);
       if (need_mask) apply_mask<C>(s, p, b, h, row, kbase);
 
+      // Row max: three-input max, four independent chains.
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < C::kBN; c += 4) {
-        mx4[0] = fmaxf(mx4[0], s[c + 0]);
-        mx4[1] = fmaxf(mx4[1], s[c + 1]);
-        mx4[2] = fmaxf(mx4[2], s[c + 2]);
-        mx4[3] = fmaxf(mx4[3], s[c + 3]);
+      for (int c = 0; c < C::kBN; c += 8) {
+        mx4[0] = fmax3(mx4[0], s[c + 0], s[c + 1]);
+        mx4[1] = fmax3(mx4[1], s[c + 2], s[c + 3]);
+        mx4[2] = fmax3(mx4[2], s[c + 4], s[c + 5]);
+        mx4[3] = fmax3(mx4[3], s[c + 6], s[c + 7]);
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
       const float m_blk = mx * sl;  // -inf stays -inf (sl > 0 whenever it is not 1)
       const float m_new = fmaxf(m_run, m_blk);
       float corr = 1.0f;
@@ -639,32 +655,37 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
       // P = 2^(s*sl - m): fp32 sum, stored to TMEM as bf16 pairs or tf32.
       const uint32_t tP = C::kAliasP ? tS : (tmem + lane_addr + C::kColP + (j & 1) * C::kPCols);
-      float sum2[2] = {0.0f, 0.0f};
+      // Pairs of scores go through packed fp32x2 FMA / add; the exponentials
+      // through the SFU one at a time.  Two packed partial sums.
+      float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int cc = 0; cc < C::kBN / 32; ++cc) {
         if constexpr (C::kTf32) {
           uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float pv = ex2(fmaf(s[cc * 32 + e], sl, -msub));
-            sum2[e & 1] += pv;
-            pk[e] = to_tf32(pv);
+          for (int e = 0; e < 16; ++e) {
+            float x0, x1;
+            ffma2(x0, x1, s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1], sl, sl, -msub, -msub);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
+            pk[2 * e] = to_tf32(p0);
+            pk[2 * e + 1] = to_tf32(p1);
           }
           tmem_st32(tP + cc * 32, pk);
         } else {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(s[cc * 32 + 2 * e], sl, -msub));
-            const float p1 = ex2(fmaf(s[cc * 32 + 2 * e + 1], sl, -msub));
-            sum2[0] += p0;
-            sum2[1] += p1;
+            float x0, x1;
+            ffma2(x0, x1, s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1], sl, sl, -msub, -msub);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st16(tP + cc * 16, pk);
         }
       }
-      l_run = l_run * corr + (sum2[0] + sum2[1]);
+      l_run = l_run * corr + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
 
       // Rescale this warp's O rows once the previous PV has landed.
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -678,7 +699,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tmem_wait_ld();
           reg_fence(r);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+          for (int e = 0; e < 32; e += 2) {
+            float o0, o1;
+            fmul2(o0, o1, __uint_as_float(r[e]), __uint_as_float(r[e + 1]), corr, corr);
+            r[e] = __float_as_uint(o0);
+            r[e + 1] = __float_as_uint(o1);
+          }
           tmem_st32(tO + cc * 32, r);
         }
       }
