@@ -33,6 +33,7 @@ std::mutex g_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
 int g_num_sms[kMaxDevices] = {0};
 long long g_timeout_cycles = 0;  // 0: not yet initialised
+int g_max_ctas = 0;              // 0: one CTA per SM
 EncodeTiledFn g_encode = nullptr;
 bool g_encode_tried = false;
 
@@ -241,6 +242,10 @@ int fa_fwd_ex(const fa_fwd_args* a) {
   la.status = g_status_ptr[dev];
   la.timeout_cycles = timeout_cycles();
   la.num_sms = g_num_sms[dev];
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    la.max_ctas = g_max_ctas;
+  }
 
   const bool f32 = a->dtype == FA_DTYPE_F32;
   switch (a->D) {
@@ -327,6 +332,11 @@ void fa_set_timeout_cycles(long long cycles) {
   fa::g_timeout_cycles = cycles > 0 ? cycles : fa::kDefaultTimeout;
 }
 
-int fa_version(void) { return 100; }
+void fa_set_max_ctas(int n) {
+  std::lock_guard<std::mutex> lk(fa::g_mu);
+  fa::g_max_ctas = n > 0 ? n : 0;
+}
+
+int fa_version(void) { return 101; }
 
 }  // extern "C"

@@ -74,11 +74,6 @@ struct Cfg {
   static constexpr int kVTStages = kVTStages_;
   static constexpr int kKStep = kTf32 ? 8 : 16;       // MMA K per instruction (32 bytes)
   static constexpr bool kAliasP = (kNQT == 2);        // P over S; PV issued before the next S
-  // Threads issuing MMAs (tile t's MMAs come from warp 1 + t when 2).
-  // Measured: with one issuer per tile the two tiles drift into lockstep
-  // (both softmaxes at once, then both tiles' MMAs) and the tensor core idles;
-  // one issuer keeps the ping-pong order.  The code supports 2 for study.
-  static constexpr int kIssuers = 1;
   static constexpr int kPCols = kTf32 ? kBN : kBN / 2;  // TMEM columns of one P tile
   static constexpr int kColO = kNQT * kBN;            // first O column
   static constexpr int kColP = kColO + kNQT * kD;     // P double buffer (non-aliased mode)
@@ -116,6 +111,7 @@ struct Cfg {
 template <class C>
 struct Ctrl {
   uint64_t q_full[2];             // TMA -> Q tile t landed
+  uint64_t q_empty[2];            // the unit's last S of tile t done: Q_t may be reloaded
   uint64_t q_ready[2];            // (tf32) Q tile t rounded in place
   uint64_t k_full[4], k_empty[4], k_ready[4];
   uint64_t v_full[4], v_empty[4];
@@ -123,7 +119,8 @@ struct Ctrl {
   uint64_t s_full[2];             // S_t computed (commit)
   uint64_t p_ready[2];            // softmax t wrote P (and rescaled O)
   uint64_t o_ready[2];            // PV_t completed (commit)
-  uint64_t drain[2];              // MMA drain at exit, one per issuing thread
+  uint64_t o_free[2];             // epilogue read O_t out of TMEM
+  uint64_t drain;                 // MMA drain at exit
   uint32_t tmem_base;
   int abort;
 };
@@ -307,11 +304,97 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
     if (c >= lim) s[c] = -INFINITY;
 }
 
+// Row max of s (raw or base-2 scores): three-input max, four chains.
+template <class C>
+__device__ __forceinline__ float row_max(const float (&s)[C::kBN]) {
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < C::kBN; c += 8) {
+    mx4[0] = fmax3(mx4[0], s[c + 0], s[c + 1]);
+    mx4[1] = fmax3(mx4[1], s[c + 2], s[c + 3]);
+    mx4[2] = fmax3(mx4[2], s[c + 4], s[c + 5]);
+    mx4[3] = fmax3(mx4[3], s[c + 6], s[c + 7]);
+  }
+  return fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
+}
+
+// One pass over a row: p = 2^(s*sl - msub) stored to TMEM at tP (bf16 pairs,
+// or tf32), the fp32 sum of p, and with kWithMax the row max of s on the
+// side.  Pairs of scores go through packed fp32x2 FMA / add; the
+// exponentials through the SFU one at a time.
+template <class C, bool kWithMax>
+__device__ __forceinline__ void p_pass(const float (&s)[C::kBN], float sl, float msub, uint32_t tP, float& sum,
+                                       float& mx) {
+  float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int cc = 0; cc < C::kBN / 32; ++cc) {
+    uint32_t pk[C::kTf32 ? 32 : 16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float s0 = s[cc * 32 + 2 * e], s1 = s[cc * 32 + 2 * e + 1];
+      if constexpr (kWithMax) mx4[e & 3] = fmax3(mx4[e & 3], s0, s1);
+      float x0, x1;
+      ffma2(x0, x1, s0, s1, sl, sl, -msub, -msub);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
+      if constexpr (C::kTf32) {
+        pk[2 * e] = to_tf32(p0);
+        pk[2 * e + 1] = to_tf32(p1);
+      } else {
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+    }
+    if constexpr (C::kTf32)
+      tmem_st32(tP + cc * 32, pk);
+    else
+      tmem_st16(tP + cc * 16, pk);
+  }
+  sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+  if constexpr (kWithMax) mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
+}
+
+// One work unit: kNQT consecutive 128-row Q tiles of one (batch, head).
+struct Unit {
+  int b, h, kvh, q0, N;
+  int nblk[2];  // KV tiles each Q tile visits (0: the tile has no rows)
+};
+
+template <class C>
+__device__ __forceinline__ Unit decode_unit(const FaParams& p, int u) {
+  // Heavy causal query blocks first; consecutive units are consecutive heads,
+  // so the H_q / H_kv heads sharing a K/V head run side by side (L2 reuse).
+  Unit w;
+  const int per_q = p.B * p.Hq;
+  const int qb_rev = u / per_q;
+  const int rem = u - qb_rev * per_q;
+  const int qb = p.causal ? (p.n_qblocks - 1 - qb_rev) : qb_rev;
+  w.b = rem / p.Hq;
+  w.h = rem - w.b * p.Hq;
+  w.kvh = w.h / p.group;
+  w.q0 = qb * (C::kBM * C::kNQT);
+  w.nblk[0] = tile_kv_blocks<C>(p, w.q0);
+  w.nblk[1] = (C::kNQT == 2) ? tile_kv_blocks<C>(p, w.q0 + C::kBM) : 0;
+  w.N = max(w.nblk[0], w.nblk[1]);
+  return w;
+}
+
+// The r-th unit of this CTA: a boustrophedon ("snake") walk over the
+// heavy-first unit list, so each CTA's total work stays balanced; -1 when done.
+__device__ __forceinline__ int unit_of(int r, int num_units) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int idx = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return idx < num_units ? idx : -1;
+}
+
+// Persistent forward kernel: each CTA walks its units; every role carries its
+// barrier phase counters from one unit to the next, so the next unit's Q and
+// K/V loads and its first S MMAs overlap the current unit's last blocks and
+// epilogue.
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const FaParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const FaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -323,41 +406,28 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit: (query block, batch, head); heavy causal blocks first,
-  //      consecutive CTAs share a K/V head (GQA) so K/V stay hot in L2.
-  const int per_q = p.B * p.Hq;
-  const int qb_rev = blockIdx.x / per_q;
-  const int rem = blockIdx.x - qb_rev * per_q;
-  const int qb = p.causal ? (p.n_qblocks - 1 - qb_rev) : qb_rev;
-  const int b = rem / p.Hq;
-  const int h = rem - b * p.Hq;
-  const int kvh = h / p.group;
-  const int q0 = qb * (C::kBM * C::kNQT);
-  int nblk[2];
-  nblk[0] = tile_kv_blocks<C>(p, q0);
-  nblk[1] = (C::kNQT == 2) ? tile_kv_blocks<C>(p, q0 + C::kBM) : 0;
-  const int N = max(nblk[0], nblk[1]);
+  const int num_units = p.n_qblocks * p.B * p.Hq;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl->q_full[t], 1);
+      mbar_init(&ctl->q_empty[t], 1);    // MMA commit after the unit's last S of tile t
       mbar_init(&ctl->q_ready[t], 2);    // one arrival per tf32 helper warp
       mbar_init(&ctl->s_full[t], 1);
       mbar_init(&ctl->p_ready[t], 4);    // one arrival per softmax warp
       mbar_init(&ctl->o_ready[t], 1);
+      mbar_init(&ctl->o_free[t], 4);     // one arrival per softmax warp after reading O
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&ctl->k_full[s], 1);
-      mbar_init(&ctl->k_empty[s], C::kIssuers);  // one commit per issuing thread
+      mbar_init(&ctl->k_empty[s], 1);
       mbar_init(&ctl->k_ready[s], 2);
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : C::kIssuers);  // tf32: released by the two transposing warps
+      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : 1);  // tf32: released by the two transposing warps
       mbar_init(&ctl->vt_full[s], 2);
-      mbar_init(&ctl->vt_empty[s], C::kIssuers);
+      mbar_init(&ctl->vt_empty[s], 1);
     }
-    mbar_init(&ctl->drain[0], 1);
-    mbar_init(&ctl->drain[1], 1);
+    mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -365,7 +435,6 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, C::kTmemCols);
@@ -382,44 +451,58 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   if (warp == 0) {
     // ===================================================== TMA producer
     if (lane == 0) {
-      int k_issued = 0, v_issued = 0;
-      bool q_issued[2] = {false, false};
-#pragma unroll
-      for (int t = 0; t < C::kNQT; ++t) {
-        if (nblk[t] == 0) continue;
-        mbar_arrive_expect_tx(&ctl->q_full[t], C::kQTileBytes);
-#pragma unroll
-        for (int c = 0; c < C::kNChunk; ++c)
-          tma_load_4d(sQ + t * C::kQTileBytes + c * (C::kBM * 128), &tmQ, &ctl->q_full[t], c * C::kChunk,
-                      q0 + t * C::kBM, h, b);
-        q_issued[t] = true;
-      }
-      for (int j = 0; j < N; ++j) {
-        {  // K_j
-          const int slot = j % C::kKStages, use = j / C::kKStages;
-          if (!wait_bounded(&ctl->k_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles)) break;
-          mbar_arrive_expect_tx(&ctl->k_full[slot], C::kKVTileBytes);
-          uint8_t* dst = sK + slot * C::kKVTileBytes;
+      int k_issued = 0, v_issued = 0;  // ring items issued (all units)
+      int q_issued[2] = {0, 0};        // Q loads issued per tile
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(r, num_units);
+        if (u < 0) break;
+        const Unit w = decode_unit<C>(p, u);
+        for (int t = 0; t < C::kNQT && ok; ++t) {
+          if (w.nblk[t] == 0) continue;
+          // Q_t's shared memory is free once the previous unit's last S_t completed.
+          if (q_issued[t] > 0)
+            ok = wait_bounded(&ctl->q_empty[t], (q_issued[t] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&ctl->q_full[t], C::kQTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kNChunk; ++c)
-            tma_load_4d(dst + c * (C::kBN * 128), &tmK, &ctl->k_full[slot], c * C::kChunk, j * C::kBN, kvh, b);
-          ++k_issued;
+            tma_load_4d(sQ + t * C::kQTileBytes + c * (C::kBM * 128), &tmQ, &ctl->q_full[t], c * C::kChunk,
+                        w.q0 + t * C::kBM, w.h, w.b);
+          ++q_issued[t];
         }
-        {  // V_j
-          const int slot = j % C::kVStages, use = j / C::kVStages;
-          if (!wait_bounded(&ctl->v_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles)) break;
-          mbar_arrive_expect_tx(&ctl->v_full[slot], C::kKVTileBytes);
-          uint8_t* dst = sV + slot * C::kKVTileBytes;
+        for (int j = 0; j < w.N && ok; ++j) {
+          {  // K_j
+            const int slot = k_issued % C::kKStages, use = k_issued / C::kKStages;
+            ok = wait_bounded(&ctl->k_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&ctl->k_full[slot], C::kKVTileBytes);
+            uint8_t* dst = sK + slot * C::kKVTileBytes;
 #pragma unroll
-          for (int c = 0; c < C::kNChunk; ++c)
-            tma_load_4d(dst + c * (C::kBN * 128), &tmV, &ctl->v_full[slot], c * C::kChunk, j * C::kBN, kvh, b);
-          ++v_issued;
+            for (int c = 0; c < C::kNChunk; ++c)
+              tma_load_4d(dst + c * (C::kBN * 128), &tmK, &ctl->k_full[slot], c * C::kChunk, j * C::kBN, w.kvh,
+                          w.b);
+            ++k_issued;
+          }
+          {  // V_j
+            const int slot = v_issued % C::kVStages, use = v_issued / C::kVStages;
+            ok = wait_bounded(&ctl->v_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&ctl->v_full[slot], C::kKVTileBytes);
+            uint8_t* dst = sV + slot * C::kKVTileBytes;
+#pragma unroll
+            for (int c = 0; c < C::kNChunk; ++c)
+              tma_load_4d(dst + c * (C::kBN * 128), &tmV, &ctl->v_full[slot], c * C::kChunk, j * C::kBN, w.kvh,
+                          w.b);
+            ++v_issued;
+          }
         }
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA lets go of its memory.
         for (int t = 0; t < 2; ++t)
-          if (q_issued[t]) wait_bounded(&ctl->q_full[t], 0, abort_flag, p.status, kDrainCycles, false);
+          if (q_issued[t] > 0)
+            wait_bounded(&ctl->q_full[t], (q_issued[t] - 1) & 1, abort_flag, p.status, kDrainCycles, false);
         for (int it = max(0, k_issued - C::kKStages); it < k_issued; ++it)
           wait_bounded(&ctl->k_full[it % C::kKStages], (it / C::kKStages) & 1, abort_flag, p.status,
                        kDrainCycles, false);
@@ -428,15 +511,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                        kDrainCycles, false);
       }
     }
-  } else if (warp == 1 || (C::kIssuers == 2 && warp == 2)) {
-    // ===================================================== MMA issuer (warp 1, and warp 2 with two issuers)
-    // Issuer i handles Q tiles [t_begin, t_end).  Every issuer walks all K/V
-    // tiles in order and commits its own arrival on each release barrier, so
-    // each release phase sees exactly kIssuers arrivals even when one tile
-    // stops early (causal).
-    const int issuer = warp - 1;
-    const int t_begin = C::kIssuers == 1 ? 0 : issuer;
-    const int t_end = C::kIssuers == 1 ? C::kNQT : issuer + 1;
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer (one thread)
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(C::kTf32, 128, C::kBN, false, false);
       constexpr uint32_t idPV = make_idesc(C::kTf32, 128, C::kD, false, !C::kTf32);
@@ -479,118 +555,154 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       };
 
+      int k_used = 0, v_used = 0;   // ring items consumed (all units)
+      int q_used[2] = {0, 0};       // Q loads consumed per tile
+      int p_seen[2] = {0, 0};       // p_ready phases consumed per tile
+      int units_done[2] = {0, 0};   // units with a non-empty tile t (o_free phases to wait)
       bool ok = true;
-      for (int t = t_begin; t < t_end && ok; ++t) {
-        if (nblk[t] == 0) continue;
-        ok = C::kTf32 ? wait_bounded(&ctl->q_ready[t], 0, abort_flag, p.status, p.timeout_cycles)
-                      : wait_bounded(&ctl->q_full[t], 0, abort_flag, p.status, p.timeout_cycles);
-      }
-      // K_0 -> S_t,0 for every tile of this issuer
-      if (ok) {
-        ok = C::kTf32 ? wait_bounded(&ctl->k_ready[0], 0, abort_flag, p.status, p.timeout_cycles)
-                      : wait_bounded(&ctl->k_full[0], 0, abort_flag, p.status, p.timeout_cycles);
-      }
-      if (ok) {
-        tc_fence_after();
-        for (int t = t_begin; t < t_end; ++t) {
-          if (nblk[t] == 0) continue;
-          issue_S(t, 0);
-          mma_commit(&ctl->s_full[t]);
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(r, num_units);
+        if (u < 0) break;
+        const Unit w = decode_unit<C>(p, u);
+        for (int t = 0; t < C::kNQT && ok; ++t) {
+          if (w.nblk[t] == 0) continue;
+          const uint32_t par = q_used[t] & 1;
+          ok = C::kTf32 ? wait_bounded(&ctl->q_ready[t], par, abort_flag, p.status, p.timeout_cycles)
+                        : wait_bounded(&ctl->q_full[t], par, abort_flag, p.status, p.timeout_cycles);
+          ++q_used[t];
         }
-        mma_commit(&ctl->k_empty[0]);
-      }
-      for (int j = 0; j < N && ok; ++j) {
-        // bf16: V ring slot; tf32: V^T ring slot
-        const int vslot = C::kTf32 ? j % C::kVTStages : j % C::kVStages;
-        const uint32_t vpar = (C::kTf32 ? j / C::kVTStages : j / C::kVStages) & 1;
-        ok = C::kTf32 ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
-                      : wait_bounded(&ctl->v_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles);
+        // K_0 -> S_t,0 for every tile
+        int kslot = k_used % C::kKStages;
+        if (ok) {
+          const uint32_t par = (k_used / C::kKStages) & 1;
+          ok = C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
+                        : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
+        }
         if (!ok) break;
-        const bool next = (j + 1 < N);
-        const int kslot = (j + 1) % C::kKStages;
-        bool k_waited = false;
-        auto wait_k = [&]() -> bool {
-          if (k_waited) return true;
-          k_waited = true;
-          const uint32_t par = ((j + 1) / C::kKStages) & 1;
-          return C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
-                          : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
-        };
-        for (int t = t_begin; t < t_end; ++t) {
-          if (!ok || j >= nblk[t]) continue;
-          ok = wait_bounded(&ctl->p_ready[t], j & 1, abort_flag, p.status, p.timeout_cycles);
+        tc_fence_after();
+        for (int t = 0; t < C::kNQT; ++t) {
+          if (w.nblk[t] == 0) continue;
+          issue_S(t, kslot);
+          mma_commit(&ctl->s_full[t]);
+          if (w.nblk[t] == 1) mma_commit(&ctl->q_empty[t]);  // the unit's last S of tile t
+        }
+        mma_commit(&ctl->k_empty[kslot]);
+        ++k_used;
+        for (int j = 0; j < w.N && ok; ++j) {
+          // bf16: V ring slot; tf32: V^T ring slot
+          const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
+          const uint32_t vpar = (C::kTf32 ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
+          ok = C::kTf32 ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
+                        : wait_bounded(&ctl->v_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles);
           if (!ok) break;
-          const bool s_next = (j + 1 < nblk[t]);
-          if (s_next) {
+          const bool next = (j + 1 < w.N);
+          kslot = k_used % C::kKStages;
+          bool k_waited = false;
+          auto wait_k = [&]() -> bool {
+            if (k_waited) return true;
+            k_waited = true;
+            const uint32_t par = (k_used / C::kKStages) & 1;
+            return C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
+                            : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
+          };
+          for (int t = 0; t < C::kNQT; ++t) {
+            if (!ok || j >= w.nblk[t]) continue;
+            ok = wait_bounded(&ctl->p_ready[t], p_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
+            ++p_seen[t];
+            // The unit's first PV overwrites O_t: the previous unit's epilogue must have read it.
+            if (ok && j == 0 && units_done[t] > 0)
+              ok = wait_bounded(&ctl->o_free[t], (units_done[t] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
+            if (!ok) break;
+            const bool s_next = (j + 1 < w.nblk[t]);
+            const bool s_last = (j + 2 == w.nblk[t]);  // S_{t,j+1} is the unit's last S of tile t
+            if (s_next) {
+              ok = wait_k();
+              if (!ok) break;
+            }
+            tc_fence_after();
+            if (C::kAliasP) {
+              issue_PV(t, j, vslot);
+              if (!s_next) mma_commit(&ctl->o_ready[t]);  // the tile's last PV of the unit
+              if (s_next) {
+                issue_S(t, kslot);
+                mma_commit(&ctl->s_full[t]);
+                if (s_last) mma_commit(&ctl->q_empty[t]);
+              }
+            } else {
+              if (s_next) {
+                issue_S(t, kslot);
+                mma_commit(&ctl->s_full[t]);
+                if (s_last) mma_commit(&ctl->q_empty[t]);
+              }
+              issue_PV(t, j, vslot);
+              mma_commit(&ctl->o_ready[t]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
+          ++v_used;
+          if (next) {
+            // Tiles that stop earlier (causal) never waited on K_{j+1}; make sure
+            // it landed before its slot is handed back.
             ok = wait_k();
             if (!ok) break;
-          }
-          tc_fence_after();
-          if (C::kAliasP) {
-            issue_PV(t, j, vslot);
-            mma_commit(&ctl->o_ready[t]);
-            if (s_next) {
-              issue_S(t, kslot);
-              mma_commit(&ctl->s_full[t]);
-            }
-          } else {
-            if (s_next) {
-              issue_S(t, kslot);
-              mma_commit(&ctl->s_full[t]);
-            }
-            issue_PV(t, j, vslot);
-            mma_commit(&ctl->o_ready[t]);
+            mma_commit(&ctl->k_empty[kslot]);
+            ++k_used;
           }
         }
-        if (!ok) break;
-        mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
-        if (next) {
-          // Tiles that stop earlier (causal) never waited on K_{j+1}; make sure
-          // it landed before this issuer's release of its slot.
-          ok = wait_k();
-          if (!ok) break;
-          mma_commit(&ctl->k_empty[kslot]);
-        }
+        for (int t = 0; t < C::kNQT; ++t)
+          if (w.nblk[t] > 0) ++units_done[t];
       }
       // Drain: every MMA this thread issued completes before TMEM is freed.
-      mma_commit(&ctl->drain[issuer]);
-      wait_bounded(&ctl->drain[issuer], 0, abort_flag, p.status, kDrainCycles, false);
+      mma_commit(&ctl->drain);
+      wait_bounded(&ctl->drain, 0, abort_flag, p.status, kDrainCycles, false);
     }
     __syncwarp();
   } else {
     // ===================================================== tf32 rounding (fp32 I/O only)
     if constexpr (C::kTf32) {
       const int ct = threadIdx.x - 64;  // 0..63
+      int q_seen[2] = {0, 0};
+      int k_seen = 0, v_seen = 0;
       bool ok = true;
-      for (int t = 0; t < C::kNQT && ok; ++t) {
-        if (nblk[t] == 0) continue;
-        ok = warp_wait(&ctl->q_full[t], 0, abort_flag, p.status, p.timeout_cycles);
-        if (!ok) break;
-        round_tf32_inplace(sQ + t * C::kQTileBytes, C::kQTileBytes, ct, 64);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
-      }
-      for (int j = 0; j < N && ok; ++j) {
-        const int slot = j % C::kKStages;
-        ok = warp_wait(&ctl->k_full[slot], (j / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
-        if (!ok) break;
-        round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, 64);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
-        // V_j -> V^T_j (K-major), then hand the V slot back to the producer.
-        const int vs = j % C::kVStages, ts = j % C::kVTStages;
-        ok = warp_wait(&ctl->v_full[vs], (j / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
-        if (!ok) break;
-        ok = warp_wait(&ctl->vt_empty[ts], ((j / C::kVTStages) & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
-        if (!ok) break;
-        transpose_v_tile<C>(sV + vs * C::kKVTileBytes, sVT + ts * C::kKVTileBytes, ct, 64);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ctl->vt_full[ts]);
-          mbar_arrive(&ctl->v_empty[vs]);
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(r, num_units);
+        if (u < 0) break;
+        const Unit w = decode_unit<C>(p, u);
+        for (int t = 0; t < C::kNQT && ok; ++t) {
+          if (w.nblk[t] == 0) continue;
+          ok = warp_wait(&ctl->q_full[t], q_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
+          ++q_seen[t];
+          if (!ok) break;
+          round_tf32_inplace(sQ + t * C::kQTileBytes, C::kQTileBytes, ct, 64);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
+        }
+        for (int j = 0; j < w.N && ok; ++j) {
+          const int slot = k_seen % C::kKStages;
+          ok = warp_wait(&ctl->k_full[slot], (k_seen / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
+          ++k_seen;
+          if (!ok) break;
+          round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, 64);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
+          // V_j -> V^T_j (K-major), then hand the V slot back to the producer.
+          const int vs = v_seen % C::kVStages, ts = v_seen % C::kVTStages;
+          ok = warp_wait(&ctl->v_full[vs], (v_seen / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          ok = warp_wait(&ctl->vt_empty[ts], ((v_seen / C::kVTStages) & 1) ^ 1, abort_flag, p.status,
+                         p.timeout_cycles);
+          ++v_seen;
+          if (!ok) break;
+          transpose_v_tile<C>(sV + vs * C::kKVTileBytes, sVT + ts * C::kKVTileBytes, ct, 64);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&ctl->vt_full[ts]);
+            mbar_arrive(&ctl->v_empty[vs]);
+          }
         }
       }
     }
@@ -600,173 +712,149 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if constexpr (C::kRegsSoftmax > 0) regs_inc<C::kRegsSoftmax>();
     const int t = (warp - 4) >> 2;
     const int tl = threadIdx.x - 128 * (1 + t);   // 0..127 = TMEM lane = tile row
-    const int r0 = q0 + t * C::kBM;
-    const int row = r0 + tl;
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + t * C::kBN;
     const uint32_t tO = tmem + lane_addr + C::kColO + t * C::kD;
-    const int nb = nblk[t];
     const float sl = p.pre_scale ? 1.0f : p.scale_log2;
-
-    float m_run = -INFINITY;  // running max, base 2 (scaled)
-    float l_run = 0.0f;       // running sum of 2^(s - m_run)
+    int blocks_seen = 0;  // s_full phases consumed (all units)
+    int units_seen = 0;   // units with rows in this tile (o_ready phases with P over S)
     bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      ok = warp_wait(&ctl->s_full[t], j & 1, abort_flag, p.status, p.timeout_cycles);
+    for (int r = 0; ok; ++r) {
+      const int u = unit_of(r, num_units);
+      if (u < 0) break;
+      const Unit w = decode_unit<C>(p, u);
+      const int nb = w.nblk[t];
+      if (nb == 0) continue;
+      const int b = w.b, h = w.h;
+      const int r0 = w.q0 + t * C::kBM;
+      const int row = r0 + tl;
+      float m_run = -INFINITY;  // running max, base 2 (scaled)
+      float l_run = 0.0f;       // running sum of 2^(s - m_run)
+      for (int j = 0; j < nb; ++j) {
+        ok = warp_wait(&ctl->s_full[t], blocks_seen & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        ++blocks_seen;
+        tc_fence_after();
+
+        float s[C::kBN];
+        {
+          uint32_t rr[C::kBN];
+#pragma unroll
+          for (int cc = 0; cc < C::kBN / 32; ++cc)
+            tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[cc * 32]));
+          tmem_wait_ld();
+          reg_fence(rr);
+#pragma unroll
+          for (int c = 0; c < C::kBN; ++c) s[c] = __uint_as_float(rr[c]);
+        }
+
+        const int kbase = j * C::kBN;
+        const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + C::kBN > p.kL ||
+                               (p.causal && kbase + C::kBN - 1 > r0);
+        if (need_mask) apply_mask<C>(s, p, b, h, row, kbase);
+
+        const float mx = row_max<C>(s);
+        const float m_blk = mx * sl;  // -inf stays -inf (sl > 0 whenever it is not 1)
+        const float m_new = fmaxf(m_run, m_blk);
+        float corr = 1.0f;
+        const bool resc = m_new > m_run + kRescaleThreshold;
+        if (resc) {
+          corr = ex2(m_run - m_new);  // 0 when m_run = -inf
+          m_run = m_new;
+        }
+        const float msub = (m_run == -INFINITY) ? 0.0f : m_run;
+
+        // P = 2^(s*sl - m): fp32 sum, stored to TMEM as bf16 pairs or tf32.
+        const uint32_t tP = C::kAliasP ? tS : (tmem + lane_addr + C::kColP + (j & 1) * C::kPCols);
+        float sum, unused;
+        p_pass<C, false>(s, sl, msub, tP, sum, unused);
+        l_run = l_run * corr + sum;
+
+        // Rescale this warp's O rows once the previous PV has landed (with P
+        // over S, S_j's completion already implies it: PV_{j-1} was issued first).
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          if constexpr (!C::kAliasP) {
+            ok = warp_wait(&ctl->o_ready[t], (blocks_seen - 2) & 1, abort_flag, p.status, p.timeout_cycles);
+            if (!ok) break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < C::kD / 32; ++cc) {
+            uint32_t rr[32];
+            tmem_ld32(tO + cc * 32, rr);
+            tmem_wait_ld();
+            reg_fence(rr);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float o0, o1;
+              fmul2(o0, o1, __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]), corr, corr);
+              rr[e] = __float_as_uint(o0);
+              rr[e + 1] = __float_as_uint(o1);
+            }
+            tmem_st32(tO + cc * 32, rr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_ready[t]);
+      }
+      if (!ok) break;
+
+      // ---- epilogue: O / l from TMEM -> I/O dtype -> global (any strides); L.
+      // o_ready completes once per PV without P over S, once per unit with it.
+      ok = warp_wait(&ctl->o_ready[t], C::kAliasP ? (uint32_t)(units_seen & 1) : (uint32_t)((blocks_seen - 1) & 1),
+                     abort_flag, p.status, p.timeout_cycles);
+      ++units_seen;
       if (!ok) break;
       tc_fence_after();
-
-      float s[C::kBN];
-      {
-        uint32_t r[C::kBN];
-#pragma unroll
-        for (int cc = 0; cc < C::kBN / 32; ++cc)
-          tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[cc * 32]));
-        tmem_wait_ld();
-        reg_fence(r);
-#pragma unroll
-        for (int c = 0; c < C::kBN; ++c) s[c] = __uint_as_float(r[c]);
-      }
-
-      const int kbase = j * C::kBN;
-      const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + C::kBN > p.kL ||
-                             (p.causal && kbase + C::kBN - 1 > r0);
-      if (need_mask) apply_mask<C>(s, p, b, h, row, kbase);
-
-      // Row max: three-input max, four independent chains.
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < C::kBN; c += 8) {
-        mx4[0] = fmax3(mx4[0], s[c + 0], s[c + 1]);
-        mx4[1] = fmax3(mx4[1], s[c + 2], s[c + 3]);
-        mx4[2] = fmax3(mx4[2], s[c + 4], s[c + 5]);
-        mx4[3] = fmax3(mx4[3], s[c + 6], s[c + 7]);
-      }
-      const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
-      const float m_blk = mx * sl;  // -inf stays -inf (sl > 0 whenever it is not 1)
-      const float m_new = fmaxf(m_run, m_blk);
-      float corr = 1.0f;
-      const bool resc = m_new > m_run + kRescaleThreshold;
-      if (resc) {
-        corr = ex2(m_run - m_new);  // 0 when m_run = -inf
-        m_run = m_new;
-      }
-      const float msub = (m_run == -INFINITY) ? 0.0f : m_run;
-
-      // P = 2^(s*sl - m): fp32 sum, stored to TMEM as bf16 pairs or tf32.
-      const uint32_t tP = C::kAliasP ? tS : (tmem + lane_addr + C::kColP + (j & 1) * C::kPCols);
-      // Pairs of scores go through packed fp32x2 FMA / add; the exponentials
-      // through the SFU one at a time.  Two packed partial sums.
-      float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int cc = 0; cc < C::kBN / 32; ++cc) {
-        if constexpr (C::kTf32) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0, x1;
-            ffma2(x0, x1, s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1], sl, sl, -msub, -msub);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
-            pk[2 * e] = to_tf32(p0);
-            pk[2 * e + 1] = to_tf32(p1);
-          }
-          tmem_st32(tP + cc * 32, pk);
-        } else {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0, x1;
-            ffma2(x0, x1, s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1], sl, sl, -msub, -msub);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tP + cc * 16, pk);
-        }
-      }
-      l_run = l_run * corr + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-
-      // Rescale this warp's O rows once the previous PV has landed.
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        ok = warp_wait(&ctl->o_ready[t], (j - 1) & 1, abort_flag, p.status, p.timeout_cycles);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < C::kD / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(tO + cc * 32, r);
-          tmem_wait_ld();
-          reg_fence(r);
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float o0, o1;
-            fmul2(o0, o1, __uint_as_float(r[e]), __uint_as_float(r[e + 1]), corr, corr);
-            r[e] = __float_as_uint(o0);
-            r[e + 1] = __float_as_uint(o1);
-          }
-          tmem_st32(tO + cc * 32, r);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->p_ready[t]);
-    }
-
-    // ---- epilogue: O / l -> I/O dtype -> swizzled smem (the dead Q tile) -> TMA store; L.
-    if (ok && nb > 0) ok = warp_wait(&ctl->o_ready[t], (nb - 1) & 1, abort_flag, p.status, p.timeout_cycles);
-    const bool do_out = ok && nb > 0;
-    uint8_t* stage = sQ + t * C::kQTileBytes;
-    if (do_out) {
-      tc_fence_after();
       const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      const bool store = row < p.qL;
+      uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                      ((long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(store ? row : 0) * p.o_ss) * C::kEsz;
 #pragma unroll
       for (int cc = 0; cc < C::kD / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tO + cc * 32, r);
+        uint32_t rr[32];
+        tmem_ld32(tO + cc * 32, rr);
         tmem_wait_ld();
-        reg_fence(r);
-        if constexpr (C::kTf32) {
-          // 32 fp32 = one 128-byte row of column block cc
-          uint8_t* rowp = stage + cc * (C::kBM * 128) + tl * 128;
+        reg_fence(rr);
+        if (cc == C::kD / 32 - 1) {
+          // O_t is read: the next unit's first PV may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->o_free[t]);
+        }
+        if (store) {
+          if constexpr (C::kTf32) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 w;
-            w.x = __float_as_uint(__uint_as_float(r[4 * u + 0]) * inv_l);
-            w.y = __float_as_uint(__uint_as_float(r[4 * u + 1]) * inv_l);
-            w.z = __float_as_uint(__uint_as_float(r[4 * u + 2]) * inv_l);
-            w.w = __float_as_uint(__uint_as_float(r[4 * u + 3]) * inv_l);
-            *reinterpret_cast<uint4*>(rowp + ((u ^ (tl & 7)) << 4)) = w;
-          }
-        } else {
-          // 32 bf16 = half of a 128-byte row: column block cc/2, 16-byte units (cc&1)*4 ..
-          uint8_t* rowp = stage + (cc >> 1) * (C::kBM * 128) + tl * 128;
+            for (int u4 = 0; u4 < 8; ++u4) {
+              float a0, a1, a2, a3;
+              fmul2(a0, a1, __uint_as_float(rr[4 * u4 + 0]), __uint_as_float(rr[4 * u4 + 1]), inv_l, inv_l);
+              fmul2(a2, a3, __uint_as_float(rr[4 * u4 + 2]), __uint_as_float(rr[4 * u4 + 3]), inv_l, inv_l);
+              dst[u4] = make_uint4(__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3));
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv_l, __uint_as_float(r[8 * u + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv_l, __uint_as_float(r[8 * u + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv_l, __uint_as_float(r[8 * u + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv_l, __uint_as_float(r[8 * u + 7]) * inv_l);
-            const int unit = (cc & 1) * 4 + u;
-            *reinterpret_cast<uint4*>(rowp + ((unit ^ (tl & 7)) << 4)) = w;
+            for (int u4 = 0; u4 < 4; ++u4) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float a0, a1;
+                fmul2(a0, a1, __uint_as_float(rr[8 * u4 + 2 * e]), __uint_as_float(rr[8 * u4 + 2 * e + 1]), inv_l,
+                      inv_l);
+                pk[e] = pack_bf16x2(a0, a1);
+              }
+              dst[u4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
           }
         }
       }
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1 + t, 128);
-    if (do_out && tl == 0 && !*abort_flag) {
-#pragma unroll
-      for (int c = 0; c < C::kNChunk; ++c)
-        tma_store_4d(&tmO, stage + c * (C::kBM * 128), c * C::kChunk, r0, h, b);
-      tma_store_commit();
-      tma_store_wait_read0();
-    }
-    if (do_out && row < p.qL) {
-      const float lse = (l_run > 0.0f) ? (m_run + lg2(l_run)) * kLn2 : -INFINITY;
-      p.lse[((long long)b * p.Hq + h) * p.qL + row] = lse;
+      if (store) {
+        const float lse = (l_run > 0.0f) ? (m_run + lg2(l_run)) * kLn2 : -INFINITY;
+        p.lse[((long long)b * p.Hq + h) * p.qL + row] = lse;
+      }
     }
   }
 

@@ -24,6 +24,7 @@ struct LaunchArgs {
   unsigned int* status;
   long long timeout_cycles;
   int num_sms;
+  int max_ctas;  // 0: one CTA per SM
 };
 
 // cuTensorMapEncodeTiled, resolved from the driver at run time (the library
@@ -65,11 +66,10 @@ inline bool encode_bhsd(CUtensorMap* map, bool f32, const void* ptr, int B, int 
 
 template <class C>
 int launch_fa_fwd(const LaunchArgs& a) {
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   if (!encode_bhsd(&tq, C::kTf32, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
   if (!encode_bhsd(&tk, C::kTf32, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
   if (!encode_bhsd(&tv, C::kTf32, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
-  if (!encode_bhsd(&to, C::kTf32, a.o, a.B, a.Hq, a.qL, a.D, a.os, C::kChunk, C::kBM)) return 4;
 
   FaParams p;
   p.B = a.B;
@@ -88,6 +88,10 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.mask_sb = a.ms[0];
   p.mask_sh = a.ms[1];
   p.mask_ss = a.ms[2];
+  p.o = a.o;
+  p.o_sb = a.os[0];
+  p.o_sh = a.os[1];
+  p.o_ss = a.os[2];
   p.lse = a.lse;
   p.status = a.status;
   p.timeout_cycles = a.timeout_cycles;
@@ -116,12 +120,17 @@ int launch_fa_fwd(const LaunchArgs& a) {
     }
     configured_device = dev;
   }
-  const long long grid = (long long)p.n_qblocks * a.B * a.Hq;
-  if (grid <= 0 || grid > 0x7fffffffLL) {
-    set_error("grid of %lld CTAs is out of range", grid);
+  // Persistent grid: one CTA per SM (or fewer when capped), each walking its
+  // share of the (query block, batch, head) units.
+  const long long units = (long long)p.n_qblocks * a.B * a.Hq;
+  if (units <= 0 || units > 0x7fffffffLL) {
+    set_error("%lld work units are out of range", units);
     return 2;
   }
-  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, to, p);
+  long long grid = a.num_sms > 0 ? a.num_sms : 1;
+  if (a.max_ctas > 0 && a.max_ctas < grid) grid = a.max_ctas;
+  if (grid > units) grid = units;
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("kernel launch failed: %s", cudaGetErrorString(e));

@@ -22,6 +22,8 @@ struct FaParams {
   float scale_log2; // scale * log2(e)
   const void* mask;
   long long mask_sb, mask_sh, mask_ss;  // mask element strides: batch, head, query row
+  void* o;                              // output, I/O dtype
+  long long o_sb, o_sh, o_ss;           // O element strides: batch, head, query row
   float* lse;                           // [B, Hq, qL] fp32, natural log
   unsigned int* status;                 // device status word (kStatus* bits)
   long long timeout_cycles;             // bound on every wait, in SM clock cycles

@@ -24,7 +24,8 @@ FA_OK, FA_ERR_INVALID_ARGUMENT, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CU
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
                 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_set_max_ctas",
+            "fa_version")
 
 
 class FaError(RuntimeError):
@@ -73,6 +74,8 @@ def load_library(path: str = LIB_PATH):
     lib.fa_sync_status.argtypes = [ctypes.c_void_p]
     lib.fa_set_timeout_cycles.restype = None
     lib.fa_set_timeout_cycles.argtypes = [ctypes.c_longlong]
+    lib.fa_set_max_ctas.restype = None
+    lib.fa_set_max_ctas.argtypes = [ctypes.c_int]
     lib.fa_version.restype = ctypes.c_int
     lib.fa_version.argtypes = []
     _lib = lib
@@ -107,6 +110,10 @@ def fa_sync_status(stream=None) -> int:
 
 def fa_set_timeout_cycles(cycles: int) -> None:
     load_library().fa_set_timeout_cycles(int(cycles))
+
+
+def fa_set_max_ctas(n: int) -> None:
+    load_library().fa_set_max_ctas(int(n))
 
 
 def fa_version() -> int:

@@ -120,6 +120,15 @@ int fa_sync_status(void* stream);
  */
 void fa_set_timeout_cycles(long long cycles);
 
+/*
+ * fa_set_max_ctas -- the forward kernel is persistent: by default it starts
+ * one CTA per SM and each CTA walks a balanced share of the (query block,
+ * batch, head) work units.  n > 0 caps the number of CTAs (for example to
+ * leave SMs to work on other streams); n <= 0 restores one per SM.  Results
+ * do not depend on it.
+ */
+void fa_set_max_ctas(int n);
+
 /* ABI version: major * 100 + minor. */
 int fa_version(void);
 

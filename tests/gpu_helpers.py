@@ -46,8 +46,9 @@ def fp32_scale(w: workloads.Workload, scale=None) -> float:
     return float(np.float32(s))
 
 
-def compare(w, o_gpu, l_gpu, o_ref, l_ref, what=""):
+def compare(w, o_gpu, l_gpu, o_ref, l_ref, what="", tol_mult=1.0, tol_mult_l=None):
     tol_o, tol_l = TOL[w.dtype]
+    tol_o, tol_l = tol_o * tol_mult, tol_l * (tol_mult if tol_mult_l is None else tol_mult_l)
     fin = np.isfinite(l_ref)
     # rows with no allowed key: O = 0, L = -inf exactly
     assert np.array_equal(np.isneginf(l_gpu), ~fin), f"{what}: -inf rows of L differ"

@@ -29,7 +29,8 @@ def _declared_functions():
 
 def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
-        ["fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_version"])
+        ["fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_max_ctas", "fa_set_timeout_cycles",
+         "fa_version"])
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -59,7 +60,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 100
+    assert fa.fa_version() == 101
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
