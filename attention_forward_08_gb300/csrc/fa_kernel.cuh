@@ -74,6 +74,13 @@ struct Cfg {
   static constexpr int kVTStages = kVTStages_;
   static constexpr int kKStep = kTf32 ? 8 : 16;       // MMA K per instruction (32 bytes)
   static constexpr bool kAliasP = (kNQT == 2);        // P over S; PV issued before the next S
+  // MMA-issuing threads.  One warp issues at most one tcgen05.mma per ~54
+  // cycles (measured), and anything else it does between MMAs adds to that,
+  // while a 128x128x16 MMA is 64 cycles of work: with two bf16 Q tiles, tile
+  // t's MMAs come from warp 1 + t and the two threads take strict turns, so
+  // the tensor core still sees PV0 S0 PV1 S1 (the ping-pong order) while each
+  // thread's waits and commits overlap the other's MMA issue.
+  static constexpr int kIssuers = (kNQT == 2 && !kTf32) ? 2 : 1;
   static constexpr int kPCols = kTf32 ? kBN : kBN / 2;  // TMEM columns of one P tile
   static constexpr int kColO = kNQT * kBN;            // first O column
   static constexpr int kColP = kColO + kNQT * kD;     // P double buffer (non-aliased mode)
@@ -120,9 +127,10 @@ struct Ctrl {
   uint64_t p_ready[2];            // softmax t wrote P (and rescaled O)
   uint64_t o_ready[2];            // PV_t completed (commit)
   uint64_t o_free[2];             // epilogue read O_t out of TMEM
-  uint64_t drain;                 // MMA drain at exit
+  uint64_t drain[2];              // MMA drain at exit, one per issuing thread
   uint32_t tmem_base;
   int abort;
+  int turn;                       // two issuers: whose MMA group goes next
 };
 
 // Bounded wait: true once the phase of `parity` completed; false after the
@@ -420,15 +428,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&ctl->k_full[s], 1);
-      mbar_init(&ctl->k_empty[s], 1);
+      mbar_init(&ctl->k_empty[s], C::kIssuers);  // one commit per issuing thread
       mbar_init(&ctl->k_ready[s], 2);
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : 1);  // tf32: released by the two transposing warps
+      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : C::kIssuers);  // tf32: released by the two transposing warps
       mbar_init(&ctl->vt_full[s], 2);
-      mbar_init(&ctl->vt_empty[s], 1);
+      mbar_init(&ctl->vt_empty[s], C::kIssuers);
     }
-    mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->drain[0], 1);
+    mbar_init(&ctl->drain[1], 1);
     ctl->abort = 0;
+    ctl->turn = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -458,12 +468,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int u = unit_of(r, num_units);
         if (u < 0) break;
         const Unit w = decode_unit<C>(p, u);
-        for (int t = 0; t < C::kNQT && ok; ++t) {
-          if (w.nblk[t] == 0) continue;
+#pragma unroll
+        for (int t = 0; t < C::kNQT; ++t) {
+          if (!ok || w.nblk[t] == 0) continue;
           // Q_t's shared memory is free once the previous unit's last S_t completed.
           if (q_issued[t] > 0)
             ok = wait_bounded(&ctl->q_empty[t], (q_issued[t] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
-          if (!ok) break;
+          if (!ok) continue;
           mbar_arrive_expect_tx(&ctl->q_full[t], C::kQTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kNChunk; ++c)
@@ -511,8 +522,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                        kDrainCycles, false);
       }
     }
-  } else if (warp == 1) {
-    // ===================================================== MMA issuer (one thread)
+  } else if (warp == 1 || (C::kIssuers == 2 && warp == 2)) {
+    // ===================================================== MMA issuer(s)
+    // Issuer i handles Q tiles [t_begin, t_end).  Every issuer walks all
+    // units and all K/V tiles in order and commits its own arrival on each
+    // release barrier, so each release phase sees exactly kIssuers arrivals.
+    const int issuer = warp - 1;
+    const int t_begin = C::kIssuers == 1 ? 0 : issuer;
+    const int t_end = C::kIssuers == 1 ? C::kNQT : issuer + 1;
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(C::kTf32, 128, C::kBN, false, false);
       constexpr uint32_t idPV = make_idesc(C::kTf32, 128, C::kD, false, !C::kTf32);
@@ -554,6 +571,29 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           mma_ts_lh<C::kTf32, 1>(dst, src + kk * 8, va + voff, v_hi, idPV, 1u);
         }
       };
+      // Two issuers take turns: turn 2g + i is issuer i's g-th MMA group.
+      volatile int* turn = &ctl->turn;
+      int my_turn = issuer;
+      auto wait_turn = [&]() -> bool {
+        if (C::kIssuers == 1) return true;
+        if (*turn == my_turn) return true;
+        const long long t0 = clock64_now();
+        while (*turn != my_turn) {
+          if (*abort_flag) return false;
+          if (clock64_now() - t0 > p.timeout_cycles) {
+            *abort_flag = 1;
+            atomicOr(p.status, kStatusTimeout);
+            return false;
+          }
+        }
+        return true;
+      };
+      auto pass_turn = [&]() {
+        if (C::kIssuers == 2) {
+          *turn = my_turn + 1;
+          my_turn += 2;
+        }
+      };
 
       int k_used = 0, v_used = 0;   // ring items consumed (all units)
       int q_used[2] = {0, 0};       // Q loads consumed per tile
@@ -564,28 +604,32 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int u = unit_of(r, num_units);
         if (u < 0) break;
         const Unit w = decode_unit<C>(p, u);
-        for (int t = 0; t < C::kNQT && ok; ++t) {
-          if (w.nblk[t] == 0) continue;
+#pragma unroll
+        for (int t = 0; t < C::kNQT; ++t) {
+          if (t < t_begin || t >= t_end || !ok || w.nblk[t] == 0) continue;
           const uint32_t par = q_used[t] & 1;
           ok = C::kTf32 ? wait_bounded(&ctl->q_ready[t], par, abort_flag, p.status, p.timeout_cycles)
                         : wait_bounded(&ctl->q_full[t], par, abort_flag, p.status, p.timeout_cycles);
           ++q_used[t];
         }
-        // K_0 -> S_t,0 for every tile
+        // K_0 -> S_t,0 for every tile of this issuer
         int kslot = k_used % C::kKStages;
         if (ok) {
           const uint32_t par = (k_used / C::kKStages) & 1;
           ok = C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
                         : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
         }
+        if (ok) ok = wait_turn();
         if (!ok) break;
         tc_fence_after();
+#pragma unroll
         for (int t = 0; t < C::kNQT; ++t) {
-          if (w.nblk[t] == 0) continue;
+          if (t < t_begin || t >= t_end || w.nblk[t] == 0) continue;
           issue_S(t, kslot);
           mma_commit(&ctl->s_full[t]);
           if (w.nblk[t] == 1) mma_commit(&ctl->q_empty[t]);  // the unit's last S of tile t
         }
+        pass_turn();
         mma_commit(&ctl->k_empty[kslot]);
         ++k_used;
         for (int j = 0; j < w.N && ok; ++j) {
@@ -605,8 +649,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             return C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
                             : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
           };
+          bool turn_taken = false;
+#pragma unroll
           for (int t = 0; t < C::kNQT; ++t) {
-            if (!ok || j >= w.nblk[t]) continue;
+            if (t < t_begin || t >= t_end || !ok || j >= w.nblk[t]) continue;
             ok = wait_bounded(&ctl->p_ready[t], p_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
             ++p_seen[t];
             // The unit's first PV overwrites O_t: the previous unit's epilogue must have read it.
@@ -618,6 +664,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (s_next) {
               ok = wait_k();
               if (!ok) break;
+            }
+            if (!turn_taken) {
+              ok = wait_turn();
+              if (!ok) break;
+              turn_taken = true;
             }
             tc_fence_after();
             if (C::kAliasP) {
@@ -639,23 +690,29 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
           }
           if (!ok) break;
+          if (!turn_taken) {  // an empty group still takes its turn
+            ok = wait_turn();
+            if (!ok) break;
+          }
+          pass_turn();
           mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
           ++v_used;
           if (next) {
             // Tiles that stop earlier (causal) never waited on K_{j+1}; make sure
-            // it landed before its slot is handed back.
+            // it landed before this issuer's release of its slot.
             ok = wait_k();
             if (!ok) break;
             mma_commit(&ctl->k_empty[kslot]);
             ++k_used;
           }
         }
+#pragma unroll
         for (int t = 0; t < C::kNQT; ++t)
-          if (w.nblk[t] > 0) ++units_done[t];
+          if (t >= t_begin && t < t_end && w.nblk[t] > 0) ++units_done[t];
       }
       // Drain: every MMA this thread issued completes before TMEM is freed.
-      mma_commit(&ctl->drain);
-      wait_bounded(&ctl->drain, 0, abort_flag, p.status, kDrainCycles, false);
+      mma_commit(&ctl->drain[issuer]);
+      wait_bounded(&ctl->drain[issuer], 0, abort_flag, p.status, kDrainCycles, false);
     }
     __syncwarp();
   } else {
@@ -669,11 +726,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int u = unit_of(r, num_units);
         if (u < 0) break;
         const Unit w = decode_unit<C>(p, u);
-        for (int t = 0; t < C::kNQT && ok; ++t) {
-          if (w.nblk[t] == 0) continue;
+#pragma unroll
+        for (int t = 0; t < C::kNQT; ++t) {
+          if (!ok || w.nblk[t] == 0) continue;
           ok = warp_wait(&ctl->q_full[t], q_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
           ++q_seen[t];
-          if (!ok) break;
+          if (!ok) continue;
           round_tf32_inplace(sQ + t * C::kQTileBytes, C::kQTileBytes, ct, 64);
           fence_proxy_async_smem();
           __syncwarp();
@@ -723,7 +781,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int u = unit_of(r, num_units);
       if (u < 0) break;
       const Unit w = decode_unit<C>(p, u);
-      const int nb = w.nblk[t];
+      const int nb = t == 0 ? w.nblk[0] : w.nblk[1];
       if (nb == 0) continue;
       const int b = w.b, h = w.h;
       const int r0 = w.q0 + t * C::kBM;
