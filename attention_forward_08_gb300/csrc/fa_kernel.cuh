@@ -101,7 +101,12 @@ struct Cfg {
   static constexpr uint32_t kOffK = kNQT * kQTileBytes;
   static constexpr uint32_t kOffV = kOffK + kKStages * kKVTileBytes;
   static constexpr uint32_t kOffVT = kOffV + kVStages * kKVTileBytes;
-  static constexpr uint32_t kOffBar = kOffVT + kVTStages * kKVTileBytes;
+  // One shared-memory slot for a TMA-loaded mask tile [kBM rows x kBN keys]
+  // (sized for a 2-byte additive mask; a 1-byte bool tile uses half).  Only
+  // where shared memory allows: bf16 I/O with one Q tile (D = 256).
+  static constexpr uint32_t kMaskSlotBytes = (!kTf32 && kNQT == 1) ? kBM * kBN * 2 : 0;
+  static constexpr uint32_t kOffM = kOffVT + kVTStages * kKVTileBytes;
+  static constexpr uint32_t kOffBar = kOffM + kMaskSlotBytes;
   static constexpr uint32_t kBarBytes = 512;
   static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 
@@ -123,6 +128,7 @@ struct Ctrl {
   uint64_t k_full[4], k_empty[4], k_ready[4];
   uint64_t v_full[4], v_empty[4];
   uint64_t vt_full[4], vt_empty[4];  // (tf32) transposed V tiles
+  uint64_t m_full, m_empty;          // mask tile in shared memory
   uint64_t s_full[2];             // S_t computed (commit)
   uint64_t p_ready[2];            // softmax t wrote P (and rescaled O)
   uint64_t o_ready[2];            // PV_t completed (commit)
@@ -284,14 +290,48 @@ __device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, in
   }
 }
 
+// Fold one row of a TMA-loaded mask tile (128-byte swizzled rows; 2-byte
+// additive values in kBN/64 column blocks, or 1-byte bool values in one) into
+// s, like fold_mask_chunk does from global memory.
 template <class C>
-__device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p, int b, int h, int row, int kbase) {
+__device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t* tile, int kind, int tl) {
+  if (kind == 1) {
+#pragma unroll
+    for (int c = 0; c < C::kBN / 16; ++c) {  // 16 keys per 16-byte unit
+      const uint4 w = *reinterpret_cast<const uint4*>(tile + (c / 8) * (C::kBM * 128) + tl * 128 +
+                                                      (((c % 8) ^ (tl & 7)) << 4));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (((ws[e >> 2] >> ((e & 3) * 8)) & 0xFFu) == 0u) s[c * 16 + e] = -INFINITY;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < C::kBN / 8; ++c) {  // 8 bf16 keys per 16-byte unit
+      const uint4 w = *reinterpret_cast<const uint4*>(tile + (c / 8) * (C::kBM * 128) + tl * 128 +
+                                                      (((c % 8) ^ (tl & 7)) << 4));
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t bits = (e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16);
+        s[c * 8 + e] = fmaf(__uint_as_float(bits), kLog2e, s[c * 8 + e]);
+      }
+    }
+  }
+}
+
+template <class C>
+__device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p, int b, int h, int row, int kbase,
+                                           const uint8_t* mask_tile, int tl) {
   // Scores to base 2 first when the mask is additive or the scale is not positive.
   if (p.pre_scale) {
 #pragma unroll
     for (int c = 0; c < C::kBN; ++c) s[c] *= p.scale_log2;
   }
-  if (p.mask_kind != 0 && row < p.qL) {
+  if constexpr (C::kMaskSlotBytes > 0) {
+    if (mask_tile) fold_mask_smem<C>(s, mask_tile, p.mask_kind, tl);
+  }
+  if (p.mask_kind != 0 && row < p.qL && !(C::kMaskSlotBytes > 0 && mask_tile)) {
     const size_t esz = (p.mask_kind == 1) ? 1 : C::kEsz;
     const char* mrow = static_cast<const char*>(p.mask) +
                        ((long long)b * p.mask_sb + (long long)h * p.mask_sh + (long long)row * p.mask_ss) * esz;
@@ -402,13 +442,15 @@ __device__ __forceinline__ int unit_of(int r, int num_units) {
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FaParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM,
+                  const FaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
   uint8_t* sVT = smem + C::kOffVT;
+  uint8_t* sM = smem + C::kOffM;
   Ctrl<C>* ctl = reinterpret_cast<Ctrl<C>*>(smem + C::kOffBar);
   volatile int* abort_flag = &ctl->abort;
 
@@ -437,6 +479,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     mbar_init(&ctl->drain[0], 1);
     mbar_init(&ctl->drain[1], 1);
+    mbar_init(&ctl->m_full, 1);
+    mbar_init(&ctl->m_empty, 4);  // one arrival per softmax warp
     ctl->abort = 0;
     ctl->turn = 0;
     fence_barrier_init();
@@ -445,6 +489,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    if (p.mask_l2 || p.mask_smem) tma_prefetch_desc(&tmM);
   }
   if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, C::kTmemCols);
@@ -462,6 +507,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // ===================================================== TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;  // ring items issued (all units)
+      int m_issued = 0;                // mask tiles issued (shared-memory mask path)
       int q_issued[2] = {0, 0};        // Q loads issued per tile
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -482,7 +528,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         w.q0 + t * C::kBM, w.h, w.b);
           ++q_issued[t];
         }
+        // Mask tiles reach L2 ahead of the softmax that reads them: blocks 0
+        // and 1 now, then block j + 2 while K_j / V_j are issued.
+        auto prefetch_mask = [&](int j) {
+          const int mesz = p.mask_kind == 1 ? 1 : C::kEsz;
+          for (int t = 0; t < C::kNQT; ++t)
+            for (int c = 0; c < (C::kBN * mesz) / 128; ++c)
+              tma_prefetch_l2_4d(&tmM, j * C::kBN + c * (128 / mesz), w.q0 + t * C::kBM, w.h, w.b);
+        };
+        if (p.mask_l2) {
+          for (int j = 0; j < min(2, w.N); ++j) prefetch_mask(j);
+        }
         for (int j = 0; j < w.N && ok; ++j) {
+          if (p.mask_l2 && j + 2 < w.N) prefetch_mask(j + 2);
           {  // K_j
             const int slot = k_issued % C::kKStages, use = k_issued / C::kKStages;
             ok = wait_bounded(&ctl->k_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
@@ -494,6 +552,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               tma_load_4d(dst + c * (C::kBN * 128), &tmK, &ctl->k_full[slot], c * C::kChunk, j * C::kBN, w.kvh,
                           w.b);
             ++k_issued;
+          }
+          if (C::kMaskSlotBytes > 0 && p.mask_smem) {  // M_j: the mask tile of block j
+            ok = wait_bounded(&ctl->m_empty, (m_issued & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+            if (!ok) break;
+            const int mesz = p.mask_kind == 1 ? 1 : 2;
+            const int boxes = (C::kBN * mesz) / 128;  // 128-byte column blocks
+            mbar_arrive_expect_tx(&ctl->m_full, (uint32_t)(C::kBM * C::kBN * mesz));
+            for (int c = 0; c < boxes; ++c)
+              tma_load_4d(sM + c * (C::kBM * 128), &tmM, &ctl->m_full, j * C::kBN + c * (128 / mesz), w.q0, w.h, w.b);
+            ++m_issued;
           }
           {  // V_j
             const int slot = v_issued % C::kVStages, use = v_issued / C::kVStages;
@@ -520,6 +588,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int it = max(0, v_issued - C::kVStages); it < v_issued; ++it)
           wait_bounded(&ctl->v_full[it % C::kVStages], (it / C::kVStages) & 1, abort_flag, p.status,
                        kDrainCycles, false);
+        if (m_issued > 0) wait_bounded(&ctl->m_full, (m_issued - 1) & 1, abort_flag, p.status, kDrainCycles, false);
       }
     }
   } else if (warp == 1 || (C::kIssuers == 2 && warp == 2)) {
@@ -775,6 +844,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t tO = tmem + lane_addr + C::kColO + t * C::kD;
     const float sl = p.pre_scale ? 1.0f : p.scale_log2;
     int blocks_seen = 0;  // s_full phases consumed (all units)
+    int masks_seen = 0;   // mask tiles consumed (shared-memory mask path)
     int units_seen = 0;   // units with rows in this tile (o_ready phases with P over S)
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -809,7 +879,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int kbase = j * C::kBN;
         const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + C::kBN > p.kL ||
                                (p.causal && kbase + C::kBN - 1 > r0);
-        if (need_mask) apply_mask<C>(s, p, b, h, row, kbase);
+        const uint8_t* mask_tile = nullptr;
+        if (C::kMaskSlotBytes > 0 && p.mask_smem) {
+          ok = warp_wait(&ctl->m_full, masks_seen & 1, abort_flag, p.status, p.timeout_cycles);
+          ++masks_seen;
+          if (!ok) break;
+          mask_tile = sM;
+        }
+        if (need_mask) apply_mask<C>(s, p, b, h, row, kbase, mask_tile, tl);
+        if (mask_tile) {  // the mask tile is folded in: the producer may load the next one
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->m_empty);
+        }
 
         const float mx = row_max<C>(s);
         const float m_blk = mx * sl;  // -inf stays -inf (sl > 0 whenever it is not 1)

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "fa_kernel.cuh"
 
 namespace fa {
@@ -66,10 +68,39 @@ inline bool encode_bhsd(CUtensorMap* map, bool f32, const void* ptr, int B, int 
 
 template <class C>
 int launch_fa_fwd(const LaunchArgs& a) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tm;
   if (!encode_bhsd(&tq, C::kTf32, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
   if (!encode_bhsd(&tk, C::kTf32, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
   if (!encode_bhsd(&tv, C::kTf32, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
+  // Mask tiles (128-byte column blocks x kBM rows, 128-byte swizzle) for the
+  // L2 prefetch and the shared-memory mask path, when the mask's layout suits
+  // TMA (aligned base, 16-byte multiple strides, no stride-0 broadcast).
+  int mask_l2 = 0, mask_smem = 0;
+  std::memset(&tm, 0, sizeof(tm));
+  if (a.mask_kind != 0 && a.mask_vec) {
+    const int mesz = a.mask_kind == 1 ? 1 : (C::kTf32 ? 4 : 2);
+    const bool fits = a.ms[2] > 0 && (a.ms[1] > 0 || a.Hq == 1) && (a.ms[0] > 0 || a.B == 1);
+    if (fits) {
+      cuuint64_t dims[4] = {(cuuint64_t)a.kL, (cuuint64_t)a.qL, (cuuint64_t)a.Hq, (cuuint64_t)a.B};
+      auto legal = [](long long bytes, int extent) -> cuuint64_t {
+        return (extent <= 1 || bytes <= 0) ? (cuuint64_t)16 : (cuuint64_t)bytes;
+      };
+      cuuint64_t strides[3] = {legal(a.ms[2] * mesz, a.qL), legal(a.ms[1] * mesz, a.Hq), legal(a.ms[0] * mesz, a.B)};
+      cuuint32_t box[4] = {(cuuint32_t)(128 / mesz), (cuuint32_t)C::kBM, 1, 1};
+      cuuint32_t estr[4] = {1, 1, 1, 1};
+      const CUtensorMapDataType dt = a.mask_kind == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : (C::kTf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+      EncodeTiledFn enc = get_encode_tiled();
+      if (enc && (C::kBN * mesz) % 128 == 0 &&
+          enc(&tm, dt, 4, const_cast<void*>(a.mask), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+              CUDA_SUCCESS) {
+        // otherwise the kernel simply reads the mask from global memory
+        mask_smem = C::kMaskSlotBytes > 0 ? 1 : 0;
+        mask_l2 = mask_smem ? 0 : 1;
+      }
+    }
+  }
 
   FaParams p;
   p.B = a.B;
@@ -83,6 +114,8 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.mask_kind = a.mask_kind;
   p.pre_scale = (a.mask_kind == 2 || !(a.scale > 0.0f)) ? 1 : 0;
   p.mask_vec = a.mask_vec;
+  p.mask_l2 = mask_l2;
+  p.mask_smem = mask_smem;
   p.scale_log2 = a.scale * kLog2e;
   p.mask = a.mask;
   p.mask_sb = a.ms[0];
@@ -130,7 +163,7 @@ int launch_fa_fwd(const LaunchArgs& a) {
   long long grid = a.num_sms > 0 ? a.num_sms : 1;
   if (a.max_ctas > 0 && a.max_ctas < grid) grid = a.max_ctas;
   if (grid > units) grid = units;
-  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, p);
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, tm, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("kernel launch failed: %s", cudaGetErrorString(e));

@@ -19,6 +19,8 @@ struct FaParams {
   int mask_kind;    // 0 none, 1 bool (uint8, nonzero keeps), 2 additive (I/O dtype)
   int pre_scale;    // scale scores before masking (additive mask, or scale <= 0)
   int mask_vec;     // mask rows 16-byte aligned: vector loads allowed
+  int mask_l2;      // a tensor map describes the mask: prefetch its tiles into L2
+  int mask_smem;    // the mask map is 128-byte swizzled: TMA-load its tiles into shared memory
   float scale_log2; // scale * log2(e)
   const void* mask;
   long long mask_sb, mask_sh, mask_ss;  // mask element strides: batch, head, query row
