@@ -21,20 +21,29 @@
 //    the transpose to token-major output folded into the epilogue.
 //
 // GB300 design (differs from the pages' Apple-GPU kernels):
-//  - warp 0 issues TMA loads: Q once, then K and V tiles through two
-//    mbarrier rings (separate K and V rings);
-//  - warp 1 owns TMEM and issues every tcgen05.mma from one thread:
-//    S = Q K^T (both operands in shared memory, K-major, 128-byte swizzle)
-//    and O += P V (P read from TMEM, V MN-major from shared memory);
-//  - warps 2-3 (fp32 I/O only) round Q and K tiles to tf32 in place;
+//  - persistent grid: one CTA per SM walks a snake-ordered share of the
+//    (query block, head, batch) work units, heavy causal blocks first; every
+//    role carries its barrier phases across units, so the next unit's loads
+//    and first MMAs overlap the current unit's last blocks and epilogue;
+//  - warp 0 issues TMA loads: Q per unit, then K, V (and, for D = 256 bf16,
+//    mask) tiles through mbarrier rings, in the order the tensor core reads
+//    them;
+//  - warp 1 (and warp 2 for two bf16 Q tiles, taking strict turns) issues
+//    every tcgen05.mma from one thread: S = Q K^T (both operands in shared
+//    memory, K-major, 128-byte swizzle) and O += P V (P read from TMEM, V
+//    MN-major from shared memory for bf16, a transposed V^T for tf32);
+//  - warps 2-3 (fp32 I/O only) round Q and K tiles to tf32 in place and
+//    transpose V;
 //  - one softmax warpgroup per 128-row Q tile: thread r owns row r (TMEM lane
 //    r), reads its S row with tcgen05.ld, applies masks, updates the base-2
 //    running max/sum, writes P back to TMEM and rescales its O row in TMEM
 //    only when the running max grows by more than 2^8 (exact: O and l share
 //    the stale max; the epilogue divides it out);
-//  - two Q tiles per CTA ping-pong on the tensor core where TMEM allows;
-//  - epilogue: O / l -> I/O dtype -> swizzled smem -> TMA store (any
-//    {batch, head, row} strides, e.g. token-major), L in fp32.
+//  - two Q tiles per CTA ping-pong on the tensor core where TMEM allows (P
+//    over S); with one tile, S and P have their own columns and S_{j+1} is
+//    computed while softmax j runs;
+//  - epilogue: O / l -> I/O dtype -> 16-byte global stores straight from
+//    registers (any {batch, head, row} strides, e.g. token-major), L in fp32;
 //  - every wait is bounded; on expiry the kernel records kStatusTimeout,
 //    drains its own copies and MMAs, frees TMEM and returns.
 #pragma once
@@ -74,6 +83,9 @@ struct Cfg {
   static constexpr int kVTStages = kVTStages_;
   static constexpr int kKStep = kTf32 ? 8 : 16;       // MMA K per instruction (32 bytes)
   static constexpr bool kAliasP = (kNQT == 2);        // P over S; PV issued before the next S
+  // K/V load order follows the tensor core's: with P over S it runs PV_j, S_{j+1}
+  // (K_j, V_j, K_{j+1}, ...); otherwise S_{j+1} goes before PV_j, so V lags K by a block.
+  static constexpr int kVLag = kAliasP ? 0 : 1;
   // MMA-issuing threads.  One warp issues at most one tcgen05.mma per ~54
   // cycles (measured), and anything else it does between MMAs adds to that,
   // while a 128x128x16 MMA is 64 cycles of work: with two bf16 Q tiles, tile
@@ -130,6 +142,7 @@ struct Ctrl {
   uint64_t vt_full[4], vt_empty[4];  // (tf32) transposed V tiles
   uint64_t m_full, m_empty;          // mask tile in shared memory
   uint64_t s_full[2];             // S_t computed (commit)
+  uint64_t s_free[2];             // (one Q tile) softmax t holds S in registers: S may be overwritten
   uint64_t p_ready[2];            // softmax t wrote P (and rescaled O)
   uint64_t o_ready[2];            // PV_t completed (commit)
   uint64_t o_free[2];             // epilogue read O_t out of TMEM
@@ -464,6 +477,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&ctl->q_empty[t], 1);    // MMA commit after the unit's last S of tile t
       mbar_init(&ctl->q_ready[t], 2);    // one arrival per tf32 helper warp
       mbar_init(&ctl->s_full[t], 1);
+      mbar_init(&ctl->s_free[t], 4);     // one arrival per softmax warp
       mbar_init(&ctl->p_ready[t], 4);    // one arrival per softmax warp
       mbar_init(&ctl->o_ready[t], 1);
       mbar_init(&ctl->o_free[t], 4);     // one arrival per softmax warp after reading O
@@ -539,7 +553,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (p.mask_l2) {
           for (int j = 0; j < min(2, w.N); ++j) prefetch_mask(j);
         }
-        for (int j = 0; j < w.N && ok; ++j) {
+        for (int j = 0; j < w.N + C::kVLag && ok; ++j) {
+          if (j < w.N) {
           if (p.mask_l2 && j + 2 < w.N) prefetch_mask(j + 2);
           {  // K_j
             const int slot = k_issued % C::kKStages, use = k_issued / C::kKStages;
@@ -563,7 +578,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               tma_load_4d(sM + c * (C::kBM * 128), &tmM, &ctl->m_full, j * C::kBN + c * (128 / mesz), w.q0, w.h, w.b);
             ++m_issued;
           }
-          {  // V_j
+          }
+          const int jv = j - C::kVLag;
+          if (jv >= 0) {  // V_jv
             const int slot = v_issued % C::kVStages, use = v_issued / C::kVStages;
             ok = wait_bounded(&ctl->v_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
@@ -571,7 +588,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint8_t* dst = sV + slot * C::kKVTileBytes;
 #pragma unroll
             for (int c = 0; c < C::kNChunk; ++c)
-              tma_load_4d(dst + c * (C::kBN * 128), &tmV, &ctl->v_full[slot], c * C::kChunk, j * C::kBN, w.kvh,
+              tma_load_4d(dst + c * (C::kBN * 128), &tmV, &ctl->v_full[slot], c * C::kChunk, jv * C::kBN, w.kvh,
                           w.b);
             ++v_issued;
           }
@@ -668,6 +685,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       int q_used[2] = {0, 0};       // Q loads consumed per tile
       int p_seen[2] = {0, 0};       // p_ready phases consumed per tile
       int units_done[2] = {0, 0};   // units with a non-empty tile t (o_free phases to wait)
+      int s_freed = 0;              // s_free phases consumed (one Q tile)
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int u = unit_of(r, num_units);
@@ -701,6 +719,45 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         pass_turn();
         mma_commit(&ctl->k_empty[kslot]);
         ++k_used;
+        if constexpr (!C::kAliasP) {
+          // One Q tile, one issuer, separate S and P columns: S_{j+1} goes to the
+          // tensor core as soon as softmax j holds S_j in registers (and K_{j+1}
+          // is ready), so it overlaps softmax j; PV_j follows once P_j is written.
+          for (int j = 0; j < w.N && ok; ++j) {
+            ok = wait_bounded(&ctl->s_free[0], s_freed & 1, abort_flag, p.status, p.timeout_cycles);
+            ++s_freed;
+            if (!ok) break;
+            if (j + 1 < w.N) {
+              kslot = k_used % C::kKStages;
+              const uint32_t par = (k_used / C::kKStages) & 1;
+              ok = C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
+                            : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
+              if (!ok) break;
+              tc_fence_after();
+              issue_S(0, kslot);
+              mma_commit(&ctl->s_full[0]);
+              if (j + 2 == w.N) mma_commit(&ctl->q_empty[0]);  // the unit's last S
+              mma_commit(&ctl->k_empty[kslot]);
+              ++k_used;
+            }
+            const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
+            const uint32_t vpar = (C::kTf32 ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
+            ok = C::kTf32 ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
+                          : wait_bounded(&ctl->v_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles);
+            if (!ok) break;
+            ok = wait_bounded(&ctl->p_ready[0], p_seen[0] & 1, abort_flag, p.status, p.timeout_cycles);
+            ++p_seen[0];
+            // The unit's first PV overwrites O: the previous unit's epilogue must have read it.
+            if (ok && j == 0 && units_done[0] > 0)
+              ok = wait_bounded(&ctl->o_free[0], (units_done[0] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
+            if (!ok) break;
+            tc_fence_after();
+            issue_PV(0, j, vslot);
+            mma_commit(&ctl->o_ready[0]);
+            mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
+            ++v_used;
+          }
+        } else
         for (int j = 0; j < w.N && ok; ++j) {
           // bf16: V ring slot; tf32: V^T ring slot
           const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
@@ -806,16 +863,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
         }
-        for (int j = 0; j < w.N && ok; ++j) {
-          const int slot = k_seen % C::kKStages;
-          ok = warp_wait(&ctl->k_full[slot], (k_seen / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
-          ++k_seen;
-          if (!ok) break;
-          round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, 64);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
-          // V_j -> V^T_j (K-major), then hand the V slot back to the producer.
+        // Same order as the producer: K_j, then V_{j - kVLag}.
+        for (int j = 0; j < w.N + C::kVLag && ok; ++j) {
+          if (j < w.N) {
+            const int slot = k_seen % C::kKStages;
+            ok = warp_wait(&ctl->k_full[slot], (k_seen / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
+            ++k_seen;
+            if (!ok) break;
+            round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, 64);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
+          }
+          if (j < C::kVLag) continue;
+          // V -> V^T (K-major), then hand the V slot back to the producer.
           const int vs = v_seen % C::kVStages, ts = v_seen % C::kVTStages;
           ok = warp_wait(&ctl->v_full[vs], (v_seen / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
           if (!ok) break;
@@ -875,6 +936,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::kBN; ++c) s[c] = __uint_as_float(rr[c]);
         }
+        if constexpr (!C::kAliasP) {  // S_t is in registers: the next S may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->s_free[t]);
+        }
 
         const int kbase = j * C::kBN;
         const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + C::kBN > p.kL ||
@@ -909,13 +975,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         p_pass<C, false>(s, sl, msub, tP, sum, unused);
         l_run = l_run * corr + sum;
 
-        // Rescale this warp's O rows once the previous PV has landed (with P
-        // over S, S_j's completion already implies it: PV_{j-1} was issued first).
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          if constexpr (!C::kAliasP) {
+        // Without P over S, o_ready completes once per PV; every phase is
+        // consumed here, in order (PV_{j-1}, issued as softmax j-1 ended), so a
+        // parity wait never runs a phase behind.  With P over S, S_j's
+        // completion already implies PV_{j-1}: it was issued first.
+        if constexpr (!C::kAliasP) {
+          if (j > 0) {
             ok = warp_wait(&ctl->o_ready[t], (blocks_seen - 2) & 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
           }
+        }
+        // Rescale this warp's O rows (the previous PV has landed).
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < C::kD / 32; ++cc) {
