@@ -99,11 +99,16 @@ struct Cfg {
   static constexpr int kTmemUsed = kAliasP ? kNQT * (kBN + kD) : (kBN + kD + 2 * kPCols);
   static constexpr uint32_t kTmemCols =
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
-  static constexpr int kThreads = 128 * (1 + kNQT);
+  // tf32 helper warps: warps 2-3, plus warps 8-11 when there is one Q tile
+  // (rounding K and transposing V then keep pace with the tensor core).
+  static constexpr bool kExtraHelpers = kTf32 && kNQT == 1;
+  static constexpr int kCvtWarps = kTf32 ? (kExtraHelpers ? 6 : 2) : 1;
+  static constexpr int kCvtThreads = 32 * kCvtWarps;
+  static constexpr int kThreads = 128 * (1 + kNQT) + (kExtraHelpers ? 128 : 0);
   // Per-thread registers at launch, and the split after setmaxnreg: the
   // control warpgroup (TMA, MMA, tf32 helpers) gives registers to the softmax
   // warpgroups.  Sums stay within the launch total (kThreads * kRegsLaunch).
-  static constexpr int kRegsLaunch = kNQT == 2 ? 168 : 255;
+  static constexpr int kRegsLaunch = kThreads == 384 ? 168 : 255;
   static constexpr int kRegsCtrl = 80;
   static constexpr int kRegsSoftmax = kNQT == 2 ? 208 : 0;  // 0: no reallocation
   static_assert(kRegsSoftmax == 0 || 128 * kRegsCtrl + 128 * kNQT * kRegsSoftmax <= kThreads * kRegsLaunch,
@@ -149,7 +154,7 @@ struct Ctrl {
   uint64_t drain[2];              // MMA drain at exit, one per issuing thread
   uint32_t tmem_base;
   int abort;
-  int turn;                       // two issuers: whose MMA group goes next
+  uint64_t turn_bar[2];           // two issuers: issuer i may issue its next MMA group
 };
 
 // Bounded wait: true once the phase of `parity` completed; false after the
@@ -448,6 +453,63 @@ __device__ __forceinline__ int unit_of(int r, int num_units) {
   return idx < num_units ? idx : -1;
 }
 
+// tf32 helper warps (fp32 I/O): round each landed Q and K tile to tf32 in
+// place and transpose each V tile into the K-major V^T ring, in the order the
+// producer loads them.  ct is this thread's index among the helper threads.
+template <class C>
+__device__ __forceinline__ void tf32_helpers(uint8_t* sQ, uint8_t* sK, uint8_t* sV, uint8_t* sVT, Ctrl<C>* ctl,
+                                             const FaParams& p, volatile int* abort_flag, int num_units, int ct,
+                                             int lane) {
+  int q_seen[2] = {0, 0};
+  int k_seen = 0, v_seen = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int u = unit_of(r, num_units);
+    if (u < 0) break;
+    const Unit w = decode_unit<C>(p, u);
+#pragma unroll
+    for (int t = 0; t < C::kNQT; ++t) {
+      if (!ok || w.nblk[t] == 0) continue;
+      ok = warp_wait(&ctl->q_full[t], q_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
+      ++q_seen[t];
+      if (!ok) continue;
+      round_tf32_inplace(sQ + t * C::kQTileBytes, C::kQTileBytes, ct, C::kCvtThreads);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
+    }
+    // Same order as the producer: K_j, then V_{j - kVLag}.
+    for (int j = 0; j < w.N + C::kVLag && ok; ++j) {
+      if (j < w.N) {
+        const int slot = k_seen % C::kKStages;
+        ok = warp_wait(&ctl->k_full[slot], (k_seen / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
+        ++k_seen;
+        if (!ok) break;
+        round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, C::kCvtThreads);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
+      }
+      if (j < C::kVLag) continue;
+      // V -> V^T (K-major), then hand the V slot back to the producer.
+      const int vs = v_seen % C::kVStages, ts = v_seen % C::kVTStages;
+      ok = warp_wait(&ctl->v_full[vs], (v_seen / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      ok = warp_wait(&ctl->vt_empty[ts], ((v_seen / C::kVTStages) & 1) ^ 1, abort_flag, p.status,
+                     p.timeout_cycles);
+      ++v_seen;
+      if (!ok) break;
+      transpose_v_tile<C>(sV + vs * C::kKVTileBytes, sVT + ts * C::kKVTileBytes, ct, C::kCvtThreads);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl->vt_full[ts]);
+        mbar_arrive(&ctl->v_empty[vs]);
+      }
+    }
+  }
+}
+
 // Persistent forward kernel: each CTA walks its units; every role carries its
 // barrier phase counters from one unit to the next, so the next unit's Q and
 // K/V loads and its first S MMAs overlap the current unit's last blocks and
@@ -475,7 +537,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl->q_full[t], 1);
       mbar_init(&ctl->q_empty[t], 1);    // MMA commit after the unit's last S of tile t
-      mbar_init(&ctl->q_ready[t], 2);    // one arrival per tf32 helper warp
+      mbar_init(&ctl->q_ready[t], C::kCvtWarps);  // one arrival per tf32 helper warp
       mbar_init(&ctl->s_full[t], 1);
       mbar_init(&ctl->s_free[t], 4);     // one arrival per softmax warp
       mbar_init(&ctl->p_ready[t], 4);    // one arrival per softmax warp
@@ -485,10 +547,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     for (int s = 0; s < 4; ++s) {
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], C::kIssuers);  // one commit per issuing thread
-      mbar_init(&ctl->k_ready[s], 2);
+      mbar_init(&ctl->k_ready[s], C::kCvtWarps);
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->v_empty[s], C::kTf32 ? 2 : C::kIssuers);  // tf32: released by the two transposing warps
-      mbar_init(&ctl->vt_full[s], 2);
+      mbar_init(&ctl->v_empty[s], C::kTf32 ? C::kCvtWarps : C::kIssuers);  // tf32: released by the helper warps
+      mbar_init(&ctl->vt_full[s], C::kCvtWarps);
       mbar_init(&ctl->vt_empty[s], C::kIssuers);
     }
     mbar_init(&ctl->drain[0], 1);
@@ -496,7 +558,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     mbar_init(&ctl->m_full, 1);
     mbar_init(&ctl->m_empty, 4);  // one arrival per softmax warp
     ctl->abort = 0;
-    ctl->turn = 0;
+    mbar_init(&ctl->turn_bar[0], 1);
+    mbar_init(&ctl->turn_bar[1], 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -542,20 +605,30 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         w.q0 + t * C::kBM, w.h, w.b);
           ++q_issued[t];
         }
-        // Mask tiles reach L2 ahead of the softmax that reads them: blocks 0
-        // and 1 now, then block j + 2 while K_j / V_j are issued.
-        auto prefetch_mask = [&](int j) {
+        // Mask tiles reach L2 two blocks ahead of their use (read by the
+        // softmax from L2, or by the shared-memory mask load): block j + 2
+        // while K_j is issued, reaching into the next unit near the end of this
+        // one; a CTA's first unit prefetches its blocks 0 and 1 up front.
+        const bool pf_mask = p.mask_l2 || p.mask_smem;
+        auto prefetch_mask = [&](const Unit& uu, int j) {
           const int mesz = p.mask_kind == 1 ? 1 : C::kEsz;
           for (int t = 0; t < C::kNQT; ++t)
             for (int c = 0; c < (C::kBN * mesz) / 128; ++c)
-              tma_prefetch_l2_4d(&tmM, j * C::kBN + c * (128 / mesz), w.q0 + t * C::kBM, w.h, w.b);
+              tma_prefetch_l2_4d(&tmM, j * C::kBN + c * (128 / mesz), uu.q0 + t * C::kBM, uu.h, uu.b);
         };
-        if (p.mask_l2) {
-          for (int j = 0; j < min(2, w.N); ++j) prefetch_mask(j);
+        const int u_next = unit_of(r + 1, num_units);
+        const Unit w_next = decode_unit<C>(p, u_next < 0 ? u : u_next);
+        if (pf_mask && r == 0) {
+          for (int j = 0; j < min(2, w.N); ++j) prefetch_mask(w, j);
         }
         for (int j = 0; j < w.N + C::kVLag && ok; ++j) {
           if (j < w.N) {
-          if (p.mask_l2 && j + 2 < w.N) prefetch_mask(j + 2);
+          if (pf_mask) {
+            if (j + 2 < w.N)
+              prefetch_mask(w, j + 2);
+            else if (u_next >= 0 && j + 2 - w.N < w_next.N)
+              prefetch_mask(w_next, j + 2 - w.N);
+          }
           {  // K_j
             const int slot = k_issued % C::kKStages, use = k_issued / C::kKStages;
             ok = wait_bounded(&ctl->k_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
@@ -657,27 +730,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           mma_ts_lh<C::kTf32, 1>(dst, src + kk * 8, va + voff, v_hi, idPV, 1u);
         }
       };
-      // Two issuers take turns: turn 2g + i is issuer i's g-th MMA group.
-      volatile int* turn = &ctl->turn;
-      int my_turn = issuer;
+      // Two issuers take turns, group by group: issuer 0's group g follows
+      // issuer 1's group g - 1, and issuer 1's group g follows issuer 0's group
+      // g.  Each hand-off is an mbarrier arrival, so the waiting thread sleeps
+      // in try_wait instead of polling next to the softmax warps.
+      int groups = 0;  // MMA groups this issuer has issued
       auto wait_turn = [&]() -> bool {
-        if (C::kIssuers == 1) return true;
-        if (*turn == my_turn) return true;
-        const long long t0 = clock64_now();
-        while (*turn != my_turn) {
-          if (*abort_flag) return false;
-          if (clock64_now() - t0 > p.timeout_cycles) {
-            *abort_flag = 1;
-            atomicOr(p.status, kStatusTimeout);
-            return false;
-          }
-        }
-        return true;
+        if (C::kIssuers == 1 || (issuer == 0 && groups == 0)) return true;
+        const int phase = issuer == 0 ? groups - 1 : groups;
+        return wait_bounded(&ctl->turn_bar[issuer], phase & 1, abort_flag, p.status, p.timeout_cycles);
       };
       auto pass_turn = [&]() {
         if (C::kIssuers == 2) {
-          *turn = my_turn + 1;
-          my_turn += 2;
+          mbar_arrive(&ctl->turn_bar[1 - issuer]);
+          ++groups;
         }
       };
 
@@ -842,59 +908,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ===================================================== tf32 rounding (fp32 I/O only)
-    if constexpr (C::kTf32) {
-      const int ct = threadIdx.x - 64;  // 0..63
-      int q_seen[2] = {0, 0};
-      int k_seen = 0, v_seen = 0;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int u = unit_of(r, num_units);
-        if (u < 0) break;
-        const Unit w = decode_unit<C>(p, u);
-#pragma unroll
-        for (int t = 0; t < C::kNQT; ++t) {
-          if (!ok || w.nblk[t] == 0) continue;
-          ok = warp_wait(&ctl->q_full[t], q_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
-          ++q_seen[t];
-          if (!ok) continue;
-          round_tf32_inplace(sQ + t * C::kQTileBytes, C::kQTileBytes, ct, 64);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
-        }
-        // Same order as the producer: K_j, then V_{j - kVLag}.
-        for (int j = 0; j < w.N + C::kVLag && ok; ++j) {
-          if (j < w.N) {
-            const int slot = k_seen % C::kKStages;
-            ok = warp_wait(&ctl->k_full[slot], (k_seen / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
-            ++k_seen;
-            if (!ok) break;
-            round_tf32_inplace(sK + slot * C::kKVTileBytes, C::kKVTileBytes, ct, 64);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
-          }
-          if (j < C::kVLag) continue;
-          // V -> V^T (K-major), then hand the V slot back to the producer.
-          const int vs = v_seen % C::kVStages, ts = v_seen % C::kVTStages;
-          ok = warp_wait(&ctl->v_full[vs], (v_seen / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
-          if (!ok) break;
-          ok = warp_wait(&ctl->vt_empty[ts], ((v_seen / C::kVTStages) & 1) ^ 1, abort_flag, p.status,
-                         p.timeout_cycles);
-          ++v_seen;
-          if (!ok) break;
-          transpose_v_tile<C>(sV + vs * C::kKVTileBytes, sVT + ts * C::kKVTileBytes, ct, 64);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&ctl->vt_full[ts]);
-            mbar_arrive(&ctl->v_empty[vs]);
-          }
-        }
-      }
-    }
+    // ===================================================== tf32 helpers (fp32 I/O only)
+    if constexpr (C::kTf32) tf32_helpers<C>(sQ, sK, sV, sVT, ctl, p, abort_flag, num_units, threadIdx.x - 64, lane);
   }
+  } else if (C::kExtraHelpers && warp >= 8) {
+    // ===================================================== more tf32 helpers (one Q tile)
+    if constexpr (C::kExtraHelpers)
+      tf32_helpers<C>(sQ, sK, sV, sVT, ctl, p, abort_flag, num_units, 64 + (threadIdx.x - 256), lane);
   } else {
     // ===================================================== softmax warpgroup t
     if constexpr (C::kRegsSoftmax > 0) regs_inc<C::kRegsSoftmax>();
