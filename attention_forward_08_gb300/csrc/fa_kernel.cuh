@@ -824,6 +824,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             ++v_used;
           }
         } else
+        // P over S (two Q tiles): per block and tile, PV_j then S_{j+1}.
         for (int j = 0; j < w.N && ok; ++j) {
           // bf16: V ring slot; tf32: V^T ring slot
           const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
@@ -863,22 +864,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               turn_taken = true;
             }
             tc_fence_after();
-            if (C::kAliasP) {
-              issue_PV(t, j, vslot);
-              if (!s_next) mma_commit(&ctl->o_ready[t]);  // the tile's last PV of the unit
-              if (s_next) {
-                issue_S(t, kslot);
-                mma_commit(&ctl->s_full[t]);
-                if (s_last) mma_commit(&ctl->q_empty[t]);
-              }
-            } else {
-              if (s_next) {
-                issue_S(t, kslot);
-                mma_commit(&ctl->s_full[t]);
-                if (s_last) mma_commit(&ctl->q_empty[t]);
-              }
-              issue_PV(t, j, vslot);
-              mma_commit(&ctl->o_ready[t]);
+            issue_PV(t, j, vslot);
+            if (!s_next) mma_commit(&ctl->o_ready[t]);  // the tile's last PV of the unit
+            if (s_next) {
+              issue_S(t, kslot);
+              mma_commit(&ctl->s_full[t]);
+              if (s_last) mma_commit(&ctl->q_empty[t]);
             }
           }
           if (!ok) break;
