@@ -4,8 +4,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never does, and this
 package imports nothing from the library: the two share no code.
 
-The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, one score row at a
-time, full-row softmax).  This module builds it with the host C compiler,
+The arithmetic lives in ``attn_oracle.c`` (the forward: plain C, fp64, one
+score row at a time, full-row softmax) and ``attn_oracle_bwd.c`` (its
+gradients, written out from the chain rule through the softmax).  This module builds it with the host C compiler,
 loads it with ctypes and marshals numpy arrays.  See the C file's header for
 the definition and the page sections it follows.
 """
@@ -21,24 +22,36 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_SRC_BWD = os.path.join(_HERE, "attn_oracle_bwd.c")
+_LIB_BWD_PATH = os.path.join(_HERE, "liboracle_bwd.so")
 _lib = None
+_lib_bwd = None
+
+
+def _compile(src: str, default_path: str, tag: str, mutant: int, out_path: str | None) -> str:
+    if out_path is None:
+        out_path = default_path if mutant == 0 else os.path.join(
+            tempfile.mkdtemp(prefix="oracle_mut"), f"lib{tag}_m{mutant}.so")
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", f"-DORACLE_MUTANT={int(mutant)}", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
 
 
 def build(mutant: int = 0, out_path: str | None = None) -> str:
-    """Compile the oracle (or a variant with a planted mistake) to a shared object.
+    """Compile the forward oracle (or a variant with a planted mistake) to a shared object.
 
     ``mutant`` 0 is the oracle itself; 1..8 each plant one known mistake and
     exist only so the tests can show that the pins catch it.
     """
-    if out_path is None:
-        out_path = _LIB_PATH if mutant == 0 else os.path.join(
-            tempfile.mkdtemp(prefix="oracle_mut"), f"liboracle_m{mutant}.so")
-    tmp = out_path + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
-           "-fno-fast-math", f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, out_path)
-    return out_path
+    return _compile(_SRC, _LIB_PATH, "oracle", mutant, out_path)
+
+
+def build_bwd(mutant: int = 0, out_path: str | None = None) -> str:
+    """Compile the gradient oracle (or a variant with planted mistake 1..6)."""
+    return _compile(_SRC_BWD, _LIB_BWD_PATH, "oracle_bwd", mutant, out_path)
 
 
 def _bind(lib):
@@ -62,6 +75,68 @@ def load(path: str | None = None):
             build()
         _lib = _bind(ctypes.CDLL(_LIB_PATH))
     return _lib
+
+
+def _bind_bwd(lib):
+    f = lib.oracle_attention_bwd
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 4 + \
+        [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_bwd_mutant_id.restype = ctypes.c_int
+    return lib
+
+
+def load_bwd(path: str | None = None):
+    """Load the gradient oracle (building it first if it is missing or stale)."""
+    global _lib_bwd
+    if path is not None:
+        return _bind_bwd(ctypes.CDLL(path))
+    if _lib_bwd is None:
+        if (not os.path.exists(_LIB_BWD_PATH)
+                or os.path.getmtime(_LIB_BWD_PATH) < os.path.getmtime(_SRC_BWD)):
+            build_bwd()
+        _lib_bwd = _bind_bwd(ctypes.CDLL(_LIB_BWD_PATH))
+    return _lib_bwd
+
+
+def _mask_arg(mask, mask_kind, shape):
+    if mask_kind == 1:
+        m = np.ascontiguousarray(np.broadcast_to(np.asarray(mask) != 0, shape).astype(np.uint8))
+        return m, m.ctypes.data
+    if mask_kind == 2:
+        m = _f64(np.broadcast_to(np.asarray(mask, dtype=np.float64), shape))
+        return m, m.ctypes.data
+    if mask_kind != 0:
+        raise ValueError("mask_kind must be 0, 1 or 2")
+    return None, None
+
+
+def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
+                  mask_kind: int = 0, n_threads: int | None = None, lib=None):
+    """dQ, dK, dV of sum(O * dO) for O = softmax(scale * q k^T + mask) v, in fp64.
+
+    Shapes and mask conventions as ``attention``; dO has the shape of q.
+    Returns (dQ [B,H_q,qL,D], dK [B,H_kv,kL,D], dV [B,H_kv,kL,D]).
+    """
+    lib = lib or load_bwd()
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, qL, D = q.shape
+    Bk, Hkv, kL, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape or dO.shape != q.shape:
+        raise ValueError("shape mismatch between q, k, v and dO")
+    keep, mptr = _mask_arg(mask, mask_kind, (B, Hq, qL, kL))
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    if n_threads is None:
+        n_threads = os.cpu_count() or 1
+    rc = lib.oracle_attention_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr, int(mask_kind),
+                                  dO.ctypes.data, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                                  B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)), int(n_threads))
+    del keep
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd rejected its arguments")
+    return dq, dk, dv
 
 
 def _f64(a) -> np.ndarray:
