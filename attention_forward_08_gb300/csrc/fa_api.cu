@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_launch.h"
 #include "fa_launch.cuh"
 
 namespace fa {
@@ -321,7 +322,7 @@ int fa_sync_status(void* stream) {
     return FA_ERR_CUDA;
   }
   if (word & kStatusTimeout) {
-    set_error("a forward kernel reached its wait bound and stopped early (status 0x%x)", word);
+    set_error("a kernel reached its wait bound and stopped early (status 0x%x)", word);
     return FA_ERR_DEVICE_TIMEOUT;
   }
   return FA_OK;
@@ -337,6 +338,91 @@ void fa_set_max_ctas(int n) {
   fa::g_max_ctas = n > 0 ? n : 0;
 }
 
-int fa_version(void) { return 101; }
+long long fa_bwd_workspace_bytes(int B, int H_q, int qL) {
+  if (B <= 0 || H_q <= 0 || qL <= 0) return -1;
+  const long long bytes = (long long)B * H_q * qL * 4;
+  return (bytes + 255) / 256 * 256;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv, int qL, int kL,
+           int D, float scale, int causal, int dtype, void* stream) {
+  using namespace fa;
+  g_err[0] = '\0';
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) {
+    set_error("q, k, v, o, dout, lse, dq, dk, dv and workspace must all be non-NULL");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || qL <= 0 || kL <= 0) {
+    set_error("B (%d), H_q (%d), H_kv (%d), qL (%d) and kL (%d) must be > 0", B, H_q, H_kv, qL, kL);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (H_q % H_kv != 0) {
+    set_error("H_q (%d) must be divisible by H_kv (%d)", H_q, H_kv);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (!std::isfinite(scale)) {
+    set_error("scale must be finite");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (dtype != FA_DTYPE_BF16) {
+    set_error(dtype == FA_DTYPE_F32 ? "the backward pass supports bf16 I/O only"
+                                    : "dtype %d is not FA_DTYPE_F32 (0) or FA_DTYPE_BF16 (1)",
+              dtype);
+    return dtype == FA_DTYPE_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
+  }
+  if (D != 64 && D != 128) {
+    set_error("head dim D = %d is not supported by the backward pass (64 or 128)", D);
+    return FA_ERR_UNSUPPORTED;
+  }
+  if ((long long)B * H_q * qL > 0x7fffffffLL || (long long)B * H_kv * kL > 0x7fffffffLL) {
+    set_error("row counts exceed 2^31 - 1");
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (workspace_bytes < fa_bwd_workspace_bytes(B, H_q, qL)) {
+    set_error("workspace of %lld bytes is smaller than the %lld required", workspace_bytes,
+              fa_bwd_workspace_bytes(B, H_q, qL));
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  const void* ptrs[10] = {q, k, v, o, dout, dq, dk, dv, workspace, lse};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) {
+      set_error("q, k, v, o, dout, lse, dq, dk, dv and workspace must be 16-byte aligned");
+      return FA_ERR_MISALIGNED;
+    }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+  }
+  int rc = device_setup(dev);
+  if (rc != FA_OK) return rc;
+  BwdLaunchArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dvec = static_cast<float*>(workspace);
+  a.B = B;
+  a.Hq = H_q;
+  a.Hkv = H_kv;
+  a.qL = qL;
+  a.kL = kL;
+  a.D = D;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = g_status_ptr[dev];
+  a.timeout_cycles = timeout_cycles();
+  return launch_bwd(a);
+}
+
+int fa_version(void) { return 102; }
 
 }  // extern "C"

@@ -1,0 +1,103 @@
+// fa_bwd.cu -- launcher for the backward pass: tensor maps, grids, the three
+// launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 I/O.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_bwd_kernel.cuh"
+#include "fa_bwd_launch.h"
+#include "fa_launch.cuh"
+
+namespace fa {
+
+namespace {
+
+template <class C>
+int set_smem_once(const void* kern, uint32_t bytes, int& configured_device) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device == dev) return 0;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) {
+    set_error("cudaFuncSetAttribute(max dynamic smem = %u): %s", (unsigned)bytes, cudaGetErrorString(e));
+    return 4;
+  }
+  configured_device = dev;
+  return 0;
+}
+
+template <int kD>
+int launch_bwd_d(const BwdLaunchArgs& a) {
+  using C = BwdCfg<kD>;
+  // 1. D_i = rowsum(O_i * dO_i)
+  const long long rows = (long long)a.B * a.Hq * a.qL;
+  constexpr int kRowsPerBlock = 256 / (kD / 8);
+  const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  fa_bwd_rowdot_kernel<kD><<<(unsigned)blocks, 256, 0, a.stream>>>(
+      static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.dvec, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("row-dot launch failed: %s", cudaGetErrorString(e));
+    return 4;
+  }
+
+  // 2. Tensor maps: 128-row tiles of 128-byte swizzled column blocks.
+  const long long qst[3] = {(long long)a.Hq * a.qL * kD, (long long)a.qL * kD, kD};
+  const long long kst[3] = {(long long)a.Hkv * a.kL * kD, (long long)a.kL * kD, kD};
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_bhsd(&tq, false, a.q, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tdo, false, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tk, false, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tv, false, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
+
+  BwdParams p;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.qL = a.qL;
+  p.kL = a.kL;
+  p.group = a.Hq / a.Hkv;
+  p.causal = a.causal;
+  p.n_qt = (a.qL + C::kTile - 1) / C::kTile;
+  p.n_kt = (a.kL + C::kTile - 1) / C::kTile;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  p.lse = a.lse;
+  p.dvec = a.dvec;
+  p.dq = a.dq;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.status = a.status;
+  p.timeout_cycles = a.timeout_cycles;
+
+  static int cfg_kv = -1, cfg_q = -1;
+  if (int rc = set_smem_once<C>((const void*)fa_bwd_dkdv_kernel<C>, C::kKVSmem, cfg_kv)) return rc;
+  if (int rc = set_smem_once<C>((const void*)fa_bwd_dq_kernel<C>, C::kQSmem, cfg_q)) return rc;
+
+  // 3. dK, dV: one CTA per (128-key tile, kvh, b).
+  const long long n_kv = (long long)p.n_kt * a.Hkv * a.B;
+  const long long n_q = (long long)p.n_qt * a.Hq * a.B;
+  if (n_kv > 0x7fffffffLL || n_q > 0x7fffffffLL) {
+    set_error("backward grid of %lld / %lld CTAs is out of range", n_kv, n_q);
+    return 2;
+  }
+  fa_bwd_dkdv_kernel<C><<<(unsigned)n_kv, C::kThreads, C::kKVSmem, a.stream>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("dK/dV launch failed: %s", cudaGetErrorString(e));
+    return 4;
+  }
+  // 4. dQ: one CTA per (128-row query tile, h, b).
+  fa_bwd_dq_kernel<C><<<(unsigned)n_q, C::kThreads, C::kQSmem, a.stream>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("dQ launch failed: %s", cudaGetErrorString(e));
+    return 4;
+  }
+  return 0;
+}
+
+}  // namespace
+
+int launch_bwd(const BwdLaunchArgs& a) { return a.D == 64 ? launch_bwd_d<64>(a) : launch_bwd_d<128>(a); }
+
+}  // namespace fa

@@ -1,0 +1,750 @@
+// fa_bwd_kernel.cuh -- FlashAttention-2 backward for sm_103a (bf16 I/O):
+// dQ, dK, dV of O = softmax(scale * Q K^T) V given dO and the forward's L.
+//
+// What it computes (per batch b, query head h, kvh = h / (H_q / H_kv)):
+//   P_ij  = exp(scale * q_i . k_j - L_i)            (L from the forward)
+//   D_i   = rowsum(O_i * dO_i)
+//   dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i)
+//   dQ_i  = scale * sum_j dS_ij k_j
+//   dK_j  = scale * sum_{h in group, i} dS_ij q_i,  dV_j = sum_{h in group, i} P_ij dO_i
+// with causal (j <= i) masking and ragged tails.  Sources:
+//  - forge "flash_attention_mma.metal", section "backward (MMA)": no online
+//    rescale (L fixes the normalisation); a query-parallel dQ kernel
+//    (S = Q K^T, P = exp(S scale - L), dP = dO V^T, dS = P (dP - D), dQ += dS K)
+//    and key-parallel dK/dV work on transposed operands (S^T = K Q^T,
+//    dP^T = V dO^T, dV += P^T dO, dK += dS^T Q) whose accumulation stays
+//    private to one K/V block: no atomics, deterministic results;
+//  - mlx-native "ops/flash_attn_train.rs", section "Phase 2 -- FA-2 backward
+//    kernel (dQ, dK, dV)": the D = rowsum(O * dO) pre-pass and its [B,H_q,qL]
+//    f32 layout.
+//
+// GB300 design:
+//  - three launches: the row-dot pre-pass (HBM-bound, 16-byte loads), the
+//    dK/dV kernel (one CTA per 128-key tile of one (b, kvh); it walks every
+//    query block of every query head of the GQA group, so the group sum stays
+//    in TMEM), and the dQ kernel (one CTA per 128-row query tile);
+//  - each CTA: warp 0 issues TMA loads (and stages L, D), warp 1 owns TMEM and
+//    issues every tcgen05.mma from one thread, warps 4-7 are one elementwise
+//    warpgroup with thread r owning TMEM lane r (a key row in dK/dV, a query
+//    row in dQ);
+//  - P and dS are rounded to bf16 and written over the fp32 S and dP columns
+//    of TMEM; the next block's S and dP MMAs are ordered behind the MMAs that
+//    read them, so the elementwise work of one block overlaps the tensor core's
+//    work on the previous one;
+//  - every wait is bounded; on expiry the kernel records kStatusTimeout,
+//    drains its copies and MMAs, frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fa_kernel.cuh"
+
+namespace fa {
+
+struct BwdParams {
+  int B, Hq, Hkv, qL, kL;
+  int group;          // Hq / Hkv
+  int causal;
+  int n_qt, n_kt;     // 128-row query tiles per (b, h), 128-key tiles per (b, kvh)
+  float scale;        // softmax scale (applied to dQ and dK in the epilogue)
+  float scale_log2;   // scale * log2(e)
+  const float* lse;   // [B, Hq, qL] natural log
+  float* dvec;        // [B, Hq, qL] D_i = rowsum(O_i * dO_i)
+  void* dq;           // [B, Hq, qL, D] bf16
+  void* dk;           // [B, Hkv, kL, D] bf16
+  void* dv;           // [B, Hkv, kL, D] bf16
+  unsigned int* status;
+  long long timeout_cycles;
+};
+
+template <int kD_>
+struct BwdCfg {
+  static constexpr int kD = kD_;
+  static constexpr int kTile = 128;                     // rows per tile (queries or keys)
+  static constexpr int kNChunk = kD / 64;               // 128-byte column blocks per row
+  static constexpr uint32_t kTileBytes = kTile * kD * 2;
+  static constexpr int kStages = kD == 64 ? 4 : 2;      // streamed-tile ring depth
+  static constexpr int kKStep = 16;                     // bf16 MMA K per instruction
+  static constexpr int kThreads = 256;
+  // TMEM columns: S (or S^T) 0..127, dP (or dP^T) 128..255, then the accumulators.
+  static constexpr int kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + kD;
+  static constexpr uint32_t kTmemCols = 512;
+  // dK/dV kernel shared memory: K, V, then Q and dO rings, then L2 and D slots.
+  static constexpr uint32_t kKVOffQ = 2 * kTileBytes;
+  static constexpr uint32_t kKVOffDO = kKVOffQ + kStages * kTileBytes;
+  static constexpr uint32_t kKVOffLD = kKVOffDO + kStages * kTileBytes;
+  static constexpr uint32_t kKVOffBar = kKVOffLD + kStages * 2 * kTile * 4;
+  static constexpr uint32_t kKVSmem = 1024 + kKVOffBar + 512;
+  // dQ kernel shared memory: Q, dO, then K and V rings.
+  static constexpr uint32_t kQOffK = 2 * kTileBytes;
+  static constexpr uint32_t kQOffV = kQOffK + kStages * kTileBytes;
+  static constexpr uint32_t kQOffBar = kQOffV + kStages * kTileBytes;
+  static constexpr uint32_t kQSmem = 1024 + kQOffBar + 512;
+  static_assert(kD == 64 || kD == 128, "backward head dims: 64 or 128");
+  static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "shared memory overflow");
+  static_assert(kColAcc1 + kD <= 512, "TMEM overflow");
+};
+
+struct BwdKVCtrl {
+  uint64_t kv_full;
+  uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4], ld_full[4], ld_empty[4];
+  uint64_t s_full, dp_full, p_ready, ds_ready, done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct BwdQCtrl {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full, s_free, dp_full, ds_ready, done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// ---------------------------------------------------------------- D pre-pass
+
+// D_i = sum_d O_id dO_id for every row of a contiguous [rows, kD] bf16 pair:
+// kD / 8 threads per row, one 16-byte load of each operand per thread, fp32
+// products, a shuffle reduction within the row's threads.
+template <int kD>
+__global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const uint4* __restrict__ o,
+                                                            const uint4* __restrict__ dout,
+                                                            float* __restrict__ dvec, long long rows) {
+  constexpr int kLanes = kD / 8;            // threads per row
+  constexpr int kRowsPerBlock = 256 / kLanes;
+  const int sub = threadIdx.x % kLanes;
+  const long long row = (long long)blockIdx.x * kRowsPerBlock + threadIdx.x / kLanes;
+  float acc = 0.0f;
+  if (row < rows) {
+    const uint4 a = __ldg(o + row * kLanes + sub);
+    const uint4 g = __ldg(dout + row * kLanes + sub);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(gw[e] << 16), acc);
+      acc = fmaf(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(gw[e] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) dvec[row] = acc;
+}
+
+// ---------------------------------------------------------------- shared pieces
+
+// S-like product: dst (+)= A[128 x kD] * B[128 x kD]^T, both K-major tiles of
+// 128-byte swizzled rows (kD / 64 column blocks of 128 rows).
+template <class C>
+__device__ __forceinline__ void bwd_mma_kmajor(uint32_t dst, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc) {
+  constexpr int kCol = (C::kTile * 128) >> 4;
+  mma_ss_lh<false, 0>(dst, a_lo, a_hi, b_lo, b_hi, idesc, 0u);
+#pragma unroll
+  for (int kk = 1; kk < C::kD / C::kKStep; ++kk)
+    mma_ss_lh<false, 1>(dst, a_lo + (kk / 4) * kCol + (kk % 4) * 2, a_hi, b_lo + (kk / 4) * kCol + (kk % 4) * 2,
+                        b_hi, idesc, 1u);
+}
+
+// Accumulating product: dst (+)= A[128 x 128] (bf16 pairs in TMEM) * B[128 x kD]
+// with B an MN-major tile in shared memory (rows = the MMA's K).
+template <class C>
+__device__ __forceinline__ void bwd_mma_tmem_a(uint32_t dst, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                               uint32_t idesc, uint32_t acc) {
+  mma_ts_lh<false, 0>(dst, a_tmem, b_lo, b_hi, idesc, acc);
+#pragma unroll
+  for (int kk = 1; kk < C::kTile / C::kKStep; ++kk)
+    mma_ts_lh<false, 1>(dst, a_tmem + kk * 8, b_lo + ((kk * C::kKStep * 128) >> 4), b_hi, idesc, 1u);
+}
+
+// Read 128 fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
+  uint32_t rr[128];
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) tmem_ld32(taddr + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[cc * 32]));
+  tmem_wait_ld();
+  reg_fence(rr);
+#pragma unroll
+  for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(rr[c]);
+}
+
+// dS = P (dP - d) chunk by chunk: read 32 fp32 dP columns, write 16 columns of
+// bf16 pairs over the part of the dP region already read.  dsub(c) gives the
+// D term of column c.
+template <class F>
+__device__ __forceinline__ void bwd_ds_pass(uint32_t tdp, const float (&p)[128], F dsub) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t rr[32];
+    tmem_ld32(tdp + cc * 32, rr);
+    tmem_wait_ld();
+    reg_fence(rr);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int c0 = cc * 32 + 2 * e;
+      const float d0 = p[c0] * (__uint_as_float(rr[2 * e]) - dsub(c0));
+      const float d1 = p[c0 + 1] * (__uint_as_float(rr[2 * e + 1]) - dsub(c0 + 1));
+      pk[e] = pack_bf16x2(d0, d1);
+    }
+    tmem_st16(tdp + cc * 16, pk);
+  }
+}
+
+// Store a 128 x kD fp32 accumulator row (this thread's lane), times `mul`, as
+// bf16 to a contiguous row of global memory (16-byte stores).
+template <class C>
+__device__ __forceinline__ void bwd_store_row(uint32_t tacc, float mul, __nv_bfloat16* dst, bool store) {
+#pragma unroll
+  for (int cc = 0; cc < C::kD / 32; ++cc) {
+    uint32_t rr[32];
+    tmem_ld32(tacc + cc * 32, rr);
+    tmem_wait_ld();
+    reg_fence(rr);
+    if (store) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(rr[8 * u + 2 * e]) * mul, __uint_as_float(rr[8 * u + 2 * e + 1]) * mul);
+        d4[u] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- dK / dV
+
+// One CTA per (128-key tile, kvh, b), heavy (early) key tiles first.  It walks
+// steps i = (query head r of the group, query block qb) and accumulates
+//   dV += P^T dO and dK += dS^T Q   (scale applied in the epilogue)
+// with S^T = K Q^T and dP^T = V dO^T recomputed per step.
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const BwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kTileBytes;
+  uint8_t* sQ = smem + C::kKVOffQ;
+  uint8_t* sDO = smem + C::kKVOffDO;
+  float* sLD = reinterpret_cast<float*>(smem + C::kKVOffLD);  // per slot: 128 L2 values, then 128 D values
+  BwdKVCtrl* ctl = reinterpret_cast<BwdKVCtrl*>(smem + C::kKVOffBar);
+  volatile int* abort_flag = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_kt = p.Hkv * p.B;
+  const int kt = blockIdx.x / per_kt;
+  const int rem = blockIdx.x - kt * per_kt;
+  const int b = rem / p.Hkv, kvh = rem - b * p.Hkv;
+  const int k0 = kt * C::kTile;
+  // Causal: only queries i >= k0 see this tile's keys.
+  const int qb0 = p.causal ? min(k0 / C::kTile, p.n_qt) : 0;
+  const int per_head = p.n_qt - qb0;
+  const int n_steps = p.group * per_head;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->kv_full, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&ctl->q_full[s], 1);
+      mbar_init(&ctl->q_empty[s], 1);
+      mbar_init(&ctl->do_full[s], 1);
+      mbar_init(&ctl->do_empty[s], 1);
+      mbar_init(&ctl->ld_full[s], 32);   // every producer lane stages its 4 queries
+      mbar_init(&ctl->ld_empty[s], 4);   // one arrival per elementwise warp
+    }
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->dp_full, 1);
+    mbar_init(&ctl->p_ready, 4);
+    mbar_init(&ctl->ds_ready, 4);
+    mbar_init(&ctl->done, 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  auto step_of = [&](int i, int& h, int& q0) {
+    const int r = i / per_head;
+    h = kvh * p.group + r;
+    q0 = (qb0 + (i - r * per_head)) * C::kTile;
+  };
+
+  if (warp == 0) {
+    // ===================================================== producer: TMA + L, D staging
+    int q_issued = 0, do_issued = 0;
+    bool ok = true;
+    if (lane == 0 && n_steps > 0) {
+      mbar_arrive_expect_tx(&ctl->kv_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kNChunk; ++c) {
+        tma_load_4d(sK + c * (C::kTile * 128), &tmK, &ctl->kv_full, c * 64, k0, kvh, b);
+        tma_load_4d(sV + c * (C::kTile * 128), &tmV, &ctl->kv_full, c * 64, k0, kvh, b);
+      }
+    }
+    for (int i = 0; i < n_steps && ok; ++i) {
+      int h, q0;
+      step_of(i, h, q0);
+      const int s = i % C::kStages, use = i / C::kStages;
+      if (lane == 0) {
+        ok = wait_bounded(&ctl->q_empty[s], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+        if (ok) {
+          mbar_arrive_expect_tx(&ctl->q_full[s], C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kNChunk; ++c)
+            tma_load_4d(sQ + s * C::kTileBytes + c * (C::kTile * 128), &tmQ, &ctl->q_full[s], c * 64, q0, h, b);
+          ++q_issued;
+          ok = wait_bounded(&ctl->do_empty[s], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+        }
+        if (ok) {
+          mbar_arrive_expect_tx(&ctl->do_full[s], C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kNChunk; ++c)
+            tma_load_4d(sDO + s * C::kTileBytes + c * (C::kTile * 128), &tmDO, &ctl->do_full[s], c * 64, q0, h, b);
+          ++do_issued;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      // L2 = L * log2(e) (+inf where the query is past qL or its row had no
+      // allowed key, so P = 0 there) and D for the block's 128 queries.
+      ok = warp_wait(&ctl->ld_empty[s], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      float* l2s = sLD + s * 2 * C::kTile;
+      const long long base = ((long long)b * p.Hq + h) * p.qL;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = lane * 4 + e, iq = q0 + c;
+        float l2 = __int_as_float(0x7f800000), dv = 0.0f;
+        if (iq < p.qL) {
+          const float L = __ldg(p.lse + base + iq);
+          if (L != -INFINITY) l2 = L * kLog2e;
+          dv = p.dvec[base + iq];
+        }
+        l2s[c] = l2;
+        l2s[C::kTile + c] = dv;
+      }
+      mbar_arrive(&ctl->ld_full[s]);
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let every copy this thread started land before the CTA lets go of its memory.
+      if (n_steps > 0) wait_bounded(&ctl->kv_full, 0, abort_flag, p.status, kDrainCycles, false);
+      for (int it = max(0, q_issued - C::kStages); it < q_issued; ++it)
+        wait_bounded(&ctl->q_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, p.status, kDrainCycles,
+                     false);
+      for (int it = max(0, do_issued - C::kStages); it < do_issued; ++it)
+        wait_bounded(&ctl->do_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, p.status, kDrainCycles,
+                     false);
+    }
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer
+    if (lane == 0 && n_steps > 0) {
+      constexpr uint32_t idS = make_idesc(false, 128, 128, false, false);     // K-major A and B
+      constexpr uint32_t idAcc = make_idesc(false, 128, C::kD, false, true);  // B MN-major
+      const uint64_t dK = make_sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = make_sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dQk = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dOk = make_sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t dQmn = make_sdesc_sw128(smem_u32(sQ), C::kTile * 128, 1024);
+      const uint64_t dOmn = make_sdesc_sw128(smem_u32(sDO), C::kTile * 128, 1024);
+      const uint32_t hi = (uint32_t)(dK >> 32), hi_mn = (uint32_t)(dQmn >> 32);
+      const uint32_t slot = C::kTileBytes >> 4;
+      auto issue_s = [&](int s) {  // S^T = K Q_s^T
+        bwd_mma_kmajor<C>(tmem + C::kColS, (uint32_t)dK, hi, (uint32_t)dQk + s * slot, hi, idS);
+      };
+      auto issue_dp = [&](int s) {  // dP^T = V dO_s^T
+        bwd_mma_kmajor<C>(tmem + C::kColDP, (uint32_t)dV, hi, (uint32_t)dOk + s * slot, hi, idS);
+      };
+      bool ok = wait_bounded(&ctl->kv_full, 0, abort_flag, p.status, p.timeout_cycles);
+      if (ok) ok = wait_bounded(&ctl->q_full[0], 0, abort_flag, p.status, p.timeout_cycles);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        mma_commit(&ctl->s_full);
+        ok = wait_bounded(&ctl->do_full[0], 0, abort_flag, p.status, p.timeout_cycles);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+        mma_commit(&ctl->dp_full);
+      }
+      for (int i = 0; i < n_steps && ok; ++i) {
+        const int s = i % C::kStages;
+        const int s1 = (i + 1) % C::kStages, use1 = (i + 1) / C::kStages;
+        const bool more = i + 1 < n_steps;
+        ok = wait_bounded(&ctl->p_ready, i & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO_i (P^T: bf16 pairs over the S^T columns)
+        bwd_mma_tmem_a<C>(tmem + C::kColAcc0, tmem + C::kColS, (uint32_t)dOmn + s * slot, hi_mn, idAcc,
+                          i > 0 ? 1u : 0u);
+        mma_commit(&ctl->do_empty[s]);
+        if (more) {
+          ok = wait_bounded(&ctl->q_full[s1], use1 & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(s1);
+          mma_commit(&ctl->s_full);
+        }
+        ok = wait_bounded(&ctl->ds_ready, i & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        tc_fence_after();
+        // dK += dS^T Q_i (dS^T: bf16 pairs over the dP^T columns)
+        bwd_mma_tmem_a<C>(tmem + C::kColAcc1, tmem + C::kColDP, (uint32_t)dQmn + s * slot, hi_mn, idAcc,
+                          i > 0 ? 1u : 0u);
+        mma_commit(&ctl->q_empty[s]);
+        if (more) {
+          ok = wait_bounded(&ctl->do_full[s1], use1 & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(s1);
+          mma_commit(&ctl->dp_full);
+        }
+      }
+      if (ok) mma_commit(&ctl->done);
+      // Drain: every MMA this thread issued completes before TMEM is freed.
+      mma_commit(&ctl->drain);
+      wait_bounded(&ctl->drain, 0, abort_flag, p.status, kDrainCycles, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ===================================================== elementwise warpgroup: thread = key row
+    const int tl = threadIdx.x - 128;
+    const int j = k0 + tl;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kColS;
+    const uint32_t tDP = tmem + lane_addr + C::kColDP;
+    const float sl = p.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < n_steps && ok; ++i) {
+      int h, q0;
+      step_of(i, h, q0);
+      const int s = i % C::kStages, use = i / C::kStages;
+      const float* l2s = sLD + s * 2 * C::kTile;
+      ok = warp_wait(&ctl->ld_full[s], use & 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      ok = warp_wait(&ctl->s_full, i & 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      tc_fence_after();
+      float pr[128];
+      tmem_ld128(tS, pr);
+      // P^T_{j,c} = 2^(s * scale * log2e - L2_c); queries c < j - q0 are causally masked,
+      // and a key row past kL gets no probability at all.
+      int lim = p.causal ? j - q0 : 0;
+      if (j >= p.kL) lim = C::kTile;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        float x0, x1;
+        ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2s[c], -l2s[c + 1]);
+        pr[c] = c < lim ? 0.0f : ex2(x0);
+        pr[c + 1] = c + 1 < lim ? 0.0f : ex2(x1);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cc * 32 + 2 * e], pr[cc * 32 + 2 * e + 1]);
+        tmem_st16(tS + cc * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_ready);
+      // dS^T = P^T (dP^T - D_c)
+      ok = warp_wait(&ctl->dp_full, i & 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      tc_fence_after();
+      bwd_ds_pass(tDP, pr, [&](int c) { return l2s[C::kTile + c]; });
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl->ds_ready);
+        mbar_arrive(&ctl->ld_empty[s]);
+      }
+    }
+    // ---- epilogue: dV and scale * dK rows (key j) as bf16
+    if (ok) {
+      const bool store = j < p.kL;
+      const long long row = ((long long)b * p.Hkv + kvh) * p.kL + (store ? j : 0);
+      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(p.dv) + row * C::kD;
+      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(p.dk) + row * C::kD;
+      if (n_steps == 0) {  // no query sees these keys: zero gradients
+        if (store) {
+          uint4* a4 = reinterpret_cast<uint4*>(dvp);
+          uint4* b4 = reinterpret_cast<uint4*>(dkp);
+          for (int u = 0; u < C::kD / 8; ++u) a4[u] = b4[u] = make_uint4(0, 0, 0, 0);
+        }
+      } else {
+        ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
+        if (ok) {
+          tc_fence_after();
+          bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, 1.0f, dvp, store);
+          bwd_store_row<C>(tmem + lane_addr + C::kColAcc1, p.scale, dkp, store);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+
+// One CTA per (128-row query tile, h, b), heavy (late, causal) tiles first.
+// Per key block j: S = Q K_j^T, dP = dO V_j^T, dS = P (dP - D), dQ += dS K_j.
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const BwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::kTileBytes;
+  uint8_t* sK = smem + C::kQOffK;
+  uint8_t* sV = smem + C::kQOffV;
+  BwdQCtrl* ctl = reinterpret_cast<BwdQCtrl*>(smem + C::kQOffBar);
+  volatile int* abort_flag = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_qt = p.Hq * p.B;
+  const int qt_rev = blockIdx.x / per_qt;
+  const int rem = blockIdx.x - qt_rev * per_qt;
+  const int b = rem / p.Hq, h = rem - b * p.Hq;
+  const int qt = p.causal ? p.n_qt - 1 - qt_rev : qt_rev;
+  const int q0 = qt * C::kTile;
+  const int kvh = h / p.group;
+  const int last = min(q0 + C::kTile, p.qL) - 1;
+  const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
+  const int n_blk = (kv_end + C::kTile - 1) / C::kTile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->q_full, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
+    }
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->s_free, 4);
+    mbar_init(&ctl->dp_full, 1);
+    mbar_init(&ctl->ds_ready, 4);
+    mbar_init(&ctl->done, 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ===================================================== producer
+    if (lane == 0 && n_blk > 0) {
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(&ctl->q_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kNChunk; ++c) {
+        tma_load_4d(sQ + c * (C::kTile * 128), &tmQ, &ctl->q_full, c * 64, q0, h, b);
+        tma_load_4d(sDO + c * (C::kTile * 128), &tmDO, &ctl->q_full, c * 64, q0, h, b);
+      }
+      for (int j = 0; j < n_blk && ok; ++j) {
+        const int s = j % C::kStages, use = j / C::kStages;
+        ok = wait_bounded(&ctl->k_empty[s], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&ctl->k_full[s], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kNChunk; ++c)
+          tma_load_4d(sK + s * C::kTileBytes + c * (C::kTile * 128), &tmK, &ctl->k_full[s], c * 64, j * C::kTile,
+                      kvh, b);
+        ++k_issued;
+        ok = wait_bounded(&ctl->v_empty[s], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&ctl->v_full[s], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kNChunk; ++c)
+          tma_load_4d(sV + s * C::kTileBytes + c * (C::kTile * 128), &tmV, &ctl->v_full[s], c * 64, j * C::kTile,
+                      kvh, b);
+        ++v_issued;
+      }
+      if (*abort_flag) {
+        wait_bounded(&ctl->q_full, 0, abort_flag, p.status, kDrainCycles, false);
+        for (int it = max(0, k_issued - C::kStages); it < k_issued; ++it)
+          wait_bounded(&ctl->k_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, p.status, kDrainCycles,
+                       false);
+        for (int it = max(0, v_issued - C::kStages); it < v_issued; ++it)
+          wait_bounded(&ctl->v_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, p.status, kDrainCycles,
+                       false);
+      }
+    }
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer
+    if (lane == 0 && n_blk > 0) {
+      constexpr uint32_t idS = make_idesc(false, 128, 128, false, false);
+      constexpr uint32_t idAcc = make_idesc(false, 128, C::kD, false, true);
+      const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dO = make_sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dVk = make_sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dKmn = make_sdesc_sw128(smem_u32(sK), C::kTile * 128, 1024);
+      const uint32_t hi = (uint32_t)(dQ >> 32), hi_mn = (uint32_t)(dKmn >> 32);
+      const uint32_t slot = C::kTileBytes >> 4;
+      auto issue_s = [&](int s) { bwd_mma_kmajor<C>(tmem + C::kColS, (uint32_t)dQ, hi, (uint32_t)dKk + s * slot, hi, idS); };
+      auto issue_dp = [&](int s) { bwd_mma_kmajor<C>(tmem + C::kColDP, (uint32_t)dO, hi, (uint32_t)dVk + s * slot, hi, idS); };
+      bool ok = wait_bounded(&ctl->q_full, 0, abort_flag, p.status, p.timeout_cycles);
+      if (ok) ok = wait_bounded(&ctl->k_full[0], 0, abort_flag, p.status, p.timeout_cycles);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        mma_commit(&ctl->s_full);
+        ok = wait_bounded(&ctl->v_full[0], 0, abort_flag, p.status, p.timeout_cycles);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
+        mma_commit(&ctl->dp_full);
+        mma_commit(&ctl->v_empty[0]);
+      }
+      for (int j = 0; j < n_blk && ok; ++j) {
+        const int s = j % C::kStages;
+        const int s1 = (j + 1) % C::kStages, use1 = (j + 1) / C::kStages;
+        const bool more = j + 1 < n_blk;
+        ok = wait_bounded(&ctl->s_free, j & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        if (more) {
+          ok = wait_bounded(&ctl->k_full[s1], use1 & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(s1);
+          mma_commit(&ctl->s_full);
+        }
+        ok = wait_bounded(&ctl->ds_ready, j & 1, abort_flag, p.status, p.timeout_cycles);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ += dS K_j (dS: bf16 pairs over the dP columns; K_j read MN-major)
+        bwd_mma_tmem_a<C>(tmem + C::kColAcc0, tmem + C::kColDP, (uint32_t)dKmn + s * slot, hi_mn, idAcc,
+                          j > 0 ? 1u : 0u);
+        mma_commit(&ctl->k_empty[s]);
+        if (more) {
+          ok = wait_bounded(&ctl->v_full[s1], use1 & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(s1);
+          mma_commit(&ctl->dp_full);
+          mma_commit(&ctl->v_empty[s1]);
+        }
+      }
+      if (ok) mma_commit(&ctl->done);
+      mma_commit(&ctl->drain);
+      wait_bounded(&ctl->drain, 0, abort_flag, p.status, kDrainCycles, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ===================================================== elementwise warpgroup: thread = query row
+    const int tl = threadIdx.x - 128;
+    const int i = q0 + tl;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kColS;
+    const uint32_t tDP = tmem + lane_addr + C::kColDP;
+    const float sl = p.scale_log2;
+    const long long rowi = ((long long)b * p.Hq + h) * p.qL + (i < p.qL ? i : 0);
+    float l2 = __int_as_float(0x7f800000), di = 0.0f;
+    if (i < p.qL) {
+      const float L = __ldg(p.lse + rowi);
+      if (L != -INFINITY) l2 = L * kLog2e;
+      di = p.dvec[rowi];
+    }
+    bool ok = true;
+    for (int j = 0; j < n_blk && ok; ++j) {
+      const int kbase = j * C::kTile;
+      ok = warp_wait(&ctl->s_full, j & 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      tc_fence_after();
+      float pr[128];
+      tmem_ld128(tS, pr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->s_free);
+      // P = 2^(s * scale * log2e - L2_i) for keys below the causal and kL limits.
+      int lim = p.kL - kbase;
+      if (p.causal) lim = min(lim, i + 1 - kbase);
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        float x0, x1;
+        ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2, -l2);
+        pr[c] = c < lim ? ex2(x0) : 0.0f;
+        pr[c + 1] = c + 1 < lim ? ex2(x1) : 0.0f;
+      }
+      ok = warp_wait(&ctl->dp_full, j & 1, abort_flag, p.status, p.timeout_cycles);
+      if (!ok) break;
+      tc_fence_after();
+      bwd_ds_pass(tDP, pr, [&](int) { return di; });
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->ds_ready);
+    }
+    if (ok) {
+      const bool store = i < p.qL;
+      __nv_bfloat16* dqp = static_cast<__nv_bfloat16*>(p.dq) + rowi * C::kD;
+      if (n_blk == 0) {
+        if (store) {
+          uint4* a4 = reinterpret_cast<uint4*>(dqp);
+          for (int u = 0; u < C::kD / 8; ++u) a4[u] = make_uint4(0, 0, 0, 0);
+        }
+      } else {
+        ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
+        if (ok) {
+          tc_fence_after();
+          bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, p.scale, dqp, store);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

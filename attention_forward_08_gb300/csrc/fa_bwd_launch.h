@@ -1,0 +1,26 @@
+// fa_bwd_launch.h -- host-side interface between the C ABI layer and the
+// backward launcher (fa_bwd.cu).  Arguments arrive already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct BwdLaunchArgs {
+  const void *q, *k, *v, *o, *dout;  // bf16, contiguous [B,H,L,D]
+  const float* lse;                  // [B, H_q, qL]
+  void *dq, *dk, *dv;                // bf16 outputs
+  float* dvec;                       // [B, H_q, qL] scratch for D = rowsum(O * dO)
+  int B, Hq, Hkv, qL, kL, D;
+  float scale;
+  int causal;
+  cudaStream_t stream;
+  unsigned int* status;
+  long long timeout_cycles;
+};
+
+// Launches the D pre-pass, the dK/dV kernel and the dQ kernel on a.stream.
+// Returns 0, or an fa_status code with the message set.
+int launch_bwd(const BwdLaunchArgs& a);
+
+}  // namespace fa

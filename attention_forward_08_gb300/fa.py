@@ -1,12 +1,13 @@
 """ctypes binding of the C ABI in ``include/fa.h`` (argument marshalling only).
 
-``fa_fwd``, ``fa_fwd_ex``, ``fa_last_error``, ``fa_sync_status``,
-``fa_set_timeout_cycles`` and ``fa_version`` mirror the C entry points one to
-one and take raw device pointers (ints).  ``attention`` is a convenience
-wrapper for torch CUDA tensors: it checks device, dtype, shape and strides
-(the buffer checks of mlx-native "ops/flash_attn_train.rs",
-`validate_buffer_size`), allocates the outputs if none are given and calls
-``fa_fwd_ex`` on the current torch stream.  Every step of the computation
+``fa_fwd``, ``fa_fwd_ex``, ``fa_bwd``, ``fa_bwd_workspace_bytes``,
+``fa_last_error``, ``fa_sync_status``, ``fa_set_timeout_cycles``,
+``fa_set_max_ctas`` and ``fa_version`` mirror the C entry points one to one
+and take raw device pointers (ints).  ``attention`` and ``attention_bwd`` are
+convenience wrappers for torch CUDA tensors: they check device, dtype, shape
+and strides (the buffer checks of mlx-native "ops/flash_attn_train.rs",
+`validate_buffer_size`), allocate outputs (and the backward's workspace) if
+none are given and call the C ABI on the current torch stream.  Every step of the computation
 runs in the CUDA library; there is no fallback.
 """
 from __future__ import annotations
@@ -25,7 +26,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED
                 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_set_max_ctas",
-            "fa_version")
+            "fa_bwd_workspace_bytes", "fa_bwd", "fa_version")
 
 
 class FaError(RuntimeError):
@@ -78,6 +79,11 @@ def load_library(path: str = LIB_PATH):
     lib.fa_set_max_ctas.argtypes = [ctypes.c_int]
     lib.fa_version.restype = ctypes.c_int
     lib.fa_version.argtypes = []
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
+    lib.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 3
+    lib.fa_bwd.restype = ctypes.c_int
+    lib.fa_bwd.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
+        [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     _lib = lib
     return lib
 
@@ -118,6 +124,17 @@ def fa_set_max_ctas(n: int) -> None:
 
 def fa_version() -> int:
     return load_library().fa_version()
+
+
+def fa_bwd_workspace_bytes(B: int, H_q: int, qL: int) -> int:
+    return load_library().fa_bwd_workspace_bytes(int(B), int(H_q), int(qL))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale, causal,
+           dtype, stream):
+    """``fa_bwd`` of include/fa.h; pointers are ints (device addresses). Returns the status."""
+    return load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes), B, H_q, H_kv,
+                                  qL, kL, D, float(scale), int(causal), int(dtype), stream)
 
 
 # ----------------------------------------------------------------- torch convenience layer
@@ -207,3 +224,47 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
                      stream=stream)
     _check(fa_fwd_ex(args))
     return out, lse
+
+
+def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
+                  stream=None):
+    """dQ, dK, dV for torch CUDA tensors; returns (dq, dk, dv).
+
+    q, o, dout: contiguous bf16 [B, H_q, qL, D]; k, v: contiguous bf16
+    [B, H_kv, kL, D]; lse: the forward's contiguous fp32 [B, H_q, qL].
+    workspace: optional device tensor of at least ``fa_bwd_workspace_bytes``
+    bytes (allocated here if None).
+    """
+    import torch
+    B, H_q, qL, D = q.shape
+    Bk, H_kv, kL, Dk = k.shape
+    if tuple(v.shape) != (Bk, H_kv, kL, Dk) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    for name, t in (("o", o), ("dout", dout)):
+        if tuple(t.shape) != (B, H_q, qL, D):
+            raise ValueError(f"{name} must be [B, H_q, qL, D] = {(B, H_q, qL, D)} (got {tuple(t.shape)})")
+    if tuple(lse.shape) != (B, H_q, qL) or lse.dtype != torch.float32:
+        raise ValueError(f"lse must be fp32 [B, H_q, qL] = {(B, H_q, qL)}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if name != "lse" and t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16 (the backward pass supports bf16 I/O)")
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    need = fa_bwd_workspace_bytes(B, H_q, qL)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds fewer than the {need} bytes required")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    _check(fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                  workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
+                  1.0 / math.sqrt(D) if scale is None else scale, causal, FA_DTYPE_BF16, stream))
+    return dq, dk, dv

@@ -15,6 +15,12 @@ and device->host copies of O and L are all inside the timed region.
 ``cpu_baseline`` times the fp64 oracle (test infrastructure, CPU) on a
 bounded sample of query rows of the same workload.
 ``--impl reference`` times that oracle alone (the CPU reference arm).
+
+``--pass bwd`` measures the backward instead: a step is one ``fa_bwd`` call
+(D pre-pass, dK/dV kernel, dQ kernel) on the forward's own O and L, and
+``value`` is TFLOP/s = 2.5x the forward's count (the five products of the
+FA-2 backward) / mean call time; its ``cpu_baseline`` times the fp64
+gradient oracle on whole GQA groups of the same workload.
 """
 from __future__ import annotations
 
@@ -38,14 +44,16 @@ import workloads  # noqa: E402
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["attention_forward_08_gb300/csrc/fa_kernel.cuh", "attention_forward_08_gb300/csrc/fa_ptx.cuh",
                   "attention_forward_08_gb300/csrc/fa_launch.cuh"]
+BWD_KERNEL_SOURCES = ["attention_forward_08_gb300/csrc/fa_bwd_kernel.cuh", "attention_forward_08_gb300/csrc/fa_bwd.cu",
+                      "attention_forward_08_gb300/csrc/fa_kernel.cuh", "attention_forward_08_gb300/csrc/fa_ptx.cuh"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 # ----------------------------------------------------------------------------- helpers
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -74,15 +82,17 @@ def algorithmic_bytes(w: workloads.Workload) -> int:
     return qo + kv + lse + mask
 
 
-def traffic_from_profiles(w: workloads.Workload):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_{w.name}.md")
+def traffic_from_profiles(w: workloads.Workload, kind: str = "fwd"):
+    """DRAM bytes per launch (per call for the backward) from a committed ncu summary, if it was
+    taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"fa_{kind}_{w.name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash():
+    src = BWD_KERNEL_SOURCES if kind == "bwd" else KERNEL_SOURCES
+    if not m or not s or s.group(1) != kernel_source_hash(src):
         return None
     return float(m.group(1))
 
@@ -392,6 +402,154 @@ def run_ours(args, w):
     return 0
 
 
+def oracle_bwd_sample(w, q, k, v, do, seconds):
+    """Time the fp64 gradient oracle on a bounded sample of the workload: whole GQA groups of batch
+    0 (as many kv heads as host threads), on the leading Ls positions of the sequence, Ls grown from
+    256 until one run takes about `seconds`."""
+    import numpy as np
+
+    import oracle
+    threads = os.cpu_count() or 1
+    group = w.H_q // w.H_kv
+    n_kv = max(1, min(w.H_kv, threads))
+
+    def run(Ls):
+        qs = q[:1, :n_kv * group, :Ls].double().numpy()
+        ks, vs = k[:1, :n_kv, :Ls].double().numpy(), v[:1, :n_kv, :Ls].double().numpy()
+        dos = do[:1, :n_kv * group, :Ls].double().numpy()
+        t0 = time.perf_counter()
+        oracle.attention_bwd(qs, ks, vs, dos, float(np.float32(w.sm_scale)), causal=w.causal, n_threads=threads)
+        return time.perf_counter() - t0
+
+    Ls = min(256, w.qL, w.kL)
+    dt = run(Ls)
+    if dt < seconds / 4 and Ls < min(w.qL, w.kL):
+        Ls = min(w.qL, w.kL, max(Ls, int(Ls * (seconds / max(dt, 1e-6)) ** 0.5) // 128 * 128))
+        dt = run(Ls)
+    sub = w.with_(B=1, H_q=n_kv * group, H_kv=n_kv, qL=Ls, kL=Ls)
+    return 2.5 * sub.flops(), dt, f"{n_kv} whole GQA groups of batch 0 on the first {Ls} positions", min(threads, n_kv)
+
+
+def run_ours_bwd(args, w):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import attention_forward_08_gb300 as fa
+    fa.load_library()
+    if w.dtype != "bf16" or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128):
+        raise SystemExit(f"--pass bwd needs an unmasked bf16 BHSD workload with D 64 or 128 ({w.name})")
+    q, k, v = workloads.make_qkv(w)
+    do = workloads.make_dout(w)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    od, lsed = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_bytes = fa.fa_bwd_workspace_bytes(w.B, w.H_q, w.qL)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ptrs = [t.data_ptr() for t in (qd, kd, vd, od, dod, lsed, dq, dk, dv, ws)]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def launch():
+        rc = fa.fa_bwd(*ptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal,
+                       fa.FA_DTYPE_BF16, stream.cuda_stream)
+        if rc != 0:
+            raise fa.FaError(rc, fa.fa_last_error())
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        launch()
+    torch.cuda.synchronize(dev)
+    assert fa.fa_sync_status(None) == 0, fa.fa_last_error()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.window[0] = time.time()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    sampler.window[1] = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    assert fa.fa_sync_status(None) == 0, fa.fa_last_error()
+    call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = max_over_ranks(sum(call_ms) / len(call_ms), world, dev)
+    flops = 2.5 * w.flops()
+    value = flops * world / (mean_ms * 1e-3) / 1e12
+
+    # end to end: pinned host inputs (q, k, v, o, dO, L) -> device -> fa_bwd -> host dq, dk, dv
+    host_in = [t.cpu().pin_memory() for t in (qd, kd, vd, od, dod, lsed)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    dev_in = (qd, kd, vd, od, dod, lsed)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        launch()
+        for h_, d_ in zip(host_out, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    clocks = sampler.summary()
+    line = {
+        "metric": "attention bwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_of(w, argparse.Namespace(gpus=world)), **{"pass": "bwd"}),
+        "roofline": {"bound": "tensor", "achieved": flops / (mean_ms * 1e-3) / 1e12, "peak": peak,
+                     "unit": "TFLOP/s", "frac": flops / (mean_ms * 1e-3) / 1e12 / peak,
+                     "traffic": traffic_from_profiles(w, "bwd"),
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "kernels": "one fa_bwd call: D pre-pass + dK/dV + dQ"},
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+                   "samples": clocks["samples"]},
+        "gpu_launches": 3 * args.steps,
+        "timed_region_s": wall,
+        "call_ms": {"min": min(call_ms), "median": statistics.median(call_ms), "max": max(call_ms)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        f, dt, what, threads = oracle_bwd_sample(w, q, k, v, do, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{what} ({dt:.1f} s, fp64 C gradient oracle, {threads} threads)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,12 +559,15 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.pass_ == "bwd":
+        return run_ours_bwd(args, w)
     return run_ours(args, w)
 
 

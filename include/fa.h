@@ -1,5 +1,6 @@
 /*
- * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 library: the forward
+ * pass (fa_fwd, fa_fwd_ex) and its gradients (fa_bwd).
  *
  * The operation (per batch b, query head h, query row i):
  *
@@ -128,6 +129,45 @@ void fa_set_timeout_cycles(long long cycles);
  * do not depend on it.
  */
 void fa_set_max_ctas(int n);
+
+/*
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
+ * B * H_q * qL query rows: one fp32 D_i = rowsum(O_i * dO_i) per row, rounded
+ * up to 256 bytes.  Returns -1 for non-positive sizes.
+ */
+long long fa_bwd_workspace_bytes(int B, int H_q, int qL);
+
+/*
+ * fa_bwd -- gradients of the forward pass (FlashAttention-2 backward).
+ *
+ * Given dout = dLoss/dO, computes (kvh = h / (H_q / H_kv))
+ *   P_ij  = exp(scale * q_i . k_j - L_i)        causal keys j > i excluded
+ *   D_i   = rowsum(O_i * dO_i)
+ *   dS_ij = P_ij * (dO_i . v_j - D_i)
+ *   dq[b,h,i,:]   = scale * sum_j dS_ij k[b,kvh,j,:]
+ *   dk[b,kvh,j,:] = scale * sum over the group's heads h and rows i of dS_ij q[b,h,i,:]
+ *   dv[b,kvh,j,:] =         sum over the group's heads h and rows i of P_ij dout[b,h,i,:]
+ * Defined by forge "flash_attention_mma.metal", section "backward (MMA)"
+ * (dQ query-parallel; dK/dV key-parallel on transposed products, summed over
+ * the query heads sharing a K/V head, no atomics) and mlx-native
+ * "ops/flash_attn_train.rs", section "Phase 2 -- FA-2 backward kernel (dQ,
+ * dK, dV)" (the D = rowsum(O * dO) pre-pass and the buffer shapes).
+ *
+ * Arguments: q, o, dout, dq [B,H_q,qL,D]; k, v, dk, dv [B,H_kv,kL,D]; all
+ * contiguous bf16 (dtype must be FA_DTYPE_BF16), 16-byte aligned.  lse
+ * [B,H_q,qL] fp32 is the forward's L (natural log; -inf rows get zero
+ * gradients).  o is the forward's output.  workspace: caller-owned device
+ * memory of at least fa_bwd_workspace_bytes(B, H_q, qL) bytes, 16-byte
+ * aligned; its contents on entry do not matter and are clobbered.  D must be
+ * 64 or 128 (else FA_ERR_UNSUPPORTED); no mask (masked training is not
+ * supported by this entry point).  dq, dk, dv are written in full (rows no
+ * query or key reaches get zeros) and must not overlap any input or each
+ * other.  Asynchronous on `stream`: three kernel launches (D pre-pass, dK/dV,
+ * dQ); validation and errors as for fa_fwd.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
+           int qL, int kL, int D, float scale, int causal, int dtype, void* stream);
 
 /* ABI version: major * 100 + minor. */
 int fa_version(void);

@@ -24,13 +24,13 @@ def fa():
 
 def _declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|void|long long|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
-        ["fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_max_ctas", "fa_set_timeout_cycles",
-         "fa_version"])
+        ["fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_sync_status",
+         "fa_set_max_ctas", "fa_set_timeout_cycles", "fa_version"])
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -60,7 +60,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 101
+    assert fa.fa_version() == 102
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -129,6 +129,38 @@ def test_error_message_cleared_on_success_path(fa):
     assert fa.fa_last_error()
     _call(fa, q=None)
     assert "non-NULL" in fa.fa_last_error()
+
+
+def _bwd_call(fa, **kw):
+    a = dict(q=P, k=P, v=P, o=P, dout=P, lse=P, dq=P, dk=P, dv=P, ws=P, ws_bytes=1 << 20, B=1, H_q=2, H_kv=2,
+             qL=128, kL=128, D=128, scale=0.125, causal=1, dtype=1, stream=None)
+    a.update(kw)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], a["ws"],
+                     a["ws_bytes"], a["B"], a["H_q"], a["H_kv"], a["qL"], a["kL"], a["D"], a["scale"], a["causal"],
+                     a["dtype"], a["stream"])
+
+
+def test_bwd_workspace_size(fa):
+    assert fa.fa_bwd_workspace_bytes(2, 32, 4096) == 2 * 32 * 4096 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, 3) == 256
+    assert fa.fa_bwd_workspace_bytes(0, 1, 3) == -1
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(dout=None), 1, "non-NULL"),
+    (dict(ws=None), 1, "non-NULL"),
+    (dict(H_q=6, H_kv=4), 1, "divisible"),
+    (dict(kL=0), 1, "> 0"),
+    (dict(scale=float("nan")), 1, "finite"),
+    (dict(dtype=0), 2, "bf16"),
+    (dict(dtype=5), 1, "dtype"),
+    (dict(D=256), 2, "head dim"),
+    (dict(ws_bytes=100), 1, "workspace"),
+    (dict(dk=P + 4), 3, "16-byte"),
+])
+def test_bwd_validation_rejects(fa, kw, status, needle):
+    assert _bwd_call(fa, **kw) == status
+    assert needle in fa.fa_last_error()
 
 
 def test_product_never_imports_the_oracle():

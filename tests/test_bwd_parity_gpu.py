@@ -1,0 +1,100 @@
+"""Backward parity on the GPU: dQ, dK, dV from the C ABI against the fp64
+gradient oracle, element by element.
+
+The GPU backward consumes what the GPU forward produced (O in bf16, L in
+fp32), as a training step would.  Tolerance (bf16 I/O): every gradient
+element within 2e-2 of the oracle's, measured relative to the largest
+|oracle| entry of that tensor, and cosine similarity >= 0.999.  The bound
+follows the arithmetic: P and dS are rounded to bf16 (relative error <= 2^-9
+each) before the dV, dK and dQ products, the inputs and the stored results
+are bf16, and accumulation is fp32; the resulting error is a few 2^-9 of the
+tensor's scale, well inside 2e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import fp32_scale
+
+pytestmark = pytest.mark.gpu
+
+S = W.small_case
+CASES = [
+    S("bwd_d128_plain", 1, 2, 2, 256, 256, 128, "bf16", seed=31),
+    S("bwd_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "bf16", causal=True, seed=32),
+    S("bwd_d64_causal_ragged", 2, 2, 1, 200, 200, 64, "bf16", causal=True, seed=33),
+    S("bwd_d128_causal_q_longer", 1, 2, 2, 300, 170, 128, "bf16", causal=True, seed=34),
+    S("bwd_d128_causal_k_longer", 1, 2, 1, 150, 420, 128, "bf16", causal=True, seed=35),
+    S("bwd_d64_plain_long_kv", 1, 2, 2, 130, 600, 64, "bf16", seed=36),
+    S("bwd_d64_tiny", 1, 1, 1, 5, 3, 64, "bf16", causal=True, seed=37),
+    S("bwd_d128_gqa8", 1, 8, 1, 256, 256, 128, "bf16", causal=True, seed=38),
+]
+
+REL_TOL = 2e-2
+COS_MIN = 0.999
+
+
+def _run(w):
+    import attention_forward_08_gb300 as fa
+    q, k, v = W.make_qkv(w)
+    do = W.make_dout(w)
+    dev = "cuda:0"
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal)
+    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, scale=w.sm_scale, causal=w.causal)
+    assert fa.fa_sync_status(None) == fa.fa.FA_OK, fa.fa_last_error()
+    return (q, k, v, do), (dq, dk, dv)
+
+
+def _compare(name, got, ref):
+    got = got.double().cpu().numpy()
+    assert np.all(np.isfinite(got)), f"{name}: non-finite gradient"
+    scale = max(np.abs(ref).max(), 1e-30)
+    err = np.abs(got - ref).max() / scale
+    a, b = got.ravel(), ref.ravel()
+    cos = float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+    assert err <= REL_TOL, f"{name}: max|d| / max|ref| = {err:.3e} > {REL_TOL} (cos {cos:.6f})"
+    assert cos >= COS_MIN, f"{name}: cosine {cos:.6f} < {COS_MIN}"
+    return err, cos
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_bwd_elementwise(w):
+    (q, k, v, do), (dq, dk, dv) = _run(w)
+    rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                      do.double().numpy(), fp32_scale(w), causal=w.causal)
+    _compare(f"{w.name} dQ", dq, rq)
+    _compare(f"{w.name} dK", dk, rk)
+    _compare(f"{w.name} dV", dv, rv)
+    if w.causal and w.kL > w.qL:
+        # keys no query reaches get exactly zero gradient
+        assert torch.count_nonzero(dk[:, :, w.qL:]).item() == 0
+        assert torch.count_nonzero(dv[:, :, w.qL:]).item() == 0
+
+
+def test_bwd_deterministic():
+    w = CASES[1]
+    _, a = _run(w)
+    _, b = _run(w)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y), "two identical backward calls differ"
+
+
+def test_bwd_gqa_sums_group_heads():
+    """dK, dV of a GQA problem equal the per-head MHA gradients (K/V repeated) summed over each group."""
+    import attention_forward_08_gb300 as fa
+    w = S("bwd_gqa_vs_mha", 1, 4, 1, 256, 256, 128, "bf16", causal=True, seed=39)
+    (q, k, v, do), (dq, dk, dv) = _run(w)
+    dev = "cuda:0"
+    kr, vr = k.repeat_interleave(4, dim=1).to(dev), v.repeat_interleave(4, dim=1).to(dev)
+    qd, dod = q.to(dev), do.to(dev)
+    o, lse = fa.attention(qd, kr, vr, scale=w.sm_scale, causal=True)
+    dq2, dk2, dv2 = fa.attention_bwd(qd, kr, vr, o, dod, lse, scale=w.sm_scale, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2)
+    for g, g2 in ((dk, dk2), (dv, dv2)):
+        s = g2.float().sum(dim=1, keepdim=True)
+        err = (g.float() - s).abs().max().item() / max(s.abs().max().item(), 1e-30)
+        assert err < 2e-2, err

@@ -10,6 +10,7 @@ the workload's I/O dtype.  Masks use their own generator (``mask_seed``):
   additive  -- N(0, 1) cast to the I/O dtype, then Bernoulli(0.1) entries set
                to -inf, with the diagonal left finite so no row is empty;
   bool      -- Bernoulli(0.9) keep, with the diagonal forced to keep.
+Backward runs draw the upstream gradient dO as N(0, 1) from seed + 500.
 """
 from __future__ import annotations
 
@@ -86,6 +87,13 @@ def make_qkv(w: Workload):
     v = torch.randn(w.B, w.H_kv, w.kL, w.D, generator=g, dtype=torch.float32)
     dt = w.torch_dtype
     return q.to(dt), k.to(dt), v.to(dt)
+
+
+def make_dout(w: Workload):
+    """The upstream gradient dO [B,H_q,qL,D] for backward runs: N(0, 1) from seed + 500, I/O dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 500)
+    return torch.randn(w.B, w.H_q, w.qL, w.D, generator=g, dtype=torch.float32).to(w.torch_dtype)
 
 
 def make_mask(w: Workload):
