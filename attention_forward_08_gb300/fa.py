@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED
                 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_set_max_ctas",
-            "fa_bwd_workspace_bytes", "fa_bwd", "fa_version")
+            "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_noalloc", "fa_version")
 
 
 class FaError(RuntimeError):
@@ -84,6 +84,9 @@ def load_library(path: str = LIB_PATH):
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_bwd_noalloc.restype = ctypes.c_int
+    lib.fa_bwd_noalloc.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + \
+        [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     _lib = lib
     return lib
 
@@ -135,6 +138,12 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q
     """``fa_bwd`` of include/fa.h; pointers are ints (device addresses). Returns the status."""
     return load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes), B, H_q, H_kv,
                                   qL, kL, D, float(scale), int(causal), int(dtype), stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, causal, dtype, stream):
+    """``fa_bwd_noalloc`` of include/fa.h (built-in scratch, no workspace). Returns the status."""
+    return load_library().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D,
+                                          float(scale), int(causal), int(dtype), stream)
 
 
 # ----------------------------------------------------------------- torch convenience layer

@@ -169,6 +169,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
            int qL, int kL, int D, float scale, int causal, int dtype, void* stream);
 
+/*
+ * fa_bwd_noalloc -- fa_bwd without a workspace argument (no counterpart on the
+ * pages; a convenience of this library).  The D vector lives in a device array
+ * compiled into the library, sized for B * H_q * qL <= 2^21 query rows (8 MiB
+ * of fp32); larger problems return FA_ERR_UNSUPPORTED with a message, before
+ * anything is launched.  Nothing is allocated: the array's address is looked
+ * up once per device.  The array is fully written before it is read, so it
+ * needs no clearing.  All calls on a device share that one array: calls that
+ * overlap in time (on different streams or host threads) race and produce
+ * wrong gradients.  Arguments, results and errors otherwise as fa_bwd.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int qL, int kL, int D, float scale,
+                   int causal, int dtype, void* stream);
+
 /* ABI version: major * 100 + minor. */
 int fa_version(void);
 

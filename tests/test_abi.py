@@ -29,7 +29,8 @@ def _declared_functions():
 
 def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
-        ["fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_sync_status",
+        ["fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc", "fa_last_error",
+         "fa_sync_status",
          "fa_set_max_ctas", "fa_set_timeout_cycles", "fa_version"])
 
 
