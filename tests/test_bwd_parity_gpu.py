@@ -55,6 +55,7 @@ def _compare(name, got, ref):
     err = np.abs(got - ref).max() / scale
     a, b = got.ravel(), ref.ravel()
     cos = float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+    print(f"{name}: max|d| / max|ref| = {err:.3e}, cos = {cos:.7f}")
     assert err <= REL_TOL, f"{name}: max|d| / max|ref| = {err:.3e} > {REL_TOL} (cos {cos:.6f})"
     assert cos >= COS_MIN, f"{name}: cosine {cos:.6f} < {COS_MIN}"
     return err, cos
