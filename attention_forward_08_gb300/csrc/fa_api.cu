@@ -104,8 +104,8 @@ int validate(const fa_fwd_args* a) {
     set_error("H_q (%d) must be divisible by H_kv (%d)", a->H_q, a->H_kv);
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (a->dtype != FA_DTYPE_F32 && a->dtype != FA_DTYPE_BF16) {
-    set_error("dtype %d is not FA_DTYPE_F32 (0) or FA_DTYPE_BF16 (1)", a->dtype);
+  if (a->dtype != FA_DTYPE_F32 && a->dtype != FA_DTYPE_BF16 && a->dtype != FA_DTYPE_F16) {
+    set_error("dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)", a->dtype);
     return FA_ERR_INVALID_ARGUMENT;
   }
   if (a->mask_kind < FA_MASK_NONE || a->mask_kind > FA_MASK_ADDITIVE) {
@@ -248,11 +248,16 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     la.max_ctas = g_max_ctas;
   }
 
-  const bool f32 = a->dtype == FA_DTYPE_F32;
-  switch (a->D) {
-    case 64: rc = f32 ? launch_f32_d64(la) : launch_bf16_d64(la); break;
-    case 128: rc = f32 ? launch_f32_d128(la) : launch_bf16_d128(la); break;
-    default: rc = f32 ? launch_f32_d256(la) : launch_bf16_d256(la); break;
+  switch (a->dtype) {
+    case FA_DTYPE_F32:
+      rc = a->D == 64 ? launch_f32_d64(la) : a->D == 128 ? launch_f32_d128(la) : launch_f32_d256(la);
+      break;
+    case FA_DTYPE_F16:
+      rc = a->D == 64 ? launch_f16_d64(la) : a->D == 128 ? launch_f16_d128(la) : launch_f16_d256(la);
+      break;
+    default:
+      rc = a->D == 64 ? launch_bf16_d64(la) : a->D == 128 ? launch_bf16_d128(la) : launch_bf16_d256(la);
+      break;
   }
   return rc;
 }
@@ -366,10 +371,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     return FA_ERR_INVALID_ARGUMENT;
   }
   if (dtype != FA_DTYPE_BF16) {
-    set_error(dtype == FA_DTYPE_F32 ? "the backward pass supports bf16 I/O only"
-                                    : "dtype %d is not FA_DTYPE_F32 (0) or FA_DTYPE_BF16 (1)",
+    const bool known = dtype == FA_DTYPE_F32 || dtype == FA_DTYPE_F16;
+    set_error(known ? "the backward pass supports bf16 I/O only"
+                    : "dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)",
               dtype);
-    return dtype == FA_DTYPE_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
+    return known ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
   }
   if (D != 64 && D != 128) {
     set_error("head dim D = %d is not supported by the backward pass (64 or 128)", D);

@@ -44,10 +44,10 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   const long long qst[3] = {(long long)a.Hq * a.qL * kD, (long long)a.qL * kD, kD};
   const long long kst[3] = {(long long)a.Hkv * a.kL * kD, (long long)a.kL * kD, kD};
   CUtensorMap tq, tk, tv, tdo;
-  if (!encode_bhsd(&tq, false, a.q, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tdo, false, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tk, false, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tv, false, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
 
   BwdParams p;
   p.B = a.B;

@@ -66,9 +66,15 @@ constexpr float kRescaleThreshold = 8.0f;
 // lets TMEM or shared memory go while the hardware still writes to them.
 constexpr long long kDrainCycles = 1LL << 33;
 
-template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_, int kVTStages_ = 0>
+template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_, int kVTStages_ = 0,
+          bool kF16_ = false>
 struct Cfg {
   static constexpr bool kTf32 = kTf32_;
+  // 16-bit I/O is bf16 unless kF16 (fp16): same kernel, other operand format.
+  static constexpr bool kF16 = kF16_;
+  static constexpr uint32_t kFmt = kTf32 ? kFmtTf32 : (kF16 ? kFmtF16 : kFmtBf16);
+  static constexpr CUtensorMapDataType kTmaType =
+      kTf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : (kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   static constexpr int kD = kD_;
   static constexpr int kEsz = kTf32 ? 4 : 2;          // bytes per stored element
   static constexpr int kChunk = 128 / kEsz;           // elements per 128-byte swizzle row
@@ -134,6 +140,7 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static_assert(kKStages >= 1 && kVStages >= 1 && kKStages <= 4 && kVStages <= 4, "ring size");
   static_assert(kTf32 ? (kVTStages >= 1 && kVTStages <= 4) : kVTStages == 0, "V^T ring is for TF32 only");
+  static_assert(!(kTf32 && kF16), "fp16 I/O uses the 16-bit path");
 };
 
 // Shared-memory control block (after the tiles).
@@ -156,6 +163,15 @@ struct Ctrl {
   int abort;
   uint64_t turn_bar[2];           // two issuers: issuer i may issue its next MMA group
 };
+
+// Two fp32 values -> the 16-bit I/O format's packed pair (`lo` in bits 0-15).
+template <class C>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (C::kF16)
+    return pack_f16x2(lo, hi);
+  else
+    return pack_bf16x2(lo, hi);
+}
 
 // Bounded wait: true once the phase of `parity` completed; false after the
 // CTA-wide abort flag is raised or `timeout` cycles pass (then it raises the
@@ -295,14 +311,14 @@ __device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, in
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const uint32_t bits = (e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16);
-            s[v * 8 + e] = fmaf(__uint_as_float(bits), kLog2e, s[v * 8 + e]);
+            const float mv = half_bits_to_f32<C::kF16>((e & 1) ? (ws[e >> 1] >> 16) : ws[e >> 1]);
+            s[v * 8 + e] = fmaf(mv, kLog2e, s[v * 8 + e]);
           }
         }
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (k0 + e < kL) s[e] = fmaf(__uint_as_float((uint32_t)__ldg(mrow + k0 + e) << 16), kLog2e, s[e]);
+          if (k0 + e < kL) s[e] = fmaf(half_bits_to_f32<C::kF16>(__ldg(mrow + k0 + e)), kLog2e, s[e]);
       }
     }
   }
@@ -331,8 +347,8 @@ __device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint32_t bits = (e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16);
-        s[c * 8 + e] = fmaf(__uint_as_float(bits), kLog2e, s[c * 8 + e]);
+        const float mv = half_bits_to_f32<C::kF16>((e & 1) ? (ws[e >> 1] >> 16) : ws[e >> 1]);
+        s[c * 8 + e] = fmaf(mv, kLog2e, s[c * 8 + e]);
       }
     }
   }
@@ -408,7 +424,7 @@ __device__ __forceinline__ void p_pass(const float (&s)[C::kBN], float sl, float
         pk[2 * e] = to_tf32(p0);
         pk[2 * e + 1] = to_tf32(p1);
       } else {
-        pk[e] = pack_bf16x2(p0, p1);
+        pk[e] = pack16x2<C>(p0, p1);
       }
     }
     if constexpr (C::kTf32)
@@ -690,8 +706,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int t_begin = C::kIssuers == 1 ? 0 : issuer;
     const int t_end = C::kIssuers == 1 ? C::kNQT : issuer + 1;
     if (lane == 0) {
-      constexpr uint32_t idS = make_idesc(C::kTf32, 128, C::kBN, false, false);
-      constexpr uint32_t idPV = make_idesc(C::kTf32, 128, C::kD, false, !C::kTf32);
+      constexpr uint32_t idS = make_idesc_fmt(C::kFmt, 128, C::kBN, false, false);
+      constexpr uint32_t idPV = make_idesc_fmt(C::kFmt, 128, C::kD, false, !C::kTf32);
       // Descriptor halves of the first K-step of each operand ring; later
       // K-steps and slots only add to the start address in the low half.
       const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -1065,7 +1081,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 float a0, a1;
                 fmul2(a0, a1, __uint_as_float(rr[8 * u4 + 2 * e]), __uint_as_float(rr[8 * u4 + 2 * e + 1]), inv_l,
                       inv_l);
-                pk[e] = pack_bf16x2(a0, a1);
+                pk[e] = pack16x2<C>(a0, a1);
               }
               dst[u4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }

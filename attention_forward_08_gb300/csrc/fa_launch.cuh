@@ -40,9 +40,9 @@ void set_error(const char* fmt, ...);
 // A [B, H, rows, D] view with element strides {sb, sh, sr} and unit inner
 // stride, tiled as {chunk elements (128 bytes), box_rows, 1, 1} with 128-byte
 // swizzle.  Rows past `rows` read as zero and are clipped on store.
-inline bool encode_bhsd(CUtensorMap* map, bool f32, const void* ptr, int B, int H, int rows, int D,
+inline bool encode_bhsd(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, int B, int H, int rows, int D,
                         const long long* st, int chunk, int box_rows) {
-  const int esz = f32 ? 4 : 2;
+  const int esz = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
   // A stride of an extent-1 dimension is never used; give it a legal value.
   auto legal = [](long long bytes, int extent) -> cuuint64_t {
@@ -56,7 +56,7 @@ inline bool encode_bhsd(CUtensorMap* map, bool f32, const void* ptr, int B, int 
     set_error("cuTensorMapEncodeTiled is not available from the CUDA driver");
     return false;
   }
-  CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+  CUresult r = enc(map, dt, 4,
                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -69,9 +69,9 @@ inline bool encode_bhsd(CUtensorMap* map, bool f32, const void* ptr, int B, int 
 template <class C>
 int launch_fa_fwd(const LaunchArgs& a) {
   CUtensorMap tq, tk, tv, tm;
-  if (!encode_bhsd(&tq, C::kTf32, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
-  if (!encode_bhsd(&tk, C::kTf32, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
-  if (!encode_bhsd(&tv, C::kTf32, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
+  if (!encode_bhsd(&tq, C::kTmaType, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
+  if (!encode_bhsd(&tk, C::kTmaType, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
+  if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
   // Mask tiles (128-byte column blocks x kBM rows, 128-byte swizzle) for the
   // L2 prefetch and the shared-memory mask path, when the mask's layout suits
   // TMA (aligned base, 16-byte multiple strides, no stride-0 broadcast).
@@ -89,7 +89,7 @@ int launch_fa_fwd(const LaunchArgs& a) {
       cuuint32_t box[4] = {(cuuint32_t)(128 / mesz), (cuuint32_t)C::kBM, 1, 1};
       cuuint32_t estr[4] = {1, 1, 1, 1};
       const CUtensorMapDataType dt = a.mask_kind == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                     : (C::kTf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+                                     : C::kTmaType;
       EncodeTiledFn enc = get_encode_tiled();
       if (enc && (C::kBN * mesz) % 128 == 0 &&
           enc(&tm, dt, 4, const_cast<void*>(a.mask), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -181,6 +181,10 @@ using CfgBf16D256 = Cfg<false, 256, 1, 128, 1, 1>;  // smem 192 KB, TMEM 512 (P 
 using CfgF32D64   = Cfg<true, 64,   2, 64, 2, 2, 2>;  // smem 160 KB, TMEM 256
 using CfgF32D128  = Cfg<true, 128,  1, 64, 2, 1, 2>;  // smem 224 KB, TMEM 320
 using CfgF32D256  = Cfg<true, 256,  1, 32, 1, 1, 1>;  // smem 224 KB, TMEM 352
+// fp16 I/O: the bf16 plans with the f16 operand format.
+using CfgF16D64   = Cfg<false, 64,  2, 128, 4, 4, 0, true>;
+using CfgF16D128  = Cfg<false, 128, 2, 128, 2, 2, 0, true>;
+using CfgF16D256  = Cfg<false, 256, 1, 128, 1, 1, 0, true>;
 
 int launch_bf16_d64(const LaunchArgs& a);
 int launch_bf16_d128(const LaunchArgs& a);
@@ -188,5 +192,8 @@ int launch_bf16_d256(const LaunchArgs& a);
 int launch_f32_d64(const LaunchArgs& a);
 int launch_f32_d128(const LaunchArgs& a);
 int launch_f32_d256(const LaunchArgs& a);
+int launch_f16_d64(const LaunchArgs& a);
+int launch_f16_d128(const LaunchArgs& a);
+int launch_f16_d256(const LaunchArgs& a);
 
 }  // namespace fa

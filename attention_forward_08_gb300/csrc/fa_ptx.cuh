@@ -224,11 +224,17 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 // Instruction descriptor, dense MMA with fp32 accumulation.
 //   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (f16 kind:
-//   1 = bf16; tf32 kind: 2 = tf32); 15 A major, 16 B major (0 = K-major,
+//   0 = f16, 1 = bf16; tf32 kind: 2 = tf32); 15 A major, 16 B major (0 = K-major,
 //   1 = MN-major); 17-22 N >> 3; 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc_fmt(uint32_t fmt, int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// A/B operand format codes: kind::f16 takes 0 = f16 or 1 = bf16 (the same for A
+// and B), kind::tf32 takes 2.
+constexpr uint32_t kFmtF16 = 0, kFmtBf16 = 1, kFmtTf32 = 2;
 __host__ __device__ constexpr uint32_t make_idesc(bool tf32, int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | ((tf32 ? 2u : 1u) << 7) | ((tf32 ? 2u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  return make_idesc_fmt(tf32 ? kFmtTf32 : kFmtBf16, M, N, a_mn_major, b_mn_major);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes
@@ -342,6 +348,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Two fp32 values -> packed f16x2, round to nearest even; `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 16-bit pattern (low half of `bits`) -> fp32: f16 (exact conversion) or bf16.
+template <bool kF16>
+__device__ __forceinline__ float half_bits_to_f32(uint32_t bits) {
+  if constexpr (kF16) {
+    float f;
+    const unsigned short h = (unsigned short)(bits & 0xFFFFu);
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+    return f;
+  } else {
+    return __uint_as_float(bits << 16);
+  }
 }
 // fp32 -> tf32 bit pattern, round to nearest, ties away from zero.
 __device__ __forceinline__ uint32_t to_tf32(float x) {

@@ -19,7 +19,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
 
-FA_DTYPE_F32, FA_DTYPE_BF16 = 0, 1
+FA_DTYPE_F32, FA_DTYPE_BF16, FA_DTYPE_F16 = 0, 1, 2
 FA_MASK_NONE, FA_MASK_BOOL, FA_MASK_ADDITIVE = 0, 1, 2
 FA_OK, FA_ERR_INVALID_ARGUMENT, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(6)
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
@@ -174,10 +174,12 @@ def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind
         raise ValueError(f"lse must be a contiguous fp32 [B, H_q, qL] = {(B, H_q, qL)} tensor")
     if q.dtype == torch.bfloat16:
         dtype = FA_DTYPE_BF16
+    elif q.dtype == torch.float16:
+        dtype = FA_DTYPE_F16
     elif q.dtype == torch.float32:
         dtype = FA_DTYPE_F32
     else:
-        raise ValueError(f"q dtype {q.dtype} is not bfloat16 or float32")
+        raise ValueError(f"q dtype {q.dtype} is not bfloat16, float16 or float32")
     for name, t in (("k", k), ("v", v), ("o", o)):
         if t.dtype != q.dtype:
             raise ValueError(f"{name} dtype {t.dtype} differs from q dtype {q.dtype}")

@@ -70,11 +70,11 @@ def load_peaks():
 def peak_for(w: workloads.Workload, peaks: dict) -> float:
     """Dense tensor peak for the workload's MMA kind (TF32 = bf16 x 1/2, the nominal ratio)."""
     bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    return bf16 if w.dtype == "bf16" else bf16 * 0.5
+    return bf16 if w.dtype in ("bf16", "f16") else bf16 * 0.5
 
 
 def algorithmic_bytes(w: workloads.Workload) -> int:
-    esz = 2 if w.dtype == "bf16" else 4
+    esz = 4 if w.dtype == "f32" else 2
     qo = 2 * w.B * w.H_q * w.qL * w.D * esz
     kv = 2 * w.B * w.H_kv * w.kL * w.D * esz
     lse = 4 * w.B * w.H_q * w.qL
@@ -377,7 +377,8 @@ def run_ours(args, w):
         "config": config_of(w, argparse.Namespace(gpus=world)),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": (f"{peak_src} bf16 dense (burst)" if w.dtype == "bf16"
+                     "peak_source": (f"{peak_src} bf16 dense (burst; f16 runs at the same rate)"
+                                     if w.dtype in ("bf16", "f16")
                                      else f"{peak_src} bf16 dense (burst) x 0.5 nominal tf32 ratio"),
                      "algorithmic_bytes": algorithmic_bytes(w),
                      "hbm_gbs": algorithmic_bytes(w) / (mean_ms * 1e-3) / 1e9},

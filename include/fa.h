@@ -42,7 +42,8 @@ extern "C" {
 
 typedef enum {
   FA_DTYPE_F32 = 0,  /* fp32 I/O, tensor-core products in TF32 (inputs rounded to nearest) */
-  FA_DTYPE_BF16 = 1  /* bf16 I/O, fp32 accumulation, P rounded to bf16 before P.V */
+  FA_DTYPE_BF16 = 1, /* bf16 I/O, fp32 accumulation, P rounded to bf16 before P.V */
+  FA_DTYPE_F16 = 2   /* fp16 I/O, fp32 accumulation, P rounded to fp16 before P.V (forward only) */
 } fa_dtype;
 
 typedef enum {

@@ -83,6 +83,7 @@ def _call(fa, **kw):
     (dict(kL=0), 1, "> 0"),
     (dict(H_q=6, H_kv=4), 1, "divisible"),
     (dict(dtype=7), 1, "dtype"),
+    (dict(dtype=3), 1, "dtype"),
     (dict(mask_kind=3, mask=P), 1, "mask_kind"),
     (dict(mask_kind=1, mask=None), 1, "mask must be non-NULL"),
     (dict(mask_kind=0, mask=P), 1, "mask must be non-NULL"),
@@ -154,6 +155,7 @@ def test_bwd_workspace_size(fa):
     (dict(kL=0), 1, "> 0"),
     (dict(scale=float("nan")), 1, "finite"),
     (dict(dtype=0), 2, "bf16"),
+    (dict(dtype=2), 2, "bf16"),
     (dict(dtype=5), 1, "dtype"),
     (dict(D=256), 2, "head dim"),
     (dict(ws_bytes=100), 1, "workspace"),

@@ -42,6 +42,10 @@ SMALL = [
     S("bf16_d64_tiny_ragged", 1, 1, 1, 5, 3, 64, "bf16", causal=True),
     S("f32_d64_tiny", 1, 1, 1, 3, 7, 64, "f32"),
     S("bf16_d128_gqa8", 1, 8, 1, 256, 256, 128, "bf16", causal=True),
+    S("f16_d128_causal_gqa", 1, 4, 2, 512, 512, 128, "f16", causal=True),
+    S("f16_d64_additive_causal_ragged", 1, 2, 2, 257, 257, 64, "f16", causal=True, mask_kind=W.MASK_ADDITIVE),
+    S("f16_d256_bool_ragged", 1, 2, 2, 200, 200, 256, "f16", mask_kind=W.MASK_BOOL),
+    S("f16_d256_additive_tma_mask", 1, 2, 2, 256, 256, 256, "f16", mask_kind=W.MASK_ADDITIVE),
 ]
 
 

@@ -31,7 +31,7 @@ class Workload:
     qL: int
     kL: int
     D: int
-    dtype: str            # "bf16" or "f32"
+    dtype: str            # "bf16", "f16" or "f32"
     causal: bool = False
     mask_kind: int = MASK_NONE
     layout: str = "bhsd"  # "bhsd", or "dit": O written token-major [seq, H*D]
@@ -45,7 +45,7 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return {"bf16": torch.bfloat16, "f16": torch.float16}.get(self.dtype, torch.float32)
 
     def flops(self) -> float:
         """Algorithmic FLOP: 4*B*H_q*qL*kL*D, halved when causal."""
@@ -76,6 +76,13 @@ WORKLOADS = {
 }
 
 BENCH_WORKLOAD = "bf16_gqa_causal_b2_hq32_hkv8_l4096_d128"
+
+# Beyond the pages' workloads: the bench workload with fp16 I/O (same seeds).
+EXTRA_WORKLOADS = {
+    "f16_gqa_causal_b2_hq32_hkv8_l4096_d128": Workload(
+        "f16_gqa_causal_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "f16", causal=True, seed=1002),
+}
+WORKLOADS.update(EXTRA_WORKLOADS)
 
 
 def make_qkv(w: Workload):
