@@ -55,11 +55,11 @@ def build_bwd(mutant: int = 0, out_path: str | None = None) -> str:
 
 
 def _bind(lib):
-    f = lib.oracle_attention
+    f = lib.oracle_attention_ex
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 2 + \
-        [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int,
-                                   ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int]
+        [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_longlong, ctypes.c_double,
+                                   ctypes.c_longlong, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int]
     lib.oracle_mutant_id.restype = ctypes.c_int
     return lib
 
@@ -146,13 +146,16 @@ def _f64(a) -> np.ndarray:
 
 def attention(q, k, v, scale: float, causal: bool = False, mask=None,
               mask_kind: int = 0, rows=None, n_threads: int | None = None,
-              lib=None):
+              lib=None, window: int = 0, softcap: float = 0.0, q_offset: int = 0):
     """O and L of softmax(scale * q k^T + mask) v in fp64.
 
     q: [B, H_q, qL, D]; k, v: [B, H_kv, kL, D] (any real dtype; widened to
     fp64 exactly).  mask: None, or [B, H_q, qL, kL] -- bool/uint8 with
     nonzero = keep (mask_kind 1) or additive real values (mask_kind 2).
     ``scale`` is used as given (pass the fp32-rounded value the GPU sees).
+    window > 0 keeps keys j > i + q_offset - window; softcap > 0 maps each
+    scaled score s to softcap * tanh(s / softcap) before the mask; q_offset
+    shifts the causal diagonal (j <= i + q_offset).
     rows: optional iterable of flat row indices (b*H_q + h)*qL + i.
     Returns (O, L): O [B,H_q,qL,D] and L [B,H_q,qL], or [n,D] and [n] for rows.
     """
@@ -185,10 +188,10 @@ def attention(q, k, v, scale: float, causal: bool = False, mask=None,
         rptr = None
     if n_threads is None:
         n_threads = os.cpu_count() or 1
-    rc = lib.oracle_attention(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr,
-                              int(mask_kind), o.ctypes.data, lse.ctypes.data,
-                              B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)),
-                              rptr, n, int(n_threads))
+    rc = lib.oracle_attention_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr,
+                                 int(mask_kind), o.ctypes.data, lse.ctypes.data,
+                                 B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)),
+                                 int(window), float(softcap), int(q_offset), rptr, n, int(n_threads))
     if rc != 0:
         raise ValueError("oracle_attention rejected its arguments")
     return o, lse

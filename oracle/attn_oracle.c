@@ -10,7 +10,9 @@
  *
  *   kvh      = h / (H_q / H_kv)                         GQA head map
  *   s_ij     = scale * sum_d q[b,h,i,d] * k[b,kvh,j,d]
- *   allowed  = (!causal || j <= i)                       causal, top-left aligned
+ *   softcap > 0:  s_ij = softcap * tanh(s_ij / softcap)  (before any mask)
+ *   allowed  = (!causal || j <= i + q_offset)            causal; q_offset 0 = top-left
+ *   window > 0:   allowed &= (j > i + q_offset - window)  sliding window of `window` keys
  *   bool mask:      allowed &= (mask[b,h,i,j] != 0)      nonzero = keep
  *   additive mask:  s_ij += mask[b,h,i,j];  allowed &= (s_ij != -inf)
  *   S_ij     = allowed ? s_ij : -inf                     (the full score row)
@@ -38,6 +40,9 @@
  * Readings where the pages are silent (each listed in the design notes):
  *  - a fully masked row has L = -inf (the empty logsumexp); forge writes 0.
  *  - the mask is added after scaling and is not itself scaled.
+ *  - window, softcap and q_offset: the pages only name the fields (forge's
+ *    `FlashParams.window`, 0 = off; mlx's `softcapping` and `ql_off`); the
+ *    definitions above are the plainest readings of those names.
  *
  * This is the definition written out row by row: the full score row S_i. is
  * materialised, then its max, its exp-sum, O and L.  No online softmax, no
@@ -64,6 +69,9 @@ typedef struct {
     long long B, Hq, Hkv, qL, kL, D;
     double scale;
     int causal;
+    long long window;            /* 0: off */
+    double softcap;              /* <= 0: off */
+    long long q_offset;
     const long long *rows;       /* optional list of flat rows ((b*Hq+h)*qL+i) */
     long long n_rows;
     long long row_begin, row_end;/* this worker's slice of [0, n_rows) */
@@ -104,11 +112,28 @@ static void oracle_row(const oracle_job *J, long long flat, long long out_index,
 #else
         double s = J->scale * dot;
 #endif
-#if ORACLE_MUTANT == 3
-        int allowed = !J->causal || j < i;        /* mistake: causal off by one */
+        if (J->softcap > 0.0) {
+#if ORACLE_MUTANT == 9
+            s = tanh(s / J->softcap);             /* mistake: cap not multiplied back */
 #else
-        int allowed = !J->causal || j <= i;
+            s = J->softcap * tanh(s / J->softcap);
 #endif
+        }
+        const long long diag = i + J->q_offset;   /* the key aligned with row i */
+#if ORACLE_MUTANT == 3
+        int allowed = !J->causal || j < diag;     /* mistake: causal off by one */
+#elif ORACLE_MUTANT == 10
+        int allowed = !J->causal || j <= i - J->q_offset;  /* mistake: offset sign */
+#else
+        int allowed = !J->causal || j <= diag;
+#endif
+        if (J->window > 0) {
+#if ORACLE_MUTANT == 11
+            allowed = allowed && (j >= diag - J->window);  /* mistake: window one key too wide */
+#else
+            allowed = allowed && (j > diag - J->window);
+#endif
+        }
         if (J->mask_kind == 1) {
             const uint8_t mv = ((const uint8_t *)J->mask)[((b * J->Hq + h) * qL + i) * kL + j];
 #if ORACLE_MUTANT == 7
@@ -169,7 +194,7 @@ static void *oracle_worker(void *arg)
 }
 
 /*
- * oracle_attention -- fp64 attention forward, O and L.
+ * oracle_attention_ex -- fp64 attention forward, O and L.
  *
  * q [B,Hq,qL,D], k and v [B,Hkv,kL,D], contiguous fp64 holding the exact
  * stored input values.  mask: NULL for mask_kind 0, else [B,Hq,qL,kL]
@@ -177,15 +202,18 @@ static void *oracle_worker(void *arg)
  * rows == NULL: every row is computed; o is [B*Hq*qL, D] and lse [B*Hq*qL].
  * rows != NULL: only the n_rows listed flat rows ((b*Hq + h)*qL + i) are
  * computed; o is [n_rows, D] and lse [n_rows], in list order.
+ * window (0 = off), softcap (<= 0 = off) and q_offset as in the header.
  * n_threads <= 0 means one thread.  Returns 0, or -1 on a bad argument.
  */
-int oracle_attention(const double *q, const double *k, const double *v,
-                     const void *mask, int mask_kind, double *o, double *lse,
-                     long long B, long long Hq, long long Hkv, long long qL,
-                     long long kL, long long D, double scale, int causal,
-                     const long long *rows, long long n_rows, int n_threads)
+int oracle_attention_ex(const double *q, const double *k, const double *v,
+                        const void *mask, int mask_kind, double *o, double *lse,
+                        long long B, long long Hq, long long Hkv, long long qL,
+                        long long kL, long long D, double scale, int causal,
+                        long long window, double softcap, long long q_offset,
+                        const long long *rows, long long n_rows, int n_threads)
 {
     if (!q || !k || !v || !o || !lse) return -1;
+    if (window < 0) return -1;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || qL <= 0 || kL <= 0 || D <= 0) return -1;
     if (Hq % Hkv != 0) return -1;
     if (mask_kind < 0 || mask_kind > 2) return -1;
@@ -213,6 +241,7 @@ int oracle_attention(const double *q, const double *k, const double *v,
         J->o = o; J->lse = lse;
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->qL = qL; J->kL = kL; J->D = D;
         J->scale = scale; J->causal = causal; J->rows = rows; J->n_rows = total;
+        J->window = window; J->softcap = softcap; J->q_offset = q_offset;
         J->row_begin = total * t / n_threads;
         J->row_end = total * (t + 1) / n_threads;
         J->scratch = scratch + (size_t)kL * (size_t)t;
@@ -229,6 +258,17 @@ int oracle_attention(const double *q, const double *k, const double *v,
 
     free(jobs); free(tids); free(scratch);
     return 0;
+}
+
+/* The plain definition: no window, no softcap, top-left causal. */
+int oracle_attention(const double *q, const double *k, const double *v,
+                     const void *mask, int mask_kind, double *o, double *lse,
+                     long long B, long long Hq, long long Hkv, long long qL,
+                     long long kL, long long D, double scale, int causal,
+                     const long long *rows, long long n_rows, int n_threads)
+{
+    return oracle_attention_ex(q, k, v, mask, mask_kind, o, lse, B, Hq, Hkv, qL, kL, D, scale, causal,
+                               0, 0.0, 0, rows, n_rows, n_threads);
 }
 
 /* Number of the planted mistake this build carries (0 for the real oracle). */

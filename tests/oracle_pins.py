@@ -11,9 +11,13 @@ disagrees with:
     and logsumexp),
   - invariants that hold exactly (key permutation, additive-mask shift,
     linearity in V, GQA == MHA with K/V repeated, mask-kind equivalences).
+  - for the sliding window, softcap and query offset: decimal brute force,
+    window of one key, equal scores in a window, bottom-right causal as the
+    suffix of the full causal problem, and a huge cap recovering plain scores.
 The pins are chosen so each planted mistake in the oracle (dropped scale,
 wrong GQA map, causal off by one, L without the max, transposed product,
-scaled mask, flipped bool polarity, missing division by l) fails one of them.
+scaled mask, flipped bool polarity, missing division by l, softcap not
+multiplied back, query-offset sign, window one key too wide) fails one.
 """
 from __future__ import annotations
 
@@ -209,7 +213,13 @@ def pin_golden_handworked(attn):
 
 # --------------------------------------------------------------------------- brute force
 
-def _decimal_attention(q, k, v, scale, causal, mask, mask_kind):
+def _decimal_tanh(x):
+    """tanh from its exponential definition, in the current Decimal context."""
+    e = (2 * x).exp()
+    return (e - 1) / (e + 1)
+
+
+def _decimal_attention(q, k, v, scale, causal, mask, mask_kind, window=0, softcap=0.0, q_offset=0):
     getcontext().prec = 50
     B, Hq, qL, D = q.shape
     Hkv, kL = k.shape[1], k.shape[2]
@@ -226,7 +236,12 @@ def _decimal_attention(q, k, v, scale, causal, mask, mask_kind):
                     dot = sum(Decimal(float(q[b, h, i, d])) * Decimal(float(k[b, kh, j, d]))
                               for d in range(D))
                     s = dscale * dot
-                    ok = (not causal) or j <= i
+                    if softcap > 0:
+                        cap = Decimal(float(softcap))
+                        s = cap * _decimal_tanh(s / cap)
+                    ok = (not causal) or j <= i + q_offset
+                    if window > 0:
+                        ok = ok and j > i + q_offset - window
                     if mask_kind == 1:
                         ok = ok and mask[b, h, i, j] != 0
                     elif mask_kind == 2:
@@ -247,6 +262,78 @@ def _decimal_attention(q, k, v, scale, causal, mask, mask_kind):
                     O[b, h, i, d] = float(sum(x * Decimal(float(v[b, kh, j, d])) for j, x in w) / l)
                 L[b, h, i] = float(m + l.ln())
     return O, L
+
+
+def pin_bruteforce_decimal_window_softcap_offset(attn):
+    """50-digit decimal brute force with a sliding window, a softcap and a query offset."""
+    r = _rng(20)
+    B, Hq, Hkv, qL, kL, D = 1, 2, 1, 5, 9, 3
+    q = 2.0 * r.standard_normal((B, Hq, qL, D))
+    k = 2.0 * r.standard_normal((B, Hkv, kL, D))
+    v = r.standard_normal((B, Hkv, kL, D))
+    amask = r.standard_normal((B, Hq, qL, kL))
+    for causal, window, softcap, q_offset, kind in ((True, 3, 0.0, 0, 0), (True, 2, 0.0, 4, 0), (False, 4, 0.0, 2, 0),
+                                                    (False, 0, 1.5, 0, 0), (True, 3, 2.0, 4, 2), (True, 0, 0.0, -2, 0)):
+        m = amask if kind == 2 else None
+        o, lse = attn(q, k, v, 0.7, causal=causal, mask=m, mask_kind=kind, window=window, softcap=softcap,
+                      q_offset=q_offset)
+        wo, wl = _decimal_attention(q, k, v, 0.7, causal, m, kind, window, softcap, q_offset)
+        what = f"causal={causal} window={window} softcap={softcap} q_offset={q_offset} kind={kind}"
+        _close(o, wo, what="decimal O " + what)
+        _close(lse, wl, what="decimal L " + what)
+
+
+def pin_window_of_one_key(attn):
+    """Causal with window 1: row i sees only key i + q_offset, so O_i = V[i + q_offset], L_i = its score."""
+    r = _rng(21)
+    B, Hq, Hkv, qL, kL, D = 1, 2, 2, 6, 9, 4
+    q, k, v = r.standard_normal((B, Hq, qL, D)), r.standard_normal((B, Hkv, kL, D)), r.standard_normal((B, Hkv, kL, D))
+    for q_offset in (0, 3):
+        o, lse = attn(q, k, v, 0.5, causal=True, window=1, q_offset=q_offset)
+        for h in range(Hq):
+            for i in range(qL):
+                j = i + q_offset
+                _close(o[0, h, i], v[0, h, j], what=f"window-1 O row {i}")
+                _close(lse[0, h, i], 0.5 * float(q[0, h, i] @ k[0, h, j]), what=f"window-1 L row {i}")
+
+
+def pin_window_equal_scores(attn):
+    """Q = 0, causal, window W: O_i = mean of V over keys (i + q_offset - W, i + q_offset], L_i = ln(count)."""
+    r = _rng(22)
+    B, Hq, Hkv, qL, kL, D = 1, 2, 1, 7, 10, 3
+    q = np.zeros((B, Hq, qL, D))
+    k, v = r.standard_normal((B, Hkv, kL, D)), r.standard_normal((B, Hkv, kL, D))
+    for W, q_offset in ((3, 0), (4, 3), (20, 2)):
+        o, lse = attn(q, k, v, 0.9, causal=True, window=W, q_offset=q_offset)
+        for i in range(qL):
+            hi = min(i + q_offset, kL - 1)
+            lo = max(0, i + q_offset - W + 1)
+            _close(o[0, 0, i], v[0, 0, lo:hi + 1].mean(axis=0), what=f"window {W} O row {i}")
+            _close(lse[0, 0, i], math.log(hi - lo + 1), what=f"window {W} L row {i}")
+
+
+def pin_q_offset_is_a_suffix(attn):
+    """Causal with q_offset = kL - qL (bottom-right) gives the last qL rows of the full causal problem."""
+    r = _rng(23)
+    B, Hq, Hkv, kL, D, qL = 1, 2, 1, 11, 4, 4
+    k, v = r.standard_normal((B, Hkv, kL, D)), r.standard_normal((B, Hkv, kL, D))
+    q_full = r.standard_normal((B, Hq, kL, D))
+    for window in (0, 5):
+        of, lf = attn(q_full, k, v, 0.6, causal=True, window=window)
+        o, lse = attn(q_full[:, :, kL - qL:], k, v, 0.6, causal=True, window=window, q_offset=kL - qL)
+        _close(o, of[:, :, kL - qL:], 0.0, "suffix O")
+        _close(lse, lf[:, :, kL - qL:], 0.0, "suffix L")
+
+
+def pin_softcap_large_cap(attn):
+    """softcap c -> infinity recovers the plain scores: c * tanh(s / c) = s - s^3 / (3 c^2) + ..."""
+    r = _rng(24)
+    B, Hq, Hkv, qL, kL, D = 1, 2, 2, 5, 8, 4
+    q, k, v = r.standard_normal((B, Hq, qL, D)), r.standard_normal((B, Hkv, kL, D)), r.standard_normal((B, Hkv, kL, D))
+    o0, l0 = attn(q, k, v, 0.5, causal=True)
+    o1, l1 = attn(q, k, v, 0.5, causal=True, softcap=1e6)
+    _close(o1, o0, 1e-9, "softcap 1e6 O")
+    _close(l1, l0, 1e-9, "softcap 1e6 L")
 
 
 def pin_bruteforce_decimal(attn):
@@ -411,5 +498,6 @@ ALL_PINS = [
     pin_one_hot_bool, pin_one_hot_additive, pin_causal_row0, pin_fully_masked_row,
     pin_large_margin, pin_golden_handworked, pin_bruteforce_decimal, pin_torch_sdpa,
     pin_key_permutation, pin_additive_shift, pin_linear_in_v, pin_gqa_equals_repeated_mha,
-    pin_mask_kind_equivalences, pin_rows_subset,
+    pin_mask_kind_equivalences, pin_rows_subset, pin_bruteforce_decimal_window_softcap_offset,
+    pin_window_of_one_key, pin_window_equal_scores, pin_q_offset_is_a_suffix, pin_softcap_large_cap,
 ]

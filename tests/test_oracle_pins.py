@@ -31,6 +31,9 @@ MUTANTS = {
     6: "mask scaled with the scores",
     7: "bool polarity flipped",
     8: "no division by l",
+    9: "softcap not multiplied back",
+    10: "query offset sign",
+    11: "window one key too wide",
 }
 
 
