@@ -120,6 +120,18 @@ int validate(const fa_fwd_args* a) {
     set_error("scale must be finite");
     return FA_ERR_INVALID_ARGUMENT;
   }
+  if (a->window < 0) {
+    set_error("window (%d) must be >= 0 (0 = no sliding window)", a->window);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->q_offset <= -(1 << 30) || a->q_offset >= (1 << 30)) {
+    set_error("q_offset (%d) must lie in (-2^30, 2^30)", a->q_offset);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (!std::isfinite(a->softcap) || a->softcap < 0.0f) {
+    set_error("softcap must be finite and >= 0 (0 = off)");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
   if (a->D != 64 && a->D != 128 && a->D != 256) {
     set_error("head dim D = %d is not supported (64, 128 or 256)", a->D);
     return FA_ERR_UNSUPPORTED;
@@ -225,6 +237,9 @@ int fa_fwd_ex(const fa_fwd_args* a) {
   la.scale = a->scale;
   la.causal = a->causal ? 1 : 0;
   la.mask_kind = a->mask_kind;
+  la.window = a->window;
+  la.q_offset = a->q_offset;
+  la.softcap = a->softcap;
   for (int i = 0; i < 3; ++i) {
     la.qs[i] = a->q_strides[i];
     la.ks[i] = a->k_strides[i];
@@ -429,6 +444,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   return launch_bwd(a);
 }
 
-int fa_version(void) { return 102; }
+int fa_version(void) { return 103; }
 
 }  // extern "C"

@@ -197,13 +197,25 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-// Number of KV tiles a 128-row Q tile starting at r0 visits (0 if it has no rows).
+// KV tiles a 128-row Q tile starting at r0 visits: [tile_kv_begin, tile_kv_blocks).
+// tile_kv_blocks is 0 when the tile has no rows, and at least 1 otherwise (a
+// tile whose rows see no key still runs one fully masked block, which writes
+// O = 0 and L = -inf).
 template <class C>
 __device__ __forceinline__ int tile_kv_blocks(const FaParams& p, int r0) {
   if (r0 >= p.qL) return 0;
   const int last = min(r0 + C::kBM, p.qL) - 1;
-  const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
-  return (kv_end + C::kBN - 1) / C::kBN;
+  const long long diag_end = (long long)last + 1 + p.q_offset;  // one past the last row's diagonal key
+  const int kv_end = p.causal ? (int)max(0LL, min((long long)p.kL, diag_end)) : p.kL;
+  return max(1, (kv_end + C::kBN - 1) / C::kBN);
+}
+// First KV tile any row of the tile starting at r0 can see (sliding window).
+template <class C>
+__device__ __forceinline__ int tile_kv_begin(const FaParams& p, int r0, int nblk) {
+  if (p.window <= 0) return 0;
+  const long long first = (long long)r0 + p.q_offset - p.window + 1;  // row r0's first key
+  const int b0 = first <= 0 ? 0 : (int)min(first / C::kBN, (long long)0x7fffffff);
+  return min(b0, max(nblk - 1, 0));
 }
 
 // Round a tile of fp32 values in shared memory to tf32 (round to nearest).
@@ -357,10 +369,20 @@ __device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t
 template <class C>
 __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p, int b, int h, int row, int kbase,
                                            const uint8_t* mask_tile, int tl) {
-  // Scores to base 2 first when the mask is additive or the scale is not positive.
+  // Scores to base 2 first when the mask is additive, a softcap applies or the
+  // scale is not positive.  The softcap c * tanh(y) (y = scale * s / c) uses
+  // tanh(y) = 1 - 2 / (2^(2 log2(e) y) + 1): one ex2 and one reciprocal, exact
+  // limits +-1 when the power overflows or underflows, and an absolute error
+  // of a few fp32 ulps of 1 near y = 0 (what the capped score needs).
   if (p.pre_scale) {
+    if (p.softcap_on) {
+      const float kin = 2.0f * kLog2e * p.softcap_in, cout = p.softcap_out;
 #pragma unroll
-    for (int c = 0; c < C::kBN; ++c) s[c] *= p.scale_log2;
+      for (int c = 0; c < C::kBN; ++c) s[c] = fmaf(-2.0f * cout, rcp_approx(ex2(s[c] * kin) + 1.0f), cout);
+    } else {
+#pragma unroll
+      for (int c = 0; c < C::kBN; ++c) s[c] *= p.scale_log2;
+    }
   }
   if constexpr (C::kMaskSlotBytes > 0) {
     if (mask_tile) fold_mask_smem<C>(s, mask_tile, p.mask_kind, tl);
@@ -378,12 +400,14 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
         fold_mask_chunk<C, 2>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec);
     }
   }
-  // Causal and tail limits: key kbase + c is allowed iff c < lim.
+  // Causal, tail and window limits: key kbase + c is allowed iff lo <= c < lim.
+  const int diag = row + p.q_offset - kbase;  // this row's diagonal key, relative to kbase
   int lim = p.kL - kbase;
-  if (p.causal) lim = min(lim, row + 1 - kbase);
+  if (p.causal) lim = min(lim, diag + 1);
+  const int lo = p.window > 0 ? diag - p.window + 1 : -1;
 #pragma unroll
   for (int c = 0; c < C::kBN; ++c)
-    if (c >= lim) s[c] = -INFINITY;
+    if (c >= lim || c < lo) s[c] = -INFINITY;
 }
 
 // Row max of s (raw or base-2 scores): three-input max, four chains.
@@ -439,7 +463,8 @@ __device__ __forceinline__ void p_pass(const float (&s)[C::kBN], float sl, float
 // One work unit: kNQT consecutive 128-row Q tiles of one (batch, head).
 struct Unit {
   int b, h, kvh, q0, N;
-  int nblk[2];  // KV tiles each Q tile visits (0: the tile has no rows)
+  int j0;       // first KV tile of the unit (the tiles share one K/V stream from j0 to N)
+  int nblk[2];  // one past each Q tile's last KV tile (0: the tile has no rows)
 };
 
 template <class C>
@@ -458,6 +483,9 @@ __device__ __forceinline__ Unit decode_unit(const FaParams& p, int u) {
   w.nblk[0] = tile_kv_blocks<C>(p, w.q0);
   w.nblk[1] = (C::kNQT == 2) ? tile_kv_blocks<C>(p, w.q0 + C::kBM) : 0;
   w.N = max(w.nblk[0], w.nblk[1]);
+  // Tile 0's rows come first, so its window starts first; tile 1 masks the
+  // (at most one) leading block it cannot see.
+  w.j0 = tile_kv_begin<C>(p, w.q0, w.nblk[0]);
   return w;
 }
 
@@ -495,7 +523,7 @@ __device__ __forceinline__ void tf32_helpers(uint8_t* sQ, uint8_t* sK, uint8_t* 
       if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
     }
     // Same order as the producer: K_j, then V_{j - kVLag}.
-    for (int j = 0; j < w.N + C::kVLag && ok; ++j) {
+    for (int j = w.j0; j < w.N + C::kVLag && ok; ++j) {
       if (j < w.N) {
         const int slot = k_seen % C::kKStages;
         ok = warp_wait(&ctl->k_full[slot], (k_seen / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
@@ -506,7 +534,7 @@ __device__ __forceinline__ void tf32_helpers(uint8_t* sQ, uint8_t* sK, uint8_t* 
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
       }
-      if (j < C::kVLag) continue;
+      if (j < w.j0 + C::kVLag) continue;
       // V -> V^T (K-major), then hand the V slot back to the producer.
       const int vs = v_seen % C::kVStages, ts = v_seen % C::kVTStages;
       ok = warp_wait(&ctl->v_full[vs], (v_seen / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
@@ -635,15 +663,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int u_next = unit_of(r + 1, num_units);
         const Unit w_next = decode_unit<C>(p, u_next < 0 ? u : u_next);
         if (pf_mask && r == 0) {
-          for (int j = 0; j < min(2, w.N); ++j) prefetch_mask(w, j);
+          for (int j = w.j0; j < min(w.j0 + 2, w.N); ++j) prefetch_mask(w, j);
         }
-        for (int j = 0; j < w.N + C::kVLag && ok; ++j) {
+        for (int j = w.j0; j < w.N + C::kVLag && ok; ++j) {
           if (j < w.N) {
           if (pf_mask) {
             if (j + 2 < w.N)
               prefetch_mask(w, j + 2);
-            else if (u_next >= 0 && j + 2 - w.N < w_next.N)
-              prefetch_mask(w_next, j + 2 - w.N);
+            else if (u_next >= 0 && w_next.j0 + j + 2 - w.N < w_next.N)
+              prefetch_mask(w_next, w_next.j0 + j + 2 - w.N);
           }
           {  // K_j
             const int slot = k_issued % C::kKStages, use = k_issued / C::kKStages;
@@ -669,7 +697,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
           }
           const int jv = j - C::kVLag;
-          if (jv >= 0) {  // V_jv
+          if (jv >= w.j0) {  // V_jv
             const int slot = v_issued % C::kVStages, use = v_issued / C::kVStages;
             ok = wait_bounded(&ctl->v_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
@@ -734,12 +762,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                                  k_hi, idS, 1u);
         }
       };
-      auto issue_PV = [&](int t, int j, int vslot) {
+      auto issue_PV = [&](int t, int j, int vslot, bool first) {
         const uint32_t pcol = C::kAliasP ? (uint32_t)(t * C::kBN) : (uint32_t)(C::kColP + (j & 1) * C::kPCols);
         const uint32_t va = v_lo + ((vslot * C::kKVTileBytes) >> 4);
         const uint32_t dst = tmem + C::kColO + t * C::kD;
         const uint32_t src = tmem + pcol;
-        mma_ts_lh<C::kTf32, 0>(dst, src, va, v_hi, idPV, j > 0 ? 1u : 0u);
+        mma_ts_lh<C::kTf32, 0>(dst, src, va, v_hi, idPV, first ? 0u : 1u);
 #pragma unroll
         for (int kk = 1; kk < C::kBN / C::kKStep; ++kk) {
           const uint32_t voff = C::kTf32 ? ((kk / 4) * (C::kD * 128) + (kk % 4) * 32) >> 4 : (kk * (C::kKStep * 128)) >> 4;
@@ -796,7 +824,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if (t < t_begin || t >= t_end || w.nblk[t] == 0) continue;
           issue_S(t, kslot);
           mma_commit(&ctl->s_full[t]);
-          if (w.nblk[t] == 1) mma_commit(&ctl->q_empty[t]);  // the unit's last S of tile t
+          if (w.nblk[t] == w.j0 + 1) mma_commit(&ctl->q_empty[t]);  // the unit's last S of tile t
         }
         pass_turn();
         mma_commit(&ctl->k_empty[kslot]);
@@ -805,7 +833,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           // One Q tile, one issuer, separate S and P columns: S_{j+1} goes to the
           // tensor core as soon as softmax j holds S_j in registers (and K_{j+1}
           // is ready), so it overlaps softmax j; PV_j follows once P_j is written.
-          for (int j = 0; j < w.N && ok; ++j) {
+          for (int j = w.j0; j < w.N && ok; ++j) {
             ok = wait_bounded(&ctl->s_free[0], s_freed & 1, abort_flag, p.status, p.timeout_cycles);
             ++s_freed;
             if (!ok) break;
@@ -830,18 +858,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             ok = wait_bounded(&ctl->p_ready[0], p_seen[0] & 1, abort_flag, p.status, p.timeout_cycles);
             ++p_seen[0];
             // The unit's first PV overwrites O: the previous unit's epilogue must have read it.
-            if (ok && j == 0 && units_done[0] > 0)
+            if (ok && j == w.j0 && units_done[0] > 0)
               ok = wait_bounded(&ctl->o_free[0], (units_done[0] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
             tc_fence_after();
-            issue_PV(0, j, vslot);
+            issue_PV(0, j, vslot, j == w.j0);
             mma_commit(&ctl->o_ready[0]);
             mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
             ++v_used;
           }
         } else
         // P over S (two Q tiles): per block and tile, PV_j then S_{j+1}.
-        for (int j = 0; j < w.N && ok; ++j) {
+        for (int j = w.j0; j < w.N && ok; ++j) {
           // bf16: V ring slot; tf32: V^T ring slot
           const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
           const uint32_t vpar = (C::kTf32 ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
@@ -865,7 +893,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             ok = wait_bounded(&ctl->p_ready[t], p_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
             ++p_seen[t];
             // The unit's first PV overwrites O_t: the previous unit's epilogue must have read it.
-            if (ok && j == 0 && units_done[t] > 0)
+            if (ok && j == w.j0 && units_done[t] > 0)
               ok = wait_bounded(&ctl->o_free[t], (units_done[t] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
             const bool s_next = (j + 1 < w.nblk[t]);
@@ -880,7 +908,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               turn_taken = true;
             }
             tc_fence_after();
-            issue_PV(t, j, vslot);
+            issue_PV(t, j, vslot, j == w.j0);
             if (!s_next) mma_commit(&ctl->o_ready[t]);  // the tile's last PV of the unit
             if (s_next) {
               issue_S(t, kslot);
@@ -946,7 +974,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int row = r0 + tl;
       float m_run = -INFINITY;  // running max, base 2 (scaled)
       float l_run = 0.0f;       // running sum of 2^(s - m_run)
-      for (int j = 0; j < nb; ++j) {
+      for (int j = w.j0; j < nb; ++j) {
         ok = warp_wait(&ctl->s_full[t], blocks_seen & 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
         ++blocks_seen;
@@ -971,7 +999,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
         const int kbase = j * C::kBN;
         const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + C::kBN > p.kL ||
-                               (p.causal && kbase + C::kBN - 1 > r0);
+                               (p.causal && kbase + C::kBN - 1 > r0 + p.q_offset) ||
+                               (p.window > 0 && kbase <= r0 + C::kBM - 1 + p.q_offset - p.window);
         const uint8_t* mask_tile = nullptr;
         if (C::kMaskSlotBytes > 0 && p.mask_smem) {
           ok = warp_wait(&ctl->m_full, masks_seen & 1, abort_flag, p.status, p.timeout_cycles);
@@ -1007,13 +1036,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // parity wait never runs a phase behind.  With P over S, S_j's
         // completion already implies PV_{j-1}: it was issued first.
         if constexpr (!C::kAliasP) {
-          if (j > 0) {
+          if (j > w.j0) {
             ok = warp_wait(&ctl->o_ready[t], (blocks_seen - 2) & 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
           }
         }
         // Rescale this warp's O rows (the previous PV has landed).
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        if (j > w.j0 && __any_sync(0xffffffffu, resc)) {
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < C::kD / 32; ++cc) {

@@ -20,6 +20,8 @@ struct LaunchArgs {
   int B, Hq, Hkv, qL, kL, D;
   float scale;
   int causal, mask_kind;
+  int window, q_offset;  // sliding window (0 = off) and causal diagonal offset
+  float softcap;         // 0 = off
   long long qs[3], ks[3], vs[3], os[3], ms[3];  // element strides: batch, head, row
   int mask_vec;
   cudaStream_t stream;
@@ -112,7 +114,12 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.n_qblocks = (a.qL + C::kBM * C::kNQT - 1) / (C::kBM * C::kNQT);
   p.causal = a.causal;
   p.mask_kind = a.mask_kind;
-  p.pre_scale = (a.mask_kind == 2 || !(a.scale > 0.0f)) ? 1 : 0;
+  p.softcap_on = a.softcap > 0.0f ? 1 : 0;
+  p.softcap_in = p.softcap_on ? a.scale / a.softcap : 0.0f;
+  p.softcap_out = p.softcap_on ? a.softcap * kLog2e : 0.0f;
+  p.window = a.window;
+  p.q_offset = a.q_offset;
+  p.pre_scale = (a.mask_kind == 2 || !(a.scale > 0.0f) || p.softcap_on) ? 1 : 0;
   p.mask_vec = a.mask_vec;
   p.mask_l2 = mask_l2;
   p.mask_smem = mask_smem;

@@ -17,11 +17,16 @@ struct FaParams {
   int n_qblocks;    // query blocks of (tiles per CTA * 128) rows per (b, h)
   int causal;       // top-left aligned: key j allowed for row i iff j <= i
   int mask_kind;    // 0 none, 1 bool (uint8, nonzero keeps), 2 additive (I/O dtype)
-  int pre_scale;    // scale scores before masking (additive mask, or scale <= 0)
+  int pre_scale;    // scale scores before masking (additive mask, softcap, or scale <= 0)
   int mask_vec;     // mask rows 16-byte aligned: vector loads allowed
   int mask_l2;      // a tensor map describes the mask: prefetch its tiles into L2
   int mask_smem;    // the mask map is 128-byte swizzled: TMA-load its tiles into shared memory
   float scale_log2; // scale * log2(e)
+  int window;       // > 0: key j allowed only if j > i + q_offset - window (sliding window)
+  int q_offset;     // causal diagonal of row i is key i + q_offset (0: top-left aligned)
+  int softcap_on;   // scores become cap * tanh(scale * s / cap) before any mask
+  float softcap_in;   // scale / cap
+  float softcap_out;  // cap * log2(e)
   const void* mask;
   long long mask_sb, mask_sh, mask_ss;  // mask element strides: batch, head, query row
   void* o;                              // output, I/O dtype

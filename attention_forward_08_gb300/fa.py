@@ -49,6 +49,7 @@ class FaFwdArgs(ctypes.Structure):
         ("v_strides", ctypes.c_longlong * 3), ("o_strides", ctypes.c_longlong * 3),
         ("mask_strides", ctypes.c_longlong * 3),
         ("stream", ctypes.c_void_p),
+        ("window", ctypes.c_int), ("q_offset", ctypes.c_int), ("softcap", ctypes.c_float),
     ]
 
 
@@ -156,7 +157,8 @@ def _strides_bhs(t, name):
     return (t.stride(0), t.stride(1), t.stride(2))
 
 
-def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind=None, stream=None) -> FaFwdArgs:
+def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind=None, stream=None, window=0,
+              q_offset=0, softcap=0.0) -> FaFwdArgs:
     """Fill ``fa_fwd_args`` from torch CUDA tensors (4-D views with unit inner stride).
 
     q, o: [B, H_q, qL, D]; k, v: [B, H_kv, kL, D]; lse: contiguous [B, H_q, qL]
@@ -192,6 +194,7 @@ def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind
     a.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
     a.causal = int(bool(causal))
     a.dtype = dtype
+    a.window, a.q_offset, a.softcap = int(window), int(q_offset), float(softcap)
     a.q_strides[:] = _strides_bhs(q, "q")
     a.k_strides[:] = _strides_bhs(k, "k")
     a.v_strides[:] = _strides_bhs(v, "v")
@@ -223,7 +226,7 @@ def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind
 
 
 def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, out=None, lse=None,
-              stream=None):
+              stream=None, window=0, q_offset=0, softcap=0.0):
     """O and L for torch CUDA tensors (see ``make_args``); returns (o, lse)."""
     import torch
     B, H_q, qL, D = q.shape
@@ -232,7 +235,7 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
     if lse is None:
         lse = torch.empty((B, H_q, qL), dtype=torch.float32, device=q.device)
     args = make_args(q, k, v, out, lse, scale=scale, causal=causal, mask=mask, mask_kind=mask_kind,
-                     stream=stream)
+                     stream=stream, window=window, q_offset=q_offset, softcap=softcap)
     _check(fa_fwd_ex(args))
     return out, lse
 

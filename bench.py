@@ -172,14 +172,16 @@ def oracle_sample(w: workloads.Workload, q, k, v, m, seconds: float):
 
     def rows_flops(rows):
         i = np.asarray(rows) % w.qL
-        n = np.minimum(i + 1, w.kL) if w.causal else np.full(len(rows), w.kL)
-        return float(np.sum(4.0 * w.D * n))
+        hi = np.minimum(i + w.q_offset, w.kL - 1) if w.causal else np.full(len(rows), w.kL - 1)
+        lo = np.maximum(0, i + w.q_offset - w.window + 1) if w.window > 0 else np.zeros(len(rows), dtype=np.int64)
+        return float(np.sum(4.0 * w.D * np.maximum(0, hi - lo + 1)))
 
     def run(n):
         rows = np.linspace(0, total_rows - 1, n).astype(np.int64).tolist()
         t0 = time.perf_counter()
         oracle.attention(qo, ko, vo, scale, causal=w.causal, mask=mo, mask_kind=w.mask_kind, rows=rows,
-                         n_threads=threads)
+                         n_threads=threads, window=w.window, softcap=float(np.float32(w.softcap)),
+                         q_offset=w.q_offset)
         return rows, time.perf_counter() - t0
 
     n = max(threads, 16)
@@ -253,7 +255,9 @@ def run_reference(args, w):
 
 
 def config_of(w, args):
+    extra = {k: getattr(w, k) for k in ("window", "softcap", "q_offset") if getattr(w, k)}
     return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "seq_len": w.qL, "kL": w.kL, "D": w.D,
+            **extra,
             "causal": w.causal, "mask": ["none", "bool", "additive"][w.mask_kind],
             "layout": "token-major O" if w.layout == "dit" else "BHSD",
             "global_batch": w.B * max(1, args.gpus), "parallelism": f"replicas x{max(1, args.gpus)}",
@@ -284,7 +288,8 @@ def run_ours(args, w):
     lsed = torch.empty((B, H, qL), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     fargs = fa.make_args(qd, kd, vd, od, lsed, scale=w.sm_scale, causal=w.causal, mask=md,
-                         mask_kind=None if md is None else w.mask_kind, stream=stream.cuda_stream)
+                         mask_kind=None if md is None else w.mask_kind, stream=stream.cuda_stream,
+                         window=w.window, q_offset=w.q_offset, softcap=w.softcap)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def launch():
@@ -442,8 +447,10 @@ def run_ours_bwd(args, w):
     torch.cuda.set_device(dev)
     import attention_forward_08_gb300 as fa
     fa.load_library()
-    if w.dtype != "bf16" or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128):
-        raise SystemExit(f"--pass bwd needs an unmasked bf16 BHSD workload with D 64 or 128 ({w.name})")
+    if (w.dtype != "bf16" or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128) or w.window
+            or w.softcap or w.q_offset):
+        raise SystemExit(f"--pass bwd needs a plain (unmasked, no window/softcap/offset) bf16 BHSD workload "
+                         f"with D 64 or 128 ({w.name})")
     q, k, v = workloads.make_qkv(w)
     do = workloads.make_dout(w)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)

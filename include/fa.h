@@ -81,6 +81,15 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  * dimension.  lse stays contiguous [B, H_q, qL].
  * Example: head-major q/k/v [H, seq, D] with token-major output
  * o[seq, H*D] is B = 1 with o_strides = {seq*H*D, D, H*D}.
+ * The last three fields extend the operation (all zero = the plain forward):
+ *   window > 0  sliding window: key j allowed only if j > i + q_offset - window
+ *               (forge "flash_attention_mma.metal" names the field `window`);
+ *   q_offset    the causal diagonal of row i is key i + q_offset (mlx-native
+ *               `ql_off`); kL - qL aligns the last query with the last key;
+ *   softcap > 0 scores become softcap * tanh(scale * q.k / softcap) before
+ *               any mask (mlx-native `softcapping`); L is the logsumexp of
+ *               the capped scores.
+ * window must be >= 0, |q_offset| < 2^30, softcap finite and >= 0.
  */
 typedef struct fa_fwd_args {
   const void* q;
@@ -100,6 +109,10 @@ typedef struct fa_fwd_args {
   long long o_strides[3];
   long long mask_strides[3];
   void* stream; /* cudaStream_t */
+  /* Added in ABI 1.03 (zero = off; zero-initialise the struct): */
+  int window;    /* > 0: sliding window, key j allowed only if j > i + q_offset - window */
+  int q_offset;  /* causal diagonal of row i is key i + q_offset (0: top-left; kL - qL: bottom-right) */
+  float softcap; /* > 0: each scaled score s becomes softcap * tanh(s / softcap), before any mask */
 } fa_fwd_args;
 
 int fa_fwd_ex(const fa_fwd_args* args);

@@ -29,13 +29,19 @@ def gpu_run(w: workloads.Workload, q, k, v, mask, scale=None):
         o = torch.full((B, H, qL, D), float("nan"), dtype=q.dtype, device=dev)
     lse = torch.full((B, H, qL), float("nan"), dtype=torch.float32, device=dev)
     fa.attention(qd, kd, vd, scale=w.sm_scale if scale is None else scale, causal=w.causal, mask=md,
-                 mask_kind=None if mask is None else w.mask_kind, out=o, lse=lse)
+                 mask_kind=None if mask is None else w.mask_kind, out=o, lse=lse, window=w.window,
+                 q_offset=w.q_offset, softcap=w.softcap)
     rc = fa.fa_sync_status(None)
     assert rc == 0, f"device status {rc}: {fa.fa_last_error()}"
     if w.layout == "dit":
         o_bhsd = o_tok.view(qL, H, D).permute(1, 0, 2).unsqueeze(0)
         return o_bhsd.double().cpu().numpy(), lse.double().cpu().numpy(), o_tok
     return o.double().cpu().numpy(), lse.double().cpu().numpy(), o
+
+
+def oracle_features(w: workloads.Workload) -> dict:
+    """The workload's window / softcap / query offset as oracle keyword arguments."""
+    return dict(window=w.window, softcap=float(np.float32(w.softcap)), q_offset=w.q_offset)
 
 
 def oracle_inputs(q, k, v, mask):

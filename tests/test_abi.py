@@ -61,7 +61,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 102
+    assert fa.fa_version() == 103
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it

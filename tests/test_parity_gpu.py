@@ -1,11 +1,12 @@
 """GPU parity: the CUDA library against the fp64 oracle on the same seeded inputs.
 
 Reduced sizes are compared element by element (several Q and KV tiles,
-ragged tails, every head dim, dtype, mask kind, causal, GQA and the
-token-major output); the five full-size workloads are compared on sampled
-rows computed one by one by the oracle, in the launch configuration the
-benchmark times.  Tolerances (inputs N(0,1)): bf16 max|dO| <= 2e-2 and
-max|dL| <= 1e-2; fp32 via TF32 max|dO| <= 2e-3 and max|dL| <= 1e-3.
+ragged tails, every head dim, dtype, mask kind, causal, GQA, the
+token-major output, sliding windows, softcaps and query offsets); the
+full-size workloads are compared on sampled rows computed one by one by the
+oracle, in the launch configuration the benchmark times.  Tolerances (inputs
+N(0,1)): bf16 max|dO| <= 2e-2 and max|dL| <= 1e-2; fp32 via TF32 max|dO| <=
+2e-3 and max|dL| <= 1e-3; fp16 a quarter of the bf16 bounds.
 """
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_helpers import compare, fp32_scale, gpu_run, oracle_inputs, sample_rows
+from gpu_helpers import oracle_features, compare, fp32_scale, gpu_run, oracle_inputs, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +58,7 @@ def _run_small(w, scale=None, mask=None, qkv=None, tol_mult=1.0, tol_mult_l=None
     o_g, l_g, _ = gpu_run(w, q, k, v, m, scale=scale)
     qo, ko, vo, mo = oracle_inputs(q, k, v, m)
     o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w, scale), causal=w.causal, mask=mo,
-                                mask_kind=w.mask_kind if m is not None else 0)
+                                mask_kind=w.mask_kind if m is not None else 0, **oracle_features(w))
     if tf32_relative and w.dtype == "f32":
         # TF32 score errors are relative to the scores; L tracks the largest score.
         big = float(np.max(np.abs(l_r[np.isfinite(l_r)]))) / 8.0
@@ -68,6 +69,40 @@ def _run_small(w, scale=None, mask=None, qkv=None, tol_mult=1.0, tol_mult_l=None
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 def test_small_elementwise(w):
     _run_small(w)
+
+
+# Sliding window, softcap and query offset on every kernel plan (two Q tiles,
+# one Q tile, TF32, masks).  Softcaps of 1.5-4 against N(0,1) inputs with a
+# raised scale make the cap bend most scores.
+FEATURES = [
+    S("swa_bf16_d128", 1, 4, 2, 700, 700, 128, "bf16", causal=True, window=200, seed=61),
+    S("swa_bf16_d64_offset", 2, 2, 1, 300, 350, 64, "bf16", causal=True, window=130, q_offset=50, seed=62),
+    S("swa_bf16_d256", 1, 2, 2, 600, 600, 256, "bf16", causal=True, window=300, seed=63),
+    S("swa_f32_d128", 1, 2, 2, 500, 500, 128, "f32", causal=True, window=256, seed=64),
+    S("swa_noncausal_f32_d64", 1, 2, 2, 300, 420, 64, "f32", window=100, seed=65),
+    S("swa_f16_d128_window1", 1, 2, 2, 260, 260, 128, "f16", causal=True, window=1, seed=66),
+    S("softcap_bf16_d128", 1, 4, 2, 384, 384, 128, "bf16", causal=True, softcap=3.0, scale=0.3, seed=67),
+    S("softcap_bf16_d256_additive", 1, 2, 2, 256, 256, 256, "bf16", mask_kind=W.MASK_ADDITIVE, softcap=2.0,
+      scale=0.2, seed=68),
+    S("softcap_f32_d128", 1, 2, 2, 300, 300, 128, "f32", softcap=4.0, seed=69),
+    S("softcap_f32_d64_causal", 1, 3, 3, 290, 290, 64, "f32", causal=True, softcap=1.5, scale=0.4, seed=70),
+    S("prefill_f16_d128", 1, 2, 2, 200, 900, 128, "f16", causal=True, q_offset=700, seed=71),
+    S("neg_offset_bf16_d128", 1, 2, 2, 300, 300, 128, "bf16", causal=True, q_offset=-50, seed=72),
+    S("all_bf16_d64_bool", 1, 2, 1, 257, 400, 64, "bf16", causal=True, mask_kind=W.MASK_BOOL, window=150,
+      softcap=2.5, q_offset=143, seed=73),
+    S("swa_offset_bf16_d256_gqa", 1, 4, 1, 333, 500, 256, "bf16", causal=True, window=170, q_offset=167, seed=74),
+]
+
+
+@pytest.mark.parametrize("w", FEATURES, ids=lambda w: w.name)
+def test_window_softcap_offset(w):
+    """fp32 cases with a raised scale take the TF32 rule of test_unusual_scales: raw scores of
+    standard deviation |scale|*sqrt(D) carry proportionally larger product errors into the cap."""
+    sd = abs(w.sm_scale) * w.D ** 0.5
+    if w.dtype == "f32" and sd > 1.0:
+        _run_small(w, tol_mult=sd, tol_mult_l=4.0 * sd)
+    else:
+        _run_small(w, tf32_relative=True)
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.3, 2.5])
@@ -158,7 +193,7 @@ def test_full_workload_sampled_rows(name):
     rows = sample_rows(w, n_per_head=3 if w.qL * w.kL > 4e6 else 8)
     qo, ko, vo, mo = oracle_inputs(q, k, v, m)
     o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w), causal=w.causal, mask=mo,
-                                mask_kind=w.mask_kind, rows=rows)
+                                mask_kind=w.mask_kind, rows=rows, **oracle_features(w))
     D = w.D
     compare(w, o_g.reshape(-1, D)[rows], l_g.reshape(-1)[rows], o_r, l_r, what=name)
 

@@ -38,6 +38,9 @@ class Workload:
     seed: int = 1000
     mask_seed: int = 2000
     scale: float = field(default=float("nan"))
+    window: int = 0        # > 0: sliding window of keys j > i + q_offset - window
+    softcap: float = 0.0   # > 0: scores capped as softcap * tanh(s / softcap)
+    q_offset: int = 0      # causal diagonal of row i is key i + q_offset
 
     @property
     def sm_scale(self) -> float:
@@ -48,9 +51,17 @@ class Workload:
         return {"bf16": torch.bfloat16, "f16": torch.float16}.get(self.dtype, torch.float32)
 
     def flops(self) -> float:
-        """Algorithmic FLOP: 4*B*H_q*qL*kL*D, halved when causal."""
-        f = 4.0 * self.B * self.H_q * self.qL * self.kL * self.D
-        return f / 2.0 if self.causal else f
+        """Algorithmic FLOP: 4*B*H_q*qL*kL*D, halved when causal; with a window
+        or a query offset, 4*B*H_q*D times the exact number of allowed (i, j) pairs."""
+        if self.window == 0 and self.q_offset == 0:
+            f = 4.0 * self.B * self.H_q * self.qL * self.kL * self.D
+            return f / 2.0 if self.causal else f
+        pairs = 0
+        for i in range(self.qL):
+            hi = min(self.kL - 1, i + self.q_offset) if self.causal else self.kL - 1
+            lo = max(0, i + self.q_offset - self.window + 1) if self.window > 0 else 0
+            pairs += max(0, hi - lo + 1)
+        return 4.0 * self.B * self.H_q * self.D * pairs
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -77,10 +88,17 @@ WORKLOADS = {
 
 BENCH_WORKLOAD = "bf16_gqa_causal_b2_hq32_hkv8_l4096_d128"
 
-# Beyond the pages' workloads: the bench workload with fp16 I/O (same seeds).
+# Beyond the pages' workloads: the bench workload with fp16 I/O, with a
+# 1024-key sliding window, and with a softcap of 20 (same seeds).
 EXTRA_WORKLOADS = {
     "f16_gqa_causal_b2_hq32_hkv8_l4096_d128": Workload(
         "f16_gqa_causal_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "f16", causal=True, seed=1002),
+    "bf16_gqa_causal_swa1024_b2_hq32_hkv8_l4096_d128": Workload(
+        "bf16_gqa_causal_swa1024_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "bf16", causal=True,
+        seed=1002, window=1024),
+    "bf16_gqa_causal_softcap20_b2_hq32_hkv8_l4096_d128": Workload(
+        "bf16_gqa_causal_softcap20_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "bf16", causal=True,
+        seed=1002, softcap=20.0),
 }
 WORKLOADS.update(EXTRA_WORKLOADS)
 
@@ -129,7 +147,8 @@ def make_inputs(w: Workload):
 
 
 def small_case(name, B, H_q, H_kv, qL, kL, D, dtype, causal=False, mask_kind=MASK_NONE,
-               layout="bhsd", seed=7, scale=float("nan")) -> Workload:
+               layout="bhsd", seed=7, scale=float("nan"), window=0, softcap=0.0, q_offset=0) -> Workload:
     """A reduced-size workload for element-by-element parity runs."""
     return Workload(name, B, H_q, H_kv, qL, kL, D, dtype, causal=causal, mask_kind=mask_kind,
-                    layout=layout, seed=seed, mask_seed=seed + 1000, scale=scale)
+                    layout=layout, seed=seed, mask_seed=seed + 1000, scale=scale, window=window,
+                    softcap=softcap, q_offset=q_offset)
