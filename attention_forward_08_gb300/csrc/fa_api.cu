@@ -263,15 +263,26 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     la.max_ctas = g_max_ctas;
   }
 
+  const bool feat = a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f;
   switch (a->dtype) {
     case FA_DTYPE_F32:
-      rc = a->D == 64 ? launch_f32_d64(la) : a->D == 128 ? launch_f32_d128(la) : launch_f32_d256(la);
+      if (feat)
+        rc = a->D == 64 ? launch_feat_f32_d64(la) : a->D == 128 ? launch_feat_f32_d128(la) : launch_feat_f32_d256(la);
+      else
+        rc = a->D == 64 ? launch_f32_d64(la) : a->D == 128 ? launch_f32_d128(la) : launch_f32_d256(la);
       break;
     case FA_DTYPE_F16:
-      rc = a->D == 64 ? launch_f16_d64(la) : a->D == 128 ? launch_f16_d128(la) : launch_f16_d256(la);
+      if (feat)
+        rc = a->D == 64 ? launch_feat_f16_d64(la) : a->D == 128 ? launch_feat_f16_d128(la) : launch_feat_f16_d256(la);
+      else
+        rc = a->D == 64 ? launch_f16_d64(la) : a->D == 128 ? launch_f16_d128(la) : launch_f16_d256(la);
       break;
     default:
-      rc = a->D == 64 ? launch_bf16_d64(la) : a->D == 128 ? launch_bf16_d128(la) : launch_bf16_d256(la);
+      if (feat)
+        rc = a->D == 64 ? launch_feat_bf16_d64(la) : a->D == 128 ? launch_feat_bf16_d128(la)
+                                                                  : launch_feat_bf16_d256(la);
+      else
+        rc = a->D == 64 ? launch_bf16_d64(la) : a->D == 128 ? launch_bf16_d128(la) : launch_bf16_d256(la);
       break;
   }
   return rc;

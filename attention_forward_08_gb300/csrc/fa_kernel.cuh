@@ -67,9 +67,12 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr long long kDrainCycles = 1LL << 33;
 
 template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_, int kVTStages_ = 0,
-          bool kF16_ = false>
+          bool kF16_ = false, bool kFeat_ = false>
 struct Cfg {
   static constexpr bool kTf32 = kTf32_;
+  // Sliding window, softcap and query offset compiled in (a separate
+  // instantiation, so the plain forward keeps its exact code).
+  static constexpr bool kFeat = kFeat_;
   // 16-bit I/O is bf16 unless kF16 (fp16): same kernel, other operand format.
   static constexpr bool kF16 = kF16_;
   static constexpr uint32_t kFmt = kTf32 ? kFmtTf32 : (kF16 ? kFmtF16 : kFmtBf16);
@@ -205,14 +208,18 @@ template <class C>
 __device__ __forceinline__ int tile_kv_blocks(const FaParams& p, int r0) {
   if (r0 >= p.qL) return 0;
   const int last = min(r0 + C::kBM, p.qL) - 1;
-  const long long diag_end = (long long)last + 1 + p.q_offset;  // one past the last row's diagonal key
+  if constexpr (!C::kFeat) {
+    const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
+    return (kv_end + C::kBN - 1) / C::kBN;
+  }
+  const long long diag_end = (long long)last + 1 + (C::kFeat ? p.q_offset : 0);  // one past the last row's diagonal key
   const int kv_end = p.causal ? (int)max(0LL, min((long long)p.kL, diag_end)) : p.kL;
   return max(1, (kv_end + C::kBN - 1) / C::kBN);
 }
 // First KV tile any row of the tile starting at r0 can see (sliding window).
 template <class C>
 __device__ __forceinline__ int tile_kv_begin(const FaParams& p, int r0, int nblk) {
-  if (p.window <= 0) return 0;
+  if (!C::kFeat || p.window <= 0) return 0;
   const long long first = (long long)r0 + p.q_offset - p.window + 1;  // row r0's first key
   const int b0 = first <= 0 ? 0 : (int)min(first / C::kBN, (long long)0x7fffffff);
   return min(b0, max(nblk - 1, 0));
@@ -375,7 +382,7 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
   // limits +-1 when the power overflows or underflows, and an absolute error
   // of a few fp32 ulps of 1 near y = 0 (what the capped score needs).
   if (p.pre_scale) {
-    if (p.softcap_on) {
+    if (C::kFeat && p.softcap_on) {
       const float kin = 2.0f * kLog2e * p.softcap_in, cout = p.softcap_out;
 #pragma unroll
       for (int c = 0; c < C::kBN; ++c) s[c] = fmaf(-2.0f * cout, rcp_approx(ex2(s[c] * kin) + 1.0f), cout);
@@ -401,10 +408,10 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
     }
   }
   // Causal, tail and window limits: key kbase + c is allowed iff lo <= c < lim.
-  const int diag = row + p.q_offset - kbase;  // this row's diagonal key, relative to kbase
+  const int diag = row + (C::kFeat ? p.q_offset : 0) - kbase;  // this row's diagonal key, relative to kbase
   int lim = p.kL - kbase;
   if (p.causal) lim = min(lim, diag + 1);
-  const int lo = p.window > 0 ? diag - p.window + 1 : -1;
+  const int lo = (C::kFeat && p.window > 0) ? diag - p.window + 1 : -1;
 #pragma unroll
   for (int c = 0; c < C::kBN; ++c)
     if (c >= lim || c < lo) s[c] = -INFINITY;
@@ -467,6 +474,15 @@ struct Unit {
   int nblk[2];  // one past each Q tile's last KV tile (0: the tile has no rows)
 };
 
+// The unit's first KV tile: a compile-time 0 without a sliding window.
+template <class C>
+__device__ __forceinline__ int unit_j0(const Unit& w) {
+  if constexpr (C::kFeat)
+    return w.j0;
+  else
+    return 0;
+}
+
 template <class C>
 __device__ __forceinline__ Unit decode_unit(const FaParams& p, int u) {
   // Heavy causal query blocks first; consecutive units are consecutive heads,
@@ -523,7 +539,7 @@ __device__ __forceinline__ void tf32_helpers(uint8_t* sQ, uint8_t* sK, uint8_t* 
       if (lane == 0) mbar_arrive(&ctl->q_ready[t]);
     }
     // Same order as the producer: K_j, then V_{j - kVLag}.
-    for (int j = w.j0; j < w.N + C::kVLag && ok; ++j) {
+    for (int j = unit_j0<C>(w); j < w.N + C::kVLag && ok; ++j) {
       if (j < w.N) {
         const int slot = k_seen % C::kKStages;
         ok = warp_wait(&ctl->k_full[slot], (k_seen / C::kKStages) & 1, abort_flag, p.status, p.timeout_cycles);
@@ -534,7 +550,7 @@ __device__ __forceinline__ void tf32_helpers(uint8_t* sQ, uint8_t* sK, uint8_t* 
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->k_ready[slot]);
       }
-      if (j < w.j0 + C::kVLag) continue;
+      if (j < unit_j0<C>(w) + C::kVLag) continue;
       // V -> V^T (K-major), then hand the V slot back to the producer.
       const int vs = v_seen % C::kVStages, ts = v_seen % C::kVTStages;
       ok = warp_wait(&ctl->v_full[vs], (v_seen / C::kVStages) & 1, abort_flag, p.status, p.timeout_cycles);
@@ -663,15 +679,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int u_next = unit_of(r + 1, num_units);
         const Unit w_next = decode_unit<C>(p, u_next < 0 ? u : u_next);
         if (pf_mask && r == 0) {
-          for (int j = w.j0; j < min(w.j0 + 2, w.N); ++j) prefetch_mask(w, j);
+          for (int j = unit_j0<C>(w); j < min(unit_j0<C>(w) + 2, w.N); ++j) prefetch_mask(w, j);
         }
-        for (int j = w.j0; j < w.N + C::kVLag && ok; ++j) {
+        for (int j = unit_j0<C>(w); j < w.N + C::kVLag && ok; ++j) {
           if (j < w.N) {
           if (pf_mask) {
             if (j + 2 < w.N)
               prefetch_mask(w, j + 2);
-            else if (u_next >= 0 && w_next.j0 + j + 2 - w.N < w_next.N)
-              prefetch_mask(w_next, w_next.j0 + j + 2 - w.N);
+            else if (u_next >= 0 && unit_j0<C>(w_next) + j + 2 - w.N < w_next.N)
+              prefetch_mask(w_next, unit_j0<C>(w_next) + j + 2 - w.N);
           }
           {  // K_j
             const int slot = k_issued % C::kKStages, use = k_issued / C::kKStages;
@@ -697,7 +713,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
           }
           const int jv = j - C::kVLag;
-          if (jv >= w.j0) {  // V_jv
+          if (jv >= unit_j0<C>(w)) {  // V_jv
             const int slot = v_issued % C::kVStages, use = v_issued / C::kVStages;
             ok = wait_bounded(&ctl->v_empty[slot], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
@@ -824,7 +840,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if (t < t_begin || t >= t_end || w.nblk[t] == 0) continue;
           issue_S(t, kslot);
           mma_commit(&ctl->s_full[t]);
-          if (w.nblk[t] == w.j0 + 1) mma_commit(&ctl->q_empty[t]);  // the unit's last S of tile t
+          if (w.nblk[t] == unit_j0<C>(w) + 1) mma_commit(&ctl->q_empty[t]);  // the unit's last S of tile t
         }
         pass_turn();
         mma_commit(&ctl->k_empty[kslot]);
@@ -833,7 +849,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           // One Q tile, one issuer, separate S and P columns: S_{j+1} goes to the
           // tensor core as soon as softmax j holds S_j in registers (and K_{j+1}
           // is ready), so it overlaps softmax j; PV_j follows once P_j is written.
-          for (int j = w.j0; j < w.N && ok; ++j) {
+          for (int j = unit_j0<C>(w); j < w.N && ok; ++j) {
             ok = wait_bounded(&ctl->s_free[0], s_freed & 1, abort_flag, p.status, p.timeout_cycles);
             ++s_freed;
             if (!ok) break;
@@ -858,18 +874,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             ok = wait_bounded(&ctl->p_ready[0], p_seen[0] & 1, abort_flag, p.status, p.timeout_cycles);
             ++p_seen[0];
             // The unit's first PV overwrites O: the previous unit's epilogue must have read it.
-            if (ok && j == w.j0 && units_done[0] > 0)
+            if (ok && j == unit_j0<C>(w) && units_done[0] > 0)
               ok = wait_bounded(&ctl->o_free[0], (units_done[0] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
             tc_fence_after();
-            issue_PV(0, j, vslot, j == w.j0);
+            issue_PV(0, j, vslot, j == unit_j0<C>(w));
             mma_commit(&ctl->o_ready[0]);
             mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
             ++v_used;
           }
         } else
         // P over S (two Q tiles): per block and tile, PV_j then S_{j+1}.
-        for (int j = w.j0; j < w.N && ok; ++j) {
+        for (int j = unit_j0<C>(w); j < w.N && ok; ++j) {
           // bf16: V ring slot; tf32: V^T ring slot
           const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
           const uint32_t vpar = (C::kTf32 ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
@@ -893,7 +909,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             ok = wait_bounded(&ctl->p_ready[t], p_seen[t] & 1, abort_flag, p.status, p.timeout_cycles);
             ++p_seen[t];
             // The unit's first PV overwrites O_t: the previous unit's epilogue must have read it.
-            if (ok && j == w.j0 && units_done[t] > 0)
+            if (ok && j == unit_j0<C>(w) && units_done[t] > 0)
               ok = wait_bounded(&ctl->o_free[t], (units_done[t] - 1) & 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
             const bool s_next = (j + 1 < w.nblk[t]);
@@ -908,7 +924,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               turn_taken = true;
             }
             tc_fence_after();
-            issue_PV(t, j, vslot, j == w.j0);
+            issue_PV(t, j, vslot, j == unit_j0<C>(w));
             if (!s_next) mma_commit(&ctl->o_ready[t]);  // the tile's last PV of the unit
             if (s_next) {
               issue_S(t, kslot);
@@ -974,7 +990,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int row = r0 + tl;
       float m_run = -INFINITY;  // running max, base 2 (scaled)
       float l_run = 0.0f;       // running sum of 2^(s - m_run)
-      for (int j = w.j0; j < nb; ++j) {
+      for (int j = unit_j0<C>(w); j < nb; ++j) {
         ok = warp_wait(&ctl->s_full[t], blocks_seen & 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
         ++blocks_seen;
@@ -998,9 +1014,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
 
         const int kbase = j * C::kBN;
+        const int q_off = C::kFeat ? p.q_offset : 0;
         const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + C::kBN > p.kL ||
-                               (p.causal && kbase + C::kBN - 1 > r0 + p.q_offset) ||
-                               (p.window > 0 && kbase <= r0 + C::kBM - 1 + p.q_offset - p.window);
+                               (p.causal && kbase + C::kBN - 1 > r0 + q_off) ||
+                               (C::kFeat && p.window > 0 && kbase <= r0 + C::kBM - 1 + q_off - p.window);
         const uint8_t* mask_tile = nullptr;
         if (C::kMaskSlotBytes > 0 && p.mask_smem) {
           ok = warp_wait(&ctl->m_full, masks_seen & 1, abort_flag, p.status, p.timeout_cycles);
@@ -1036,13 +1053,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // parity wait never runs a phase behind.  With P over S, S_j's
         // completion already implies PV_{j-1}: it was issued first.
         if constexpr (!C::kAliasP) {
-          if (j > w.j0) {
+          if (j > unit_j0<C>(w)) {
             ok = warp_wait(&ctl->o_ready[t], (blocks_seen - 2) & 1, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
           }
         }
         // Rescale this warp's O rows (the previous PV has landed).
-        if (j > w.j0 && __any_sync(0xffffffffu, resc)) {
+        if (j > unit_j0<C>(w) && __any_sync(0xffffffffu, resc)) {
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < C::kD / 32; ++cc) {

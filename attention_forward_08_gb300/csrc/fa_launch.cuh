@@ -192,6 +192,9 @@ using CfgF32D256  = Cfg<true, 256,  1, 32, 1, 1, 1>;  // smem 224 KB, TMEM 352
 using CfgF16D64   = Cfg<false, 64,  2, 128, 4, 4, 0, true>;
 using CfgF16D128  = Cfg<false, 128, 2, 128, 2, 2, 0, true>;
 using CfgF16D256  = Cfg<false, 256, 1, 128, 1, 1, 0, true>;
+// The same plans with sliding window, softcap and query offset compiled in.
+template <class C>
+using WithFeat = Cfg<C::kTf32, C::kD, C::kNQT, C::kBN, C::kKStages, C::kVStages, C::kVTStages, C::kF16, true>;
 
 int launch_bf16_d64(const LaunchArgs& a);
 int launch_bf16_d128(const LaunchArgs& a);
@@ -202,5 +205,15 @@ int launch_f32_d256(const LaunchArgs& a);
 int launch_f16_d64(const LaunchArgs& a);
 int launch_f16_d128(const LaunchArgs& a);
 int launch_f16_d256(const LaunchArgs& a);
+// Dispatch to the plain or the feature instantiation of a plan.
+int launch_feat_bf16_d64(const LaunchArgs& a);
+int launch_feat_bf16_d128(const LaunchArgs& a);
+int launch_feat_bf16_d256(const LaunchArgs& a);
+int launch_feat_f32_d64(const LaunchArgs& a);
+int launch_feat_f32_d128(const LaunchArgs& a);
+int launch_feat_f32_d256(const LaunchArgs& a);
+int launch_feat_f16_d64(const LaunchArgs& a);
+int launch_feat_f16_d128(const LaunchArgs& a);
+int launch_feat_f16_d256(const LaunchArgs& a);
 
 }  // namespace fa
