@@ -8,6 +8,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -35,6 +36,7 @@ unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
 int g_num_sms[kMaxDevices] = {0};
 long long g_timeout_cycles = 0;  // 0: not yet initialised
 int g_max_ctas = 0;              // 0: one CTA per SM
+int g_q_tiles = 0;               // 0: choose per call; 1 or 2: Q tiles per CTA for bf16/fp16 D <= 128
 EncodeTiledFn g_encode = nullptr;
 bool g_encode_tried = false;
 
@@ -264,6 +266,19 @@ int fa_fwd_ex(const fa_fwd_args* a) {
   }
 
   const bool feat = a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f;
+  // bf16 / fp16 at D <= 128 (no window, softcap or offset): one Q tile per CTA
+  // when the two-tile work units cannot occupy every SM.
+  bool one_tile = false;
+  if (!feat && a->dtype != FA_DTYPE_F32 && a->D <= 128) {
+    int policy;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      policy = g_q_tiles;
+    }
+    const long long units2 = (long long)((a->qL + 255) / 256) * a->B * a->H_q;
+    const int sms = la.max_ctas > 0 ? std::min(la.max_ctas, la.num_sms) : la.num_sms;
+    one_tile = policy == 1 || (policy == 0 && units2 < sms);
+  }
   switch (a->dtype) {
     case FA_DTYPE_F32:
       if (feat)
@@ -272,13 +287,17 @@ int fa_fwd_ex(const fa_fwd_args* a) {
         rc = a->D == 64 ? launch_f32_d64(la) : a->D == 128 ? launch_f32_d128(la) : launch_f32_d256(la);
       break;
     case FA_DTYPE_F16:
-      if (feat)
+      if (one_tile)
+        rc = a->D == 64 ? launch_q1_f16_d64(la) : launch_q1_f16_d128(la);
+      else if (feat)
         rc = a->D == 64 ? launch_feat_f16_d64(la) : a->D == 128 ? launch_feat_f16_d128(la) : launch_feat_f16_d256(la);
       else
         rc = a->D == 64 ? launch_f16_d64(la) : a->D == 128 ? launch_f16_d128(la) : launch_f16_d256(la);
       break;
     default:
-      if (feat)
+      if (one_tile)
+        rc = a->D == 64 ? launch_q1_bf16_d64(la) : launch_q1_bf16_d128(la);
+      else if (feat)
         rc = a->D == 64 ? launch_feat_bf16_d64(la) : a->D == 128 ? launch_feat_bf16_d128(la)
                                                                   : launch_feat_bf16_d256(la);
       else
@@ -362,6 +381,11 @@ int fa_sync_status(void* stream) {
 void fa_set_timeout_cycles(long long cycles) {
   std::lock_guard<std::mutex> lk(fa::g_mu);
   fa::g_timeout_cycles = cycles > 0 ? cycles : fa::kDefaultTimeout;
+}
+
+void fa_set_q_tiles(int n) {
+  std::lock_guard<std::mutex> lk(fa::g_mu);
+  fa::g_q_tiles = (n == 1 || n == 2) ? n : 0;
 }
 
 void fa_set_max_ctas(int n) {

@@ -192,6 +192,13 @@ using CfgF32D256  = Cfg<true, 256,  1, 32, 1, 1, 1>;  // smem 224 KB, TMEM 352
 using CfgF16D64   = Cfg<false, 64,  2, 128, 4, 4, 0, true>;
 using CfgF16D128  = Cfg<false, 128, 2, 128, 2, 2, 0, true>;
 using CfgF16D256  = Cfg<false, 256, 1, 128, 1, 1, 0, true>;
+// One Q tile per CTA (S and P in their own TMEM columns, S_{j+1} overlapping
+// softmax j) for bf16 / fp16 D 64 and 128: chosen when two-tile work units
+// cannot fill the GPU, since a one-tile unit's block chain is shorter.
+using CfgBf16D64Q1  = Cfg<false, 64,  1, 128, 4, 4>;        // smem 176 KB (incl. mask slot), TMEM 320
+using CfgBf16D128Q1 = Cfg<false, 128, 1, 128, 2, 2>;        // smem 192 KB, TMEM 384
+using CfgF16D64Q1   = Cfg<false, 64,  1, 128, 4, 4, 0, true>;
+using CfgF16D128Q1  = Cfg<false, 128, 1, 128, 2, 2, 0, true>;
 // The same plans with sliding window, softcap and query offset compiled in.
 template <class C>
 using WithFeat = Cfg<C::kTf32, C::kD, C::kNQT, C::kBN, C::kKStages, C::kVStages, C::kVTStages, C::kF16, true>;
@@ -205,6 +212,10 @@ int launch_f32_d256(const LaunchArgs& a);
 int launch_f16_d64(const LaunchArgs& a);
 int launch_f16_d128(const LaunchArgs& a);
 int launch_f16_d256(const LaunchArgs& a);
+int launch_q1_bf16_d64(const LaunchArgs& a);
+int launch_q1_bf16_d128(const LaunchArgs& a);
+int launch_q1_f16_d64(const LaunchArgs& a);
+int launch_q1_f16_d128(const LaunchArgs& a);
 // Dispatch to the plain or the feature instantiation of a plan.
 int launch_feat_bf16_d64(const LaunchArgs& a);
 int launch_feat_bf16_d128(const LaunchArgs& a);

@@ -26,6 +26,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED
                 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_set_max_ctas",
+            "fa_set_q_tiles",
             "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_noalloc", "fa_version")
 
 
@@ -78,6 +79,8 @@ def load_library(path: str = LIB_PATH):
     lib.fa_set_timeout_cycles.argtypes = [ctypes.c_longlong]
     lib.fa_set_max_ctas.restype = None
     lib.fa_set_max_ctas.argtypes = [ctypes.c_int]
+    lib.fa_set_q_tiles.restype = None
+    lib.fa_set_q_tiles.argtypes = [ctypes.c_int]
     lib.fa_version.restype = ctypes.c_int
     lib.fa_version.argtypes = []
     lib.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
@@ -124,6 +127,10 @@ def fa_set_timeout_cycles(cycles: int) -> None:
 
 def fa_set_max_ctas(n: int) -> None:
     load_library().fa_set_max_ctas(int(n))
+
+
+def fa_set_q_tiles(n: int) -> None:
+    load_library().fa_set_q_tiles(int(n))
 
 
 def fa_version() -> int:

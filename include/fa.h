@@ -145,6 +145,15 @@ void fa_set_timeout_cycles(long long cycles);
 void fa_set_max_ctas(int n);
 
 /*
+ * fa_set_q_tiles -- for bf16 / fp16 I/O at D <= 128 without window, softcap
+ * or offset, each CTA owns two 128-row Q tiles (their softmax ping-pongs on
+ * the tensor core) unless that leaves SMs without work, in which case it
+ * owns one (shorter per-unit critical path).  n = 1 or 2 forces that choice,
+ * any other value restores the automatic one.  Results do not depend on it.
+ */
+void fa_set_q_tiles(int n);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
  * B * H_q * qL query rows: one fp32 D_i = rowsum(O_i * dO_i) per row, rounded
  * up to 256 bytes.  Returns -1 for non-positive sizes.

@@ -31,7 +31,7 @@ def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
         ["fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc", "fa_last_error",
          "fa_sync_status",
-         "fa_set_max_ctas", "fa_set_timeout_cycles", "fa_version"])
+         "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_timeout_cycles", "fa_version"])
 
 
 def test_library_exports_every_declared_symbol(fa):

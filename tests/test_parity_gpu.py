@@ -71,6 +71,22 @@ def test_small_elementwise(w):
     _run_small(w)
 
 
+# bf16 / fp16 at D <= 128 run with two Q tiles per CTA, or one when two-tile
+# units cannot fill the GPU (every small case above): force each plan.
+TWO_PLANS = [w for w in SMALL if w.dtype in ("bf16", "f16") and w.D <= 128]
+
+
+@pytest.mark.parametrize("q_tiles", [1, 2])
+@pytest.mark.parametrize("w", TWO_PLANS, ids=lambda w: w.name)
+def test_small_both_tile_plans(w, q_tiles):
+    import attention_forward_08_gb300 as fa
+    fa.fa_set_q_tiles(q_tiles)
+    try:
+        _run_small(w)
+    finally:
+        fa.fa_set_q_tiles(0)
+
+
 # Sliding window, softcap and query offset on every kernel plan (two Q tiles,
 # one Q tile, TF32, masks).  Softcaps of 1.5-4 against N(0,1) inputs with a
 # raised scale make the cap bend most scores.
@@ -210,12 +226,16 @@ PERSISTENT = [
 
 @pytest.mark.parametrize("max_ctas", [1, 3])
 @pytest.mark.parametrize("w", PERSISTENT, ids=lambda w: w.name)
-def test_persistent_many_units_per_cta(w, max_ctas):
+@pytest.mark.parametrize("q_tiles", [0, 1])
+def test_persistent_many_units_per_cta(w, max_ctas, q_tiles):
     """The kernel is persistent: with the CTA count capped, each CTA walks many work units
-    (down to one CTA doing all of them), carrying its barrier phases from unit to unit."""
+    (down to one CTA doing all of them), carrying its barrier phases from unit to unit; with
+    the one-Q-tile plan forced as well where it exists."""
     import attention_forward_08_gb300 as fa
     fa.fa_set_max_ctas(max_ctas)
+    fa.fa_set_q_tiles(q_tiles)
     try:
         _run_small(w)
     finally:
         fa.fa_set_max_ctas(0)
+        fa.fa_set_q_tiles(0)
