@@ -278,11 +278,19 @@ __device__ __forceinline__ void transpose_v_tile(const uint8_t* src, uint8_t* ds
   }
 }
 
+// Fold two additive mask values into a pair of scores: s += m * f, with
+// f = 1 / scale while the scores are raw (the softmax's scale * log2(e)
+// factor then covers mask and score alike) or f = log2(e) once they are
+// scaled to base 2 (after a softcap, or for a non-positive scale).
+__device__ __forceinline__ void fold_add2(float& s0, float& s1, float m0, float m1, float f) {
+  ffma2(s0, s1, m0, m1, f, f, s0, s1);
+}
+
 // Load 32 mask entries [k0, k0+32) of one row and fold them into s[off .. off+32):
-// additive: s += mask * log2(e) (s already scaled to base 2); bool: s = -inf
-// where the mask is zero.  Keys >= kL are left alone (cut by the tail limit).
+// additive: fold_add2; bool: s = -inf where the mask is zero.  Keys >= kL are
+// left alone (cut by the tail limit).
 template <class C, int kMaskKind>
-__device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, int k0, int kL, bool vec) {
+__device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, int k0, int kL, bool vec, float f) {
   if constexpr (kMaskKind == 1) {
     const uint8_t* mrow = static_cast<const uint8_t*>(mrow_v);
     if (vec && k0 + 32 <= kL) {
@@ -310,15 +318,13 @@ __device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, in
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const float4 w = __ldg(m4 + v);
-          s[v * 4 + 0] = fmaf(w.x, kLog2e, s[v * 4 + 0]);
-          s[v * 4 + 1] = fmaf(w.y, kLog2e, s[v * 4 + 1]);
-          s[v * 4 + 2] = fmaf(w.z, kLog2e, s[v * 4 + 2]);
-          s[v * 4 + 3] = fmaf(w.w, kLog2e, s[v * 4 + 3]);
+          fold_add2(s[v * 4 + 0], s[v * 4 + 1], w.x, w.y, f);
+          fold_add2(s[v * 4 + 2], s[v * 4 + 3], w.z, w.w, f);
         }
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (k0 + e < kL) s[e] = fmaf(__ldg(mrow + k0 + e), kLog2e, s[e]);
+          if (k0 + e < kL) s[e] = fmaf(__ldg(mrow + k0 + e), f, s[e]);
       }
     } else {
       const uint16_t* mrow = static_cast<const uint16_t*>(mrow_v);
@@ -329,15 +335,14 @@ __device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, in
           const uint4 w = __ldg(m4 + v);
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float mv = half_bits_to_f32<C::kF16>((e & 1) ? (ws[e >> 1] >> 16) : ws[e >> 1]);
-            s[v * 8 + e] = fmaf(mv, kLog2e, s[v * 8 + e]);
-          }
+          for (int e = 0; e < 8; e += 2)
+            fold_add2(s[v * 8 + e], s[v * 8 + e + 1], half_bits_to_f32<C::kF16>(ws[e >> 1]),
+                      half_bits_to_f32<C::kF16>(ws[e >> 1] >> 16), f);
         }
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (k0 + e < kL) s[e] = fmaf(half_bits_to_f32<C::kF16>(__ldg(mrow + k0 + e)), kLog2e, s[e]);
+          if (k0 + e < kL) s[e] = fmaf(half_bits_to_f32<C::kF16>(__ldg(mrow + k0 + e)), f, s[e]);
       }
     }
   }
@@ -347,7 +352,7 @@ __device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, in
 // additive values in kBN/64 column blocks, or 1-byte bool values in one) into
 // s, like fold_mask_chunk does from global memory.
 template <class C>
-__device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t* tile, int kind, int tl) {
+__device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t* tile, int kind, int tl, float f) {
   if (kind == 1) {
 #pragma unroll
     for (int c = 0; c < C::kBN / 16; ++c) {  // 16 keys per 16-byte unit
@@ -365,10 +370,9 @@ __device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t
                                                       (((c % 8) ^ (tl & 7)) << 4));
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float mv = half_bits_to_f32<C::kF16>((e & 1) ? (ws[e >> 1] >> 16) : ws[e >> 1]);
-        s[c * 8 + e] = fmaf(mv, kLog2e, s[c * 8 + e]);
-      }
+      for (int e = 0; e < 8; e += 2)
+        fold_add2(s[c * 8 + e], s[c * 8 + e + 1], half_bits_to_f32<C::kF16>(ws[e >> 1]),
+                  half_bits_to_f32<C::kF16>(ws[e >> 1] >> 16), f);
     }
   }
 }
@@ -376,11 +380,12 @@ __device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t
 template <class C>
 __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p, int b, int h, int row, int kbase,
                                            const uint8_t* mask_tile, int tl) {
-  // Scores to base 2 first when the mask is additive, a softcap applies or the
-  // scale is not positive.  The softcap c * tanh(y) (y = scale * s / c) uses
-  // tanh(y) = 1 - 2 / (2^(2 log2(e) y) + 1): one ex2 and one reciprocal, exact
-  // limits +-1 when the power overflows or underflows, and an absolute error
-  // of a few fp32 ulps of 1 near y = 0 (what the capped score needs).
+  // Scores to base 2 first when a softcap applies, the scale is not positive,
+  // or an additive mask meets either.  The softcap c * tanh(y) (y = scale * s
+  // / c) uses tanh(y) = 1 - 2 / (2^(2 log2(e) y) + 1): one ex2 and one
+  // reciprocal, exact limits +-1 when the power overflows or underflows, and
+  // an absolute error of a few fp32 ulps of 1 near y = 0 (what the capped
+  // score needs).
   if (p.pre_scale) {
     if (C::kFeat && p.softcap_on) {
       const float kin = 2.0f * kLog2e * p.softcap_in, cout = p.softcap_out;
@@ -391,8 +396,9 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
       for (int c = 0; c < C::kBN; ++c) s[c] *= p.scale_log2;
     }
   }
+  const float f = p.mask_natural ? p.inv_scale : kLog2e;  // additive mask factor
   if constexpr (C::kMaskSlotBytes > 0) {
-    if (mask_tile) fold_mask_smem<C>(s, mask_tile, p.mask_kind, tl);
+    if (mask_tile) fold_mask_smem<C>(s, mask_tile, p.mask_kind, tl, f);
   }
   if (p.mask_kind != 0 && row < p.qL && !(C::kMaskSlotBytes > 0 && mask_tile)) {
     const size_t esz = (p.mask_kind == 1) ? 1 : C::kEsz;
@@ -402,9 +408,9 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
 #pragma unroll
     for (int cc = 0; cc < C::kBN / 32; ++cc) {
       if (p.mask_kind == 1)
-        fold_mask_chunk<C, 1>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec);
+        fold_mask_chunk<C, 1>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec, f);
       else
-        fold_mask_chunk<C, 2>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec);
+        fold_mask_chunk<C, 2>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec, f);
     }
   }
   // Causal, tail and window limits: key kbase + c is allowed iff lo <= c < lim.
@@ -412,9 +418,11 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
   int lim = p.kL - kbase;
   if (p.causal) lim = min(lim, diag + 1);
   const int lo = (C::kFeat && p.window > 0) ? diag - p.window + 1 : -1;
+  if (lim < C::kBN || lo > 0) {  // most blocks lie wholly inside the limits
 #pragma unroll
-  for (int c = 0; c < C::kBN; ++c)
-    if (c >= lim || c < lo) s[c] = -INFINITY;
+    for (int c = 0; c < C::kBN; ++c)
+      if (c >= lim || c < lo) s[c] = -INFINITY;
+  }
 }
 
 // Row max of s (raw or base-2 scores): three-input max, four chains.

@@ -119,7 +119,12 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.softcap_out = p.softcap_on ? a.softcap * kLog2e : 0.0f;
   p.window = a.window;
   p.q_offset = a.q_offset;
-  p.pre_scale = (a.mask_kind == 2 || !(a.scale > 0.0f) || p.softcap_on) ? 1 : 0;
+  // An additive mask with a positive scale folds as s + mask / scale, so the
+  // scores stay in raw units and the softmax's own scale * log2(e) factor
+  // applies to both; otherwise scores go to base 2 before the mask.
+  p.mask_natural = (a.mask_kind == 2 && a.scale > 0.0f && !p.softcap_on) ? 1 : 0;
+  p.inv_scale = p.mask_natural ? 1.0f / a.scale : 0.0f;
+  p.pre_scale = ((a.mask_kind == 2 && !p.mask_natural) || !(a.scale > 0.0f) || p.softcap_on) ? 1 : 0;
   p.mask_vec = a.mask_vec;
   p.mask_l2 = mask_l2;
   p.mask_smem = mask_smem;

@@ -22,6 +22,8 @@ struct FaParams {
   int mask_l2;      // a tensor map describes the mask: prefetch its tiles into L2
   int mask_smem;    // the mask map is 128-byte swizzled: TMA-load its tiles into shared memory
   float scale_log2; // scale * log2(e)
+  int mask_natural; // additive mask, scale > 0, no softcap: fold s + mask / scale (raw score units)
+  float inv_scale;  // 1 / scale (when mask_natural)
   int window;       // > 0: key j allowed only if j > i + q_offset - window (sliding window)
   int q_offset;     // causal diagonal of row i is key i + q_offset (0: top-left aligned)
   int softcap_on;   // scores become cap * tanh(scale * s / cap) before any mask
