@@ -59,7 +59,12 @@ def _bind(lib):
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 2 + \
         [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_longlong, ctypes.c_double,
-                                   ctypes.c_longlong, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int]
+                                   ctypes.c_longlong, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint64,
+                                   ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int]
+    g = lib.oracle_dropout_keep
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_double, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_longlong,
+                  ctypes.c_void_p]
     lib.oracle_mutant_id.restype = ctypes.c_int
     return lib
 
@@ -146,7 +151,8 @@ def _f64(a) -> np.ndarray:
 
 def attention(q, k, v, scale: float, causal: bool = False, mask=None,
               mask_kind: int = 0, rows=None, n_threads: int | None = None,
-              lib=None, window: int = 0, softcap: float = 0.0, q_offset: int = 0):
+              lib=None, window: int = 0, softcap: float = 0.0, q_offset: int = 0,
+              dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """O and L of softmax(scale * q k^T + mask) v in fp64.
 
     q: [B, H_q, qL, D]; k, v: [B, H_kv, kL, D] (any real dtype; widened to
@@ -155,7 +161,9 @@ def attention(q, k, v, scale: float, causal: bool = False, mask=None,
     ``scale`` is used as given (pass the fp32-rounded value the GPU sees).
     window > 0 keeps keys j > i + q_offset - window; softcap > 0 maps each
     scaled score s to softcap * tanh(s / softcap) before the mask; q_offset
-    shifts the causal diagonal (j <= i + q_offset).
+    shifts the causal diagonal (j <= i + q_offset).  dropout_p > 0 scales each
+    weight of O by keep in {0, 1 / (1 - p)} from the counter-based generator
+    keyed by seed at counter offset + position / 4; L is unchanged.
     rows: optional iterable of flat row indices (b*H_q + h)*qL + i.
     Returns (O, L): O [B,H_q,qL,D] and L [B,H_q,qL], or [n,D] and [n] for rows.
     """
@@ -191,7 +199,16 @@ def attention(q, k, v, scale: float, causal: bool = False, mask=None,
     rc = lib.oracle_attention_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr,
                                  int(mask_kind), o.ctypes.data, lse.ctypes.data,
                                  B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)),
-                                 int(window), float(softcap), int(q_offset), rptr, n, int(n_threads))
+                                 int(window), float(softcap), int(q_offset), float(dropout_p), int(seed),
+                                 int(offset), rptr, n, int(n_threads))
     if rc != 0:
         raise ValueError("oracle_attention rejected its arguments")
     return o, lse
+
+
+def dropout_keep(p: float, seed: int, offset: int, first: int, n: int, lib=None):
+    """The generator's multipliers (1 / (1 - p) or 0) of n consecutive positions from `first`."""
+    lib = lib or load()
+    out = np.empty(n, dtype=np.float64)
+    lib.oracle_dropout_keep(float(p), int(seed), int(offset), int(first), int(n), out.ctypes.data)
+    return out

@@ -13,6 +13,9 @@
  *   softcap > 0:  s_ij = softcap * tanh(s_ij / softcap)  (before any mask)
  *   allowed  = (!causal || j <= i + q_offset)            causal; q_offset 0 = top-left
  *   window > 0:   allowed &= (j > i + q_offset - window)  sliding window of `window` keys
+ *   dropout p > 0: O_i = sum_j P_ij * keep_ij * v_j with P the softmax row above
+ *                  (its l uses every allowed key) and keep_ij = 1 / (1 - p) or 0
+ *                  from a counter-based generator (below); L is unchanged.
  *   bool mask:      allowed &= (mask[b,h,i,j] != 0)      nonzero = keep
  *   additive mask:  s_ij += mask[b,h,i,j];  allowed &= (s_ij != -inf)
  *   S_ij     = allowed ? s_ij : -inf                     (the full score row)
@@ -36,6 +39,13 @@
  *    key ("matching the public masked_softmax"); causal keeps token <= row.
  *  - oxibonsai "dit_attention_flash.rs", module doc: full-row max-subtracted
  *    softmax is the CPU reference the flash kernel must match.
+ *
+ * Dropout generator (ruDNN "dense_attention.rs", functions `keep` and
+ * `keep_global`): position = ((b*Hq + h)*qL + i)*kL + j; the Philox4x32-10
+ * block cipher (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+ * as 1, 2, 3", SC11) with key (seed_lo, seed_hi) and counter (low 64 bits =
+ * offset + position / 4, high 64 bits = 0); word position % 4 of its output,
+ * u = (word >> 8) * 2^-24; keep iff u >= p (p = 1 drops everything).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - a fully masked row has L = -inf (the empty logsumexp); forge writes 0.
@@ -72,12 +82,52 @@ typedef struct {
     long long window;            /* 0: off */
     double softcap;              /* <= 0: off */
     long long q_offset;
+    double dropout_p;            /* 0: off */
+    uint64_t seed, offset;       /* dropout generator key and counter offset */
     const long long *rows;       /* optional list of flat rows ((b*Hq+h)*qL+i) */
     long long n_rows;
     long long row_begin, row_end;/* this worker's slice of [0, n_rows) */
     double *scratch;             /* kL doubles for the score row */
     int status;
 } oracle_job;
+
+/* Philox4x32-10: ten rounds of the published round function (multipliers
+ * 0xD2511F53 and 0xCD9E8D57 on words 0 and 2, Weyl key increments 0x9E3779B9
+ * and 0xBB67AE85). */
+static void philox4x32_10(const uint32_t ctr[4], uint32_t k0, uint32_t k1, uint32_t out[4])
+{
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * x0;
+        const uint64_t p2 = (uint64_t)0xCD9E8D57u * x2;
+        const uint32_t y0 = (uint32_t)(p2 >> 32) ^ x1 ^ k0;
+        const uint32_t y1 = (uint32_t)p2;
+        const uint32_t y2 = (uint32_t)(p0 >> 32) ^ x3 ^ k1;
+        const uint32_t y3 = (uint32_t)p0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* The dropout multiplier of one (b, h, i, j) position: 1 / (1 - p) or 0. */
+static double dropout_keep(const oracle_job *J, uint64_t position)
+{
+    if (J->dropout_p >= 1.0) return 0.0;
+    const uint64_t ctr64 = J->offset + position / 4;
+    const uint32_t ctr[4] = {(uint32_t)ctr64, (uint32_t)(ctr64 >> 32), 0u, 0u};
+    uint32_t out[4];
+    philox4x32_10(ctr, (uint32_t)J->seed, (uint32_t)(J->seed >> 32), out);
+    const double u = (double)(out[position % 4] >> 8) / 16777216.0;
+#if ORACLE_MUTANT == 12
+    return u < J->dropout_p ? 1.0 / (1.0 - J->dropout_p) : 0.0;   /* mistake: keep test inverted */
+#elif ORACLE_MUTANT == 13
+    return u >= J->dropout_p ? 1.0 : 0.0;                         /* mistake: kept weights not rescaled */
+#else
+    return u >= J->dropout_p ? 1.0 / (1.0 - J->dropout_p) : 0.0;
+#endif
+}
 
 static void oracle_row(const oracle_job *J, long long flat, long long out_index, double *S)
 {
@@ -169,8 +219,9 @@ static void oracle_row(const oracle_job *J, long long flat, long long out_index,
     for (long long j = 0; j < kL; ++j) l += exp(S[j] - m);
     for (long long d = 0; d < D; ++d) oi[d] = 0.0;
     for (long long j = 0; j < kL; ++j) {
-        const double p = exp(S[j] - m);
+        double p = exp(S[j] - m);
         if (p == 0.0) continue;                    /* exp(-inf) = 0 contributes nothing */
+        if (J->dropout_p > 0.0) p *= dropout_keep(J, (uint64_t)(flat * kL + j));
         for (long long d = 0; d < D; ++d) oi[d] += p * vb[j * D + d];
     }
 #if ORACLE_MUTANT != 8
@@ -202,7 +253,8 @@ static void *oracle_worker(void *arg)
  * rows == NULL: every row is computed; o is [B*Hq*qL, D] and lse [B*Hq*qL].
  * rows != NULL: only the n_rows listed flat rows ((b*Hq + h)*qL + i) are
  * computed; o is [n_rows, D] and lse [n_rows], in list order.
- * window (0 = off), softcap (<= 0 = off) and q_offset as in the header.
+ * window (0 = off), softcap (<= 0 = off), q_offset and dropout (p = 0 off,
+ * seed, offset) as in the header.
  * n_threads <= 0 means one thread.  Returns 0, or -1 on a bad argument.
  */
 int oracle_attention_ex(const double *q, const double *k, const double *v,
@@ -210,10 +262,12 @@ int oracle_attention_ex(const double *q, const double *k, const double *v,
                         long long B, long long Hq, long long Hkv, long long qL,
                         long long kL, long long D, double scale, int causal,
                         long long window, double softcap, long long q_offset,
+                        double dropout_p, uint64_t seed, uint64_t offset,
                         const long long *rows, long long n_rows, int n_threads)
 {
     if (!q || !k || !v || !o || !lse) return -1;
     if (window < 0) return -1;
+    if (!(dropout_p >= 0.0 && dropout_p <= 1.0)) return -1;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || qL <= 0 || kL <= 0 || D <= 0) return -1;
     if (Hq % Hkv != 0) return -1;
     if (mask_kind < 0 || mask_kind > 2) return -1;
@@ -242,6 +296,7 @@ int oracle_attention_ex(const double *q, const double *k, const double *v,
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->qL = qL; J->kL = kL; J->D = D;
         J->scale = scale; J->causal = causal; J->rows = rows; J->n_rows = total;
         J->window = window; J->softcap = softcap; J->q_offset = q_offset;
+        J->dropout_p = dropout_p; J->seed = seed; J->offset = offset;
         J->row_begin = total * t / n_threads;
         J->row_end = total * (t + 1) / n_threads;
         J->scratch = scratch + (size_t)kL * (size_t)t;
@@ -268,7 +323,18 @@ int oracle_attention(const double *q, const double *k, const double *v,
                      const long long *rows, long long n_rows, int n_threads)
 {
     return oracle_attention_ex(q, k, v, mask, mask_kind, o, lse, B, Hq, Hkv, qL, kL, D, scale, causal,
-                               0, 0.0, 0, rows, n_rows, n_threads);
+                               0, 0.0, 0, 0.0, 0, 0, rows, n_rows, n_threads);
+}
+
+/* The dropout multipliers of `n` consecutive positions starting at `first`
+ * (for tests of the generator itself). */
+int oracle_dropout_keep(double p, uint64_t seed, uint64_t offset, uint64_t first, long long n, double *out)
+{
+    oracle_job J;
+    memset(&J, 0, sizeof(J));
+    J.dropout_p = p; J.seed = seed; J.offset = offset;
+    for (long long t = 0; t < n; ++t) out[t] = dropout_keep(&J, first + (uint64_t)t);
+    return 0;
 }
 
 /* Number of the planted mistake this build carries (0 for the real oracle). */

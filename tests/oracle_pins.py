@@ -336,6 +336,66 @@ def pin_softcap_large_cap(attn):
     _close(l1, l0, 1e-9, "softcap 1e6 L")
 
 
+# --------------------------------------------------------------------------- dropout
+
+def _dropout_inputs(seed):
+    r = _rng(seed)
+    B, Hq, Hkv, qL, kL, D = 1, 2, 1, 6, 12, 4
+    return (r.standard_normal((B, Hq, qL, D)), r.standard_normal((B, Hkv, kL, D)),
+            r.standard_normal((B, Hkv, kL, D)))
+
+
+def pin_dropout_p0_and_p1(attn):
+    """p = 0 is the plain forward bit for bit; p = 1 drops every weight (O = 0) and leaves L alone."""
+    q, k, v = _dropout_inputs(30)
+    o0, l0 = attn(q, k, v, 0.5, causal=True)
+    o1, l1 = attn(q, k, v, 0.5, causal=True, dropout_p=0.0, seed=99, offset=5)
+    _close(o1, o0, 0.0, "p=0 O")
+    _close(l1, l0, 0.0, "p=0 L")
+    o2, l2 = attn(q, k, v, 0.5, causal=True, dropout_p=1.0, seed=99, offset=5)
+    assert np.all(o2 == 0.0), "p=1 must drop every weight"
+    _close(l2, l0, 0.0, "p=1 L")
+
+
+def pin_dropout_keep_rate():
+    """The generator keeps a fraction 1 - p of positions (binomial bounds) with multipliers {0, 1/(1-p)}."""
+    import oracle
+    for p, seed, offset in ((0.2, 7, 0), (0.65, 2 ** 40 + 3, 2 ** 33 - 5)):
+        n = 400_000
+        keep = oracle.dropout_keep(p, seed, offset, 12345, n)
+        assert set(np.unique(keep)) <= {0.0, 1.0 / (1.0 - p)}, "multipliers must be 0 or 1/(1-p)"
+        frac = float(np.mean(keep > 0))
+        sd = math.sqrt(p * (1 - p) / n)
+        assert abs(frac - (1 - p)) < 6 * sd, f"keep rate {frac:.5f} for p={p}"
+
+
+def pin_dropout_unbiased(attn):
+    """Averaged over many seeds, the dropped-out O converges to the plain O (the 1/(1-p) rescale)."""
+    q, k, v = _dropout_inputs(31)
+    o0, _ = attn(q, k, v, 0.5, causal=True)
+    samples = np.stack([attn(q, k, v, 0.5, causal=True, dropout_p=0.3, seed=1000 + t)[0] for t in range(400)])
+    mean, sd = samples.mean(axis=0), samples.std(axis=0) / math.sqrt(len(samples))
+    assert np.all(np.abs(mean - o0) <= 6 * sd + 1e-12), "dropout is biased"
+
+
+def pin_dropout_position_map(attn):
+    """O rebuilt from the plain softmax weights and the generator at position ((b H_q + h) qL + i) kL + j."""
+    import oracle
+    q, k, v = _dropout_inputs(32)
+    B, Hq, qL, D = q.shape
+    kL = k.shape[2]
+    scale, p, seed, offset = 0.5, 0.4, 77, 2 ** 35 + 1
+    o, lse = attn(q, k, v, scale, causal=False, dropout_p=p, seed=seed, offset=offset)
+    group = Hq // k.shape[1]
+    for h in range(Hq):
+        sc = scale * q[0, h] @ k[0, h // group].T
+        w = np.exp(sc - sc.max(axis=1, keepdims=True))
+        w /= w.sum(axis=1, keepdims=True)
+        for i in range(qL):
+            keep = oracle.dropout_keep(p, seed, offset, ((0 * Hq + h) * qL + i) * kL, kL)
+            _close(o[0, h, i], (w[i] * keep) @ v[0, h // group], 1e-12, f"dropout row {h},{i}")
+
+
 def pin_bruteforce_decimal(attn):
     """50-digit decimal brute force on tiny inputs, every feature switched on in turn."""
     r = _rng(9)
@@ -500,4 +560,7 @@ ALL_PINS = [
     pin_key_permutation, pin_additive_shift, pin_linear_in_v, pin_gqa_equals_repeated_mha,
     pin_mask_kind_equivalences, pin_rows_subset, pin_bruteforce_decimal_window_softcap_offset,
     pin_window_of_one_key, pin_window_equal_scores, pin_q_offset_is_a_suffix, pin_softcap_large_cap,
+    pin_dropout_p0_and_p1, pin_dropout_unbiased, pin_dropout_position_map,
 ]
+# Pins of the generator alone (no attention callable).
+GENERATOR_PINS = [pin_dropout_keep_rate]

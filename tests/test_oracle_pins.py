@@ -9,7 +9,7 @@ import functools
 import pytest
 
 import oracle
-from oracle_pins import ALL_PINS
+from oracle_pins import ALL_PINS, GENERATOR_PINS
 
 
 def _attn(lib):
@@ -34,6 +34,8 @@ MUTANTS = {
     9: "softcap not multiplied back",
     10: "query offset sign",
     11: "window one key too wide",
+    12: "dropout keep test inverted",
+    13: "dropout weights not rescaled",
 }
 
 
@@ -49,6 +51,11 @@ def test_pins_catch_planted_mistake(mutant, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin catches mutant {mutant} ({MUTANTS[mutant]})"
+
+
+@pytest.mark.parametrize("pin", GENERATOR_PINS, ids=lambda p: p.__name__)
+def test_generator_pin(pin, oracle_lib):
+    pin()
 
 
 def test_oracle_rejects_bad_arguments(oracle_lib):
