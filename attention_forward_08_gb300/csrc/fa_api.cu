@@ -134,6 +134,14 @@ int validate(const fa_fwd_args* a) {
     set_error("softcap must be finite and >= 0 (0 = off)");
     return FA_ERR_INVALID_ARGUMENT;
   }
+  if (!(a->dropout_p >= 0.0f && a->dropout_p <= 1.0f)) {
+    set_error("dropout_p must lie in [0, 1]");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->dropout_p > 0.0f && a->kL % 4 != 0) {
+    set_error("dropout needs kL (%d) to be a multiple of 4", a->kL);
+    return FA_ERR_UNSUPPORTED;
+  }
   if (a->D != 64 && a->D != 128 && a->D != 256) {
     set_error("head dim D = %d is not supported (64, 128 or 256)", a->D);
     return FA_ERR_UNSUPPORTED;
@@ -242,6 +250,9 @@ int fa_fwd_ex(const fa_fwd_args* a) {
   la.window = a->window;
   la.q_offset = a->q_offset;
   la.softcap = a->softcap;
+  la.dropout_p = a->dropout_p;
+  la.dropout_seed = a->dropout_seed;
+  la.dropout_offset = a->dropout_offset;
   for (int i = 0; i < 3; ++i) {
     la.qs[i] = a->q_strides[i];
     la.ks[i] = a->k_strides[i];
@@ -265,7 +276,7 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     la.max_ctas = g_max_ctas;
   }
 
-  const bool feat = a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f;
+  const bool feat = a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f || a->dropout_p != 0.0f;
   // bf16 / fp16 at D <= 128 (no window, softcap or offset): one Q tile per CTA
   // when the two-tile work units cannot occupy every SM.
   bool one_tile = false;
@@ -479,6 +490,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   return launch_bwd(a);
 }
 
-int fa_version(void) { return 103; }
+int fa_version(void) { return 104; }
 
 }  // extern "C"

@@ -475,6 +475,77 @@ __device__ __forceinline__ void p_pass(const float (&s)[C::kBN], float sl, float
   if constexpr (kWithMax) mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
 }
 
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC11): ten rounds of the
+// published round function on the counter (c0, c1, 0, 0) with key (k0, k1).
+// Not inlined: one instance at a time keeps the softmax's registers for the
+// scores (the dropout path calls it once per 4 keys).
+static __device__ __noinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
+  uint32_t x0 = c0, x1 = c1, x2 = 0u, x3 = 0u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
+    const uint32_t hi2 = __umulhi(0xCD9E8D57u, x2), lo2 = 0xCD9E8D57u * x2;
+    x0 = hi2 ^ x1 ^ k0;
+    x1 = lo2;
+    x2 = hi0 ^ x3 ^ k1;
+    x3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint4(x0, x1, x2, x3);
+}
+
+// Dropout multipliers of one row's block: position ((b H_q + h) qL + row) kL
+// + key, counter = offset + position / 4, word = position % 4 (kL is a
+// multiple of 4, so a block of 4 keys is one counter).
+struct DropRow {
+  unsigned long long ctr;  // counter of the row's key kbase
+  __device__ __forceinline__ void keep4(const FaParams& p, int group, float (&m)[4]) const {
+    const unsigned long long c = ctr + (unsigned long long)group;
+    const uint4 r = philox_10((uint32_t)c, (uint32_t)(c >> 32), p.seed_lo, p.seed_hi);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m[e] = (w[e] >> 8) >= p.drop_threshold ? p.drop_scale : 0.0f;
+  }
+};
+
+// p_pass with dropout: the same P and sum, but the stored P (what P V
+// reads) carries each key's dropout multiplier; the sum (l) does not.
+template <class C>
+__device__ __forceinline__ void p_pass_dropout(const float (&s)[C::kBN], float sl, float msub, uint32_t tP, float& sum,
+                                               const FaParams& p, const DropRow& dr) {
+  float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int cc = 0; cc < C::kBN / 32; ++cc) {
+    uint32_t pk[C::kTf32 ? 32 : 16];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {  // 8 groups of 4 keys
+      float m[4];
+      dr.keep4(p, cc * 8 + g, m);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int e = 2 * g + hh;  // pair index in the chunk
+        float x0, x1;
+        ffma2(x0, x1, s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1], sl, sl, -msub, -msub);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
+        const float d0 = p0 * m[2 * hh], d1 = p1 * m[2 * hh + 1];
+        if constexpr (C::kTf32) {
+          pk[2 * e] = to_tf32(d0);
+          pk[2 * e + 1] = to_tf32(d1);
+        } else {
+          pk[e] = pack16x2<C>(d0, d1);
+        }
+      }
+    }
+    if constexpr (C::kTf32)
+      tmem_st32(tP + cc * 32, pk);
+    else
+      tmem_st16(tP + cc * 16, pk);
+  }
+  sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+}
+
 // One work unit: kNQT consecutive 128-row Q tiles of one (batch, head).
 struct Unit {
   int b, h, kvh, q0, N;
@@ -1053,7 +1124,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // P = 2^(s*sl - m): fp32 sum, stored to TMEM as bf16 pairs or tf32.
         const uint32_t tP = C::kAliasP ? tS : (tmem + lane_addr + C::kColP + (j & 1) * C::kPCols);
         float sum, unused;
-        p_pass<C, false>(s, sl, msub, tP, sum, unused);
+        if (C::kFeat && p.dropout_on) {
+          const DropRow dr{p.drop_offset +
+                           ((((unsigned long long)b * p.Hq + h) * p.qL + row) * p.kL + kbase) / 4ull};
+          p_pass_dropout<C>(s, sl, msub, tP, sum, p, dr);
+        } else {
+          p_pass<C, false>(s, sl, msub, tP, sum, unused);
+        }
         l_run = l_run * corr + sum;
 
         // Without P over S, o_ready completes once per PV; every phase is

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstring>
 
 #include "fa_kernel.cuh"
@@ -22,6 +23,8 @@ struct LaunchArgs {
   int causal, mask_kind;
   int window, q_offset;  // sliding window (0 = off) and causal diagonal offset
   float softcap;         // 0 = off
+  float dropout_p;       // 0 = off
+  unsigned long long dropout_seed, dropout_offset;
   long long qs[3], ks[3], vs[3], os[3], ms[3];  // element strides: batch, head, row
   int mask_vec;
   cudaStream_t stream;
@@ -117,6 +120,12 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.softcap_on = a.softcap > 0.0f ? 1 : 0;
   p.softcap_in = p.softcap_on ? a.scale / a.softcap : 0.0f;
   p.softcap_out = p.softcap_on ? a.softcap * kLog2e : 0.0f;
+  p.dropout_on = a.dropout_p > 0.0f ? 1 : 0;
+  p.drop_threshold = p.dropout_on ? (unsigned int)std::ceil((double)a.dropout_p * 16777216.0) : 0u;
+  p.drop_scale = a.dropout_p < 1.0f ? (float)(1.0 / (1.0 - (double)a.dropout_p)) : 0.0f;
+  p.seed_lo = (unsigned int)a.dropout_seed;
+  p.seed_hi = (unsigned int)(a.dropout_seed >> 32);
+  p.drop_offset = a.dropout_offset;
   p.window = a.window;
   p.q_offset = a.q_offset;
   // An additive mask with a positive scale folds as s + mask / scale, so the

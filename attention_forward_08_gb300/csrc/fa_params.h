@@ -22,6 +22,11 @@ struct FaParams {
   int mask_l2;      // a tensor map describes the mask: prefetch its tiles into L2
   int mask_smem;    // the mask map is 128-byte swizzled: TMA-load its tiles into shared memory
   float scale_log2; // scale * log2(e)
+  int dropout_on;       // weights of O kept with probability 1 - p (counter-based generator)
+  unsigned int drop_threshold;  // keep iff (word >> 8) >= drop_threshold = ceil(p * 2^24)
+  float drop_scale;     // 1 / (1 - p) (0 when p = 1)
+  unsigned int seed_lo, seed_hi;
+  unsigned long long drop_offset;  // counter of position 0
   int mask_natural; // additive mask, scale > 0, no softcap: fold s + mask / scale (raw score units)
   float inv_scale;  // 1 / scale (when mask_natural)
   int window;       // > 0: key j allowed only if j > i + q_offset - window (sliding window)

@@ -51,6 +51,7 @@ class FaFwdArgs(ctypes.Structure):
         ("mask_strides", ctypes.c_longlong * 3),
         ("stream", ctypes.c_void_p),
         ("window", ctypes.c_int), ("q_offset", ctypes.c_int), ("softcap", ctypes.c_float),
+        ("dropout_p", ctypes.c_float), ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_ulonglong),
     ]
 
 
@@ -165,7 +166,7 @@ def _strides_bhs(t, name):
 
 
 def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind=None, stream=None, window=0,
-              q_offset=0, softcap=0.0) -> FaFwdArgs:
+              q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0) -> FaFwdArgs:
     """Fill ``fa_fwd_args`` from torch CUDA tensors (4-D views with unit inner stride).
 
     q, o: [B, H_q, qL, D]; k, v: [B, H_kv, kL, D]; lse: contiguous [B, H_q, qL]
@@ -202,6 +203,7 @@ def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind
     a.causal = int(bool(causal))
     a.dtype = dtype
     a.window, a.q_offset, a.softcap = int(window), int(q_offset), float(softcap)
+    a.dropout_p, a.dropout_seed, a.dropout_offset = float(dropout_p), int(dropout_seed), int(dropout_offset)
     a.q_strides[:] = _strides_bhs(q, "q")
     a.k_strides[:] = _strides_bhs(k, "k")
     a.v_strides[:] = _strides_bhs(v, "v")
@@ -233,7 +235,7 @@ def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind
 
 
 def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, out=None, lse=None,
-              stream=None, window=0, q_offset=0, softcap=0.0):
+              stream=None, window=0, q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0):
     """O and L for torch CUDA tensors (see ``make_args``); returns (o, lse)."""
     import torch
     B, H_q, qL, D = q.shape
@@ -242,7 +244,8 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
     if lse is None:
         lse = torch.empty((B, H_q, qL), dtype=torch.float32, device=q.device)
     args = make_args(q, k, v, out, lse, scale=scale, causal=causal, mask=mask, mask_kind=mask_kind,
-                     stream=stream, window=window, q_offset=q_offset, softcap=softcap)
+                     stream=stream, window=window, q_offset=q_offset, softcap=softcap, dropout_p=dropout_p,
+                     dropout_seed=dropout_seed, dropout_offset=dropout_offset)
     _check(fa_fwd_ex(args))
     return out, lse
 

@@ -181,7 +181,8 @@ def oracle_sample(w: workloads.Workload, q, k, v, m, seconds: float):
         t0 = time.perf_counter()
         oracle.attention(qo, ko, vo, scale, causal=w.causal, mask=mo, mask_kind=w.mask_kind, rows=rows,
                          n_threads=threads, window=w.window, softcap=float(np.float32(w.softcap)),
-                         q_offset=w.q_offset)
+                         q_offset=w.q_offset, dropout_p=float(np.float32(w.dropout_p)), seed=w.dropout_seed,
+                         offset=w.dropout_offset)
         return rows, time.perf_counter() - t0
 
     n = max(threads, 16)
@@ -255,7 +256,7 @@ def run_reference(args, w):
 
 
 def config_of(w, args):
-    extra = {k: getattr(w, k) for k in ("window", "softcap", "q_offset") if getattr(w, k)}
+    extra = {k: getattr(w, k) for k in ("window", "softcap", "q_offset", "dropout_p") if getattr(w, k)}
     return {"workload": w.name, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv, "seq_len": w.qL, "kL": w.kL, "D": w.D,
             **extra,
             "causal": w.causal, "mask": ["none", "bool", "additive"][w.mask_kind],
@@ -289,7 +290,8 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     fargs = fa.make_args(qd, kd, vd, od, lsed, scale=w.sm_scale, causal=w.causal, mask=md,
                          mask_kind=None if md is None else w.mask_kind, stream=stream.cuda_stream,
-                         window=w.window, q_offset=w.q_offset, softcap=w.softcap)
+                         window=w.window, q_offset=w.q_offset, softcap=w.softcap, dropout_p=w.dropout_p,
+                         dropout_seed=w.dropout_seed, dropout_offset=w.dropout_offset)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def launch():
@@ -448,7 +450,7 @@ def run_ours_bwd(args, w):
     import attention_forward_08_gb300 as fa
     fa.load_library()
     if (w.dtype != "bf16" or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128) or w.window
-            or w.softcap or w.q_offset):
+            or w.softcap or w.q_offset or w.dropout_p):
         raise SystemExit(f"--pass bwd needs a plain (unmasked, no window/softcap/offset) bf16 BHSD workload "
                          f"with D 64 or 128 ({w.name})")
     q, k, v = workloads.make_qkv(w)

@@ -90,6 +90,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  *               any mask (mlx-native `softcapping`); L is the logsumexp of
  *               the capped scores.
  * window must be >= 0, |q_offset| < 2^30, softcap finite and >= 0.
+ *   dropout_p   in [0, 1]; > 0 multiplies each weight P_ij of O by 0 or
+ *               1 / (1 - p) (ruDNN "dense_attention.rs", `keep`): position
+ *               ((b*H_q + h)*qL + i)*kL + j, Philox4x32-10 keyed by
+ *               dropout_seed on the counter dropout_offset + position / 4,
+ *               word position % 4, kept iff (word >> 8) * 2^-24 >= p.  L and
+ *               the softmax normaliser are unaffected.  kL must be a
+ *               multiple of 4 (else FA_ERR_UNSUPPORTED).
  */
 typedef struct fa_fwd_args {
   const void* q;
@@ -113,6 +120,10 @@ typedef struct fa_fwd_args {
   int window;    /* > 0: sliding window, key j allowed only if j > i + q_offset - window */
   int q_offset;  /* causal diagonal of row i is key i + q_offset (0: top-left; kL - qL: bottom-right) */
   float softcap; /* > 0: each scaled score s becomes softcap * tanh(s / softcap), before any mask */
+  /* Added in ABI 1.04 (zero = off): */
+  float dropout_p;                   /* keep each weight of O with probability 1 - p, scaled by 1/(1-p) */
+  unsigned long long dropout_seed;   /* generator key */
+  unsigned long long dropout_offset; /* generator counter of position 0 */
 } fa_fwd_args;
 
 int fa_fwd_ex(const fa_fwd_args* args);

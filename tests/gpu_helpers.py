@@ -30,7 +30,8 @@ def gpu_run(w: workloads.Workload, q, k, v, mask, scale=None):
     lse = torch.full((B, H, qL), float("nan"), dtype=torch.float32, device=dev)
     fa.attention(qd, kd, vd, scale=w.sm_scale if scale is None else scale, causal=w.causal, mask=md,
                  mask_kind=None if mask is None else w.mask_kind, out=o, lse=lse, window=w.window,
-                 q_offset=w.q_offset, softcap=w.softcap)
+                 q_offset=w.q_offset, softcap=w.softcap, dropout_p=w.dropout_p, dropout_seed=w.dropout_seed,
+                 dropout_offset=w.dropout_offset)
     rc = fa.fa_sync_status(None)
     assert rc == 0, f"device status {rc}: {fa.fa_last_error()}"
     if w.layout == "dit":
@@ -40,8 +41,10 @@ def gpu_run(w: workloads.Workload, q, k, v, mask, scale=None):
 
 
 def oracle_features(w: workloads.Workload) -> dict:
-    """The workload's window / softcap / query offset as oracle keyword arguments."""
-    return dict(window=w.window, softcap=float(np.float32(w.softcap)), q_offset=w.q_offset)
+    """The workload's window / softcap / query offset / dropout as oracle keyword arguments
+    (real-valued ones rounded to the fp32 values the GPU receives)."""
+    return dict(window=w.window, softcap=float(np.float32(w.softcap)), q_offset=w.q_offset,
+                dropout_p=float(np.float32(w.dropout_p)), seed=w.dropout_seed, offset=w.dropout_offset)
 
 
 def oracle_inputs(q, k, v, mask):

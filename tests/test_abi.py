@@ -61,7 +61,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 103
+    assert fa.fa_version() == 104
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -114,6 +114,22 @@ def test_misaligned_strides_rejected(fa):
     assert "strides" in fa.fa_last_error()
     a.o_strides[:] = (2 * 64 * 64, 64 * 64, 32)        # rows overlap: stride < D
     assert fa.fa_fwd_ex(a) == 1
+
+
+def test_dropout_arguments_validated(fa):
+    """fa_fwd_ex: dropout_p outside [0, 1] is invalid; dropout with kL not a multiple of 4 is unsupported."""
+    a = fa.FaFwdArgs()
+    a.q = a.k = a.v = a.o = a.lse = P
+    a.B, a.H_q, a.H_kv, a.qL, a.kL, a.D = 1, 2, 2, 64, 64, 64
+    a.scale, a.dtype = 0.125, 1
+    for t in (a.q_strides, a.k_strides, a.v_strides, a.o_strides):
+        t[:] = (2 * 64 * 64, 64 * 64, 64)
+    a.dropout_p = 1.5
+    assert fa.fa_fwd_ex(a) == 1 and "dropout_p" in fa.fa_last_error()
+    a.dropout_p, a.kL = 0.1, 66
+    for t in (a.k_strides, a.v_strides):
+        t[:] = (2 * 66 * 64, 66 * 64, 64)
+    assert fa.fa_fwd_ex(a) == 2 and "multiple of 4" in fa.fa_last_error()
 
 
 def test_no_gpu_is_a_cuda_error(fa):

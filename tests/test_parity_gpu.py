@@ -110,6 +110,26 @@ FEATURES = [
 ]
 
 
+# Dropout (kL a multiple of 4): keep decisions must agree exactly with the
+# oracle's generator, so O compares at the usual bounds; p = 1 gives O = 0.
+DROPOUT = [
+    S("drop_bf16_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "bf16", causal=True, dropout_p=0.1, dropout_seed=7,
+      dropout_offset=3, seed=81),
+    S("drop_bf16_d64_plain", 2, 2, 2, 256, 320, 64, "bf16", dropout_p=0.5, dropout_seed=2 ** 40 + 11, seed=82),
+    S("drop_bf16_d256_additive", 1, 2, 2, 256, 256, 256, "bf16", mask_kind=W.MASK_ADDITIVE, dropout_p=0.25,
+      dropout_seed=5, dropout_offset=2 ** 34, seed=83),
+    S("drop_f32_d128", 1, 2, 2, 300, 300, 128, "f32", dropout_p=0.2, dropout_seed=9, seed=84),
+    S("drop_f16_d64_window_causal", 1, 2, 1, 260, 260, 64, "f16", causal=True, window=100, dropout_p=0.3,
+      dropout_seed=13, dropout_offset=77, seed=85),
+    S("drop_all_bf16_d128", 1, 2, 2, 200, 200, 128, "bf16", causal=True, dropout_p=1.0, dropout_seed=1, seed=86),
+]
+
+
+@pytest.mark.parametrize("w", DROPOUT, ids=lambda w: w.name)
+def test_dropout(w):
+    _run_small(w)
+
+
 @pytest.mark.parametrize("w", FEATURES, ids=lambda w: w.name)
 def test_window_softcap_offset(w):
     """fp32 cases with a raised scale take the TF32 rule of test_unusual_scales: raw scores of

@@ -41,6 +41,9 @@ class Workload:
     window: int = 0        # > 0: sliding window of keys j > i + q_offset - window
     softcap: float = 0.0   # > 0: scores capped as softcap * tanh(s / softcap)
     q_offset: int = 0      # causal diagonal of row i is key i + q_offset
+    dropout_p: float = 0.0  # > 0: weights of O dropped with probability p (counter-based generator)
+    dropout_seed: int = 0
+    dropout_offset: int = 0
 
     @property
     def sm_scale(self) -> float:
@@ -89,7 +92,7 @@ WORKLOADS = {
 BENCH_WORKLOAD = "bf16_gqa_causal_b2_hq32_hkv8_l4096_d128"
 
 # Beyond the pages' workloads: the bench workload with fp16 I/O, with a
-# 1024-key sliding window, and with a softcap of 20 (same seeds).
+# 1024-key sliding window, with a softcap of 20, and with dropout 0.1 (same seeds).
 EXTRA_WORKLOADS = {
     "f16_gqa_causal_b2_hq32_hkv8_l4096_d128": Workload(
         "f16_gqa_causal_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "f16", causal=True, seed=1002),
@@ -99,6 +102,9 @@ EXTRA_WORKLOADS = {
     "bf16_gqa_causal_softcap20_b2_hq32_hkv8_l4096_d128": Workload(
         "bf16_gqa_causal_softcap20_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "bf16", causal=True,
         seed=1002, softcap=20.0),
+    "bf16_gqa_causal_dropout10_b2_hq32_hkv8_l4096_d128": Workload(
+        "bf16_gqa_causal_dropout10_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "bf16", causal=True,
+        seed=1002, dropout_p=0.1, dropout_seed=2024, dropout_offset=0),
 }
 WORKLOADS.update(EXTRA_WORKLOADS)
 
@@ -147,8 +153,10 @@ def make_inputs(w: Workload):
 
 
 def small_case(name, B, H_q, H_kv, qL, kL, D, dtype, causal=False, mask_kind=MASK_NONE,
-               layout="bhsd", seed=7, scale=float("nan"), window=0, softcap=0.0, q_offset=0) -> Workload:
+               layout="bhsd", seed=7, scale=float("nan"), window=0, softcap=0.0, q_offset=0,
+               dropout_p=0.0, dropout_seed=0, dropout_offset=0) -> Workload:
     """A reduced-size workload for element-by-element parity runs."""
     return Workload(name, B, H_q, H_kv, qL, kL, D, dtype, causal=causal, mask_kind=mask_kind,
                     layout=layout, seed=seed, mask_seed=seed + 1000, scale=scale, window=window,
-                    softcap=softcap, q_offset=q_offset)
+                    softcap=softcap, q_offset=q_offset, dropout_p=dropout_p, dropout_seed=dropout_seed,
+                    dropout_offset=dropout_offset)
