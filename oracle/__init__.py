@@ -65,6 +65,9 @@ def _bind(lib):
     g.restype = ctypes.c_int
     g.argtypes = [ctypes.c_double, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_longlong,
                   ctypes.c_void_p]
+    g = lib.oracle_philox4x32_10
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_void_p]
     lib.oracle_mutant_id.restype = ctypes.c_int
     return lib
 
@@ -204,6 +207,16 @@ def attention(q, k, v, scale: float, causal: bool = False, mask=None,
     if rc != 0:
         raise ValueError("oracle_attention rejected its arguments")
     return o, lse
+
+
+def philox4x32_10(counter, key, lib=None):
+    """The four output words of one Philox4x32-10 block (counter: 4 words, key: 2 words)."""
+    lib = lib or load()
+    ctr = np.ascontiguousarray(counter, dtype=np.uint32)
+    assert ctr.shape == (4,)
+    out = np.empty(4, dtype=np.uint32)
+    lib.oracle_philox4x32_10(ctr.ctypes.data, int(key[0]) & 0xFFFFFFFF, int(key[1]) & 0xFFFFFFFF, out.ctypes.data)
+    return out
 
 
 def dropout_keep(p: float, seed: int, offset: int, first: int, n: int, lib=None):

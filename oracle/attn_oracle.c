@@ -105,8 +105,10 @@ static void philox4x32_10(const uint32_t ctr[4], uint32_t k0, uint32_t k1, uint3
         const uint32_t y2 = (uint32_t)(p0 >> 32) ^ x3 ^ k1;
         const uint32_t y3 = (uint32_t)p0;
         x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+#if ORACLE_MUTANT != 14   /* mistake 14: the key is not raised between rounds */
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
+#endif
     }
     out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
 }
@@ -334,6 +336,14 @@ int oracle_dropout_keep(double p, uint64_t seed, uint64_t offset, uint64_t first
     memset(&J, 0, sizeof(J));
     J.dropout_p = p; J.seed = seed; J.offset = offset;
     for (long long t = 0; t < n; ++t) out[t] = dropout_keep(&J, first + (uint64_t)t);
+    return 0;
+}
+
+/* One Philox4x32-10 block: the four output words of counter `ctr` under the
+ * key (k0, k1), for tests of the generator against an independent copy. */
+int oracle_philox4x32_10(const uint32_t *ctr, uint32_t k0, uint32_t k1, uint32_t *out)
+{
+    philox4x32_10(ctr, k0, k1, out);
     return 0;
 }
 

@@ -357,16 +357,59 @@ def pin_dropout_p0_and_p1(attn):
     _close(l2, l0, 0.0, "p=1 L")
 
 
-def pin_dropout_keep_rate():
+def pin_dropout_keep_rate(lib=None):
     """The generator keeps a fraction 1 - p of positions (binomial bounds) with multipliers {0, 1/(1-p)}."""
     import oracle
     for p, seed, offset in ((0.2, 7, 0), (0.65, 2 ** 40 + 3, 2 ** 33 - 5)):
         n = 400_000
-        keep = oracle.dropout_keep(p, seed, offset, 12345, n)
+        keep = oracle.dropout_keep(p, seed, offset, 12345, n, lib=lib)
         assert set(np.unique(keep)) <= {0.0, 1.0 / (1.0 - p)}, "multipliers must be 0 or 1/(1-p)"
         frac = float(np.mean(keep > 0))
         sd = math.sqrt(p * (1 - p) / n)
         assert abs(frac - (1 - p)) < 6 * sd, f"keep rate {frac:.5f} for p={p}"
+
+
+def _triton_philox_words(seeds, offsets):
+    """Philox4x32-10 words from Triton's generator on the CPU (its interpreter), in a child process."""
+    import subprocess
+    import sys
+    try:
+        import triton  # noqa: F401
+    except ImportError:
+        import pytest
+        pytest.skip("triton is not installed: no independent Philox at hand")
+    script = os.path.join(os.path.dirname(os.path.abspath(__file__)), "philox_triton_words.py")
+    req = json.dumps({"seeds": [str(s) for s in seeds], "offsets": [str(o) for o in offsets]})
+    res = subprocess.run([sys.executable, script, req], capture_output=True, text=True, timeout=600,
+                         env=dict(os.environ, TRITON_INTERPRET="1"))
+    assert res.returncode == 0, res.stderr[-2000:]
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def pin_philox_matches_triton(lib=None):
+    """The oracle's Philox4x32-10 block equals Triton's, word for word, and its dropout multipliers are
+    the contract's decision on those words: word (position mod 4) of the block at counter
+    offset + position / 4 (64-bit, carry into the high word), kept iff (word >> 8) / 2^24 >= p."""
+    import oracle
+    M64 = (1 << 64) - 1
+    seeds = [0, 1, 0x1234567890ABCDEF, M64, 2 ** 40 + 3]
+    offsets = [0, 1, 2, 3, 2 ** 31, 2 ** 32 - 1, 2 ** 32, 2 ** 32 + 1, 2 ** 33 - 5, 0xDEADBEEFCAFEF00D, M64 - 1, M64]
+    words = _triton_philox_words(seeds, offsets)
+    for seed, per_seed in zip(seeds, words):
+        for off, ref in zip(offsets, per_seed):
+            got = oracle.philox4x32_10([off & 0xFFFFFFFF, off >> 32, 0, 0], (seed & 0xFFFFFFFF, seed >> 32), lib=lib)
+            assert [int(x) for x in got] == ref, f"Philox block differs at seed {seed:#x}, counter {off:#x}"
+    # the decision chain: position -> counter and word, threshold, multiplier
+    for p, seed, offset, first in ((0.3, 0x1234567890ABCDEF, 2 ** 32 - 3, 5), (0.85, 7, M64 - 2, 0)):
+        n = 40
+        blocks = sorted({(offset + (first + t) // 4) & M64 for t in range(n)})
+        bw = dict(zip(blocks, _triton_philox_words([seed], blocks)[0]))
+        keep = oracle.dropout_keep(p, seed, offset, first, n, lib=lib)
+        for t in range(n):
+            pos = first + t
+            word = bw[(offset + pos // 4) & M64][pos % 4]
+            want = 1.0 / (1.0 - p) if (word >> 8) / 16777216.0 >= p else 0.0
+            assert keep[t] == want, f"multiplier at position {pos}: {keep[t]} vs {want}"
 
 
 def pin_dropout_unbiased(attn):
@@ -563,4 +606,4 @@ ALL_PINS = [
     pin_dropout_p0_and_p1, pin_dropout_unbiased, pin_dropout_position_map,
 ]
 # Pins of the generator alone (no attention callable).
-GENERATOR_PINS = [pin_dropout_keep_rate]
+GENERATOR_PINS = [pin_dropout_keep_rate, pin_philox_matches_triton]

@@ -36,6 +36,7 @@ MUTANTS = {
     11: "window one key too wide",
     12: "dropout keep test inverted",
     13: "dropout weights not rescaled",
+    14: "Philox key not raised between rounds",
 }
 
 
@@ -50,12 +51,17 @@ def test_pins_catch_planted_mistake(mutant, tmp_path):
             pin(attn)
         except AssertionError:
             caught.append(pin.__name__)
+    for pin in GENERATOR_PINS if not caught else ():
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
     assert caught, f"no pin catches mutant {mutant} ({MUTANTS[mutant]})"
 
 
 @pytest.mark.parametrize("pin", GENERATOR_PINS, ids=lambda p: p.__name__)
 def test_generator_pin(pin, oracle_lib):
-    pin()
+    pin(oracle_lib)
 
 
 def test_oracle_rejects_bad_arguments(oracle_lib):
