@@ -505,12 +505,14 @@ struct DropRow {
     const uint4 r = philox_10((uint32_t)c, (uint32_t)(c >> 32), p.seed_lo, p.seed_hi);
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) m[e] = (w[e] >> 8) >= p.drop_threshold ? p.drop_scale : 0.0f;
+    for (int e = 0; e < 4; ++e) m[e] = (w[e] >> 8) >= p.drop_threshold ? 1.0f : 0.0f;
   }
 };
 
 // p_pass with dropout: the same P and sum, but the stored P (what P V
-// reads) carries each key's dropout multiplier; the sum (l) does not.
+// reads) is zero for dropped keys; the sum (l) keeps them.  The 1 / (1 - p)
+// of kept keys is applied to O in fp32 by the epilogue, so P carries no
+// rounding of it.
 template <class C>
 __device__ __forceinline__ void p_pass_dropout(const float (&s)[C::kBN], float sl, float msub, uint32_t tP, float& sum,
                                                const FaParams& p, const DropRow& dr) {
@@ -1176,7 +1178,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       ++units_seen;
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+      // with dropout, kept weights also take 1 / (1 - p) here (0 when p = 1)
+      const float inv_l = (l_run > 0.0f) ? (C::kFeat && p.dropout_on ? p.drop_scale : 1.0f) / l_run : 0.0f;
       const bool store = row < p.qL;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       ((long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(store ? row : 0) * p.o_ss) * C::kEsz;
