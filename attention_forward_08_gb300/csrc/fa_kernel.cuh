@@ -1183,41 +1183,52 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const bool store = row < p.qL;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       ((long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(store ? row : 0) * p.o_ss) * C::kEsz;
+      // Up to 128 columns of O per TMEM wait (one latency instead of four), so
+      // the next unit's first PV may overwrite O_t before the stores go out
+      // (measured: 391 -> 385 us on a non-causal B2 H32 L4096 D128 problem).
+      constexpr int kBatch = C::kD / 32 < 4 ? C::kD / 32 : 4;
 #pragma unroll
-      for (int cc = 0; cc < C::kD / 32; ++cc) {
-        uint32_t rr[32];
-        tmem_ld32(tO + cc * 32, rr);
+      for (int c0 = 0; c0 < C::kD / 32; c0 += kBatch) {
+        uint32_t rb[kBatch][32];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) tmem_ld32(tO + (c0 + i) * 32, rb[i]);
         tmem_wait_ld();
-        reg_fence(rr);
-        if (cc == C::kD / 32 - 1) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) reg_fence(rb[i]);
+        if (c0 + kBatch == C::kD / 32) {
           // O_t is read: the next unit's first PV may overwrite it.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->o_free[t]);
         }
-        if (store) {
-          if constexpr (C::kTf32) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
 #pragma unroll
-            for (int u4 = 0; u4 < 8; ++u4) {
-              float a0, a1, a2, a3;
-              fmul2(a0, a1, __uint_as_float(rr[4 * u4 + 0]), __uint_as_float(rr[4 * u4 + 1]), inv_l, inv_l);
-              fmul2(a2, a3, __uint_as_float(rr[4 * u4 + 2]), __uint_as_float(rr[4 * u4 + 3]), inv_l, inv_l);
-              dst[u4] = make_uint4(__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3));
-            }
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+        for (int i = 0; i < kBatch; ++i) {
+          const int cc = c0 + i;
+          const uint32_t (&rr)[32] = rb[i];
+          if (store) {
+            if constexpr (C::kTf32) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
 #pragma unroll
-            for (int u4 = 0; u4 < 4; ++u4) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float a0, a1;
-                fmul2(a0, a1, __uint_as_float(rr[8 * u4 + 2 * e]), __uint_as_float(rr[8 * u4 + 2 * e + 1]), inv_l,
-                      inv_l);
-                pk[e] = pack16x2<C>(a0, a1);
+              for (int u4 = 0; u4 < 8; ++u4) {
+                float a0, a1, a2, a3;
+                fmul2(a0, a1, __uint_as_float(rr[4 * u4 + 0]), __uint_as_float(rr[4 * u4 + 1]), inv_l, inv_l);
+                fmul2(a2, a3, __uint_as_float(rr[4 * u4 + 2]), __uint_as_float(rr[4 * u4 + 3]), inv_l, inv_l);
+                dst[u4] = make_uint4(__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3));
               }
-              dst[u4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+#pragma unroll
+              for (int u4 = 0; u4 < 4; ++u4) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float a0, a1;
+                  fmul2(a0, a1, __uint_as_float(rr[8 * u4 + 2 * e]), __uint_as_float(rr[8 * u4 + 2 * e + 1]), inv_l,
+                        inv_l);
+                  pk[e] = pack16x2<C>(a0, a1);
+                }
+                dst[u4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
             }
           }
         }
