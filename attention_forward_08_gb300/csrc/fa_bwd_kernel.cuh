@@ -70,6 +70,9 @@ struct BwdCfg {
   static constexpr int kThreads = 256;
   // TMEM columns: S (or S^T) 0..127, dP (or dP^T) 128..255, then the accumulators.
   static constexpr int kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + kD;
+  // dQ kernel: a second dP buffer after dQ, so dP_{j+1} need not wait for dQ_j
+  // to read dS_j.
+  static constexpr int kColDP2 = 384;
   static constexpr uint32_t kTmemCols = 512;
   // dK/dV kernel shared memory: K, V, then Q and dO rings, then L2 and D slots.
   static constexpr uint32_t kKVOffQ = 2 * kTileBytes;
@@ -79,12 +82,14 @@ struct BwdCfg {
   static constexpr uint32_t kKVSmem = 1024 + kKVOffBar + 512;
   // dQ kernel shared memory: Q, dO, then K and V rings.
   static constexpr uint32_t kQOffK = 2 * kTileBytes;
-  static constexpr uint32_t kQOffV = kQOffK + kStages * kTileBytes;
+  static constexpr int kQKStages = kD == 64 ? 4 : 3;  // dQ kernel K ring (K_j is read by S_j and dQ_j)
+  static constexpr uint32_t kQOffV = kQOffK + kQKStages * kTileBytes;
   static constexpr uint32_t kQOffBar = kQOffV + kStages * kTileBytes;
   static constexpr uint32_t kQSmem = 1024 + kQOffBar + 512;
   static_assert(kD == 64 || kD == 128, "backward head dims: 64 or 128");
   static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "shared memory overflow");
   static_assert(kColAcc1 + kD <= 512, "TMEM overflow");
+  static_assert(kColAcc0 + kD <= kColDP2 && kColDP2 + 128 <= 512, "dQ kernel TMEM overflow");
 };
 
 struct BwdKVCtrl {
@@ -98,10 +103,14 @@ struct BwdKVCtrl {
 struct BwdQCtrl {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full, s_free, dp_full, ds_ready, done, drain;
+  // dp_full / ds_ready per dP buffer: a phase of buffer b can only complete
+  // after its previous phase was waited for, so parity waits cannot skip one.
+  uint64_t s_full, s_free, dp_full[2], ds_ready[2], done, drain;
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(sizeof(BwdKVCtrl) <= 512 && sizeof(BwdQCtrl) <= 512, "barrier block overflow");
 
 // ---------------------------------------------------------------- D pre-pass
 
@@ -552,8 +561,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     mbar_init(&ctl->s_full, 1);
     mbar_init(&ctl->s_free, 4);
-    mbar_init(&ctl->dp_full, 1);
-    mbar_init(&ctl->ds_ready, 4);
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&ctl->dp_full[d], 1);
+      mbar_init(&ctl->ds_ready[d], 4);
+    }
     mbar_init(&ctl->done, 1);
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -586,28 +597,29 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tma_load_4d(sDO + c * (C::kTile * 128), &tmDO, &ctl->q_full, c * 64, q0, h, b);
       }
       for (int j = 0; j < n_blk && ok; ++j) {
-        const int s = j % C::kStages, use = j / C::kStages;
-        ok = wait_bounded(&ctl->k_empty[s], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+        const int sk = j % C::kQKStages, uk = j / C::kQKStages;
+        const int sv = j % C::kStages, uv = j / C::kStages;
+        ok = wait_bounded(&ctl->k_empty[sk], (uk & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
-        mbar_arrive_expect_tx(&ctl->k_full[s], C::kTileBytes);
+        mbar_arrive_expect_tx(&ctl->k_full[sk], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kNChunk; ++c)
-          tma_load_4d(sK + s * C::kTileBytes + c * (C::kTile * 128), &tmK, &ctl->k_full[s], c * 64, j * C::kTile,
+          tma_load_4d(sK + sk * C::kTileBytes + c * (C::kTile * 128), &tmK, &ctl->k_full[sk], c * 64, j * C::kTile,
                       kvh, b);
         ++k_issued;
-        ok = wait_bounded(&ctl->v_empty[s], (use & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
+        ok = wait_bounded(&ctl->v_empty[sv], (uv & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
-        mbar_arrive_expect_tx(&ctl->v_full[s], C::kTileBytes);
+        mbar_arrive_expect_tx(&ctl->v_full[sv], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kNChunk; ++c)
-          tma_load_4d(sV + s * C::kTileBytes + c * (C::kTile * 128), &tmV, &ctl->v_full[s], c * 64, j * C::kTile,
+          tma_load_4d(sV + sv * C::kTileBytes + c * (C::kTile * 128), &tmV, &ctl->v_full[sv], c * 64, j * C::kTile,
                       kvh, b);
         ++v_issued;
       }
       if (*abort_flag) {
         wait_bounded(&ctl->q_full, 0, abort_flag, p.status, kDrainCycles, false);
-        for (int it = max(0, k_issued - C::kStages); it < k_issued; ++it)
-          wait_bounded(&ctl->k_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, p.status, kDrainCycles,
+        for (int it = max(0, k_issued - C::kQKStages); it < k_issued; ++it)
+          wait_bounded(&ctl->k_full[it % C::kQKStages], (it / C::kQKStages) & 1, abort_flag, p.status, kDrainCycles,
                        false);
         for (int it = max(0, v_issued - C::kStages); it < v_issued; ++it)
           wait_bounded(&ctl->v_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, p.status, kDrainCycles,
@@ -627,7 +639,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const uint32_t hi = (uint32_t)(dQ >> 32), hi_mn = (uint32_t)(dKmn >> 32);
       const uint32_t slot = C::kTileBytes >> 4;
       auto issue_s = [&](int s) { bwd_mma_kmajor<C>(tmem + C::kColS, (uint32_t)dQ, hi, (uint32_t)dKk + s * slot, hi, idS); };
-      auto issue_dp = [&](int s) { bwd_mma_kmajor<C>(tmem + C::kColDP, (uint32_t)dO, hi, (uint32_t)dVk + s * slot, hi, idS); };
+      // dP_j goes to buffer j % 2 (kColDP or kColDP2)
+      auto dp_col = [](int j) { return (uint32_t)((j & 1) ? C::kColDP2 : C::kColDP); };
+      auto issue_dp = [&](int s, int j) {
+        bwd_mma_kmajor<C>(tmem + dp_col(j), (uint32_t)dO, hi, (uint32_t)dVk + s * slot, hi, idS);
+      };
       bool ok = wait_bounded(&ctl->q_full, 0, abort_flag, p.status, p.timeout_cycles);
       if (ok) ok = wait_bounded(&ctl->k_full[0], 0, abort_flag, p.status, p.timeout_cycles);
       if (ok) {
@@ -638,38 +654,39 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       if (ok) {
         tc_fence_after();
-        issue_dp(0);
-        mma_commit(&ctl->dp_full);
+        issue_dp(0, 0);
+        mma_commit(&ctl->dp_full[0]);
         mma_commit(&ctl->v_empty[0]);
       }
+      // Tensor-core order per block: S_{j+1}, dP_{j+1}, dQ_j.  dP_{j+1} overwrites
+      // the buffer of dS_{j-1}, which dQ_{j-1} (issued before it) has read.
       for (int j = 0; j < n_blk && ok; ++j) {
-        const int s = j % C::kStages;
-        const int s1 = (j + 1) % C::kStages, use1 = (j + 1) / C::kStages;
+        const int s = j % C::kQKStages;  // K slot of block j
+        const int sk1 = (j + 1) % C::kQKStages, uk1 = (j + 1) / C::kQKStages;
+        const int sv1 = (j + 1) % C::kStages, uv1 = (j + 1) / C::kStages;
         const bool more = j + 1 < n_blk;
         ok = wait_bounded(&ctl->s_free, j & 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
         if (more) {
-          ok = wait_bounded(&ctl->k_full[s1], use1 & 1, abort_flag, p.status, p.timeout_cycles);
+          ok = wait_bounded(&ctl->k_full[sk1], uk1 & 1, abort_flag, p.status, p.timeout_cycles);
           if (!ok) break;
           tc_fence_after();
-          issue_s(s1);
+          issue_s(sk1);
           mma_commit(&ctl->s_full);
+          ok = wait_bounded(&ctl->v_full[sv1], uv1 & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(sv1, j + 1);
+          mma_commit(&ctl->dp_full[(j + 1) & 1]);
+          mma_commit(&ctl->v_empty[sv1]);
         }
-        ok = wait_bounded(&ctl->ds_ready, j & 1, abort_flag, p.status, p.timeout_cycles);
+        ok = wait_bounded(&ctl->ds_ready[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
         tc_fence_after();
-        // dQ += dS K_j (dS: bf16 pairs over the dP columns; K_j read MN-major)
-        bwd_mma_tmem_a<C>(tmem + C::kColAcc0, tmem + C::kColDP, (uint32_t)dKmn + s * slot, hi_mn, idAcc,
+        // dQ += dS K_j (dS: bf16 pairs over dP_j's columns; K_j read MN-major)
+        bwd_mma_tmem_a<C>(tmem + C::kColAcc0, tmem + dp_col(j), (uint32_t)dKmn + s * slot, hi_mn, idAcc,
                           j > 0 ? 1u : 0u);
         mma_commit(&ctl->k_empty[s]);
-        if (more) {
-          ok = wait_bounded(&ctl->v_full[s1], use1 & 1, abort_flag, p.status, p.timeout_cycles);
-          if (!ok) break;
-          tc_fence_after();
-          issue_dp(s1);
-          mma_commit(&ctl->dp_full);
-          mma_commit(&ctl->v_empty[s1]);
-        }
       }
       if (ok) mma_commit(&ctl->done);
       mma_commit(&ctl->drain);
@@ -683,6 +700,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS;
     const uint32_t tDP = tmem + lane_addr + C::kColDP;
+    const uint32_t tDP2 = tmem + lane_addr + C::kColDP2;
     const float sl = p.scale_log2;
     const long long rowi = ((long long)b * p.Hq + h) * p.qL + (i < p.qL ? i : 0);
     float l2 = __int_as_float(0x7f800000), di = 0.0f;
@@ -712,14 +730,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         pr[c] = c < lim ? ex2(x0) : 0.0f;
         pr[c + 1] = c + 1 < lim ? ex2(x1) : 0.0f;
       }
-      ok = warp_wait(&ctl->dp_full, j & 1, abort_flag, p.status, p.timeout_cycles);
+      ok = warp_wait(&ctl->dp_full[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
-      bwd_ds_pass(tDP, pr, [&](int) { return di; });
+      bwd_ds_pass((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; });
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->ds_ready);
+      if (lane == 0) mbar_arrive(&ctl->ds_ready[j & 1]);
     }
     if (ok) {
       const bool store = i < p.qL;
