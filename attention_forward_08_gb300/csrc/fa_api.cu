@@ -431,9 +431,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     set_error("scale must be finite");
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (dtype != FA_DTYPE_BF16) {
-    const bool known = dtype == FA_DTYPE_F32 || dtype == FA_DTYPE_F16;
-    set_error(known ? "the backward pass supports bf16 I/O only"
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) {
+    const bool known = dtype == FA_DTYPE_F32;
+    set_error(known ? "the backward pass supports bf16 and fp16 I/O only"
                     : "dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)",
               dtype);
     return known ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
@@ -476,6 +476,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.dk = dk;
   a.dv = dv;
   a.dvec = static_cast<float*>(workspace);
+  a.f16 = dtype == FA_DTYPE_F16;
   a.B = B;
   a.Hq = H_q;
   a.Hkv = H_kv;
@@ -490,6 +491,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   return launch_bwd(a);
 }
 
-int fa_version(void) { return 104; }
+int fa_version(void) { return 105; }
 
 }  // extern "C"

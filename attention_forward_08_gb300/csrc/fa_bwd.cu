@@ -1,5 +1,5 @@
 // fa_bwd.cu -- launcher for the backward pass: tensor maps, grids, the three
-// launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 I/O.
+// launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 or fp16 I/O.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -25,14 +25,14 @@ int set_smem_once(const void* kern, uint32_t bytes, int& configured_device) {
   return 0;
 }
 
-template <int kD>
+template <int kD, bool kF16>
 int launch_bwd_d(const BwdLaunchArgs& a) {
-  using C = BwdCfg<kD>;
+  using C = BwdCfg<kD, kF16>;
   // 1. D_i = rowsum(O_i * dO_i)
   const long long rows = (long long)a.B * a.Hq * a.qL;
   constexpr int kRowsPerBlock = 256 / (kD / 8);
   const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-  fa_bwd_rowdot_kernel<kD><<<(unsigned)blocks, 256, 0, a.stream>>>(
+  fa_bwd_rowdot_kernel<kD, kF16><<<(unsigned)blocks, 256, 0, a.stream>>>(
       static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.dvec, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -44,10 +44,10 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   const long long qst[3] = {(long long)a.Hq * a.qL * kD, (long long)a.qL * kD, kD};
   const long long kst[3] = {(long long)a.Hkv * a.kL * kD, (long long)a.kL * kD, kD};
   CUtensorMap tq, tk, tv, tdo;
-  if (!encode_bhsd(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tdo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tq, C::kTmaType, a.q, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tdo, C::kTmaType, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tk, C::kTmaType, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
+  if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
 
   BwdParams p;
   p.B = a.B;
@@ -98,6 +98,9 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
 
 }  // namespace
 
-int launch_bwd(const BwdLaunchArgs& a) { return a.D == 64 ? launch_bwd_d<64>(a) : launch_bwd_d<128>(a); }
+int launch_bwd(const BwdLaunchArgs& a) {
+  if (a.f16) return a.D == 64 ? launch_bwd_d<64, true>(a) : launch_bwd_d<128, true>(a);
+  return a.D == 64 ? launch_bwd_d<64, false>(a) : launch_bwd_d<128, false>(a);
+}
 
 }  // namespace fa

@@ -1,4 +1,4 @@
-// fa_bwd_kernel.cuh -- FlashAttention-2 backward for sm_103a (bf16 I/O):
+// fa_bwd_kernel.cuh -- FlashAttention-2 backward for sm_103a (bf16 or fp16 I/O):
 // dQ, dK, dV of O = softmax(scale * Q K^T) V given dO and the forward's L.
 //
 // What it computes (per batch b, query head h, kvh = h / (H_q / H_kv)):
@@ -27,7 +27,7 @@
 //    issues every tcgen05.mma from one thread, warps 4-7 are one elementwise
 //    warpgroup with thread r owning TMEM lane r (a key row in dK/dV, a query
 //    row in dQ);
-//  - P and dS are rounded to bf16 and written over the fp32 S and dP columns
+//  - P and dS are rounded to the I/O format (bf16 or fp16) and written over the fp32 S and dP columns
 //    of TMEM; the next block's S and dP MMAs are ordered behind the MMAs that
 //    read them, so the elementwise work of one block overlaps the tensor core's
 //    work on the previous one;
@@ -52,16 +52,21 @@ struct BwdParams {
   float scale_log2;   // scale * log2(e)
   const float* lse;   // [B, Hq, qL] natural log
   float* dvec;        // [B, Hq, qL] D_i = rowsum(O_i * dO_i)
-  void* dq;           // [B, Hq, qL, D] bf16
-  void* dk;           // [B, Hkv, kL, D] bf16
-  void* dv;           // [B, Hkv, kL, D] bf16
+  void* dq;           // [B, Hq, qL, D] (I/O format)
+  void* dk;           // [B, Hkv, kL, D]
+  void* dv;           // [B, Hkv, kL, D]
   unsigned int* status;
   long long timeout_cycles;
 };
 
-template <int kD_>
+template <int kD_, bool kF16_ = false>
 struct BwdCfg {
   static constexpr int kD = kD_;
+  // 16-bit I/O is bf16 unless kF16 (fp16): same kernels, other operand format.
+  static constexpr bool kF16 = kF16_;
+  static constexpr uint32_t kFmt = kF16 ? kFmtF16 : kFmtBf16;
+  static constexpr CUtensorMapDataType kTmaType =
+      kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   static constexpr int kTile = 128;                     // rows per tile (queries or keys)
   static constexpr int kNChunk = kD / 64;               // 128-byte column blocks per row
   static constexpr uint32_t kTileBytes = kTile * kD * 2;
@@ -114,10 +119,10 @@ static_assert(sizeof(BwdKVCtrl) <= 512 && sizeof(BwdQCtrl) <= 512, "barrier bloc
 
 // ---------------------------------------------------------------- D pre-pass
 
-// D_i = sum_d O_id dO_id for every row of a contiguous [rows, kD] bf16 pair:
-// kD / 8 threads per row, one 16-byte load of each operand per thread, fp32
-// products, a shuffle reduction within the row's threads.
-template <int kD>
+// D_i = sum_d O_id dO_id for every row of a contiguous [rows, kD] 16-bit pair
+// (bf16, or fp16 with kF16): kD / 8 threads per row, one 16-byte load of each
+// operand per thread, fp32 products, a shuffle reduction within the row's threads.
+template <int kD, bool kF16>
 __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const uint4* __restrict__ o,
                                                             const uint4* __restrict__ dout,
                                                             float* __restrict__ dvec, long long rows) {
@@ -132,8 +137,8 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const uint4* __restr
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(gw[e] << 16), acc);
-      acc = fmaf(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(gw[e] & 0xFFFF0000u), acc);
+      acc = fmaf(half_bits_to_f32<kF16>(aw[e]), half_bits_to_f32<kF16>(gw[e]), acc);
+      acc = fmaf(half_bits_to_f32<kF16>(aw[e] >> 16), half_bits_to_f32<kF16>(gw[e] >> 16), acc);
     }
   }
 #pragma unroll
@@ -179,9 +184,9 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
 }
 
 // dS = P (dP - d) chunk by chunk: read 32 fp32 dP columns, write 16 columns of
-// bf16 pairs over the part of the dP region already read.  dsub(c) gives the
+// 16-bit pairs over the part of the dP region already read.  dsub(c) gives the
 // D term of column c.
-template <class F>
+template <class C, class F>
 __device__ __forceinline__ void bwd_ds_pass(uint32_t tdp, const float (&p)[128], F dsub) {
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
@@ -195,16 +200,16 @@ __device__ __forceinline__ void bwd_ds_pass(uint32_t tdp, const float (&p)[128],
       const int c0 = cc * 32 + 2 * e;
       const float d0 = p[c0] * (__uint_as_float(rr[2 * e]) - dsub(c0));
       const float d1 = p[c0 + 1] * (__uint_as_float(rr[2 * e + 1]) - dsub(c0 + 1));
-      pk[e] = pack_bf16x2(d0, d1);
+      pk[e] = pack16x2<C>(d0, d1);
     }
     tmem_st16(tdp + cc * 16, pk);
   }
 }
 
-// Store a 128 x kD fp32 accumulator row (this thread's lane), times `mul`, as
-// bf16 to a contiguous row of global memory (16-byte stores).
+// Store a 128 x kD fp32 accumulator row (this thread's lane), times `mul`, in
+// the 16-bit I/O format to a contiguous row of global memory (16-byte stores).
 template <class C>
-__device__ __forceinline__ void bwd_store_row(uint32_t tacc, float mul, __nv_bfloat16* dst, bool store) {
+__device__ __forceinline__ void bwd_store_row(uint32_t tacc, float mul, uint16_t* dst, bool store) {
 #pragma unroll
   for (int cc = 0; cc < C::kD / 32; ++cc) {
     uint32_t rr[32];
@@ -218,7 +223,7 @@ __device__ __forceinline__ void bwd_store_row(uint32_t tacc, float mul, __nv_bfl
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(rr[8 * u + 2 * e]) * mul, __uint_as_float(rr[8 * u + 2 * e + 1]) * mul);
+          pk[e] = pack16x2<C>(__uint_as_float(rr[8 * u + 2 * e]) * mul, __uint_as_float(rr[8 * u + 2 * e + 1]) * mul);
         d4[u] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
@@ -366,8 +371,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else if (warp == 1) {
     // ===================================================== MMA issuer
     if (lane == 0 && n_steps > 0) {
-      constexpr uint32_t idS = make_idesc(false, 128, 128, false, false);     // K-major A and B
-      constexpr uint32_t idAcc = make_idesc(false, 128, C::kD, false, true);  // B MN-major
+      constexpr uint32_t idS = make_idesc_fmt(C::kFmt, 128, 128, false, false);     // K-major A and B
+      constexpr uint32_t idAcc = make_idesc_fmt(C::kFmt, 128, C::kD, false, true);  // B MN-major
       const uint64_t dK = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV = make_sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dQk = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -470,7 +475,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cc * 32 + 2 * e], pr[cc * 32 + 2 * e + 1]);
+        for (int e = 0; e < 16; ++e) pk[e] = pack16x2<C>(pr[cc * 32 + 2 * e], pr[cc * 32 + 2 * e + 1]);
         tmem_st16(tS + cc * 16, pk);
       }
       tmem_wait_st();
@@ -481,7 +486,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       ok = warp_wait(&ctl->dp_full, i & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
-      bwd_ds_pass(tDP, pr, [&](int c) { return l2s[C::kTile + c]; });
+      bwd_ds_pass<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; });
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -494,8 +499,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (ok) {
       const bool store = j < p.kL;
       const long long row = ((long long)b * p.Hkv + kvh) * p.kL + (store ? j : 0);
-      __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(p.dv) + row * C::kD;
-      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(p.dk) + row * C::kD;
+      uint16_t* dvp = static_cast<uint16_t*>(p.dv) + row * C::kD;
+      uint16_t* dkp = static_cast<uint16_t*>(p.dk) + row * C::kD;
       if (n_steps == 0) {  // no query sees these keys: zero gradients
         if (store) {
           uint4* a4 = reinterpret_cast<uint4*>(dvp);
@@ -629,8 +634,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else if (warp == 1) {
     // ===================================================== MMA issuer
     if (lane == 0 && n_blk > 0) {
-      constexpr uint32_t idS = make_idesc(false, 128, 128, false, false);
-      constexpr uint32_t idAcc = make_idesc(false, 128, C::kD, false, true);
+      constexpr uint32_t idS = make_idesc_fmt(C::kFmt, 128, 128, false, false);
+      constexpr uint32_t idAcc = make_idesc_fmt(C::kFmt, 128, C::kD, false, true);
       const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dO = make_sdesc_sw128(smem_u32(sDO), 16, 1024);
       const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);
@@ -733,7 +738,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       ok = warp_wait(&ctl->dp_full[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
-      bwd_ds_pass((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; });
+      bwd_ds_pass<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; });
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -741,7 +746,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     if (ok) {
       const bool store = i < p.qL;
-      __nv_bfloat16* dqp = static_cast<__nv_bfloat16*>(p.dq) + rowi * C::kD;
+      uint16_t* dqp = static_cast<uint16_t*>(p.dq) + rowi * C::kD;
       if (n_blk == 0) {
         if (store) {
           uint4* a4 = reinterpret_cast<uint4*>(dqp);

@@ -7,9 +7,10 @@
 namespace fa {
 
 struct BwdLaunchArgs {
-  const void *q, *k, *v, *o, *dout;  // bf16, contiguous [B,H,L,D]
+  const void *q, *k, *v, *o, *dout;  // bf16 (fp16 when f16), contiguous [B,H,L,D]
   const float* lse;                  // [B, H_q, qL]
-  void *dq, *dk, *dv;                // bf16 outputs
+  void *dq, *dk, *dv;                // outputs in the same format
+  bool f16;                          // fp16 I/O instead of bf16
   float* dvec;                       // [B, H_q, qL] scratch for D = rowsum(O * dO)
   int B, Hq, Hkv, qL, kL, D;
   float scale;

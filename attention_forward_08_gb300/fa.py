@@ -254,7 +254,7 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
                   stream=None):
     """dQ, dK, dV for torch CUDA tensors; returns (dq, dk, dv).
 
-    q, o, dout: contiguous bf16 [B, H_q, qL, D]; k, v: contiguous bf16
+    q, o, dout: contiguous bf16 or fp16 [B, H_q, qL, D]; k, v: the same dtype,
     [B, H_kv, kL, D]; lse: the forward's contiguous fp32 [B, H_q, qL].
     workspace: optional device tensor of at least ``fa_bwd_workspace_bytes``
     bytes (allocated here if None).
@@ -272,8 +272,10 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("lse", lse)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
-        if name != "lse" and t.dtype != torch.bfloat16:
-            raise ValueError(f"{name} must be bfloat16 (the backward pass supports bf16 I/O)")
+        if name != "lse" and t.dtype != q.dtype:
+            raise ValueError(f"{name} must have q's dtype {q.dtype}")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("the backward pass supports bfloat16 and float16 I/O")
     if dq is None:
         dq = torch.empty_like(q)
     if dk is None:
@@ -290,5 +292,6 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
     _check(fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                   workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
-                  1.0 / math.sqrt(D) if scale is None else scale, causal, FA_DTYPE_BF16, stream))
+                  1.0 / math.sqrt(D) if scale is None else scale, causal,
+                  FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16, stream))
     return dq, dk, dv

@@ -449,10 +449,10 @@ def run_ours_bwd(args, w):
     torch.cuda.set_device(dev)
     import attention_forward_08_gb300 as fa
     fa.load_library()
-    if (w.dtype != "bf16" or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128) or w.window
-            or w.softcap or w.q_offset or w.dropout_p):
-        raise SystemExit(f"--pass bwd needs a plain (unmasked, no window/softcap/offset) bf16 BHSD workload "
-                         f"with D 64 or 128 ({w.name})")
+    if (w.dtype not in ("bf16", "f16") or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128)
+            or w.window or w.softcap or w.q_offset or w.dropout_p):
+        raise SystemExit(f"--pass bwd needs a plain (unmasked, no window/softcap/offset/dropout) bf16 or fp16 "
+                         f"BHSD workload with D 64 or 128 ({w.name})")
     q, k, v = workloads.make_qkv(w)
     do = workloads.make_dout(w)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
@@ -466,7 +466,7 @@ def run_ours_bwd(args, w):
 
     def launch():
         rc = fa.fa_bwd(*ptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal,
-                       fa.FA_DTYPE_BF16, stream.cuda_stream)
+                       fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16, stream.cuda_stream)
         if rc != 0:
             raise fa.FaError(rc, fa.fa_last_error())
 

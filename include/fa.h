@@ -188,7 +188,8 @@ long long fa_bwd_workspace_bytes(int B, int H_q, int qL);
  * dK, dV)" (the D = rowsum(O * dO) pre-pass and the buffer shapes).
  *
  * Arguments: q, o, dout, dq [B,H_q,qL,D]; k, v, dk, dv [B,H_kv,kL,D]; all
- * contiguous bf16 (dtype must be FA_DTYPE_BF16), 16-byte aligned.  lse
+ * contiguous bf16 or fp16 (dtype FA_DTYPE_BF16 or FA_DTYPE_F16; P and dS are
+ * rounded to that format before their products), 16-byte aligned.  lse
  * [B,H_q,qL] fp32 is the forward's L (natural log; -inf rows get zero
  * gradients).  o is the forward's output.  workspace: caller-owned device
  * memory of at least fa_bwd_workspace_bytes(B, H_q, qL) bytes, 16-byte
@@ -218,7 +219,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int qL, int kL, int D, float scale,
                    int causal, int dtype, void* stream);
 
-/* ABI version: major * 100 + minor. */
+/* ABI version: major * 100 + minor (1.05: fa_bwd and fa_bwd_noalloc accept
+ * FA_DTYPE_F16). */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -61,7 +61,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 104
+    assert fa.fa_version() == 105
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -170,8 +170,7 @@ def test_bwd_workspace_size(fa):
     (dict(H_q=6, H_kv=4), 1, "divisible"),
     (dict(kL=0), 1, "> 0"),
     (dict(scale=float("nan")), 1, "finite"),
-    (dict(dtype=0), 2, "bf16"),
-    (dict(dtype=2), 2, "bf16"),
+    (dict(dtype=0), 2, "bf16 and fp16"),
     (dict(dtype=5), 1, "dtype"),
     (dict(D=256), 2, "head dim"),
     (dict(ws_bytes=100), 1, "workspace"),
