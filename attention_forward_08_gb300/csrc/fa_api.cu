@@ -276,7 +276,8 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     la.max_ctas = g_max_ctas;
   }
 
-  const bool feat = a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f || a->dropout_p != 0.0f;
+  const bool drop = a->dropout_p != 0.0f;
+  const bool feat = drop || a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f;
   // bf16 / fp16 at D <= 128 (no window, softcap or offset): one Q tile per CTA
   // when the two-tile work units cannot occupy every SM.
   bool one_tile = false;
@@ -292,7 +293,9 @@ int fa_fwd_ex(const fa_fwd_args* a) {
   }
   switch (a->dtype) {
     case FA_DTYPE_F32:
-      if (feat)
+      if (drop)
+        rc = a->D == 64 ? launch_drop_f32_d64(la) : a->D == 128 ? launch_drop_f32_d128(la) : launch_drop_f32_d256(la);
+      else if (feat)
         rc = a->D == 64 ? launch_feat_f32_d64(la) : a->D == 128 ? launch_feat_f32_d128(la) : launch_feat_f32_d256(la);
       else
         rc = a->D == 64 ? launch_f32_d64(la) : a->D == 128 ? launch_f32_d128(la) : launch_f32_d256(la);
@@ -300,6 +303,8 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     case FA_DTYPE_F16:
       if (one_tile)
         rc = a->D == 64 ? launch_q1_f16_d64(la) : launch_q1_f16_d128(la);
+      else if (drop)
+        rc = a->D == 64 ? launch_drop_f16_d64(la) : a->D == 128 ? launch_drop_f16_d128(la) : launch_drop_f16_d256(la);
       else if (feat)
         rc = a->D == 64 ? launch_feat_f16_d64(la) : a->D == 128 ? launch_feat_f16_d128(la) : launch_feat_f16_d256(la);
       else
@@ -308,6 +313,9 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     default:
       if (one_tile)
         rc = a->D == 64 ? launch_q1_bf16_d64(la) : launch_q1_bf16_d128(la);
+      else if (drop)
+        rc = a->D == 64 ? launch_drop_bf16_d64(la) : a->D == 128 ? launch_drop_bf16_d128(la)
+                                                                  : launch_drop_bf16_d256(la);
       else if (feat)
         rc = a->D == 64 ? launch_feat_bf16_d64(la) : a->D == 128 ? launch_feat_bf16_d128(la)
                                                                   : launch_feat_bf16_d256(la);

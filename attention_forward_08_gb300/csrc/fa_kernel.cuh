@@ -67,12 +67,15 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr long long kDrainCycles = 1LL << 33;
 
 template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_, int kVTStages_ = 0,
-          bool kF16_ = false, bool kFeat_ = false>
+          bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false>
 struct Cfg {
   static constexpr bool kTf32 = kTf32_;
   // Sliding window, softcap and query offset compiled in (a separate
   // instantiation, so the plain forward keeps its exact code).
   static constexpr bool kFeat = kFeat_;
+  // Dropout compiled in as well (its own instantiation again: its keep-bit
+  // bookkeeping costs the other features 3-5%).
+  static constexpr bool kDrop = kDrop_;
   // 16-bit I/O is bf16 unless kF16 (fp16): same kernel, other operand format.
   static constexpr bool kF16 = kF16_;
   static constexpr uint32_t kFmt = kTf32 ? kFmtTf32 : (kF16 ? kFmtF16 : kFmtBf16);
@@ -129,10 +132,18 @@ struct Cfg {
   static constexpr uint32_t kOffVT = kOffV + kVStages * kKVTileBytes;
   // One shared-memory slot for a TMA-loaded mask tile [kBM rows x kBN keys]
   // (sized for a 2-byte additive mask; a 1-byte bool tile uses half).  Only
-  // where shared memory allows: bf16 I/O with one Q tile (D = 256).
-  static constexpr uint32_t kMaskSlotBytes = (!kTf32 && kNQT == 1) ? kBM * kBN * 2 : 0;
+  // where shared memory allows: 16-bit I/O with one Q tile, except in the
+  // dropout instantiation, whose keep bits take the room (its masks are read
+  // from L2).
+  static constexpr uint32_t kMaskSlotBytes = (!kTf32 && kNQT == 1 && !kDrop) ? kBM * kBN * 2 : 0;
   static constexpr uint32_t kOffM = kOffVT + kVTStages * kKVTileBytes;
-  static constexpr uint32_t kOffBar = kOffM + kMaskSlotBytes;
+  // Dropout keep bits of each row's next block (kBN / 8 bytes per row) in
+  // shared memory for 16-bit I/O, whose softmax warps have no registers to
+  // spare; in registers for fp32 I/O.
+  static constexpr bool kDropSmem = kDrop && !kTf32;
+  static constexpr uint32_t kDropBytes = kDropSmem ? kNQT * kBM * (kBN / 8) : 0;
+  static constexpr uint32_t kOffDrop = kOffM + kMaskSlotBytes;
+  static constexpr uint32_t kOffBar = kOffDrop + kDropBytes;
   static constexpr uint32_t kBarBytes = 512;
   static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 
@@ -144,6 +155,7 @@ struct Cfg {
   static_assert(kKStages >= 1 && kVStages >= 1 && kKStages <= 4 && kVStages <= 4, "ring size");
   static_assert(kTf32 ? (kVTStages >= 1 && kVTStages <= 4) : kVTStages == 0, "V^T ring is for TF32 only");
   static_assert(!(kTf32 && kF16), "fp16 I/O uses the 16-bit path");
+  static_assert(!kDrop || kFeat, "the dropout instantiation includes the other features");
 };
 
 // Shared-memory control block (after the tiles).
@@ -479,7 +491,7 @@ __device__ __forceinline__ void p_pass(const float (&s)[C::kBN], float sl, float
 // published round function on the counter (c0, c1, 0, 0) with key (k0, k1).
 // Not inlined: one instance at a time keeps the softmax's registers for the
 // scores (the dropout path calls it once per 4 keys).
-static __device__ __noinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
+__device__ __forceinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
   uint32_t x0 = c0, x1 = c1, x2 = 0u, x3 = 0u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
@@ -495,49 +507,58 @@ static __device__ __noinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_
   return make_uint4(x0, x1, x2, x3);
 }
 
-// Dropout multipliers of one row's block: position ((b H_q + h) qL + row) kL
-// + key, counter = offset + position / 4, word = position % 4 (kL is a
-// multiple of 4, so a block of 4 keys is one counter).
-struct DropRow {
-  unsigned long long ctr;  // counter of the row's key kbase
-  __device__ __forceinline__ void keep4(const FaParams& p, int group, float (&m)[4]) const {
-    const unsigned long long c = ctr + (unsigned long long)group;
-    const uint4 r = philox_10((uint32_t)c, (uint32_t)(c >> 32), p.seed_lo, p.seed_hi);
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+// Keep bits of one row's block of 32 * kWords keys: bit i of word q is key
+// kbase + 32 q + i.
+// Position ((b H_q + h) qL + row) kL + key, counter = offset + position / 4,
+// word = position % 4 (kL is a multiple of 4, so 4 keys share one counter);
+// `ctr` is the counter of key kbase.  Computed for block j + 1 while the warp
+// would otherwise wait for S_{j+1}, so the generator stays off the softmax's
+// critical path.
+// One keep word: 8 generator blocks of 4 keys from counter `ctr`.
+__device__ __forceinline__ uint32_t drop_word(const FaParams& p, unsigned long long ctr) {
+  uint32_t acc = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) m[e] = (w[e] >> 8) >= p.drop_threshold ? 1.0f : 0.0f;
+  for (int g = 0; g < 8; ++g) {
+    const unsigned long long c = ctr + (unsigned long long)g;
+    const uint4 r = philox_10((uint32_t)c, (uint32_t)(c >> 32), p.seed_lo, p.seed_hi);
+    acc |= ((r.x >> 8) >= p.drop_threshold ? 1u : 0u) << (4 * g);
+    acc |= ((r.y >> 8) >= p.drop_threshold ? 1u : 0u) << (4 * g + 1);
+    acc |= ((r.z >> 8) >= p.drop_threshold ? 1u : 0u) << (4 * g + 2);
+    acc |= ((r.w >> 8) >= p.drop_threshold ? 1u : 0u) << (4 * g + 3);
   }
-};
+  return acc;
+}
+template <int kWords>
+__device__ __forceinline__ void drop_bits(const FaParams& p, unsigned long long ctr, uint32_t (&kb)[kWords]) {
+#pragma unroll
+  for (int q = 0; q < kWords; ++q) kb[q] = drop_word(p, ctr + (unsigned long long)(q * 8));
+}
 
 // p_pass with dropout: the same P and sum, but the stored P (what P V
 // reads) is zero for dropped keys; the sum (l) keeps them.  The 1 / (1 - p)
 // of kept keys is applied to O in fp32 by the epilogue, so P carries no
 // rounding of it.
-template <class C>
+template <class C, class KB>
 __device__ __forceinline__ void p_pass_dropout(const float (&s)[C::kBN], float sl, float msub, uint32_t tP, float& sum,
-                                               const FaParams& p, const DropRow& dr) {
+                                               const KB& keep_word) {  // keep_word(cc): bits of keys 32 cc ..
   float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int cc = 0; cc < C::kBN / 32; ++cc) {
     uint32_t pk[C::kTf32 ? 32 : 16];
+    const uint32_t kw = keep_word(cc);
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {  // 8 groups of 4 keys
-      float m[4];
-      dr.keep4(p, cc * 8 + g, m);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int e = 2 * g + hh;  // pair index in the chunk
-        float x0, x1;
-        ffma2(x0, x1, s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1], sl, sl, -msub, -msub);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
-        const float d0 = p0 * m[2 * hh], d1 = p1 * m[2 * hh + 1];
-        if constexpr (C::kTf32) {
-          pk[2 * e] = to_tf32(d0);
-          pk[2 * e + 1] = to_tf32(d1);
-        } else {
-          pk[e] = pack16x2<C>(d0, d1);
-        }
+    for (int e = 0; e < 16; ++e) {
+      float x0, x1;
+      ffma2(x0, x1, s[cc * 32 + 2 * e], s[cc * 32 + 2 * e + 1], sl, sl, -msub, -msub);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      fadd2(sum4[(e & 1) * 2], sum4[(e & 1) * 2 + 1], p0, p1);
+      if constexpr (C::kTf32) {
+        pk[2 * e] = to_tf32((kw >> (2 * e)) & 1u ? p0 : 0.0f);
+        pk[2 * e + 1] = to_tf32((kw >> (2 * e + 1)) & 1u ? p1 : 0.0f);
+      } else {
+        // the pair's two keep bits widened to a 16-bit lane mask
+        const uint32_t t = (kw >> (2 * e)) & 3u;
+        pk[e] = pack16x2<C>(p0, p1) & ((t & 1u) * 0x0000FFFFu + (t >> 1) * 0xFFFF0000u);
       }
     }
     if constexpr (C::kTf32)
@@ -1071,6 +1092,35 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const int row = r0 + tl;
       float m_run = -INFINITY;  // running max, base 2 (scaled)
       float l_run = 0.0f;       // running sum of 2^(s - m_run)
+      // Dropout: the keep bits of the block the loop is about to process (the
+      // generator counter of key kbase of this row, as a function).
+      auto drop_ctr = [&](int jb) {
+        return p.drop_offset + (((unsigned long long)b * p.Hq + h) * p.qL + row) * (unsigned long long)(p.kL / 4) +
+               (unsigned long long)(jb * (C::kBN / 4));
+      };
+      constexpr int kKW = C::kBN / 32;  // keep words per row and block
+      uint32_t kb[C::kDropSmem ? 1 : kKW];
+#pragma unroll
+      for (int q = 0; q < (C::kDropSmem ? 1 : kKW); ++q) kb[q] = 0u;
+      uint32_t* kb_smem = reinterpret_cast<uint32_t*>(smem + C::kOffDrop) + (t * C::kBM + tl) * kKW;
+      auto next_bits = [&](int jb) {
+        if constexpr (C::kDropSmem) {
+          // one word at a time (a fully unrolled row block interleaves 32
+          // generator chains and runs out of registers)
+          const unsigned long long c0 = drop_ctr(jb);
+#pragma unroll 1
+          for (int q = 0; q < kKW; ++q) kb_smem[q] = drop_word(p, c0 + (unsigned long long)(q * 8));
+        } else {
+          drop_bits(p, drop_ctr(jb), kb);
+        }
+      };
+      auto keep_word = [&](int cc) -> uint32_t {
+        if constexpr (C::kDropSmem)
+          return kb_smem[cc];
+        else
+          return kb[cc];
+      };
+      if (C::kDrop) next_bits(unit_j0<C>(w));
       for (int j = unit_j0<C>(w); j < nb; ++j) {
         ok = warp_wait(&ctl->s_full[t], blocks_seen & 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
@@ -1126,10 +1176,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         // P = 2^(s*sl - m): fp32 sum, stored to TMEM as bf16 pairs or tf32.
         const uint32_t tP = C::kAliasP ? tS : (tmem + lane_addr + C::kColP + (j & 1) * C::kPCols);
         float sum, unused;
-        if (C::kFeat && p.dropout_on) {
-          const DropRow dr{p.drop_offset +
-                           ((((unsigned long long)b * p.Hq + h) * p.qL + row) * p.kL + kbase) / 4ull};
-          p_pass_dropout<C>(s, sl, msub, tP, sum, p, dr);
+        if (C::kDrop) {
+          p_pass_dropout<C>(s, sl, msub, tP, sum, keep_word);
         } else {
           p_pass<C, false>(s, sl, msub, tP, sum, unused);
         }
@@ -1168,6 +1216,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->p_ready[t]);
+        if (C::kDrop && j + 1 < nb) next_bits(j + 1);
       }
       if (!ok) break;
 
@@ -1179,7 +1228,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       // with dropout, kept weights also take 1 / (1 - p) here (0 when p = 1)
-      const float inv_l = (l_run > 0.0f) ? (C::kFeat && p.dropout_on ? p.drop_scale : 1.0f) / l_run : 0.0f;
+      const float inv_l = (l_run > 0.0f) ? (C::kDrop ? p.drop_scale : 1.0f) / l_run : 0.0f;
       const bool store = row < p.qL;
       uint8_t* orow = static_cast<uint8_t*>(p.o) +
                       ((long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(store ? row : 0) * p.o_ss) * C::kEsz;

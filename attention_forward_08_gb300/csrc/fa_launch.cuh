@@ -216,6 +216,8 @@ using CfgF16D128Q1  = Cfg<false, 128, 1, 128, 2, 2, 0, true>;
 // The same plans with sliding window, softcap and query offset compiled in.
 template <class C>
 using WithFeat = Cfg<C::kTf32, C::kD, C::kNQT, C::kBN, C::kKStages, C::kVStages, C::kVTStages, C::kF16, true>;
+template <class C>
+using WithDrop = Cfg<C::kTf32, C::kD, C::kNQT, C::kBN, C::kKStages, C::kVStages, C::kVTStages, C::kF16, true, true>;
 
 int launch_bf16_d64(const LaunchArgs& a);
 int launch_bf16_d128(const LaunchArgs& a);
@@ -240,5 +242,15 @@ int launch_feat_f32_d256(const LaunchArgs& a);
 int launch_feat_f16_d64(const LaunchArgs& a);
 int launch_feat_f16_d128(const LaunchArgs& a);
 int launch_feat_f16_d256(const LaunchArgs& a);
+// ... and of the dropout instantiation (the features plus dropout).
+int launch_drop_bf16_d64(const LaunchArgs& a);
+int launch_drop_bf16_d128(const LaunchArgs& a);
+int launch_drop_bf16_d256(const LaunchArgs& a);
+int launch_drop_f32_d64(const LaunchArgs& a);
+int launch_drop_f32_d128(const LaunchArgs& a);
+int launch_drop_f32_d256(const LaunchArgs& a);
+int launch_drop_f16_d64(const LaunchArgs& a);
+int launch_drop_f16_d128(const LaunchArgs& a);
+int launch_drop_f16_d256(const LaunchArgs& a);
 
 }  // namespace fa

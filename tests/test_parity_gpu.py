@@ -122,6 +122,10 @@ DROPOUT = [
     S("drop_f16_d64_window_causal", 1, 2, 1, 260, 260, 64, "f16", causal=True, window=100, dropout_p=0.3,
       dropout_seed=13, dropout_offset=77, seed=85),
     S("drop_all_bf16_d128", 1, 2, 2, 200, 200, 128, "bf16", causal=True, dropout_p=1.0, dropout_seed=1, seed=86),
+    S("drop_f16_d256_bool", 1, 2, 2, 200, 200, 256, "f16", mask_kind=W.MASK_BOOL, dropout_p=0.4, dropout_seed=21,
+      seed=87),
+    S("drop_bf16_d128_softcap_offset", 1, 4, 2, 192, 320, 128, "bf16", causal=True, q_offset=128, softcap=15.0,
+      dropout_p=0.15, dropout_seed=3, seed=88),
 ]
 
 
