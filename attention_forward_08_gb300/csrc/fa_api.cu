@@ -138,6 +138,10 @@ int validate(const fa_fwd_args* a) {
     set_error("dropout_p must lie in [0, 1]");
     return FA_ERR_INVALID_ARGUMENT;
   }
+  if (a->workspace_bytes < 0 || (a->workspace && (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)) {
+    set_error("workspace must be 256-byte aligned and workspace_bytes >= 0");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
   if (a->dropout_p > 0.0f && a->kL % 4 != 0) {
     set_error("dropout needs kL (%d) to be a multiple of 4", a->kL);
     return FA_ERR_UNSUPPORTED;
@@ -189,6 +193,21 @@ int validate(const fa_fwd_args* a) {
   return FA_OK;
 }
 
+long long align256(long long bytes) { return (bytes + 255) / 256 * 256; }
+
+// Workspace of the pre-rounded fp32 plan (0: the plan does not apply).  It
+// pays off once every work unit streams many key blocks, where rounding K and
+// transposing V per tile in shared memory costs the kernel most; it covers
+// the plain forward (masks allowed, no window, softcap, offset or dropout).
+long long pre_workspace_bytes(const fa_fwd_args* a) {
+  if (a->dtype != FA_DTYPE_F32 || a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f ||
+      a->dropout_p != 0.0f || a->kL < 1024 || (long long)a->B * a->H_kv > 65535)
+    return 0;
+  const long long vt_row = (a->kL + 3) / 4 * 4;
+  return align256((long long)a->B * a->H_q * a->qL * a->D * 4) + align256((long long)a->B * a->H_kv * a->kL * a->D * 4) +
+         align256((long long)a->B * a->H_kv * a->D * vt_row * 4);
+}
+
 }  // namespace
 
 void set_error(const char* fmt, ...) {
@@ -221,6 +240,14 @@ int fa_fwd_ex(const fa_fwd_args* a) {
   g_err[0] = '\0';
   int rc = validate(a);
   if (rc != FA_OK) return rc;
+  // fp32 with a workspace: round Q and K and transpose V once in HBM, then
+  // run the plan that streams them by TMA (no helper warps).
+  const long long pre_bytes = pre_workspace_bytes(a);
+  if (a->workspace && pre_bytes > 0 && a->workspace_bytes < pre_bytes) {
+    set_error("workspace of %lld bytes is smaller than the %lld this call needs (fa_fwd_workspace_bytes)",
+              a->workspace_bytes, pre_bytes);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -260,6 +287,7 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     la.os[i] = a->o_strides[i];
     la.ms[i] = a->mask_kind ? a->mask_strides[i] : 0;
   }
+  la.vt_row = 0;
   la.mask_vec = 0;
   if (a->mask_kind != FA_MASK_NONE) {
     const int mesz = (a->mask_kind == FA_MASK_BOOL) ? 1 : (a->dtype == FA_DTYPE_F32 ? 4 : 2);
@@ -290,6 +318,27 @@ int fa_fwd_ex(const fa_fwd_args* a) {
     const long long units2 = (long long)((a->qL + 255) / 256) * a->B * a->H_q;
     const int sms = la.max_ctas > 0 ? std::min(la.max_ctas, la.num_sms) : la.num_sms;
     one_tile = policy == 1 || (policy == 0 && units2 < sms);
+  }
+  if (a->workspace && pre_bytes > 0) {
+    uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+    float* qr = reinterpret_cast<float*>(ws);
+    float* kr = reinterpret_cast<float*>(ws + align256((long long)a->B * a->H_q * a->qL * a->D * 4));
+    float* vt = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(kr) +
+                                         align256((long long)a->B * a->H_kv * a->kL * a->D * 4));
+    la.vt_row = (a->kL + 3) / 4 * 4;
+    rc = launch_tf32_prep(la, qr, kr, vt);
+    if (rc != FA_OK) return rc;
+    const long long Dl = a->D;
+    la.q = qr;
+    la.qs[0] = (long long)a->H_q * a->qL * Dl;
+    la.qs[1] = (long long)a->qL * Dl;
+    la.qs[2] = Dl;
+    la.k = kr;
+    la.ks[0] = (long long)a->H_kv * a->kL * Dl;
+    la.ks[1] = (long long)a->kL * Dl;
+    la.ks[2] = Dl;
+    la.v = vt;
+    return a->D == 64 ? launch_pre_f32_d64(la) : a->D == 128 ? launch_pre_f32_d128(la) : launch_pre_f32_d256(la);
   }
   switch (a->dtype) {
     case FA_DTYPE_F32:
@@ -324,6 +373,13 @@ int fa_fwd_ex(const fa_fwd_args* a) {
       break;
   }
   return rc;
+}
+
+long long fa_fwd_workspace_bytes(const fa_fwd_args* a) {
+  using namespace fa;
+  g_err[0] = '\0';
+  if (validate(a) != FA_OK) return -1;
+  return pre_workspace_bytes(a);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q, int H_kv, int qL,
@@ -499,6 +555,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   return launch_bwd(a);
 }
 
-int fa_version(void) { return 105; }
+int fa_version(void) { return 106; }
 
 }  // extern "C"

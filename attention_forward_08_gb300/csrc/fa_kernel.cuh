@@ -67,9 +67,16 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr long long kDrainCycles = 1LL << 33;
 
 template <bool kTf32_, int kD_, int kNQT_, int kBN_, int kKStages_, int kVStages_, int kVTStages_ = 0,
-          bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false>
+          bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false, bool kPre_ = false>
 struct Cfg {
   static constexpr bool kTf32 = kTf32_;
+  // fp32 I/O whose Q and K arrive already rounded to tf32 and whose V arrives
+  // rounded and transposed ([B, H_kv, D, keys], from the pre-pass): the
+  // producer loads the K-major V^T tiles straight into the V ring and no
+  // helper warps run.  Otherwise fp32 I/O rounds and transposes in shared
+  // memory with helper warps.
+  static constexpr bool kPre = kPre_;
+  static constexpr bool kHelpers = kTf32 && !kPre;
   // Sliding window, softcap and query offset compiled in (a separate
   // instantiation, so the plain forward keeps its exact code).
   static constexpr bool kFeat = kFeat_;
@@ -113,8 +120,8 @@ struct Cfg {
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
   // tf32 helper warps: warps 2-3, plus warps 8-11 when there is one Q tile
   // (rounding K and transposing V then keep pace with the tensor core).
-  static constexpr bool kExtraHelpers = kTf32 && kNQT == 1;
-  static constexpr int kCvtWarps = kTf32 ? (kExtraHelpers ? 6 : 2) : 1;
+  static constexpr bool kExtraHelpers = kHelpers && kNQT == 1;
+  static constexpr int kCvtWarps = kHelpers ? (kExtraHelpers ? 6 : 2) : 1;
   static constexpr int kCvtThreads = 32 * kCvtWarps;
   static constexpr int kThreads = 128 * (1 + kNQT) + (kExtraHelpers ? 128 : 0);
   // Per-thread registers at launch, and the split after setmaxnreg: the
@@ -153,7 +160,9 @@ struct Cfg {
   static_assert(kTmemUsed <= 512, "TMEM overflow");
   static_assert(kSmemBytes <= 232448, "shared memory overflow");
   static_assert(kKStages >= 1 && kVStages >= 1 && kKStages <= 4 && kVStages <= 4, "ring size");
-  static_assert(kTf32 ? (kVTStages >= 1 && kVTStages <= 4) : kVTStages == 0, "V^T ring is for TF32 only");
+  static_assert(kHelpers ? (kVTStages >= 1 && kVTStages <= 4) : kVTStages == 0,
+                "the V^T ring is for TF32 with helper warps only");
+  static_assert(!kPre || kTf32, "pre-rounded inputs are fp32");
   static_assert(!(kTf32 && kF16), "fp16 I/O uses the 16-bit path");
   static_assert(!kDrop || kFeat, "the dropout instantiation includes the other features");
 };
@@ -711,7 +720,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&ctl->k_empty[s], C::kIssuers);  // one commit per issuing thread
       mbar_init(&ctl->k_ready[s], C::kCvtWarps);
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->v_empty[s], C::kTf32 ? C::kCvtWarps : C::kIssuers);  // tf32: released by the helper warps
+      mbar_init(&ctl->v_empty[s], C::kHelpers ? C::kCvtWarps : C::kIssuers);  // tf32: released by the helper warps
       mbar_init(&ctl->vt_full[s], C::kCvtWarps);
       mbar_init(&ctl->vt_empty[s], C::kIssuers);
     }
@@ -821,10 +830,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(&ctl->v_full[slot], C::kKVTileBytes);
             uint8_t* dst = sV + slot * C::kKVTileBytes;
+            if constexpr (C::kPre) {
+              // V^T [.., D, keys]: 32-key column blocks of D rows (K-major B of O += P V)
 #pragma unroll
-            for (int c = 0; c < C::kNChunk; ++c)
-              tma_load_4d(dst + c * (C::kBN * 128), &tmV, &ctl->v_full[slot], c * C::kChunk, jv * C::kBN, w.kvh,
-                          w.b);
+              for (int c = 0; c < C::kBN / 32; ++c)
+                tma_load_4d(dst + c * (C::kD * 128), &tmV, &ctl->v_full[slot], jv * C::kBN + c * 32, 0, w.kvh, w.b);
+            } else {
+#pragma unroll
+              for (int c = 0; c < C::kNChunk; ++c)
+                tma_load_4d(dst + c * (C::kBN * 128), &tmV, &ctl->v_full[slot], c * C::kChunk, jv * C::kBN, w.kvh,
+                            w.b);
+            }
             ++v_issued;
           }
         }
@@ -861,7 +877,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // tf32: V^T tile, rows = D (the MMA's N), keys along the 128-byte rows (K-major).
       // bf16: V tile, rows = keys (the MMA's K), 128 bytes of D per row; D column
       // blocks are kBN*128 bytes apart (LBO), 8-key groups 1024 apart (SBO).
-      const uint64_t dV = C::kTf32 ? make_sdesc_sw128(smem_u32(sVT), 16, 1024)
+      const uint64_t dV = C::kTf32 ? make_sdesc_sw128(smem_u32(C::kHelpers ? sVT : sV), 16, 1024)
                                    : make_sdesc_sw128(smem_u32(sV), C::kBN * 128, 1024);
       const uint32_t q_lo = (uint32_t)dQ, q_hi = (uint32_t)(dQ >> 32);
       const uint32_t k_lo = (uint32_t)dK, k_hi = (uint32_t)(dK >> 32);
@@ -923,7 +939,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int t = 0; t < C::kNQT; ++t) {
           if (t < t_begin || t >= t_end || !ok || w.nblk[t] == 0) continue;
           const uint32_t par = q_used[t] & 1;
-          ok = C::kTf32 ? wait_bounded(&ctl->q_ready[t], par, abort_flag, p.status, p.timeout_cycles)
+          ok = C::kHelpers ? wait_bounded(&ctl->q_ready[t], par, abort_flag, p.status, p.timeout_cycles)
                         : wait_bounded(&ctl->q_full[t], par, abort_flag, p.status, p.timeout_cycles);
           ++q_used[t];
         }
@@ -931,7 +947,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         int kslot = k_used % C::kKStages;
         if (ok) {
           const uint32_t par = (k_used / C::kKStages) & 1;
-          ok = C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
+          ok = C::kHelpers ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
                         : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
         }
         if (ok) ok = wait_turn();
@@ -958,7 +974,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (j + 1 < w.N) {
               kslot = k_used % C::kKStages;
               const uint32_t par = (k_used / C::kKStages) & 1;
-              ok = C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
+              ok = C::kHelpers ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
                             : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
               if (!ok) break;
               tc_fence_after();
@@ -968,9 +984,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               mma_commit(&ctl->k_empty[kslot]);
               ++k_used;
             }
-            const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
-            const uint32_t vpar = (C::kTf32 ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
-            ok = C::kTf32 ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
+            const int vslot = C::kHelpers ? v_used % C::kVTStages : v_used % C::kVStages;
+            const uint32_t vpar = (C::kHelpers ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
+            ok = C::kHelpers ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
                           : wait_bounded(&ctl->v_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles);
             if (!ok) break;
             ok = wait_bounded(&ctl->p_ready[0], p_seen[0] & 1, abort_flag, p.status, p.timeout_cycles);
@@ -982,16 +998,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             tc_fence_after();
             issue_PV(0, j, vslot, j == unit_j0<C>(w));
             mma_commit(&ctl->o_ready[0]);
-            mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
+            mma_commit(C::kHelpers ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
             ++v_used;
           }
         } else
         // P over S (two Q tiles): per block and tile, PV_j then S_{j+1}.
         for (int j = unit_j0<C>(w); j < w.N && ok; ++j) {
           // bf16: V ring slot; tf32: V^T ring slot
-          const int vslot = C::kTf32 ? v_used % C::kVTStages : v_used % C::kVStages;
-          const uint32_t vpar = (C::kTf32 ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
-          ok = C::kTf32 ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
+          const int vslot = C::kHelpers ? v_used % C::kVTStages : v_used % C::kVStages;
+          const uint32_t vpar = (C::kHelpers ? v_used / C::kVTStages : v_used / C::kVStages) & 1;
+          ok = C::kHelpers ? wait_bounded(&ctl->vt_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles)
                         : wait_bounded(&ctl->v_full[vslot], vpar, abort_flag, p.status, p.timeout_cycles);
           if (!ok) break;
           const bool next = (j + 1 < w.N);
@@ -1001,7 +1017,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (k_waited) return true;
             k_waited = true;
             const uint32_t par = (k_used / C::kKStages) & 1;
-            return C::kTf32 ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
+            return C::kHelpers ? wait_bounded(&ctl->k_ready[kslot], par, abort_flag, p.status, p.timeout_cycles)
                             : wait_bounded(&ctl->k_full[kslot], par, abort_flag, p.status, p.timeout_cycles);
           };
           bool turn_taken = false;
@@ -1040,7 +1056,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!ok) break;
           }
           pass_turn();
-          mma_commit(C::kTf32 ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
+          mma_commit(C::kHelpers ? &ctl->vt_empty[vslot] : &ctl->v_empty[vslot]);
           ++v_used;
           if (next) {
             // Tiles that stop earlier (causal) never waited on K_{j+1}; make sure
@@ -1062,7 +1078,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     __syncwarp();
   } else {
     // ===================================================== tf32 helpers (fp32 I/O only)
-    if constexpr (C::kTf32) tf32_helpers<C>(sQ, sK, sV, sVT, ctl, p, abort_flag, num_units, threadIdx.x - 64, lane);
+    if constexpr (C::kHelpers) tf32_helpers<C>(sQ, sK, sV, sVT, ctl, p, abort_flag, num_units, threadIdx.x - 64, lane);
   }
   } else if (C::kExtraHelpers && warp >= 8) {
     // ===================================================== more tf32 helpers (one Q tile)

@@ -26,6 +26,7 @@ struct LaunchArgs {
   float dropout_p;       // 0 = off
   unsigned long long dropout_seed, dropout_offset;
   long long qs[3], ks[3], vs[3], os[3], ms[3];  // element strides: batch, head, row
+  long long vt_row;      // pre-rounded fp32 plans: v is V^T [B, H_kv, D, vt_row] (keys innermost)
   int mask_vec;
   cudaStream_t stream;
   unsigned int* status;
@@ -71,12 +72,41 @@ inline bool encode_bhsd(CUtensorMap* map, CUtensorMapDataType dt, const void* pt
   return true;
 }
 
+// The transposed, tf32-rounded V of the pre-rounded fp32 plans: V^T
+// [B, H_kv, D, vt_row] fp32 (vt_row >= kL, a multiple of 4), tiled as
+// {32 keys (128 bytes), D rows} with 128-byte swizzle: one K-major column block
+// of the O += P V operand per load.  Keys past kL read as zero.
+inline bool encode_vt(CUtensorMap* map, const void* ptr, int B, int H, int kL, int D, long long vt_row) {
+  cuuint64_t dims[4] = {(cuuint64_t)kL, (cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)B};
+  const long long row = vt_row * 4, head = row * D, batch = head * H;
+  cuuint64_t strides[3] = {(cuuint64_t)row, (cuuint64_t)(H > 1 ? head : 16), (cuuint64_t)(B > 1 ? batch : 16)};
+  cuuint32_t box[4] = {32, (cuuint32_t)D, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) {
+    set_error("cuTensorMapEncodeTiled is not available from the CUDA driver");
+    return false;
+  }
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled (V^T) failed (CUresult %d)", (int)r);
+    return false;
+  }
+  return true;
+}
+
 template <class C>
 int launch_fa_fwd(const LaunchArgs& a) {
   CUtensorMap tq, tk, tv, tm;
   if (!encode_bhsd(&tq, C::kTmaType, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
   if (!encode_bhsd(&tk, C::kTmaType, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
-  if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
+  if constexpr (C::kPre) {
+    if (!encode_vt(&tv, a.v, a.B, a.Hkv, a.kL, a.D, a.vt_row)) return 4;
+  } else {
+    if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
+  }
   // Mask tiles (128-byte column blocks x kBM rows, 128-byte swizzle) for the
   // L2 prefetch and the shared-memory mask path, when the mask's layout suits
   // TMA (aligned base, 16-byte multiple strides, no stride-0 broadcast).
@@ -202,6 +232,12 @@ using CfgBf16D256 = Cfg<false, 256, 1, 128, 1, 1>;  // smem 192 KB, TMEM 512 (P 
 using CfgF32D64   = Cfg<true, 64,   2, 64, 2, 2, 2>;  // smem 160 KB, TMEM 256
 using CfgF32D128  = Cfg<true, 128,  1, 64, 2, 1, 2>;  // smem 224 KB, TMEM 320
 using CfgF32D256  = Cfg<true, 256,  1, 32, 1, 1, 1>;  // smem 224 KB, TMEM 352
+// fp32 with the pre-pass (Q, K rounded, V rounded and transposed in HBM): no
+// helper warps; the V ring holds K-major V^T tiles.
+//                       tf32  D   Q tiles BN K   V  VT  f16    feat   drop   pre
+using CfgF32PreD64  = Cfg<true, 64,  1, 64, 4, 4, 0, false, false, false, true>;  // smem 160 KB, TMEM 256
+using CfgF32PreD128 = Cfg<true, 128, 1, 64, 3, 2, 0, false, false, false, true>;  // smem 224 KB, TMEM 320
+using CfgF32PreD256 = Cfg<true, 256, 1, 32, 2, 1, 0, false, false, false, true>;  // smem 224 KB, TMEM 352
 // fp16 I/O: the bf16 plans with the f16 operand format.
 using CfgF16D64   = Cfg<false, 64,  2, 128, 4, 4, 0, true>;
 using CfgF16D128  = Cfg<false, 128, 2, 128, 2, 2, 0, true>;
@@ -242,6 +278,12 @@ int launch_feat_f32_d256(const LaunchArgs& a);
 int launch_feat_f16_d64(const LaunchArgs& a);
 int launch_feat_f16_d128(const LaunchArgs& a);
 int launch_feat_f16_d256(const LaunchArgs& a);
+// ... and of the pre-rounded fp32 plans, with the pre-pass that feeds them
+// (defined in fa_tf32_prep.cu).
+int launch_pre_f32_d64(const LaunchArgs& a);
+int launch_pre_f32_d128(const LaunchArgs& a);
+int launch_pre_f32_d256(const LaunchArgs& a);
+int launch_tf32_prep(const LaunchArgs& a, float* qr, float* kr, float* vt);
 // ... and of the dropout instantiation (the features plus dropout).
 int launch_drop_bf16_d64(const LaunchArgs& a);
 int launch_drop_bf16_d128(const LaunchArgs& a);

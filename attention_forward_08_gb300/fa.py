@@ -52,6 +52,7 @@ class FaFwdArgs(ctypes.Structure):
         ("stream", ctypes.c_void_p),
         ("window", ctypes.c_int), ("q_offset", ctypes.c_int), ("softcap", ctypes.c_float),
         ("dropout_p", ctypes.c_float), ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_ulonglong),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_longlong),
     ]
 
 
@@ -72,6 +73,8 @@ def load_library(path: str = LIB_PATH):
         [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     lib.fa_fwd_ex.restype = ctypes.c_int
     lib.fa_fwd_ex.argtypes = [ctypes.POINTER(FaFwdArgs)]
+    lib.fa_fwd_workspace_bytes.restype = ctypes.c_longlong
+    lib.fa_fwd_workspace_bytes.argtypes = [ctypes.POINTER(FaFwdArgs)]
     lib.fa_last_error.restype = ctypes.c_char_p
     lib.fa_last_error.argtypes = []
     lib.fa_sync_status.restype = ctypes.c_int
@@ -112,6 +115,11 @@ def fa_fwd(q, k, v, o, lse, B, H_q, H_kv, qL, kL, D, scale, causal, mask, mask_k
 
 def fa_fwd_ex(args: FaFwdArgs) -> int:
     return load_library().fa_fwd_ex(ctypes.byref(args))
+
+
+def fa_fwd_workspace_bytes(args: FaFwdArgs) -> int:
+    """``fa_fwd_workspace_bytes`` of include/fa.h: scratch bytes the fastest plan wants (0: none, -1: invalid)."""
+    return load_library().fa_fwd_workspace_bytes(ctypes.byref(args))
 
 
 def fa_last_error() -> str:
@@ -234,9 +242,38 @@ def make_args(q, k, v, o, lse, *, scale=None, causal=False, mask=None, mask_kind
     return a
 
 
+def attach_workspace(args, device, workspace=None):
+    """Give ``args`` the scratch its fastest plan needs (``fa_fwd_workspace_bytes``):
+    ``workspace`` if given (a device tensor), else a new one from torch's
+    allocator on the current stream; ``workspace=False`` leaves the call
+    without.  Returns the tensor or None.  A call on another stream than the
+    current one should pass its own workspace and keep it alive until the call
+    has run."""
+    import torch
+    if workspace is False:
+        return None
+    need = fa_fwd_workspace_bytes(args)
+    if need < 0:
+        _check(FA_ERR_INVALID_ARGUMENT)
+    if need == 0:
+        return None
+    if workspace is None:
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=device)
+    base = workspace.data_ptr()
+    start = (base + 255) // 256 * 256
+    if workspace.numel() * workspace.element_size() - (start - base) < need:
+        raise ValueError(f"workspace holds fewer than the {need} bytes (256-byte aligned) required")
+    args.workspace, args.workspace_bytes = start, need
+    return workspace
+
+
 def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, out=None, lse=None,
-              stream=None, window=0, q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0):
-    """O and L for torch CUDA tensors (see ``make_args``); returns (o, lse)."""
+              stream=None, window=0, q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0,
+              workspace=None):
+    """O and L for torch CUDA tensors (see ``make_args``); returns (o, lse).
+
+    workspace: scratch for plans that want one (see ``attach_workspace``):
+    None allocates it when needed, False runs without."""
     import torch
     B, H_q, qL, D = q.shape
     if out is None:
@@ -246,7 +283,9 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
     args = make_args(q, k, v, out, lse, scale=scale, causal=causal, mask=mask, mask_kind=mask_kind,
                      stream=stream, window=window, q_offset=q_offset, softcap=softcap, dropout_p=dropout_p,
                      dropout_seed=dropout_seed, dropout_offset=dropout_offset)
+    ws = attach_workspace(args, q.device, workspace)
     _check(fa_fwd_ex(args))
+    del ws  # torch hands the block out again only to work queued later on the same stream
     return out, lse
 
 

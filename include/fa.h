@@ -124,9 +124,28 @@ typedef struct fa_fwd_args {
   float dropout_p;                   /* keep each weight of O with probability 1 - p, scaled by 1/(1-p) */
   unsigned long long dropout_seed;   /* generator key */
   unsigned long long dropout_offset; /* generator counter of position 0 */
+  /* Added in ABI 1.06 (NULL / 0 = none): */
+  void* workspace;           /* optional caller-owned device scratch, 256-byte aligned */
+  long long workspace_bytes; /* its size in bytes */
 } fa_fwd_args;
 
 int fa_fwd_ex(const fa_fwd_args* args);
+
+/*
+ * fa_fwd_workspace_bytes -- device scratch that lets fa_fwd_ex run the faster
+ * plan for these arguments (all fields filled as for the call), or 0 when no
+ * plan needs one; -1 (with the message set) when the arguments are invalid.
+ * Today: fp32 I/O (TF32) without window, softcap, offset or dropout and with
+ * kL >= 1024, where the library rounds Q and K to tf32 and transposes V once
+ * into the workspace (one extra launch) instead of per tile inside the kernel:
+ * 4 * (B*H_q*qL*D + B*H_kv*kL*D + B*H_kv*D*ceil4(kL)) bytes, each part rounded
+ * up to 256.  Results are the same either way (both round to nearest before
+ * the products).  fa_fwd_ex uses the workspace when workspace is non-NULL and
+ * this function returns > 0; a non-NULL workspace smaller than that is
+ * FA_ERR_INVALID_ARGUMENT.  The contents on entry do not matter; they are
+ * clobbered, and the workspace must not overlap any argument.
+ */
+long long fa_fwd_workspace_bytes(const fa_fwd_args* args);
 
 /* Message for the last non-FA_OK return on the calling thread ("" if none). */
 const char* fa_last_error(void);
@@ -220,7 +239,7 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    int causal, int dtype, void* stream);
 
 /* ABI version: major * 100 + minor (1.05: fa_bwd and fa_bwd_noalloc accept
- * FA_DTYPE_F16). */
+ * FA_DTYPE_F16; 1.06: fa_fwd_args.workspace, fa_fwd_workspace_bytes). */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -15,8 +15,9 @@ import workloads
 TOL = {"bf16": (2e-2, 1e-2), "f16": (5e-3, 2.5e-3), "f32": (2e-3, 1e-3)}
 
 
-def gpu_run(w: workloads.Workload, q, k, v, mask, scale=None):
-    """Copy the CPU inputs to cuda:0, run the library, return (O, L) as fp64 numpy, O in [B,H,qL,D]."""
+def gpu_run(w: workloads.Workload, q, k, v, mask, scale=None, workspace=None):
+    """Copy the CPU inputs to cuda:0, run the library, return (O, L) as fp64 numpy, O in [B,H,qL,D].
+    workspace=False runs without the library's scratch (fp32: the in-kernel tf32 helper plan)."""
     import attention_forward_08_gb300 as fa
     dev = torch.device("cuda:0")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -31,7 +32,7 @@ def gpu_run(w: workloads.Workload, q, k, v, mask, scale=None):
     fa.attention(qd, kd, vd, scale=w.sm_scale if scale is None else scale, causal=w.causal, mask=md,
                  mask_kind=None if mask is None else w.mask_kind, out=o, lse=lse, window=w.window,
                  q_offset=w.q_offset, softcap=w.softcap, dropout_p=w.dropout_p, dropout_seed=w.dropout_seed,
-                 dropout_offset=w.dropout_offset)
+                 dropout_offset=w.dropout_offset, workspace=workspace)
     rc = fa.fa_sync_status(None)
     assert rc == 0, f"device status {rc}: {fa.fa_last_error()}"
     if w.layout == "dit":

@@ -29,7 +29,8 @@ def _declared_functions():
 
 def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
-        ["fa_fwd", "fa_fwd_ex", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc", "fa_last_error",
+        ["fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc",
+         "fa_last_error",
          "fa_sync_status",
          "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_timeout_cycles", "fa_version"])
 
@@ -61,7 +62,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 105
+    assert fa.fa_version() == 106
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -130,6 +131,41 @@ def test_dropout_arguments_validated(fa):
     for t in (a.k_strides, a.v_strides):
         t[:] = (2 * 66 * 64, 66 * 64, 64)
     assert fa.fa_fwd_ex(a) == 2 and "multiple of 4" in fa.fa_last_error()
+
+
+def _fwd_args(fa, dtype, B, H_q, H_kv, qL, kL, D):
+    a = fa.FaFwdArgs()
+    a.q = a.k = a.v = a.o = a.lse = P
+    a.B, a.H_q, a.H_kv, a.qL, a.kL, a.D = B, H_q, H_kv, qL, kL, D
+    a.scale, a.dtype = D ** -0.5, dtype
+    a.q_strides[:] = a.o_strides[:] = (H_q * qL * D, qL * D, D)
+    a.k_strides[:] = a.v_strides[:] = (H_kv * kL * D, kL * D, D)
+    return a
+
+
+def test_forward_workspace_size(fa):
+    """fa_fwd_workspace_bytes: the tf32 pre-pass plan (fp32, plain, kL >= 1024) wants rounded Q and K and a
+    transposed V with rows padded to 4 keys, each part 256-byte aligned; other calls want nothing."""
+    al = lambda n: (n + 255) // 256 * 256
+    a = _fwd_args(fa, 0, 2, 4, 2, 300, 1030, 128)
+    want = al(2 * 4 * 300 * 128 * 4) + al(2 * 2 * 1030 * 128 * 4) + al(2 * 2 * 128 * 1032 * 4)
+    assert fa.fa_fwd_workspace_bytes(a) == want
+    assert fa.fa_fwd_workspace_bytes(_fwd_args(fa, 1, 2, 4, 2, 300, 1030, 128)) == 0   # bf16
+    assert fa.fa_fwd_workspace_bytes(_fwd_args(fa, 0, 1, 2, 2, 128, 128, 64)) == 0     # short kL
+    a.window = 64
+    assert fa.fa_fwd_workspace_bytes(a) == 0
+    a.window, a.H_q = 0, 3                                                            # 3 % 2 != 0
+    assert fa.fa_fwd_workspace_bytes(a) == -1 and "divisible" in fa.fa_last_error()
+
+
+def test_forward_workspace_validated(fa):
+    """fa_fwd_ex: a misaligned workspace, or one smaller than the plan needs, is rejected before any launch."""
+    a = _fwd_args(fa, 0, 1, 2, 2, 256, 2048, 64)
+    need = fa.fa_fwd_workspace_bytes(a)
+    a.workspace, a.workspace_bytes = P + 16, need
+    assert fa.fa_fwd_ex(a) == 1 and "256-byte" in fa.fa_last_error()
+    a.workspace, a.workspace_bytes = P, need - 256
+    assert fa.fa_fwd_ex(a) == 1 and "smaller" in fa.fa_last_error()
 
 
 def test_no_gpu_is_a_cuda_error(fa):

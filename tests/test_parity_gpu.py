@@ -50,12 +50,13 @@ SMALL = [
 ]
 
 
-def _run_small(w, scale=None, mask=None, qkv=None, tol_mult=1.0, tol_mult_l=None, tf32_relative=False):
+def _run_small(w, scale=None, mask=None, qkv=None, tol_mult=1.0, tol_mult_l=None, tf32_relative=False,
+               workspace=None):
     if qkv is None:
         q, k, v, m = W.make_inputs(w)
     else:
         (q, k, v), m = qkv, mask
-    o_g, l_g, _ = gpu_run(w, q, k, v, m, scale=scale)
+    o_g, l_g, _ = gpu_run(w, q, k, v, m, scale=scale, workspace=workspace)
     qo, ko, vo, mo = oracle_inputs(q, k, v, m)
     o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w, scale), causal=w.causal, mask=mo,
                                 mask_kind=w.mask_kind if m is not None else 0, **oracle_features(w))
@@ -85,6 +86,30 @@ def test_small_both_tile_plans(w, q_tiles):
         _run_small(w)
     finally:
         fa.fa_set_q_tiles(0)
+
+
+# fp32 I/O has two plans once kL >= 1024: the tf32 pre-pass (Q, K rounded and V
+# rounded and transposed in a workspace, then a TMA-only kernel) and the
+# in-kernel helper warps (no workspace).  Both against the oracle: ragged kL
+# (V^T rows padded to 4 keys), GQA, causal, each head dim, an additive mask.
+FP32_PLANS = [
+    S("f32pre_d128_ragged_kl", 1, 2, 2, 300, 1030, 128, "f32", seed=91),
+    S("f32pre_d64_causal_gqa", 1, 4, 2, 1030, 1030, 64, "f32", causal=True, seed=92),
+    S("f32pre_d256_additive", 1, 2, 2, 260, 1024, 256, "f32", mask_kind=W.MASK_ADDITIVE, seed=93),
+    S("f32pre_d128_b2_causal_qlonger", 2, 2, 1, 1300, 1100, 128, "f32", causal=True, seed=94),
+]
+
+
+@pytest.mark.parametrize("workspace", [None, False], ids=["prepass", "helpers"])
+@pytest.mark.parametrize("w", FP32_PLANS, ids=lambda w: w.name)
+def test_fp32_both_plans(w, workspace):
+    import attention_forward_08_gb300 as fa
+    q, k, v, m = W.make_inputs(w)
+    qd = q.cuda()
+    args = fa.make_args(qd, k.cuda(), v.cuda(), torch.empty_like(qd), torch.empty((w.B, w.H_q, w.qL), device="cuda"),
+                        scale=w.sm_scale, causal=w.causal)
+    assert fa.fa_fwd_workspace_bytes(args) > 0  # the pre-pass plan applies to these shapes
+    _run_small(w, qkv=(q, k, v), mask=m, workspace=workspace)
 
 
 # Sliding window, softcap and query offset on every kernel plan (two Q tiles,
