@@ -97,6 +97,60 @@ def traffic_from_profiles(w: workloads.Workload, kind: str = "fwd"):
     return float(m.group(1))
 
 
+class CopyPipeline:
+    """End-to-end steps: upload the step's inputs from pinned host memory, make the
+    call, download its results to pinned host memory, with uploads, calls and
+    downloads on three streams and two device buffer sets, so that step s+1's
+    upload and step s-1's download overlap step s's call.  (Splitting the copies
+    over more streams measured no faster: one upload stream already saturates
+    the host link.)  Each set is (device inputs, device outputs, pinned host
+    outputs, launch(stream_handle))."""
+
+    def __init__(self, dev, host_in, sets):
+        import torch
+        self.torch = torch
+        self.host_in, self.sets = host_in, sets
+        self.up, self.compute, self.down = (torch.cuda.Stream(dev) for _ in range(3))
+        self.ev = {k: [torch.cuda.Event() for _ in sets] for k in ("up", "comp", "down")}
+
+    def step(self, s):
+        torch = self.torch
+        b = s % len(self.sets)
+        din, dout, hout, launch = self.sets[b]
+        with torch.cuda.stream(self.up):
+            self.up.wait_event(self.ev["comp"][b])      # the last call reading this set's inputs is done
+            for d_, h_ in zip(din, self.host_in):
+                d_.copy_(h_, non_blocking=True)
+            self.ev["up"][b].record(self.up)
+        self.compute.wait_event(self.ev["up"][b])
+        self.compute.wait_event(self.ev["down"][b])     # this set's last outputs have left the device
+        launch(self.compute.cuda_stream)
+        self.ev["comp"][b].record(self.compute)
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(self.ev["comp"][b])
+            for h_, d_ in zip(hout, dout):
+                h_.copy_(d_, non_blocking=True)
+            self.ev["down"][b].record(self.down)
+
+    def time_ms(self, steps, warmup, dev, world):
+        torch = self.torch
+        for s in range(warmup):
+            self.step(s)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.compute)
+        for s in range(steps):
+            self.step(s)
+        self.compute.wait_stream(self.up)
+        self.compute.wait_stream(self.down)
+        e1.record(self.compute)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return e0.elapsed_time(e1) / steps
+
+
 class ClockSampler:
     """Samples nvidia-smi SM clocks and throttle reasons while running."""
 
@@ -337,41 +391,37 @@ def run_ours(args, w):
     flops = w.flops()
     value = flops * world / (mean_ms * 1e-3) / 1e12
 
-    # ---- end to end through the C ABI: pinned host inputs -> device -> forward -> host outputs
-    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    mh = None if m is None else m.pin_memory()
-    oh = torch.empty(od.shape, dtype=q.dtype).pin_memory() if w.layout != "dit" else \
-        torch.empty((qL, H * D), dtype=q.dtype).pin_memory()
-    lh = torch.empty((B, H, qL), dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (0 if mh is None else mh.numel() * mh.element_size())
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
-    o_dev_src = o_tok if w.layout == "dit" else od
+    # ---- end to end through the C ABI: pinned host inputs -> device -> forward -> host outputs,
+    # uploads / calls / downloads pipelined over three streams (CopyPipeline)
+    host_in = [t.pin_memory() for t in ((q, k, v) if m is None else (q, k, v, m))]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
 
-    def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        if mh is not None:
-            md.copy_(mh, non_blocking=True)
-        launch()
-        oh.copy_(o_dev_src, non_blocking=True)
-        lh.copy_(lsed, non_blocking=True)
+    def make_set():
+        din = [t.to(dev) for t in host_in]
+        if w.layout == "dit":
+            o_t = torch.empty((qL, H * D), dtype=q.dtype, device=dev)
+            o_v = o_t.view(qL, H, D).permute(1, 0, 2).unsqueeze(0)
+        else:
+            o_t = o_v = torch.empty((B, H, qL, D), dtype=q.dtype, device=dev)
+        l_t = torch.empty((B, H, qL), dtype=torch.float32, device=dev)
+        sargs = fa.make_args(din[0], din[1], din[2], o_v, l_t, scale=w.sm_scale, causal=w.causal,
+                             mask=None if m is None else din[3], mask_kind=None if m is None else w.mask_kind,
+                             window=w.window, q_offset=w.q_offset, softcap=w.softcap, dropout_p=w.dropout_p,
+                             dropout_seed=w.dropout_seed, dropout_offset=w.dropout_offset)
+        sws = fa.attach_workspace(sargs, dev)
 
-    for _ in range(max(1, min(args.warmup, 3))):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+        def launch_on(stream_handle, sargs=sargs, sws=sws):
+            sargs.stream = stream_handle
+            rc = fa.fa_fwd_ex(sargs)
+            if rc != 0:
+                raise fa.FaError(rc, fa.fa_last_error())
+        hout = [torch.empty(o_t.shape, dtype=o_t.dtype).pin_memory(), torch.empty(l_t.shape).pin_memory()]
+        return din, [o_t, l_t], hout, launch_on
+
+    pipe = CopyPipeline(dev, host_in, [make_set(), make_set()])
+    d2h = sum(t.numel() * t.element_size() for t in pipe.sets[0][2])
     e_steps = max(3, min(args.steps, 50))
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+    e2e_ms = max_over_ranks(pipe.time_ms(e_steps, max(2, min(args.warmup, 4)), dev, world), world, dev)
     e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
@@ -506,31 +556,28 @@ def run_ours_bwd(args, w):
     flops = 2.5 * w.flops()
     value = flops * world / (mean_ms * 1e-3) / 1e12
 
-    # end to end: pinned host inputs (q, k, v, o, dO, L) -> device -> fa_bwd -> host dq, dk, dv
+    # end to end: pinned host inputs (q, k, v, o, dO, L) -> device -> fa_bwd -> host dq, dk, dv,
+    # uploads / calls / downloads pipelined over three streams (CopyPipeline)
     host_in = [t.cpu().pin_memory() for t in (qd, kd, vd, od, dod, lsed)]
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
-    dev_in = (qd, kd, vd, od, dod, lsed)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
 
-    def e2e_step():
-        for d_, h_ in zip(dev_in, host_in):
-            d_.copy_(h_, non_blocking=True)
-        launch()
-        for h_, d_ in zip(host_out, (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
+    def make_set():
+        din = [torch.empty_like(t) for t in (qd, kd, vd, od, dod, lsed)]
+        dout = [torch.empty_like(t) for t in (qd, kd, vd)]
+        sws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        sptrs = [t.data_ptr() for t in din] + [t.data_ptr() for t in dout] + [sws.data_ptr()]
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+        def launch_on(stream_handle, sptrs=sptrs, sws=sws):
+            rc = fa.fa_bwd(*sptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal,
+                           fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16, stream_handle)
+            if rc != 0:
+                raise fa.FaError(rc, fa.fa_last_error())
+        return din, dout, [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dout], launch_on
+
+    pipe = CopyPipeline(dev, host_in, [make_set(), make_set()])
+    d2h = sum(t.numel() * t.element_size() for t in pipe.sets[0][2])
     e_steps = max(3, min(args.steps, 20))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+    e2e_ms = max_over_ranks(pipe.time_ms(e_steps, 3, dev, world), world, dev)
 
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"]
