@@ -19,6 +19,10 @@
  * Rows with no allowed key have P = 0 and contribute nothing.  The mask and
  * the scale receive no gradient.
  *
+ * Allowed keys follow the forward's definition: j <= i + q_offset when
+ * causal (q_offset 0 = top-left), and with a sliding window (window > 0)
+ * j > i + q_offset - window as well.
+ *
  * Sources (web pages on the FlashAttention-2 forward and backward):
  *  - forge "flash_attention_mma.metal", section "backward (MMA)": the three
  *    products per block (S = Q K^T, dP = dO V^T, dS = P (dP - D) scale,
@@ -56,6 +60,7 @@ typedef struct {
     long long B, Hq, Hkv, qL, kL, D;
     double scale;
     int causal;
+    long long window, q_offset;  /* 0: off / top-left */
     long long g_begin, g_end;   /* this worker's (b, kvh) groups */
     double *S, *P, *dP;         /* kL doubles each */
 } bwd_job;
@@ -88,10 +93,18 @@ static void bwd_group(const bwd_job *J, long long grp)
                 double dot = 0.0;
                 for (long long d = 0; d < D; ++d) dot += qi[d] * kb[j * D + d];
                 double s = J->scale * dot;
+                const long long diag = i + J->q_offset;   /* the key aligned with row i */
 #if ORACLE_MUTANT == 5
-                int allowed = !J->causal || j < i;     /* mistake: causal off by one */
+                int allowed = !J->causal || j < diag;     /* mistake: causal off by one */
+#elif ORACLE_MUTANT == 7
+                int allowed = !J->causal || j <= i - J->q_offset;   /* mistake: offset sign */
 #else
-                int allowed = !J->causal || j <= i;
+                int allowed = !J->causal || j <= diag;
+#endif
+#if ORACLE_MUTANT == 8
+                if (J->window > 0) allowed = allowed && (j >= diag - J->window);  /* mistake: one key too wide */
+#else
+                if (J->window > 0) allowed = allowed && (j > diag - J->window);
 #endif
                 if (J->mask_kind == 1) {
                     allowed = allowed && ((const uint8_t *)J->mask)[((b * J->Hq + h) * qL + i) * kL + j] != 0;
@@ -159,12 +172,13 @@ static void *bwd_worker(void *arg)
  * dq [B,Hq,qL,D], dk and dv [B,Hkv,kL,D] are written in full.
  * n_threads <= 0 means one thread.  Returns 0, or -1 on a bad argument.
  */
-int oracle_attention_bwd(const double *q, const double *k, const double *v, const void *mask, int mask_kind,
-                         const double *dO, double *dq, double *dk, double *dv, long long B, long long Hq,
-                         long long Hkv, long long qL, long long kL, long long D, double scale, int causal,
-                         int n_threads)
+int oracle_attention_bwd_ex(const double *q, const double *k, const double *v, const void *mask, int mask_kind,
+                            const double *dO, double *dq, double *dk, double *dv, long long B, long long Hq,
+                            long long Hkv, long long qL, long long kL, long long D, double scale, int causal,
+                            long long window, long long q_offset, int n_threads)
 {
     if (!q || !k || !v || !dO || !dq || !dk || !dv) return -1;
+    if (window < 0) return -1;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || qL <= 0 || kL <= 0 || D <= 0) return -1;
     if (Hq % Hkv != 0) return -1;
     if (mask_kind < 0 || mask_kind > 2) return -1;
@@ -186,6 +200,7 @@ int oracle_attention_bwd(const double *q, const double *k, const double *v, cons
         J->dq = dq; J->dk = dk; J->dv = dv;
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->qL = qL; J->kL = kL; J->D = D;
         J->scale = scale; J->causal = causal;
+        J->window = window; J->q_offset = q_offset;
         J->g_begin = groups * t / n_threads;
         J->g_end = groups * (t + 1) / n_threads;
         J->S = scratch + (size_t)kL * (3 * (size_t)t);
@@ -202,6 +217,16 @@ int oracle_attention_bwd(const double *q, const double *k, const double *v, cons
     for (int t = started + 1; t < n_threads; ++t) bwd_worker(&jobs[t]);
     free(jobs); free(tids); free(scratch);
     return 0;
+}
+
+/* The plain gradients: no window, top-left causal. */
+int oracle_attention_bwd(const double *q, const double *k, const double *v, const void *mask, int mask_kind,
+                         const double *dO, double *dq, double *dk, double *dv, long long B, long long Hq,
+                         long long Hkv, long long qL, long long kL, long long D, double scale, int causal,
+                         int n_threads)
+{
+    return oracle_attention_bwd_ex(q, k, v, mask, mask_kind, dO, dq, dk, dv, B, Hq, Hkv, qL, kL, D, scale, causal,
+                                   0, 0, n_threads);
 }
 
 /* Number of the planted mistake this build carries (0 for the real oracle). */

@@ -36,6 +36,8 @@ MUTANTS = {
     4: "wrong heads summed into dK dV",
     5: "causal off by one",
     6: "dQ sign",
+    7: "query offset sign",
+    8: "window one key too wide",
 }
 
 
