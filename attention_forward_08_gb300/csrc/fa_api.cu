@@ -474,11 +474,19 @@ long long fa_bwd_workspace_bytes(int B, int H_q, int qL) {
   return (bytes + 255) / 256 * 256;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
-           void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv, int qL, int kL,
-           int D, float scale, int causal, int dtype, void* stream) {
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+              void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
+              int qL, int kL, int D, float scale, int causal, int window, int q_offset, int dtype, void* stream) {
   using namespace fa;
   g_err[0] = '\0';
+  if (window < 0) {
+    set_error("window (%d) must be >= 0 (0 = no sliding window)", window);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (q_offset <= -(1 << 30) || q_offset >= (1 << 30)) {
+    set_error("|q_offset| (%d) must be < 2^30", q_offset);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) {
     set_error("q, k, v, o, dout, lse, dq, dk, dv and workspace must all be non-NULL");
     return FA_ERR_INVALID_ARGUMENT;
@@ -549,12 +557,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.D = D;
   a.scale = scale;
   a.causal = causal ? 1 : 0;
+  a.window = window;
+  a.q_offset = q_offset;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = g_status_ptr[dev];
   a.timeout_cycles = timeout_cycles();
   return launch_bwd(a);
 }
 
-int fa_version(void) { return 106; }
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv, int qL, int kL,
+           int D, float scale, int causal, int dtype, void* stream) {
+  return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale,
+                   causal, 0, 0, dtype, stream);
+}
+
+int fa_version(void) { return 107; }
 
 }  // extern "C"

@@ -1,5 +1,6 @@
 // fa_bwd.cu -- launcher for the backward pass: tensor maps, grids, the three
-// launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 or fp16 I/O.
+// launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 or fp16 I/O,
+// with or without sliding window / causal diagonal offset.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -25,9 +26,9 @@ int set_smem_once(const void* kern, uint32_t bytes, int& configured_device) {
   return 0;
 }
 
-template <int kD, bool kF16>
+template <int kD, bool kF16, bool kFeat>
 int launch_bwd_d(const BwdLaunchArgs& a) {
-  using C = BwdCfg<kD, kF16>;
+  using C = BwdCfg<kD, kF16, kFeat>;
   // 1. D_i = rowsum(O_i * dO_i)
   const long long rows = (long long)a.B * a.Hq * a.qL;
   constexpr int kRowsPerBlock = 256 / (kD / 8);
@@ -57,6 +58,8 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   p.kL = a.kL;
   p.group = a.Hq / a.Hkv;
   p.causal = a.causal;
+  p.window = a.window;
+  p.q_offset = a.q_offset;
   p.n_qt = (a.qL + C::kTile - 1) / C::kTile;
   p.n_kt = (a.kL + C::kTile - 1) / C::kTile;
   p.scale = a.scale;
@@ -99,8 +102,12 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
 }  // namespace
 
 int launch_bwd(const BwdLaunchArgs& a) {
-  if (a.f16) return a.D == 64 ? launch_bwd_d<64, true>(a) : launch_bwd_d<128, true>(a);
-  return a.D == 64 ? launch_bwd_d<64, false>(a) : launch_bwd_d<128, false>(a);
+  if (a.window != 0 || a.q_offset != 0) {
+    if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true>(a) : launch_bwd_d<128, true, true>(a);
+    return a.D == 64 ? launch_bwd_d<64, false, true>(a) : launch_bwd_d<128, false, true>(a);
+  }
+  if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, false>(a) : launch_bwd_d<128, true, false>(a);
+  return a.D == 64 ? launch_bwd_d<64, false, false>(a) : launch_bwd_d<128, false, false>(a);
 }
 
 }  // namespace fa

@@ -47,6 +47,8 @@ struct BwdParams {
   int B, Hq, Hkv, qL, kL;
   int group;          // Hq / Hkv
   int causal;
+  int window;         // > 0: key j allowed only if j > i + q_offset - window (kFeat kernels)
+  int q_offset;       // causal diagonal of row i is key i + q_offset (kFeat kernels)
   int n_qt, n_kt;     // 128-row query tiles per (b, h), 128-key tiles per (b, kvh)
   float scale;        // softmax scale (applied to dQ and dK in the epilogue)
   float scale_log2;   // scale * log2(e)
@@ -59,11 +61,14 @@ struct BwdParams {
   long long timeout_cycles;
 };
 
-template <int kD_, bool kF16_ = false>
+template <int kD_, bool kF16_ = false, bool kFeat_ = false>
 struct BwdCfg {
   static constexpr int kD = kD_;
   // 16-bit I/O is bf16 unless kF16 (fp16): same kernels, other operand format.
   static constexpr bool kF16 = kF16_;
+  // Sliding window and causal diagonal offset compiled in (their own
+  // instantiations: the plain kernels keep their exact code).
+  static constexpr bool kFeat = kFeat_;
   static constexpr uint32_t kFmt = kF16 ? kFmtF16 : kFmtBf16;
   static constexpr CUtensorMapDataType kTmaType =
       kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -257,9 +262,25 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int rem = blockIdx.x - kt * per_kt;
   const int b = rem / p.Hkv, kvh = rem - b * p.Hkv;
   const int k0 = kt * C::kTile;
-  // Causal: only queries i >= k0 see this tile's keys.
-  const int qb0 = p.causal ? min(k0 / C::kTile, p.n_qt) : 0;
-  const int per_head = p.n_qt - qb0;
+  // Query blocks that see this tile's keys: causal, row i sees key j when
+  // j <= i + q_offset, so rows from k0 - q_offset; with a window, row i sees
+  // key j only while j > i + q_offset - window, so rows below
+  // j_max - q_offset + window.
+  int qb0, qb_end;
+  if constexpr (C::kFeat) {
+    const long long first = (long long)k0 - p.q_offset;
+    qb0 = !p.causal || first <= 0 ? 0 : (int)min(first / C::kTile, (long long)p.n_qt);
+    qb_end = p.n_qt;
+    if (p.window > 0) {
+      const long long jmax = min(k0 + C::kTile, p.kL) - 1;
+      const long long last_row = jmax - p.q_offset + p.window - 1;  // the last row that sees key jmax
+      qb_end = last_row < 0 ? 0 : (int)min(last_row / C::kTile + 1, (long long)p.n_qt);
+    }
+  } else {
+    qb0 = p.causal ? min(k0 / C::kTile, p.n_qt) : 0;
+    qb_end = p.n_qt;
+  }
+  const int per_head = max(0, qb_end - qb0);
   const int n_steps = p.group * per_head;
 
   if (threadIdx.x == 0) {
@@ -461,15 +482,30 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       float pr[128];
       tmem_ld128(tS, pr);
       // P^T_{j,c} = 2^(s * scale * log2e - L2_c); queries c < j - q0 are causally masked,
-      // and a key row past kL gets no probability at all.
-      int lim = p.causal ? j - q0 : 0;
-      if (j >= p.kL) lim = C::kTile;
+      // and a key row past kL gets no probability at all.  With the features:
+      // queries c < j - q_offset - q0 (causal) or c >= j - q_offset + window - q0
+      // (window) see no key j.
+      if constexpr (C::kFeat) {
+        int lim = p.causal ? j - p.q_offset - q0 : -(1 << 30);
+        int hi = p.window > 0 ? j - p.q_offset + p.window - q0 : (1 << 30);
+        if (j >= p.kL) lim = C::kTile;
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        float x0, x1;
-        ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2s[c], -l2s[c + 1]);
-        pr[c] = c < lim ? 0.0f : ex2(x0);
-        pr[c + 1] = c + 1 < lim ? 0.0f : ex2(x1);
+        for (int c = 0; c < 128; c += 2) {
+          float x0, x1;
+          ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2s[c], -l2s[c + 1]);
+          pr[c] = (c < lim || c >= hi) ? 0.0f : ex2(x0);
+          pr[c + 1] = (c + 1 < lim || c + 1 >= hi) ? 0.0f : ex2(x1);
+        }
+      } else {
+        int lim = p.causal ? j - q0 : 0;
+        if (j >= p.kL) lim = C::kTile;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          float x0, x1;
+          ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2s[c], -l2s[c + 1]);
+          pr[c] = c < lim ? 0.0f : ex2(x0);
+          pr[c + 1] = c + 1 < lim ? 0.0f : ex2(x1);
+        }
       }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -553,8 +589,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int q0 = qt * C::kTile;
   const int kvh = h / p.group;
   const int last = min(q0 + C::kTile, p.qL) - 1;
-  const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
-  const int n_blk = (kv_end + C::kTile - 1) / C::kTile;
+  // Key blocks [jb0, jb0 + n_blk) that the tile's rows see: up to the causal
+  // diagonal (row i: key i + q_offset), from the window's first key of row q0.
+  int jb0 = 0, n_blk;
+  if constexpr (C::kFeat) {
+    const long long diag_end = (long long)last + 1 + p.q_offset;
+    const int kv_end = p.causal ? (int)max(0LL, min((long long)p.kL, diag_end)) : p.kL;
+    const int nb = (kv_end + C::kTile - 1) / C::kTile;
+    if (p.window > 0) {
+      const long long first = (long long)q0 + p.q_offset - p.window + 1;
+      jb0 = first <= 0 ? 0 : (int)min(first / C::kTile, (long long)nb);
+    }
+    n_blk = nb - jb0;
+  } else {
+    const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
+    n_blk = (kv_end + C::kTile - 1) / C::kTile;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
@@ -609,7 +659,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mbar_arrive_expect_tx(&ctl->k_full[sk], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kNChunk; ++c)
-          tma_load_4d(sK + sk * C::kTileBytes + c * (C::kTile * 128), &tmK, &ctl->k_full[sk], c * 64, j * C::kTile,
+          tma_load_4d(sK + sk * C::kTileBytes + c * (C::kTile * 128), &tmK, &ctl->k_full[sk], c * 64, (jb0 + j) * C::kTile,
                       kvh, b);
         ++k_issued;
         ok = wait_bounded(&ctl->v_empty[sv], (uv & 1) ^ 1, abort_flag, p.status, p.timeout_cycles);
@@ -617,7 +667,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mbar_arrive_expect_tx(&ctl->v_full[sv], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kNChunk; ++c)
-          tma_load_4d(sV + sv * C::kTileBytes + c * (C::kTile * 128), &tmV, &ctl->v_full[sv], c * 64, j * C::kTile,
+          tma_load_4d(sV + sv * C::kTileBytes + c * (C::kTile * 128), &tmV, &ctl->v_full[sv], c * 64, (jb0 + j) * C::kTile,
                       kvh, b);
         ++v_issued;
       }
@@ -716,7 +766,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     bool ok = true;
     for (int j = 0; j < n_blk && ok; ++j) {
-      const int kbase = j * C::kTile;
+      const int kbase = (jb0 + j) * C::kTile;
       ok = warp_wait(&ctl->s_full, j & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
@@ -725,15 +775,26 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->s_free);
-      // P = 2^(s * scale * log2e - L2_i) for keys below the causal and kL limits.
-      int lim = p.kL - kbase;
-      if (p.causal) lim = min(lim, i + 1 - kbase);
+      // P = 2^(s * scale * log2e - L2_i) for keys below the causal and kL limits
+      // (and, with the features, from the window's first key on).
+      int lim = p.kL - kbase, lo = -(1 << 30);
+      if constexpr (C::kFeat) {
+        if (p.causal) lim = min(lim, i + p.q_offset + 1 - kbase);
+        if (p.window > 0) lo = i + p.q_offset - p.window + 1 - kbase;
+      } else {
+        if (p.causal) lim = min(lim, i + 1 - kbase);
+      }
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
         float x0, x1;
         ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2, -l2);
-        pr[c] = c < lim ? ex2(x0) : 0.0f;
-        pr[c + 1] = c + 1 < lim ? ex2(x1) : 0.0f;
+        if constexpr (C::kFeat) {
+          pr[c] = (c < lim && c >= lo) ? ex2(x0) : 0.0f;
+          pr[c + 1] = (c + 1 < lim && c + 1 >= lo) ? ex2(x1) : 0.0f;
+        } else {
+          pr[c] = c < lim ? ex2(x0) : 0.0f;
+          pr[c + 1] = c + 1 < lim ? ex2(x1) : 0.0f;
+        }
       }
       ok = warp_wait(&ctl->dp_full[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;

@@ -15,6 +15,7 @@ struct BwdLaunchArgs {
   int B, Hq, Hkv, qL, kL, D;
   float scale;
   int causal;
+  int window, q_offset;              // sliding window (0 = off) and causal diagonal offset
   cudaStream_t stream;
   unsigned int* status;
   long long timeout_cycles;

@@ -92,6 +92,9 @@ def load_library(path: str = LIB_PATH):
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_bwd_ex.restype = ctypes.c_int
+    lib.fa_bwd_ex.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
+        [ctypes.c_float] + [ctypes.c_int] * 4 + [ctypes.c_void_p]
     lib.fa_bwd_noalloc.restype = ctypes.c_int
     lib.fa_bwd_noalloc.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + \
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
@@ -155,6 +158,14 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q
     """``fa_bwd`` of include/fa.h; pointers are ints (device addresses). Returns the status."""
     return load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes), B, H_q, H_kv,
                                   qL, kL, D, float(scale), int(causal), int(dtype), stream)
+
+
+def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale, causal,
+              window, q_offset, dtype, stream):
+    """``fa_bwd_ex`` of include/fa.h (fa_bwd with a sliding window / causal diagonal offset). Returns the status."""
+    return load_library().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes), B, H_q, H_kv,
+                                     qL, kL, D, float(scale), int(causal), int(window), int(q_offset), int(dtype),
+                                     stream)
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, causal, dtype, stream):
@@ -290,7 +301,7 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
 
 
 def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
-                  stream=None):
+                  stream=None, window=0, q_offset=0):
     """dQ, dK, dV for torch CUDA tensors; returns (dq, dk, dv).
 
     q, o, dout: contiguous bf16 or fp16 [B, H_q, qL, D]; k, v: the same dtype,
@@ -328,9 +339,9 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
         raise ValueError(f"workspace holds fewer than the {need} bytes required")
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    _check(fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-                  workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
-                  1.0 / math.sqrt(D) if scale is None else scale, causal,
-                  FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16, stream))
+    _check(fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                     workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
+                     1.0 / math.sqrt(D) if scale is None else scale, causal, window, q_offset,
+                     FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16, stream))
     return dq, dk, dv

@@ -224,6 +224,18 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int qL, int kL, int D, float scale, int causal, int dtype, void* stream);
 
 /*
+ * fa_bwd_ex -- fa_bwd for a forward that used a sliding window and/or a
+ * causal diagonal offset (fa_fwd_args.window and .q_offset, same meaning and
+ * limits: window >= 0, |q_offset| < 2^30): key j takes part in row i's
+ * softmax only if j <= i + q_offset (causal) and j > i + q_offset - window
+ * (window > 0).  window = q_offset = 0 is fa_bwd.  Softcap and dropout have
+ * no backward here.  Arguments, results and errors otherwise as fa_bwd.
+ */
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+              void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
+              int qL, int kL, int D, float scale, int causal, int window, int q_offset, int dtype, void* stream);
+
+/*
  * fa_bwd_noalloc -- fa_bwd without a workspace argument (no counterpart on the
  * pages; a convenience of this library).  The D vector lives in a device array
  * compiled into the library, sized for B * H_q * qL <= 2^21 query rows (8 MiB
@@ -239,7 +251,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    int causal, int dtype, void* stream);
 
 /* ABI version: major * 100 + minor (1.05: fa_bwd and fa_bwd_noalloc accept
- * FA_DTYPE_F16; 1.06: fa_fwd_args.workspace, fa_fwd_workspace_bytes). */
+ * FA_DTYPE_F16; 1.06: fa_fwd_args.workspace, fa_fwd_workspace_bytes; 1.07:
+ * fa_bwd_ex). */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -29,7 +29,8 @@ def _declared_functions():
 
 def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
-        ["fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc",
+        ["fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_bytes",
+         "fa_bwd_noalloc",
          "fa_last_error",
          "fa_sync_status",
          "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_timeout_cycles", "fa_version"])
@@ -62,7 +63,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 106
+    assert fa.fa_version() == 107
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -214,6 +215,14 @@ def test_bwd_workspace_size(fa):
 ])
 def test_bwd_validation_rejects(fa, kw, status, needle):
     assert _bwd_call(fa, **kw) == status
+    assert needle in fa.fa_last_error()
+
+
+@pytest.mark.parametrize("window,q_offset,needle", [(-1, 0, "window"), (0, 1 << 30, "q_offset"),
+                                                    (0, -(1 << 30), "q_offset")])
+def test_bwd_ex_validation_rejects(fa, window, q_offset, needle):
+    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, P, 1 << 20, 1, 2, 2, 128, 128, 128, 0.125, 1, window, q_offset, 1,
+                        None) == 1
     assert needle in fa.fa_last_error()
 
 

@@ -35,6 +35,12 @@ CASES = [
     S("bwd_f16_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "f16", causal=True, seed=41),
     S("bwd_f16_d64_ragged", 2, 2, 1, 200, 200, 64, "f16", causal=True, seed=42),
     S("bwd_f16_d128_plain_long_kv", 1, 2, 2, 130, 600, 128, "f16", seed=43),
+    # sliding window / causal diagonal offset (fa_bwd_ex)
+    S("bwd_swa_d128_causal_gqa", 1, 4, 2, 640, 640, 128, "bf16", causal=True, window=200, seed=51),
+    S("bwd_offset_d64_bottom_right", 1, 2, 1, 300, 560, 64, "bf16", causal=True, q_offset=260, seed=52),
+    S("bwd_swa_offset_f16_d128", 2, 2, 2, 384, 500, 128, "f16", causal=True, window=150, q_offset=116, seed=53),
+    S("bwd_window_noncausal_d64", 1, 2, 2, 256, 400, 64, "bf16", window=100, seed=54),
+    S("bwd_negative_offset_d128", 1, 2, 2, 300, 300, 128, "bf16", causal=True, q_offset=-150, seed=55),
 ]
 
 REL_TOL = {"bf16": 2e-2, "f16": 5e-3}
@@ -47,8 +53,9 @@ def _run(w):
     do = W.make_dout(w)
     dev = "cuda:0"
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
-    o, lse = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal)
-    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, scale=w.sm_scale, causal=w.causal)
+    o, lse = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal, window=w.window, q_offset=w.q_offset)
+    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, scale=w.sm_scale, causal=w.causal, window=w.window,
+                                  q_offset=w.q_offset)
     assert fa.fa_sync_status(None) == fa.fa.FA_OK, fa.fa_last_error()
     return (q, k, v, do), (dq, dk, dv)
 
@@ -70,12 +77,13 @@ def _compare(name, got, ref, rel_tol=REL_TOL["bf16"]):
 def test_bwd_elementwise(w):
     (q, k, v, do), (dq, dk, dv) = _run(w)
     rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
-                                      do.double().numpy(), fp32_scale(w), causal=w.causal)
+                                      do.double().numpy(), fp32_scale(w), causal=w.causal, window=w.window,
+                                      q_offset=w.q_offset)
     tol = REL_TOL[w.dtype]
     _compare(f"{w.name} dQ", dq, rq, tol)
     _compare(f"{w.name} dK", dk, rk, tol)
     _compare(f"{w.name} dV", dv, rv, tol)
-    if w.causal and w.kL > w.qL:
+    if w.causal and w.kL > w.qL and w.q_offset == 0 and w.window == 0:
         # keys no query reaches get exactly zero gradient
         assert torch.count_nonzero(dk[:, :, w.qL:]).item() == 0
         assert torch.count_nonzero(dv[:, :, w.qL:]).item() == 0
