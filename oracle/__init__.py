@@ -50,7 +50,7 @@ def build(mutant: int = 0, out_path: str | None = None) -> str:
 
 
 def build_bwd(mutant: int = 0, out_path: str | None = None) -> str:
-    """Compile the gradient oracle (or a variant with planted mistake 1..8)."""
+    """Compile the gradient oracle (or a variant with planted mistake 1..9)."""
     return _compile(_SRC_BWD, _LIB_BWD_PATH, "oracle_bwd", mutant, out_path)
 
 
@@ -93,7 +93,8 @@ def _bind_bwd(lib):
     f = lib.oracle_attention_bwd_ex
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 4 + \
-        [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_int]
+        [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_double,
+                                   ctypes.c_int]
     lib.oracle_bwd_mutant_id.restype = ctypes.c_int
     return lib
 
@@ -124,11 +125,12 @@ def _mask_arg(mask, mask_kind, shape):
 
 
 def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
-                  mask_kind: int = 0, n_threads: int | None = None, lib=None, window: int = 0, q_offset: int = 0):
+                  mask_kind: int = 0, n_threads: int | None = None, lib=None, window: int = 0, q_offset: int = 0,
+                  softcap: float = 0.0):
     """dQ, dK, dV of sum(O * dO) for O = softmax(scale * q k^T + mask) v, in fp64.
 
     Shapes and mask conventions as ``attention``; dO has the shape of q.
-    window / q_offset: the forward's sliding window and causal diagonal offset.
+    window / q_offset / softcap: the forward's sliding window, causal diagonal offset and softcap.
     Returns (dQ [B,H_q,qL,D], dK [B,H_kv,kL,D], dV [B,H_kv,kL,D]).
     """
     lib = lib or load_bwd()
@@ -146,7 +148,7 @@ def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
     rc = lib.oracle_attention_bwd_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr, int(mask_kind),
                                      dO.ctypes.data, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
                                      B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)), int(window),
-                                     int(q_offset), int(n_threads))
+                                     int(q_offset), float(softcap), int(n_threads))
     del keep
     if rc != 0:
         raise ValueError("oracle_attention_bwd rejected its arguments")

@@ -21,7 +21,9 @@
  *
  * Allowed keys follow the forward's definition: j <= i + q_offset when
  * causal (q_offset 0 = top-left), and with a sliding window (window > 0)
- * j > i + q_offset - window as well.
+ * j > i + q_offset - window as well.  With a softcap c > 0 the forward's
+ * scaled score s becomes t = c tanh(s / c) before any mask, so the chain rule
+ * multiplies dS by dt/ds = 1 - tanh(s / c)^2.
  *
  * Sources (web pages on the FlashAttention-2 forward and backward):
  *  - forge "flash_attention_mma.metal", section "backward (MMA)": the three
@@ -61,8 +63,9 @@ typedef struct {
     double scale;
     int causal;
     long long window, q_offset;  /* 0: off / top-left */
+    double softcap;              /* <= 0: off */
     long long g_begin, g_end;   /* this worker's (b, kvh) groups */
-    double *S, *P, *dP;         /* kL doubles each */
+    double *S, *P, *dP, *G;     /* kL doubles each (G: dt/ds of the softcap, 1 without) */
 } bwd_job;
 
 static void bwd_group(const bwd_job *J, long long grp)
@@ -93,6 +96,12 @@ static void bwd_group(const bwd_job *J, long long grp)
                 double dot = 0.0;
                 for (long long d = 0; d < D; ++d) dot += qi[d] * kb[j * D + d];
                 double s = J->scale * dot;
+                J->G[j] = 1.0;
+                if (J->softcap > 0.0) {
+                    const double th = tanh(s / J->softcap);
+                    s = J->softcap * th;
+                    J->G[j] = 1.0 - th * th;
+                }
                 const long long diag = i + J->q_offset;   /* the key aligned with row i */
 #if ORACLE_MUTANT == 5
                 int allowed = !J->causal || j < diag;     /* mistake: causal off by one */
@@ -131,9 +140,11 @@ static void bwd_group(const bwd_job *J, long long grp)
             for (long long j = 0; j < kL; ++j) {
                 if (P[j] == 0.0) continue;
 #if ORACLE_MUTANT == 2
-                const double dS = P[j] * (dP[j] + Di);       /* mistake: sign of the D term */
+                const double dS = P[j] * (dP[j] + Di) * J->G[j];   /* mistake: sign of the D term */
+#elif ORACLE_MUTANT == 9
+                const double dS = P[j] * (dP[j] - Di);             /* mistake: softcap derivative dropped */
 #else
-                const double dS = P[j] * (dP[j] - Di);
+                const double dS = P[j] * (dP[j] - Di) * J->G[j];
 #endif
                 for (long long d = 0; d < D; ++d) {
                     dqi[d] += J->scale * dS * kb[j * D + d];
@@ -175,10 +186,10 @@ static void *bwd_worker(void *arg)
 int oracle_attention_bwd_ex(const double *q, const double *k, const double *v, const void *mask, int mask_kind,
                             const double *dO, double *dq, double *dk, double *dv, long long B, long long Hq,
                             long long Hkv, long long qL, long long kL, long long D, double scale, int causal,
-                            long long window, long long q_offset, int n_threads)
+                            long long window, long long q_offset, double softcap, int n_threads)
 {
     if (!q || !k || !v || !dO || !dq || !dk || !dv) return -1;
-    if (window < 0) return -1;
+    if (window < 0 || !(softcap >= 0.0)) return -1;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || qL <= 0 || kL <= 0 || D <= 0) return -1;
     if (Hq % Hkv != 0) return -1;
     if (mask_kind < 0 || mask_kind > 2) return -1;
@@ -189,7 +200,7 @@ int oracle_attention_bwd_ex(const double *q, const double *k, const double *v, c
     if ((long long)n_threads > groups) n_threads = (int)groups;
     bwd_job *jobs = (bwd_job *)calloc((size_t)n_threads, sizeof(bwd_job));
     pthread_t *tids = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
-    double *scratch = (double *)malloc(sizeof(double) * 3 * (size_t)kL * (size_t)n_threads);
+    double *scratch = (double *)malloc(sizeof(double) * 4 * (size_t)kL * (size_t)n_threads);
     if (!jobs || !tids || !scratch) {
         free(jobs); free(tids); free(scratch);
         return -1;
@@ -200,12 +211,13 @@ int oracle_attention_bwd_ex(const double *q, const double *k, const double *v, c
         J->dq = dq; J->dk = dk; J->dv = dv;
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->qL = qL; J->kL = kL; J->D = D;
         J->scale = scale; J->causal = causal;
-        J->window = window; J->q_offset = q_offset;
+        J->window = window; J->q_offset = q_offset; J->softcap = softcap;
         J->g_begin = groups * t / n_threads;
         J->g_end = groups * (t + 1) / n_threads;
-        J->S = scratch + (size_t)kL * (3 * (size_t)t);
+        J->S = scratch + (size_t)kL * (4 * (size_t)t);
         J->P = J->S + kL;
         J->dP = J->P + kL;
+        J->G = J->dP + kL;
     }
     int started = 0;
     for (int t = 1; t < n_threads; ++t) {
@@ -219,14 +231,14 @@ int oracle_attention_bwd_ex(const double *q, const double *k, const double *v, c
     return 0;
 }
 
-/* The plain gradients: no window, top-left causal. */
+/* The plain gradients: no window, top-left causal, no softcap. */
 int oracle_attention_bwd(const double *q, const double *k, const double *v, const void *mask, int mask_kind,
                          const double *dO, double *dq, double *dk, double *dv, long long B, long long Hq,
                          long long Hkv, long long qL, long long kL, long long D, double scale, int causal,
                          int n_threads)
 {
     return oracle_attention_bwd_ex(q, k, v, mask, mask_kind, dO, dq, dk, dv, B, Hq, Hkv, qL, kL, D, scale, causal,
-                                   0, 0, n_threads);
+                                   0, 0, 0.0, n_threads);
 }
 
 /* Number of the planted mistake this build carries (0 for the real oracle). */

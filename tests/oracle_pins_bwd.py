@@ -14,7 +14,8 @@ gradients disagree with:
     every softmax row unchanged, so sum_j dK_j = 0; gradients are linear in dO).
 Each planted mistake (dropped scale in dK, sign of the D term, q in place of
 dO in dV, wrong heads summed into dK/dV, causal off by one, dQ sign, the
-query offset's sign, a window one key too wide) fails one.
+query offset's sign, a window one key too wide, the softcap's derivative
+dropped) fails one.
 """
 from __future__ import annotations
 
@@ -94,6 +95,35 @@ def pin_finite_differences(grad, fwd):
                 an = float(np.sum(dx * e))
                 assert abs(fd - an) <= 1e-6 * (1.0 + abs(fd)), \
                     f"d{which} case {(B, Hq, Hkv, qL, kL, D, causal, kind)}: fd {fd:.9f} vs {an:.9f}"
+
+
+def pin_finite_differences_softcap(grad, fwd):
+    """The same directional derivatives with a softcap (the forward oracle's softcap is pinned on its
+    own), with scores large enough for the cap to bend them, alone and with a causal window."""
+    r = _rng(107)
+    eps = 1e-5
+    for (B, Hq, Hkv, qL, kL, D, causal, window, cap) in (
+            (1, 2, 1, 6, 7, 4, False, 0, 1.5),
+            (1, 2, 2, 7, 7, 3, True, 3, 2.5)):
+        q, k, v, g = _inputs(r, B, Hq, Hkv, qL, kL, D)
+        scale = 1.3
+        dq, dk, dv = grad(q, k, v, g, scale, causal=causal, window=window, softcap=cap)
+
+        def loss(qq, kk, vv):
+            o, _ = fwd(qq, kk, vv, scale, causal=causal, window=window, softcap=cap)
+            return float(np.sum(o * g))
+
+        for which, x, dx in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            for _ in range(2):
+                e = r.standard_normal(x.shape)
+                args_p, args_m = [q, k, v], [q, k, v]
+                idx = "qkv".index(which)
+                args_p[idx] = x + eps * e
+                args_m[idx] = x - eps * e
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+                an = float(np.sum(dx * e))
+                assert abs(fd - an) <= 1e-6 * (1.0 + abs(fd)), \
+                    f"d{which} softcap {cap}: fd {fd:.9f} vs {an:.9f}"
 
 
 def pin_finite_differences_window_offset(grad, fwd):
@@ -216,6 +246,7 @@ def pin_linear_in_dout(grad, fwd):
 ALL_PINS = [
     pin_finite_differences,
     pin_finite_differences_window_offset,
+    pin_finite_differences_softcap,
     pin_torch_autograd,
     pin_uniform_weights_dv,
     pin_equal_values_no_qk_gradient,

@@ -38,6 +38,7 @@ MUTANTS = {
     6: "dQ sign",
     7: "query offset sign",
     8: "window one key too wide",
+    9: "softcap derivative dropped",
 }
 
 
