@@ -476,9 +476,14 @@ long long fa_bwd_workspace_bytes(int B, int H_q, int qL) {
 
 int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
               void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
-              int qL, int kL, int D, float scale, int causal, int window, int q_offset, int dtype, void* stream) {
+              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap, int dtype,
+              void* stream) {
   using namespace fa;
   g_err[0] = '\0';
+  if (!(std::isfinite(softcap) && softcap >= 0.0f)) {
+    set_error("softcap must be finite and >= 0 (0 = off)");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
   if (window < 0) {
     set_error("window (%d) must be >= 0 (0 = no sliding window)", window);
     return FA_ERR_INVALID_ARGUMENT;
@@ -559,6 +564,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   a.causal = causal ? 1 : 0;
   a.window = window;
   a.q_offset = q_offset;
+  a.softcap = softcap;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = g_status_ptr[dev];
   a.timeout_cycles = timeout_cycles();
@@ -569,7 +575,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv, int qL, int kL,
            int D, float scale, int causal, int dtype, void* stream) {
   return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale,
-                   causal, 0, 0, dtype, stream);
+                   causal, 0, 0, 0.0f, dtype, stream);
 }
 
 int fa_version(void) { return 107; }

@@ -1,6 +1,6 @@
 // fa_bwd.cu -- launcher for the backward pass: tensor maps, grids, the three
 // launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 or fp16 I/O,
-// with or without sliding window / causal diagonal offset.
+// with or without sliding window / causal diagonal offset / softcap.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -60,6 +60,10 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   p.causal = a.causal;
   p.window = a.window;
   p.q_offset = a.q_offset;
+  p.softcap_on = a.softcap > 0.0f ? 1 : 0;
+  p.softcap_kin = p.softcap_on ? 2.0f * kLog2e * (a.scale / a.softcap) : 0.0f;
+  p.softcap_out = p.softcap_on ? a.softcap * kLog2e : 0.0f;
+  p.softcap_inv = p.softcap_on ? 1.0f / p.softcap_out : 0.0f;
   p.n_qt = (a.qL + C::kTile - 1) / C::kTile;
   p.n_kt = (a.kL + C::kTile - 1) / C::kTile;
   p.scale = a.scale;
@@ -102,7 +106,7 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
 }  // namespace
 
 int launch_bwd(const BwdLaunchArgs& a) {
-  if (a.window != 0 || a.q_offset != 0) {
+  if (a.window != 0 || a.q_offset != 0 || a.softcap != 0.0f) {
     if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true>(a) : launch_bwd_d<128, true, true>(a);
     return a.D == 64 ? launch_bwd_d<64, false, true>(a) : launch_bwd_d<128, false, true>(a);
   }

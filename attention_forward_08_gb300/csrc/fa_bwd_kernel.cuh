@@ -49,6 +49,10 @@ struct BwdParams {
   int causal;
   int window;         // > 0: key j allowed only if j > i + q_offset - window (kFeat kernels)
   int q_offset;       // causal diagonal of row i is key i + q_offset (kFeat kernels)
+  int softcap_on;     // kFeat kernels: scores t = c tanh(scale s / c) (as the forward)
+  float softcap_kin;  // 2 log2(e) scale / c
+  float softcap_out;  // c log2(e): t in base-2 units is softcap_out * tanh(...)
+  float softcap_inv;  // 1 / softcap_out
   int n_qt, n_kt;     // 128-row query tiles per (b, h), 128-key tiles per (b, kvh)
   float scale;        // softmax scale (applied to dQ and dK in the epilogue)
   float scale_log2;   // scale * log2(e)
@@ -205,6 +209,39 @@ __device__ __forceinline__ void bwd_ds_pass(uint32_t tdp, const float (&p)[128],
       const int c0 = cc * 32 + 2 * e;
       const float d0 = p[c0] * (__uint_as_float(rr[2 * e]) - dsub(c0));
       const float d1 = p[c0 + 1] * (__uint_as_float(rr[2 * e + 1]) - dsub(c0 + 1));
+      pk[e] = pack16x2<C>(d0, d1);
+    }
+    tmem_st16(tdp + cc * 16, pk);
+  }
+}
+
+// The softcap's factor dt/ds = 1 - tanh^2 of one probability p > 0 of a row
+// whose logsumexp (base 2) is l2: t = log2(p) + l2 = softcap_out * tanh.
+// Recovered from p instead of kept (no registers spare between the two
+// passes); 0 where p = 0 (dS is 0 there anyway).
+__device__ __forceinline__ float softcap_factor(float p, float l2, float inv_out) {
+  const float th = (lg2(p) + l2) * inv_out;
+  return p > 0.0f ? fmaf(-th, th, 1.0f) : 0.0f;
+}
+
+// bwd_ds_pass with the softcap's factor: dS = P (dP - d) (1 - tanh^2);
+// l2(c) gives the base-2 logsumexp of column c's row.
+template <class C, class F, class L>
+__device__ __forceinline__ void bwd_ds_pass_softcap(uint32_t tdp, const float (&p)[128], F dsub, L l2,
+                                                    float inv_out) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t rr[32];
+    tmem_ld32(tdp + cc * 32, rr);
+    tmem_wait_ld();
+    reg_fence(rr);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int c0 = cc * 32 + 2 * e;
+      const float d0 = p[c0] * (__uint_as_float(rr[2 * e]) - dsub(c0)) * softcap_factor(p[c0], l2(c0), inv_out);
+      const float d1 =
+          p[c0 + 1] * (__uint_as_float(rr[2 * e + 1]) - dsub(c0 + 1)) * softcap_factor(p[c0 + 1], l2(c0 + 1), inv_out);
       pk[e] = pack16x2<C>(d0, d1);
     }
     tmem_st16(tdp + cc * 16, pk);
@@ -489,10 +526,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         int lim = p.causal ? j - p.q_offset - q0 : -(1 << 30);
         int hi = p.window > 0 ? j - p.q_offset + p.window - q0 : (1 << 30);
         if (j >= p.kL) lim = C::kTile;
+        if (p.softcap_on) {  // base-2 capped score, as the forward computes it
+          const float kin = p.softcap_kin, cout = p.softcap_out;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) pr[c] = fmaf(-2.0f * cout, rcp_approx(ex2(pr[c] * kin) + 1.0f), cout);
+        }
+        const float sf = p.softcap_on ? 1.0f : sl;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
           float x0, x1;
-          ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2s[c], -l2s[c + 1]);
+          ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2s[c], -l2s[c + 1]);
           pr[c] = (c < lim || c >= hi) ? 0.0f : ex2(x0);
           pr[c + 1] = (c + 1 < lim || c + 1 >= hi) ? 0.0f : ex2(x1);
         }
@@ -522,7 +565,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       ok = warp_wait(&ctl->dp_full, i & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
-      bwd_ds_pass<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; });
+      if (C::kFeat && p.softcap_on)
+        bwd_ds_pass_softcap<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; }, [&](int c) { return l2s[c]; },
+                               p.softcap_inv);
+      else
+        bwd_ds_pass<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; });
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -784,10 +831,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       } else {
         if (p.causal) lim = min(lim, i + 1 - kbase);
       }
+      float sq = sl;
+      if constexpr (C::kFeat) {
+        if (p.softcap_on) {  // base-2 capped score, as the forward computes it
+          const float kin = p.softcap_kin, cout = p.softcap_out;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) pr[c] = fmaf(-2.0f * cout, rcp_approx(ex2(pr[c] * kin) + 1.0f), cout);
+          sq = 1.0f;
+        }
+      }
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
         float x0, x1;
-        ffma2(x0, x1, pr[c], pr[c + 1], sl, sl, -l2, -l2);
+        ffma2(x0, x1, pr[c], pr[c + 1], sq, sq, -l2, -l2);
         if constexpr (C::kFeat) {
           pr[c] = (c < lim && c >= lo) ? ex2(x0) : 0.0f;
           pr[c + 1] = (c + 1 < lim && c + 1 >= lo) ? ex2(x1) : 0.0f;
@@ -799,7 +855,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       ok = warp_wait(&ctl->dp_full[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
-      bwd_ds_pass<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; });
+      if (C::kFeat && p.softcap_on)
+        bwd_ds_pass_softcap<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
+                               p.softcap_inv);
+      else
+        bwd_ds_pass<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; });
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -16,6 +16,7 @@ struct BwdLaunchArgs {
   float scale;
   int causal;
   int window, q_offset;              // sliding window (0 = off) and causal diagonal offset
+  float softcap;                     // 0 = off
   cudaStream_t stream;
   unsigned int* status;
   long long timeout_cycles;

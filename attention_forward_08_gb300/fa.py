@@ -94,7 +94,7 @@ def load_library(path: str = LIB_PATH):
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     lib.fa_bwd_ex.restype = ctypes.c_int
     lib.fa_bwd_ex.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
-        [ctypes.c_float] + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+        [ctypes.c_float] + [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
     lib.fa_bwd_noalloc.restype = ctypes.c_int
     lib.fa_bwd_noalloc.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + \
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
@@ -161,11 +161,12 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q
 
 
 def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale, causal,
-              window, q_offset, dtype, stream):
-    """``fa_bwd_ex`` of include/fa.h (fa_bwd with a sliding window / causal diagonal offset). Returns the status."""
+              window, q_offset, softcap, dtype, stream):
+    """``fa_bwd_ex`` of include/fa.h (fa_bwd with a sliding window / causal diagonal offset / softcap).
+    Returns the status."""
     return load_library().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes), B, H_q, H_kv,
-                                     qL, kL, D, float(scale), int(causal), int(window), int(q_offset), int(dtype),
-                                     stream)
+                                     qL, kL, D, float(scale), int(causal), int(window), int(q_offset),
+                                     float(softcap), int(dtype), stream)
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, causal, dtype, stream):
@@ -301,7 +302,7 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
 
 
 def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
-                  stream=None, window=0, q_offset=0):
+                  stream=None, window=0, q_offset=0, softcap=0.0):
     """dQ, dK, dV for torch CUDA tensors; returns (dq, dk, dv).
 
     q, o, dout: contiguous bf16 or fp16 [B, H_q, qL, D]; k, v: the same dtype,
@@ -342,6 +343,6 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
     _check(fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                      workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
-                     1.0 / math.sqrt(D) if scale is None else scale, causal, window, q_offset,
+                     1.0 / math.sqrt(D) if scale is None else scale, causal, window, q_offset, softcap,
                      FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16, stream))
     return dq, dk, dv

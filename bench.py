@@ -482,7 +482,7 @@ def oracle_bwd_sample(w, q, k, v, do, seconds):
         dos = do[:1, :n_kv * group, :Ls].double().numpy()
         t0 = time.perf_counter()
         oracle.attention_bwd(qs, ks, vs, dos, float(np.float32(w.sm_scale)), causal=w.causal, n_threads=threads,
-                             window=w.window, q_offset=w.q_offset)
+                             window=w.window, q_offset=w.q_offset, softcap=float(np.float32(w.softcap)))
         return time.perf_counter() - t0
 
     Ls = min(256, w.qL, w.kL)
@@ -506,13 +506,14 @@ def run_ours_bwd(args, w):
     import attention_forward_08_gb300 as fa
     fa.load_library()
     if (w.dtype not in ("bf16", "f16") or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128)
-            or w.softcap or w.dropout_p):
+            or w.dropout_p):
         raise SystemExit(f"--pass bwd needs an unmasked bf16 or fp16 BHSD workload with D 64 or 128, without "
-                         f"softcap or dropout ({w.name})")
+                         f"dropout ({w.name})")
     q, k, v = workloads.make_qkv(w)
     do = workloads.make_dout(w)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
-    od, lsed = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal, window=w.window, q_offset=w.q_offset)
+    od, lsed = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal, window=w.window, q_offset=w.q_offset,
+                            softcap=w.softcap)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     ws_bytes = fa.fa_bwd_workspace_bytes(w.B, w.H_q, w.qL)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -522,7 +523,8 @@ def run_ours_bwd(args, w):
 
     def launch():
         rc = fa.fa_bwd_ex(*ptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal, w.window,
-                          w.q_offset, fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16, stream.cuda_stream)
+                          w.q_offset, w.softcap, fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16,
+                          stream.cuda_stream)
         if rc != 0:
             raise fa.FaError(rc, fa.fa_last_error())
 
@@ -570,8 +572,8 @@ def run_ours_bwd(args, w):
 
         def launch_on(stream_handle, sptrs=sptrs, sws=sws):
             rc = fa.fa_bwd_ex(*sptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal,
-                              w.window, w.q_offset, fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16,
-                              stream_handle)
+                              w.window, w.q_offset, w.softcap,
+                              fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16, stream_handle)
             if rc != 0:
                 raise fa.FaError(rc, fa.fa_last_error())
         return din, dout, [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dout], launch_on

@@ -224,16 +224,19 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int qL, int kL, int D, float scale, int causal, int dtype, void* stream);
 
 /*
- * fa_bwd_ex -- fa_bwd for a forward that used a sliding window and/or a
- * causal diagonal offset (fa_fwd_args.window and .q_offset, same meaning and
- * limits: window >= 0, |q_offset| < 2^30): key j takes part in row i's
- * softmax only if j <= i + q_offset (causal) and j > i + q_offset - window
- * (window > 0).  window = q_offset = 0 is fa_bwd.  Softcap and dropout have
- * no backward here.  Arguments, results and errors otherwise as fa_bwd.
+ * fa_bwd_ex -- fa_bwd for a forward that used a sliding window, a causal
+ * diagonal offset and/or a softcap (fa_fwd_args.window, .q_offset, .softcap,
+ * same meaning and limits: window >= 0, |q_offset| < 2^30, softcap finite
+ * and >= 0): key j takes part in row i's softmax only if j <= i + q_offset
+ * (causal) and j > i + q_offset - window (window > 0); with softcap c > 0
+ * the scores are t = c tanh(scale q.k / c), so dS carries the factor
+ * 1 - tanh^2 (recovered from P and L).  All zero is fa_bwd.  Dropout has no
+ * backward here.  Arguments, results and errors otherwise as fa_bwd.
  */
 int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
               void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
-              int qL, int kL, int D, float scale, int causal, int window, int q_offset, int dtype, void* stream);
+              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap, int dtype,
+              void* stream);
 
 /*
  * fa_bwd_noalloc -- fa_bwd without a workspace argument (no counterpart on the

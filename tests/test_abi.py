@@ -218,11 +218,12 @@ def test_bwd_validation_rejects(fa, kw, status, needle):
     assert needle in fa.fa_last_error()
 
 
-@pytest.mark.parametrize("window,q_offset,needle", [(-1, 0, "window"), (0, 1 << 30, "q_offset"),
-                                                    (0, -(1 << 30), "q_offset")])
-def test_bwd_ex_validation_rejects(fa, window, q_offset, needle):
-    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, P, 1 << 20, 1, 2, 2, 128, 128, 128, 0.125, 1, window, q_offset, 1,
-                        None) == 1
+@pytest.mark.parametrize("window,q_offset,softcap,needle", [(-1, 0, 0.0, "window"), (0, 1 << 30, 0.0, "q_offset"),
+                                                            (0, -(1 << 30), 0.0, "q_offset"),
+                                                            (0, 0, -1.0, "softcap"), (0, 0, float("inf"), "softcap")])
+def test_bwd_ex_validation_rejects(fa, window, q_offset, softcap, needle):
+    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, P, 1 << 20, 1, 2, 2, 128, 128, 128, 0.125, 1, window, q_offset,
+                        softcap, 1, None) == 1
     assert needle in fa.fa_last_error()
 
 

@@ -41,7 +41,12 @@ CASES = [
     S("bwd_swa_offset_f16_d128", 2, 2, 2, 384, 500, 128, "f16", causal=True, window=150, q_offset=116, seed=53),
     S("bwd_window_noncausal_d64", 1, 2, 2, 256, 400, 64, "bf16", window=100, seed=54),
     S("bwd_negative_offset_d128", 1, 2, 2, 300, 300, 128, "bf16", causal=True, q_offset=-150, seed=55),
+    # softcap (fa_bwd_ex): scale raised so the cap bends most scores
+    S("bwd_softcap_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "bf16", causal=True, softcap=2.0, seed=56),
+    S("bwd_softcap_window_f16_d64", 1, 2, 1, 300, 420, 64, "f16", causal=True, window=120, q_offset=120,
+      softcap=3.0, seed=57),
 ]
+SOFTCAP_SCALE = 0.35  # scale * |q.k| ~ 0.35 * sqrt(D) * N(0, 1): several times the cap
 
 REL_TOL = {"bf16": 2e-2, "f16": 5e-3}
 COS_MIN = 0.999
@@ -53,9 +58,11 @@ def _run(w):
     do = W.make_dout(w)
     dev = "cuda:0"
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
-    o, lse = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal, window=w.window, q_offset=w.q_offset)
-    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, scale=w.sm_scale, causal=w.causal, window=w.window,
-                                  q_offset=w.q_offset)
+    scale = SOFTCAP_SCALE if w.softcap else w.sm_scale
+    o, lse = fa.attention(qd, kd, vd, scale=scale, causal=w.causal, window=w.window, q_offset=w.q_offset,
+                          softcap=w.softcap)
+    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, scale=scale, causal=w.causal, window=w.window,
+                                  q_offset=w.q_offset, softcap=w.softcap)
     assert fa.fa_sync_status(None) == fa.fa.FA_OK, fa.fa_last_error()
     return (q, k, v, do), (dq, dk, dv)
 
@@ -77,8 +84,9 @@ def _compare(name, got, ref, rel_tol=REL_TOL["bf16"]):
 def test_bwd_elementwise(w):
     (q, k, v, do), (dq, dk, dv) = _run(w)
     rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
-                                      do.double().numpy(), fp32_scale(w), causal=w.causal, window=w.window,
-                                      q_offset=w.q_offset)
+                                      do.double().numpy(),
+                                      fp32_scale(w, SOFTCAP_SCALE if w.softcap else None), causal=w.causal,
+                                      window=w.window, q_offset=w.q_offset, softcap=float(np.float32(w.softcap)))
     tol = REL_TOL[w.dtype]
     _compare(f"{w.name} dQ", dq, rq, tol)
     _compare(f"{w.name} dK", dk, rk, tol)
