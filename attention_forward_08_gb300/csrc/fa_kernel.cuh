@@ -5,7 +5,9 @@
 // What it computes (per batch b, query head h, query row i):
 //   O_i = softmax_j(scale * q_i . k_j + mask_ij) v_j,  L_i = m_i + ln(l_i)
 // with causal (j <= i) masking, GQA (K/V head = h / (H_q / H_kv)), optional
-// bool (nonzero keeps) or additive masks, and ragged tails.  Sources:
+// bool (nonzero keeps) or additive masks, and ragged tails; in the feature
+// instantiations also a sliding window, a causal diagonal offset, a softcap
+// and (its own instantiations) dropout.  Sources:
 //  - mlx-native "ops/flash_attn_train.rs", module doc "Algorithm": FA-2
 //    online softmax with the score pre-scaled by scale*log2(e) so the running
 //    max and sum live in base 2, and L = m2 * ln2 + ln(l2) written per row;
@@ -32,8 +34,9 @@
 //    every tcgen05.mma from one thread: S = Q K^T (both operands in shared
 //    memory, K-major, 128-byte swizzle) and O += P V (P read from TMEM, V
 //    MN-major from shared memory for bf16, a transposed V^T for tf32);
-//  - warps 2-3 (fp32 I/O only) round Q and K tiles to tf32 in place and
-//    transpose V;
+//  - warps 2-3 (fp32 I/O without the pre-pass only) round Q and K tiles to
+//    tf32 in place and transpose V; the pre-rounded fp32 plans load V^T tiles
+//    from HBM instead;
 //  - one softmax warpgroup per 128-row Q tile: thread r owns row r (TMEM lane
 //    r), reads its S row with tcgen05.ld, applies masks, updates the base-2
 //    running max/sum, writes P back to TMEM and rescales its O row in TMEM
