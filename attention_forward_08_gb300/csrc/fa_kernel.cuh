@@ -499,16 +499,24 @@ __device__ __forceinline__ void p_pass(const float (&s)[C::kBN], float sl, float
   if constexpr (kWithMax) mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
 }
 
+// One 32 x 32 -> 64-bit product as a single wide multiply: high and low words.
+__device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
+  asm("{\n\t.reg .b64 w;\n\tmul.wide.u32 w, %2, %3;\n\tmov.b64 {%1, %0}, w;\n\t}"
+      : "=r"(hi), "=r"(lo)
+      : "r"(a), "r"(b));
+}
+
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC11): ten rounds of the
 // published round function on the counter (c0, c1, 0, 0) with key (k0, k1).
-// Not inlined: one instance at a time keeps the softmax's registers for the
-// scores (the dropout path calls it once per 4 keys).
+// The dropout path runs it once per 4 keys, between the softmax passes (the
+// scores are dead there), so it is inlined.
 __device__ __forceinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
   uint32_t x0 = c0, x1 = c1, x2 = 0u, x3 = 0u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
-    const uint32_t hi2 = __umulhi(0xCD9E8D57u, x2), lo2 = 0xCD9E8D57u * x2;
+    uint32_t hi0, lo0, hi2, lo2;
+    mul_wide(0xD2511F53u, x0, hi0, lo0);
+    mul_wide(0xCD9E8D57u, x2, hi2, lo2);
     x0 = hi2 ^ x1 ^ k0;
     x1 = lo2;
     x2 = hi0 ^ x3 ^ k1;
