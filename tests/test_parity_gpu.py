@@ -263,6 +263,29 @@ def test_full_workload_sampled_rows(name):
     compare(w, o_g.reshape(-1, D)[rows], l_g.reshape(-1)[rows], o_r, l_r, what=name)
 
 
+# Long sequences: 256 key blocks per unit, row and position arithmetic past
+# 2^31 (the dropout case's positions ((b H_q + h) qL + i) kL + j reach 2^32,
+# on top of a 2^33 counter offset), and the fp32 pre-pass at size.
+LONG = [
+    S("long_bf16_causal_gqa_l32768_d128", 1, 4, 2, 32768, 32768, 128, "bf16", causal=True, seed=95),
+    S("long_bf16_dropout_l32768_d64", 1, 4, 1, 32768, 32768, 64, "bf16", causal=True, dropout_p=0.2,
+      dropout_seed=77, dropout_offset=2 ** 33, seed=96),
+    S("long_f32_prepass_l16384_d128", 1, 2, 2, 16384, 16384, 128, "f32", seed=97),
+]
+
+
+@pytest.mark.parametrize("w", LONG, ids=lambda w: w.name)
+def test_long_sequence_sampled_rows(w):
+    q, k, v, m = W.make_inputs(w)
+    o_g, l_g, _ = gpu_run(w, q, k, v, m)
+    assert np.all(np.isfinite(o_g)) and np.all(np.isfinite(l_g))
+    rows = sample_rows(w, n_per_head=4)
+    qo, ko, vo, mo = oracle_inputs(q, k, v, m)
+    o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w), causal=w.causal, mask=mo, mask_kind=w.mask_kind,
+                                rows=rows, **oracle_features(w))
+    compare(w, o_g.reshape(-1, w.D)[rows], l_g.reshape(-1)[rows], o_r, l_r, what=w.name)
+
+
 PERSISTENT = [
     S("bf16_d128_causal_gqa_units", 2, 4, 2, 520, 520, 128, "bf16", causal=True),
     S("bf16_d64_plain_units", 1, 3, 3, 300, 500, 64, "bf16"),
