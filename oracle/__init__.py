@@ -50,7 +50,7 @@ def build(mutant: int = 0, out_path: str | None = None) -> str:
 
 
 def build_bwd(mutant: int = 0, out_path: str | None = None) -> str:
-    """Compile the gradient oracle (or a variant with planted mistake 1..9)."""
+    """Compile the gradient oracle (or a variant with planted mistake 1..10)."""
     return _compile(_SRC_BWD, _LIB_BWD_PATH, "oracle_bwd", mutant, out_path)
 
 
@@ -94,7 +94,7 @@ def _bind_bwd(lib):
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 4 + \
         [ctypes.c_longlong] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_double,
-                                   ctypes.c_int]
+                                   ctypes.c_void_p, ctypes.c_int]
     lib.oracle_bwd_mutant_id.restype = ctypes.c_int
     return lib
 
@@ -126,11 +126,13 @@ def _mask_arg(mask, mask_kind, shape):
 
 def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
                   mask_kind: int = 0, n_threads: int | None = None, lib=None, window: int = 0, q_offset: int = 0,
-                  softcap: float = 0.0):
+                  softcap: float = 0.0, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
     """dQ, dK, dV of sum(O * dO) for O = softmax(scale * q k^T + mask) v, in fp64.
 
     Shapes and mask conventions as ``attention``; dO has the shape of q.
     window / q_offset / softcap: the forward's sliding window, causal diagonal offset and softcap.
+    dropout_p / seed / offset: the forward's dropout; its multipliers come from the forward
+    oracle's generator (``dropout_keep``) and enter the gradient oracle as an input.
     Returns (dQ [B,H_q,qL,D], dK [B,H_kv,kL,D], dV [B,H_kv,kL,D]).
     """
     lib = lib or load_bwd()
@@ -145,10 +147,14 @@ def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
     dv = np.empty_like(v)
     if n_threads is None:
         n_threads = os.cpu_count() or 1
+    keep = None
+    if dropout_p > 0.0:
+        keep = np.ascontiguousarray(dropout_keep(dropout_p, seed, offset, 0, B * Hq * qL * kL))
+    kptr = None if keep is None else keep.ctypes.data
     rc = lib.oracle_attention_bwd_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr, int(mask_kind),
                                      dO.ctypes.data, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
                                      B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)), int(window),
-                                     int(q_offset), float(softcap), int(n_threads))
+                                     int(q_offset), float(softcap), kptr, int(n_threads))
     del keep
     if rc != 0:
         raise ValueError("oracle_attention_bwd rejected its arguments")

@@ -23,7 +23,11 @@
  * causal (q_offset 0 = top-left), and with a sliding window (window > 0)
  * j > i + q_offset - window as well.  With a softcap c > 0 the forward's
  * scaled score s becomes t = c tanh(s / c) before any mask, so the chain rule
- * multiplies dS by dt/ds = 1 - tanh(s / c)^2.
+ * multiplies dS by dt/ds = 1 - tanh(s / c)^2.  With dropout the forward's
+ * weights are W_ij = P_ij Z_ij, Z_ij in {0, 1/(1-p)} (the multipliers are an
+ * input here, drawn by the forward oracle's generator), so
+ *   dV_j  = sum_i P_ij Z_ij dO_i,   D_i = sum_j P_ij Z_ij dP_ij  (= dO_i . O_i),
+ *   dS_ij = P_ij (Z_ij dP_ij - D_i).
  *
  * Sources (web pages on the FlashAttention-2 forward and backward):
  *  - forge "flash_attention_mma.metal", section "backward (MMA)": the three
@@ -64,6 +68,7 @@ typedef struct {
     int causal;
     long long window, q_offset;  /* 0: off / top-left */
     double softcap;              /* <= 0: off */
+    const double *keep;          /* [B, Hq, qL, kL] dropout multipliers, or NULL */
     long long g_begin, g_end;   /* this worker's (b, kvh) groups */
     double *S, *P, *dP, *G;     /* kL doubles each (G: dt/ds of the softcap, 1 without) */
 } bwd_job;
@@ -130,12 +135,13 @@ static void bwd_group(const bwd_job *J, long long grp)
             for (long long j = 0; j < kL; ++j) { P[j] = exp(S[j] - m); l += P[j]; }
             for (long long j = 0; j < kL; ++j) P[j] /= l;
             /* dP_ij = dO_i . v_j and D_i = sum_j P_ij dP_ij */
+            const double *zi = J->keep ? J->keep + ((b * J->Hq + h) * qL + i) * kL : NULL;
             double Di = 0.0;
             for (long long j = 0; j < kL; ++j) {
                 double dot = 0.0;
                 for (long long d = 0; d < D; ++d) dot += doi[d] * vb[j * D + d];
-                dP[j] = dot;
-                Di += P[j] * dot;
+                dP[j] = zi ? zi[j] * dot : dot;      /* dLoss/dP_ij through the dropped weight */
+                Di += P[j] * dP[j];
             }
             for (long long j = 0; j < kL; ++j) {
                 if (P[j] == 0.0) continue;
@@ -155,8 +161,10 @@ static void bwd_group(const bwd_job *J, long long grp)
 #endif
 #if ORACLE_MUTANT == 3
                     dvb[j * D + d] += P[j] * qi[d];             /* mistake: q in place of dO */
+#elif ORACLE_MUTANT == 10
+                    dvb[j * D + d] += P[j] * doi[d];            /* mistake: dropout dropped from dV */
 #else
-                    dvb[j * D + d] += P[j] * doi[d];
+                    dvb[j * D + d] += (zi ? P[j] * zi[j] : P[j]) * doi[d];
 #endif
                 }
             }
@@ -186,7 +194,8 @@ static void *bwd_worker(void *arg)
 int oracle_attention_bwd_ex(const double *q, const double *k, const double *v, const void *mask, int mask_kind,
                             const double *dO, double *dq, double *dk, double *dv, long long B, long long Hq,
                             long long Hkv, long long qL, long long kL, long long D, double scale, int causal,
-                            long long window, long long q_offset, double softcap, int n_threads)
+                            long long window, long long q_offset, double softcap, const double *keep,
+                            int n_threads)
 {
     if (!q || !k || !v || !dO || !dq || !dk || !dv) return -1;
     if (window < 0 || !(softcap >= 0.0)) return -1;
@@ -211,7 +220,7 @@ int oracle_attention_bwd_ex(const double *q, const double *k, const double *v, c
         J->dq = dq; J->dk = dk; J->dv = dv;
         J->B = B; J->Hq = Hq; J->Hkv = Hkv; J->qL = qL; J->kL = kL; J->D = D;
         J->scale = scale; J->causal = causal;
-        J->window = window; J->q_offset = q_offset; J->softcap = softcap;
+        J->window = window; J->q_offset = q_offset; J->softcap = softcap; J->keep = keep;
         J->g_begin = groups * t / n_threads;
         J->g_end = groups * (t + 1) / n_threads;
         J->S = scratch + (size_t)kL * (4 * (size_t)t);
@@ -238,7 +247,7 @@ int oracle_attention_bwd(const double *q, const double *k, const double *v, cons
                          int n_threads)
 {
     return oracle_attention_bwd_ex(q, k, v, mask, mask_kind, dO, dq, dk, dv, B, Hq, Hkv, qL, kL, D, scale, causal,
-                                   0, 0, 0.0, n_threads);
+                                   0, 0, 0.0, NULL, n_threads);
 }
 
 /* Number of the planted mistake this build carries (0 for the real oracle). */

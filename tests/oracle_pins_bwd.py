@@ -15,7 +15,7 @@ gradients disagree with:
 Each planted mistake (dropped scale in dK, sign of the D term, q in place of
 dO in dV, wrong heads summed into dK/dV, causal off by one, dQ sign, the
 query offset's sign, a window one key too wide, the softcap's derivative
-dropped) fails one.
+dropped, dropout left out of dV) fails one.
 """
 from __future__ import annotations
 
@@ -124,6 +124,35 @@ def pin_finite_differences_softcap(grad, fwd):
                 an = float(np.sum(dx * e))
                 assert abs(fd - an) <= 1e-6 * (1.0 + abs(fd)), \
                     f"d{which} softcap {cap}: fd {fd:.9f} vs {an:.9f}"
+
+
+def pin_finite_differences_dropout(grad, fwd):
+    """The same directional derivatives with dropout: the forward oracle's generator fixes the
+    multipliers for a given seed, so the loss is smooth in q, k and v."""
+    r = _rng(109)
+    eps = 1e-5
+    for (B, Hq, Hkv, qL, kL, D, causal, p, seed, off) in (
+            (1, 2, 1, 6, 8, 4, False, 0.3, 11, 0),
+            (2, 2, 2, 5, 8, 3, True, 0.5, 2 ** 40 + 5, 2 ** 32 - 3)):
+        q, k, v, g = _inputs(r, B, Hq, Hkv, qL, kL, D)
+        scale = 0.45
+        dq, dk, dv = grad(q, k, v, g, scale, causal=causal, dropout_p=p, seed=seed, offset=off)
+
+        def loss(qq, kk, vv):
+            o, _ = fwd(qq, kk, vv, scale, causal=causal, dropout_p=p, seed=seed, offset=off)
+            return float(np.sum(o * g))
+
+        for which, x, dx in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            for _ in range(2):
+                e = r.standard_normal(x.shape)
+                args_p, args_m = [q, k, v], [q, k, v]
+                idx = "qkv".index(which)
+                args_p[idx] = x + eps * e
+                args_m[idx] = x - eps * e
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+                an = float(np.sum(dx * e))
+                assert abs(fd - an) <= 1e-6 * (1.0 + abs(fd)), \
+                    f"d{which} dropout {p}: fd {fd:.9f} vs {an:.9f}"
 
 
 def pin_finite_differences_window_offset(grad, fwd):
@@ -247,6 +276,7 @@ ALL_PINS = [
     pin_finite_differences,
     pin_finite_differences_window_offset,
     pin_finite_differences_softcap,
+    pin_finite_differences_dropout,
     pin_torch_autograd,
     pin_uniform_weights_dv,
     pin_equal_values_no_qk_gradient,

@@ -39,6 +39,7 @@ MUTANTS = {
     7: "query offset sign",
     8: "window one key too wide",
     9: "softcap derivative dropped",
+    10: "dropout left out of dV",
 }
 
 
