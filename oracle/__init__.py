@@ -141,7 +141,7 @@ def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
     Bk, Hkv, kL, Dk = k.shape
     if (Bk, Dk) != (B, D) or v.shape != k.shape or dO.shape != q.shape:
         raise ValueError("shape mismatch between q, k, v and dO")
-    keep, mptr = _mask_arg(mask, mask_kind, (B, Hq, qL, kL))
+    mask_arr, mptr = _mask_arg(mask, mask_kind, (B, Hq, qL, kL))  # held until the call returns
     dq = np.empty_like(q)
     dk = np.empty_like(k)
     dv = np.empty_like(v)
@@ -155,7 +155,7 @@ def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
                                      dO.ctypes.data, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
                                      B, Hq, Hkv, qL, kL, D, float(scale), int(bool(causal)), int(window),
                                      int(q_offset), float(softcap), kptr, int(n_threads))
-    del keep
+    del keep, mask_arr
     if rc != 0:
         raise ValueError("oracle_attention_bwd rejected its arguments")
     return dq, dk, dv
