@@ -81,6 +81,9 @@ int device_setup(int dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Words per row of the backward's keep mask: 4 (128 keys) per 128-key block.
+long long keep_row_words(int kL) { return ((long long)kL + 127) / 128 * 4; }
+
 // Bytes of a stride that TMA will use (extent-1 dimensions are never stepped).
 bool stride_ok(long long elems, int extent, int esz) {
   if (extent <= 1) return true;
@@ -474,12 +477,29 @@ long long fa_bwd_workspace_bytes(int B, int H_q, int qL) {
   return (bytes + 255) / 256 * 256;
 }
 
+long long fa_bwd_ex_workspace_bytes(int B, int H_q, int qL, int kL, float dropout_p) {
+  const long long dvec = fa_bwd_workspace_bytes(B, H_q, qL);
+  if (dvec < 0 || kL <= 0 || !(dropout_p >= 0.0f && dropout_p <= 1.0f)) return -1;
+  if (dropout_p == 0.0f) return dvec;
+  // keep mask: 4 words (128 keys) per row and 128-key block
+  return dvec + (long long)B * H_q * qL * fa::keep_row_words(kL) * 4;
+}
+
 int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
               void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
-              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap, int dtype,
+              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap,
+              float dropout_p, unsigned long long dropout_seed, unsigned long long dropout_offset, int dtype,
               void* stream) {
   using namespace fa;
   g_err[0] = '\0';
+  if (!(dropout_p >= 0.0f && dropout_p <= 1.0f)) {
+    set_error("dropout_p must lie in [0, 1]");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (dropout_p > 0.0f && kL % 4 != 0) {
+    set_error("dropout needs kL (%d) to be a multiple of 4", kL);
+    return FA_ERR_UNSUPPORTED;
+  }
   if (!(std::isfinite(softcap) && softcap >= 0.0f)) {
     set_error("softcap must be finite and >= 0 (0 = off)");
     return FA_ERR_INVALID_ARGUMENT;
@@ -523,9 +543,9 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     set_error("row counts exceed 2^31 - 1");
     return FA_ERR_UNSUPPORTED;
   }
-  if (workspace_bytes < fa_bwd_workspace_bytes(B, H_q, qL)) {
-    set_error("workspace of %lld bytes is smaller than the %lld required", workspace_bytes,
-              fa_bwd_workspace_bytes(B, H_q, qL));
+  const long long ws_need = fa_bwd_ex_workspace_bytes(B, H_q, qL, kL, dropout_p);
+  if (workspace_bytes < ws_need) {
+    set_error("workspace of %lld bytes is smaller than the %lld required", workspace_bytes, ws_need);
     return FA_ERR_INVALID_ARGUMENT;
   }
   const void* ptrs[10] = {q, k, v, o, dout, dq, dk, dv, workspace, lse};
@@ -565,6 +585,13 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   a.window = window;
   a.q_offset = q_offset;
   a.softcap = softcap;
+  a.dropout_p = dropout_p;
+  a.dropout_seed = dropout_seed;
+  a.dropout_offset = dropout_offset;
+  a.keep_row_words = keep_row_words(kL);
+  a.keep_mask = dropout_p > 0.0f ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
+                                                               fa_bwd_workspace_bytes(B, H_q, qL))
+                                 : nullptr;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = g_status_ptr[dev];
   a.timeout_cycles = timeout_cycles();
@@ -575,9 +602,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv, int qL, int kL,
            int D, float scale, int causal, int dtype, void* stream) {
   return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale,
-                   causal, 0, 0, 0.0f, dtype, stream);
+                   causal, 0, 0, 0.0f, 0.0f, 0ull, 0ull, dtype, stream);
 }
 
-int fa_version(void) { return 107; }
+int fa_version(void) { return 108; }
 
 }  // extern "C"

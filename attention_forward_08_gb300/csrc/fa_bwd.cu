@@ -1,8 +1,12 @@
 // fa_bwd.cu -- launcher for the backward pass: tensor maps, grids, the three
 // launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 or fp16 I/O,
-// with or without sliding window / causal diagonal offset / softcap.
+// with or without sliding window / causal diagonal offset / softcap, and
+// with dropout.
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
 
 #include "fa_bwd_kernel.cuh"
 #include "fa_bwd_launch.h"
@@ -26,9 +30,9 @@ int set_smem_once(const void* kern, uint32_t bytes, int& configured_device) {
   return 0;
 }
 
-template <int kD, bool kF16, bool kFeat>
+template <int kD, bool kF16, bool kFeat, bool kDrop = false>
 int launch_bwd_d(const BwdLaunchArgs& a) {
-  using C = BwdCfg<kD, kF16, kFeat>;
+  using C = BwdCfg<kD, kF16, kFeat, kDrop>;
   // 1. D_i = rowsum(O_i * dO_i)
   const long long rows = (long long)a.B * a.Hq * a.qL;
   constexpr int kRowsPerBlock = 256 / (kD / 8);
@@ -64,6 +68,14 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   p.softcap_kin = p.softcap_on ? 2.0f * kLog2e * (a.scale / a.softcap) : 0.0f;
   p.softcap_out = p.softcap_on ? a.softcap * kLog2e : 0.0f;
   p.softcap_inv = p.softcap_on ? 1.0f / p.softcap_out : 0.0f;
+  p.dropout_on = kDrop ? 1 : 0;
+  p.drop_threshold = kDrop ? (unsigned int)std::ceil((double)a.dropout_p * 16777216.0) : 0u;
+  p.drop_scale = kDrop && a.dropout_p < 1.0f ? (float)(1.0 / (1.0 - (double)a.dropout_p)) : 0.0f;
+  p.seed_lo = (unsigned int)a.dropout_seed;
+  p.seed_hi = (unsigned int)(a.dropout_seed >> 32);
+  p.drop_offset = a.dropout_offset;
+  p.keep_mask = a.keep_mask;
+  p.keep_row_words = a.keep_row_words;
   p.n_qt = (a.qL + C::kTile - 1) / C::kTile;
   p.n_kt = (a.kL + C::kTile - 1) / C::kTile;
   p.scale = a.scale;
@@ -80,20 +92,37 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   if (int rc = set_smem_once<C>((const void*)fa_bwd_dkdv_kernel<C>, C::kKVSmem, cfg_kv)) return rc;
   if (int rc = set_smem_once<C>((const void*)fa_bwd_dq_kernel<C>, C::kQSmem, cfg_q)) return rc;
 
-  // 3. dK, dV: one CTA per (128-key tile, kvh, b).
   const long long n_kv = (long long)p.n_kt * a.Hkv * a.B;
   const long long n_q = (long long)p.n_qt * a.Hq * a.B;
   if (n_kv > 0x7fffffffLL || n_q > 0x7fffffffLL) {
     set_error("backward grid of %lld / %lld CTAs is out of range", n_kv, n_q);
     return 2;
   }
+
+  // 3. Dropout: the forward's keep decisions, once for both kernels.
+  if constexpr (kDrop) {
+    const int n_kb = p.n_kt;
+    const long long n_units = (long long)a.B * a.Hq * p.n_qt * n_kb;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+    const unsigned grid = (unsigned)std::min<long long>(n_units, (long long)sms * 8);
+    fa_bwd_keep_mask_kernel<<<grid, 256, 0, a.stream>>>(p, n_kb, n_units);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      set_error("keep-mask launch failed: %s", cudaGetErrorString(e));
+      return 4;
+    }
+  }
+
+  // 4. dK, dV: one CTA per (128-key tile, kvh, b).
   fa_bwd_dkdv_kernel<C><<<(unsigned)n_kv, C::kThreads, C::kKVSmem, a.stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("dK/dV launch failed: %s", cudaGetErrorString(e));
     return 4;
   }
-  // 4. dQ: one CTA per (128-row query tile, h, b).
+  // 5. dQ: one CTA per (128-row query tile, h, b).
   fa_bwd_dq_kernel<C><<<(unsigned)n_q, C::kThreads, C::kQSmem, a.stream>>>(tq, tk, tv, tdo, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -106,6 +135,10 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
 }  // namespace
 
 int launch_bwd(const BwdLaunchArgs& a) {
+  if (a.dropout_p != 0.0f) {
+    if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true, true>(a) : launch_bwd_d<128, true, true, true>(a);
+    return a.D == 64 ? launch_bwd_d<64, false, true, true>(a) : launch_bwd_d<128, false, true, true>(a);
+  }
   if (a.window != 0 || a.q_offset != 0 || a.softcap != 0.0f) {
     if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true>(a) : launch_bwd_d<128, true, true>(a);
     return a.D == 64 ? launch_bwd_d<64, false, true>(a) : launch_bwd_d<128, false, true>(a);

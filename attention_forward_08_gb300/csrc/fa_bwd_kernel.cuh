@@ -53,6 +53,17 @@ struct BwdParams {
   float softcap_kin;  // 2 log2(e) scale / c
   float softcap_out;  // c log2(e): t in base-2 units is softcap_out * tanh(...)
   float softcap_inv;  // 1 / softcap_out
+  int dropout_on;     // kDrop kernels: the forward's weights were P_ij Z_ij, Z in {0, drop_scale}
+  unsigned int drop_threshold;  // keep iff (word >> 8) >= threshold (ceil(p 2^24))
+  float drop_scale;   // 1 / (1 - p), 0 when p = 1
+  unsigned int seed_lo, seed_hi;
+  unsigned long long drop_offset;  // generator counter of position 0
+  // The forward's keep decisions, written by the keep-mask pre-pass: row
+  // (b H_q + h) qL + i holds keep_row_words words; bit x of word w is key
+  // 32 w + x.  Only the (128-row, 128-key) tiles some row of which can see
+  // some key of are written; the others are never needed (P = 0 there).
+  uint32_t* keep_mask;
+  long long keep_row_words;  // a multiple of 4 (16-byte rows of 128-key blocks)
   int n_qt, n_kt;     // 128-row query tiles per (b, h), 128-key tiles per (b, kvh)
   float scale;        // softmax scale (applied to dQ and dK in the epilogue)
   float scale_log2;   // scale * log2(e)
@@ -65,7 +76,7 @@ struct BwdParams {
   long long timeout_cycles;
 };
 
-template <int kD_, bool kF16_ = false, bool kFeat_ = false>
+template <int kD_, bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false>
 struct BwdCfg {
   static constexpr int kD = kD_;
   // 16-bit I/O is bf16 unless kF16 (fp16): same kernels, other operand format.
@@ -73,6 +84,9 @@ struct BwdCfg {
   // Sliding window and causal diagonal offset compiled in (their own
   // instantiations: the plain kernels keep their exact code).
   static constexpr bool kFeat = kFeat_;
+  // Dropout as well (its own instantiations again; implies kFeat).
+  static constexpr bool kDrop = kDrop_;
+  static_assert(!kDrop || kFeat, "the dropout instantiation includes the other features");
   static constexpr uint32_t kFmt = kF16 ? kFmtF16 : kFmtBf16;
   static constexpr CUtensorMapDataType kTmaType =
       kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -92,7 +106,12 @@ struct BwdCfg {
   static constexpr uint32_t kKVOffQ = 2 * kTileBytes;
   static constexpr uint32_t kKVOffDO = kKVOffQ + kStages * kTileBytes;
   static constexpr uint32_t kKVOffLD = kKVOffDO + kStages * kTileBytes;
-  static constexpr uint32_t kKVOffBar = kKVOffLD + kStages * 2 * kTile * 4;
+  // dK/dV kernel with dropout: per stage, the block's 128 query rows' keep
+  // words for this key tile (16 bytes a row, staged with L and D); then each
+  // key row's transposed words for the current step (16 bytes a key).
+  static constexpr uint32_t kKVOffKB = kKVOffLD + kStages * 2 * kTile * 4;
+  static constexpr uint32_t kKVOffKeep = kKVOffKB + (kDrop ? kStages * kTile * 16 : 0);
+  static constexpr uint32_t kKVOffBar = kKVOffKeep + (kDrop ? kTile * 16 : 0);
   static constexpr uint32_t kKVSmem = 1024 + kKVOffBar + 512;
   // dQ kernel shared memory: Q, dO, then K and V rings.
   static constexpr uint32_t kQOffK = 2 * kTileBytes;
@@ -153,6 +172,48 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const uint4* __restr
 #pragma unroll
   for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && sub == 0) dvec[row] = acc;
+}
+
+// ---------------------------------------------------------------- keep-mask pre-pass
+
+// The forward's dropout decisions for the backward: position ((b H_q + h) qL
+// + i) kL + j, one Philox4x32-10 block per 4 keys at counter offset +
+// position / 4 (kL is a multiple of 4), keep iff word >> 8 >= threshold;
+// written as p.keep_mask's row words for every (128-row, 128-key) tile some
+// row of which can see some key of.  A unit of work is one tile: warp w draws
+// rows w, w + 8, ..., lane l the block of keys 4 l .. 4 l + 3, and the 4-bit
+// results of 8 lanes become one word with three shuffles.  Throughput-bound
+// on the integer pipes (the 32 x 32-bit multiplies), at full occupancy.
+__global__ void __launch_bounds__(256) fa_bwd_keep_mask_kernel(const BwdParams p, int n_kb, long long n_units) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned long long row_ctr = (unsigned long long)(p.kL / 4);
+  const uint32_t thr = p.drop_threshold;
+  for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const int kb = (int)(u % n_kb);
+    const long long rest = u / n_kb;
+    const int r0 = (int)(rest % p.n_qt) * 128;
+    const long long bh = rest / p.n_qt;
+    const int r1 = min(r0 + 128, p.qL) - 1, c0 = kb * 128, c1 = min(c0 + 128, p.kL) - 1;
+    // Row i sees keys i + q_offset - window < j <= i + q_offset (the causal
+    // and window limits); over rows r0 .. r1 those ranges join into one.
+    if (p.causal && (long long)c0 > (long long)r1 + p.q_offset) continue;
+    if (p.window > 0 && (long long)c1 < (long long)r0 + p.q_offset - p.window + 1) continue;
+#pragma unroll 4
+    for (int t = 0; t < 16; ++t) {
+      const int i = r0 + warp + 8 * t;
+      const unsigned long long c =
+          p.drop_offset + ((unsigned long long)bh * p.qL + i) * row_ctr + (unsigned long long)(c0 / 4 + lane);
+      const uint4 w = philox_10((uint32_t)c, (uint32_t)(c >> 32), p.seed_lo, p.seed_hi);
+      const uint32_t nib = ((w.x >> 8) >= thr ? 1u : 0u) | ((w.y >> 8) >= thr ? 2u : 0u) |
+                           ((w.z >> 8) >= thr ? 4u : 0u) | ((w.w >> 8) >= thr ? 8u : 0u);
+      uint32_t x = nib << (4 * (lane & 7));
+      x |= __shfl_xor_sync(0xffffffffu, x, 1);
+      x |= __shfl_xor_sync(0xffffffffu, x, 2);
+      x |= __shfl_xor_sync(0xffffffffu, x, 4);
+      if (i < p.qL && (lane & 7) == 0)
+        p.keep_mask[((long long)bh * p.qL + i) * p.keep_row_words + c0 / 32 + (lane >> 3)] = x;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- shared pieces
@@ -222,6 +283,59 @@ __device__ __forceinline__ void bwd_ds_pass(uint32_t tdp, const float (&p)[128],
 __device__ __forceinline__ float softcap_factor(float p, float l2, float inv_out) {
   const float th = (lg2(p) + l2) * inv_out;
   return p > 0.0f ? fmaf(-th, th, 1.0f) : 0.0f;
+}
+
+// Transposes a 32 x 32 bit matrix held one row per lane (bit k of lane l's
+// word = element (l, k)) so that lane k ends with column k (bit l = element
+// (l, k)): five butterfly stages, each swapping the off-diagonal half-blocks
+// of every 2j x 2j block between lanes l and l ^ j (the register form of the
+// recursive block transpose, Hacker's Delight, section 7-3).
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+  constexpr uint32_t kMask[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int j = 16 >> st;
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+    const uint32_t upper = ((y >> j) ^ x) & kMask[st];         // lanes with bit j set
+    const uint32_t lower = (((x >> j) ^ y) & kMask[st]) << j;  // lanes with bit j clear
+    x ^= (lane & j) ? upper : lower;
+  }
+  return x;
+}
+
+// The dropout multiplier of one column from its keep bit: scale or 0, by
+// integer masking (selects per element cost registers here).
+__device__ __forceinline__ float keep_mult(uint32_t word, int bit, float scale) {
+  return __int_as_float(__float_as_int(scale) & (0u - ((word >> bit) & 1u)));
+}
+
+// dS with dropout (and, when inv_out > 0, the softcap's factor):
+// dS = P (Z dP - d) f, Z = keep_mult(bits, scale); kword(cc) gives the keep
+// word of columns 32 cc .. 32 cc + 31.
+template <class C, class F, class L, class K>
+__device__ __forceinline__ void bwd_ds_pass_drop(uint32_t tdp, const float (&p)[128], F dsub, L l2, float inv_out,
+                                                 K kword, float scale) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t rr[32];
+    tmem_ld32(tdp + cc * 32, rr);
+    tmem_wait_ld();
+    reg_fence(rr);
+    uint32_t pk[16];
+    const uint32_t kw = kword(cc);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int c0 = cc * 32 + 2 * e;
+      float d0 = p[c0] * fmaf(keep_mult(kw, 2 * e, scale), __uint_as_float(rr[2 * e]), -dsub(c0));
+      float d1 = p[c0 + 1] * fmaf(keep_mult(kw, 2 * e + 1, scale), __uint_as_float(rr[2 * e + 1]), -dsub(c0 + 1));
+      if (inv_out > 0.0f) {
+        d0 *= softcap_factor(p[c0], l2(c0), inv_out);
+        d1 *= softcap_factor(p[c0 + 1], l2(c0 + 1), inv_out);
+      }
+      pk[e] = pack16x2<C>(d0, d1);
+    }
+    tmem_st16(tdp + cc * 16, pk);
+  }
 }
 
 // bwd_ds_pass with the softcap's factor: dS = P (dP - d) (1 - tanh^2);
@@ -413,6 +527,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         l2s[c] = l2;
         l2s[C::kTile + c] = dv;
+        if constexpr (C::kDrop) {  // the row's keep words of this key tile
+          uint4 kb = make_uint4(0u, 0u, 0u, 0u);
+          if (iq < p.qL)
+            kb = __ldg(reinterpret_cast<const uint4*>(p.keep_mask + (base + iq) * p.keep_row_words + k0 / 32));
+          reinterpret_cast<uint4*>(smem + C::kKVOffKB)[s * C::kTile + c] = kb;
+        }
       }
       mbar_arrive(&ctl->ld_full[s]);
     }
@@ -505,6 +625,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t tS = tmem + lane_addr + C::kColS;
     const uint32_t tDP = tmem + lane_addr + C::kColDP;
     const float sl = p.scale_log2;
+    // Dropout: this key row's keep bits for the step (bit c of word q: query
+    // row q0 + 32 q + c), transposed from the staged row words while the MMA
+    // warp computes S^T.
+    uint4* keep_smem = reinterpret_cast<uint4*>(smem + C::kKVOffKeep) + tl;
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i) {
       int h, q0;
@@ -513,6 +637,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const float* l2s = sLD + s * 2 * C::kTile;
       ok = warp_wait(&ctl->ld_full[s], use & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
+      if constexpr (C::kDrop) {
+        // Lane l reads row 32 q + l's word for this warp's 32 keys; the
+        // transpose hands lane k the column of key k0 + 32 (warp & 3) + k.
+        const uint32_t* kb = reinterpret_cast<const uint32_t*>(smem + C::kKVOffKB) + s * C::kTile * 4 + (warp & 3);
+        uint32_t kw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) kw[q] = warp_transpose32(kb[(32 * q + lane) * 4], lane);
+        *keep_smem = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+      }
       ok = warp_wait(&ctl->s_full, i & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
@@ -550,11 +683,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           pr[c + 1] = c + 1 < lim ? 0.0f : ex2(x1);
         }
       }
+      const uint32_t* keep_words = reinterpret_cast<const uint32_t*>(keep_smem);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t pk[16];
+        const uint32_t kw = C::kDrop ? keep_words[cc] : 0u;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack16x2<C>(pr[cc * 32 + 2 * e], pr[cc * 32 + 2 * e + 1]);
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = pack16x2<C>(pr[cc * 32 + 2 * e], pr[cc * 32 + 2 * e + 1]);
+          if constexpr (C::kDrop) {  // dV takes the dropped weights P Z (Z's scale in the epilogue)
+            const uint32_t t2 = (kw >> (2 * e)) & 3u;
+            pk[e] &= (t2 & 1u) * 0x0000FFFFu + (t2 >> 1) * 0xFFFF0000u;
+          }
+        }
         tmem_st16(tS + cc * 16, pk);
       }
       tmem_wait_st();
@@ -565,11 +706,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       ok = warp_wait(&ctl->dp_full, i & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
-      if (C::kFeat && p.softcap_on)
+      if constexpr (C::kDrop) {
+        bwd_ds_pass_drop<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; }, [&](int c) { return l2s[c]; },
+                            p.softcap_on ? p.softcap_inv : 0.0f, [&](int cc) { return keep_words[cc]; },
+                            p.drop_scale);
+      } else if (C::kFeat && p.softcap_on) {
         bwd_ds_pass_softcap<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; }, [&](int c) { return l2s[c]; },
                                p.softcap_inv);
-      else
+      } else {
         bwd_ds_pass<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; });
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -577,6 +723,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mbar_arrive(&ctl->ds_ready);
         mbar_arrive(&ctl->ld_empty[s]);
       }
+
     }
     // ---- epilogue: dV and scale * dK rows (key j) as bf16
     if (ok) {
@@ -594,7 +741,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
         if (ok) {
           tc_fence_after();
-          bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, 1.0f, dvp, store);
+          bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, C::kDrop ? p.drop_scale : 1.0f, dvp, store);
           bwd_store_row<C>(tmem + lane_addr + C::kColAcc1, p.scale, dkp, store);
         }
       }
@@ -814,6 +961,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_blk && ok; ++j) {
       const int kbase = (jb0 + j) * C::kTile;
+      // Dropout: this row's keep bits of block j (bit x of word q: key
+      // kbase + 32 q + x), loaded while S_j is computed.
+      uint32_t kw[4] = {0u, 0u, 0u, 0u};
+      if constexpr (C::kDrop) {
+        if (i < p.qL) {
+          const uint4 k4 = __ldg(reinterpret_cast<const uint4*>(p.keep_mask + rowi * p.keep_row_words + kbase / 32));
+          kw[0] = k4.x;
+          kw[1] = k4.y;
+          kw[2] = k4.z;
+          kw[3] = k4.w;
+        }
+      }
       ok = warp_wait(&ctl->s_full, j & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
@@ -855,11 +1014,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       ok = warp_wait(&ctl->dp_full[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
-      if (C::kFeat && p.softcap_on)
+      if constexpr (C::kDrop) {
+        bwd_ds_pass_drop<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
+                            p.softcap_on ? p.softcap_inv : 0.0f, [&](int cc) { return kw[cc]; }, p.drop_scale);
+      } else if (C::kFeat && p.softcap_on) {
         bwd_ds_pass_softcap<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
                                p.softcap_inv);
-      else
+      } else {
         bwd_ds_pass<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; });
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

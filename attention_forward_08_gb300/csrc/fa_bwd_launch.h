@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 namespace fa {
 
@@ -17,6 +18,11 @@ struct BwdLaunchArgs {
   int causal;
   int window, q_offset;              // sliding window (0 = off) and causal diagonal offset
   float softcap;                     // 0 = off
+  float dropout_p;                   // 0 = off: the forward's dropout, regenerated from
+  unsigned long long dropout_seed;   //   the same seed and offset (counter-based keep
+  unsigned long long dropout_offset; //   contract, as in the forward)
+  uint32_t* keep_mask;               // dropout: [B, H_q, qL, keep_row_words] scratch for the
+  long long keep_row_words;          //   keep decisions (4 * ceil(kL / 128) words a row)
   cudaStream_t stream;
   unsigned int* status;
   long long timeout_cycles;

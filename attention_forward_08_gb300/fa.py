@@ -25,9 +25,9 @@ FA_OK, FA_ERR_INVALID_ARGUMENT, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CU
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
                 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
-EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_last_error", "fa_sync_status", "fa_set_timeout_cycles", "fa_set_max_ctas",
-            "fa_set_q_tiles",
-            "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_noalloc", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_last_error", "fa_sync_status",
+            "fa_set_timeout_cycles", "fa_set_max_ctas", "fa_set_q_tiles", "fa_bwd_workspace_bytes",
+            "fa_bwd_ex_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_bwd_noalloc", "fa_version")
 
 
 class FaError(RuntimeError):
@@ -89,12 +89,15 @@ def load_library(path: str = LIB_PATH):
     lib.fa_version.argtypes = []
     lib.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
     lib.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 3
+    lib.fa_bwd_ex_workspace_bytes.restype = ctypes.c_longlong
+    lib.fa_bwd_ex_workspace_bytes.argtypes = [ctypes.c_int] * 4 + [ctypes.c_float]
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     lib.fa_bwd_ex.restype = ctypes.c_int
     lib.fa_bwd_ex.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
-        [ctypes.c_float] + [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
+        [ctypes.c_float] + [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_float, ctypes.c_ulonglong,
+                                                 ctypes.c_ulonglong, ctypes.c_int, ctypes.c_void_p]
     lib.fa_bwd_noalloc.restype = ctypes.c_int
     lib.fa_bwd_noalloc.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + \
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
@@ -153,6 +156,11 @@ def fa_bwd_workspace_bytes(B: int, H_q: int, qL: int) -> int:
     return load_library().fa_bwd_workspace_bytes(int(B), int(H_q), int(qL))
 
 
+def fa_bwd_ex_workspace_bytes(B: int, H_q: int, qL: int, kL: int, dropout_p: float = 0.0) -> int:
+    """``fa_bwd_ex_workspace_bytes`` of include/fa.h (adds the keep mask when dropout_p > 0)."""
+    return load_library().fa_bwd_ex_workspace_bytes(int(B), int(H_q), int(qL), int(kL), float(dropout_p))
+
+
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale, causal,
            dtype, stream):
     """``fa_bwd`` of include/fa.h; pointers are ints (device addresses). Returns the status."""
@@ -161,12 +169,13 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q
 
 
 def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H_q, H_kv, qL, kL, D, scale, causal,
-              window, q_offset, softcap, dtype, stream):
-    """``fa_bwd_ex`` of include/fa.h (fa_bwd with a sliding window / causal diagonal offset / softcap).
-    Returns the status."""
+              window, q_offset, softcap, dropout_p, dropout_seed, dropout_offset, dtype, stream):
+    """``fa_bwd_ex`` of include/fa.h (fa_bwd with a sliding window / causal diagonal offset / softcap /
+    the forward's dropout). Returns the status."""
     return load_library().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes), B, H_q, H_kv,
                                      qL, kL, D, float(scale), int(causal), int(window), int(q_offset),
-                                     float(softcap), int(dtype), stream)
+                                     float(softcap), float(dropout_p), int(dropout_seed) & (2**64 - 1),
+                                     int(dropout_offset) & (2**64 - 1), int(dtype), stream)
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, causal, dtype, stream):
@@ -302,12 +311,16 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
 
 
 def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
-                  stream=None, window=0, q_offset=0, softcap=0.0):
+                  stream=None, window=0, q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0):
     """dQ, dK, dV for torch CUDA tensors; returns (dq, dk, dv).
+
+    window, q_offset, softcap, dropout_p, dropout_seed, dropout_offset: the
+    forward's (``attention``), so that the backward sees the same softmax and
+    regenerates the same keep decisions.
 
     q, o, dout: contiguous bf16 or fp16 [B, H_q, qL, D]; k, v: the same dtype,
     [B, H_kv, kL, D]; lse: the forward's contiguous fp32 [B, H_q, qL].
-    workspace: optional device tensor of at least ``fa_bwd_workspace_bytes``
+    workspace: optional device tensor of at least ``fa_bwd_ex_workspace_bytes``
     bytes (allocated here if None).
     """
     import torch
@@ -333,7 +346,9 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
         dk = torch.empty_like(k)
     if dv is None:
         dv = torch.empty_like(v)
-    need = fa_bwd_workspace_bytes(B, H_q, qL)
+    need = fa_bwd_ex_workspace_bytes(B, H_q, qL, kL, dropout_p)
+    if need < 0:
+        raise ValueError(f"dropout_p must lie in [0, 1] (got {dropout_p})")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < need:
@@ -344,5 +359,5 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                      workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
                      1.0 / math.sqrt(D) if scale is None else scale, causal, window, q_offset, softcap,
-                     FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16, stream))
+                     dropout_p, dropout_seed, dropout_offset, FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16, stream))
     return dq, dk, dv

@@ -482,7 +482,8 @@ def oracle_bwd_sample(w, q, k, v, do, seconds):
         dos = do[:1, :n_kv * group, :Ls].double().numpy()
         t0 = time.perf_counter()
         oracle.attention_bwd(qs, ks, vs, dos, float(np.float32(w.sm_scale)), causal=w.causal, n_threads=threads,
-                             window=w.window, q_offset=w.q_offset, softcap=float(np.float32(w.softcap)))
+                             window=w.window, q_offset=w.q_offset, softcap=float(np.float32(w.softcap)),
+                             dropout_p=float(np.float32(w.dropout_p)), seed=w.dropout_seed, offset=w.dropout_offset)
         return time.perf_counter() - t0
 
     Ls = min(256, w.qL, w.kL)
@@ -505,17 +506,16 @@ def run_ours_bwd(args, w):
     torch.cuda.set_device(dev)
     import attention_forward_08_gb300 as fa
     fa.load_library()
-    if (w.dtype not in ("bf16", "f16") or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128)
-            or w.dropout_p):
-        raise SystemExit(f"--pass bwd needs an unmasked bf16 or fp16 BHSD workload with D 64 or 128, without "
-                         f"dropout ({w.name})")
+    if w.dtype not in ("bf16", "f16") or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128):
+        raise SystemExit(f"--pass bwd needs an unmasked bf16 or fp16 BHSD workload with D 64 or 128 ({w.name})")
     q, k, v = workloads.make_qkv(w)
     do = workloads.make_dout(w)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
     od, lsed = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal, window=w.window, q_offset=w.q_offset,
-                            softcap=w.softcap)
+                            softcap=w.softcap, dropout_p=w.dropout_p, dropout_seed=w.dropout_seed,
+                            dropout_offset=w.dropout_offset)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws_bytes = fa.fa_bwd_workspace_bytes(w.B, w.H_q, w.qL)
+    ws_bytes = fa.fa_bwd_ex_workspace_bytes(w.B, w.H_q, w.qL, w.kL, w.dropout_p)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ptrs = [t.data_ptr() for t in (qd, kd, vd, od, dod, lsed, dq, dk, dv, ws)]
@@ -523,7 +523,7 @@ def run_ours_bwd(args, w):
 
     def launch():
         rc = fa.fa_bwd_ex(*ptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal, w.window,
-                          w.q_offset, w.softcap, fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16,
+                          w.q_offset, w.softcap, w.dropout_p, w.dropout_seed, w.dropout_offset, fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16,
                           stream.cuda_stream)
         if rc != 0:
             raise fa.FaError(rc, fa.fa_last_error())
@@ -572,7 +572,7 @@ def run_ours_bwd(args, w):
 
         def launch_on(stream_handle, sptrs=sptrs, sws=sws):
             rc = fa.fa_bwd_ex(*sptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal,
-                              w.window, w.q_offset, w.softcap,
+                              w.window, w.q_offset, w.softcap, w.dropout_p, w.dropout_seed, w.dropout_offset,
                               fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16, stream_handle)
             if rc != 0:
                 raise fa.FaError(rc, fa.fa_last_error())
@@ -595,12 +595,13 @@ def run_ours_bwd(args, w):
                      "unit": "TFLOP/s", "frac": flops / (mean_ms * 1e-3) / 1e12 / peak,
                      "traffic": traffic_from_profiles(w, "bwd"),
                      "peak_source": f"{peak_src} bf16 dense (burst)",
-                     "kernels": "one fa_bwd call: D pre-pass + dK/dV + dQ"},
+                     "kernels": "one fa_bwd_ex call: D pre-pass + " + ("keep-mask pre-pass + " if w.dropout_p else "")
+                                + "dK/dV + dQ"},
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
                    "samples": clocks["samples"]},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (4 if w.dropout_p else 3) * args.steps,
         "timed_region_s": wall,
         "call_ms": {"min": min(call_ms), "median": statistics.median(call_ms), "max": max(call_ms)},
     }

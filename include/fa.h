@@ -224,18 +224,38 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int qL, int kL, int D, float scale, int causal, int dtype, void* stream);
 
 /*
+ * fa_bwd_ex_workspace_bytes -- bytes of scratch fa_bwd_ex needs: those of
+ * fa_bwd_workspace_bytes, plus, when dropout_p > 0, the keep decisions of
+ * every (row, key) pair as a bit mask, 16 bytes per row and 128-key block
+ * (B * H_q * qL * ceil(kL / 128) * 16 bytes).  -1 for non-positive sizes or
+ * dropout_p outside [0, 1].  Pure function of its arguments.
+ */
+long long fa_bwd_ex_workspace_bytes(int B, int H_q, int qL, int kL, float dropout_p);
+
+/*
  * fa_bwd_ex -- fa_bwd for a forward that used a sliding window, a causal
  * diagonal offset and/or a softcap (fa_fwd_args.window, .q_offset, .softcap,
  * same meaning and limits: window >= 0, |q_offset| < 2^30, softcap finite
  * and >= 0): key j takes part in row i's softmax only if j <= i + q_offset
  * (causal) and j > i + q_offset - window (window > 0); with softcap c > 0
  * the scores are t = c tanh(scale q.k / c), so dS carries the factor
- * 1 - tanh^2 (recovered from P and L).  All zero is fa_bwd.  Dropout has no
- * backward here.  Arguments, results and errors otherwise as fa_bwd.
+ * 1 - tanh^2 (recovered from P and L).  dropout_p, dropout_seed and
+ * dropout_offset are the forward's (the fa_fwd_args fields of the same names;
+ * p outside [0, 1]: FA_ERR_INVALID_ARGUMENT; p > 0 with kL not a multiple of
+ * 4: FA_ERR_UNSUPPORTED).  The backward regenerates the forward's keep
+ * decisions Z_ij in {0, 1 / (1 - p)} from the same counter-based generator,
+ * so that dV = (P Z)^T dO and dS = P (Z dP - D) with D = rowsum(dO O), O the
+ * forward's (dropped) output: the chain rule through the forward's dropout
+ * (ruDNN "dense_attention.rs", `keep`).  The workspace must hold
+ * fa_bwd_ex_workspace_bytes(B, H_q, qL, kL, dropout_p) bytes (with dropout
+ * the decisions are drawn once into it, by a fourth launch, and read by both
+ * gradient kernels).  All zero is fa_bwd.  Arguments, results and errors
+ * otherwise as fa_bwd.
  */
 int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
               void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
-              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap, int dtype,
+              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap,
+              float dropout_p, unsigned long long dropout_seed, unsigned long long dropout_offset, int dtype,
               void* stream);
 
 /*
@@ -255,7 +275,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 
 /* ABI version: major * 100 + minor (1.05: fa_bwd and fa_bwd_noalloc accept
  * FA_DTYPE_F16; 1.06: fa_fwd_args.workspace, fa_fwd_workspace_bytes; 1.07:
- * fa_bwd_ex). */
+ * fa_bwd_ex; 1.08: fa_bwd_ex takes the forward's dropout arguments,
+ * fa_bwd_ex_workspace_bytes). */
 int fa_version(void);
 
 #ifdef __cplusplus

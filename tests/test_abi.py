@@ -30,7 +30,7 @@ def _declared_functions():
 def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
         ["fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_bytes",
-         "fa_bwd_noalloc",
+         "fa_bwd_ex_workspace_bytes", "fa_bwd_noalloc",
          "fa_last_error",
          "fa_sync_status",
          "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_timeout_cycles", "fa_version"])
@@ -63,7 +63,7 @@ def test_args_struct_matches_header(tmp_path):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 107
+    assert fa.fa_version() == 108
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -201,6 +201,24 @@ def test_bwd_workspace_size(fa):
     assert fa.fa_bwd_workspace_bytes(0, 1, 3) == -1
 
 
+def test_bwd_ex_workspace_size(fa):
+    # no dropout: the D vector alone; with dropout: plus 16 bytes per row and 128-key block
+    assert fa.fa_bwd_ex_workspace_bytes(2, 32, 4096, 4096, 0.0) == fa.fa_bwd_workspace_bytes(2, 32, 4096)
+    assert fa.fa_bwd_ex_workspace_bytes(2, 32, 4096, 4096, 0.1) == 2 * 32 * 4096 * 4 + 2 * 32 * 4096 * 32 * 16
+    assert fa.fa_bwd_ex_workspace_bytes(1, 1, 3, 200, 1.0) == 256 + 3 * 2 * 16
+    assert fa.fa_bwd_ex_workspace_bytes(1, 1, 3, 0, 0.1) == -1
+    assert fa.fa_bwd_ex_workspace_bytes(1, 1, 3, 8, 1.5) == -1
+    assert fa.fa_bwd_ex_workspace_bytes(0, 1, 3, 8, 0.0) == -1
+
+
+def test_bwd_ex_rejects_workspace_without_room_for_the_keep_mask(fa):
+    # enough for the D vector, not for the keep mask of a dropout call
+    need = fa.fa_bwd_ex_workspace_bytes(1, 2, 128, 128, 0.1)
+    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, P, need - 16, 1, 2, 2, 128, 128, 128, 0.125, 1, 0, 0, 0.0, 0.1,
+                        7, 0, 1, None) == 1
+    assert "workspace" in fa.fa_last_error()
+
+
 @pytest.mark.parametrize("kw,status,needle", [
     (dict(dout=None), 1, "non-NULL"),
     (dict(ws=None), 1, "non-NULL"),
@@ -218,12 +236,15 @@ def test_bwd_validation_rejects(fa, kw, status, needle):
     assert needle in fa.fa_last_error()
 
 
-@pytest.mark.parametrize("window,q_offset,softcap,needle", [(-1, 0, 0.0, "window"), (0, 1 << 30, 0.0, "q_offset"),
-                                                            (0, -(1 << 30), 0.0, "q_offset"),
-                                                            (0, 0, -1.0, "softcap"), (0, 0, float("inf"), "softcap")])
-def test_bwd_ex_validation_rejects(fa, window, q_offset, softcap, needle):
-    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, P, 1 << 20, 1, 2, 2, 128, 128, 128, 0.125, 1, window, q_offset,
-                        softcap, 1, None) == 1
+@pytest.mark.parametrize("window,q_offset,softcap,drop_p,kL,status,needle", [
+    (-1, 0, 0.0, 0.0, 128, 1, "window"), (0, 1 << 30, 0.0, 0.0, 128, 1, "q_offset"),
+    (0, -(1 << 30), 0.0, 0.0, 128, 1, "q_offset"), (0, 0, -1.0, 0.0, 128, 1, "softcap"),
+    (0, 0, float("inf"), 0.0, 128, 1, "softcap"), (0, 0, 0.0, -0.1, 128, 1, "dropout_p"),
+    (0, 0, 0.0, 1.5, 128, 1, "dropout_p"), (0, 0, 0.0, float("nan"), 128, 1, "dropout_p"),
+    (0, 0, 0.0, 0.1, 130, 2, "multiple of 4")])
+def test_bwd_ex_validation_rejects(fa, window, q_offset, softcap, drop_p, kL, status, needle):
+    assert fa.fa_bwd_ex(P, P, P, P, P, P, P, P, P, P, 1 << 20, 1, 2, 2, 128, kL, 128, 0.125, 1, window, q_offset,
+                        softcap, drop_p, 7, 0, 1, None) == status
     assert needle in fa.fa_last_error()
 
 

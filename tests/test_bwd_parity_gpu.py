@@ -10,7 +10,10 @@ each) before the dV, dK and dQ products, the inputs and the stored results
 are bf16, and accumulation is fp32; the resulting error is a few 2^-9 of the
 tensor's scale, well inside 2e-2.  fp16 I/O (P and dS rounded to fp16,
 relative error <= 2^-11) gets a quarter of that bound, 5e-3, as the forward's
-fp16 tolerance does.
+fp16 tolerance does.  With dropout the backward regenerates the forward's
+keep decisions from the same seed and offset; the oracle takes its
+multipliers from the forward oracle's generator, so a backward that drew
+other bits than the forward fails the comparison.
 """
 import numpy as np
 import pytest
@@ -45,6 +48,17 @@ CASES = [
     S("bwd_softcap_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "bf16", causal=True, softcap=2.0, seed=56),
     S("bwd_softcap_window_f16_d64", 1, 2, 1, 300, 420, 64, "f16", causal=True, window=120, q_offset=120,
       softcap=3.0, seed=57),
+    # dropout (fa_bwd_ex): the forward's seed and offset; kL a multiple of 4
+    S("bwd_dropout_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "bf16", causal=True, dropout_p=0.1,
+      dropout_seed=2024, seed=61),
+    S("bwd_dropout_f16_d64_ragged", 2, 2, 1, 200, 200, 64, "f16", causal=True, dropout_p=0.3,
+      dropout_seed=77, dropout_offset=12345, seed=62),
+    S("bwd_dropout_d64_noncausal_long_kv", 1, 2, 2, 130, 600, 64, "bf16", dropout_p=0.5, dropout_seed=5,
+      seed=63),
+    S("bwd_dropout_softcap_window_d128", 1, 2, 1, 300, 420, 128, "bf16", causal=True, window=120, q_offset=120,
+      softcap=3.0, dropout_p=0.2, dropout_seed=9, seed=64),
+    S("bwd_dropout_offset_past_2p32_d128", 1, 2, 2, 256, 256, 128, "bf16", causal=True, dropout_p=0.15,
+      dropout_seed=(1 << 40) + 3, dropout_offset=(1 << 33) + 5, seed=65),
 ]
 SOFTCAP_SCALE = 0.35  # scale * |q.k| ~ 0.35 * sqrt(D) * N(0, 1): several times the cap
 
@@ -59,10 +73,11 @@ def _run(w):
     dev = "cuda:0"
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
     scale = SOFTCAP_SCALE if w.softcap else w.sm_scale
+    drop = dict(dropout_p=w.dropout_p, dropout_seed=w.dropout_seed, dropout_offset=w.dropout_offset)
     o, lse = fa.attention(qd, kd, vd, scale=scale, causal=w.causal, window=w.window, q_offset=w.q_offset,
-                          softcap=w.softcap)
+                          softcap=w.softcap, **drop)
     dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, scale=scale, causal=w.causal, window=w.window,
-                                  q_offset=w.q_offset, softcap=w.softcap)
+                                  q_offset=w.q_offset, softcap=w.softcap, **drop)
     assert fa.fa_sync_status(None) == fa.fa.FA_OK, fa.fa_last_error()
     return (q, k, v, do), (dq, dk, dv)
 
@@ -86,7 +101,9 @@ def test_bwd_elementwise(w):
     rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
                                       do.double().numpy(),
                                       fp32_scale(w, SOFTCAP_SCALE if w.softcap else None), causal=w.causal,
-                                      window=w.window, q_offset=w.q_offset, softcap=float(np.float32(w.softcap)))
+                                      window=w.window, q_offset=w.q_offset, softcap=float(np.float32(w.softcap)),
+                                      dropout_p=float(np.float32(w.dropout_p)), seed=w.dropout_seed,
+                                      offset=w.dropout_offset)
     tol = REL_TOL[w.dtype]
     _compare(f"{w.name} dQ", dq, rq, tol)
     _compare(f"{w.name} dK", dk, rk, tol)
@@ -121,3 +138,22 @@ def test_bwd_gqa_sums_group_heads():
         s = g2.float().sum(dim=1, keepdim=True)
         err = (g.float() - s).abs().max().item() / max(s.abs().max().item(), 1e-30)
         assert err < 2e-2, err
+
+
+def test_bwd_dropout_all_dropped_gives_zero_gradients():
+    """p = 1 drops every weight: O = 0, so D = 0 and dS = P (0 dP - 0) = 0; all three gradients are exactly 0."""
+    w = S("bwd_dropout_p1", 1, 2, 1, 256, 256, 64, "bf16", causal=True, dropout_p=1.0, dropout_seed=3, seed=66)
+    _, grads = _run(w)
+    for g in grads:
+        assert torch.count_nonzero(g).item() == 0
+
+
+def test_bwd_dropout_seed_changes_gradients():
+    """Another seed gives other keep decisions and so other gradients; the same seed repeats them exactly."""
+    w = CASES[-1]
+    _, a = _run(w)
+    _, b = _run(w)
+    _, c = _run(w.with_(dropout_seed=w.dropout_seed + 1))
+    for x, y, z in zip(a, b, c):
+        assert torch.equal(x, y)
+        assert not torch.equal(x, z)
