@@ -101,13 +101,24 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
 
   // 3. Dropout: the forward's keep decisions, once for both kernels.
   if constexpr (kDrop) {
-    const int n_kb = p.n_kt;
-    const long long n_units = (long long)a.B * a.Hq * p.n_qt * n_kb;
+    const long long n_units = (long long)a.B * a.Hq * p.n_qt * p.n_kt;
+    if (n_units > 0x7fffffffLL) {  // the kernel's 32-bit unit index u + gridDim.x must not wrap
+      set_error("dropout keep mask of %lld tiles is out of range", n_units);
+      return 2;
+    }
+    KeepMaskArgs ka;
+    uint32_t k0 = (uint32_t)a.dropout_seed, k1 = (uint32_t)(a.dropout_seed >> 32);
+    for (int r = 0; r < 10; ++r, k0 += 0x9E3779B9u, k1 += 0xBB67AE85u) {  // Philox4x32 key schedule
+      ka.rk0[r] = k0;
+      ka.rk1[r] = k1;
+    }
+    ka.n_kb = (uint32_t)p.n_kt;
+    ka.n_units = (uint32_t)n_units;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
     const unsigned grid = (unsigned)std::min<long long>(n_units, (long long)sms * 8);
-    fa_bwd_keep_mask_kernel<<<grid, 256, 0, a.stream>>>(p, n_kb, n_units);
+    fa_bwd_keep_mask_kernel<<<grid, 256, 0, a.stream>>>(p, ka);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
       set_error("keep-mask launch failed: %s", cudaGetErrorString(e));

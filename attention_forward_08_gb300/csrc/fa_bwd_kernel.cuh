@@ -176,6 +176,31 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const uint4* __restr
 
 // ---------------------------------------------------------------- keep-mask pre-pass
 
+// Arguments of the keep-mask pre-pass beyond BwdParams: the ten round keys of
+// Philox4x32-10 for the seed (key words raised by the published constants
+// each round), computed once on the host.
+struct KeepMaskArgs {
+  uint32_t rk0[10], rk1[10];
+  uint32_t n_kb, n_units;  // 128-key blocks per row; (b, h, row tile, key block) units
+};
+
+// The published Philox4x32-10 round function (Salmon, Moraes, Dror, Shaw,
+// SC11) with the round keys taken from the pre-pass arguments.
+__device__ __forceinline__ uint4 philox_10_rk(uint32_t c0, uint32_t c1, const KeepMaskArgs& ka) {
+  uint32_t x0 = c0, x1 = c1, x2 = 0u, x3 = 0u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    uint32_t hi0, lo0, hi2, lo2;
+    mul_wide(0xD2511F53u, x0, hi0, lo0);
+    mul_wide(0xCD9E8D57u, x2, hi2, lo2);
+    x0 = hi2 ^ x1 ^ ka.rk0[r];
+    x1 = lo2;
+    x2 = hi0 ^ x3 ^ ka.rk1[r];
+    x3 = lo0;
+  }
+  return make_uint4(x0, x1, x2, x3);
+}
+
 // The forward's dropout decisions for the backward: position ((b H_q + h) qL
 // + i) kL + j, one Philox4x32-10 block per 4 keys at counter offset +
 // position / 4 (kL is a multiple of 4), keep iff word >> 8 >= threshold;
@@ -183,35 +208,38 @@ __global__ void __launch_bounds__(256) fa_bwd_rowdot_kernel(const uint4* __restr
 // row of which can see some key of.  A unit of work is one tile: warp w draws
 // rows w, w + 8, ..., lane l the block of keys 4 l .. 4 l + 3, and the 4-bit
 // results of 8 lanes become one word with three shuffles.  Throughput-bound
-// on the integer pipes (the 32 x 32-bit multiplies), at full occupancy.
-__global__ void __launch_bounds__(256) fa_bwd_keep_mask_kernel(const BwdParams p, int n_kb, long long n_units) {
+// on the integer pipes (the 32 x 32-bit multiplies): 8 CTAs of 256 threads
+// per SM (32 registers), 32-bit unit decoding (the host keeps n_units below
+// 2^31, so u + gridDim.x cannot wrap), counters and destinations advanced by
+// adds.
+__global__ void __launch_bounds__(256, 8) fa_bwd_keep_mask_kernel(const BwdParams p, const KeepMaskArgs ka) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long row_ctr = (unsigned long long)(p.kL / 4);
-  const uint32_t thr = p.drop_threshold;
-  for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int kb = (int)(u % n_kb);
-    const long long rest = u / n_kb;
-    const int r0 = (int)(rest % p.n_qt) * 128;
-    const long long bh = rest / p.n_qt;
-    const int r1 = min(r0 + 128, p.qL) - 1, c0 = kb * 128, c1 = min(c0 + 128, p.kL) - 1;
+  const uint32_t thr = p.drop_threshold, nqt = (uint32_t)p.n_qt;
+  for (uint32_t u = blockIdx.x; u < ka.n_units; u += gridDim.x) {
+    const uint32_t kb = u % ka.n_kb, rest = u / ka.n_kb;
+    const int r0 = (int)(rest % nqt) * 128;
+    const uint32_t bh = rest / nqt;
+    const int r1 = min(r0 + 128, p.qL) - 1, c0 = (int)kb * 128, c1 = min(c0 + 128, p.kL) - 1;
     // Row i sees keys i + q_offset - window < j <= i + q_offset (the causal
     // and window limits); over rows r0 .. r1 those ranges join into one.
     if (p.causal && (long long)c0 > (long long)r1 + p.q_offset) continue;
     if (p.window > 0 && (long long)c1 < (long long)r0 + p.q_offset - p.window + 1) continue;
+    const long long row = (long long)bh * p.qL + r0 + warp;
+    unsigned long long c = p.drop_offset + (unsigned long long)row * row_ctr + (unsigned long long)(c0 / 4 + lane);
+    uint32_t* dst = p.keep_mask + row * p.keep_row_words + c0 / 32 + (lane >> 3);
 #pragma unroll 4
     for (int t = 0; t < 16; ++t) {
-      const int i = r0 + warp + 8 * t;
-      const unsigned long long c =
-          p.drop_offset + ((unsigned long long)bh * p.qL + i) * row_ctr + (unsigned long long)(c0 / 4 + lane);
-      const uint4 w = philox_10((uint32_t)c, (uint32_t)(c >> 32), p.seed_lo, p.seed_hi);
+      const uint4 w = philox_10_rk((uint32_t)c, (uint32_t)(c >> 32), ka);
       const uint32_t nib = ((w.x >> 8) >= thr ? 1u : 0u) | ((w.y >> 8) >= thr ? 2u : 0u) |
                            ((w.z >> 8) >= thr ? 4u : 0u) | ((w.w >> 8) >= thr ? 8u : 0u);
       uint32_t x = nib << (4 * (lane & 7));
       x |= __shfl_xor_sync(0xffffffffu, x, 1);
       x |= __shfl_xor_sync(0xffffffffu, x, 2);
       x |= __shfl_xor_sync(0xffffffffu, x, 4);
-      if (i < p.qL && (lane & 7) == 0)
-        p.keep_mask[((long long)bh * p.qL + i) * p.keep_row_words + c0 / 32 + (lane >> 3)] = x;
+      if (r0 + warp + 8 * t < p.qL && (lane & 7) == 0) *dst = x;
+      c += 8 * row_ctr;
+      dst += 8 * p.keep_row_words;
     }
   }
 }
@@ -309,10 +337,10 @@ __device__ __forceinline__ float keep_mult(uint32_t word, int bit, float scale) 
   return __int_as_float(__float_as_int(scale) & (0u - ((word >> bit) & 1u)));
 }
 
-// dS with dropout (and, when inv_out > 0, the softcap's factor):
-// dS = P (Z dP - d) f, Z = keep_mult(bits, scale); kword(cc) gives the keep
-// word of columns 32 cc .. 32 cc + 31.
-template <class C, class F, class L, class K>
+// dS with dropout (and, with kCap, the softcap's factor): dS = P (Z dP - d)
+// f, Z = keep_mult(bits, scale); kword(cc) gives the keep word of columns
+// 32 cc .. 32 cc + 31.
+template <class C, bool kCap, class F, class L, class K>
 __device__ __forceinline__ void bwd_ds_pass_drop(uint32_t tdp, const float (&p)[128], F dsub, L l2, float inv_out,
                                                  K kword, float scale) {
 #pragma unroll
@@ -328,7 +356,7 @@ __device__ __forceinline__ void bwd_ds_pass_drop(uint32_t tdp, const float (&p)[
       const int c0 = cc * 32 + 2 * e;
       float d0 = p[c0] * fmaf(keep_mult(kw, 2 * e, scale), __uint_as_float(rr[2 * e]), -dsub(c0));
       float d1 = p[c0 + 1] * fmaf(keep_mult(kw, 2 * e + 1, scale), __uint_as_float(rr[2 * e + 1]), -dsub(c0 + 1));
-      if (inv_out > 0.0f) {
+      if constexpr (kCap) {
         d0 *= softcap_factor(p[c0], l2(c0), inv_out);
         d1 *= softcap_factor(p[c0 + 1], l2(c0 + 1), inv_out);
       }
@@ -707,9 +735,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if constexpr (C::kDrop) {
-        bwd_ds_pass_drop<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; }, [&](int c) { return l2s[c]; },
-                            p.softcap_on ? p.softcap_inv : 0.0f, [&](int cc) { return keep_words[cc]; },
-                            p.drop_scale);
+        auto dsub = [&](int c) { return l2s[C::kTile + c]; };
+        auto l2c = [&](int c) { return l2s[c]; };
+        auto kword = [&](int cc) { return keep_words[cc]; };
+        if (p.softcap_on)
+          bwd_ds_pass_drop<C, true>(tDP, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
+        else
+          bwd_ds_pass_drop<C, false>(tDP, pr, dsub, l2c, 0.0f, kword, p.drop_scale);
       } else if (C::kFeat && p.softcap_on) {
         bwd_ds_pass_softcap<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; }, [&](int c) { return l2s[c]; },
                                p.softcap_inv);
@@ -1015,8 +1047,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if constexpr (C::kDrop) {
-        bwd_ds_pass_drop<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
-                            p.softcap_on ? p.softcap_inv : 0.0f, [&](int cc) { return kw[cc]; }, p.drop_scale);
+        const uint32_t tdp = (j & 1) ? tDP2 : tDP;
+        auto dsub = [&](int) { return di; };
+        auto l2c = [&](int) { return l2; };
+        auto kword = [&](int cc) { return kw[cc]; };
+        if (p.softcap_on)
+          bwd_ds_pass_drop<C, true>(tdp, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
+        else
+          bwd_ds_pass_drop<C, false>(tdp, pr, dsub, l2c, 0.0f, kword, p.drop_scale);
       } else if (C::kFeat && p.softcap_on) {
         bwd_ds_pass_softcap<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
                                p.softcap_inv);
