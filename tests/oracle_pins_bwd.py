@@ -9,7 +9,8 @@ gradients disagree with:
   - an independent library routine (torch fp64 CPU autograd through
     scaled_dot_product_attention, K/V repeated per GQA group),
   - closed forms (Q = 0 gives uniform weights, so dV_j sums dO_i / n_i over
-    the rows that see key j; rows of equal V make O independent of Q and K),
+    the rows that see key j, each times its dropout multiplier when there is
+    dropout; rows of equal V make O independent of Q and K),
   - invariants that hold exactly (shifting every key by the same vector leaves
     every softmax row unchanged, so sum_j dK_j = 0; gradients are linear in dO).
 Each planted mistake (dropped scale in dK, sign of the D term, q in place of
@@ -236,6 +237,30 @@ def pin_uniform_weights_dv(grad, fwd):
         _close(dv, want, 1e-12, f"dV closed form causal={causal}")
 
 
+def pin_uniform_weights_dv_dropout(grad, fwd):
+    """Q = 0 with dropout: row i weighs its n_i allowed keys by Z_ij / n_i, so dV_j sums
+    Z_ij dO_i / n_i; Z_ij is the forward oracle generator's multiplier at position
+    ((b H_q + h) qL + i) kL + j."""
+    import oracle
+    r = _rng(113)
+    B, Hq, Hkv, qL, kL, D = 1, 4, 2, 6, 8, 3
+    q = np.zeros((B, Hq, qL, D))
+    _, k, v, g = _inputs(r, B, Hq, Hkv, qL, kL, D)
+    p, seed, off = 0.4, 77, 5
+    z = oracle.dropout_keep(p, seed, off, 0, B * Hq * qL * kL).reshape(B, Hq, qL, kL)
+    assert 0 < int(np.sum(z == 0.0)) < z.size  # some weights dropped, some kept
+    rep = Hq // Hkv
+    for causal in (False, True):
+        _, _, dv = grad(q, k, v, g, 0.8, causal=causal, dropout_p=p, seed=seed, offset=off)
+        want = np.zeros_like(v)
+        for h in range(Hq):
+            for i in range(qL):
+                n = (i + 1) if causal else kL
+                for j in range(n):
+                    want[0, h // rep, j] += z[0, h, i, j] * g[0, h, i] / n
+        _close(dv, want, 1e-12, f"dV closed form with dropout causal={causal}")
+
+
 def pin_equal_values_no_qk_gradient(grad, fwd):
     """Every V row equal: O_i = V_0 whatever the weights, so dQ = dK = 0 and dV_j = sum_i P_ij dO_i."""
     r = _rng(104)
@@ -279,6 +304,7 @@ ALL_PINS = [
     pin_finite_differences_dropout,
     pin_torch_autograd,
     pin_uniform_weights_dv,
+    pin_uniform_weights_dv_dropout,
     pin_equal_values_no_qk_gradient,
     pin_key_shift_invariance,
     pin_linear_in_dout,
