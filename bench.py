@@ -277,10 +277,42 @@ def barrier(world: int):
 
 # ----------------------------------------------------------------------------- arms
 
+def run_reference_bwd(args, w):
+    """The reference arm of ``--pass bwd``: the fp64 gradient oracle, timed on a bounded sample of
+    the workload each step (``oracle_bwd_sample``), on the backward's metric."""
+    check_bwd_workload(w)
+    q, k, v = workloads.make_qkv(w)
+    do = workloads.make_dout(w)
+    per_step = max(2.0, min(15.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_bwd_sample(w, q, k, v, do, per_step / 4)
+    flops = secs = 0.0
+    threads, sample = 1, ""
+    for _ in range(args.steps):
+        f, dt, sample, threads = oracle_bwd_sample(w, q, k, v, do, per_step)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": "attention bwd TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(config_of(w, args), **{"pass": "bwd"}),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {sample}, fp64 C gradient oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.pass_ == "bwd":
+        return run_reference_bwd(args, w)
     q, k, v, m = workloads.make_inputs(w)
     per_step = max(2.0, min(15.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -495,6 +527,11 @@ def oracle_bwd_sample(w, q, k, v, do, seconds):
     return 2.5 * sub.flops(), dt, f"{n_kv} whole GQA groups of batch 0 on the first {Ls} positions", min(threads, n_kv)
 
 
+def check_bwd_workload(w):
+    if w.dtype not in ("bf16", "f16") or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128):
+        raise SystemExit(f"--pass bwd needs an unmasked bf16 or fp16 BHSD workload with D 64 or 128 ({w.name})")
+
+
 def run_ours_bwd(args, w):
     import torch
     world, rank, local = dist_env()
@@ -506,8 +543,7 @@ def run_ours_bwd(args, w):
     torch.cuda.set_device(dev)
     import attention_forward_08_gb300 as fa
     fa.load_library()
-    if w.dtype not in ("bf16", "f16") or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128):
-        raise SystemExit(f"--pass bwd needs an unmasked bf16 or fp16 BHSD workload with D 64 or 128 ({w.name})")
+    check_bwd_workload(w)
     q, k, v = workloads.make_qkv(w)
     do = workloads.make_dout(w)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)

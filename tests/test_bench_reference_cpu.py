@@ -1,0 +1,29 @@
+"""bench.py's reference arm (the fp64 oracle on the host cores) on CPU: one
+short run of each pass prints the contract's JSON line, on the metric of the
+pass it was asked for."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("pass_,workload,metric", [
+    ("fwd", "fp32_b1_h2_l128_d64", "attention fwd TFLOP/s"),
+    ("bwd", "bf16_causal_b4_h8_l1024_d64", "attention bwd TFLOP/s"),
+])
+def test_reference_line(pass_, workload, metric):
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--pass", pass_, "--workload", workload,
+                          "--steps", "1", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == metric
+    assert line["config"]["workload"] == workload
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["higher_is_better"] is True and line["steps"] == 1 and line["warmup"] == 3
