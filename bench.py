@@ -82,6 +82,20 @@ def algorithmic_bytes(w: workloads.Workload) -> int:
     return qo + kv + lse + mask
 
 
+EX2_PER_CLK_PER_SM = 32  # special-function-unit exponentials per clock per SM on this GPU generation
+
+
+def exp_roofline(w: workloads.Workload, mean_ms: float, sms: int, sm_mhz):
+    """Secondary roofline of the softmax's exponentials: one ex2 per allowed score (the FLOP
+    count's 4 D per score) per call, against SMs x 32 ex2 per clock x the median SM clock sampled
+    during the timed region -- a derived peak, not a measured one (None without a clock sample)."""
+    achieved = w.flops() / (4.0 * w.D) / (mean_ms * 1e-3) / 1e9
+    peak = sms * EX2_PER_CLK_PER_SM * sm_mhz * 1e-3 if sm_mhz else None
+    return {"bound": "sfu", "achieved": achieved, "peak": peak, "unit": "Gexp/s",
+            "frac": achieved / peak if peak else None,
+            "peak_source": f"derived: {sms} SMs x {EX2_PER_CLK_PER_SM} ex2/clk x median sampled SM clock"}
+
+
 def traffic_from_profiles(w: workloads.Workload, kind: str = "fwd"):
     """DRAM bytes per launch (per call for the backward) from a committed ncu summary, if it was
     taken on the current kernel source."""
@@ -483,6 +497,8 @@ def run_ours(args, w):
         "gpu_launches": launches_per_call * args.steps,
         "timed_region_s": wall,
         "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)},
+        "exp_roofline": exp_roofline(w, mean_ms, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                     clocks["sm_mhz"]),
     }
     if rank == 0 and not args.no_cpu_baseline:
         f, dt, nrows, threads = oracle_sample(w, q, k, v, m, seconds=args.cpu_seconds)
