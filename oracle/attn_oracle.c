@@ -347,5 +347,5 @@ int oracle_philox4x32_10(const uint32_t *ctr, uint32_t k0, uint32_t k1, uint32_t
     return 0;
 }
 
-/* Number of the planted mistake this build carries (0 for the real oracle). */
+/* Number of the planted mistake this compiled library carries (0 for the real oracle). */
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

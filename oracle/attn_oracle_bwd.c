@@ -250,5 +250,5 @@ int oracle_attention_bwd(const double *q, const double *k, const double *v, cons
                                    0, 0, 0.0, NULL, n_threads);
 }
 
-/* Number of the planted mistake this build carries (0 for the real oracle). */
+/* Number of the planted mistake this compiled library carries (0 for the real oracle). */
 int oracle_bwd_mutant_id(void) { return ORACLE_MUTANT; }
