@@ -81,6 +81,15 @@ int device_setup(int dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+// B * H * L > cap for positive B, H, L, without forming the product (which
+// can exceed the int64 range): B * H < 2^62 always fits, and
+// L > floor(cap / (B * H)) holds exactly when L * B * H > cap.
+bool rows_exceed(int B, int H, int L, long long cap) { return (long long)L > cap / ((long long)B * H); }
+
+namespace {
+
 // Words per row of the backward's keep mask: 4 (128 keys) per 128-key block.
 long long keep_row_words(int kL) { return ((long long)kL + 127) / 128 * 4; }
 
@@ -153,6 +162,13 @@ int validate(const fa_fwd_args* a) {
     set_error("head dim D = %d is not supported (64, 128 or 256)", a->D);
     return FA_ERR_UNSUPPORTED;
   }
+  // Work units and flat L indices must fit the kernel's int32 arithmetic
+  // (key rows too: no device holds a K of 2^31 rows, and the workspace sizes
+  // below multiply them).
+  if (rows_exceed(a->B, a->H_q, a->qL, 0x7fffffffLL) || rows_exceed(a->B, a->H_kv, a->kL, 0x7fffffffLL)) {
+    set_error("B * H_q * qL or B * H_kv * kL exceeds 2^31 - 1");
+    return FA_ERR_UNSUPPORTED;
+  }
   const int esz = a->dtype == FA_DTYPE_F32 ? 4 : 2;
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->o)) {
     set_error("q, k, v and o must be 16-byte aligned");
@@ -187,11 +203,6 @@ int validate(const fa_fwd_args* a) {
         set_error("mask strides must be >= 0");
         return FA_ERR_INVALID_ARGUMENT;
       }
-  }
-  // Work units and flat L indices must fit the kernel's int32 arithmetic.
-  if ((long long)a->B * a->H_q * a->qL > 0x7fffffffLL) {
-    set_error("B * H_q * qL = %lld exceeds 2^31 - 1", (long long)a->B * a->H_q * a->qL);
-    return FA_ERR_UNSUPPORTED;
   }
   return FA_OK;
 }
@@ -232,6 +243,69 @@ EncodeTiledFn get_encode_tiled() {
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
   return g_encode;
+}
+
+int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 const void* dq, const void* dk, const void* dv, int B, int H_q, int H_kv, int qL, int kL, int D,
+                 float scale, int window, int q_offset, float softcap, float dropout_p, int dtype) {
+  if (!(dropout_p >= 0.0f && dropout_p <= 1.0f)) {
+    set_error("dropout_p must lie in [0, 1]");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (dropout_p > 0.0f && kL % 4 != 0) {
+    set_error("dropout needs kL (%d) to be a multiple of 4", kL);
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (!(std::isfinite(softcap) && softcap >= 0.0f)) {
+    set_error("softcap must be finite and >= 0 (0 = off)");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (window < 0) {
+    set_error("window (%d) must be >= 0 (0 = no sliding window)", window);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (q_offset <= -(1 << 30) || q_offset >= (1 << 30)) {
+    set_error("|q_offset| (%d) must be < 2^30", q_offset);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) {
+    set_error("q, k, v, o, dout, lse, dq, dk and dv must all be non-NULL");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || qL <= 0 || kL <= 0) {
+    set_error("B (%d), H_q (%d), H_kv (%d), qL (%d) and kL (%d) must be > 0", B, H_q, H_kv, qL, kL);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (H_q % H_kv != 0) {
+    set_error("H_q (%d) must be divisible by H_kv (%d)", H_q, H_kv);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (!std::isfinite(scale)) {
+    set_error("scale must be finite");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) {
+    const bool known = dtype == FA_DTYPE_F32;
+    set_error(known ? "the backward pass supports bf16 and fp16 I/O only"
+                    : "dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)",
+              dtype);
+    return known ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
+  }
+  if (D != 64 && D != 128) {
+    set_error("head dim D = %d is not supported by the backward pass (64 or 128)", D);
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (rows_exceed(B, H_q, qL, 0x7fffffffLL) || rows_exceed(B, H_kv, kL, 0x7fffffffLL)) {
+    set_error("row counts exceed 2^31 - 1");
+    return FA_ERR_UNSUPPORTED;
+  }
+  const void* ptrs[9] = {q, k, v, o, dout, dq, dk, dv, lse};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) {
+      set_error("q, k, v, o, dout, lse, dq, dk, dv and workspace must be 16-byte aligned");
+      return FA_ERR_MISALIGNED;
+    }
+  return FA_OK;
 }
 
 }  // namespace fa
@@ -472,7 +546,7 @@ void fa_set_max_ctas(int n) {
 }
 
 long long fa_bwd_workspace_bytes(int B, int H_q, int qL) {
-  if (B <= 0 || H_q <= 0 || qL <= 0) return -1;
+  if (B <= 0 || H_q <= 0 || qL <= 0 || fa::rows_exceed(B, H_q, qL, 0x7fffffffLL)) return -1;
   const long long bytes = (long long)B * H_q * qL * 4;
   return (bytes + 255) / 256 * 256;
 }
@@ -492,75 +566,29 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               void* stream) {
   using namespace fa;
   g_err[0] = '\0';
-  if (!(dropout_p >= 0.0f && dropout_p <= 1.0f)) {
-    set_error("dropout_p must lie in [0, 1]");
+  int rc = validate_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, window, q_offset,
+                        softcap, dropout_p, dtype);
+  if (rc != FA_OK) return rc;
+  if (!workspace) {
+    set_error("workspace must be non-NULL");
     return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (dropout_p > 0.0f && kL % 4 != 0) {
-    set_error("dropout needs kL (%d) to be a multiple of 4", kL);
-    return FA_ERR_UNSUPPORTED;
-  }
-  if (!(std::isfinite(softcap) && softcap >= 0.0f)) {
-    set_error("softcap must be finite and >= 0 (0 = off)");
-    return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (window < 0) {
-    set_error("window (%d) must be >= 0 (0 = no sliding window)", window);
-    return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (q_offset <= -(1 << 30) || q_offset >= (1 << 30)) {
-    set_error("|q_offset| (%d) must be < 2^30", q_offset);
-    return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) {
-    set_error("q, k, v, o, dout, lse, dq, dk, dv and workspace must all be non-NULL");
-    return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (B <= 0 || H_q <= 0 || H_kv <= 0 || qL <= 0 || kL <= 0) {
-    set_error("B (%d), H_q (%d), H_kv (%d), qL (%d) and kL (%d) must be > 0", B, H_q, H_kv, qL, kL);
-    return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (H_q % H_kv != 0) {
-    set_error("H_q (%d) must be divisible by H_kv (%d)", H_q, H_kv);
-    return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (!std::isfinite(scale)) {
-    set_error("scale must be finite");
-    return FA_ERR_INVALID_ARGUMENT;
-  }
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) {
-    const bool known = dtype == FA_DTYPE_F32;
-    set_error(known ? "the backward pass supports bf16 and fp16 I/O only"
-                    : "dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)",
-              dtype);
-    return known ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
-  }
-  if (D != 64 && D != 128) {
-    set_error("head dim D = %d is not supported by the backward pass (64 or 128)", D);
-    return FA_ERR_UNSUPPORTED;
-  }
-  if ((long long)B * H_q * qL > 0x7fffffffLL || (long long)B * H_kv * kL > 0x7fffffffLL) {
-    set_error("row counts exceed 2^31 - 1");
-    return FA_ERR_UNSUPPORTED;
   }
   const long long ws_need = fa_bwd_ex_workspace_bytes(B, H_q, qL, kL, dropout_p);
   if (workspace_bytes < ws_need) {
     set_error("workspace of %lld bytes is smaller than the %lld required", workspace_bytes, ws_need);
     return FA_ERR_INVALID_ARGUMENT;
   }
-  const void* ptrs[10] = {q, k, v, o, dout, dq, dk, dv, workspace, lse};
-  for (const void* ptr : ptrs)
-    if (!aligned16(ptr)) {
-      set_error("q, k, v, o, dout, lse, dq, dk, dv and workspace must be 16-byte aligned");
-      return FA_ERR_MISALIGNED;
-    }
+  if (!aligned16(workspace)) {
+    set_error("workspace must be 16-byte aligned");
+    return FA_ERR_MISALIGNED;
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
     set_error("cudaGetDevice: %s", cudaGetErrorString(e));
     return FA_ERR_CUDA;
   }
-  int rc = device_setup(dev);
+  rc = device_setup(dev);
   if (rc != FA_OK) return rc;
   BwdLaunchArgs a;
   a.q = q;

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "fa_bwd_kernel.cuh"
@@ -17,16 +18,16 @@ namespace fa {
 namespace {
 
 template <class C>
-int set_smem_once(const void* kern, uint32_t bytes, int& configured_device) {
+int set_smem_once(const void* kern, uint32_t bytes, std::atomic<unsigned long long>& configured) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured_device == dev) return 0;
+  if (device_bit_set(configured, dev)) return 0;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute(max dynamic smem = %u): %s", (unsigned)bytes, cudaGetErrorString(e));
     return 4;
   }
-  configured_device = dev;
+  device_bit_mark(configured, dev);
   return 0;
 }
 
@@ -88,7 +89,7 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   p.status = a.status;
   p.timeout_cycles = a.timeout_cycles;
 
-  static int cfg_kv = -1, cfg_q = -1;
+  static std::atomic<unsigned long long> cfg_kv{0}, cfg_q{0};
   if (int rc = set_smem_once<C>((const void*)fa_bwd_dkdv_kernel<C>, C::kKVSmem, cfg_kv)) return rc;
   if (int rc = set_smem_once<C>((const void*)fa_bwd_dq_kernel<C>, C::kQSmem, cfg_q)) return rc;
 

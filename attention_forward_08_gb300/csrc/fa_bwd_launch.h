@@ -32,4 +32,13 @@ struct BwdLaunchArgs {
 // Returns 0, or an fa_status code with the message set.
 int launch_bwd(const BwdLaunchArgs& a);
 
+// B * H * L > cap for positive B, H, L, computed without overflow.
+bool rows_exceed(int B, int H, int L, long long cap);
+
+// Checks a backward call's arguments other than its workspace (fa_bwd_ex's
+// rules); returns FA_OK or an fa_status code with the message set.
+int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 const void* dq, const void* dk, const void* dv, int B, int H_q, int H_kv, int qL, int kL, int D,
+                 float scale, int window, int q_offset, float softcap, float dropout_p, int dtype);
+
 }  // namespace fa

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_launch.h"
 #include "fa_launch.cuh"
 
 namespace {
@@ -27,12 +28,17 @@ float* g_scratch_ptr[kMaxDevices] = {nullptr};
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int qL,
                               int kL, int D, float scale, int causal, int dtype, void* stream) {
-  if (B > 0 && H_q > 0 && qL > 0 && (long long)B * H_q * qL > kNoAllocRows) {
-    fa::set_error("B * H_q * qL = %lld query rows exceed the %lld rows of fa_bwd_noalloc's built-in scratch; "
+  // One factor at a time: B * H_q * qL itself may not fit in 64 bits.
+  if (B > 0 && H_q > 0 && qL > 0 && fa::rows_exceed(B, H_q, qL, kNoAllocRows)) {
+    fa::set_error("B * H_q * qL query rows exceed the %lld rows of fa_bwd_noalloc's built-in scratch; "
                   "call fa_bwd with a workspace instead",
-                  (long long)B * H_q * qL, kNoAllocRows);
+                  kNoAllocRows);
     return FA_ERR_UNSUPPORTED;
   }
+  // The remaining argument checks come before any CUDA call, as for fa_bwd.
+  int rc = fa::validate_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, 0, 0, 0.0f, 0.0f,
+                            dtype);
+  if (rc != FA_OK) return rc;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {

@@ -201,6 +201,19 @@ def test_bwd_workspace_size(fa):
     assert fa.fa_bwd_workspace_bytes(0, 1, 3) == -1
 
 
+def test_row_counts_never_overflow(fa):
+    """Row counts whose product leaves the int64 range are refused, not wrapped: the forward, the
+    backward and the workspace size queries compare one factor at a time."""
+    big = 1 << 21
+    assert _call(fa, B=big, H_q=big, H_kv=big, qL=big, kL=128) == 2
+    assert "2^31" in fa.fa_last_error()
+    assert _call(fa, B=1, H_q=2, H_kv=2, qL=128, kL=2**31 - 1) == 2
+    assert _bwd_call(fa, B=big, H_q=big, H_kv=big, qL=big) == 2
+    assert fa.fa_bwd_workspace_bytes(big, big, big) == -1
+    assert fa.fa_bwd_ex_workspace_bytes(big, big, big, 128, 0.1) == -1
+    assert fa.fa_bwd_workspace_bytes(1, 1, 2**31 - 1) == (4 * (2**31 - 1) + 255) // 256 * 256
+
+
 def test_bwd_ex_workspace_size(fa):
     # no dropout: the D vector alone; with dropout: plus 16 bytes per row and 128-key block
     assert fa.fa_bwd_ex_workspace_bytes(2, 32, 4096, 4096, 0.0) == fa.fa_bwd_workspace_bytes(2, 32, 4096)

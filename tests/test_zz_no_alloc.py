@@ -29,6 +29,29 @@ def test_noalloc_rejects_oversize(fa):
     assert "built-in scratch" in fa.fa_last_error()
 
 
+def _noalloc(fa, B, H_q, qL, dq=0x10000):
+    P = 0x10000
+    return fa.fa.fa_bwd_noalloc(P, P, P, P, P, P, dq, P, P, B, H_q, 1, qL, 128, 128, 0.088, 1,
+                                fa.FA_DTYPE_BF16, None)
+
+
+def test_noalloc_limit_edge(fa):
+    """Exactly 2^21 query rows fit the built-in scratch: the call passes the size guard and reaches the
+    ordinary argument checks (a NULL dq is then the error); one row more is refused."""
+    rc = _noalloc(fa, 1, 2, 1 << 20, dq=None)
+    assert rc == fa.fa.FA_ERR_INVALID_ARGUMENT
+    assert "built-in scratch" not in fa.fa_last_error() and "non-NULL" in fa.fa_last_error()
+    assert _noalloc(fa, 1, 1, (1 << 21) + 1) == fa.fa.FA_ERR_UNSUPPORTED
+    assert "built-in scratch" in fa.fa_last_error()
+    assert _noalloc(fa, 3, 1, 699051) == fa.fa.FA_ERR_UNSUPPORTED        # 3 * 699051 = 2^21 + 1
+
+
+def test_noalloc_row_count_does_not_wrap(fa):
+    """B * H_q * qL = 2^63 would wrap a 64-bit product negative; the guard compares one factor at a time."""
+    assert _noalloc(fa, 1 << 21, 1 << 21, 1 << 21) == fa.fa.FA_ERR_UNSUPPORTED
+    assert _noalloc(fa, 2**31 - 1, 2**31 - 1, 2**31 - 1) == fa.fa.FA_ERR_UNSUPPORTED
+
+
 def _problem(w):
     q, k, v = W.make_qkv(w)
     do = W.make_dout(w)
