@@ -417,7 +417,7 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
       for (int c = 0; c < C::kBN; ++c) s[c] = fmaf(-2.0f * cout, rcp_approx(ex2(s[c] * kin) + 1.0f), cout);
     } else {
 #pragma unroll
-      for (int c = 0; c < C::kBN; ++c) s[c] *= p.scale_log2;
+      for (int c = 0; c < C::kBN; c += 2) fmul2(s[c], s[c + 1], s[c], s[c + 1], p.scale_log2, p.scale_log2);
     }
   }
   const float f = p.mask_natural ? p.inv_scale : kLog2e;  // additive mask factor

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -42,6 +43,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();  // defined in fa_api.cu
 void set_error(const char* fmt, ...);
+
+// One bit per device ordinal (0-63) recording that a per-kernel attribute has
+// been set there.  Atomic, so host threads may launch concurrently; two
+// threads racing on the first launch both set the (idempotent) attribute.
+inline bool device_bit_set(const std::atomic<unsigned long long>& bits, int dev) {
+  return dev >= 0 && dev < 64 && ((bits.load(std::memory_order_acquire) >> dev) & 1ull);
+}
+inline void device_bit_mark(std::atomic<unsigned long long>& bits, int dev) {
+  if (dev >= 0 && dev < 64) bits.fetch_or(1ull << dev, std::memory_order_release);
+}
 
 // A [B, H, rows, D] view with element strides {sb, sh, sr} and unit inner
 // stride, tiled as {chunk elements (128 bytes), box_rows, 1, 1} with 128-byte
@@ -158,11 +169,18 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.drop_offset = a.dropout_offset;
   p.window = a.window;
   p.q_offset = a.q_offset;
-  // An additive mask with a positive scale folds as s + mask / scale, so the
-  // scores stay in raw units and the softmax's own scale * log2(e) factor
-  // applies to both; otherwise scores go to base 2 before the mask.
-  p.mask_natural = (a.mask_kind == 2 && a.scale > 0.0f && !p.softcap_on) ? 1 : 0;
-  p.inv_scale = p.mask_natural ? 1.0f / a.scale : 0.0f;
+  // An additive mask with a positive scale may fold as s + mask / scale, so
+  // the scores stay in raw units and the softmax's own scale * log2(e) factor
+  // applies to both; otherwise scores go to base 2 before the mask.  The raw
+  // fold is taken only when 1 / scale is finite and no mask value of the
+  // type can overflow mask / scale (headroom 2^8 below the fp32 limit): in
+  // practice fp16 masks at any normal scale, never bf16 or fp32 masks, whose
+  // largest values (~2^128) would reach infinity.
+  const double mask_max = C::kTf32 ? 3.4028234663852886e38 : (C::kF16 ? 65504.0 : 3.3895313892515355e38);
+  const float inv_scale = a.scale > 0.0f ? 1.0f / a.scale : 0.0f;
+  const bool natural_ok = a.scale > 0.0f && std::isfinite(inv_scale) && mask_max * (double)inv_scale < 0x1p120;
+  p.mask_natural = (a.mask_kind == 2 && natural_ok && !p.softcap_on) ? 1 : 0;
+  p.inv_scale = p.mask_natural ? inv_scale : 0.0f;
   p.pre_scale = ((a.mask_kind == 2 && !p.mask_natural) || !(a.scale > 0.0f) || p.softcap_on) ? 1 : 0;
   p.mask_vec = a.mask_vec;
   p.mask_l2 = mask_l2;
@@ -181,10 +199,10 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.timeout_cycles = a.timeout_cycles;
 
   auto kern = fa_fwd_kernel<C>;
-  static int configured_device = -1;  // attribute set once per device (per instantiation)
+  static std::atomic<unsigned long long> configured{0};  // attributes set, per device (per instantiation)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured_device != dev) {
+  if (!device_bit_set(configured, dev)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) {
       set_error("cudaFuncSetAttribute(max dynamic smem = %u): %s", (unsigned)C::kSmemBytes, cudaGetErrorString(e));
@@ -202,7 +220,7 @@ int launch_fa_fwd(const LaunchArgs& a) {
         return 4;
       }
     }
-    configured_device = dev;
+    device_bit_mark(configured, dev);
   }
   // Persistent grid: one CTA per SM (or fewer when capped), each walking its
   // share of the (query block, batch, head) units.
