@@ -288,6 +288,15 @@ def attach_workspace(args, device, workspace=None):
     return workspace
 
 
+def _keep_until_stream_done(t, stream, device):
+    """Tell torch's caching allocator that ``t`` (allocated on the current
+    stream) is used by work queued on ``stream`` (a raw cudaStream_t), so its
+    memory is not handed out again before that work has run."""
+    import torch
+    if stream != torch.cuda.current_stream(device).cuda_stream:
+        t.record_stream(torch.cuda.ExternalStream(stream, device=device))
+
+
 def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, out=None, lse=None,
               stream=None, window=0, q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0,
               workspace=None):
@@ -305,6 +314,8 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
                      stream=stream, window=window, q_offset=q_offset, softcap=softcap, dropout_p=dropout_p,
                      dropout_seed=dropout_seed, dropout_offset=dropout_offset)
     ws = attach_workspace(args, q.device, workspace)
+    if ws is not None and workspace is None and stream is not None:
+        _keep_until_stream_done(ws, stream, q.device)
     _check(fa_fwd_ex(args))
     del ws  # torch hands the block out again only to work queued later on the same stream
     return out, lse
@@ -346,15 +357,25 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
         dk = torch.empty_like(k)
     if dv is None:
         dv = torch.empty_like(v)
+    # the kernels write every element of dq, dk and dv through raw pointers: a
+    # wrong size or layout would be written out of bounds
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if tuple(t.shape) != tuple(like.shape) or t.dtype != like.dtype:
+            raise ValueError(f"{name} must be {like.dtype} {tuple(like.shape)} (got {t.dtype} {tuple(t.shape)})")
+        if not t.is_cuda or t.device != q.device or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor on {q.device}")
     need = fa_bwd_ex_workspace_bytes(B, H_q, qL, kL, dropout_p)
     if need < 0:
         raise ValueError(f"dropout_p must lie in [0, 1] (got {dropout_p})")
-    if workspace is None:
+    own_workspace = workspace is None
+    if own_workspace:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace holds fewer than the {need} bytes required")
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif own_workspace:
+        _keep_until_stream_done(workspace, stream, q.device)
     _check(fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                      workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
