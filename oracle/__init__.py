@@ -126,13 +126,15 @@ def _mask_arg(mask, mask_kind, shape):
 
 def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
                   mask_kind: int = 0, n_threads: int | None = None, lib=None, window: int = 0, q_offset: int = 0,
-                  softcap: float = 0.0, dropout_p: float = 0.0, seed: int = 0, offset: int = 0):
+                  softcap: float = 0.0, dropout_p: float = 0.0, seed: int = 0, offset: int = 0, keep=None):
     """dQ, dK, dV of sum(O * dO) for O = softmax(scale * q k^T + mask) v, in fp64.
 
     Shapes and mask conventions as ``attention``; dO has the shape of q.
     window / q_offset / softcap: the forward's sliding window, causal diagonal offset and softcap.
     dropout_p / seed / offset: the forward's dropout; its multipliers come from the forward
     oracle's generator (``dropout_keep``) and enter the gradient oracle as an input.
+    keep: instead, the multipliers themselves ([B, H_q, qL, kL] fp64), e.g. those of a slice of
+    a larger problem, whose generator positions are not this call's.
     Returns (dQ [B,H_q,qL,D], dK [B,H_kv,kL,D], dV [B,H_kv,kL,D]).
     """
     lib = lib or load_bwd()
@@ -147,8 +149,11 @@ def attention_bwd(q, k, v, dO, scale: float, causal: bool = False, mask=None,
     dv = np.empty_like(v)
     if n_threads is None:
         n_threads = os.cpu_count() or 1
-    keep = None
-    if dropout_p > 0.0:
+    if keep is not None:
+        keep = _f64(keep)
+        if keep.shape != (B, Hq, qL, kL):
+            raise ValueError("keep must be [B, H_q, qL, kL]")
+    elif dropout_p > 0.0:
         keep = np.ascontiguousarray(dropout_keep(dropout_p, seed, offset, 0, B * Hq * qL * kL))
     kptr = None if keep is None else keep.ctypes.data
     rc = lib.oracle_attention_bwd_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, mptr, int(mask_kind),

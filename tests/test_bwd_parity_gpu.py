@@ -157,3 +157,58 @@ def test_bwd_dropout_seed_changes_gradients():
     for x, y, z in zip(a, b, c):
         assert torch.equal(x, y)
         assert not torch.equal(x, z)
+
+
+# The benchmarked backward at its full size (B2, H_q 32 / H_kv 8, L 4096, D 128, causal): the
+# multi-wave grid and the long per-CTA loops (each dK/dV CTA walks 4 heads x up to 32 query
+# blocks) are only exercised at this size.
+BENCH_BWD = W.WORKLOADS["bf16_gqa_causal_b2_hq32_hkv8_l4096_d128"]
+BENCH_BWD_DROPOUT = W.WORKLOADS["bf16_gqa_causal_dropout10_b2_hq32_hkv8_l4096_d128"]
+
+
+def _gpu_bwd_full(w):
+    import attention_forward_08_gb300 as fa
+    q, k, v = W.make_qkv(w)
+    do = W.make_dout(w)
+    dev = "cuda:0"
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    drop = dict(dropout_p=w.dropout_p, dropout_seed=w.dropout_seed, dropout_offset=w.dropout_offset)
+    o, lse = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal, **drop)
+    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, scale=w.sm_scale, causal=w.causal, **drop)
+    assert fa.fa_sync_status(None) == fa.fa.FA_OK, fa.fa_last_error()
+    return (q, k, v, do), (dq.cpu(), dk.cpu(), dv.cpu())
+
+
+def test_bwd_bench_workload_every_element():
+    """Every element of dQ, dK and dV of the benchmarked backward against the gradient oracle
+    (all 16 GQA groups, the oracle's threads one group each)."""
+    w = BENCH_BWD
+    (q, k, v, do), (dq, dk, dv) = _gpu_bwd_full(w)
+    rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                      do.double().numpy(), fp32_scale(w), causal=True)
+    _compare(f"{w.name} dQ", dq, rq)
+    _compare(f"{w.name} dK", dk, rk)
+    _compare(f"{w.name} dV", dv, rv)
+
+
+@pytest.mark.parametrize("b,kvh", [(0, 0), (1, 5)])
+def test_bwd_bench_dropout_workload_one_group(b, kvh):
+    """The benchmarked dropout backward (p 0.1, seed 2024) on one whole GQA group: dQ of its four
+    query heads and dK, dV of its K/V head, element by element.  The oracle runs on the group's
+    slice, with the generator's multipliers at the full problem's positions
+    ((b H_q + h) qL + i) kL + j."""
+    w = BENCH_BWD_DROPOUT
+    (q, k, v, do), (dq, dk, dv) = _gpu_bwd_full(w)
+    g = w.H_q // w.H_kv
+    heads = list(range(kvh * g, (kvh + 1) * g))
+    keep = np.stack([oracle.dropout_keep(float(np.float32(w.dropout_p)), w.dropout_seed, w.dropout_offset,
+                                         ((b * w.H_q + h) * w.qL) * w.kL, w.qL * w.kL).reshape(w.qL, w.kL)
+                     for h in heads])[None]
+    sl = lambda t: t[b:b + 1, heads].double().numpy()
+    rq, rk, rv = oracle.attention_bwd(sl(q), k[b:b + 1, kvh:kvh + 1].double().numpy(),
+                                      v[b:b + 1, kvh:kvh + 1].double().numpy(), sl(do), fp32_scale(w),
+                                      causal=True, keep=keep)
+    del keep
+    _compare(f"{w.name} b{b} kvh{kvh} dQ", dq[b:b + 1, heads], rq)
+    _compare(f"{w.name} b{b} kvh{kvh} dK", dk[b:b + 1, kvh:kvh + 1], rk)
+    _compare(f"{w.name} b{b} kvh{kvh} dV", dv[b:b + 1, kvh:kvh + 1], rv)

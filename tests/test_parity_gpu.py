@@ -187,6 +187,23 @@ def test_unusual_scales(scale, dtype, D):
                tol_mult_l=mult_l)
 
 
+@pytest.mark.parametrize("scale", [1e-39, 1e-6])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 64), ("f16", 256), ("bf16", 256)])
+def test_extreme_scale_additive_mask(scale, dtype, D):
+    """An additive mask of 0 and +-1e4 entries with a subnormal scale (1e-39: 1 / scale is not a
+    finite fp32) and a tiny normal one (1e-6: mask / scale = 1e10).  The mask decides the weights:
+    each row averages V over its keys of the largest mask value.  Mask values are not divided by
+    the scale where that could overflow, so no 0 * inf or inf - inf reaches the softmax."""
+    w = S(f"{dtype}_d{D}_tiny_scale_mask", 1, 2, 2, 200, 260, D, dtype, mask_kind=W.MASK_ADDITIVE, seed=98)
+    q, k, v = W.make_qkv(w)
+    g = torch.Generator().manual_seed(99)
+    u = torch.rand(1, 2, 200, 260, generator=g)
+    m = torch.zeros(1, 2, 200, 260)
+    m[u < 0.08] = 1e4
+    m[(u >= 0.08) & (u < 0.2)] = -1e4
+    _run_small(w, scale=scale, mask=m.to(w.torch_dtype), qkv=(q, k, v))
+
+
 @pytest.mark.parametrize("dtype,D", [("bf16", 64), ("bf16", 128), ("bf16", 256), ("f32", 128)])
 def test_rising_scores_rescale_every_block(dtype, D):
     """Keys drift along q so each KV block's max exceeds the last by ~12 (base 2): the running
@@ -246,15 +263,29 @@ def test_repeat_is_deterministic():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+# Full-size workloads whose fp64 oracle finishes in seconds (at most ~2e10 multiply-adds) are
+# compared on every row; the larger ones on sampled rows.
+def _oracle_cheap(w):
+    return 2.0 * w.B * w.H_q * w.qL * w.kL * w.D <= 2e10
+
+
 @pytest.mark.parametrize("name", list(W.WORKLOADS), ids=list(W.WORKLOADS))
 def test_full_workload_sampled_rows(name):
-    """Full-size workloads: every output finite where it should be, and sampled rows vs the oracle."""
+    """Full-size workloads: every output finite where it should be, and every row (cheap workloads:
+    C1, C2 and both D = 256 masked workloads, whose last Q tile holds 80 rows) or sampled rows vs
+    the oracle."""
     w = W.WORKLOADS[name]
     q, k, v, m = W.make_inputs(w)
     o_g, l_g, _ = gpu_run(w, q, k, v, m)
     # properties over every row
     assert np.all(np.isfinite(o_g)), "non-finite O"
     assert np.all(np.isfinite(l_g)), "every row of these workloads has an allowed key"
+    if _oracle_cheap(w):
+        qo, ko, vo, mo = oracle_inputs(q, k, v, m)
+        o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w), causal=w.causal, mask=mo,
+                                    mask_kind=w.mask_kind, **oracle_features(w))
+        compare(w, o_g, l_g, o_r, l_r, what=name + " (every row)")
+        return
     rows = sample_rows(w, n_per_head=3 if w.qL * w.kL > 4e6 else 8)
     qo, ko, vo, mo = oracle_inputs(q, k, v, m)
     o_r, l_r = oracle.attention(qo, ko, vo, fp32_scale(w), causal=w.causal, mask=mo,
