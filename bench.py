@@ -166,29 +166,86 @@ class CopyPipeline:
 
 
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+    """Samples the SM clock, power and clock-event (throttle) reasons of one GPU while running:
+    read-only NVML queries (libnvidia-ml through ctypes) every ``period`` seconds, or nvidia-smi
+    every 100 ms where NVML cannot be loaded.  Samples are tagged with the phase they fall in
+    (``mark(phase)``): the summary of a phase uses that phase's samples only."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, uuid: str | None = None, period: float = 0.001):
         self.gpu = gpu_index
-        self.samples = []
+        self.period = period
+        self.samples = []   # (phase, sm_mhz, max_mhz, power_w, [reasons])
+        self.phase = None
         self._stop = threading.Event()
         self._thread = None
-        self.window = [None, None]
+        self.source = "nvidia-smi"
+        self._nvml = self._open_nvml(gpu_index, uuid)
+
+    def _open_nvml(self, index, uuid):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            ok = False
+            if uuid:
+                for u in (uuid, "GPU-" + uuid):
+                    if lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0:
+                        ok = True
+                        break
+            if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                return None
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.source = "nvml"
+            return lib, h, reasons
+        except (OSError, AttributeError):
+            return None
+
+    def _sample_nvml(self):
+        import ctypes
+        lib, h, reasons_fn = self._nvml
+        sm, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) != 0:  # NVML_CLOCK_SM
+            return None
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+        reasons_fn(h, ctypes.byref(rs))
+        names = [n for n, bit in self.REASON_BITS.items() if rs.value & bit]
+        return float(sm.value), float(mx.value), mw.value / 1000.0, names
+
+    def _sample_smi(self):
+        out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=5).stdout.strip()
+        parts = [p.strip() for p in out.split(",")]
+        if len(parts) < 8:
+            return None
+        num = lambda x: float(x) if x.replace(".", "", 1).isdigit() else None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        return (num(parts[0]), num(parts[1]), num(parts[2]),
+                [names[i] for i in range(4) if parts[4 + i].lower() == "active"])
 
     def _run(self):
         while not self._stop.is_set():
             try:
-                out = subprocess.run(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
-                                     timeout=5).stdout.strip()
-                self.samples.append((time.time(), out))
+                smp = self._sample_nvml() if self._nvml else self._sample_smi()
+                if smp is not None and smp[0] is not None:
+                    self.samples.append((self.phase, *smp))
             except Exception:
                 pass
-            self._stop.wait(0.1)
+            self._stop.wait(self.period if self._nvml else 0.1)
+
+    def mark(self, phase):
+        self.phase = phase
 
     def start(self):
         self._thread = threading.Thread(target=self._run, daemon=True)
@@ -198,30 +255,66 @@ class ClockSampler:
         self._stop.set()
         if self._thread:
             self._thread.join(timeout=10)
+        if self._nvml:
+            self._nvml[0].nvmlShutdown()
 
-    def summary(self):
-        t0, t1 = self.window
-        rows = []
-        for ts, line in self.samples:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            rows.append((ts, parts))
-        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1] or rows
+    def summary(self, phase="timed"):
+        """Median SM clock, max clock and active reasons over the samples of ``phase`` only (never
+        idle time: a phase without samples reports none)."""
+        inside = [smp for smp in self.samples if smp[0] == phase]
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        sm = [x[1] for x in inside]
+        mx = [x[2] for x in inside if x[2]]
+        pw = [x[3] for x in inside if x[3] is not None]
+        reasons = sorted({r for x in inside for r in x[4]})
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(inside),
+                "source": self.source}
 
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(p[0]) for _, p in inside if num(p[0]) is not None]
-        mx = [num(p[1]) for _, p in inside if num(p[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, p in inside for i in range(4) if p[4 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(inside)}
+
+def make_sampler(dev):
+    """A ClockSampler for torch device ``dev`` (matched to NVML by UUID where torch reports it)."""
+    import torch
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+    index = int(vis) if vis.isdigit() else dev.index
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    return ClockSampler(index, uuid)
+
+
+SOAK_SECONDS = 1.0  # back-to-back steps, sampled, right before the timed steps
+
+
+def soak(step_fn, sampler, dev):
+    """Run ``step_fn`` back to back for about SOAK_SECONDS (untimed), so the clock record covers the
+    kernel at a sustained load, not only the few milliseconds of the timed steps."""
+    import torch
+    sampler.mark("soak")
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < SOAK_SECONDS:
+        for _ in range(8):
+            step_fn()
+        n += 8
+        torch.cuda.synchronize(dev)
+    sampler.mark(None)
+    return n
+
+
+def clocks_record(sampler):
+    """The line's ``clocks``: the timed steps' own samples, plus the soak's beside them."""
+    timed, soaked = sampler.summary("timed"), sampler.summary("soak")
+    rec = {k: timed[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}
+    rec.update({"sm_min_mhz": timed.get("sm_min_mhz"), "power_w_max": timed.get("power_w_max"),
+                "source": timed["source"], "window": "timed steps only",
+                "soak": {k: soaked.get(k) for k in ("sm_mhz", "sm_min_mhz", "sm_max_mhz", "power_w_max", "reasons",
+                                                    "samples")}})
+    rec["soak"]["seconds"] = SOAK_SECONDS
+    return rec
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
@@ -408,15 +501,18 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     assert fa.fa_sync_status(None) == 0, fa.fa_last_error()
 
-    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[0])
-                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else dev.index)
+    sampler = make_sampler(dev)
     sampler.start()
-    time.sleep(0.3)
+
+    def soak_step():
+        flush.fill_(1)
+        launch()
+    soak(soak_step, sampler, dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    sampler.window[0] = time.time()
+    sampler.mark("timed")
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
@@ -426,8 +522,7 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - t_wall
-    sampler.window[1] = time.time()
-    time.sleep(0.2)
+    sampler.mark(None)
     sampler.stop()
     rc = fa.fa_sync_status(None)
     assert rc == 0, fa.fa_last_error()
@@ -474,7 +569,7 @@ def run_ours(args, w):
     peak = peak_for(w, peaks)
     achieved = flops / (mean_ms * 1e-3) / 1e12
     traffic = traffic_from_profiles(w)
-    clocks = sampler.summary()
+    clocks = clocks_record(sampler)
 
     line = {
         "metric": "attention fwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -492,8 +587,7 @@ def run_ours(args, w):
                      "hbm_gbs": algorithmic_bytes(w) / (mean_ms * 1e-3) / 1e9},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
-                   "samples": clocks["samples"]},
+        "clocks": clocks,
         "gpu_launches": launches_per_call * args.steps,
         "timed_region_s": wall,
         "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)},
@@ -585,14 +679,18 @@ def run_ours_bwd(args, w):
         launch()
     torch.cuda.synchronize(dev)
     assert fa.fa_sync_status(None) == 0, fa.fa_last_error()
-    sampler = ClockSampler(dev.index)
+    sampler = make_sampler(dev)
     sampler.start()
-    time.sleep(0.3)
+
+    def soak_step():
+        flush.fill_(1)
+        launch()
+    soak(soak_step, sampler, dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    sampler.window[0] = time.time()
+    sampler.mark("timed")
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
@@ -602,8 +700,7 @@ def run_ours_bwd(args, w):
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - t_wall
-    sampler.window[1] = time.time()
-    time.sleep(0.2)
+    sampler.mark(None)
     sampler.stop()
     assert fa.fa_sync_status(None) == 0, fa.fa_last_error()
     call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -637,7 +734,7 @@ def run_ours_bwd(args, w):
 
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"]
-    clocks = sampler.summary()
+    clocks = clocks_record(sampler)
     line = {
         "metric": "attention bwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
@@ -651,8 +748,7 @@ def run_ours_bwd(args, w):
                                 + "dK/dV + dQ"},
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
-                   "samples": clocks["samples"]},
+        "clocks": clocks,
         "gpu_launches": (4 if w.dropout_p else 3) * args.steps,
         "timed_region_s": wall,
         "call_ms": {"min": min(call_ms), "median": statistics.median(call_ms), "max": max(call_ms)},

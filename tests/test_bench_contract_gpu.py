@@ -33,3 +33,7 @@ def test_default_bench_line_has_the_contract_keys():
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0
     assert line["gpu_launches"] >= line["steps"]
     assert set(line["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    # the clock record covers the timed steps themselves (and, beside them, a sustained soak)
+    clk = line["clocks"]
+    assert clk["window"] == "timed steps only" and clk["samples"] >= 1, clk
+    assert clk["sm_mhz"] is not None and clk["soak"]["samples"] >= 1, clk
