@@ -589,9 +589,11 @@ __device__ __forceinline__ void p_pass_dropout(const float (&s)[C::kBN], float s
   sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
 }
 
-// One work unit: kNQT consecutive 128-row Q tiles of one (batch, head).
+// One work unit: kNQT 128-row Q tiles of one batch: consecutive row tiles of one
+// head, or (head pairs) the same rows of two heads that share a K/V head.
 struct Unit {
   int b, h, kvh, q0, N;
+  int th[2], tr[2];  // head and first row of Q tile t
   int j0;       // first KV tile of the unit (the tiles share one K/V stream from j0 to N)
   int nblk[2];  // one past each Q tile's last KV tile (0: the tile has no rows)
 };
@@ -607,23 +609,31 @@ __device__ __forceinline__ int unit_j0(const Unit& w) {
 
 template <class C>
 __device__ __forceinline__ Unit decode_unit(const FaParams& p, int u) {
-  // Heavy causal query blocks first; consecutive units are consecutive heads,
-  // so the H_q / H_kv heads sharing a K/V head run side by side (L2 reuse).
+  // Heavy causal query blocks first; consecutive units are consecutive heads
+  // (or head pairs), so the H_q / H_kv heads sharing a K/V head run side by
+  // side (L2 reuse).  With head pairs both tiles cover the same rows, so they
+  // visit the same K/V blocks and finish together (a causal row pair would
+  // leave the second tile one block alone at the end of every unit).
   Unit w;
-  const int per_q = p.B * p.Hq;
+  const int per_q = p.B * p.hq_units;
   const int qb_rev = u / per_q;
   const int rem = u - qb_rev * per_q;
   const int qb = p.causal ? (p.n_qblocks - 1 - qb_rev) : qb_rev;
-  w.b = rem / p.Hq;
-  w.h = rem - w.b * p.Hq;
+  w.b = rem / p.hq_units;
+  const int hu = rem - w.b * p.hq_units;
+  w.h = p.head_pairs ? 2 * hu : hu;
   w.kvh = w.h / p.group;
-  w.q0 = qb * (C::kBM * C::kNQT);
-  w.nblk[0] = tile_kv_blocks<C>(p, w.q0);
-  w.nblk[1] = (C::kNQT == 2) ? tile_kv_blocks<C>(p, w.q0 + C::kBM) : 0;
+  w.q0 = qb * (p.head_pairs ? C::kBM : C::kBM * C::kNQT);
+  w.th[0] = w.h;
+  w.th[1] = p.head_pairs ? w.h + 1 : w.h;
+  w.tr[0] = w.q0;
+  w.tr[1] = p.head_pairs ? w.q0 : w.q0 + C::kBM;
+  w.nblk[0] = tile_kv_blocks<C>(p, w.tr[0]);
+  w.nblk[1] = (C::kNQT == 2) ? tile_kv_blocks<C>(p, w.tr[1]) : 0;
   w.N = max(w.nblk[0], w.nblk[1]);
-  // Tile 0's rows come first, so its window starts first; tile 1 masks the
-  // (at most one) leading block it cannot see.
-  w.j0 = tile_kv_begin<C>(p, w.q0, w.nblk[0]);
+  // Tile 0's rows come first (or equal), so its window starts first; tile 1
+  // masks the (at most one) leading block it cannot see.
+  w.j0 = tile_kv_begin<C>(p, w.tr[0], w.nblk[0]);
   return w;
 }
 
@@ -713,7 +723,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_units = p.n_qblocks * p.B * p.Hq;
+  const int num_units = p.n_qblocks * p.B * p.hq_units;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -784,7 +794,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::kNChunk; ++c)
             tma_load_4d(sQ + t * C::kQTileBytes + c * (C::kBM * 128), &tmQ, &ctl->q_full[t], c * C::kChunk,
-                        w.q0 + t * C::kBM, w.h, w.b);
+                        t == 0 ? w.tr[0] : w.tr[1], t == 0 ? w.th[0] : w.th[1], w.b);
           ++q_issued[t];
         }
         // Mask tiles reach L2 two blocks ahead of their use (read by the
@@ -794,9 +804,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const bool pf_mask = p.mask_l2 || p.mask_smem;
         auto prefetch_mask = [&](const Unit& uu, int j) {
           const int mesz = p.mask_kind == 1 ? 1 : C::kEsz;
+#pragma unroll
           for (int t = 0; t < C::kNQT; ++t)
             for (int c = 0; c < (C::kBN * mesz) / 128; ++c)
-              tma_prefetch_l2_4d(&tmM, j * C::kBN + c * (128 / mesz), uu.q0 + t * C::kBM, uu.h, uu.b);
+              tma_prefetch_l2_4d(&tmM, j * C::kBN + c * (128 / mesz), t == 0 ? uu.tr[0] : uu.tr[1],
+                                 t == 0 ? uu.th[0] : uu.th[1], uu.b);
         };
         const int u_next = unit_of(r + 1, num_units);
         const Unit w_next = decode_unit<C>(p, u_next < 0 ? u : u_next);
@@ -830,7 +842,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const int boxes = (C::kBN * mesz) / 128;  // 128-byte column blocks
             mbar_arrive_expect_tx(&ctl->m_full, (uint32_t)(C::kBM * C::kBN * mesz));
             for (int c = 0; c < boxes; ++c)
-              tma_load_4d(sM + c * (C::kBM * 128), &tmM, &ctl->m_full, j * C::kBN + c * (128 / mesz), w.q0, w.h, w.b);
+              tma_load_4d(sM + c * (C::kBM * 128), &tmM, &ctl->m_full, j * C::kBN + c * (128 / mesz), w.tr[0], w.th[0],
+                          w.b);
             ++m_issued;
           }
           }
@@ -1114,8 +1127,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const Unit w = decode_unit<C>(p, u);
       const int nb = t == 0 ? w.nblk[0] : w.nblk[1];
       if (nb == 0) continue;
-      const int b = w.b, h = w.h;
-      const int r0 = w.q0 + t * C::kBM;
+      const int b = w.b, h = t == 0 ? w.th[0] : w.th[1];
+      const int r0 = t == 0 ? w.tr[0] : w.tr[1];
       const int row = r0 + tl;
       float m_run = -INFINITY;  // running max, base 2 (scaled)
       float l_run = 0.0f;       // running sum of 2^(s - m_run)

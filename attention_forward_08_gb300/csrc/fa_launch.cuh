@@ -155,7 +155,16 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.qL = a.qL;
   p.kL = a.kL;
   p.group = a.Hq / a.Hkv;
-  p.n_qblocks = (a.qL + C::kBM * C::kNQT - 1) / (C::kBM * C::kNQT);
+  // Two Q tiles per unit: two consecutive row tiles of one head, or, with a
+  // sliding window or dropout, two heads of one K/V head at the same 128 rows
+  // when the query heads per K/V head come in pairs (both tiles then see the
+  // same key blocks: measured 154 -> 136 us with a 1024-key window and 779 ->
+  // 730 us with dropout 0.1 on the causal B2 H32/8 L4096 D128 workload; the
+  // plain causal forward runs 1-2% faster with row pairs).
+  p.head_pairs = (C::kNQT == 2 && (a.Hq / a.Hkv) % 2 == 0 && (a.window > 0 || a.dropout_p > 0.0f)) ? 1 : 0;
+  p.hq_units = p.head_pairs ? a.Hq / 2 : a.Hq;
+  const int unit_rows = p.head_pairs ? C::kBM : C::kBM * C::kNQT;
+  p.n_qblocks = (a.qL + unit_rows - 1) / unit_rows;
   p.causal = a.causal;
   p.mask_kind = a.mask_kind;
   p.softcap_on = a.softcap > 0.0f ? 1 : 0;
@@ -224,7 +233,7 @@ int launch_fa_fwd(const LaunchArgs& a) {
   }
   // Persistent grid: one CTA per SM (or fewer when capped), each walking its
   // share of the (query block, batch, head) units.
-  const long long units = (long long)p.n_qblocks * a.B * a.Hq;
+  const long long units = (long long)p.n_qblocks * a.B * p.hq_units;
   if (units <= 0 || units > 0x7fffffffLL) {
     set_error("%lld work units are out of range", units);
     return 2;

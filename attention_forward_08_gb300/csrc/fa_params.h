@@ -14,7 +14,9 @@ enum : unsigned int {
 struct FaParams {
   int B, Hq, Hkv, qL, kL;
   int group;        // Hq / Hkv: query heads per K/V head
-  int n_qblocks;    // query blocks of (tiles per CTA * 128) rows per (b, h)
+  int n_qblocks;    // query blocks per (b, head unit): 128 rows with head pairs, else tiles per CTA * 128
+  int head_pairs;   // two Q tiles per unit are heads 2u and 2u + 1 (one K/V head) at the same rows
+  int hq_units;     // head units per batch: H_q / 2 with head pairs, else H_q
   int causal;       // top-left aligned: key j allowed for row i iff j <= i
   int mask_kind;    // 0 none, 1 bool (uint8, nonzero keeps), 2 additive (I/O dtype)
   int pre_scale;    // scale scores before masking (additive mask, softcap, or scale <= 0)

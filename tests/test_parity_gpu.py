@@ -324,6 +324,10 @@ PERSISTENT = [
     S("f32_d64_causal_units", 1, 3, 1, 300, 300, 64, "f32", causal=True),
     S("f32_d128_tokenmajor_units", 1, 3, 3, 260, 260, 128, "f32", layout="dit"),
     S("f32_d256_additive_units", 1, 2, 2, 170, 200, 256, "f32", mask_kind=W.MASK_ADDITIVE),
+    # two heads of one K/V head per unit (sliding window / dropout with an even GQA group)
+    S("swa_bf16_d64_gqa4_head_pairs_units", 2, 8, 2, 520, 520, 64, "bf16", causal=True, window=150, seed=77),
+    S("drop_f16_d128_gqa2_head_pairs_units", 1, 4, 2, 300, 300, 128, "f16", causal=True, dropout_p=0.2,
+      dropout_seed=4, seed=78),
 ]
 
 
