@@ -286,7 +286,8 @@ def make_sampler(dev):
     return ClockSampler(index, uuid)
 
 
-SOAK_SECONDS = 1.0  # back-to-back steps, sampled, right before the timed steps
+SOAK_SECONDS = 1.0  # back-to-back steps, sampled, right before the timed steps (--soak-seconds)
+SOAK = {"seconds": SOAK_SECONDS}
 
 
 def soak(step_fn, sampler, dev):
@@ -296,7 +297,7 @@ def soak(step_fn, sampler, dev):
     sampler.mark("soak")
     t0 = time.perf_counter()
     n = 0
-    while time.perf_counter() - t0 < SOAK_SECONDS:
+    while n == 0 or time.perf_counter() - t0 < SOAK["seconds"]:
         for _ in range(8):
             step_fn()
         n += 8
@@ -313,7 +314,7 @@ def clocks_record(sampler):
                 "source": timed["source"], "window": "timed steps only",
                 "soak": {k: soaked.get(k) for k in ("sm_mhz", "sm_min_mhz", "sm_max_mhz", "power_w_max", "reasons",
                                                     "samples")}})
-    rec["soak"]["seconds"] = SOAK_SECONDS
+    rec["soak"]["seconds"] = SOAK["seconds"]
     return rec
 
 
@@ -775,10 +776,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
+    ap.add_argument("--soak-seconds", type=float, default=SOAK_SECONDS,
+                    help="sampled back-to-back steps before the timed ones (0: one batch of 8, e.g. under ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = workloads.WORKLOADS[args.workload]
+    SOAK.update(seconds=max(0.0, args.soak_seconds))
     if args.impl == "reference":
         return run_reference(args, w)
     if args.pass_ == "bwd":
