@@ -245,61 +245,78 @@ EncodeTiledFn get_encode_tiled() {
   return g_encode;
 }
 
-int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                 const void* dq, const void* dk, const void* dv, int B, int H_q, int H_kv, int qL, int kL, int D,
-                 float scale, int window, int q_offset, float softcap, float dropout_p, int dtype) {
-  if (!(dropout_p >= 0.0f && dropout_p <= 1.0f)) {
+int validate_bwd(const fa_bwd_args* a) {
+  if (!(a->dropout_p >= 0.0f && a->dropout_p <= 1.0f)) {
     set_error("dropout_p must lie in [0, 1]");
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (dropout_p > 0.0f && kL % 4 != 0) {
-    set_error("dropout needs kL (%d) to be a multiple of 4", kL);
+  if (a->dropout_p > 0.0f && a->kL % 4 != 0) {
+    set_error("dropout needs kL (%d) to be a multiple of 4", a->kL);
     return FA_ERR_UNSUPPORTED;
   }
-  if (!(std::isfinite(softcap) && softcap >= 0.0f)) {
+  if (!(std::isfinite(a->softcap) && a->softcap >= 0.0f)) {
     set_error("softcap must be finite and >= 0 (0 = off)");
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (window < 0) {
-    set_error("window (%d) must be >= 0 (0 = no sliding window)", window);
+  if (a->window < 0) {
+    set_error("window (%d) must be >= 0 (0 = no sliding window)", a->window);
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (q_offset <= -(1 << 30) || q_offset >= (1 << 30)) {
-    set_error("|q_offset| (%d) must be < 2^30", q_offset);
+  if (a->q_offset <= -(1 << 30) || a->q_offset >= (1 << 30)) {
+    set_error("|q_offset| (%d) must be < 2^30", a->q_offset);
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) {
+  if (!a->q || !a->k || !a->v || !a->o || !a->dout || !a->lse || !a->dq || !a->dk || !a->dv) {
     set_error("q, k, v, o, dout, lse, dq, dk and dv must all be non-NULL");
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (B <= 0 || H_q <= 0 || H_kv <= 0 || qL <= 0 || kL <= 0) {
-    set_error("B (%d), H_q (%d), H_kv (%d), qL (%d) and kL (%d) must be > 0", B, H_q, H_kv, qL, kL);
+  if (a->B <= 0 || a->H_q <= 0 || a->H_kv <= 0 || a->qL <= 0 || a->kL <= 0) {
+    set_error("B (%d), H_q (%d), H_kv (%d), qL (%d) and kL (%d) must be > 0", a->B, a->H_q, a->H_kv, a->qL, a->kL);
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (H_q % H_kv != 0) {
-    set_error("H_q (%d) must be divisible by H_kv (%d)", H_q, H_kv);
+  if (a->H_q % a->H_kv != 0) {
+    set_error("H_q (%d) must be divisible by H_kv (%d)", a->H_q, a->H_kv);
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (!std::isfinite(scale)) {
+  if (!std::isfinite(a->scale)) {
     set_error("scale must be finite");
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) {
-    const bool known = dtype == FA_DTYPE_F32;
+  if (a->mask_kind < FA_MASK_NONE || a->mask_kind > FA_MASK_ADDITIVE) {
+    set_error("mask_kind %d is not 0 (none), 1 (bool) or 2 (additive)", a->mask_kind);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if ((a->mask_kind != FA_MASK_NONE) != (a->mask != nullptr)) {
+    set_error("mask must be non-NULL exactly when mask_kind != 0 (mask_kind %d, mask %p)", a->mask_kind, a->mask);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->mask_kind != FA_MASK_NONE) {
+    for (int i = 0; i < 3; ++i)
+      if (a->mask_strides[i] < 0) {
+        set_error("mask strides must be >= 0");
+        return FA_ERR_INVALID_ARGUMENT;
+      }
+  }
+  if (a->dtype != FA_DTYPE_BF16 && a->dtype != FA_DTYPE_F16) {
+    const bool known = a->dtype == FA_DTYPE_F32;
     set_error(known ? "the backward pass supports bf16 and fp16 I/O only"
                     : "dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)",
-              dtype);
+              a->dtype);
     return known ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
   }
-  if (D != 64 && D != 128) {
-    set_error("head dim D = %d is not supported by the backward pass (64 or 128)", D);
+  if (a->D != 64 && a->D != 128) {
+    set_error("head dim D = %d is not supported by the backward pass (64 or 128)", a->D);
     return FA_ERR_UNSUPPORTED;
   }
-  if (rows_exceed(B, H_q, qL, 0x7fffffffLL) || rows_exceed(B, H_kv, kL, 0x7fffffffLL)) {
+  if (a->mask_kind != FA_MASK_NONE && a->softcap != 0.0f) {
+    set_error("the backward pass does not combine a mask with a softcap");
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (rows_exceed(a->B, a->H_q, a->qL, 0x7fffffffLL) || rows_exceed(a->B, a->H_kv, a->kL, 0x7fffffffLL)) {
     set_error("row counts exceed 2^31 - 1");
     return FA_ERR_UNSUPPORTED;
   }
-  const void* ptrs[9] = {q, k, v, o, dout, dq, dk, dv, lse};
+  const void* ptrs[9] = {a->q, a->k, a->v, a->o, a->dout, a->dq, a->dk, a->dv, a->lse};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) {
       set_error("q, k, v, o, dout, lse, dq, dk, dv and workspace must be 16-byte aligned");
@@ -551,6 +568,13 @@ long long fa_bwd_workspace_bytes(int B, int H_q, int qL) {
   return (bytes + 255) / 256 * 256;
 }
 
+namespace {
+// Queries per key row of the backward's key-major mask copy: whole 128-row
+// query blocks, so a block's 128 entries never leave the row.
+long long mask_t_ld(int qL) { return ((long long)qL + 127) / 128 * 128; }
+long long align256_ll(long long bytes) { return (bytes + 255) / 256 * 256; }
+}  // namespace
+
 long long fa_bwd_ex_workspace_bytes(int B, int H_q, int qL, int kL, float dropout_p) {
   const long long dvec = fa_bwd_workspace_bytes(B, H_q, qL);
   if (dvec < 0 || kL <= 0 || !(dropout_p >= 0.0f && dropout_p <= 1.0f)) return -1;
@@ -559,27 +583,41 @@ long long fa_bwd_ex_workspace_bytes(int B, int H_q, int qL, int kL, float dropou
   return dvec + (long long)B * H_q * qL * fa::keep_row_words(kL) * 4;
 }
 
-int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-              void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
-              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap,
-              float dropout_p, unsigned long long dropout_seed, unsigned long long dropout_offset, int dtype,
-              void* stream) {
+long long fa_bwd_full_workspace_bytes(const fa_bwd_args* a) {
   using namespace fa;
   g_err[0] = '\0';
-  int rc = validate_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, window, q_offset,
-                        softcap, dropout_p, dtype);
+  if (!a) {
+    set_error("args is NULL");
+    return -1;
+  }
+  if (validate_bwd(a) != FA_OK) return -1;
+  const long long base = fa_bwd_ex_workspace_bytes(a->B, a->H_q, a->qL, a->kL, a->dropout_p);
+  if (a->mask_kind == FA_MASK_NONE) return base;
+  const int esz = a->mask_kind == FA_MASK_BOOL ? 1 : 2;
+  return align256_ll(base) + align256_ll((long long)a->B * a->H_q * a->kL * mask_t_ld(a->qL) * esz);
+}
+
+int fa_bwd_full(const fa_bwd_args* args) {
+  using namespace fa;
+  g_err[0] = '\0';
+  if (!args) {
+    set_error("args is NULL");
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  const fa_bwd_args& x = *args;
+  int rc = validate_bwd(&x);
   if (rc != FA_OK) return rc;
-  if (!workspace) {
+  if (!x.workspace) {
     set_error("workspace must be non-NULL");
     return FA_ERR_INVALID_ARGUMENT;
   }
-  const long long ws_need = fa_bwd_ex_workspace_bytes(B, H_q, qL, kL, dropout_p);
-  if (workspace_bytes < ws_need) {
-    set_error("workspace of %lld bytes is smaller than the %lld required", workspace_bytes, ws_need);
+  const long long ws_need = fa_bwd_full_workspace_bytes(&x);
+  if (x.workspace_bytes < ws_need) {
+    set_error("workspace of %lld bytes is smaller than the %lld required", x.workspace_bytes, ws_need);
     return FA_ERR_INVALID_ARGUMENT;
   }
-  if (!aligned16(workspace)) {
-    set_error("workspace must be 16-byte aligned");
+  if (!aligned16(x.workspace) || (x.mask_kind != FA_MASK_NONE && (reinterpret_cast<uintptr_t>(x.workspace) & 255u))) {
+    set_error(x.mask_kind != FA_MASK_NONE ? "workspace must be 256-byte aligned" : "workspace must be 16-byte aligned");
     return FA_ERR_MISALIGNED;
   }
   int dev = 0;
@@ -591,6 +629,61 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   rc = device_setup(dev);
   if (rc != FA_OK) return rc;
   BwdLaunchArgs a;
+  a.q = x.q;
+  a.k = x.k;
+  a.v = x.v;
+  a.o = x.o;
+  a.dout = x.dout;
+  a.lse = x.lse;
+  a.dq = x.dq;
+  a.dk = x.dk;
+  a.dv = x.dv;
+  a.dvec = static_cast<float*>(x.workspace);
+  a.f16 = x.dtype == FA_DTYPE_F16;
+  a.B = x.B;
+  a.Hq = x.H_q;
+  a.Hkv = x.H_kv;
+  a.qL = x.qL;
+  a.kL = x.kL;
+  a.D = x.D;
+  a.scale = x.scale;
+  a.causal = x.causal ? 1 : 0;
+  a.window = x.window;
+  a.q_offset = x.q_offset;
+  a.softcap = x.softcap;
+  a.dropout_p = x.dropout_p;
+  a.dropout_seed = x.dropout_seed;
+  a.dropout_offset = x.dropout_offset;
+  a.keep_row_words = keep_row_words(x.kL);
+  const long long base = fa_bwd_ex_workspace_bytes(x.B, x.H_q, x.qL, x.kL, x.dropout_p);
+  a.keep_mask = x.dropout_p > 0.0f ? reinterpret_cast<uint32_t*>(static_cast<char*>(x.workspace) +
+                                                                 fa_bwd_workspace_bytes(x.B, x.H_q, x.qL))
+                                   : nullptr;
+  a.mask_kind = x.mask_kind;
+  a.mask = x.mask;
+  for (int i = 0; i < 3; ++i) a.ms[i] = x.mask_kind ? x.mask_strides[i] : 0;
+  a.mask_t = x.mask_kind ? static_cast<char*>(x.workspace) + align256_ll(base) : nullptr;
+  a.mask_t_ld = mask_t_ld(x.qL);
+  a.mask_vec = 0;
+  if (x.mask_kind != FA_MASK_NONE) {
+    const int mesz = x.mask_kind == FA_MASK_BOOL ? 1 : 2;
+    bool vec = aligned16(x.mask);
+    for (int i = 0; i < 3; ++i) vec = vec && ((a.ms[i] * mesz) % 16 == 0);
+    a.mask_vec = vec ? 1 : 0;
+  }
+  a.stream = static_cast<cudaStream_t>(x.stream);
+  a.status = g_status_ptr[dev];
+  a.timeout_cycles = timeout_cycles();
+  return launch_bwd(a);
+}
+
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+              void* dq, void* dk, void* dv, void* workspace, long long workspace_bytes, int B, int H_q, int H_kv,
+              int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap,
+              float dropout_p, unsigned long long dropout_seed, unsigned long long dropout_offset, int dtype,
+              void* stream) {
+  fa_bwd_args a;
+  std::memset(&a, 0, sizeof(a));
   a.q = q;
   a.k = k;
   a.v = v;
@@ -600,30 +693,25 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.dvec = static_cast<float*>(workspace);
-  a.f16 = dtype == FA_DTYPE_F16;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   a.B = B;
-  a.Hq = H_q;
-  a.Hkv = H_kv;
+  a.H_q = H_q;
+  a.H_kv = H_kv;
   a.qL = qL;
   a.kL = kL;
   a.D = D;
   a.scale = scale;
-  a.causal = causal ? 1 : 0;
+  a.causal = causal;
   a.window = window;
   a.q_offset = q_offset;
   a.softcap = softcap;
   a.dropout_p = dropout_p;
   a.dropout_seed = dropout_seed;
   a.dropout_offset = dropout_offset;
-  a.keep_row_words = keep_row_words(kL);
-  a.keep_mask = dropout_p > 0.0f ? reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) +
-                                                               fa_bwd_workspace_bytes(B, H_q, qL))
-                                 : nullptr;
-  a.stream = static_cast<cudaStream_t>(stream);
-  a.status = g_status_ptr[dev];
-  a.timeout_cycles = timeout_cycles();
-  return launch_bwd(a);
+  a.dtype = dtype;
+  a.stream = stream;
+  return fa_bwd_full(&a);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
@@ -633,6 +721,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
                    causal, 0, 0, 0.0f, 0.0f, 0ull, 0ull, dtype, stream);
 }
 
-int fa_version(void) { return 108; }
+int fa_version(void) { return 109; }
 
 }  // extern "C"

@@ -1,160 +1,20 @@
-// fa_bwd.cu -- launcher for the backward pass: tensor maps, grids, the three
-// launches (D pre-pass, dK/dV, dQ) for head dims 64 and 128, bf16 or fp16 I/O,
-// with or without sliding window / causal diagonal offset / softcap, and
-// with dropout.
-#include <cuda.h>
-#include <cuda_runtime.h>
-
-#include <algorithm>
-#include <atomic>
-#include <cmath>
-
-#include "fa_bwd_kernel.cuh"
-#include "fa_bwd_launch.h"
-#include "fa_launch.cuh"
+// fa_bwd.cu -- the backward pass's dispatcher (launch_bwd) and the plain
+// plans: head dims 64 and 128, bf16 or fp16 I/O, no window, offset, softcap,
+// dropout or mask.  The other plans live in fa_bwd_feat.cu, fa_bwd_drop.cu and
+// fa_bwd_mask.cu (separate translation units, compiled in parallel).
+#include "fa_bwd_impl.cuh"
 
 namespace fa {
 
-namespace {
-
-template <class C>
-int set_smem_once(const void* kern, uint32_t bytes, std::atomic<unsigned long long>& configured) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (device_bit_set(configured, dev)) return 0;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) {
-    set_error("cudaFuncSetAttribute(max dynamic smem = %u): %s", (unsigned)bytes, cudaGetErrorString(e));
-    return 4;
-  }
-  device_bit_mark(configured, dev);
-  return 0;
-}
-
-template <int kD, bool kF16, bool kFeat, bool kDrop = false>
-int launch_bwd_d(const BwdLaunchArgs& a) {
-  using C = BwdCfg<kD, kF16, kFeat, kDrop>;
-  // 1. D_i = rowsum(O_i * dO_i)
-  const long long rows = (long long)a.B * a.Hq * a.qL;
-  constexpr int kRowsPerBlock = 256 / (kD / 8);
-  const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-  fa_bwd_rowdot_kernel<kD, kF16><<<(unsigned)blocks, 256, 0, a.stream>>>(
-      static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.dvec, rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    set_error("row-dot launch failed: %s", cudaGetErrorString(e));
-    return 4;
-  }
-
-  // 2. Tensor maps: 128-row tiles of 128-byte swizzled column blocks.
-  const long long qst[3] = {(long long)a.Hq * a.qL * kD, (long long)a.qL * kD, kD};
-  const long long kst[3] = {(long long)a.Hkv * a.kL * kD, (long long)a.kL * kD, kD};
-  CUtensorMap tq, tk, tv, tdo;
-  if (!encode_bhsd(&tq, C::kTmaType, a.q, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tdo, C::kTmaType, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tk, C::kTmaType, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
-  if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
-
-  BwdParams p;
-  p.B = a.B;
-  p.Hq = a.Hq;
-  p.Hkv = a.Hkv;
-  p.qL = a.qL;
-  p.kL = a.kL;
-  p.group = a.Hq / a.Hkv;
-  p.causal = a.causal;
-  p.window = a.window;
-  p.q_offset = a.q_offset;
-  p.softcap_on = a.softcap > 0.0f ? 1 : 0;
-  p.softcap_kin = p.softcap_on ? 2.0f * kLog2e * (a.scale / a.softcap) : 0.0f;
-  p.softcap_out = p.softcap_on ? a.softcap * kLog2e : 0.0f;
-  p.softcap_inv = p.softcap_on ? 1.0f / p.softcap_out : 0.0f;
-  p.dropout_on = kDrop ? 1 : 0;
-  p.drop_threshold = kDrop ? (unsigned int)std::ceil((double)a.dropout_p * 16777216.0) : 0u;
-  p.drop_scale = kDrop && a.dropout_p < 1.0f ? (float)(1.0 / (1.0 - (double)a.dropout_p)) : 0.0f;
-  p.seed_lo = (unsigned int)a.dropout_seed;
-  p.seed_hi = (unsigned int)(a.dropout_seed >> 32);
-  p.drop_offset = a.dropout_offset;
-  p.keep_mask = a.keep_mask;
-  p.keep_row_words = a.keep_row_words;
-  p.n_qt = (a.qL + C::kTile - 1) / C::kTile;
-  p.n_kt = (a.kL + C::kTile - 1) / C::kTile;
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * kLog2e;
-  p.lse = a.lse;
-  p.dvec = a.dvec;
-  p.dq = a.dq;
-  p.dk = a.dk;
-  p.dv = a.dv;
-  p.status = a.status;
-  p.timeout_cycles = a.timeout_cycles;
-
-  static std::atomic<unsigned long long> cfg_kv{0}, cfg_q{0};
-  if (int rc = set_smem_once<C>((const void*)fa_bwd_dkdv_kernel<C>, C::kKVSmem, cfg_kv)) return rc;
-  if (int rc = set_smem_once<C>((const void*)fa_bwd_dq_kernel<C>, C::kQSmem, cfg_q)) return rc;
-
-  const long long n_kv = (long long)p.n_kt * a.Hkv * a.B;
-  const long long n_q = (long long)p.n_qt * a.Hq * a.B;
-  if (n_kv > 0x7fffffffLL || n_q > 0x7fffffffLL) {
-    set_error("backward grid of %lld / %lld CTAs is out of range", n_kv, n_q);
-    return 2;
-  }
-
-  // 3. Dropout: the forward's keep decisions, once for both kernels.
-  if constexpr (kDrop) {
-    const long long n_units = (long long)a.B * a.Hq * p.n_qt * p.n_kt;
-    if (n_units > 0x7fffffffLL) {  // the kernel's 32-bit unit index u + gridDim.x must not wrap
-      set_error("dropout keep mask of %lld tiles is out of range", n_units);
-      return 2;
-    }
-    KeepMaskArgs ka;
-    uint32_t k0 = (uint32_t)a.dropout_seed, k1 = (uint32_t)(a.dropout_seed >> 32);
-    for (int r = 0; r < 10; ++r, k0 += 0x9E3779B9u, k1 += 0xBB67AE85u) {  // Philox4x32 key schedule
-      ka.rk0[r] = k0;
-      ka.rk1[r] = k1;
-    }
-    ka.n_kb = (uint32_t)p.n_kt;
-    ka.n_units = (uint32_t)n_units;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
-    const unsigned grid = (unsigned)std::min<long long>(n_units, (long long)sms * 8);
-    fa_bwd_keep_mask_kernel<<<grid, 256, 0, a.stream>>>(p, ka);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) {
-      set_error("keep-mask launch failed: %s", cudaGetErrorString(e));
-      return 4;
-    }
-  }
-
-  // 4. dK, dV: one CTA per (128-key tile, kvh, b).
-  fa_bwd_dkdv_kernel<C><<<(unsigned)n_kv, C::kThreads, C::kKVSmem, a.stream>>>(tq, tk, tv, tdo, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    set_error("dK/dV launch failed: %s", cudaGetErrorString(e));
-    return 4;
-  }
-  // 5. dQ: one CTA per (128-row query tile, h, b).
-  fa_bwd_dq_kernel<C><<<(unsigned)n_q, C::kThreads, C::kQSmem, a.stream>>>(tq, tk, tv, tdo, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    set_error("dQ launch failed: %s", cudaGetErrorString(e));
-    return 4;
-  }
-  return 0;
-}
-
-}  // namespace
+int launch_bwd_feat(const BwdLaunchArgs& a);  // fa_bwd_feat.cu
+int launch_bwd_drop(const BwdLaunchArgs& a);  // fa_bwd_drop.cu
+int launch_bwd_mask(const BwdLaunchArgs& a);  // fa_bwd_mask.cu
 
 int launch_bwd(const BwdLaunchArgs& a) {
-  if (a.dropout_p != 0.0f) {
-    if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true, true>(a) : launch_bwd_d<128, true, true, true>(a);
-    return a.D == 64 ? launch_bwd_d<64, false, true, true>(a) : launch_bwd_d<128, false, true, true>(a);
-  }
-  if (a.window != 0 || a.q_offset != 0 || a.softcap != 0.0f) {
-    if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true>(a) : launch_bwd_d<128, true, true>(a);
-    return a.D == 64 ? launch_bwd_d<64, false, true>(a) : launch_bwd_d<128, false, true>(a);
-  }
+  using namespace bwd_impl;
+  if (a.mask_kind != 0) return launch_bwd_mask(a);
+  if (a.dropout_p != 0.0f) return launch_bwd_drop(a);
+  if (a.window != 0 || a.q_offset != 0 || a.softcap != 0.0f) return launch_bwd_feat(a);
   if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, false>(a) : launch_bwd_d<128, true, false>(a);
   return a.D == 64 ? launch_bwd_d<64, false, false>(a) : launch_bwd_d<128, false, false>(a);
 }

@@ -1,0 +1,12 @@
+// fa_bwd_feat.cu -- backward plans with sliding window / causal offset / softcap.
+#include "fa_bwd_impl.cuh"
+
+namespace fa {
+
+int launch_bwd_feat(const BwdLaunchArgs& a) {
+  using namespace bwd_impl;
+  if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true>(a) : launch_bwd_d<128, true, true>(a);
+  return a.D == 64 ? launch_bwd_d<64, false, true>(a) : launch_bwd_d<128, false, true>(a);
+}
+
+}  // namespace fa

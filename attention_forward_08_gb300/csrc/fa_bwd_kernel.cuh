@@ -64,6 +64,16 @@ struct BwdParams {
   // some key of are written; the others are never needed (P = 0 there).
   uint32_t* keep_mask;
   long long keep_row_words;  // a multiple of 4 (16-byte rows of 128-key blocks)
+  // The forward's mask (kFeat kernels): 1 bool (uint8, nonzero keeps), 2
+  // additive (I/O format, added to the scaled score); the dQ kernel reads its
+  // rows, the dK/dV kernel a key-major copy (written by the transpose pre-pass,
+  // zero past qL) whose rows hold mask_t_ld entries (a multiple of 128).
+  int mask_kind;
+  const void* mask;
+  long long mask_sb, mask_sh, mask_ss;
+  int mask_vec;
+  const void* mask_t;
+  long long mask_t_ld;
   int n_qt, n_kt;     // 128-row query tiles per (b, h), 128-key tiles per (b, kvh)
   float scale;        // softmax scale (applied to dQ and dK in the epilogue)
   float scale_log2;   // scale * log2(e)
@@ -76,7 +86,7 @@ struct BwdParams {
   long long timeout_cycles;
 };
 
-template <int kD_, bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false>
+template <int kD_, bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false, bool kMask_ = false>
 struct BwdCfg {
   static constexpr int kD = kD_;
   // 16-bit I/O is bf16 unless kF16 (fp16): same kernels, other operand format.
@@ -87,6 +97,10 @@ struct BwdCfg {
   // Dropout as well (its own instantiations again; implies kFeat).
   static constexpr bool kDrop = kDrop_;
   static_assert(!kDrop || kFeat, "the dropout instantiation includes the other features");
+  // The forward's bool or additive mask (its own instantiations again: the
+  // mask words cost registers that the other feature kernels keep free).
+  static constexpr bool kMask = kMask_;
+  static_assert(!kMask || kFeat, "the mask instantiation includes the other features");
   static constexpr uint32_t kFmt = kF16 ? kFmtF16 : kFmtBf16;
   static constexpr CUtensorMapDataType kTmaType =
       kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -212,7 +226,8 @@ __device__ __forceinline__ uint4 philox_10_rk(uint32_t c0, uint32_t c1, const Ke
 // per SM (32 registers), 32-bit unit decoding (the host keeps n_units below
 // 2^31, so u + gridDim.x cannot wrap), counters and destinations advanced by
 // adds.
-__global__ void __launch_bounds__(256, 8) fa_bwd_keep_mask_kernel(const BwdParams p, const KeepMaskArgs ka) {
+// (static: each backward translation unit that launches it has its own copy)
+static __global__ void __launch_bounds__(256, 8) fa_bwd_keep_mask_kernel(const BwdParams p, const KeepMaskArgs ka) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned long long row_ctr = (unsigned long long)(p.kL / 4);
   const uint32_t thr = p.drop_threshold, nqt = (uint32_t)p.n_qt;
@@ -311,6 +326,100 @@ __device__ __forceinline__ void bwd_ds_pass(uint32_t tdp, const float (&p)[128],
 __device__ __forceinline__ float softcap_factor(float p, float l2, float inv_out) {
   const float th = (lg2(p) + l2) * inv_out;
   return p > 0.0f ? fmaf(-th, th, 1.0f) : 0.0f;
+}
+
+// The forward's mask on 128 consecutive entries (keys of a query row, or queries
+// of a key row in the key-major copy) as packed words: bool, 4 bytes a word
+// (words 0..31); additive, two 16-bit values a word (words 0..63).  With
+// `vec` the 128 entries are read with 16-byte loads; otherwise only the first
+// `n` are read one by one and the rest stay 0 (excluded for bool, no
+// addition for additive; callers cut those entries by their limits anyway).
+template <bool kBool>
+__device__ __forceinline__ void bwd_load_mask128(uint32_t (&mw)[64], const void* src, bool vec, int n) {
+  constexpr int kWords = kBool ? 32 : 64;
+  if (vec) {
+    const uint4* s4 = static_cast<const uint4*>(src);
+#pragma unroll
+    for (int v = 0; v < kWords / 4; ++v) {
+      const uint4 w = __ldg(s4 + v);
+      mw[4 * v] = w.x;
+      mw[4 * v + 1] = w.y;
+      mw[4 * v + 2] = w.z;
+      mw[4 * v + 3] = w.w;
+    }
+  } else {
+    // every index compile-time, so the words stay in registers
+    constexpr int kPer = kBool ? 4 : 2;
+#pragma unroll
+    for (int v = 0; v < kWords; ++v) {
+      uint32_t w = 0u;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const int c = v * kPer + e;
+        if (c < n) {
+          if constexpr (kBool)
+            w |= (uint32_t)__ldg(static_cast<const uint8_t*>(src) + c) << (8 * e);
+          else
+            w |= (uint32_t)__ldg(static_cast<const uint16_t*>(src) + c) << (16 * e);
+        }
+      }
+      mw[v] = w;
+    }
+  }
+}
+
+// Probabilities of 128 scores with the forward's mask folded in: p = 2^(x)
+// with x = s * sf - l2 (+ m * log2(e) for an additive mask), 0 where the entry
+// lies outside [lo, lim) (the row's limits) or a bool mask excludes it.  l2(c)
+// gives the base-2 logsumexp of entry c's query row.
+template <class C, int kKind, class L2>
+__device__ __forceinline__ void bwd_p_masked(float (&pr)[128], float sf, L2 l2, const uint32_t (&mw)[64], int lo,
+                                             int lim) {
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    float x0, x1;
+    ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2(c), -l2(c + 1));
+    bool a0 = c >= lo && c < lim, a1 = c + 1 >= lo && c + 1 < lim;
+    if constexpr (kKind == 2) {
+      const uint32_t w = mw[c >> 1];
+      ffma2(x0, x1, half_bits_to_f32<C::kF16>(w), half_bits_to_f32<C::kF16>(w >> 16), kLog2e, kLog2e, x0, x1);
+    } else {
+      const uint32_t w = mw[c >> 2] >> (8 * (c & 3));
+      a0 = a0 && (w & 0xFFu) != 0u;
+      a1 = a1 && (w & 0xFF00u) != 0u;
+    }
+    pr[c] = a0 ? ex2(x0) : 0.0f;
+    pr[c + 1] = a1 ? ex2(x1) : 0.0f;
+  }
+}
+
+// Key-major copy of the forward's mask for the key-parallel kernel:
+// mask_t[(b H_q + h) kL + j][i] = mask[b, h, i, j] for i < qL, 0 for qL <= i <
+// ld.  32 x 32 tiles through shared memory (coalesced reads and writes); the
+// grid walks (key tile, query tile, (b, h)), the last dimension in a loop.
+template <class T>
+__global__ void __launch_bounds__(256) fa_bwd_mask_transpose_kernel(const T* __restrict__ mask, long long sb,
+                                                                    long long sh, long long ss, int Hq, int BH,
+                                                                    int qL, int kL, long long ld,
+                                                                    T* __restrict__ mask_t) {
+  __shared__ T tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  const int j0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+  for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
+    const int b = bh / Hq, h = bh - b * Hq;
+    const T* src = mask + (long long)b * sb + (long long)h * sh;
+    for (int r = ty; r < 32; r += 8) {
+      const int i = i0 + r, j = j0 + tx;
+      tile[r][tx] = (i < qL && j < kL) ? src[(long long)i * ss + j] : T(0);
+    }
+    __syncthreads();
+    T* dst = mask_t + (long long)bh * kL * ld;
+    for (int r = ty; r < 32; r += 8) {
+      const int j = j0 + r, i = i0 + tx;
+      if (j < kL && i < ld) dst[(long long)j * ld + i] = tile[tx][r];
+    }
+    __syncthreads();
+  }
 }
 
 // Transposes a 32 x 32 bit matrix held one row per lane (bit k of lane l's
@@ -694,6 +803,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       step_of(i, h, q0);
       const int s = i % C::kStages, use = i / C::kStages;
       const float* l2s = sLD + s * 2 * C::kTile;
+      // The forward's mask for this key and the step's 128 queries (key-major
+      // copy: contiguous, 16-byte aligned), loaded before S^T lands.
+      uint32_t mw[64];
+      if constexpr (C::kMask) {
+        if (p.mask_kind != 0 && j < p.kL) {
+          const long long off = (((long long)b * p.Hq + h) * p.kL + j) * p.mask_t_ld + q0;
+          if (p.mask_kind == 1)
+            bwd_load_mask128<true>(mw, static_cast<const uint8_t*>(p.mask_t) + off, true, 128);
+          else
+            bwd_load_mask128<false>(mw, static_cast<const uint16_t*>(p.mask_t) + off, true, 128);
+        }
+      }
       ok = warp_wait(&ctl->ld_full[s], use & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       if constexpr (C::kDrop) {
@@ -724,12 +845,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int c = 0; c < 128; ++c) pr[c] = fmaf(-2.0f * cout, rcp_approx(ex2(pr[c] * kin) + 1.0f), cout);
         }
         const float sf = p.softcap_on ? 1.0f : sl;
+        if (C::kMask && p.mask_kind == 2 && j < p.kL) {
+          bwd_p_masked<C, 2>(pr, sf, [&](int c) { return l2s[c]; }, mw, lim, hi);
+        } else if (C::kMask && p.mask_kind == 1 && j < p.kL) {
+          bwd_p_masked<C, 1>(pr, sf, [&](int c) { return l2s[c]; }, mw, lim, hi);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          float x0, x1;
-          ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2s[c], -l2s[c + 1]);
-          pr[c] = (c < lim || c >= hi) ? 0.0f : ex2(x0);
-          pr[c + 1] = (c + 1 < lim || c + 1 >= hi) ? 0.0f : ex2(x1);
+          for (int c = 0; c < 128; c += 2) {
+            float x0, x1;
+            ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2s[c], -l2s[c + 1]);
+            pr[c] = (c < lim || c >= hi) ? 0.0f : ex2(x0);
+            pr[c + 1] = (c + 1 < lim || c + 1 >= hi) ? 0.0f : ex2(x1);
+          }
         }
       } else {
         int lim = p.causal ? j - q0 : 0;
@@ -1037,6 +1164,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           kw[3] = k4.w;
         }
       }
+      // The forward's mask on this row's keys of block j, loaded before S_j lands.
+      uint32_t mw[64];
+      if constexpr (C::kMask) {
+        if (p.mask_kind != 0 && i < p.qL) {
+          const long long off = (long long)b * p.mask_sb + (long long)h * p.mask_sh + (long long)i * p.mask_ss + kbase;
+          const bool vec = p.mask_vec != 0 && kbase + 128 <= p.kL;
+          const int n = min(128, p.kL - kbase);
+          if (p.mask_kind == 1)
+            bwd_load_mask128<true>(mw, static_cast<const uint8_t*>(p.mask) + off, vec, n);
+          else
+            bwd_load_mask128<false>(mw, static_cast<const uint16_t*>(p.mask) + off, vec, n);
+        }
+      }
       ok = warp_wait(&ctl->s_full, j & 1, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
@@ -1063,16 +1203,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           sq = 1.0f;
         }
       }
+      if (C::kMask && p.mask_kind == 2 && i < p.qL) {
+        bwd_p_masked<C, 2>(pr, sq, [&](int) { return l2; }, mw, lo, lim);
+      } else if (C::kMask && p.mask_kind == 1 && i < p.qL) {
+        bwd_p_masked<C, 1>(pr, sq, [&](int) { return l2; }, mw, lo, lim);
+      } else {
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        float x0, x1;
-        ffma2(x0, x1, pr[c], pr[c + 1], sq, sq, -l2, -l2);
-        if constexpr (C::kFeat) {
-          pr[c] = (c < lim && c >= lo) ? ex2(x0) : 0.0f;
-          pr[c + 1] = (c + 1 < lim && c + 1 >= lo) ? ex2(x1) : 0.0f;
-        } else {
-          pr[c] = c < lim ? ex2(x0) : 0.0f;
-          pr[c + 1] = c + 1 < lim ? ex2(x1) : 0.0f;
+        for (int c = 0; c < 128; c += 2) {
+          float x0, x1;
+          ffma2(x0, x1, pr[c], pr[c + 1], sq, sq, -l2, -l2);
+          if constexpr (C::kFeat) {
+            pr[c] = (c < lim && c >= lo) ? ex2(x0) : 0.0f;
+            pr[c + 1] = (c + 1 < lim && c + 1 >= lo) ? ex2(x1) : 0.0f;
+          } else {
+            pr[c] = c < lim ? ex2(x0) : 0.0f;
+            pr[c + 1] = c + 1 < lim ? ex2(x1) : 0.0f;
+          }
         }
       }
       ok = warp_wait(&ctl->dp_full[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);

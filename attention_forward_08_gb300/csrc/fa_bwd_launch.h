@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fa.h"
+
 namespace fa {
 
 struct BwdLaunchArgs {
@@ -23,6 +25,12 @@ struct BwdLaunchArgs {
   unsigned long long dropout_offset; //   contract, as in the forward)
   uint32_t* keep_mask;               // dropout: [B, H_q, qL, keep_row_words] scratch for the
   long long keep_row_words;          //   keep decisions (4 * ceil(kL / 128) words a row)
+  int mask_kind;                     // the forward's mask: 0 none, 1 bool (uint8), 2 additive (I/O format)
+  const void* mask;                  // [B, H_q, qL, kL] through ms (element strides; key stride 1)
+  long long ms[3];
+  int mask_vec;                      // mask rows 16-byte aligned: vector loads
+  void* mask_t;                      // scratch: key-major copy [B, H_q, kL, mask_t_ld]
+  long long mask_t_ld;
   cudaStream_t stream;
   unsigned int* status;
   long long timeout_cycles;
@@ -35,10 +43,8 @@ int launch_bwd(const BwdLaunchArgs& a);
 // B * H * L > cap for positive B, H, L, computed without overflow.
 bool rows_exceed(int B, int H, int L, long long cap);
 
-// Checks a backward call's arguments other than its workspace (fa_bwd_ex's
-// rules); returns FA_OK or an fa_status code with the message set.
-int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                 const void* dq, const void* dk, const void* dv, int B, int H_q, int H_kv, int qL, int kL, int D,
-                 float scale, int window, int q_offset, float softcap, float dropout_p, int dtype);
+// Checks a backward call's arguments other than its workspace; returns
+// FA_OK or an fa_status code with the message set.
+int validate_bwd(const fa_bwd_args* a);
 
 }  // namespace fa

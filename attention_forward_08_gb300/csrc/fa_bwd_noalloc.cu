@@ -4,6 +4,7 @@
 // array's address is looked up once per device with cudaGetSymbolAddress.
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "fa.h"
@@ -36,8 +37,27 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     return FA_ERR_UNSUPPORTED;
   }
   // The remaining argument checks come before any CUDA call, as for fa_bwd.
-  int rc = fa::validate_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, 0, 0, 0.0f, 0.0f,
-                            dtype);
+  fa_bwd_args chk;
+  std::memset(&chk, 0, sizeof(chk));
+  chk.q = q;
+  chk.k = k;
+  chk.v = v;
+  chk.o = o;
+  chk.dout = dout;
+  chk.lse = lse;
+  chk.dq = dq;
+  chk.dk = dk;
+  chk.dv = dv;
+  chk.B = B;
+  chk.H_q = H_q;
+  chk.H_kv = H_kv;
+  chk.qL = qL;
+  chk.kL = kL;
+  chk.D = D;
+  chk.scale = scale;
+  chk.causal = causal;
+  chk.dtype = dtype;
+  int rc = fa::validate_bwd(&chk);
   if (rc != FA_OK) return rc;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

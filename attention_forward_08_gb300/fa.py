@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED
 
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_last_error", "fa_sync_status",
             "fa_set_timeout_cycles", "fa_set_max_ctas", "fa_set_q_tiles", "fa_bwd_workspace_bytes",
-            "fa_bwd_ex_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_bwd_noalloc", "fa_version")
+            "fa_bwd_ex_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_bwd_full", "fa_bwd_full_workspace_bytes",
+            "fa_bwd_noalloc", "fa_version")
 
 
 class FaError(RuntimeError):
@@ -53,6 +54,23 @@ class FaFwdArgs(ctypes.Structure):
         ("window", ctypes.c_int), ("q_offset", ctypes.c_int), ("softcap", ctypes.c_float),
         ("dropout_p", ctypes.c_float), ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_ulonglong),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_longlong),
+    ]
+
+
+class FaBwdArgs(ctypes.Structure):
+    """Layout of ``fa_bwd_args`` in include/fa.h."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("o", ctypes.c_void_p),
+        ("dout", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_longlong),
+        ("B", ctypes.c_int), ("H_q", ctypes.c_int), ("H_kv", ctypes.c_int),
+        ("qL", ctypes.c_int), ("kL", ctypes.c_int), ("D", ctypes.c_int),
+        ("scale", ctypes.c_float), ("causal", ctypes.c_int),
+        ("window", ctypes.c_int), ("q_offset", ctypes.c_int), ("softcap", ctypes.c_float),
+        ("dropout_p", ctypes.c_float), ("dropout_seed", ctypes.c_ulonglong), ("dropout_offset", ctypes.c_ulonglong),
+        ("mask", ctypes.c_void_p), ("mask_kind", ctypes.c_int), ("mask_strides", ctypes.c_longlong * 3),
+        ("dtype", ctypes.c_int), ("stream", ctypes.c_void_p),
     ]
 
 
@@ -98,6 +116,10 @@ def load_library(path: str = LIB_PATH):
     lib.fa_bwd_ex.argtypes = [ctypes.c_void_p] * 10 + [ctypes.c_longlong] + [ctypes.c_int] * 6 + \
         [ctypes.c_float] + [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_float, ctypes.c_ulonglong,
                                                  ctypes.c_ulonglong, ctypes.c_int, ctypes.c_void_p]
+    lib.fa_bwd_full.restype = ctypes.c_int
+    lib.fa_bwd_full.argtypes = [ctypes.POINTER(FaBwdArgs)]
+    lib.fa_bwd_full_workspace_bytes.restype = ctypes.c_longlong
+    lib.fa_bwd_full_workspace_bytes.argtypes = [ctypes.POINTER(FaBwdArgs)]
     lib.fa_bwd_noalloc.restype = ctypes.c_int
     lib.fa_bwd_noalloc.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + \
         [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
@@ -176,6 +198,16 @@ def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, 
                                      qL, kL, D, float(scale), int(causal), int(window), int(q_offset),
                                      float(softcap), float(dropout_p), int(dropout_seed) & (2**64 - 1),
                                      int(dropout_offset) & (2**64 - 1), int(dtype), stream)
+
+
+def fa_bwd_full(args: FaBwdArgs) -> int:
+    """``fa_bwd_full`` of include/fa.h (every backward option in one argument block). Returns the status."""
+    return load_library().fa_bwd_full(ctypes.byref(args))
+
+
+def fa_bwd_full_workspace_bytes(args: FaBwdArgs) -> int:
+    """``fa_bwd_full_workspace_bytes`` of include/fa.h (-1: invalid arguments)."""
+    return load_library().fa_bwd_full_workspace_bytes(ctypes.byref(args))
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H_q, H_kv, qL, kL, D, scale, causal, dtype, stream):
@@ -322,17 +354,20 @@ def attention(q, k, v, *, scale=None, causal=False, mask=None, mask_kind=None, o
 
 
 def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, dk=None, dv=None, workspace=None,
-                  stream=None, window=0, q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0):
+                  stream=None, window=0, q_offset=0, softcap=0.0, dropout_p=0.0, dropout_seed=0, dropout_offset=0,
+                  mask=None, mask_kind=None):
     """dQ, dK, dV for torch CUDA tensors; returns (dq, dk, dv).
 
-    window, q_offset, softcap, dropout_p, dropout_seed, dropout_offset: the
-    forward's (``attention``), so that the backward sees the same softmax and
-    regenerates the same keep decisions.
+    window, q_offset, softcap, dropout_p, dropout_seed, dropout_offset, mask,
+    mask_kind: the forward's (``attention``), so that the backward sees the
+    same softmax and regenerates the same keep decisions.
 
     q, o, dout: contiguous bf16 or fp16 [B, H_q, qL, D]; k, v: the same dtype,
     [B, H_kv, kL, D]; lse: the forward's contiguous fp32 [B, H_q, qL].
-    workspace: optional device tensor of at least ``fa_bwd_ex_workspace_bytes``
-    bytes (allocated here if None).
+    mask: None, bool/uint8 (nonzero keeps) or additive in q's dtype,
+    broadcastable to [B, H_q, qL, kL] through its strides.
+    workspace: optional device tensor of at least ``fa_bwd_full_workspace_bytes``
+    bytes, 256-byte aligned (allocated here if None).
     """
     import torch
     B, H_q, qL, D = q.shape
@@ -364,21 +399,50 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
             raise ValueError(f"{name} must be {like.dtype} {tuple(like.shape)} (got {t.dtype} {tuple(t.shape)})")
         if not t.is_cuda or t.device != q.device or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor on {q.device}")
-    need = fa_bwd_ex_workspace_bytes(B, H_q, qL, kL, dropout_p)
+    a = FaBwdArgs()
+    a.q, a.k, a.v, a.o, a.dout, a.lse = (t.data_ptr() for t in (q, k, v, o, dout, lse))
+    a.dq, a.dk, a.dv = dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    a.B, a.H_q, a.H_kv, a.qL, a.kL, a.D = B, H_q, H_kv, qL, kL, D
+    a.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
+    a.causal = int(bool(causal))
+    a.window, a.q_offset, a.softcap = int(window), int(q_offset), float(softcap)
+    a.dropout_p = float(dropout_p)
+    a.dropout_seed, a.dropout_offset = int(dropout_seed) & (2**64 - 1), int(dropout_offset) & (2**64 - 1)
+    a.dtype = FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16
+    if mask is None:
+        a.mask, a.mask_kind = None, FA_MASK_NONE
+    else:
+        if mask_kind is None:
+            mask_kind = FA_MASK_BOOL if mask.dtype in (torch.bool, torch.uint8) else FA_MASK_ADDITIVE
+        if mask_kind == FA_MASK_BOOL:
+            if mask.dtype == torch.bool:
+                mask = mask.view(torch.uint8)
+            if mask.dtype != torch.uint8:
+                raise ValueError("a bool mask must be torch.bool or torch.uint8")
+        elif mask.dtype != q.dtype:
+            raise ValueError(f"an additive mask must have q's dtype {q.dtype} (got {mask.dtype})")
+        if not mask.is_cuda:
+            raise ValueError("mask must be a CUDA tensor")
+        mask = mask.expand(B, H_q, qL, kL)
+        if mask.stride(3) != 1:
+            raise ValueError("mask must have unit stride along the key dimension")
+        a.mask, a.mask_kind = mask.data_ptr(), int(mask_kind)
+        a.mask_strides[:] = (mask.stride(0), mask.stride(1), mask.stride(2))
+    need = fa_bwd_full_workspace_bytes(a)
     if need < 0:
-        raise ValueError(f"dropout_p must lie in [0, 1] (got {dropout_p})")
+        _check(FA_ERR_INVALID_ARGUMENT)
     own_workspace = workspace is None
     if own_workspace:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    if workspace.numel() * workspace.element_size() < need:
-        raise ValueError(f"workspace holds fewer than the {need} bytes required")
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=q.device)
+    base = workspace.data_ptr()
+    start = (base + 255) // 256 * 256
+    if workspace.numel() * workspace.element_size() - (start - base) < need:
+        raise ValueError(f"workspace holds fewer than the {need} bytes (256-byte aligned) required")
+    a.workspace, a.workspace_bytes = start, need
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif own_workspace:
         _keep_until_stream_done(workspace, stream, q.device)
-    _check(fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-                     workspace.numel() * workspace.element_size(), B, H_q, H_kv, qL, kL, D,
-                     1.0 / math.sqrt(D) if scale is None else scale, causal, window, q_offset, softcap,
-                     dropout_p, dropout_seed, dropout_offset, FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16, stream))
+    a.stream = stream
+    _check(fa_bwd_full(a))
     return dq, dk, dv

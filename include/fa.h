@@ -273,10 +273,67 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int qL, int kL, int D, float scale,
                    int causal, int dtype, void* stream);
 
+/*
+ * fa_bwd_args / fa_bwd_full -- the backward pass with every option of the
+ * forward in one argument block (ABI 1.09).  The fields mean what the fa_bwd
+ * and fa_bwd_ex arguments of the same names mean; zero-initialise the struct
+ * and fill what the forward used.  Added here:
+ *   mask, mask_kind, mask_strides -- the forward's mask, with the
+ *     fa_fwd_args conventions: mask_kind FA_MASK_BOOL (uint8, nonzero keeps
+ *     the key) or FA_MASK_ADDITIVE (the I/O dtype, added to the scaled score,
+ *     -inf excludes the key); element strides {batch, head, row} with unit key
+ *     stride, 0 broadcasting that dimension; mask NULL exactly when mask_kind
+ *     is FA_MASK_NONE.  The gradients are those of the masked softmax the
+ *     forward computed (ruDNN "dense_attention.rs", `backward` and
+ *     `backward_kv_owned`: mask kinds 1 and 2 with the same `allowed` and
+ *     additive rules as its `forward`):
+ *     P_ij = exp(scale q_i.k_j + m_ij - L_i), 0 where the key is excluded, so
+ *     excluded keys and rows without any allowed key get zero gradient.  A
+ *     mask together with a softcap is FA_ERR_UNSUPPORTED.
+ * Scratch: fa_bwd_full_workspace_bytes(args) bytes, 256-byte aligned: the
+ * D vector, the dropout keep decisions (dropout_p > 0) and, with a mask, a
+ * key-major copy of the mask for the key-parallel kernel (B * H_q * kL *
+ * ceil(qL / 128) * 128 elements), each part starting on a 256-byte boundary;
+ * a fifth launch writes that copy.  Results and errors otherwise as fa_bwd_ex.
+ */
+typedef struct fa_bwd_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* workspace;           /* 256-byte aligned, fa_bwd_full_workspace_bytes(args) bytes */
+  long long workspace_bytes;
+  int B, H_q, H_kv, qL, kL, D;
+  float scale;
+  int causal;
+  int window;
+  int q_offset;
+  float softcap;
+  float dropout_p;
+  unsigned long long dropout_seed;
+  unsigned long long dropout_offset;
+  const void* mask;
+  int mask_kind;
+  long long mask_strides[3];
+  int dtype;
+  void* stream; /* cudaStream_t */
+} fa_bwd_args;
+
+int fa_bwd_full(const fa_bwd_args* args);
+
+/* Bytes of scratch fa_bwd_full needs for these arguments; -1 (with the message
+ * set) when they are invalid. */
+long long fa_bwd_full_workspace_bytes(const fa_bwd_args* args);
+
 /* ABI version: major * 100 + minor (1.05: fa_bwd and fa_bwd_noalloc accept
  * FA_DTYPE_F16; 1.06: fa_fwd_args.workspace, fa_fwd_workspace_bytes; 1.07:
  * fa_bwd_ex; 1.08: fa_bwd_ex takes the forward's dropout arguments,
- * fa_bwd_ex_workspace_bytes). */
+ * fa_bwd_ex_workspace_bytes; 1.09: fa_bwd_args, fa_bwd_full with masks). */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -30,7 +30,7 @@ def _declared_functions():
 def test_header_declares_the_abi():
     assert _declared_functions() == sorted(
         ["fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_bwd_workspace_bytes",
-         "fa_bwd_ex_workspace_bytes", "fa_bwd_noalloc",
+         "fa_bwd_ex_workspace_bytes", "fa_bwd_full", "fa_bwd_full_workspace_bytes", "fa_bwd_noalloc",
          "fa_last_error",
          "fa_sync_status",
          "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_timeout_cycles", "fa_version"])
@@ -45,25 +45,27 @@ def test_library_exports_every_declared_symbol(fa):
     assert set(_declared_functions()) <= exported
 
 
-def test_args_struct_matches_header(tmp_path):
-    """ctypes' FaFwdArgs has the same size and field offsets as the C struct."""
-    from attention_forward_08_gb300.fa import FaFwdArgs
-    fields = [f for f, _ in FaFwdArgs._fields_]
+@pytest.mark.parametrize("cname,pyname", [("fa_fwd_args", "FaFwdArgs"), ("fa_bwd_args", "FaBwdArgs")])
+def test_args_struct_matches_header(tmp_path, cname, pyname):
+    """ctypes' argument structs have the same size and field offsets as the C structs."""
+    from attention_forward_08_gb300 import fa as binding
+    S = getattr(binding, pyname)
+    fields = [f for f, _ in S._fields_]
     src = tmp_path / "layout.c"
     src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "fa.h"\nint main(void){\n'
-                   '  printf("%zu\\n", sizeof(fa_fwd_args));\n'
-                   + "".join(f'  printf("%zu\\n", offsetof(fa_fwd_args, {f}));\n' for f in fields)
+                   f'  printf("%zu\\n", sizeof({cname}));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof({cname}, {f}));\n' for f in fields)
                    + "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", f"-I{ROOT}/include", str(src), "-o", str(exe)], check=True)
     vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(FaFwdArgs)
+    assert vals[0] == ctypes.sizeof(S)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(FaFwdArgs, f).offset == off, f
+        assert getattr(S, f).offset == off, f
 
 
 def test_version(fa):
-    assert fa.fa_version() == 108
+    assert fa.fa_version() == 109
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -280,3 +282,45 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.load_library(str(tmp_path / "missing.so"))
         finally:
             binding._lib = saved
+
+
+def _bwd_args(fa, **kw):
+    a = fa.FaBwdArgs()
+    a.q = a.k = a.v = a.o = a.dout = a.lse = a.dq = a.dk = a.dv = P
+    a.workspace, a.workspace_bytes = P, 1 << 30
+    a.B, a.H_q, a.H_kv, a.qL, a.kL, a.D = 1, 2, 2, 200, 300, 128
+    a.scale, a.causal, a.dtype = 0.088, 1, 1
+    for k_, v_ in kw.items():
+        if k_ == "mask_strides":
+            a.mask_strides[:] = v_
+        else:
+            setattr(a, k_, v_)
+    return a
+
+
+def test_bwd_full_workspace_with_mask(fa):
+    """fa_bwd_full_workspace_bytes: the D vector, then (dropout) the keep words, then (mask) a key-major copy of
+    the mask with whole 128-row query blocks per key, each part 256-byte aligned."""
+    al = lambda n: (n + 255) // 256 * 256
+    base = fa.fa_bwd_ex_workspace_bytes(1, 2, 200, 300, 0.0)
+    assert fa.fa.fa_bwd_full_workspace_bytes(_bwd_args(fa)) == base
+    a = _bwd_args(fa, mask=P, mask_kind=2, mask_strides=(2 * 200 * 300, 200 * 300, 300))
+    assert fa.fa.fa_bwd_full_workspace_bytes(a) == al(base) + al(1 * 2 * 300 * 256 * 2)
+    a = _bwd_args(fa, mask=P, mask_kind=1, mask_strides=(0, 0, 300), dropout_p=0.1)
+    base = fa.fa_bwd_ex_workspace_bytes(1, 2, 200, 300, 0.1)
+    assert fa.fa.fa_bwd_full_workspace_bytes(a) == al(base) + al(1 * 2 * 300 * 256 * 1)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(mask=P, mask_kind=0), 1, "mask must be non-NULL"),
+    (dict(mask=None, mask_kind=2), 1, "mask must be non-NULL"),
+    (dict(mask=P, mask_kind=3), 1, "mask_kind"),
+    (dict(mask=P, mask_kind=1, mask_strides=(0, -1, 300)), 1, "strides"),
+    (dict(mask=P, mask_kind=2, softcap=5.0), 2, "softcap"),
+    (dict(mask=P, mask_kind=2, workspace=P + 16), 3, "256-byte"),
+    (dict(mask=P, mask_kind=2, workspace_bytes=1024), 1, "workspace"),
+])
+def test_bwd_full_validation_rejects(fa, kw, status, needle):
+    a = _bwd_args(fa, **kw)
+    assert fa.fa.fa_bwd_full(a) == status
+    assert needle in fa.fa_last_error()

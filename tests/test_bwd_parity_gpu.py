@@ -212,3 +212,74 @@ def test_bwd_bench_dropout_workload_one_group(b, kvh):
     _compare(f"{w.name} b{b} kvh{kvh} dQ", dq[b:b + 1, heads], rq)
     _compare(f"{w.name} b{b} kvh{kvh} dK", dk[b:b + 1, kvh:kvh + 1], rk)
     _compare(f"{w.name} b{b} kvh{kvh} dV", dv[b:b + 1, kvh:kvh + 1], rv)
+
+
+# The forward's mask in the backward (fa_bwd_full): bool (nonzero keeps) and additive (-inf excludes),
+# with causal, GQA, ragged tails, fp16, dropout and a sliding window; mask rows whose byte stride is not a
+# multiple of 16 take the element-wise load path.
+MASKED = [
+    S("bwd_mask_bool_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "bf16", causal=True, mask_kind=W.MASK_BOOL, seed=71),
+    S("bwd_mask_add_d64_ragged_unaligned", 2, 2, 1, 200, 333, 64, "bf16", mask_kind=W.MASK_ADDITIVE, seed=72),
+    S("bwd_mask_add_f16_d128_causal", 1, 2, 2, 300, 300, 128, "f16", causal=True, mask_kind=W.MASK_ADDITIVE,
+      seed=73),
+    S("bwd_mask_bool_f16_d64_q_longer", 1, 2, 2, 260, 130, 64, "f16", mask_kind=W.MASK_BOOL, seed=74),
+    S("bwd_mask_bool_d64_dropout", 1, 2, 1, 256, 256, 64, "bf16", causal=True, mask_kind=W.MASK_BOOL,
+      dropout_p=0.2, dropout_seed=31, seed=75),
+    S("bwd_mask_add_d128_window", 1, 2, 2, 300, 300, 128, "bf16", causal=True, mask_kind=W.MASK_ADDITIVE,
+      window=100, seed=76),
+    S("bwd_mask_add_d128_gqa_long_kv", 1, 4, 1, 130, 520, 128, "bf16", mask_kind=W.MASK_ADDITIVE, seed=77),
+]
+
+
+def _run_masked(w, mask=None):
+    import attention_forward_08_gb300 as fa
+    q, k, v, m = W.make_inputs(w)
+    if mask is not None:
+        m = mask
+    do = W.make_dout(w)
+    dev = "cuda:0"
+    qd, kd, vd, dod, md = q.to(dev), k.to(dev), v.to(dev), do.to(dev), m.to(dev)
+    kw = dict(scale=w.sm_scale, causal=w.causal, window=w.window, q_offset=w.q_offset, dropout_p=w.dropout_p,
+              dropout_seed=w.dropout_seed, dropout_offset=w.dropout_offset, mask=md, mask_kind=w.mask_kind)
+    o, lse = fa.attention(qd, kd, vd, **kw)
+    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, **kw)
+    assert fa.fa_sync_status(None) == fa.fa.FA_OK, fa.fa_last_error()
+    rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                      do.double().numpy(), fp32_scale(w), causal=w.causal, mask=m.double().numpy(),
+                                      mask_kind=w.mask_kind, window=w.window, q_offset=w.q_offset,
+                                      dropout_p=float(np.float32(w.dropout_p)), seed=w.dropout_seed,
+                                      offset=w.dropout_offset)
+    tol = REL_TOL[w.dtype]
+    _compare(f"{w.name} dQ", dq, rq, tol)
+    _compare(f"{w.name} dK", dk, rk, tol)
+    _compare(f"{w.name} dV", dv, rv, tol)
+    return (dq, dk, dv), lse
+
+
+@pytest.mark.parametrize("w", MASKED, ids=lambda w: w.name)
+def test_bwd_masked(w):
+    _run_masked(w)
+
+
+def test_bwd_masked_empty_rows_and_keys():
+    """Rows whose bool mask keeps no key (L = -inf) get dQ = 0 exactly, and keys no row keeps get dK = dV = 0."""
+    w = S("bwd_mask_bool_empty", 1, 2, 2, 256, 256, 128, "bf16", mask_kind=W.MASK_BOOL, seed=78)
+    g = torch.Generator().manual_seed(6)
+    m = (torch.rand(1, 2, 256, 256, generator=g) < 0.6).to(torch.uint8)
+    m[0, 0, 17] = 0
+    m[0, 1, 130:140] = 0
+    m[0, :, :, 200] = 0
+    (dq, dk, dv), lse = _run_masked(w, mask=m)
+    assert torch.isneginf(lse[0, 0, 17]) and torch.isneginf(lse[0, 1, 130:140]).all()
+    assert torch.count_nonzero(dq[0, 0, 17]).item() == 0 and torch.count_nonzero(dq[0, 1, 130:140]).item() == 0
+    assert torch.count_nonzero(dk[0, :, 200]).item() == 0 and torch.count_nonzero(dv[0, :, 200]).item() == 0
+
+
+def test_bwd_masked_broadcast_strides():
+    """An additive mask broadcast over batch and heads through zero strides."""
+    w = S("bwd_mask_add_bcast", 2, 2, 2, 200, 264, 64, "bf16", causal=True, mask_kind=W.MASK_ADDITIVE, seed=79)
+    g = torch.Generator().manual_seed(8)
+    base = torch.randn(1, 1, 200, 264, generator=g).to(torch.bfloat16)
+    base[0, 0, torch.rand(200, 264, generator=g) < 0.1] = float("-inf")
+    base[0, 0, torch.arange(200), torch.arange(200)] = 0.0
+    _run_masked(w, mask=base)  # [1, 1, qL, kL]: the binding expands it with zero strides
