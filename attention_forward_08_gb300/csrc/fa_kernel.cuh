@@ -124,16 +124,20 @@ struct Cfg {
   // tf32 helper warps: warps 2-3, plus warps 8-11 when there is one Q tile
   // (rounding K and transposing V then keep pace with the tensor core).
   static constexpr bool kExtraHelpers = kHelpers && kNQT == 1;
+  // One Q tile with 16-bit I/O (no dropout): two softmax warpgroups share the
+  // tile, each taking 64 of a block's 128 keys for all 128 rows, so every SM
+  // sub-partition runs two softmax warps (one alone leaves its latency bare).
+  static constexpr bool kSplitRows = kNQT == 1 && !kTf32 && !kDrop;
   static constexpr int kCvtWarps = kHelpers ? (kExtraHelpers ? 6 : 2) : 1;
   static constexpr int kCvtThreads = 32 * kCvtWarps;
-  static constexpr int kThreads = 128 * (1 + kNQT) + (kExtraHelpers ? 128 : 0);
+  static constexpr int kThreads = 128 * (1 + kNQT) + (kExtraHelpers || kSplitRows ? 128 : 0);
   // Per-thread registers at launch, and the split after setmaxnreg: the
   // control warpgroup (TMA, MMA, tf32 helpers) gives registers to the softmax
   // warpgroups.  Sums stay within the launch total (kThreads * kRegsLaunch).
   static constexpr int kRegsLaunch = kThreads == 384 ? 168 : 255;
   static constexpr int kRegsCtrl = 80;
-  static constexpr int kRegsSoftmax = kNQT == 2 ? 208 : 0;  // 0: no reallocation
-  static_assert(kRegsSoftmax == 0 || 128 * kRegsCtrl + 128 * kNQT * kRegsSoftmax <= kThreads * kRegsLaunch,
+  static constexpr int kRegsSoftmax = (kNQT == 2 || kSplitRows) ? 208 : 0;  // 0: no reallocation
+  static_assert(kRegsSoftmax == 0 || 128 * kRegsCtrl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
                 "register split exceeds the launch allocation");
   static constexpr uint32_t kQTileBytes = kBM * kD * kEsz;
   static constexpr uint32_t kKVTileBytes = kBN * kD * kEsz;
@@ -375,13 +379,15 @@ __device__ __forceinline__ void fold_mask_chunk(float* s, const void* mrow_v, in
 // Fold one row of a TMA-loaded mask tile (128-byte swizzled rows; 2-byte
 // additive values in kBN/64 column blocks, or 1-byte bool values in one) into
 // s, like fold_mask_chunk does from global memory.
-template <class C>
-__device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t* tile, int kind, int tl, float f) {
+template <class C, int kCols = C::kBN>
+__device__ __forceinline__ void fold_mask_smem(float (&s)[kCols], const uint8_t* tile, int kind, int tl, float f,
+                                               int coff = 0) {  // coff: the tile column of s[0] (a multiple of 16)
   if (kind == 1) {
 #pragma unroll
-    for (int c = 0; c < C::kBN / 16; ++c) {  // 16 keys per 16-byte unit
-      const uint4 w = *reinterpret_cast<const uint4*>(tile + (c / 8) * (C::kBM * 128) + tl * 128 +
-                                                      (((c % 8) ^ (tl & 7)) << 4));
+    for (int c = 0; c < kCols / 16; ++c) {  // 16 keys per 16-byte unit
+      const int un = coff / 16 + c;
+      const uint4 w = *reinterpret_cast<const uint4*>(tile + (un / 8) * (C::kBM * 128) + tl * 128 +
+                                                      (((un % 8) ^ (tl & 7)) << 4));
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 16; ++e)
@@ -389,9 +395,10 @@ __device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < C::kBN / 8; ++c) {  // 8 bf16 keys per 16-byte unit
-      const uint4 w = *reinterpret_cast<const uint4*>(tile + (c / 8) * (C::kBM * 128) + tl * 128 +
-                                                      (((c % 8) ^ (tl & 7)) << 4));
+    for (int c = 0; c < kCols / 8; ++c) {  // 8 bf16 keys per 16-byte unit
+      const int un = coff / 8 + c;
+      const uint4 w = *reinterpret_cast<const uint4*>(tile + (un / 8) * (C::kBM * 128) + tl * 128 +
+                                                      (((un % 8) ^ (tl & 7)) << 4));
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 8; e += 2)
@@ -401,9 +408,10 @@ __device__ __forceinline__ void fold_mask_smem(float (&s)[C::kBN], const uint8_t
   }
 }
 
-template <class C>
-__device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p, int b, int h, int row, int kbase,
-                                           const uint8_t* mask_tile, int tl) {
+template <class C, int kCols = C::kBN>
+__device__ __forceinline__ void apply_mask(float (&s)[kCols], const FaParams& p, int b, int h, int row, int kbase,
+                                           const uint8_t* mask_tile, int tl, int coff = 0) {
+  // s holds keys kbase .. kbase + kCols - 1; coff is their first column in the block's mask tile.
   // Scores to base 2 first when a softcap applies, the scale is not positive,
   // or an additive mask meets either.  The softcap c * tanh(y) (y = scale * s
   // / c) uses tanh(y) = 1 - 2 / (2^(2 log2(e) y) + 1): one ex2 and one
@@ -414,15 +422,15 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
     if (C::kFeat && p.softcap_on) {
       const float kin = 2.0f * kLog2e * p.softcap_in, cout = p.softcap_out;
 #pragma unroll
-      for (int c = 0; c < C::kBN; ++c) s[c] = fmaf(-2.0f * cout, rcp_approx(ex2(s[c] * kin) + 1.0f), cout);
+      for (int c = 0; c < kCols; ++c) s[c] = fmaf(-2.0f * cout, rcp_approx(ex2(s[c] * kin) + 1.0f), cout);
     } else {
 #pragma unroll
-      for (int c = 0; c < C::kBN; c += 2) fmul2(s[c], s[c + 1], s[c], s[c + 1], p.scale_log2, p.scale_log2);
+      for (int c = 0; c < kCols; c += 2) fmul2(s[c], s[c + 1], s[c], s[c + 1], p.scale_log2, p.scale_log2);
     }
   }
   const float f = p.mask_natural ? p.inv_scale : kLog2e;  // additive mask factor
   if constexpr (C::kMaskSlotBytes > 0) {
-    if (mask_tile) fold_mask_smem<C>(s, mask_tile, p.mask_kind, tl, f);
+    if (mask_tile) fold_mask_smem<C, kCols>(s, mask_tile, p.mask_kind, tl, f, coff);
   }
   if (p.mask_kind != 0 && row < p.qL && !(C::kMaskSlotBytes > 0 && mask_tile)) {
     const size_t esz = (p.mask_kind == 1) ? 1 : C::kEsz;
@@ -430,7 +438,7 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
                        ((long long)b * p.mask_sb + (long long)h * p.mask_sh + (long long)row * p.mask_ss) * esz;
     const bool vec = p.mask_vec != 0;
 #pragma unroll
-    for (int cc = 0; cc < C::kBN / 32; ++cc) {
+    for (int cc = 0; cc < kCols / 32; ++cc) {
       if (p.mask_kind == 1)
         fold_mask_chunk<C, 1>(s + cc * 32, mrow, kbase + cc * 32, p.kL, vec, f);
       else
@@ -442,19 +450,19 @@ __device__ __forceinline__ void apply_mask(float (&s)[C::kBN], const FaParams& p
   int lim = p.kL - kbase;
   if (p.causal) lim = min(lim, diag + 1);
   const int lo = (C::kFeat && p.window > 0) ? diag - p.window + 1 : -1;
-  if (lim < C::kBN || lo > 0) {  // most blocks lie wholly inside the limits
+  if (lim < kCols || lo > 0) {  // most blocks lie wholly inside the limits
 #pragma unroll
-    for (int c = 0; c < C::kBN; ++c)
+    for (int c = 0; c < kCols; ++c)
       if (c >= lim || c < lo) s[c] = -INFINITY;
   }
 }
 
 // Row max of s (raw or base-2 scores): three-input max, four chains.
-template <class C>
-__device__ __forceinline__ float row_max(const float (&s)[C::kBN]) {
+template <class C, int kCols = C::kBN>
+__device__ __forceinline__ float row_max(const float (&s)[kCols]) {
   float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int c = 0; c < C::kBN; c += 8) {
+  for (int c = 0; c < kCols; c += 8) {
     mx4[0] = fmax3(mx4[0], s[c + 0], s[c + 1]);
     mx4[1] = fmax3(mx4[1], s[c + 2], s[c + 3]);
     mx4[2] = fmax3(mx4[2], s[c + 4], s[c + 5]);
@@ -467,13 +475,13 @@ __device__ __forceinline__ float row_max(const float (&s)[C::kBN]) {
 // or tf32), the fp32 sum of p, and with kWithMax the row max of s on the
 // side.  Pairs of scores go through packed fp32x2 FMA / add; the
 // exponentials through the SFU one at a time.
-template <class C, bool kWithMax>
-__device__ __forceinline__ void p_pass(const float (&s)[C::kBN], float sl, float msub, uint32_t tP, float& sum,
+template <class C, bool kWithMax, int kCols = C::kBN>
+__device__ __forceinline__ void p_pass(const float (&s)[kCols], float sl, float msub, uint32_t tP, float& sum,
                                        float& mx) {
   float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int cc = 0; cc < C::kBN / 32; ++cc) {
+  for (int cc = 0; cc < kCols / 32; ++cc) {
     uint32_t pk[C::kTf32 ? 32 : 16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
@@ -702,6 +710,226 @@ __device__ __forceinline__ void tf32_helpers(uint8_t* sQ, uint8_t* sK, uint8_t* 
   }
 }
 
+// Softmax of a one-Q-tile plan on two warpgroups (kSplitRows): warpgroup g
+// (warps 4 + 4 g .. 7 + 4 g) owns keys 64 g .. 64 g + 63 of every block for
+// all 128 rows (thread = TMEM lane = row), and half of O's columns in the
+// epilogue.  The two halves of a row share one running max: each block's half
+// maxima are exchanged through the block's P buffer in TMEM (free at that
+// point: the P V that last read it has completed), each warpgroup writing its
+// value into a column of the OTHER half, which that half reads before
+// overwriting it with its P; the row sums meet the same way in the epilogue.
+//
+// Sync supplies the schedule and the hand-offs: next(r, b, h, r0, j0, nb) (the
+// r-th unit: batch, head, this CTA's first row, key blocks [j0, nb); false when
+// done), wait_s / wait_m / wait_o (bounded waits on S landed, the mask tile
+// landed, P V landed) and the arrivals s_free / m_free / p_ready / o_free.
+template <class C, class Sync>
+__device__ __forceinline__ void softmax_split_rows(Sync& sy, uint8_t* sM, uint32_t tmem, const FaParams& p, int warp,
+                                                   int lane) {
+  constexpr int kHalf = C::kBN / 2;                 // keys per warpgroup
+  constexpr int kHalfD = C::kD / 2;                 // O columns per warpgroup in the epilogue
+  const int g = (warp - 4) >> 2;                    // 0: keys 0..63, 1: keys 64..127
+  const int tl = threadIdx.x - 128 * (1 + g);       // row of the tile
+  const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_addr + g * kHalf;
+  const uint32_t tO = tmem + lane_addr + C::kColO;
+  const float sl = p.pre_scale ? 1.0f : p.scale_log2;
+  // TMEM column (relative to a P buffer) this warpgroup writes for the other
+  // half to read, and the one it reads: column 0 lies in half 0's P, column
+  // kHalf / 2 in half 1's.
+  const uint32_t x_put = g == 0 ? kHalf / 2 : 0, x_get = g == 0 ? 0 : kHalf / 2;
+  int blocks_seen = 0, masks_seen = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    int b, h, r0, j0, nb;
+    if (!sy.next(r, b, h, r0, j0, nb)) break;
+    if (nb == 0) continue;
+    const int row = r0 + tl;
+    float m_run = -INFINITY;  // running max of the whole row, base 2 (scaled)
+    float l_run = 0.0f;       // this half's running sum of 2^(s - m_run)
+    for (int j = j0; j < nb; ++j) {
+      ok = sy.wait_s(blocks_seen & 1);
+      if (!ok) break;
+      ++blocks_seen;
+      tc_fence_after();
+      float s[kHalf];
+      {
+        uint32_t rr[kHalf];
+#pragma unroll
+        for (int cc = 0; cc < kHalf / 32; ++cc)
+          tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[cc * 32]));
+        tmem_wait_ld();
+        reg_fence(rr);
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) s[c] = __uint_as_float(rr[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) sy.s_free();
+
+      const int kbase = j * C::kBN + g * kHalf;  // this half's first key
+      const int q_off = C::kFeat ? p.q_offset : 0;
+      const bool need_mask = p.pre_scale || p.mask_kind != 0 || kbase + kHalf > p.kL ||
+                             (p.causal && kbase + kHalf - 1 > r0 + q_off) ||
+                             (C::kFeat && p.window > 0 && kbase <= r0 + C::kBM - 1 + q_off - p.window);
+      const uint8_t* mask_tile = nullptr;
+      if (C::kMaskSlotBytes > 0 && p.mask_smem) {
+        ok = sy.wait_m(masks_seen & 1);
+        ++masks_seen;
+        if (!ok) break;
+        mask_tile = sM;
+      }
+      if (need_mask) apply_mask<C, kHalf>(s, p, b, h, row, kbase, mask_tile, tl, g * kHalf);
+      if (mask_tile) {
+        __syncwarp();
+        if (lane == 0) sy.m_free();
+      }
+
+      // The row's block max from both halves.
+      const uint32_t tP = tmem + lane_addr + C::kColP + (j & 1) * C::kPCols;
+      const float mx_half = row_max<C, kHalf>(s);
+      tmem_st1(tP + x_put, __float_as_uint(mx_half));
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      const float mx_other = __uint_as_float(tmem_ld1(tP + x_get));
+      tmem_wait_ld();
+      const float mx = fmaxf(mx_half, mx_other);
+
+      const float m_blk = mx * sl;  // -inf stays -inf (sl > 0 whenever it is not 1)
+      const float m_new = fmaxf(m_run, m_blk);
+      float corr = 1.0f;
+      const bool resc = m_new > m_run + kRescaleThreshold;
+      if (resc) {
+        corr = ex2(m_run - m_new);  // 0 when m_run = -inf
+        m_run = m_new;
+      }
+      const float msub = (m_run == -INFINITY) ? 0.0f : m_run;
+      float sum, unused;
+      p_pass<C, false, kHalf>(s, sl, msub, tP + g * (kHalf / 2), sum, unused);
+      l_run = l_run * corr + sum;
+
+      // PV_{j-1} has landed before this half's O columns are rescaled.
+      if (j > j0) {
+        ok = sy.wait_o((blocks_seen - 2) & 1);
+        if (!ok) break;
+      }
+      if (j > j0 && __any_sync(0xffffffffu, resc)) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < kHalfD / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tO + g * kHalfD + cc * 32, rr);
+          tmem_wait_ld();
+          reg_fence(rr);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float o0, o1;
+            fmul2(o0, o1, __uint_as_float(rr[e]), __uint_as_float(rr[e + 1]), corr, corr);
+            rr[e] = __float_as_uint(o0);
+            rr[e + 1] = __float_as_uint(o1);
+          }
+          tmem_st32(tO + g * kHalfD + cc * 32, rr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) sy.p_ready();
+    }
+    if (!ok) break;
+
+    // ---- epilogue: this half's O columns / l -> I/O dtype -> global; L by half 0.
+    ok = sy.wait_o((blocks_seen - 1) & 1);
+    if (!ok) break;
+    tc_fence_after();
+    {  // the row sum of both halves (both P buffers are free: the last P V has completed)
+      const uint32_t tX = tmem + lane_addr + C::kColP;
+      tmem_st1(tX + x_put, __float_as_uint(l_run));
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      l_run += __uint_as_float(tmem_ld1(tX + x_get));
+      tmem_wait_ld();
+      // the next unit's first exchange may write these columns only after both halves read them
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+    }
+    const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+    const bool store = row < p.qL;
+    uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                    ((long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(store ? row : 0) * p.o_ss) * C::kEsz +
+                    g * kHalfD * C::kEsz;
+    constexpr int kBatch = kHalfD / 32 < 4 ? kHalfD / 32 : 4;
+#pragma unroll
+    for (int c0 = 0; c0 < kHalfD / 32; c0 += kBatch) {
+      uint32_t rb[kBatch][32];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) tmem_ld32(tO + g * kHalfD + (c0 + i) * 32, rb[i]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) reg_fence(rb[i]);
+      if (c0 + kBatch == kHalfD / 32) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) sy.o_free();
+      }
+      if (store) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + (c0 + i) * 64);
+#pragma unroll
+          for (int u4 = 0; u4 < 4; ++u4) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float a0, a1;
+              fmul2(a0, a1, __uint_as_float(rb[i][8 * u4 + 2 * e]), __uint_as_float(rb[i][8 * u4 + 2 * e + 1]),
+                    inv_l, inv_l);
+              pk[e] = pack16x2<C>(a0, a1);
+            }
+            dst[u4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
+      }
+    }
+    if (store && g == 0) {
+      const float lse = (l_run > 0.0f) ? (m_run + lg2(l_run)) * kLn2 : -INFINITY;
+      p.lse[((long long)b * p.Hq + h) * p.qL + row] = lse;
+    }
+  }
+}
+
+// The one-CTA plans' hand-offs for softmax_split_rows.
+template <class C>
+struct LocalSync {
+  Ctrl<C>* ctl;
+  const FaParams& p;
+  volatile int* abort;
+  int num_units;
+  __device__ bool next(int r, int& b, int& h, int& r0, int& j0, int& nb) {
+    const int u = unit_of(r, num_units);
+    if (u < 0) return false;
+    const Unit w = decode_unit<C>(p, u);
+    b = w.b;
+    h = w.th[0];
+    r0 = w.tr[0];
+    j0 = unit_j0<C>(w);
+    nb = w.nblk[0];
+    return true;
+  }
+  __device__ bool wait_s(uint32_t par) { return warp_wait(&ctl->s_full[0], par, abort, p.status, p.timeout_cycles); }
+  __device__ bool wait_m(uint32_t par) { return warp_wait(&ctl->m_full, par, abort, p.status, p.timeout_cycles); }
+  __device__ bool wait_o(uint32_t par) { return warp_wait(&ctl->o_ready[0], par, abort, p.status, p.timeout_cycles); }
+  __device__ void s_free() { mbar_arrive(&ctl->s_free[0]); }
+  __device__ void m_free() { mbar_arrive(&ctl->m_empty); }
+  __device__ void p_ready() { mbar_arrive(&ctl->p_ready[0]); }
+  __device__ void o_free() { mbar_arrive(&ctl->o_free[0]); }
+};
+
 // Persistent forward kernel: each CTA walks its units; every role carries its
 // barrier phase counters from one unit to the next, so the next unit's Q and
 // K/V loads and its first S MMAs overlap the current unit's last blocks and
@@ -731,10 +959,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&ctl->q_empty[t], 1);    // MMA commit after the unit's last S of tile t
       mbar_init(&ctl->q_ready[t], C::kCvtWarps);  // one arrival per tf32 helper warp
       mbar_init(&ctl->s_full[t], 1);
-      mbar_init(&ctl->s_free[t], 4);     // one arrival per softmax warp
-      mbar_init(&ctl->p_ready[t], 4);    // one arrival per softmax warp
+      mbar_init(&ctl->s_free[t], C::kSplitRows ? 8 : 4);   // one arrival per softmax warp
+      mbar_init(&ctl->p_ready[t], C::kSplitRows ? 8 : 4);  // one arrival per softmax warp
       mbar_init(&ctl->o_ready[t], 1);
-      mbar_init(&ctl->o_free[t], 4);     // one arrival per softmax warp after reading O
+      mbar_init(&ctl->o_free[t], C::kSplitRows ? 8 : 4);   // one arrival per softmax warp after reading O
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&ctl->k_full[s], 1);
@@ -748,7 +976,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     mbar_init(&ctl->drain[0], 1);
     mbar_init(&ctl->drain[1], 1);
     mbar_init(&ctl->m_full, 1);
-    mbar_init(&ctl->m_empty, 4);  // one arrival per softmax warp
+    mbar_init(&ctl->m_empty, C::kSplitRows ? 8 : 4);  // one arrival per softmax warp
     ctl->abort = 0;
     mbar_init(&ctl->turn_bar[0], 1);
     mbar_init(&ctl->turn_bar[1], 1);
@@ -1108,6 +1336,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // ===================================================== more tf32 helpers (one Q tile)
     if constexpr (C::kExtraHelpers)
       tf32_helpers<C>(sQ, sK, sV, sVT, ctl, p, abort_flag, num_units, 64 + (threadIdx.x - 256), lane);
+  } else if (C::kSplitRows) {
+    // ===================================================== two softmax warpgroups of one Q tile
+    if constexpr (C::kSplitRows) {
+      regs_inc<C::kRegsSoftmax>();
+      LocalSync<C> sy{ctl, p, abort_flag, num_units};
+      softmax_split_rows<C>(sy, sM, tmem, p, warp, lane);
+    }
   } else {
     // ===================================================== softmax warpgroup t
     if constexpr (C::kRegsSoftmax > 0) regs_inc<C::kRegsSoftmax>();

@@ -108,16 +108,10 @@ inline bool encode_vt(CUtensorMap* map, const void* ptr, int B, int H, int kL, i
   return true;
 }
 
+// The mask tensor map (when the mask suits TMA) and the kernel's parameter
+// block for instantiation C's tiling (its kBM, kNQT and element type).
 template <class C>
-int launch_fa_fwd(const LaunchArgs& a) {
-  CUtensorMap tq, tk, tv, tm;
-  if (!encode_bhsd(&tq, C::kTmaType, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
-  if (!encode_bhsd(&tk, C::kTmaType, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
-  if constexpr (C::kPre) {
-    if (!encode_vt(&tv, a.v, a.B, a.Hkv, a.kL, a.D, a.vt_row)) return 4;
-  } else {
-    if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
-  }
+void setup_params(const LaunchArgs& a, CUtensorMap& tm, FaParams& p) {
   // Mask tiles (128-byte column blocks x kBM rows, 128-byte swizzle) for the
   // L2 prefetch and the shared-memory mask path, when the mask's layout suits
   // TMA (aligned base, 16-byte multiple strides, no stride-0 broadcast).
@@ -148,7 +142,6 @@ int launch_fa_fwd(const LaunchArgs& a) {
     }
   }
 
-  FaParams p;
   p.B = a.B;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -206,7 +199,20 @@ int launch_fa_fwd(const LaunchArgs& a) {
   p.lse = a.lse;
   p.status = a.status;
   p.timeout_cycles = a.timeout_cycles;
+}
 
+template <class C>
+int launch_fa_fwd(const LaunchArgs& a) {
+  CUtensorMap tq, tk, tv, tm;
+  if (!encode_bhsd(&tq, C::kTmaType, a.q, a.B, a.Hq, a.qL, a.D, a.qs, C::kChunk, C::kBM)) return 4;
+  if (!encode_bhsd(&tk, C::kTmaType, a.k, a.B, a.Hkv, a.kL, a.D, a.ks, C::kChunk, C::kBN)) return 4;
+  if constexpr (C::kPre) {
+    if (!encode_vt(&tv, a.v, a.B, a.Hkv, a.kL, a.D, a.vt_row)) return 4;
+  } else {
+    if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
+  }
+  FaParams p;
+  setup_params<C>(a, tm, p);
   auto kern = fa_fwd_kernel<C>;
   static std::atomic<unsigned long long> configured{0};  // attributes set, per device (per instantiation)
   int dev = 0;

@@ -346,3 +346,23 @@ def test_persistent_many_units_per_cta(w, max_ctas, q_tiles):
     finally:
         fa.fa_set_max_ctas(0)
         fa.fa_set_q_tiles(0)
+
+
+# One Q tile per CTA (bf16 / fp16 at D = 256, and at D <= 128 for small grids) runs two softmax
+# warpgroups, each on 64 of a block's 128 keys: every D = 256 case with the grid capped (one and
+# three CTAs walking every unit), plus a causal GQA case with more units than SMs.
+D256 = [w for w in SMALL if w.D == 256 and w.dtype != "f32"] + [
+    S("bf16_d256_causal_gqa_units", 2, 4, 2, 700, 700, 256, "bf16", causal=True, seed=111),
+    S("f16_d256_additive_q_longer", 1, 2, 1, 520, 300, 256, "f16", mask_kind=W.MASK_ADDITIVE, seed=112),
+]
+
+
+@pytest.mark.parametrize("max_ctas", [0, 1, 3])
+@pytest.mark.parametrize("w", D256, ids=lambda w: w.name)
+def test_d256_split_rows(w, max_ctas):
+    import attention_forward_08_gb300 as fa
+    fa.fa_set_max_ctas(max_ctas)
+    try:
+        _run_small(w)
+    finally:
+        fa.fa_set_max_ctas(0)
