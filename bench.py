@@ -247,6 +247,24 @@ class ClockSampler:
     def mark(self, phase):
         self.phase = phase
 
+    def sample_now(self):
+        """One sample from the calling thread (NVML only), tagged with the current phase."""
+        if not self._nvml:
+            return
+        try:
+            smp = self._sample_nvml()
+            if smp is not None:
+                self.samples.append((self.phase, *smp))
+        except Exception:
+            pass
+
+    def sample_until(self, event, period=0.0002, limit=30.0):
+        """Sample every `period` seconds until the CUDA event has completed (the timed steps have run)."""
+        t0 = time.perf_counter()
+        while not event.query() and time.perf_counter() - t0 < limit:
+            self.sample_now()
+            time.sleep(period)
+
     def start(self):
         self._thread = threading.Thread(target=self._run, daemon=True)
         self._thread.start()
@@ -520,6 +538,7 @@ def run_ours(args, w):
         starts[i].record(stream)
         launch()
         ends[i].record(stream)
+    sampler.sample_until(ends[-1])  # clock samples while the timed steps run, however short they are
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - t_wall
@@ -698,6 +717,7 @@ def run_ours_bwd(args, w):
         starts[i].record(stream)
         launch()
         ends[i].record(stream)
+    sampler.sample_until(ends[-1])  # clock samples while the timed steps run, however short they are
     torch.cuda.synchronize(dev)
     barrier(world)
     wall = time.perf_counter() - t_wall
