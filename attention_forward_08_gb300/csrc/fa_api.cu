@@ -304,8 +304,14 @@ int validate_bwd(const fa_bwd_args* a) {
               a->dtype);
     return known ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
   }
-  if (a->D != 64 && a->D != 128) {
-    set_error("head dim D = %d is not supported by the backward pass (64 or 128)", a->D);
+  if (a->D != 64 && a->D != 128 && a->D != 256) {
+    set_error("head dim D = %d is not supported by the backward pass (64, 128 or 256)", a->D);
+    return FA_ERR_UNSUPPORTED;
+  }
+  if (a->D == 256 && (a->mask_kind != FA_MASK_NONE || a->dropout_p != 0.0f || a->window != 0 || a->q_offset != 0 ||
+                      a->softcap != 0.0f)) {
+    set_error("at D = 256 the backward pass takes causal or full attention only (no mask, window, q_offset, "
+              "softcap or dropout)");
     return FA_ERR_UNSUPPORTED;
   }
   if (a->mask_kind != FA_MASK_NONE && a->softcap != 0.0f) {

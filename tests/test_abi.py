@@ -242,7 +242,8 @@ def test_bwd_ex_rejects_workspace_without_room_for_the_keep_mask(fa):
     (dict(scale=float("nan")), 1, "finite"),
     (dict(dtype=0), 2, "bf16 and fp16"),
     (dict(dtype=5), 1, "dtype"),
-    (dict(D=256), 2, "head dim"),
+    (dict(D=96), 2, "head dim"),
+    (dict(D=512), 2, "head dim"),
     (dict(ws_bytes=100), 1, "workspace"),
     (dict(dk=P + 4), 3, "16-byte"),
 ])
@@ -319,6 +320,12 @@ def test_bwd_full_workspace_with_mask(fa):
     (dict(mask=P, mask_kind=2, softcap=5.0), 2, "softcap"),
     (dict(mask=P, mask_kind=2, workspace=P + 16), 3, "256-byte"),
     (dict(mask=P, mask_kind=2, workspace_bytes=1024), 1, "workspace"),
+    # head dim 256: causal or full attention only
+    (dict(D=256, mask=P, mask_kind=1), 2, "D = 256"),
+    (dict(D=256, window=64), 2, "D = 256"),
+    (dict(D=256, q_offset=100), 2, "D = 256"),
+    (dict(D=256, softcap=5.0), 2, "D = 256"),
+    (dict(D=256, dropout_p=0.1), 2, "D = 256"),
 ])
 def test_bwd_full_validation_rejects(fa, kw, status, needle):
     a = _bwd_args(fa, **kw)

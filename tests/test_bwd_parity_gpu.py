@@ -38,6 +38,16 @@ CASES = [
     S("bwd_f16_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "f16", causal=True, seed=41),
     S("bwd_f16_d64_ragged", 2, 2, 1, 200, 200, 64, "f16", causal=True, seed=42),
     S("bwd_f16_d128_plain_long_kv", 1, 2, 2, 130, 600, 128, "f16", seed=43),
+    # head dim 256 (causal or full attention): two CTAs per 128-key tile, 64-query steps; 64-key dQ blocks
+    S("bwd_d256_plain", 1, 2, 2, 256, 256, 256, "bf16", seed=44),
+    S("bwd_d256_causal_gqa", 1, 4, 2, 384, 384, 256, "bf16", causal=True, seed=45),
+    S("bwd_d256_causal_ragged", 2, 2, 1, 200, 200, 256, "bf16", causal=True, seed=46),
+    S("bwd_d256_causal_q_longer", 1, 2, 2, 300, 170, 256, "bf16", causal=True, seed=47),
+    S("bwd_d256_causal_k_longer", 1, 2, 1, 150, 420, 256, "bf16", causal=True, seed=48),
+    S("bwd_d256_plain_long_kv", 1, 2, 2, 130, 600, 256, "bf16", seed=49),
+    S("bwd_d256_tiny", 1, 1, 1, 5, 3, 256, "bf16", causal=True, seed=50),
+    S("bwd_f16_d256_causal_gqa", 1, 4, 2, 384, 384, 256, "f16", causal=True, seed=58),
+    S("bwd_f16_d256_plain_ragged", 1, 2, 1, 250, 333, 256, "f16", seed=59),
     # sliding window / causal diagonal offset (fa_bwd_ex)
     S("bwd_swa_d128_causal_gqa", 1, 4, 2, 640, 640, 128, "bf16", causal=True, window=200, seed=51),
     S("bwd_offset_d64_bottom_right", 1, 2, 1, 300, 560, 64, "bf16", causal=True, q_offset=260, seed=52),
@@ -183,6 +193,19 @@ def test_bwd_bench_workload_every_element():
     """Every element of dQ, dK and dV of the benchmarked backward against the gradient oracle
     (all 16 GQA groups, the oracle's threads one group each)."""
     w = BENCH_BWD
+    (q, k, v, do), (dq, dk, dv) = _gpu_bwd_full(w)
+    rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                      do.double().numpy(), fp32_scale(w), causal=True)
+    _compare(f"{w.name} dQ", dq, rq)
+    _compare(f"{w.name} dK", dk, rk)
+    _compare(f"{w.name} dV", dv, rv)
+
+
+def test_bwd_d256_multi_wave_every_element():
+    """Head dim 256 at the size of the D = 256 forward workload (B1, H_q 8, L 2000) with GQA 4:1 and
+    causal masking: 256 dK/dV CTAs (two per 128-key tile) and 128 dQ CTAs, each dK/dV CTA walking 4
+    heads x up to 32 query steps; every element against the gradient oracle."""
+    w = S("bwd_d256_causal_gqa_h8_l2000", 1, 8, 2, 2000, 2000, 256, "bf16", causal=True, seed=67)
     (q, k, v, do), (dq, dk, dv) = _gpu_bwd_full(w)
     rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
                                       do.double().numpy(), fp32_scale(w), causal=True)
