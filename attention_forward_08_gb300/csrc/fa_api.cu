@@ -297,12 +297,16 @@ int validate_bwd(const fa_bwd_args* a) {
         return FA_ERR_INVALID_ARGUMENT;
       }
   }
-  if (a->dtype != FA_DTYPE_BF16 && a->dtype != FA_DTYPE_F16) {
-    const bool known = a->dtype == FA_DTYPE_F32;
-    set_error(known ? "the backward pass supports bf16 and fp16 I/O only"
-                    : "dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)",
-              a->dtype);
-    return known ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARGUMENT;
+  if (a->dtype != FA_DTYPE_BF16 && a->dtype != FA_DTYPE_F16 && a->dtype != FA_DTYPE_F32) {
+    set_error("dtype %d is not FA_DTYPE_F32 (0), FA_DTYPE_BF16 (1) or FA_DTYPE_F16 (2)", a->dtype);
+    return FA_ERR_INVALID_ARGUMENT;
+  }
+  if (a->dtype == FA_DTYPE_F32 &&
+      (a->D == 256 || a->mask_kind != FA_MASK_NONE || a->dropout_p != 0.0f || a->window != 0 || a->q_offset != 0 ||
+       a->softcap != 0.0f)) {
+    set_error("with fp32 I/O the backward pass takes D = 64 or 128 and causal or full attention only (no mask, "
+              "window, q_offset, softcap or dropout)");
+    return FA_ERR_UNSUPPORTED;
   }
   if (a->D != 64 && a->D != 128 && a->D != 256) {
     set_error("head dim D = %d is not supported by the backward pass (64, 128 or 256)", a->D);
@@ -598,6 +602,8 @@ long long fa_bwd_full_workspace_bytes(const fa_bwd_args* a) {
   }
   if (validate_bwd(a) != FA_OK) return -1;
   const long long base = fa_bwd_ex_workspace_bytes(a->B, a->H_q, a->qL, a->kL, a->dropout_p);
+  if (a->dtype == FA_DTYPE_F32)
+    return align256_ll(base) + bwd_tf32_layout(a->B, a->H_q, a->H_kv, a->qL, a->kL, a->D).bytes;
   if (a->mask_kind == FA_MASK_NONE) return base;
   const int esz = a->mask_kind == FA_MASK_BOOL ? 1 : 2;
   return align256_ll(base) + align256_ll((long long)a->B * a->H_q * a->kL * mask_t_ld(a->qL) * esz);
@@ -646,6 +652,8 @@ int fa_bwd_full(const fa_bwd_args* args) {
   a.dv = x.dv;
   a.dvec = static_cast<float*>(x.workspace);
   a.f16 = x.dtype == FA_DTYPE_F16;
+  a.f32 = x.dtype == FA_DTYPE_F32;
+  a.t32_ws = a.f32 ? static_cast<char*>(x.workspace) + align256_ll(fa_bwd_workspace_bytes(x.B, x.H_q, x.qL)) : nullptr;
   a.B = x.B;
   a.Hq = x.H_q;
   a.Hkv = x.H_kv;
@@ -688,6 +696,10 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               int qL, int kL, int D, float scale, int causal, int window, int q_offset, float softcap,
               float dropout_p, unsigned long long dropout_seed, unsigned long long dropout_offset, int dtype,
               void* stream) {
+  if (dtype == FA_DTYPE_F32) {  // its workspace size depends on more than this entry's sizing function sees
+    fa::set_error("fa_bwd and fa_bwd_ex take bf16 and fp16 I/O; fp32 goes through fa_bwd_full");
+    return FA_ERR_UNSUPPORTED;
+  }
   fa_bwd_args a;
   std::memset(&a, 0, sizeof(a));
   a.q = q;
@@ -727,6 +739,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
                    causal, 0, 0, 0.0f, 0.0f, 0ull, 0ull, dtype, stream);
 }
 
-int fa_version(void) { return 109; }
+int fa_version(void) { return 110; }
 
 }  // extern "C"

@@ -144,17 +144,6 @@ __device__ __forceinline__ void bwd256_store_row(uint32_t tacc, float mul, uint1
   }
 }
 
-// Read 64 fp32 TMEM columns of this lane.
-__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&x)[64]) {
-  uint32_t rr[64];
-  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
-  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-  tmem_wait_ld();
-  reg_fence(rr);
-#pragma unroll
-  for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(rr[c]);
-}
-
 // ---------------------------------------------------------------- dK / dV
 
 // Grid: 2 CTAs (D halves) per (128-key tile, kvh, b), heavy (early) key tiles first.

@@ -285,6 +285,17 @@ __device__ __forceinline__ void bwd_mma_tmem_a(uint32_t dst, uint32_t a_tmem, ui
     mma_ts_lh<false, 1>(dst, a_tmem + kk * 8, b_lo + ((kk * C::kKStep * 128) >> 4), b_hi, idesc, 1u);
 }
 
+// Read 64 fp32 TMEM columns of this lane.
+__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&x)[64]) {
+  uint32_t rr[64];
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
+  tmem_wait_ld();
+  reg_fence(rr);
+#pragma unroll
+  for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(rr[c]);
+}
+
 // Read 128 fp32 TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
   uint32_t rr[128];

@@ -14,6 +14,8 @@ struct BwdLaunchArgs {
   const float* lse;                  // [B, H_q, qL]
   void *dq, *dk, *dv;                // outputs in the same format
   bool f16;                          // fp16 I/O instead of bf16
+  bool f32;                          // fp32 I/O (TF32 products)
+  void* t32_ws;                      // fp32: scratch for the rounded copies and transposes (BwdTf32Layout)
   float* dvec;                       // [B, H_q, qL] scratch for D = rowsum(O * dO)
   int B, Hq, Hkv, qL, kL, D;
   float scale;
@@ -35,6 +37,33 @@ struct BwdLaunchArgs {
   unsigned int* status;
   long long timeout_cycles;
 };
+
+// fp32 backward scratch (after the D vector; every part 256-byte aligned):
+// tf32-rounded copies of Q, dO [B, H_q, qL, D] and K, V [B, H_kv, kL, D],
+// then tf32-rounded transposes Q^T, dO^T [B, H_q, D, qt_row] and
+// K^T [B, H_kv, D, kt_row], rows rounded up to 4 entries (16 bytes).
+struct BwdTf32Layout {
+  long long qr, dor, kr, vr, qt, dot, kt;  // byte offsets
+  long long qt_row, kt_row;
+  long long bytes;
+};
+inline BwdTf32Layout bwd_tf32_layout(int B, int Hq, int Hkv, int qL, int kL, int D) {
+  auto al = [](long long n) { return (n + 255) / 256 * 256; };
+  BwdTf32Layout l;
+  l.qt_row = ((long long)qL + 3) / 4 * 4;
+  l.kt_row = ((long long)kL + 3) / 4 * 4;
+  const long long nq = al((long long)B * Hq * qL * D * 4), nk = al((long long)B * Hkv * kL * D * 4);
+  const long long nqt = al((long long)B * Hq * D * l.qt_row * 4), nkt = al((long long)B * Hkv * D * l.kt_row * 4);
+  l.qr = 0;
+  l.dor = l.qr + nq;
+  l.kr = l.dor + nq;
+  l.vr = l.kr + nk;
+  l.qt = l.vr + nk;
+  l.dot = l.qt + nqt;
+  l.kt = l.dot + nqt;
+  l.bytes = l.kt + nkt;
+  return l;
+}
 
 // Launches the D pre-pass, the dK/dV kernel and the dQ kernel on a.stream.
 // Returns 0, or an fa_status code with the message set.

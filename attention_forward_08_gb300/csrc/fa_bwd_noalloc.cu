@@ -59,6 +59,10 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   chk.dtype = dtype;
   int rc = fa::validate_bwd(&chk);
   if (rc != FA_OK) return rc;
+  if (dtype == FA_DTYPE_F32) {  // the fp32 plans need a workspace for their rounded copies
+    fa::set_error("fa_bwd_noalloc takes bf16 and fp16 I/O; fp32 goes through fa_bwd_full");
+    return FA_ERR_UNSUPPORTED;
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {

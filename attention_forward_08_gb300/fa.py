@@ -362,8 +362,9 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
     mask_kind: the forward's (``attention``), so that the backward sees the
     same softmax and regenerates the same keep decisions.
 
-    q, o, dout: contiguous bf16 or fp16 [B, H_q, qL, D]; k, v: the same dtype,
-    [B, H_kv, kL, D]; lse: the forward's contiguous fp32 [B, H_q, qL].
+    q, o, dout: contiguous bf16, fp16 or fp32 [B, H_q, qL, D]; k, v: the same
+    dtype, [B, H_kv, kL, D]; lse: the forward's contiguous fp32 [B, H_q, qL].
+    fp32 (TF32 products) takes D 64 or 128 and causal or full attention only.
     mask: None, bool/uint8 (nonzero keeps) or additive in q's dtype,
     broadcastable to [B, H_q, qL, kL] through its strides.
     workspace: optional device tensor of at least ``fa_bwd_full_workspace_bytes``
@@ -384,8 +385,8 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
         if name != "lse" and t.dtype != q.dtype:
             raise ValueError(f"{name} must have q's dtype {q.dtype}")
-    if q.dtype not in (torch.bfloat16, torch.float16):
-        raise ValueError("the backward pass supports bfloat16 and float16 I/O")
+    if q.dtype not in (torch.bfloat16, torch.float16, torch.float32):
+        raise ValueError("the backward pass supports bfloat16, float16 and float32 I/O")
     if dq is None:
         dq = torch.empty_like(q)
     if dk is None:
@@ -408,7 +409,7 @@ def attention_bwd(q, k, v, o, dout, lse, *, scale=None, causal=False, dq=None, d
     a.window, a.q_offset, a.softcap = int(window), int(q_offset), float(softcap)
     a.dropout_p = float(dropout_p)
     a.dropout_seed, a.dropout_offset = int(dropout_seed) & (2**64 - 1), int(dropout_offset) & (2**64 - 1)
-    a.dtype = FA_DTYPE_F16 if q.dtype == torch.float16 else FA_DTYPE_BF16
+    a.dtype = {torch.float16: FA_DTYPE_F16, torch.float32: FA_DTYPE_F32}.get(q.dtype, FA_DTYPE_BF16)
     if mask is None:
         a.mask, a.mask_kind = None, FA_MASK_NONE
     else:

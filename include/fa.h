@@ -213,8 +213,10 @@ long long fa_bwd_workspace_bytes(int B, int H_q, int qL);
  * gradients).  o is the forward's output.  workspace: caller-owned device
  * memory of at least fa_bwd_workspace_bytes(B, H_q, qL) bytes, 16-byte
  * aligned; its contents on entry do not matter and are clobbered.  D must be
- * 64 or 128 (else FA_ERR_UNSUPPORTED); no mask (masked training is not
- * supported by this entry point).  dq, dk, dv are written in full (rows no
+ * 64, 128 or 256 (else FA_ERR_UNSUPPORTED); no mask here (fa_bwd_full takes
+ * one).  At D = 256 the backward takes causal or full attention only: the
+ * window, offset, softcap, dropout and mask of fa_bwd_ex and fa_bwd_full
+ * return FA_ERR_UNSUPPORTED there.  dq, dk, dv are written in full (rows no
  * query or key reaches get zeros) and must not overlap any input or each
  * other.  Asynchronous on `stream`: three kernel launches (D pre-pass, dK/dV,
  * dQ); validation and errors as for fa_fwd.
@@ -333,7 +335,8 @@ long long fa_bwd_full_workspace_bytes(const fa_bwd_args* args);
 /* ABI version: major * 100 + minor (1.05: fa_bwd and fa_bwd_noalloc accept
  * FA_DTYPE_F16; 1.06: fa_fwd_args.workspace, fa_fwd_workspace_bytes; 1.07:
  * fa_bwd_ex; 1.08: fa_bwd_ex takes the forward's dropout arguments,
- * fa_bwd_ex_workspace_bytes; 1.09: fa_bwd_args, fa_bwd_full with masks). */
+ * fa_bwd_ex_workspace_bytes; 1.09: fa_bwd_args, fa_bwd_full with masks;
+ * 1.10: the backward at D = 256). */
 int fa_version(void);
 
 #ifdef __cplusplus

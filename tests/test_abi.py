@@ -65,7 +65,7 @@ def test_args_struct_matches_header(tmp_path, cname, pyname):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 109
+    assert fa.fa_version() == 110
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it
@@ -312,6 +312,25 @@ def test_bwd_full_workspace_with_mask(fa):
     assert fa.fa.fa_bwd_full_workspace_bytes(a) == al(base) + al(1 * 2 * 300 * 256 * 1)
 
 
+def test_bwd_full_workspace_fp32(fa):
+    """fp32: the D vector, then tf32-rounded Q, dO, K, V and the transposes Q^T, dO^T [B, H_q, D, qL
+    rounded up to 4] and K^T [B, H_kv, D, kL rounded up to 4], each part 256-byte aligned."""
+    al = lambda n: (n + 255) // 256 * 256
+    a = _bwd_args(fa, dtype=0, qL=201, kL=299, D=64)
+    qt, kt = (201 + 3) // 4 * 4, (299 + 3) // 4 * 4
+    expect = (al(al(1 * 2 * 201 * 4)) + 2 * al(1 * 2 * 201 * 64 * 4) + 2 * al(1 * 2 * 299 * 64 * 4)
+              + 2 * al(1 * 2 * 64 * qt * 4) + al(1 * 2 * 64 * kt * 4))
+    assert fa.fa.fa_bwd_full_workspace_bytes(a) == expect
+    a.workspace_bytes = expect - 1
+    assert fa.fa.fa_bwd_full(a) == 1 and "workspace" in fa.fa_last_error()
+
+
+def test_bwd_entries_without_full_workspace_refuse_fp32(fa):
+    assert _bwd_call(fa, dtype=0) == 2 and "fa_bwd_full" in fa.fa_last_error()
+    assert fa.fa.fa_bwd_noalloc(P, P, P, P, P, P, P, P, P, 1, 2, 2, 128, 128, 64, 0.125, 1, 0, None) == 2
+    assert "fa_bwd_full" in fa.fa_last_error()
+
+
 @pytest.mark.parametrize("kw,status,needle", [
     (dict(mask=P, mask_kind=0), 1, "mask must be non-NULL"),
     (dict(mask=None, mask_kind=2), 1, "mask must be non-NULL"),
@@ -320,6 +339,12 @@ def test_bwd_full_workspace_with_mask(fa):
     (dict(mask=P, mask_kind=2, softcap=5.0), 2, "softcap"),
     (dict(mask=P, mask_kind=2, workspace=P + 16), 3, "256-byte"),
     (dict(mask=P, mask_kind=2, workspace_bytes=1024), 1, "workspace"),
+    # fp32: D 64 or 128, causal or full attention only
+    (dict(dtype=0, D=256), 2, "fp32"),
+    (dict(dtype=0, window=64), 2, "fp32"),
+    (dict(dtype=0, mask=P, mask_kind=1), 2, "fp32"),
+    (dict(dtype=0, dropout_p=0.1), 2, "fp32"),
+    (dict(dtype=7), 1, "dtype"),
     # head dim 256: causal or full attention only
     (dict(D=256, mask=P, mask_kind=1), 2, "D = 256"),
     (dict(D=256, window=64), 2, "D = 256"),

@@ -10,7 +10,8 @@ each) before the dV, dK and dQ products, the inputs and the stored results
 are bf16, and accumulation is fp32; the resulting error is a few 2^-9 of the
 tensor's scale, well inside 2e-2.  fp16 I/O (P and dS rounded to fp16,
 relative error <= 2^-11) gets a quarter of that bound, 5e-3, as the forward's
-fp16 tolerance does.  With dropout the backward regenerates the forward's
+fp16 tolerance does; so does fp32 I/O, whose products run on the TF32 tensor cores (inputs, P and dS
+rounded to tf32, relative error <= 2^-11 each; accumulation and outputs fp32).  With dropout the backward regenerates the forward's
 keep decisions from the same seed and offset; the oracle takes its
 multipliers from the forward oracle's generator, so a backward that drew
 other bits than the forward fails the comparison.
@@ -48,6 +49,15 @@ CASES = [
     S("bwd_d256_tiny", 1, 1, 1, 5, 3, 256, "bf16", causal=True, seed=50),
     S("bwd_f16_d256_causal_gqa", 1, 4, 2, 384, 384, 256, "f16", causal=True, seed=58),
     S("bwd_f16_d256_plain_ragged", 1, 2, 1, 250, 333, 256, "f16", seed=59),
+    # fp32 I/O on the TF32 tensor cores (fa_bwd_full): separate dV, dK and dQ kernels
+    S("bwd_f32_d64_plain", 1, 2, 2, 128, 128, 64, "f32", seed=81),
+    S("bwd_f32_d64_causal_ragged", 2, 2, 1, 200, 200, 64, "f32", causal=True, seed=82),
+    S("bwd_f32_d128_causal_gqa", 1, 4, 2, 384, 384, 128, "f32", causal=True, seed=83),
+    S("bwd_f32_d128_plain_long_kv", 1, 2, 2, 130, 600, 128, "f32", seed=84),
+    S("bwd_f32_d128_causal_k_longer", 1, 2, 1, 150, 420, 128, "f32", causal=True, seed=85),
+    S("bwd_f32_d128_causal_q_longer", 1, 2, 2, 300, 170, 128, "f32", causal=True, seed=86),
+    S("bwd_f32_d64_tiny", 1, 1, 1, 5, 3, 64, "f32", causal=True, seed=87),
+    S("bwd_f32_d64_gqa8_noncausal", 1, 8, 1, 256, 333, 64, "f32", seed=88),
     # sliding window / causal diagonal offset (fa_bwd_ex)
     S("bwd_swa_d128_causal_gqa", 1, 4, 2, 640, 640, 128, "bf16", causal=True, window=200, seed=51),
     S("bwd_offset_d64_bottom_right", 1, 2, 1, 300, 560, 64, "bf16", causal=True, q_offset=260, seed=52),
@@ -72,7 +82,7 @@ CASES = [
 ]
 SOFTCAP_SCALE = 0.35  # scale * |q.k| ~ 0.35 * sqrt(D) * N(0, 1): several times the cap
 
-REL_TOL = {"bf16": 2e-2, "f16": 5e-3}
+REL_TOL = {"bf16": 2e-2, "f16": 5e-3, "f32": 5e-3}
 COS_MIN = 0.999
 
 
@@ -199,6 +209,19 @@ def test_bwd_bench_workload_every_element():
     _compare(f"{w.name} dQ", dq, rq)
     _compare(f"{w.name} dK", dk, rk)
     _compare(f"{w.name} dV", dv, rv)
+
+
+def test_bwd_f32_dit_workload_every_element():
+    """fp32 at the size of the fp32 DiT joint-attention forward workload (B1, H 24, L 4608, D 128,
+    non-causal): 864 CTAs in each of the dV, dK and dQ kernels, 72 steps per CTA; every element
+    against the gradient oracle."""
+    w = S("bwd_f32_dit_h24_l4608_d128", 1, 24, 24, 4608, 4608, 128, "f32", seed=89)
+    (q, k, v, do), (dq, dk, dv) = _gpu_bwd_full(w)
+    rq, rk, rv = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                      do.double().numpy(), fp32_scale(w), causal=False)
+    _compare(f"{w.name} dQ", dq, rq, REL_TOL["f32"])
+    _compare(f"{w.name} dK", dk, rk, REL_TOL["f32"])
+    _compare(f"{w.name} dV", dv, rv, REL_TOL["f32"])
 
 
 def test_bwd_d256_multi_wave_every_element():
