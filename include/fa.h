@@ -292,11 +292,23 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  *     P_ij = exp(scale q_i.k_j + m_ij - L_i), 0 where the key is excluded, so
  *     excluded keys and rows without any allowed key get zero gradient.  A
  *     mask together with a softcap is FA_ERR_UNSUPPORTED.
+ *   dtype FA_DTYPE_F32 -- fp32 inputs and gradients, the products on the
+ *     TF32 tensor cores (inputs, P and dS rounded to tf32, accumulation in
+ *     fp32), following forge "flash_attention_mma.metal", section "backward
+ *     (MMA)" (an fp32 backward with separate dQ, dV and dK kernels).  D 64 or
+ *     128, causal or full attention, GQA; a mask, window, q_offset, softcap
+ *     or dropout with fp32 is FA_ERR_UNSUPPORTED.  Only this entry point takes
+ *     fp32 (fa_bwd, fa_bwd_ex and fa_bwd_noalloc return FA_ERR_UNSUPPORTED).
  * Scratch: fa_bwd_full_workspace_bytes(args) bytes, 256-byte aligned: the
  * D vector, the dropout keep decisions (dropout_p > 0) and, with a mask, a
  * key-major copy of the mask for the key-parallel kernel (B * H_q * kL *
  * ceil(qL / 128) * 128 elements), each part starting on a 256-byte boundary;
- * a fifth launch writes that copy.  Results and errors otherwise as fa_bwd_ex.
+ * a fifth launch writes that copy.  fp32: after the D vector, tf32-rounded
+ * copies of q, dout [B,H_q,qL,D] and k, v [B,H_kv,kL,D], then the rounded
+ * transposes of q and dout [B,H_q,D,ceil(qL/4)*4] and of k
+ * [B,H_kv,D,ceil(kL/4)*4] (each part 256-byte aligned; eight pre-pass
+ * launches, then the dV, dK and dQ kernels).  Results and errors otherwise as
+ * fa_bwd_ex.
  */
 typedef struct fa_bwd_args {
   const void* q;
