@@ -157,8 +157,17 @@ struct Cfg {
   static constexpr bool kDropSmem = kDrop && !kTf32;
   static constexpr uint32_t kDropBytes = kDropSmem ? kNQT * kBM * (kBN / 8) : 0;
   static constexpr uint32_t kOffDrop = kOffM + kMaskSlotBytes;
-  static constexpr uint32_t kOffBar = kOffDrop + kDropBytes;
   static constexpr uint32_t kBarBytes = 512;
+  // Two-tile 16-bit plans: each softmax warp stages its 32 rows of O, one
+  // 128-byte column block at a time (4 KB), in shared memory, so the global
+  // stores of the epilogue write whole 128-byte lines (four rows per warp
+  // instruction) instead of 16 bytes of 32 different rows.  Only where the
+  // 32 KB fit.
+  static constexpr uint32_t kOStageBytes = 8 * 32 * 128;
+  static constexpr bool kOStage =
+      kAliasP && !kTf32 && 1024 + kOffDrop + kDropBytes + kOStageBytes + kBarBytes <= 232448;
+  static constexpr uint32_t kOffOStage = kOffDrop + kDropBytes;
+  static constexpr uint32_t kOffBar = kOffOStage + (kOStage ? kOStageBytes : 0);
   static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 
   static_assert(kD % kChunk == 0, "head dim must be a whole number of 128-byte rows");
@@ -1525,6 +1534,43 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->o_free[t]);
         }
+        if constexpr (C::kOStage) {
+          // Through this warp's staging slot, one 128-byte column block (64
+          // columns) at a time: each lane writes its row's eight 16-byte pieces
+          // (piece k of row r at r * 128 + (k ^ (r & 7)) * 16: conflict-free),
+          // then each group of 8 lanes reads one row back and stores it whole.
+          uint8_t* slot = smem + C::kOffOStage + (warp - 4) * (32 * 128);
+          uint8_t* obase = static_cast<uint8_t*>(p.o) + ((long long)b * p.o_sb + (long long)h * p.o_sh) * C::kEsz;
+          const long long row_bytes = p.o_ss * C::kEsz;
+          const int wrow0 = row - lane;  // the warp's first row
+#pragma unroll
+          for (int hh = 0; hh < kBatch / 2; ++hh) {
+            const int blk = c0 / 2 + hh;  // 128-byte column block of the row
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t(&rr)[32] = rb[2 * hh + k / 4];
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float a0, a1;
+                fmul2(a0, a1, __uint_as_float(rr[(k % 4) * 8 + 2 * e]), __uint_as_float(rr[(k % 4) * 8 + 2 * e + 1]),
+                      inv_l, inv_l);
+                pk[e] = pack16x2<C>(a0, a1);
+              }
+              *reinterpret_cast<uint4*>(slot + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int lr = 4 * i + (lane >> 3), k = lane & 7;
+              const uint4 v = *reinterpret_cast<const uint4*>(slot + lr * 128 + ((k ^ (lr & 7)) << 4));
+              if (wrow0 + lr < p.qL)
+                *reinterpret_cast<uint4*>(obase + (long long)(wrow0 + lr) * row_bytes + blk * 128 + k * 16) = v;
+            }
+            __syncwarp();  // the slot is rewritten for the next column block
+          }
+        } else {
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
           const int cc = c0 + i;
@@ -1555,6 +1601,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               }
             }
           }
+        }
         }
       }
       if (store) {
