@@ -16,8 +16,10 @@ and device->host copies of O and L are all inside the timed region.
 bounded sample of query rows of the same workload.
 ``--impl reference`` times that oracle alone (the CPU reference arm).
 
-``--pass bwd`` measures the backward instead: a step is one ``fa_bwd`` call
-(D pre-pass, dK/dV kernel, dQ kernel) on the forward's own O and L, and
+``--pass bwd`` measures the backward instead: a step is one ``fa_bwd_full``
+call (D pre-pass, dK/dV kernel, dQ kernel, plus the keep-mask and mask
+pre-passes where the workload has dropout or a mask, or the tf32 copies and
+separate dV, dK, dQ kernels for fp32) on the forward's own O and L, and
 ``value`` is TFLOP/s = 2.5x the forward's count (the five products of the
 FA-2 backward) / mean call time; its ``cpu_baseline`` times the fp64
 gradient oracle on whole GQA groups of the same workload.
@@ -407,15 +409,15 @@ def run_reference_bwd(args, w):
     """The reference arm of ``--pass bwd``: the fp64 gradient oracle, timed on a bounded sample of
     the workload each step (``oracle_bwd_sample``), on the backward's metric."""
     check_bwd_workload(w)
-    q, k, v = workloads.make_qkv(w)
+    q, k, v, m = workloads.make_inputs(w)
     do = workloads.make_dout(w)
     per_step = max(2.0, min(15.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_bwd_sample(w, q, k, v, do, per_step / 4)
+        oracle_bwd_sample(w, q, k, v, do, per_step / 4, m)
     flops = secs = 0.0
     threads, sample = 1, ""
     for _ in range(args.steps):
-        f, dt, sample, threads = oracle_bwd_sample(w, q, k, v, do, per_step)
+        f, dt, sample, threads = oracle_bwd_sample(w, q, k, v, do, per_step, m)
         flops += f
         secs += dt
     value = flops / secs / 1e12
@@ -424,7 +426,7 @@ def run_reference_bwd(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(config_of(w, args), **{"pass": "bwd"}),
+        "config": dict(config_of(w, args), **{"pass": "bwd", "layout": "BHSD"}),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"per step: {sample}, fp64 C gradient oracle"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -627,7 +629,7 @@ def run_ours(args, w):
     return 0
 
 
-def oracle_bwd_sample(w, q, k, v, do, seconds):
+def oracle_bwd_sample(w, q, k, v, do, seconds, m=None):
     """Time the fp64 gradient oracle on a bounded sample of the workload: whole GQA groups of batch
     0 (as many kv heads as host threads), on the leading Ls positions of the sequence, Ls grown from
     256 until one run takes about `seconds`."""
@@ -642,8 +644,13 @@ def oracle_bwd_sample(w, q, k, v, do, seconds):
         qs = q[:1, :n_kv * group, :Ls].double().numpy()
         ks, vs = k[:1, :n_kv, :Ls].double().numpy(), v[:1, :n_kv, :Ls].double().numpy()
         dos = do[:1, :n_kv * group, :Ls].double().numpy()
+        mk = {}
+        if m is not None:
+            ms = m.expand(w.B, w.H_q, w.qL, w.kL)[:1, :n_kv * group, :Ls, :Ls]
+            mk = dict(mask=(ms.numpy().astype(np.uint8) if w.mask_kind == 1 else ms.double().numpy()),
+                      mask_kind=w.mask_kind)
         t0 = time.perf_counter()
-        oracle.attention_bwd(qs, ks, vs, dos, float(np.float32(w.sm_scale)), causal=w.causal, n_threads=threads,
+        oracle.attention_bwd(qs, ks, vs, dos, float(np.float32(w.sm_scale)), causal=w.causal, n_threads=threads, **mk,
                              window=w.window, q_offset=w.q_offset, softcap=float(np.float32(w.softcap)),
                              dropout_p=float(np.float32(w.dropout_p)), seed=w.dropout_seed, offset=w.dropout_offset)
         return time.perf_counter() - t0
@@ -658,8 +665,42 @@ def oracle_bwd_sample(w, q, k, v, do, seconds):
 
 
 def check_bwd_workload(w):
-    if w.dtype not in ("bf16", "f16") or w.mask_kind != 0 or w.layout != "bhsd" or w.D not in (64, 128):
-        raise SystemExit(f"--pass bwd needs an unmasked bf16 or fp16 BHSD workload with D 64 or 128 ({w.name})")
+    """The backward's scope: bf16 / fp16 at D 64 and 128 with every forward option (a mask not with a
+    softcap); D 256 and fp32 (D 64, 128) with causal or full attention only."""
+    feats = w.window or w.q_offset or w.softcap or w.dropout_p
+    if w.dtype == "f32":
+        ok = w.D in (64, 128) and not feats and w.mask_kind == 0
+    elif w.D == 256:
+        ok = not feats and w.mask_kind == 0
+    else:
+        ok = w.D in (64, 128) and not (w.mask_kind and w.softcap)
+    if not ok:
+        raise SystemExit(f"--pass bwd does not cover this workload ({w.name}): bf16/fp16 D 64 or 128 with any "
+                         "forward option, D 256 and fp32 D 64 or 128 without a mask, window, offset, softcap or "
+                         "dropout")
+
+
+def bwd_args(fa, w, ptrs, mask, stream_handle):
+    """fa_bwd_args for one call: ptrs = q, k, v, o, dout, lse, dq, dk, dv (device addresses)."""
+    a = fa.FaBwdArgs()
+    a.q, a.k, a.v, a.o, a.dout, a.lse, a.dq, a.dk, a.dv = ptrs
+    a.B, a.H_q, a.H_kv, a.qL, a.kL, a.D = w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D
+    a.scale, a.causal = w.sm_scale, int(w.causal)
+    a.window, a.q_offset, a.softcap = w.window, w.q_offset, w.softcap
+    a.dropout_p, a.dropout_seed, a.dropout_offset = w.dropout_p, w.dropout_seed, w.dropout_offset
+    a.dtype = {"f16": fa.FA_DTYPE_F16, "f32": fa.FA_DTYPE_F32}.get(w.dtype, fa.FA_DTYPE_BF16)
+    if mask is not None:
+        a.mask, a.mask_kind = mask.data_ptr(), w.mask_kind
+        a.mask_strides[:] = (mask.stride(0), mask.stride(1), mask.stride(2))
+    a.stream = stream_handle
+    return a
+
+
+def bwd_launches(w) -> int:
+    """Kernel launches of one backward call."""
+    if w.dtype == "f32":
+        return 11  # row-dot, four tf32 copies, three transposes, dV, dK, dQ
+    return 3 + (1 if w.dropout_p else 0) + (1 if w.mask_kind else 0)
 
 
 def run_ours_bwd(args, w):
@@ -674,23 +715,26 @@ def run_ours_bwd(args, w):
     import attention_forward_08_gb300 as fa
     fa.load_library()
     check_bwd_workload(w)
-    q, k, v = workloads.make_qkv(w)
+    q, k, v, m = workloads.make_inputs(w)
     do = workloads.make_dout(w)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    md = None if m is None else m.to(dev)
+    # the forward's O in BHSD (the DiT workload's token-major O is a forward output layout)
     od, lsed = fa.attention(qd, kd, vd, scale=w.sm_scale, causal=w.causal, window=w.window, q_offset=w.q_offset,
                             softcap=w.softcap, dropout_p=w.dropout_p, dropout_seed=w.dropout_seed,
-                            dropout_offset=w.dropout_offset)
+                            dropout_offset=w.dropout_offset, mask=md, mask_kind=w.mask_kind or None)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws_bytes = fa.fa_bwd_ex_workspace_bytes(w.B, w.H_q, w.qL, w.kL, w.dropout_p)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ptrs = [t.data_ptr() for t in (qd, kd, vd, od, dod, lsed, dq, dk, dv, ws)]
+    args_c = bwd_args(fa, w, [t.data_ptr() for t in (qd, kd, vd, od, dod, lsed, dq, dk, dv)], md, stream.cuda_stream)
+    ws_bytes = fa.fa_bwd_full_workspace_bytes(args_c)
+    if ws_bytes < 0:
+        raise fa.FaError(fa.FA_ERR_INVALID_ARGUMENT, fa.fa_last_error())
+    ws = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
+    args_c.workspace, args_c.workspace_bytes = (ws.data_ptr() + 255) // 256 * 256, ws_bytes
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def launch():
-        rc = fa.fa_bwd_ex(*ptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal, w.window,
-                          w.q_offset, w.softcap, w.dropout_p, w.dropout_seed, w.dropout_offset, fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16,
-                          stream.cuda_stream)
+        rc = fa.fa_bwd_full(args_c)
         if rc != 0:
             raise fa.FaError(rc, fa.fa_last_error())
 
@@ -737,13 +781,13 @@ def run_ours_bwd(args, w):
     def make_set():
         din = [torch.empty_like(t) for t in (qd, kd, vd, od, dod, lsed)]
         dout = [torch.empty_like(t) for t in (qd, kd, vd)]
-        sws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        sptrs = [t.data_ptr() for t in din] + [t.data_ptr() for t in dout] + [sws.data_ptr()]
+        sws = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
+        sptrs = [t.data_ptr() for t in din] + [t.data_ptr() for t in dout]
 
         def launch_on(stream_handle, sptrs=sptrs, sws=sws):
-            rc = fa.fa_bwd_ex(*sptrs, ws_bytes, w.B, w.H_q, w.H_kv, w.qL, w.kL, w.D, w.sm_scale, w.causal,
-                              w.window, w.q_offset, w.softcap, w.dropout_p, w.dropout_seed, w.dropout_offset,
-                              fa.FA_DTYPE_F16 if w.dtype == "f16" else fa.FA_DTYPE_BF16, stream_handle)
+            a = bwd_args(fa, w, sptrs, md, stream_handle)  # the mask stays resident, as the bench's K/V would not
+            a.workspace, a.workspace_bytes = (sws.data_ptr() + 255) // 256 * 256, ws_bytes
+            rc = fa.fa_bwd_full(a)
             if rc != 0:
                 raise fa.FaError(rc, fa.fa_last_error())
         return din, dout, [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dout], launch_on
@@ -754,28 +798,30 @@ def run_ours_bwd(args, w):
     e2e_ms = max_over_ranks(pipe.time_ms(e_steps, 3, dev, world), world, dev)
 
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops"]
+    peak = peak_for(w, peaks)
     clocks = clocks_record(sampler)
     line = {
         "metric": "attention bwd TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_of(w, argparse.Namespace(gpus=world)), **{"pass": "bwd"}),
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": dict(config_of(w, argparse.Namespace(gpus=world)), **{"pass": "bwd", "layout": "BHSD"}),
         "roofline": {"bound": "tensor", "achieved": flops / (mean_ms * 1e-3) / 1e12, "peak": peak,
                      "unit": "TFLOP/s", "frac": flops / (mean_ms * 1e-3) / 1e12 / peak,
                      "traffic": traffic_from_profiles(w, "bwd"),
-                     "peak_source": f"{peak_src} bf16 dense (burst)",
-                     "kernels": "one fa_bwd_ex call: D pre-pass + " + ("keep-mask pre-pass + " if w.dropout_p else "")
-                                + "dK/dV + dQ"},
+                     "peak_source": f"{peak_src} bf16 dense (burst)" + (", x0.5 for TF32" if w.dtype == "f32" else ""),
+                     "kernels": "one fa_bwd_full call: D pre-pass + "
+                                + ("tf32 copies and transposes + dV + dK + dQ" if w.dtype == "f32" else
+                                   ("keep-mask pre-pass + " if w.dropout_p else "")
+                                   + ("mask transpose + " if w.mask_kind else "") + "dK/dV + dQ")},
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "clocks": clocks,
-        "gpu_launches": (4 if w.dropout_p else 3) * args.steps,
+        "gpu_launches": bwd_launches(w) * args.steps,
         "timed_region_s": wall,
         "call_ms": {"min": min(call_ms), "median": statistics.median(call_ms), "max": max(call_ms)},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        f, dt, what, threads = oracle_bwd_sample(w, q, k, v, do, args.cpu_seconds)
+        f, dt, what, threads = oracle_bwd_sample(w, q, k, v, do, args.cpu_seconds, m)
         line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{what} ({dt:.1f} s, fp64 C gradient oracle, {threads} threads)"}
     if rank == 0:

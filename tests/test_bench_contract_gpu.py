@@ -37,3 +37,22 @@ def test_default_bench_line_has_the_contract_keys():
     clk = line["clocks"]
     assert clk["window"] == "timed steps only" and clk["samples"] >= 1, clk
     assert clk["sm_mhz"] is not None and clk["soak"]["samples"] >= 1, clk
+
+
+@pytest.mark.parametrize("workload,dtype,launches", [
+    ("bf16_h8_l2000_d256", "bf16", 3),            # head dim 256
+    ("fp32_b1_h2_l128_d64", "f32", 11),           # fp32 on the TF32 tensor cores
+    ("bf16_bool_mask_h8_l2000_d128", "bf16", 4),  # the forward's mask (one more pre-pass)
+])
+def test_bwd_bench_lines(workload, dtype, launches):
+    res = subprocess.run([sys.executable, "bench.py", "--pass", "bwd", "--workload", workload, "--steps", "3",
+                          "--warmup", "3", "--cpu-seconds", "1"], cwd=ROOT, capture_output=True, text=True,
+                         timeout=900)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["metric"] == "attention bwd TFLOP/s" and line["dtype"] == dtype
+    assert line["config"]["workload"] == workload and line["config"]["pass"] == "bwd"
+    assert line["value"] > 0 and line["gpu_launches"] == launches * line["steps"]
+    r = line["roofline"]
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9 and 0.0 < r["frac"] < 1.5
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] > 0

@@ -14,6 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 @pytest.mark.parametrize("pass_,workload,metric", [
     ("fwd", "fp32_b1_h2_l128_d64", "attention fwd TFLOP/s"),
     ("bwd", "bf16_causal_b4_h8_l1024_d64", "attention bwd TFLOP/s"),
+    ("bwd", "bf16_bool_mask_h8_l2000_d128", "attention bwd TFLOP/s"),
 ])
 def test_reference_line(pass_, workload, metric):
     res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--pass", pass_, "--workload", workload,

@@ -92,7 +92,8 @@ WORKLOADS = {
 BENCH_WORKLOAD = "bf16_gqa_causal_b2_hq32_hkv8_l4096_d128"
 
 # Beyond the pages' workloads: the bench workload with fp16 I/O, with a
-# 1024-key sliding window, with a softcap of 20, and with dropout 0.1 (same seeds).
+# 1024-key sliding window, with a softcap of 20, and with dropout 0.1 (same seeds);
+# two backward shapes.
 EXTRA_WORKLOADS = {
     "f16_gqa_causal_b2_hq32_hkv8_l4096_d128": Workload(
         "f16_gqa_causal_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "f16", causal=True, seed=1002),
@@ -105,6 +106,11 @@ EXTRA_WORKLOADS = {
     "bf16_gqa_causal_dropout10_b2_hq32_hkv8_l4096_d128": Workload(
         "bf16_gqa_causal_dropout10_b2_hq32_hkv8_l4096_d128", 2, 32, 8, 4096, 4096, 128, "bf16", causal=True,
         seed=1002, dropout_p=0.1, dropout_seed=2024, dropout_offset=0),
+    # The D = 256 shape of the masked workloads without a mask (the head dim the backward
+    # takes at 256), and at D = 128 with the bool mask (a masked backward).
+    "bf16_h8_l2000_d256": Workload("bf16_h8_l2000_d256", 1, 8, 8, 2000, 2000, 256, "bf16", seed=1004),
+    "bf16_bool_mask_h8_l2000_d128": Workload(
+        "bf16_bool_mask_h8_l2000_d128", 1, 8, 8, 2000, 2000, 128, "bf16", mask_kind=MASK_BOOL, seed=1004),
 }
 WORKLOADS.update(EXTRA_WORKLOADS)
 
