@@ -142,15 +142,16 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   if constexpr (kMask) {
     if (a.mask_kind != 0) {
       const int BH = a.B * a.Hq;
-      dim3 grid((unsigned)((a.kL + 31) / 32), (unsigned)((a.mask_t_ld + 31) / 32), (unsigned)std::min(BH, 65535));
+      const int tile = a.mask_kind == 1 ? 128 : 64;  // entries per tile side (128 bytes)
+      dim3 grid((unsigned)((a.kL + tile - 1) / tile), (unsigned)(a.mask_t_ld / tile), (unsigned)std::min(BH, 65535));
       if (a.mask_kind == 1)
         fa_bwd_mask_transpose_kernel<uint8_t><<<grid, 256, 0, a.stream>>>(
             static_cast<const uint8_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_t_ld,
-            static_cast<uint8_t*>(a.mask_t));
+            a.mask_vec, static_cast<uint8_t*>(a.mask_t));
       else
         fa_bwd_mask_transpose_kernel<uint16_t><<<grid, 256, 0, a.stream>>>(
             static_cast<const uint16_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_t_ld,
-            static_cast<uint16_t*>(a.mask_t));
+            a.mask_vec, static_cast<uint16_t*>(a.mask_t));
       e = cudaGetLastError();
       if (e != cudaSuccess) {
         set_error("mask transpose launch failed: %s", cudaGetErrorString(e));

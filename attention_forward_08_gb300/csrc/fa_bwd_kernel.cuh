@@ -406,28 +406,78 @@ __device__ __forceinline__ void bwd_p_masked(float (&pr)[128], float sf, L2 l2, 
 
 // Key-major copy of the forward's mask for the key-parallel kernel:
 // mask_t[(b H_q + h) kL + j][i] = mask[b, h, i, j] for i < qL, 0 for qL <= i <
-// ld.  32 x 32 tiles through shared memory (coalesced reads and writes); the
-// grid walks (key tile, query tile, (b, h)), the last dimension in a loop.
+// ld.  HBM-bound: a CTA moves a tile of kR query rows x 128 bytes of keys (kE
+// entries to a 32-bit word, kR = 32 kE: 128 x 128 bool, 64 x 64 16-bit) with
+// 16-byte loads into shared memory (rows 33 words apart: conflict-free
+// stores), then each lane takes a word column of kE consecutive rows,
+// transposes that kE x kE block in registers with byte permutes, and the warp
+// writes whole 128-byte rows of the copy.  The grid walks (key tile, query
+// tile, (b, h)), the last dimension in a loop.  `vec`: the mask's base and
+// row strides are 16-byte multiples (else every entry is read on its own).
 template <class T>
 __global__ void __launch_bounds__(256) fa_bwd_mask_transpose_kernel(const T* __restrict__ mask, long long sb,
                                                                     long long sh, long long ss, int Hq, int BH,
-                                                                    int qL, int kL, long long ld,
+                                                                    int qL, int kL, long long ld, int vec,
                                                                     T* __restrict__ mask_t) {
-  __shared__ T tile[32][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-  const int j0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+  constexpr int kE = 4 / sizeof(T);  // entries per 32-bit word
+  constexpr int kR = 32 * kE;        // query rows per tile (one 128-byte output row)
+  constexpr int kK = 32 * kE;        // keys per tile (one 128-byte input row)
+  __shared__ uint32_t tile[kR][33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j0 = blockIdx.x * kK, i0 = blockIdx.y * kR;
+  const bool full = vec && j0 + kK <= kL;
   for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
     const int b = bh / Hq, h = bh - b * Hq;
     const T* src = mask + (long long)b * sb + (long long)h * sh;
-    for (int r = ty; r < 32; r += 8) {
-      const int i = i0 + r, j = j0 + tx;
-      tile[r][tx] = (i < qL && j < kL) ? src[(long long)i * ss + j] : T(0);
+    // rows of the tile: 8 lanes per row, 16 bytes a lane
+#pragma unroll
+    for (int it = 0; it < kR / 32; ++it) {
+      const int ch = threadIdx.x + it * 256, r = ch >> 3, c16 = ch & 7;
+      const int i = i0 + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (i < qL) {
+        const T* row = src + (long long)i * ss + j0 + c16 * (4 * kE);
+        if (full) {
+          v = __ldg(reinterpret_cast<const uint4*>(row));
+        } else {
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int e = 0; e < 4 * kE; ++e)
+            if (j0 + c16 * (4 * kE) + e < kL) w[e / kE] |= (uint32_t)row[e] << (8 * sizeof(T) * (e % kE));
+          v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      tile[r][c16 * 4 + 0] = v.x;
+      tile[r][c16 * 4 + 1] = v.y;
+      tile[r][c16 * 4 + 2] = v.z;
+      tile[r][c16 * 4 + 3] = v.w;
     }
     __syncthreads();
-    T* dst = mask_t + (long long)bh * kL * ld;
-    for (int r = ty; r < 32; r += 8) {
-      const int j = j0 + r, i = i0 + tx;
-      if (j < kL && i < ld) dst[(long long)j * ld + i] = tile[tx][r];
+    // word column c (keys j0 + kE c ..) of rows kE lane .. kE lane + kE - 1 -> kE output rows
+    T* dst = mask_t + (long long)bh * kL * ld + i0;
+#pragma unroll
+    for (int cw = 0; cw < 4; ++cw) {
+      const int c = warp * 4 + cw;
+      uint32_t out[kE];
+      if constexpr (kE == 4) {
+        const uint32_t r0 = tile[4 * lane][c], r1 = tile[4 * lane + 1][c];
+        const uint32_t r2 = tile[4 * lane + 2][c], r3 = tile[4 * lane + 3][c];
+        const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r0, r1, 0x7362);
+        const uint32_t t2 = __byte_perm(r2, r3, 0x5140), t3 = __byte_perm(r2, r3, 0x7362);
+        out[0] = __byte_perm(t0, t2, 0x5410);
+        out[1] = __byte_perm(t0, t2, 0x7632);
+        out[2] = __byte_perm(t1, t3, 0x5410);
+        out[3] = __byte_perm(t1, t3, 0x7632);
+      } else {
+        const uint32_t r0 = tile[2 * lane][c], r1 = tile[2 * lane + 1][c];
+        out[0] = __byte_perm(r0, r1, 0x5410);
+        out[1] = __byte_perm(r0, r1, 0x7632);
+      }
+#pragma unroll
+      for (int e = 0; e < kE; ++e) {
+        const int j = j0 + kE * c + e;
+        if (j < kL) reinterpret_cast<uint32_t*>(dst + (long long)j * ld)[lane] = out[e];
+      }
     }
     __syncthreads();
   }
