@@ -605,8 +605,10 @@ long long fa_bwd_full_workspace_bytes(const fa_bwd_args* a) {
   if (a->dtype == FA_DTYPE_F32)
     return align256_ll(base) + bwd_tf32_layout(a->B, a->H_q, a->H_kv, a->qL, a->kL, a->D).bytes;
   if (a->mask_kind == FA_MASK_NONE) return base;
-  const int esz = a->mask_kind == FA_MASK_BOOL ? 1 : 2;
-  return align256_ll(base) + align256_ll((long long)a->B * a->H_q * a->kL * mask_t_ld(a->qL) * esz);
+  if (a->mask_kind == FA_MASK_BOOL)  // keep bits, key-major then row-major
+    return align256_ll(base) + align256_ll((long long)a->B * a->H_q * a->kL * (mask_t_ld(a->qL) / 32) * 4) +
+           align256_ll((long long)a->B * a->H_q * a->qL * keep_row_words(a->kL) * 4);
+  return align256_ll(base) + align256_ll((long long)a->B * a->H_q * a->kL * mask_t_ld(a->qL) * 2);
 }
 
 int fa_bwd_full(const fa_bwd_args* args) {
@@ -676,8 +678,16 @@ int fa_bwd_full(const fa_bwd_args* args) {
   a.mask_kind = x.mask_kind;
   a.mask = x.mask;
   for (int i = 0; i < 3; ++i) a.ms[i] = x.mask_kind ? x.mask_strides[i] : 0;
-  a.mask_t = x.mask_kind ? static_cast<char*>(x.workspace) + align256_ll(base) : nullptr;
+  char* mask_ws = static_cast<char*>(x.workspace) + align256_ll(base);
+  a.mask_t = x.mask_kind == FA_MASK_ADDITIVE ? mask_ws : nullptr;
   a.mask_t_ld = mask_t_ld(x.qL);
+  a.mask_tbits_ld = mask_t_ld(x.qL) / 32;
+  a.mask_rbits_ld = keep_row_words(x.kL);
+  a.mask_tbits = x.mask_kind == FA_MASK_BOOL ? reinterpret_cast<uint32_t*>(mask_ws) : nullptr;
+  a.mask_rbits = x.mask_kind == FA_MASK_BOOL
+                     ? reinterpret_cast<uint32_t*>(mask_ws + align256_ll((long long)x.B * x.H_q * x.kL *
+                                                                          a.mask_tbits_ld * 4))
+                     : nullptr;
   a.mask_vec = 0;
   if (x.mask_kind != FA_MASK_NONE) {
     const int mesz = x.mask_kind == FA_MASK_BOOL ? 1 : 2;

@@ -88,6 +88,10 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   p.mask_vec = a.mask_vec;
   p.mask_t = a.mask_t;
   p.mask_t_ld = a.mask_t_ld;
+  p.mask_tbits = a.mask_tbits;
+  p.mask_tbits_ld = a.mask_tbits_ld;
+  p.mask_rbits = a.mask_rbits;
+  p.mask_rbits_ld = a.mask_rbits_ld;
   p.n_qt = (a.qL + C::kTile - 1) / C::kTile;
   p.n_kt = (a.kL + C::kTile - 1) / C::kTile;
   p.scale = a.scale;
@@ -138,16 +142,17 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
     }
   }
 
-  // 4. The forward's mask, key-major, for the dK/dV kernel.
+  // 4. The forward's mask: bool as keep bits (row-major and key-major), additive
+  // as a key-major copy for the dK/dV kernel.
   if constexpr (kMask) {
     if (a.mask_kind != 0) {
       const int BH = a.B * a.Hq;
       const int tile = a.mask_kind == 1 ? 128 : 64;  // entries per tile side (128 bytes)
       dim3 grid((unsigned)((a.kL + tile - 1) / tile), (unsigned)(a.mask_t_ld / tile), (unsigned)std::min(BH, 65535));
       if (a.mask_kind == 1)
-        fa_bwd_mask_transpose_kernel<uint8_t><<<grid, 256, 0, a.stream>>>(
-            static_cast<const uint8_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_t_ld,
-            a.mask_vec, static_cast<uint8_t*>(a.mask_t));
+        fa_bwd_mask_bits_kernel<<<grid, 256, 0, a.stream>>>(
+            static_cast<const uint8_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_vec,
+            a.mask_tbits, a.mask_tbits_ld, a.mask_rbits, a.mask_rbits_ld);
       else
         fa_bwd_mask_transpose_kernel<uint16_t><<<grid, 256, 0, a.stream>>>(
             static_cast<const uint16_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_t_ld,

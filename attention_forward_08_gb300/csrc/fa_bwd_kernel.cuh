@@ -74,6 +74,13 @@ struct BwdParams {
   int mask_vec;
   const void* mask_t;
   long long mask_t_ld;
+  // A bool mask reaches the kernels as keep bits written by the pre-pass (the
+  // dropout keep words' layout): row-major for the dQ kernel, key-major for
+  // the dK/dV kernel, 16 bytes per row (or key) and 128-entry block.
+  const uint32_t* mask_tbits;
+  long long mask_tbits_ld;
+  const uint32_t* mask_rbits;
+  long long mask_rbits_ld;
   int n_qt, n_kt;     // 128-row query tiles per (b, h), 128-key tiles per (b, kvh)
   float scale;        // softmax scale (applied to dQ and dK in the epilogue)
   float scale_log2;   // scale * log2(e)
@@ -339,69 +346,100 @@ __device__ __forceinline__ float softcap_factor(float p, float l2, float inv_out
   return p > 0.0f ? fmaf(-th, th, 1.0f) : 0.0f;
 }
 
-// The forward's mask on 128 consecutive entries (keys of a query row, or queries
-// of a key row in the key-major copy) as packed words: bool, 4 bytes a word
-// (words 0..31); additive, two 16-bit values a word (words 0..63).  With
-// `vec` the 128 entries are read with 16-byte loads; otherwise only the first
-// `n` are read one by one and the rest stay 0 (excluded for bool, no
-// addition for additive; callers cut those entries by their limits anyway).
-template <bool kBool>
-__device__ __forceinline__ void bwd_load_mask128(uint32_t (&mw)[64], const void* src, bool vec, int n) {
-  constexpr int kWords = kBool ? 32 : 64;
-  if (vec) {
-    const uint4* s4 = static_cast<const uint4*>(src);
+// Probabilities of 128 scores under a bool mask given as keep bits (bit c of
+// mw[0..3] for entry c): p = 2^(s * sf - l2), 0 where the entry lies outside
+// [lo, lim) (the row's limits) or its bit is clear.
+template <class L2, int N>
+__device__ __forceinline__ void bwd_p_keepbits(float (&pr)[128], float sf, L2 l2, const uint32_t (&mw)[N], int lo,
+                                               int lim) {
+  static_assert(N >= 4, "four keep words");
 #pragma unroll
-    for (int v = 0; v < kWords / 4; ++v) {
-      const uint4 w = __ldg(s4 + v);
+  for (int c = 0; c < 128; c += 2) {
+    float x0, x1;
+    ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2(c), -l2(c + 1));
+    const uint32_t w = mw[c >> 5] >> (c & 31);
+    const bool a0 = c >= lo && c < lim && (w & 1u) != 0u;
+    const bool a1 = c + 1 >= lo && c + 1 < lim && (w & 2u) != 0u;
+    pr[c] = a0 ? ex2(x0) : 0.0f;
+    pr[c + 1] = a1 ? ex2(x1) : 0.0f;
+  }
+}
+
+// Probabilities of 128 scores with an additive mask read in 16-byte chunks
+// from its row (`row`: 128 entries; prefetched into L1 before the scores
+// landed): p = 2^(s * sf - l2 + m * log2(e)), 0 outside [lo, lim).  Without
+// `vec` only the first `n` entries are read, one by one (the rest add 0).
+template <class C, class L2>
+__device__ __forceinline__ void bwd_p_additive(float (&pr)[128], float sf, L2 l2, const uint16_t* row, bool vec,
+                                               int n, int lo, int lim) {
+#pragma unroll
+  for (int cc = 0; cc < 16; ++cc) {
+    uint32_t w[4];
+    if (vec) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + cc);
+      w[0] = v.x;
+      w[1] = v.y;
+      w[2] = v.z;
+      w[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 8 * cc + 2 * e;
+        w[e] = (c < n ? (uint32_t)__ldg(row + c) : 0u) | (c + 1 < n ? (uint32_t)__ldg(row + c + 1) << 16 : 0u);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 8 * cc + 2 * e;
+      float x0, x1;
+      ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2(c), -l2(c + 1));
+      ffma2(x0, x1, half_bits_to_f32<C::kF16>(w[e]), half_bits_to_f32<C::kF16>(w[e] >> 16), kLog2e, kLog2e, x0, x1);
+      pr[c] = (c >= lo && c < lim) ? ex2(x0) : 0.0f;
+      pr[c + 1] = (c + 1 >= lo && c + 1 < lim) ? ex2(x1) : 0.0f;
+    }
+  }
+}
+
+// An additive mask's 128 entries of a row as 64 packed words (16-byte loads
+// with `vec`; otherwise the first `n` one by one, the rest 0).
+__device__ __forceinline__ void bwd_load_additive128(uint32_t (&mw)[64], const uint16_t* row, bool vec, int n) {
+  if (vec) {
+#pragma unroll
+    for (int v = 0; v < 16; ++v) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(row) + v);
       mw[4 * v] = w.x;
       mw[4 * v + 1] = w.y;
       mw[4 * v + 2] = w.z;
       mw[4 * v + 3] = w.w;
     }
   } else {
-    // every index compile-time, so the words stay in registers
-    constexpr int kPer = kBool ? 4 : 2;
 #pragma unroll
-    for (int v = 0; v < kWords; ++v) {
-      uint32_t w = 0u;
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) {
-        const int c = v * kPer + e;
-        if (c < n) {
-          if constexpr (kBool)
-            w |= (uint32_t)__ldg(static_cast<const uint8_t*>(src) + c) << (8 * e);
-          else
-            w |= (uint32_t)__ldg(static_cast<const uint16_t*>(src) + c) << (16 * e);
-        }
-      }
-      mw[v] = w;
-    }
+    for (int v = 0; v < 64; ++v)  // every index compile-time: the words stay in registers
+      mw[v] = (2 * v < n ? (uint32_t)__ldg(row + 2 * v) : 0u) |
+              (2 * v + 1 < n ? (uint32_t)__ldg(row + 2 * v + 1) << 16 : 0u);
   }
 }
 
-// Probabilities of 128 scores with the forward's mask folded in: p = 2^(x)
-// with x = s * sf - l2 (+ m * log2(e) for an additive mask), 0 where the entry
-// lies outside [lo, lim) (the row's limits) or a bool mask excludes it.  l2(c)
-// gives the base-2 logsumexp of entry c's query row.
-template <class C, int kKind, class L2>
-__device__ __forceinline__ void bwd_p_masked(float (&pr)[128], float sf, L2 l2, const uint32_t (&mw)[64], int lo,
-                                             int lim) {
+// bwd_p_additive with the 128 entries already in registers (mw, as loaded by
+// bwd_load_additive128).
+template <class C, class L2>
+__device__ __forceinline__ void bwd_p_additive_regs(float (&pr)[128], float sf, L2 l2, const uint32_t (&mw)[64],
+                                                    int lo, int lim) {
 #pragma unroll
   for (int c = 0; c < 128; c += 2) {
     float x0, x1;
     ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2(c), -l2(c + 1));
-    bool a0 = c >= lo && c < lim, a1 = c + 1 >= lo && c + 1 < lim;
-    if constexpr (kKind == 2) {
-      const uint32_t w = mw[c >> 1];
-      ffma2(x0, x1, half_bits_to_f32<C::kF16>(w), half_bits_to_f32<C::kF16>(w >> 16), kLog2e, kLog2e, x0, x1);
-    } else {
-      const uint32_t w = mw[c >> 2] >> (8 * (c & 3));
-      a0 = a0 && (w & 0xFFu) != 0u;
-      a1 = a1 && (w & 0xFF00u) != 0u;
-    }
-    pr[c] = a0 ? ex2(x0) : 0.0f;
-    pr[c + 1] = a1 ? ex2(x1) : 0.0f;
+    const uint32_t w = mw[c >> 1];
+    ffma2(x0, x1, half_bits_to_f32<C::kF16>(w), half_bits_to_f32<C::kF16>(w >> 16), kLog2e, kLog2e, x0, x1);
+    pr[c] = (c >= lo && c < lim) ? ex2(x0) : 0.0f;
+    pr[c + 1] = (c + 1 >= lo && c + 1 < lim) ? ex2(x1) : 0.0f;
   }
+}
+
+// Pull a 128-entry mask row (up to 256 bytes) into L1 ahead of its use.
+__device__ __forceinline__ void prefetch_row_l1(const void* row, int bytes) {
+  for (int o = 0; o < bytes; o += 128)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(static_cast<const char*>(row) + o));
 }
 
 // Key-major copy of the forward's mask for the key-parallel kernel:
@@ -478,6 +516,89 @@ __global__ void __launch_bounds__(256) fa_bwd_mask_transpose_kernel(const T* __r
         const int j = j0 + kE * c + e;
         if (j < kL) reinterpret_cast<uint32_t*>(dst + (long long)j * ld)[lane] = out[e];
       }
+    }
+    __syncthreads();
+  }
+}
+
+// Keep flags of four mask bytes as four bits (bit e: byte e nonzero): the
+// high bit of each byte of ((w & 0x7f..) + 0x7f..) | w is set iff the byte is
+// nonzero; one multiply gathers the four flags into bits 28..31 (the partial
+// products of lower flags land below bit 28 without carries).
+__device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t w) {
+  const uint32_t t = ((((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w) >> 7) & 0x01010101u;
+  return (t * 0x10204080u) >> 28;
+}
+
+// A bool mask as keep bits for both gradient kernels (one read of the mask):
+//   rbits[((b H_q + h) qL + i) rld + w] bit x = mask[b, h, i, 32 w + x] != 0
+//   tbits[((b H_q + h) kL + j) tld + w] bit x = mask[b, h, 32 w + x, j] != 0
+// with 4 words per 128-entry block (rld = 4 ceil(kL / 128), tld = 4 ceil(qL /
+// 128)); entries past qL or kL are 0.  A CTA loads a 128 x 128 tile as the
+// transpose does (rows 144 bytes apart: conflict-free 16-byte accesses), then
+// lane r of warp w turns tile row 32 (w % 4) + r into four keep words, warps
+// 0-3 store them (row-major), and each warp transposes two of the four
+// 32 x 32 bit blocks of its rows with 32 ballots each (key-major).  Grid as the
+// uint8 transpose: (key tile, query tile, (b, h) in a loop).
+static __global__ void __launch_bounds__(256) fa_bwd_mask_bits_kernel(const uint8_t* __restrict__ mask, long long sb,
+                                                                      long long sh, long long ss, int Hq, int BH,
+                                                                      int qL, int kL, int vec,
+                                                                      uint32_t* __restrict__ tbits, long long tld,
+                                                                      uint32_t* __restrict__ rbits, long long rld) {
+  __shared__ __align__(16) uint32_t tile[128][36];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j0 = blockIdx.x * 128, i0 = blockIdx.y * 128;
+  const bool full = vec && j0 + 128 <= kL;
+  const int rg = warp & 3, r = 32 * rg + lane;  // this lane's tile row
+  for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
+    const int b = bh / Hq, h = bh - b * Hq;
+    const uint8_t* src = mask + (long long)b * sb + (long long)h * sh;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int ch = threadIdx.x + it * 256, rr = ch >> 3, c16 = ch & 7;
+      const int i = i0 + rr;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (i < qL) {
+        const uint8_t* row = src + (long long)i * ss + j0 + c16 * 16;
+        if (full) {
+          v = __ldg(reinterpret_cast<const uint4*>(row));
+        } else {
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (j0 + c16 * 16 + e < kL) w[e / 4] |= (uint32_t)row[e] << (8 * (e % 4));
+          v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      *reinterpret_cast<uint4*>(&tile[rr][c16 * 4]) = v;
+    }
+    __syncthreads();
+    uint32_t kw[4];  // bit x of kw[g]: key 32 g + x of row r
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t bits = 0u;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(&tile[r][8 * g + 4 * q]);
+        bits |= (nonzero_bytes4(v.x) | nonzero_bytes4(v.y) << 4 | nonzero_bytes4(v.z) << 8 |
+                 nonzero_bytes4(v.w) << 12) << (16 * q);
+      }
+      kw[g] = bits;
+    }
+    if (warp < 4 && i0 + r < qL)
+      *reinterpret_cast<uint4*>(rbits + ((long long)bh * qL + i0 + r) * rld + j0 / 32) =
+          make_uint4(kw[0], kw[1], kw[2], kw[3]);
+#pragma unroll
+    for (int gg = 0; gg < 2; ++gg) {
+      const int g = 2 * (warp >> 2) + gg;
+      const uint32_t kg = gg == 0 ? (warp < 4 ? kw[0] : kw[2]) : (warp < 4 ? kw[1] : kw[3]);
+      uint32_t mine = 0u;  // lane x: key 32 g + x over rows 32 rg .. 32 rg + 31
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const uint32_t t = __ballot_sync(0xffffffffu, (kg >> x) & 1u);
+        if (lane == x) mine = t;
+      }
+      if (j0 + 32 * g + lane < kL) tbits[((long long)bh * kL + j0 + 32 * g + lane) * tld + i0 / 32 + rg] = mine;
     }
     __syncthreads();
   }
@@ -866,14 +987,19 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       const float* l2s = sLD + s * 2 * C::kTile;
       // The forward's mask for this key and the step's 128 queries (key-major
       // copy: contiguous, 16-byte aligned), loaded before S^T lands.
-      uint32_t mw[64];
+      uint32_t mw[4];
+      const uint16_t* madd = nullptr;
       if constexpr (C::kMask) {
-        if (p.mask_kind != 0 && j < p.kL) {
-          const long long off = (((long long)b * p.Hq + h) * p.kL + j) * p.mask_t_ld + q0;
-          if (p.mask_kind == 1)
-            bwd_load_mask128<true>(mw, static_cast<const uint8_t*>(p.mask_t) + off, true, 128);
-          else
-            bwd_load_mask128<false>(mw, static_cast<const uint16_t*>(p.mask_t) + off, true, 128);
+        if (p.mask_kind == 1 && j < p.kL) {  // keep bits of the step's 128 queries
+          const uint4 kb = __ldg(reinterpret_cast<const uint4*>(
+              p.mask_tbits + (((long long)b * p.Hq + h) * p.kL + j) * p.mask_tbits_ld + q0 / 32));
+          mw[0] = kb.x;
+          mw[1] = kb.y;
+          mw[2] = kb.z;
+          mw[3] = kb.w;
+        } else if (p.mask_kind == 2 && j < p.kL) {  // the key-major copy's row, read in the P pass
+          madd = static_cast<const uint16_t*>(p.mask_t) + (((long long)b * p.Hq + h) * p.kL + j) * p.mask_t_ld + q0;
+          prefetch_row_l1(madd, 256);
         }
       }
       ok = warp_wait(&ctl->ld_full[s], use & 1, abort_flag, p.status, p.timeout_cycles);
@@ -907,9 +1033,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         const float sf = p.softcap_on ? 1.0f : sl;
         if (C::kMask && p.mask_kind == 2 && j < p.kL) {
-          bwd_p_masked<C, 2>(pr, sf, [&](int c) { return l2s[c]; }, mw, lim, hi);
+          bwd_p_additive<C>(pr, sf, [&](int c) { return l2s[c]; }, madd, true, 128, lim, hi);
         } else if (C::kMask && p.mask_kind == 1 && j < p.kL) {
-          bwd_p_masked<C, 1>(pr, sf, [&](int c) { return l2s[c]; }, mw, lim, hi);
+          bwd_p_keepbits(pr, sf, [&](int c) { return l2s[c]; }, mw, lim, hi);
         } else {
 #pragma unroll
           for (int c = 0; c < 128; c += 2) {
@@ -1226,16 +1352,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       }
       // The forward's mask on this row's keys of block j, loaded before S_j lands.
+      // (the dQ kernel holds an additive mask's 64 words in registers: its rows
+      // lie far apart in the mask, so reading them inside the P pass would
+      // expose each load's latency)
       uint32_t mw[64];
       if constexpr (C::kMask) {
-        if (p.mask_kind != 0 && i < p.qL) {
-          const long long off = (long long)b * p.mask_sb + (long long)h * p.mask_sh + (long long)i * p.mask_ss + kbase;
-          const bool vec = p.mask_vec != 0 && kbase + 128 <= p.kL;
-          const int n = min(128, p.kL - kbase);
-          if (p.mask_kind == 1)
-            bwd_load_mask128<true>(mw, static_cast<const uint8_t*>(p.mask) + off, vec, n);
-          else
-            bwd_load_mask128<false>(mw, static_cast<const uint16_t*>(p.mask) + off, vec, n);
+        if (p.mask_kind == 1 && i < p.qL) {  // keep bits of block j's 128 keys, in mw[0..3]
+          const uint4 kb = __ldg(reinterpret_cast<const uint4*>(
+              p.mask_rbits + (((long long)b * p.Hq + h) * p.qL + i) * p.mask_rbits_ld + kbase / 32));
+          mw[0] = kb.x;
+          mw[1] = kb.y;
+          mw[2] = kb.z;
+          mw[3] = kb.w;
+        } else if (p.mask_kind == 2 && i < p.qL) {
+          const uint16_t* row = static_cast<const uint16_t*>(p.mask) + (long long)b * p.mask_sb +
+                                (long long)h * p.mask_sh + (long long)i * p.mask_ss + kbase;
+          bwd_load_additive128(mw, row, p.mask_vec != 0 && kbase + 128 <= p.kL, min(128, p.kL - kbase));
         }
       }
       ok = warp_wait(&ctl->s_full, j & 1, abort_flag, p.status, p.timeout_cycles);
@@ -1265,9 +1397,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
       }
       if (C::kMask && p.mask_kind == 2 && i < p.qL) {
-        bwd_p_masked<C, 2>(pr, sq, [&](int) { return l2; }, mw, lo, lim);
+        bwd_p_additive_regs<C>(pr, sq, [&](int) { return l2; }, mw, lo, lim);
       } else if (C::kMask && p.mask_kind == 1 && i < p.qL) {
-        bwd_p_masked<C, 1>(pr, sq, [&](int) { return l2; }, mw, lo, lim);
+        bwd_p_keepbits(pr, sq, [&](int) { return l2; }, mw, lo, lim);
       } else {
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {

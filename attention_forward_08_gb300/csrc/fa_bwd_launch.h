@@ -31,8 +31,12 @@ struct BwdLaunchArgs {
   const void* mask;                  // [B, H_q, qL, kL] through ms (element strides; key stride 1)
   long long ms[3];
   int mask_vec;                      // mask rows 16-byte aligned: vector loads
-  void* mask_t;                      // scratch: key-major copy [B, H_q, kL, mask_t_ld]
+  void* mask_t;                      // additive: scratch key-major copy [B, H_q, kL, mask_t_ld]
   long long mask_t_ld;
+  uint32_t* mask_tbits;              // bool: scratch keep bits, key-major [B, H_q, kL, mask_tbits_ld words]
+  long long mask_tbits_ld;           //   (bit x of word w: query 32 w + x)
+  uint32_t* mask_rbits;              // bool: scratch keep bits, row-major [B, H_q, qL, mask_rbits_ld words]
+  long long mask_rbits_ld;           //   (bit x of word w: key 32 w + x)
   cudaStream_t stream;
   unsigned int* status;
   long long timeout_cycles;

@@ -300,8 +300,9 @@ def _bwd_args(fa, **kw):
 
 
 def test_bwd_full_workspace_with_mask(fa):
-    """fa_bwd_full_workspace_bytes: the D vector, then (dropout) the keep words, then (mask) a key-major copy of
-    the mask with whole 128-row query blocks per key, each part 256-byte aligned."""
+    """fa_bwd_full_workspace_bytes: the D vector, then (dropout) the keep words, then (additive mask) a key-major
+    copy of the mask with whole 128-row query blocks per key, or (bool mask) its keep bits key-major and
+    row-major, 16 bytes per row (key) and 128-entry block; each part 256-byte aligned."""
     al = lambda n: (n + 255) // 256 * 256
     base = fa.fa_bwd_ex_workspace_bytes(1, 2, 200, 300, 0.0)
     assert fa.fa.fa_bwd_full_workspace_bytes(_bwd_args(fa)) == base
@@ -309,7 +310,8 @@ def test_bwd_full_workspace_with_mask(fa):
     assert fa.fa.fa_bwd_full_workspace_bytes(a) == al(base) + al(1 * 2 * 300 * 256 * 2)
     a = _bwd_args(fa, mask=P, mask_kind=1, mask_strides=(0, 0, 300), dropout_p=0.1)
     base = fa.fa_bwd_ex_workspace_bytes(1, 2, 200, 300, 0.1)
-    assert fa.fa.fa_bwd_full_workspace_bytes(a) == al(base) + al(1 * 2 * 300 * 256 * 1)
+    assert fa.fa.fa_bwd_full_workspace_bytes(a) == al(base) + al(1 * 2 * 300 * (256 // 32) * 4) + \
+        al(1 * 2 * 200 * (3 * 4) * 4)
 
 
 def test_bwd_full_workspace_fp32(fa):
