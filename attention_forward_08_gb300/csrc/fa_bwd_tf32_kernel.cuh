@@ -112,8 +112,8 @@ __device__ __forceinline__ void t32_store64(uint32_t taddr, const float (&x)[64]
   }
 }
 
-// Grid: dV, dK -- one CTA per (128-key tile, kvh, b), early key tiles first;
-// dQ -- one CTA per (128-row query tile, h, b), late (causal: heavy) tiles first.
+// Grid: dV, dK -- one CTA per (128-key tile, kvh, b); dQ -- one CTA per
+// (128-row query tile, h, b).  Causal: heavy tiles first; else head-major.
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_bwd_tf32_kernel(const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
@@ -132,21 +132,38 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // ---- this CTA's work: (b, resident head, resident row 0) and its steps
   int b, rh, r0, n_steps, per_head = 1, s0 = 0;
+  // Causal: tile-major, heavy tiles first (the longest CTAs start first).
+  // Otherwise every CTA does the same work: head-major, so the CTAs running at
+  // a time share few heads and the operands they stream stay in L2.
   if constexpr (C::kRole == kT32DQ) {
     const int n_qt = (p.qL + C::kRows - 1) / C::kRows;
     const int per_qt = p.Hq * p.B;
-    const int qt_rev = blockIdx.x / per_qt;
-    const int rem = blockIdx.x - qt_rev * per_qt;
+    int qt, rem;
+    if (p.causal) {
+      const int qt_rev = blockIdx.x / per_qt;
+      rem = blockIdx.x - qt_rev * per_qt;
+      qt = n_qt - 1 - qt_rev;
+    } else {
+      rem = blockIdx.x / n_qt;
+      qt = blockIdx.x - rem * n_qt;
+    }
     b = rem / p.Hq;
     rh = rem - b * p.Hq;
-    r0 = (p.causal ? n_qt - 1 - qt_rev : qt_rev) * C::kRows;
+    r0 = qt * C::kRows;
     const int last = min(r0 + C::kRows, p.qL) - 1;
     const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
     n_steps = (kv_end + C::kStep - 1) / C::kStep;
   } else {
     const int per_kt = p.Hkv * p.B;
-    const int kt = blockIdx.x / per_kt;
-    const int rem = blockIdx.x - kt * per_kt;
+    const int n_kt = (p.kL + C::kRows - 1) / C::kRows;
+    int kt, rem;
+    if (p.causal) {
+      kt = blockIdx.x / per_kt;
+      rem = blockIdx.x - kt * per_kt;
+    } else {
+      rem = blockIdx.x / n_kt;
+      kt = blockIdx.x - rem * n_kt;
+    }
     b = rem / p.Hkv;
     rh = rem - b * p.Hkv;
     r0 = kt * C::kRows;

@@ -44,10 +44,32 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 L2_FLUSH_BYTES = 512 << 20
-KERNEL_SOURCES = ["attention_forward_08_gb300/csrc/fa_kernel.cuh", "attention_forward_08_gb300/csrc/fa_ptx.cuh",
-                  "attention_forward_08_gb300/csrc/fa_launch.cuh"]
-BWD_KERNEL_SOURCES = ["attention_forward_08_gb300/csrc/fa_bwd_kernel.cuh", "attention_forward_08_gb300/csrc/fa_bwd.cu",
-                      "attention_forward_08_gb300/csrc/fa_kernel.cuh", "attention_forward_08_gb300/csrc/fa_ptx.cuh"]
+CSRC = "attention_forward_08_gb300/csrc/"
+KERNEL_SOURCES = [CSRC + f for f in ("fa_kernel.cuh", "fa_ptx.cuh", "fa_launch.cuh", "fa_params.h")]
+
+
+def kernel_sources(w: workloads.Workload, kind: str = "fwd") -> list:
+    """The sources the plan of `w` compiles from (the hash that marks a committed ncu summary as
+    taken on the current code covers these, so an edit to another plan leaves it valid)."""
+    if kind == "fwd":
+        extra = ("fa_tf32_prep.cu", "fa_tf32_ops.cuh") if w.dtype == "f32" else ()
+        return KERNEL_SOURCES + [CSRC + f for f in extra]
+    common = ("fa_bwd_kernel.cuh", "fa_bwd_impl.cuh", "fa_bwd_launch.h", "fa_bwd.cu")
+    if w.dtype == "f32":
+        plan = ("fa_bwd_tf32_kernel.cuh", "fa_bwd_tf32.cu", "fa_tf32_ops.cuh")
+    elif w.D == 256:
+        plan = ("fa_bwd256_kernel.cuh", "fa_bwd256.cu")
+    elif w.mask_kind:
+        plan = ("fa_bwd_mask.cu",)
+    elif w.dropout_p > 0:
+        plan = ("fa_bwd_drop.cu",)
+    elif w.window or w.softcap or w.q_offset:
+        plan = ("fa_bwd_feat.cu",)
+    else:
+        plan = ()
+    return KERNEL_SOURCES + [CSRC + f for f in common + plan]
+
+
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -107,8 +129,7 @@ def traffic_from_profiles(w: workloads.Workload, kind: str = "fwd"):
     text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    src = BWD_KERNEL_SOURCES if kind == "bwd" else KERNEL_SOURCES
-    if not m or not s or s.group(1) != kernel_source_hash(src):
+    if not m or not s or s.group(1) != kernel_source_hash(kernel_sources(w, kind)):
         return None
     return float(m.group(1))
 
