@@ -34,9 +34,13 @@ int set_smem_once(const void* kern, uint32_t bytes, std::atomic<unsigned long lo
   return 0;
 }
 
-template <int kD, bool kF16, bool kFeat, bool kDrop = false, bool kMask = false>
+template <int kD, bool kF16, bool kFeat, bool kDrop = false, int kMask = 0>
 int launch_bwd_d(const BwdLaunchArgs& a) {
   using C = BwdCfg<kD, kF16, kFeat, kDrop, kMask>;
+  if (a.mask_kind != kMask) {
+    set_error("backward plan for mask kind %d given mask kind %d", kMask, a.mask_kind);
+    return 2;
+  }
   // 1. D_i = rowsum(O_i * dO_i)
   const long long rows = (long long)a.B * a.Hq * a.qL;
   constexpr int kRowsPerBlock = 256 / (kD / 8);
@@ -144,24 +148,22 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
 
   // 4. The forward's mask: bool as keep bits (row-major and key-major), additive
   // as a key-major copy for the dK/dV kernel.
-  if constexpr (kMask) {
-    if (a.mask_kind != 0) {
-      const int BH = a.B * a.Hq;
-      const int tile = a.mask_kind == 1 ? 128 : 64;  // entries per tile side (128 bytes)
-      dim3 grid((unsigned)((a.kL + tile - 1) / tile), (unsigned)(a.mask_t_ld / tile), (unsigned)std::min(BH, 65535));
-      if (a.mask_kind == 1)
-        fa_bwd_mask_bits_kernel<<<grid, 256, 0, a.stream>>>(
-            static_cast<const uint8_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_vec,
-            a.mask_tbits, a.mask_tbits_ld, a.mask_rbits, a.mask_rbits_ld);
-      else
-        fa_bwd_mask_transpose_kernel<uint16_t><<<grid, 256, 0, a.stream>>>(
-            static_cast<const uint16_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_t_ld,
-            a.mask_vec, static_cast<uint16_t*>(a.mask_t));
-      e = cudaGetLastError();
-      if (e != cudaSuccess) {
-        set_error("mask transpose launch failed: %s", cudaGetErrorString(e));
-        return 4;
-      }
+  if constexpr (kMask != 0) {
+    const int BH = a.B * a.Hq;
+    constexpr int kSide = kMask == 1 ? 128 : 64;  // entries per tile side (128 bytes)
+    dim3 grid((unsigned)((a.kL + kSide - 1) / kSide), (unsigned)(a.mask_t_ld / kSide), (unsigned)std::min(BH, 65535));
+    if constexpr (kMask == 1)
+      fa_bwd_mask_bits_kernel<<<grid, 256, 0, a.stream>>>(
+          static_cast<const uint8_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_vec,
+          a.causal, a.q_offset, a.mask_tbits, a.mask_tbits_ld, a.mask_rbits, a.mask_rbits_ld);
+    else
+      fa_bwd_mask_transpose_kernel<uint16_t><<<grid, 256, 0, a.stream>>>(
+          static_cast<const uint16_t*>(a.mask), a.ms[0], a.ms[1], a.ms[2], a.Hq, BH, a.qL, a.kL, a.mask_t_ld,
+          a.mask_vec, a.causal, a.q_offset, static_cast<uint16_t*>(a.mask_t));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      set_error("mask transpose launch failed: %s", cudaGetErrorString(e));
+      return 4;
     }
   }
 

@@ -93,7 +93,7 @@ struct BwdParams {
   long long timeout_cycles;
 };
 
-template <int kD_, bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false, bool kMask_ = false>
+template <int kD_, bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false, int kMask_ = 0>
 struct BwdCfg {
   static constexpr int kD = kD_;
   // 16-bit I/O is bf16 unless kF16 (fp16): same kernels, other operand format.
@@ -104,9 +104,13 @@ struct BwdCfg {
   // Dropout as well (its own instantiations again; implies kFeat).
   static constexpr bool kDrop = kDrop_;
   static_assert(!kDrop || kFeat, "the dropout instantiation includes the other features");
-  // The forward's bool or additive mask (its own instantiations again: the
-  // mask words cost registers that the other feature kernels keep free).
-  static constexpr bool kMask = kMask_;
+  // The forward's mask, 1 bool or 2 additive (their own instantiations again:
+  // the mask words cost registers that the other feature kernels keep free).
+  // A mask excludes the softcap (the launch refuses the pair), so the mask
+  // kernels carry no softcap code: one probability pass each.
+  static constexpr int kMaskKind = kMask_;
+  static constexpr bool kMask = kMask_ != 0;
+  static_assert(kMask_ >= 0 && kMask_ <= 2, "mask kinds: 0 none, 1 bool, 2 additive");
   static_assert(!kMask || kFeat, "the mask instantiation includes the other features");
   static constexpr uint32_t kFmt = kF16 ? kFmtF16 : kFmtBf16;
   static constexpr CUtensorMapDataType kTmaType =
@@ -346,6 +350,21 @@ __device__ __forceinline__ float softcap_factor(float p, float l2, float inv_out
   return p > 0.0f ? fmaf(-th, th, 1.0f) : 0.0f;
 }
 
+// Bit x set for the entries base + x (x < 32) inside [lo, hi).
+__device__ __forceinline__ uint32_t range_bits32(int lo, int hi, int base) {
+  const int a = min(max(lo - base, 0), 32), b = min(max(hi - base, 0), 32);
+  return (uint32_t)((1ull << b) - 1ull) & ~(uint32_t)((1ull << a) - 1ull);
+}
+
+// The row's limits [lo, lim) over a 128-entry block as four words of
+// allowed bits, ANDed with keep words when there are some: each entry then
+// costs one bit test instead of two compares.
+template <int N>
+__device__ __forceinline__ void allowed_words(uint32_t (&aw)[4], const uint32_t (&mw)[N], bool keep, int lo, int lim) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) aw[q] = range_bits32(lo, lim, 32 * q) & (keep ? mw[q] : 0xFFFFFFFFu);
+}
+
 // Probabilities of 128 scores under a bool mask given as keep bits (bit c of
 // mw[0..3] for entry c): p = 2^(s * sf - l2), 0 where the entry lies outside
 // [lo, lim) (the row's limits) or its bit is clear.
@@ -353,15 +372,14 @@ template <class L2, int N>
 __device__ __forceinline__ void bwd_p_keepbits(float (&pr)[128], float sf, L2 l2, const uint32_t (&mw)[N], int lo,
                                                int lim) {
   static_assert(N >= 4, "four keep words");
+  uint32_t aw[4];
+  allowed_words(aw, mw, true, lo, lim);
 #pragma unroll
   for (int c = 0; c < 128; c += 2) {
     float x0, x1;
     ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2(c), -l2(c + 1));
-    const uint32_t w = mw[c >> 5] >> (c & 31);
-    const bool a0 = c >= lo && c < lim && (w & 1u) != 0u;
-    const bool a1 = c + 1 >= lo && c + 1 < lim && (w & 2u) != 0u;
-    pr[c] = a0 ? ex2(x0) : 0.0f;
-    pr[c + 1] = a1 ? ex2(x1) : 0.0f;
+    pr[c] = (aw[c >> 5] & (1u << (c & 31))) ? ex2(x0) : 0.0f;
+    pr[c + 1] = (aw[c >> 5] & (2u << (c & 31))) ? ex2(x1) : 0.0f;
   }
 }
 
@@ -372,6 +390,8 @@ __device__ __forceinline__ void bwd_p_keepbits(float (&pr)[128], float sf, L2 l2
 template <class C, class L2>
 __device__ __forceinline__ void bwd_p_additive(float (&pr)[128], float sf, L2 l2, const uint16_t* row, bool vec,
                                                int n, int lo, int lim) {
+  uint32_t aw[4];
+  allowed_words(aw, aw, false, lo, lim);
 #pragma unroll
   for (int cc = 0; cc < 16; ++cc) {
     uint32_t w[4];
@@ -394,8 +414,8 @@ __device__ __forceinline__ void bwd_p_additive(float (&pr)[128], float sf, L2 l2
       float x0, x1;
       ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2(c), -l2(c + 1));
       ffma2(x0, x1, half_bits_to_f32<C::kF16>(w[e]), half_bits_to_f32<C::kF16>(w[e] >> 16), kLog2e, kLog2e, x0, x1);
-      pr[c] = (c >= lo && c < lim) ? ex2(x0) : 0.0f;
-      pr[c + 1] = (c + 1 >= lo && c + 1 < lim) ? ex2(x1) : 0.0f;
+      pr[c] = (aw[c >> 5] & (1u << (c & 31))) ? ex2(x0) : 0.0f;
+      pr[c + 1] = (aw[c >> 5] & (2u << (c & 31))) ? ex2(x1) : 0.0f;
     }
   }
 }
@@ -425,14 +445,16 @@ __device__ __forceinline__ void bwd_load_additive128(uint32_t (&mw)[64], const u
 template <class C, class L2>
 __device__ __forceinline__ void bwd_p_additive_regs(float (&pr)[128], float sf, L2 l2, const uint32_t (&mw)[64],
                                                     int lo, int lim) {
+  uint32_t aw[4];
+  allowed_words(aw, mw, false, lo, lim);
 #pragma unroll
   for (int c = 0; c < 128; c += 2) {
     float x0, x1;
     ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2(c), -l2(c + 1));
     const uint32_t w = mw[c >> 1];
     ffma2(x0, x1, half_bits_to_f32<C::kF16>(w), half_bits_to_f32<C::kF16>(w >> 16), kLog2e, kLog2e, x0, x1);
-    pr[c] = (c >= lo && c < lim) ? ex2(x0) : 0.0f;
-    pr[c + 1] = (c + 1 >= lo && c + 1 < lim) ? ex2(x1) : 0.0f;
+    pr[c] = (aw[c >> 5] & (1u << (c & 31))) ? ex2(x0) : 0.0f;
+    pr[c + 1] = (aw[c >> 5] & (2u << (c & 31))) ? ex2(x1) : 0.0f;
   }
 }
 
@@ -440,6 +462,12 @@ __device__ __forceinline__ void bwd_p_additive_regs(float (&pr)[128], float sf, 
 __device__ __forceinline__ void prefetch_row_l1(const void* row, int bytes) {
   for (int o = 0; o < bytes; o += 128)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(static_cast<const char*>(row) + o));
+}
+
+// The same into L2, a step before that (`bytes` within the row).
+__device__ __forceinline__ void prefetch_row_l2(const void* row, int bytes) {
+  for (int o = 0; o < bytes; o += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(row) + o));
 }
 
 // Key-major copy of the forward's mask for the key-parallel kernel:
@@ -452,10 +480,14 @@ __device__ __forceinline__ void prefetch_row_l1(const void* row, int bytes) {
 // writes whole 128-byte rows of the copy.  The grid walks (key tile, query
 // tile, (b, h)), the last dimension in a loop.  `vec`: the mask's base and
 // row strides are 16-byte multiples (else every entry is read on its own).
+// Causal (diagonal of row i at key i + q_offset): a tile whose rows see none of
+// its keys is skipped, as the gradient kernels zero its entries through their
+// causal limits whatever the copy holds there.
 template <class T>
 __global__ void __launch_bounds__(256) fa_bwd_mask_transpose_kernel(const T* __restrict__ mask, long long sb,
                                                                     long long sh, long long ss, int Hq, int BH,
                                                                     int qL, int kL, long long ld, int vec,
+                                                                    int causal, int q_offset,
                                                                     T* __restrict__ mask_t) {
   constexpr int kE = 4 / sizeof(T);  // entries per 32-bit word
   constexpr int kR = 32 * kE;        // query rows per tile (one 128-byte output row)
@@ -463,6 +495,7 @@ __global__ void __launch_bounds__(256) fa_bwd_mask_transpose_kernel(const T* __r
   __shared__ uint32_t tile[kR][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = blockIdx.x * kK, i0 = blockIdx.y * kR;
+  if (causal && (long long)j0 > (long long)i0 + (kR - 1) + q_offset) return;
   const bool full = vec && j0 + kK <= kL;
   for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
     const int b = bh / Hq, h = bh - b * Hq;
@@ -521,6 +554,24 @@ __global__ void __launch_bounds__(256) fa_bwd_mask_transpose_kernel(const T* __r
   }
 }
 
+// Transposes a 32 x 32 bit matrix held one row per lane (bit k of lane l's
+// word = element (l, k)) so that lane k ends with column k (bit l = element
+// (l, k)): five butterfly stages, each swapping the off-diagonal half-blocks
+// of every 2j x 2j block between lanes l and l ^ j (the register form of the
+// recursive block transpose, Hacker's Delight, section 7-3).
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+  constexpr uint32_t kMask[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int j = 16 >> st;
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+    const uint32_t upper = ((y >> j) ^ x) & kMask[st];         // lanes with bit j set
+    const uint32_t lower = (((x >> j) ^ y) & kMask[st]) << j;  // lanes with bit j clear
+    x ^= (lane & j) ? upper : lower;
+  }
+  return x;
+}
+
 // Keep flags of four mask bytes as four bits (bit e: byte e nonzero): the
 // high bit of each byte of ((w & 0x7f..) + 0x7f..) | w is set iff the byte is
 // nonzero; one multiply gathers the four flags into bits 28..31 (the partial
@@ -536,18 +587,20 @@ __device__ __forceinline__ uint32_t nonzero_bytes4(uint32_t w) {
 // with 4 words per 128-entry block (rld = 4 ceil(kL / 128), tld = 4 ceil(qL /
 // 128)); entries past qL or kL are 0.  A CTA loads a 128 x 128 tile as the
 // transpose does (rows 144 bytes apart: conflict-free 16-byte accesses), then
-// lane r of warp w turns tile row 32 (w % 4) + r into four keep words, warps
-// 0-3 store them (row-major), and each warp transposes two of the four
-// 32 x 32 bit blocks of its rows with 32 ballots each (key-major).  Grid as the
-// uint8 transpose: (key tile, query tile, (b, h) in a loop).
+// lane r of warp w turns half of tile row 32 (w % 4) + r (keys 64 (w / 4) ..
+// + 63) into two keep words, stores them (row-major) and transposes the two
+// 32 x 32 bit blocks of its warp's rows in registers (key-major).  Grid as the
+// uint8 transpose: (key tile, query tile, (b, h) in a loop).  Causal: tiles
+// whose rows see none of their keys are skipped, as in the transpose.
 static __global__ void __launch_bounds__(256) fa_bwd_mask_bits_kernel(const uint8_t* __restrict__ mask, long long sb,
                                                                       long long sh, long long ss, int Hq, int BH,
-                                                                      int qL, int kL, int vec,
+                                                                      int qL, int kL, int vec, int causal, int q_offset,
                                                                       uint32_t* __restrict__ tbits, long long tld,
                                                                       uint32_t* __restrict__ rbits, long long rld) {
   __shared__ __align__(16) uint32_t tile[128][36];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = blockIdx.x * 128, i0 = blockIdx.y * 128;
+  if (causal && (long long)j0 > (long long)i0 + 127 + q_offset) return;
   const bool full = vec && j0 + 128 <= kL;
   const int rg = warp & 3, r = 32 * rg + lane;  // this lane's tile row
   for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
@@ -573,9 +626,11 @@ static __global__ void __launch_bounds__(256) fa_bwd_mask_bits_kernel(const uint
       *reinterpret_cast<uint4*>(&tile[rr][c16 * 4]) = v;
     }
     __syncthreads();
-    uint32_t kw[4];  // bit x of kw[g]: key 32 g + x of row r
+    const int hk = warp >> 2;  // this warp's half of the tile's keys
+    uint32_t kw[2];            // bit x of kw[gg]: key 32 (2 hk + gg) + x of row r
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int gg = 0; gg < 2; ++gg) {
+      const int g = 2 * hk + gg;
       uint32_t bits = 0u;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -583,43 +638,20 @@ static __global__ void __launch_bounds__(256) fa_bwd_mask_bits_kernel(const uint
         bits |= (nonzero_bytes4(v.x) | nonzero_bytes4(v.y) << 4 | nonzero_bytes4(v.z) << 8 |
                  nonzero_bytes4(v.w) << 12) << (16 * q);
       }
-      kw[g] = bits;
+      kw[gg] = bits;
     }
-    if (warp < 4 && i0 + r < qL)
-      *reinterpret_cast<uint4*>(rbits + ((long long)bh * qL + i0 + r) * rld + j0 / 32) =
-          make_uint4(kw[0], kw[1], kw[2], kw[3]);
+    if (i0 + r < qL)
+      *reinterpret_cast<uint2*>(rbits + ((long long)bh * qL + i0 + r) * rld + j0 / 32 + 2 * hk) =
+          make_uint2(kw[0], kw[1]);
 #pragma unroll
     for (int gg = 0; gg < 2; ++gg) {
-      const int g = 2 * (warp >> 2) + gg;
-      const uint32_t kg = gg == 0 ? (warp < 4 ? kw[0] : kw[2]) : (warp < 4 ? kw[1] : kw[3]);
-      uint32_t mine = 0u;  // lane x: key 32 g + x over rows 32 rg .. 32 rg + 31
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const uint32_t t = __ballot_sync(0xffffffffu, (kg >> x) & 1u);
-        if (lane == x) mine = t;
-      }
+      const int g = 2 * hk + gg;
+      // lane x: key 32 g + x, bit l = row 32 rg + l
+      const uint32_t mine = warp_transpose32(kw[gg], lane);
       if (j0 + 32 * g + lane < kL) tbits[((long long)bh * kL + j0 + 32 * g + lane) * tld + i0 / 32 + rg] = mine;
     }
     __syncthreads();
   }
-}
-
-// Transposes a 32 x 32 bit matrix held one row per lane (bit k of lane l's
-// word = element (l, k)) so that lane k ends with column k (bit l = element
-// (l, k)): five butterfly stages, each swapping the off-diagonal half-blocks
-// of every 2j x 2j block between lanes l and l ^ j (the register form of the
-// recursive block transpose, Hacker's Delight, section 7-3).
-__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
-  constexpr uint32_t kMask[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
-#pragma unroll
-  for (int st = 0; st < 5; ++st) {
-    const int j = 16 >> st;
-    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
-    const uint32_t upper = ((y >> j) ^ x) & kMask[st];         // lanes with bit j set
-    const uint32_t lower = (((x >> j) ^ y) & kMask[st]) << j;  // lanes with bit j clear
-    x ^= (lane & j) ? upper : lower;
-  }
-  return x;
 }
 
 // Keep bits to masks in two steps.  keep_bytes spreads bits shift .. shift
@@ -979,27 +1011,52 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     // row q0 + 32 q + c), transposed from the staged row words while the MMA
     // warp computes S^T.
     uint4* keep_smem = reinterpret_cast<uint4*>(smem + C::kKVOffKeep) + tl;
+    // The forward's mask for this key and a step's 128 queries: keep bits
+    // (16 bytes) or the key-major copy's row (256 bytes; contiguous, 16-byte
+    // aligned).  The next step's are fetched a step ahead (bits into
+    // registers, a row into L2), so their DRAM latency hides behind this step.
+    auto tbits_at = [&](int hh, int qq) {
+      return reinterpret_cast<const uint4*>(p.mask_tbits + (((long long)b * p.Hq + hh) * p.kL + j) * p.mask_tbits_ld +
+                                            qq / 32);
+    };
+    auto madd_at = [&](int hh, int qq) {
+      return static_cast<const uint16_t*>(p.mask_t) + (((long long)b * p.Hq + hh) * p.kL + j) * p.mask_t_ld + qq;
+    };
+    uint4 kb_next = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (C::kMask) {
+      if (j < p.kL && n_steps > 0) {
+        int h0, q00;
+        step_of(0, h0, q00);
+        if constexpr (C::kMaskKind == 1)
+          kb_next = __ldg(tbits_at(h0, q00));
+        else
+          prefetch_row_l2(madd_at(h0, q00), 256);
+      }
+    }
     bool ok = true;
     for (int i = 0; i < n_steps && ok; ++i) {
       int h, q0;
       step_of(i, h, q0);
       const int s = i % C::kStages, use = i / C::kStages;
       const float* l2s = sLD + s * 2 * C::kTile;
-      // The forward's mask for this key and the step's 128 queries (key-major
-      // copy: contiguous, 16-byte aligned), loaded before S^T lands.
       uint32_t mw[4];
       const uint16_t* madd = nullptr;
       if constexpr (C::kMask) {
-        if (p.mask_kind == 1 && j < p.kL) {  // keep bits of the step's 128 queries
-          const uint4 kb = __ldg(reinterpret_cast<const uint4*>(
-              p.mask_tbits + (((long long)b * p.Hq + h) * p.kL + j) * p.mask_tbits_ld + q0 / 32));
-          mw[0] = kb.x;
-          mw[1] = kb.y;
-          mw[2] = kb.z;
-          mw[3] = kb.w;
-        } else if (p.mask_kind == 2 && j < p.kL) {  // the key-major copy's row, read in the P pass
-          madd = static_cast<const uint16_t*>(p.mask_t) + (((long long)b * p.Hq + h) * p.kL + j) * p.mask_t_ld + q0;
-          prefetch_row_l1(madd, 256);
+        if (j < p.kL) {
+          int hn = h, qn = q0;
+          const bool more = i + 1 < n_steps;
+          if (more) step_of(i + 1, hn, qn);
+          if constexpr (C::kMaskKind == 1) {  // keep bits of the step's 128 queries
+            mw[0] = kb_next.x;
+            mw[1] = kb_next.y;
+            mw[2] = kb_next.z;
+            mw[3] = kb_next.w;
+            if (more) kb_next = __ldg(tbits_at(hn, qn));
+          } else {  // the row, read in the P pass
+            madd = madd_at(h, q0);
+            prefetch_row_l1(madd, 256);
+            if (more) prefetch_row_l2(madd_at(hn, qn), 256);
+          }
         }
       }
       ok = warp_wait(&ctl->ld_full[s], use & 1, abort_flag, p.status, p.timeout_cycles);
@@ -1026,23 +1083,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         int lim = p.causal ? j - p.q_offset - q0 : -(1 << 30);
         int hi = p.window > 0 ? j - p.q_offset + p.window - q0 : (1 << 30);
         if (j >= p.kL) lim = C::kTile;
-        if (p.softcap_on) {  // base-2 capped score, as the forward computes it
+        const bool capped = !C::kMask && p.softcap_on;  // a mask excludes the softcap
+        if (capped) {  // base-2 capped score, as the forward computes it
           const float kin = p.softcap_kin, cout = p.softcap_out;
 #pragma unroll
           for (int c = 0; c < 128; ++c) pr[c] = fmaf(-2.0f * cout, rcp_approx(ex2(pr[c] * kin) + 1.0f), cout);
         }
-        const float sf = p.softcap_on ? 1.0f : sl;
-        if (C::kMask && p.mask_kind == 2 && j < p.kL) {
-          bwd_p_additive<C>(pr, sf, [&](int c) { return l2s[c]; }, madd, true, 128, lim, hi);
-        } else if (C::kMask && p.mask_kind == 1 && j < p.kL) {
-          bwd_p_keepbits(pr, sf, [&](int c) { return l2s[c]; }, mw, lim, hi);
+        const float sf = capped ? 1.0f : sl;
+        if (C::kMask && j < p.kL) {
+          if constexpr (C::kMaskKind == 2)
+            bwd_p_additive<C>(pr, sf, [&](int c) { return l2s[c]; }, madd, true, 128, lim, hi);
+          else
+            bwd_p_keepbits(pr, sf, [&](int c) { return l2s[c]; }, mw, lim, hi);
         } else {
+          uint32_t aw[4];
+          allowed_words(aw, aw, false, lim, hi);
 #pragma unroll
           for (int c = 0; c < 128; c += 2) {
             float x0, x1;
             ffma2(x0, x1, pr[c], pr[c + 1], sf, sf, -l2s[c], -l2s[c + 1]);
-            pr[c] = (c < lim || c >= hi) ? 0.0f : ex2(x0);
-            pr[c + 1] = (c + 1 < lim || c + 1 >= hi) ? 0.0f : ex2(x1);
+            pr[c] = (aw[c >> 5] & (1u << (c & 31))) ? ex2(x0) : 0.0f;
+            pr[c + 1] = (aw[c >> 5] & (2u << (c & 31))) ? ex2(x1) : 0.0f;
           }
         }
       } else {
@@ -1084,11 +1145,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         auto dsub = [&](int c) { return l2s[C::kTile + c]; };
         auto l2c = [&](int c) { return l2s[c]; };
         auto kword = [&](int cc) { return keep_words[cc]; };
-        if (p.softcap_on)
-          bwd_ds_pass_drop<C, true, true>(tDP, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
+        if (!C::kMask && p.softcap_on)
+          bwd_ds_pass_drop<C, !C::kMask, true>(tDP, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
         else
           bwd_ds_pass_drop<C, false, true>(tDP, pr, dsub, l2c, 0.0f, kword, p.drop_scale);
-      } else if (C::kFeat && p.softcap_on) {
+      } else if (C::kFeat && !C::kMask && p.softcap_on) {
         bwd_ds_pass_softcap<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; }, [&](int c) { return l2s[c]; },
                                p.softcap_inv);
       } else {
@@ -1336,6 +1397,26 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (L != -INFINITY) l2 = L * kLog2e;
       di = p.dvec[rowi];
     }
+    // The forward's mask on this row: keep bits of a 128-key block (16 bytes,
+    // fetched a block ahead into registers) or the additive row (fetched a
+    // block ahead into L2, then loaded into registers before S_j lands).
+    auto rbits_at = [&](int kb) {
+      return reinterpret_cast<const uint4*>(p.mask_rbits + (((long long)b * p.Hq + h) * p.qL + i) * p.mask_rbits_ld +
+                                            kb / 32);
+    };
+    auto mrow_at = [&](int kb) {
+      return static_cast<const uint16_t*>(p.mask) + (long long)b * p.mask_sb + (long long)h * p.mask_sh +
+             (long long)i * p.mask_ss + kb;
+    };
+    uint4 rb_next = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (C::kMask) {
+      if (i < p.qL && n_blk > 0) {
+        if constexpr (C::kMaskKind == 1)
+          rb_next = __ldg(rbits_at(jb0 * C::kTile));
+        else
+          prefetch_row_l2(mrow_at(jb0 * C::kTile), 2 * min(128, p.kL - jb0 * C::kTile));
+      }
+    }
     bool ok = true;
     for (int j = 0; j < n_blk && ok; ++j) {
       const int kbase = (jb0 + j) * C::kTile;
@@ -1355,19 +1436,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // (the dQ kernel holds an additive mask's 64 words in registers: its rows
       // lie far apart in the mask, so reading them inside the P pass would
       // expose each load's latency)
-      uint32_t mw[64];
+      uint32_t mw[C::kMaskKind == 2 ? 64 : 4];
       if constexpr (C::kMask) {
-        if (p.mask_kind == 1 && i < p.qL) {  // keep bits of block j's 128 keys, in mw[0..3]
-          const uint4 kb = __ldg(reinterpret_cast<const uint4*>(
-              p.mask_rbits + (((long long)b * p.Hq + h) * p.qL + i) * p.mask_rbits_ld + kbase / 32));
-          mw[0] = kb.x;
-          mw[1] = kb.y;
-          mw[2] = kb.z;
-          mw[3] = kb.w;
-        } else if (p.mask_kind == 2 && i < p.qL) {
-          const uint16_t* row = static_cast<const uint16_t*>(p.mask) + (long long)b * p.mask_sb +
-                                (long long)h * p.mask_sh + (long long)i * p.mask_ss + kbase;
-          bwd_load_additive128(mw, row, p.mask_vec != 0 && kbase + 128 <= p.kL, min(128, p.kL - kbase));
+        if (i < p.qL) {
+          const bool more = j + 1 < n_blk;
+          if constexpr (C::kMaskKind == 1) {  // keep bits of block j's 128 keys
+            mw[0] = rb_next.x;
+            mw[1] = rb_next.y;
+            mw[2] = rb_next.z;
+            mw[3] = rb_next.w;
+            if (more) rb_next = __ldg(rbits_at(kbase + C::kTile));
+          } else {
+            bwd_load_additive128(mw, mrow_at(kbase), p.mask_vec != 0 && kbase + 128 <= p.kL, min(128, p.kL - kbase));
+            if (more) prefetch_row_l2(mrow_at(kbase + C::kTile), 2 * min(128, p.kL - kbase - C::kTile));
+          }
         }
       }
       ok = warp_wait(&ctl->s_full, j & 1, abort_flag, p.status, p.timeout_cycles);
@@ -1388,7 +1470,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (p.causal) lim = min(lim, i + 1 - kbase);
       }
       float sq = sl;
-      if constexpr (C::kFeat) {
+      if constexpr (C::kFeat && !C::kMask) {
         if (p.softcap_on) {  // base-2 capped score, as the forward computes it
           const float kin = p.softcap_kin, cout = p.softcap_out;
 #pragma unroll
@@ -1396,18 +1478,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           sq = 1.0f;
         }
       }
-      if (C::kMask && p.mask_kind == 2 && i < p.qL) {
-        bwd_p_additive_regs<C>(pr, sq, [&](int) { return l2; }, mw, lo, lim);
-      } else if (C::kMask && p.mask_kind == 1 && i < p.qL) {
-        bwd_p_keepbits(pr, sq, [&](int) { return l2; }, mw, lo, lim);
+      if (C::kMask && i < p.qL) {
+        if constexpr (C::kMaskKind == 2)
+          bwd_p_additive_regs<C>(pr, sq, [&](int) { return l2; }, mw, lo, lim);
+        else
+          bwd_p_keepbits(pr, sq, [&](int) { return l2; }, mw, lo, lim);
       } else {
+        uint32_t aw[4];
+        if constexpr (C::kFeat) allowed_words(aw, aw, false, lo, lim);
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
           float x0, x1;
           ffma2(x0, x1, pr[c], pr[c + 1], sq, sq, -l2, -l2);
           if constexpr (C::kFeat) {
-            pr[c] = (c < lim && c >= lo) ? ex2(x0) : 0.0f;
-            pr[c + 1] = (c + 1 < lim && c + 1 >= lo) ? ex2(x1) : 0.0f;
+            pr[c] = (aw[c >> 5] & (1u << (c & 31))) ? ex2(x0) : 0.0f;
+            pr[c + 1] = (aw[c >> 5] & (2u << (c & 31))) ? ex2(x1) : 0.0f;
           } else {
             pr[c] = c < lim ? ex2(x0) : 0.0f;
             pr[c + 1] = c + 1 < lim ? ex2(x1) : 0.0f;
@@ -1422,11 +1507,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         auto dsub = [&](int) { return di; };
         auto l2c = [&](int) { return l2; };
         auto kword = [&](int cc) { return kw[cc]; };
-        if (p.softcap_on)
-          bwd_ds_pass_drop<C, true, false>(tdp, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
+        if (!C::kMask && p.softcap_on)
+          bwd_ds_pass_drop<C, !C::kMask, false>(tdp, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
         else
           bwd_ds_pass_drop<C, false, false>(tdp, pr, dsub, l2c, 0.0f, kword, p.drop_scale);
-      } else if (C::kFeat && p.softcap_on) {
+      } else if (C::kFeat && !C::kMask && p.softcap_on) {
         bwd_ds_pass_softcap<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
                                p.softcap_inv);
       } else {

@@ -1,5 +1,5 @@
-// fa_bwd_mask.cu -- backward plans with the forward's bool or additive mask
-// (with or without dropout, window and offset).
+// fa_bwd_mask.cu -- backward plans with the forward's bool mask (with or
+// without dropout, window and offset).
 #include "fa_bwd_impl.cuh"
 
 namespace fa {
@@ -7,13 +7,11 @@ namespace fa {
 int launch_bwd_mask(const BwdLaunchArgs& a) {
   using namespace bwd_impl;
   if (a.dropout_p != 0.0f) {
-    if (a.f16)
-      return a.D == 64 ? launch_bwd_d<64, true, true, true, true>(a) : launch_bwd_d<128, true, true, true, true>(a);
-    return a.D == 64 ? launch_bwd_d<64, false, true, true, true>(a) : launch_bwd_d<128, false, true, true, true>(a);
+    if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true, true, 1>(a) : launch_bwd_d<128, true, true, true, 1>(a);
+    return a.D == 64 ? launch_bwd_d<64, false, true, true, 1>(a) : launch_bwd_d<128, false, true, true, 1>(a);
   }
-  if (a.f16)
-    return a.D == 64 ? launch_bwd_d<64, true, true, false, true>(a) : launch_bwd_d<128, true, true, false, true>(a);
-  return a.D == 64 ? launch_bwd_d<64, false, true, false, true>(a) : launch_bwd_d<128, false, true, false, true>(a);
+  if (a.f16) return a.D == 64 ? launch_bwd_d<64, true, true, false, 1>(a) : launch_bwd_d<128, true, true, false, 1>(a);
+  return a.D == 64 ? launch_bwd_d<64, false, true, false, 1>(a) : launch_bwd_d<128, false, true, false, 1>(a);
 }
 
 }  // namespace fa

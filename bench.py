@@ -60,7 +60,7 @@ def kernel_sources(w: workloads.Workload, kind: str = "fwd") -> list:
     elif w.D == 256:
         plan = ("fa_bwd256_kernel.cuh", "fa_bwd256.cu")
     elif w.mask_kind:
-        plan = ("fa_bwd_mask.cu",)
+        plan = ("fa_bwd_mask.cu",) if w.mask_kind == 1 else ("fa_bwd_mask_add.cu",)
     elif w.dropout_p > 0:
         plan = ("fa_bwd_drop.cu",)
     elif w.window or w.softcap or w.q_offset:

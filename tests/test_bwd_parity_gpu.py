@@ -274,6 +274,14 @@ MASKED = [
     S("bwd_mask_add_d128_window", 1, 2, 2, 300, 300, 128, "bf16", causal=True, mask_kind=W.MASK_ADDITIVE,
       window=100, seed=76),
     S("bwd_mask_add_d128_gqa_long_kv", 1, 4, 1, 130, 520, 128, "bf16", mask_kind=W.MASK_ADDITIVE, seed=77),
+    # causal with the diagonal moved right (kL > qL): the mask pre-passes skip the tiles no row of which
+    # sees any key, on a 128 (bool) or 64 (additive) grid that the offset does not align with
+    S("bwd_mask_bool_causal_offset", 1, 2, 2, 200, 456, 128, "bf16", causal=True, q_offset=200,
+      mask_kind=W.MASK_BOOL, seed=80),
+    S("bwd_mask_add_d64_causal_offset", 1, 2, 1, 300, 520, 64, "bf16", causal=True, q_offset=220,
+      mask_kind=W.MASK_ADDITIVE, seed=81),
+    S("bwd_mask_bool_negative_offset", 1, 2, 2, 300, 300, 64, "bf16", causal=True, q_offset=-150,
+      mask_kind=W.MASK_BOOL, seed=82),
 ]
 
 
