@@ -34,11 +34,12 @@ int set_smem_once(const void* kern, uint32_t bytes, std::atomic<unsigned long lo
   return 0;
 }
 
-template <int kD, bool kF16, bool kFeat, bool kDrop = false, int kMask = 0>
+template <int kD, bool kF16, bool kFeat, bool kDrop = false, int kMask = 0, bool kCap = false>
 int launch_bwd_d(const BwdLaunchArgs& a) {
-  using C = BwdCfg<kD, kF16, kFeat, kDrop, kMask>;
-  if (a.mask_kind != kMask) {
-    set_error("backward plan for mask kind %d given mask kind %d", kMask, a.mask_kind);
+  using C = BwdCfg<kD, kF16, kFeat, kDrop, kMask, kCap>;
+  if (a.mask_kind != kMask || (!kCap && a.softcap != 0.0f)) {
+    set_error("backward plan for mask kind %d%s given mask kind %d, softcap %g", kMask, kCap ? " with a softcap" : "",
+              a.mask_kind, (double)a.softcap);
     return 2;
   }
   // 1. D_i = rowsum(O_i * dO_i)

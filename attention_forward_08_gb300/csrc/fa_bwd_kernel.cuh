@@ -93,7 +93,8 @@ struct BwdParams {
   long long timeout_cycles;
 };
 
-template <int kD_, bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false, int kMask_ = 0>
+template <int kD_, bool kF16_ = false, bool kFeat_ = false, bool kDrop_ = false, int kMask_ = 0,
+          bool kCap_ = kFeat_ && kMask_ == 0>
 struct BwdCfg {
   static constexpr int kD = kD_;
   // 16-bit I/O is bf16 unless kF16 (fp16): same kernels, other operand format.
@@ -112,6 +113,10 @@ struct BwdCfg {
   static constexpr bool kMask = kMask_ != 0;
   static_assert(kMask_ >= 0 && kMask_ <= 2, "mask kinds: 0 none, 1 bool, 2 additive");
   static_assert(!kMask || kFeat, "the mask instantiation includes the other features");
+  // The softcap's code (a feature kernel's option; its own instantiations, so
+  // that window, offset and dropout kernels without a softcap carry none).
+  static constexpr bool kCap = kCap_;
+  static_assert(!kCap || (kFeat && !kMask), "the softcap needs the feature kernels and no mask");
   static constexpr uint32_t kFmt = kF16 ? kFmtF16 : kFmtBf16;
   static constexpr CUtensorMapDataType kTmaType =
       kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -1083,7 +1088,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         int lim = p.causal ? j - p.q_offset - q0 : -(1 << 30);
         int hi = p.window > 0 ? j - p.q_offset + p.window - q0 : (1 << 30);
         if (j >= p.kL) lim = C::kTile;
-        const bool capped = !C::kMask && p.softcap_on;  // a mask excludes the softcap
+        const bool capped = C::kCap && p.softcap_on;
         if (capped) {  // base-2 capped score, as the forward computes it
           const float kin = p.softcap_kin, cout = p.softcap_out;
 #pragma unroll
@@ -1145,11 +1150,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         auto dsub = [&](int c) { return l2s[C::kTile + c]; };
         auto l2c = [&](int c) { return l2s[c]; };
         auto kword = [&](int cc) { return keep_words[cc]; };
-        if (!C::kMask && p.softcap_on)
-          bwd_ds_pass_drop<C, !C::kMask, true>(tDP, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
+        if (C::kCap && p.softcap_on)
+          bwd_ds_pass_drop<C, C::kCap, true>(tDP, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
         else
           bwd_ds_pass_drop<C, false, true>(tDP, pr, dsub, l2c, 0.0f, kword, p.drop_scale);
-      } else if (C::kFeat && !C::kMask && p.softcap_on) {
+      } else if (C::kCap && p.softcap_on) {
         bwd_ds_pass_softcap<C>(tDP, pr, [&](int c) { return l2s[C::kTile + c]; }, [&](int c) { return l2s[c]; },
                                p.softcap_inv);
       } else {
@@ -1470,7 +1475,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (p.causal) lim = min(lim, i + 1 - kbase);
       }
       float sq = sl;
-      if constexpr (C::kFeat && !C::kMask) {
+      if constexpr (C::kCap) {
         if (p.softcap_on) {  // base-2 capped score, as the forward computes it
           const float kin = p.softcap_kin, cout = p.softcap_out;
 #pragma unroll
@@ -1507,11 +1512,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         auto dsub = [&](int) { return di; };
         auto l2c = [&](int) { return l2; };
         auto kword = [&](int cc) { return kw[cc]; };
-        if (!C::kMask && p.softcap_on)
-          bwd_ds_pass_drop<C, !C::kMask, false>(tdp, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
+        if (C::kCap && p.softcap_on)
+          bwd_ds_pass_drop<C, C::kCap, false>(tdp, pr, dsub, l2c, p.softcap_inv, kword, p.drop_scale);
         else
           bwd_ds_pass_drop<C, false, false>(tdp, pr, dsub, l2c, 0.0f, kword, p.drop_scale);
-      } else if (C::kFeat && !C::kMask && p.softcap_on) {
+      } else if (C::kCap && p.softcap_on) {
         bwd_ds_pass_softcap<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
                                p.softcap_inv);
       } else {

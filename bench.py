@@ -62,9 +62,9 @@ def kernel_sources(w: workloads.Workload, kind: str = "fwd") -> list:
     elif w.mask_kind:
         plan = ("fa_bwd_mask.cu",) if w.mask_kind == 1 else ("fa_bwd_mask_add.cu",)
     elif w.dropout_p > 0:
-        plan = ("fa_bwd_drop.cu",)
+        plan = ("fa_bwd_drop.cu",) + (("fa_bwd_drop_cap.cu",) if w.softcap else ())
     elif w.window or w.softcap or w.q_offset:
-        plan = ("fa_bwd_feat.cu",)
+        plan = ("fa_bwd_feat.cu",) + (("fa_bwd_feat_cap.cu",) if w.softcap else ())
     else:
         plan = ()
     return KERNEL_SOURCES + [CSRC + f for f in common + plan]
