@@ -168,6 +168,7 @@ struct Cfg {
       kAliasP && !kTf32 && 1024 + kOffDrop + kDropBytes + kOStageBytes + kBarBytes <= 232448;
   static constexpr uint32_t kOffOStage = kOffDrop + kDropBytes;
   static constexpr uint32_t kOffBar = kOffOStage + (kOStage ? kOStageBytes : 0);
+  static_assert(!kOStage || kOffOStage % 1024 == 0, "the O staging slots are 128-byte-swizzled TMA boxes");
   static constexpr uint32_t kSmemBytes = 1024 + kOffBar + kBarBytes;  // + alignment slack
 
   static_assert(kD % kChunk == 0, "head dim must be a whole number of 128-byte rows");
@@ -947,7 +948,7 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmM,
-                  const FaParams p) {
+                  const __grid_constant__ CUtensorMap tmO, const FaParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -1537,15 +1538,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if constexpr (C::kOStage) {
           // Through this warp's staging slot, one 128-byte column block (64
           // columns) at a time: each lane writes its row's eight 16-byte pieces
-          // (piece k of row r at r * 128 + (k ^ (r & 7)) * 16: conflict-free),
-          // then each group of 8 lanes reads one row back and stores it whole.
+          // (piece k of row r at r * 128 + (k ^ (r & 7)) * 16: conflict-free,
+          // and the layout of a 128-byte-swizzled TMA box of 32 rows), then one
+          // lane hands the block to a TMA store (rows past qL are clipped).
           uint8_t* slot = smem + C::kOffOStage + (warp - 4) * (32 * 128);
-          uint8_t* obase = static_cast<uint8_t*>(p.o) + ((long long)b * p.o_sb + (long long)h * p.o_sh) * C::kEsz;
-          const long long row_bytes = p.o_ss * C::kEsz;
           const int wrow0 = row - lane;  // the warp's first row
 #pragma unroll
           for (int hh = 0; hh < kBatch / 2; ++hh) {
             const int blk = c0 / 2 + hh;  // 128-byte column block of the row
+            if (lane == 0) tma_store_wait_read0();  // the slot's previous store has read it
+            __syncwarp();
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint32_t(&rr)[32] = rb[2 * hh + k / 4];
@@ -1560,15 +1562,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               *reinterpret_cast<uint4*>(slot + lane * 128 + ((k ^ (lane & 7)) << 4)) =
                   make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            fence_proxy_async_smem();
             __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int lr = 4 * i + (lane >> 3), k = lane & 7;
-              const uint4 v = *reinterpret_cast<const uint4*>(slot + lr * 128 + ((k ^ (lr & 7)) << 4));
-              if (wrow0 + lr < p.qL)
-                *reinterpret_cast<uint4*>(obase + (long long)(wrow0 + lr) * row_bytes + blk * 128 + k * 16) = v;
+            if (lane == 0 && wrow0 < p.qL) {
+              tma_store_4d(&tmO, slot, blk * C::kChunk, wrow0, h, b);
+              tma_store_commit();
             }
-            __syncwarp();  // the slot is rewritten for the next column block
           }
         } else {
 #pragma unroll
@@ -1611,6 +1610,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
   }
 
+  if constexpr (C::kOStage) {
+    if (warp >= 4 && lane == 0) tma_store_wait0();  // the epilogue's O stores are complete
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

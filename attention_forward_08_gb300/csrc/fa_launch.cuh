@@ -211,6 +211,12 @@ int launch_fa_fwd(const LaunchArgs& a) {
   } else {
     if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, a.D, a.vs, C::kChunk, C::kBN)) return 4;
   }
+  // O as 32-row, 128-byte boxes for the staged epilogue's TMA stores.
+  CUtensorMap to;
+  std::memset(&to, 0, sizeof(to));
+  if constexpr (C::kOStage) {
+    if (!encode_bhsd(&to, C::kTmaType, a.o, a.B, a.Hq, a.qL, a.D, a.os, C::kChunk, 32)) return 4;
+  }
   FaParams p;
   setup_params<C>(a, tm, p);
   auto kern = fa_fwd_kernel<C>;
@@ -247,7 +253,7 @@ int launch_fa_fwd(const LaunchArgs& a) {
   long long grid = a.num_sms > 0 ? a.num_sms : 1;
   if (a.max_ctas > 0 && a.max_ctas < grid) grid = a.max_ctas;
   if (grid > units) grid = units;
-  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, tm, p);
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, tm, to, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("kernel launch failed: %s", cudaGetErrorString(e));

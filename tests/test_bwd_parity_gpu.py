@@ -260,6 +260,42 @@ def test_bwd_bench_dropout_workload_one_group(b, kvh):
     _compare(f"{w.name} b{b} kvh{kvh} dV", dv[b:b + 1, kvh:kvh + 1], rv)
 
 
+def test_bwd_bool_mask_workload_every_element():
+    """The benchmarked bool-mask backward (B1, H 8, L 2000, D 128; a tenth of the entries dropped,
+    the diagonal kept): the keep-bits pre-pass, 128 dK/dV and 128 dQ CTAs; every element of dQ, dK
+    and dV against the gradient oracle."""
+    _run_masked(W.WORKLOADS["bf16_bool_mask_h8_l2000_d128"])
+
+
+def test_bwd_bool_mask_bench_shape_one_group():
+    """A bool mask on the benchmarked causal shape (B2, H_q 32, H_kv 8, L 4096, D 128): the bits
+    pre-pass skips the tiles above the diagonal and the gradient kernels fetch each step's keep
+    words a step ahead, over up to 128 steps per dK/dV CTA.  dQ of one GQA group's four query
+    heads and dK, dV of its K/V head, element by element."""
+    import attention_forward_08_gb300 as fa
+    w = BENCH_BWD.with_(name="bwd_bool_mask_bench_shape", mask_kind=W.MASK_BOOL)
+    q, k, v, m = W.make_inputs(w)
+    do = W.make_dout(w)
+    dev = "cuda:0"
+    qd, kd, vd, dod, md = q.to(dev), k.to(dev), v.to(dev), do.to(dev), m.to(dev)
+    kw = dict(scale=w.sm_scale, causal=True, mask=md, mask_kind=W.MASK_BOOL)
+    o, lse = fa.attention(qd, kd, vd, **kw)
+    dq, dk, dv = fa.attention_bwd(qd, kd, vd, o, dod, lse, **kw)
+    assert fa.fa_sync_status(None) == fa.fa.FA_OK, fa.fa_last_error()
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    del qd, kd, vd, dod, md, o, lse
+    b, kvh = 1, 3
+    g = w.H_q // w.H_kv
+    heads = list(range(kvh * g, (kvh + 1) * g))
+    sl = lambda t: t[b:b + 1, heads].double().numpy()
+    rq, rk, rv = oracle.attention_bwd(sl(q), k[b:b + 1, kvh:kvh + 1].double().numpy(),
+                                      v[b:b + 1, kvh:kvh + 1].double().numpy(), sl(do), fp32_scale(w),
+                                      causal=True, mask=sl(m), mask_kind=W.MASK_BOOL)
+    _compare(f"{w.name} b{b} kvh{kvh} dQ", dq[b:b + 1, heads], rq)
+    _compare(f"{w.name} b{b} kvh{kvh} dK", dk[b:b + 1, kvh:kvh + 1], rk)
+    _compare(f"{w.name} b{b} kvh{kvh} dV", dv[b:b + 1, kvh:kvh + 1], rv)
+
+
 # The forward's mask in the backward (fa_bwd_full): bool (nonzero keeps) and additive (-inf excludes),
 # with causal, GQA, ragged tails, fp16, dropout and a sliding window; mask rows whose byte stride is not a
 # multiple of 16 take the element-wise load path.
