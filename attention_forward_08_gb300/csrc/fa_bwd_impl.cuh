@@ -62,6 +62,11 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   if (!encode_bhsd(&tdo, C::kTmaType, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kTile)) return 4;
   if (!encode_bhsd(&tk, C::kTmaType, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
   if (!encode_bhsd(&tv, C::kTmaType, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kTile)) return 4;
+  // the gradients as 32-row, 128-byte boxes for the epilogues' TMA stores
+  CUtensorMap tdq, tdk, tdv;
+  if (!encode_bhsd(&tdq, C::kTmaType, a.dq, a.B, a.Hq, a.qL, kD, qst, 64, 32)) return 4;
+  if (!encode_bhsd(&tdk, C::kTmaType, a.dk, a.B, a.Hkv, a.kL, kD, kst, 64, 32)) return 4;
+  if (!encode_bhsd(&tdv, C::kTmaType, a.dv, a.B, a.Hkv, a.kL, kD, kst, 64, 32)) return 4;
 
   BwdParams p;
   p.B = a.B;
@@ -169,14 +174,14 @@ int launch_bwd_d(const BwdLaunchArgs& a) {
   }
 
   // 5. dK, dV: one CTA per (128-key tile, kvh, b).
-  fa_bwd_dkdv_kernel<C><<<(unsigned)n_kv, C::kThreads, C::kKVSmem, a.stream>>>(tq, tk, tv, tdo, p);
+  fa_bwd_dkdv_kernel<C><<<(unsigned)n_kv, C::kThreads, C::kKVSmem, a.stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("dK/dV launch failed: %s", cudaGetErrorString(e));
     return 4;
   }
   // 6. dQ: one CTA per (128-row query tile, h, b).
-  fa_bwd_dq_kernel<C><<<(unsigned)n_q, C::kThreads, C::kQSmem, a.stream>>>(tq, tk, tv, tdo, p);
+  fa_bwd_dq_kernel<C><<<(unsigned)n_q, C::kThreads, C::kQSmem, a.stream>>>(tq, tk, tv, tdo, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("dQ launch failed: %s", cudaGetErrorString(e));

@@ -750,7 +750,9 @@ __device__ __forceinline__ void bwd_ds_pass_softcap(uint32_t tdp, const float (&
 }
 
 // Store a 128 x kD fp32 accumulator row (this thread's lane), times `mul`, in
-// the 16-bit I/O format to a contiguous row of global memory (16-byte stores).
+// the 16-bit I/O format to a contiguous row of global memory (16-byte stores;
+// the additive-mask kernels' epilogue, whose registers the staged one would
+// push into spills).
 template <class C>
 __device__ __forceinline__ void bwd_store_row(uint32_t tacc, float mul, uint16_t* dst, bool store) {
 #pragma unroll
@@ -773,6 +775,46 @@ __device__ __forceinline__ void bwd_store_row(uint32_t tacc, float mul, uint16_t
   }
 }
 
+// The epilogue of one fp32 accumulator through TMA stores: this warp's 32
+// rows (its TMEM lanes), scaled and packed to the I/O format, staged as kD / 64
+// boxes of 32 rows x 128 bytes with the 128-byte swizzle (row r's 16-byte
+// piece k at r * 128 + (k ^ (r & 7)) * 16: conflict-free) in `slot` -- ring
+// space that the finished MMAs no longer read, 1024-byte aligned -- then stored
+// by lane 0 at rows row0 .. row0 + 31 of (head, batch); rows past the tensor's
+// extent are clipped.  One TMEM load wait per 64 columns.
+template <class C>
+__device__ __forceinline__ void bwd_store_tile_tma(uint32_t tacc, float mul, uint8_t* slot, const CUtensorMap* map,
+                                                   int row0, int extent, int head, int batch, int lane) {
+  constexpr int kBlk = C::kD / 64;  // 128-byte column blocks
+#pragma unroll
+  for (int blk = 0; blk < kBlk; ++blk) {
+    uint32_t rr[2][32];
+    tmem_ld32(tacc + blk * 64, rr[0]);
+    tmem_ld32(tacc + blk * 64 + 32, rr[1]);
+    tmem_wait_ld();
+    reg_fence(rr[0]);
+    reg_fence(rr[1]);
+    uint8_t* box = slot + blk * (32 * 128);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // piece k: columns 8k .. 8k + 7 of the block
+      const uint32_t(&r)[32] = rr[k / 4];
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        pk[e] = pack16x2<C>(__uint_as_float(r[(k % 4) * 8 + 2 * e]) * mul,
+                            __uint_as_float(r[(k % 4) * 8 + 2 * e + 1]) * mul);
+      *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < extent) {
+#pragma unroll
+    for (int blk = 0; blk < kBlk; ++blk) tma_store_4d(map, slot + blk * (32 * 128), blk * 64, row0, head, batch);
+    tma_store_commit();
+  }
+}
+
 // ---------------------------------------------------------------- dK / dV
 
 // One CTA per (128-key tile, kvh, b), heavy (early) key tiles first.  It walks
@@ -783,6 +825,7 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1185,8 +1228,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
         if (ok) {
           tc_fence_after();
-          bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, C::kDrop ? p.drop_scale : 1.0f, dvp, store);
-          bwd_store_row<C>(tmem + lane_addr + C::kColAcc1, p.scale, dkp, store);
+          if constexpr (C::kMaskKind == 2) {
+            bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, C::kDrop ? p.drop_scale : 1.0f, dvp, store);
+            bwd_store_row<C>(tmem + lane_addr + C::kColAcc1, p.scale, dkp, store);
+          } else {  // staged in the Q and dO rings (every load of them consumed)
+            constexpr int kSlot = (C::kD / 64) * 32 * 128;
+            const int row0 = k0 + 32 * (warp & 3);
+            bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc0, C::kDrop ? p.drop_scale : 1.0f,
+                                  sQ + (warp & 3) * kSlot, &tmDV, row0, p.kL, kvh, b, lane);
+            bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc1, p.scale, sDO + (warp & 3) * kSlot, &tmDK, row0,
+                                  p.kL, kvh, b, lane);
+            if (lane == 0) tma_store_wait0();
+          }
         }
       }
     }
@@ -1208,6 +1261,7 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const __grid_constant__ CUtensorMap tmDQ,
                      const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1539,7 +1593,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
         if (ok) {
           tc_fence_after();
-          bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, p.scale, dqp, store);
+          if constexpr (C::kMaskKind == 2) {
+            bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, p.scale, dqp, store);
+          } else {  // staged in the K ring (every load of it consumed)
+            constexpr int kSlot = (C::kD / 64) * 32 * 128;
+            bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc0, p.scale, sK + (warp & 3) * kSlot, &tmDQ,
+                                  q0 + 32 * (warp & 3), p.qL, h, b, lane);
+            if (lane == 0) tma_store_wait0();
+          }
         }
       }
     }
