@@ -43,6 +43,11 @@ int launch_bwd256_t(const BwdLaunchArgs& a) {
   if (!encode_bhsd(&q_do, C::kTmaType, a.dout, a.B, a.Hq, a.qL, kD, qst, 64, C::kQT)) return 4;
   if (!encode_bhsd(&q_k, C::kTmaType, a.k, a.B, a.Hkv, a.kL, kD, kst, 64, C::kKB)) return 4;
   if (!encode_bhsd(&q_v, C::kTmaType, a.v, a.B, a.Hkv, a.kL, kD, kst, 64, C::kKB)) return 4;
+  // the gradients as 32-row, 128-byte boxes for the epilogues' TMA stores
+  CUtensorMap t_dq, t_dk, t_dv;
+  if (!encode_bhsd(&t_dq, C::kTmaType, a.dq, a.B, a.Hq, a.qL, kD, qst, 64, 32)) return 4;
+  if (!encode_bhsd(&t_dk, C::kTmaType, a.dk, a.B, a.Hkv, a.kL, kD, kst, 64, 32)) return 4;
+  if (!encode_bhsd(&t_dv, C::kTmaType, a.dv, a.B, a.Hkv, a.kL, kD, kst, 64, 32)) return 4;
 
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -76,14 +81,15 @@ int launch_bwd256_t(const BwdLaunchArgs& a) {
     return 2;
   }
   // 3. dK, dV: two CTAs (halves of D) per (128-key tile, kvh, b).
-  fa_bwd256_dkdv_kernel<C><<<(unsigned)n_kv, C::kThreads, C::kKVSmem, a.stream>>>(kv_q, kv_k, kv_v, kv_do, p);
+  fa_bwd256_dkdv_kernel<C><<<(unsigned)n_kv, C::kThreads, C::kKVSmem, a.stream>>>(kv_q, kv_k, kv_v, kv_do, t_dk, t_dv,
+                                                                                 p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("dK/dV launch failed: %s", cudaGetErrorString(e));
     return 4;
   }
   // 4. dQ: one CTA per (128-row query tile, h, b).
-  fa_bwd256_dq_kernel<C><<<(unsigned)n_q, C::kThreads, C::kQSmem, a.stream>>>(q_q, q_k, q_v, q_do, p);
+  fa_bwd256_dq_kernel<C><<<(unsigned)n_q, C::kThreads, C::kQSmem, a.stream>>>(q_q, q_k, q_v, q_do, t_dq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("dQ launch failed: %s", cudaGetErrorString(e));

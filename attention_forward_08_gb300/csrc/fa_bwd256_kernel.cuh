@@ -58,6 +58,10 @@ struct Bwd256Cfg {
   static constexpr int kColS = 0, kColDP = 64, kColDP2 = 128, kColDQ = 256;
   static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "shared memory overflow");
   static_assert(kColDK + kHalfD <= 512 && kColDQ + kD <= 512, "TMEM overflow");
+  // The epilogues stage their gradients in rings the finished MMAs no longer read.
+  static_assert(kQStages * kQSBytes >= kKT * kHalfD * 2 && kDOStages * kQSBytes >= kKT * kHalfD * 2 &&
+                    kKStages * kKBBytes >= kQT * kD * 2,
+                "epilogue staging space");
 };
 
 struct Bwd256KVCtrl {
@@ -121,29 +125,6 @@ __device__ __forceinline__ void bwd256_ds_pass(uint32_t tdp, const float (&p)[64
   }
 }
 
-// Store kCols fp32 TMEM columns of this lane, times `mul`, as 16-bit values (16-byte stores).
-template <class C, int kCols>
-__device__ __forceinline__ void bwd256_store_row(uint32_t tacc, float mul, uint16_t* dst, bool store) {
-#pragma unroll
-  for (int cc = 0; cc < kCols / 32; ++cc) {
-    uint32_t rr[32];
-    tmem_ld32(tacc + cc * 32, rr);
-    tmem_wait_ld();
-    reg_fence(rr);
-    if (store) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          pk[e] = pack16x2<C>(__uint_as_float(rr[8 * u + 2 * e]) * mul, __uint_as_float(rr[8 * u + 2 * e + 1]) * mul);
-        d4[u] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------- dK / dV
 
 // Grid: 2 CTAs (D halves) per (128-key tile, kvh, b), heavy (early) key tiles first.
@@ -151,6 +132,7 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_bwd256_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                          const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                           const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -421,8 +403,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
         if (ok) {
           tc_fence_after();
-          bwd256_store_row<C, C::kHalfD>(tmem + lane_addr + C::kColDV, 1.0f, dvp, store);
-          bwd256_store_row<C, C::kHalfD>(tmem + lane_addr + C::kColDK, p.scale, dkp, store);
+          // this CTA's column half of dV and dK, staged in the Q and dO rings (every load consumed)
+          constexpr int kSlot = (C::kHalfD / 64) * 32 * 128;
+          const int row0 = k0 + 32 * (warp & 3);
+          bwd_store_tile_tma<C, C::kHalfD>(tmem + lane_addr + C::kColDV, 1.0f, sQ + (warp & 3) * kSlot, &tmDV,
+                                           half * C::kHalfD, row0, p.kL, kvh, b, lane);
+          bwd_store_tile_tma<C, C::kHalfD>(tmem + lane_addr + C::kColDK, p.scale, sDO + (warp & 3) * kSlot, &tmDK,
+                                           half * C::kHalfD, row0, p.kL, kvh, b, lane);
+          if (lane == 0) tma_store_wait0();
         }
       }
     }
@@ -444,7 +432,7 @@ template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_bwd256_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                        const BwdParams p) {
+                        const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -655,7 +643,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
         if (ok) {
           tc_fence_after();
-          bwd256_store_row<C, C::kD>(tmem + lane_addr + C::kColDQ, p.scale, dqp, store);
+          // staged in the K ring (every load consumed)
+          constexpr int kSlot = (C::kD / 64) * 32 * 128;
+          bwd_store_tile_tma<C, C::kD>(tmem + lane_addr + C::kColDQ, p.scale, sK + (warp & 3) * kSlot, &tmDQ, 0,
+                                       q0 + 32 * (warp & 3), p.qL, h, b, lane);
+          if (lane == 0) tma_store_wait0();
         }
       }
     }

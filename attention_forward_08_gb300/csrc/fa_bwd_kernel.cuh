@@ -153,6 +153,9 @@ struct BwdCfg {
   static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "shared memory overflow");
   static_assert(kColAcc1 + kD <= 512, "TMEM overflow");
   static_assert(kColAcc0 + kD <= kColDP2 && kColDP2 + 128 <= 512, "dQ kernel TMEM overflow");
+  // The epilogues stage their gradients in rings the finished MMAs no longer read.
+  static_assert(kStages * kTileBytes >= kTile * kD * 2 && kQKStages * kTileBytes >= kTile * kD * 2,
+                "epilogue staging space");
 };
 
 struct BwdKVCtrl {
@@ -775,17 +778,18 @@ __device__ __forceinline__ void bwd_store_row(uint32_t tacc, float mul, uint16_t
   }
 }
 
-// The epilogue of one fp32 accumulator through TMA stores: this warp's 32
-// rows (its TMEM lanes), scaled and packed to the I/O format, staged as kD / 64
-// boxes of 32 rows x 128 bytes with the 128-byte swizzle (row r's 16-byte
-// piece k at r * 128 + (k ^ (r & 7)) * 16: conflict-free) in `slot` -- ring
-// space that the finished MMAs no longer read, 1024-byte aligned -- then stored
-// by lane 0 at rows row0 .. row0 + 31 of (head, batch); rows past the tensor's
-// extent are clipped.  One TMEM load wait per 64 columns.
-template <class C>
+// The epilogue of one fp32 accumulator through TMA stores: kCols columns of
+// this warp's 32 rows (its TMEM lanes), scaled and packed to the I/O format,
+// staged as kCols / 64 boxes of 32 rows x 128 bytes with the 128-byte swizzle
+// (row r's 16-byte piece k at r * 128 + (k ^ (r & 7)) * 16: conflict-free) in
+// `slot` -- ring space that the finished MMAs no longer read, 1024-byte
+// aligned -- then stored by lane 0 at columns x0 .., rows row0 .. row0 + 31 of
+// (head, batch); rows past the tensor's extent are clipped.  One TMEM load
+// wait per 64 columns.
+template <class C, int kCols = C::kD>
 __device__ __forceinline__ void bwd_store_tile_tma(uint32_t tacc, float mul, uint8_t* slot, const CUtensorMap* map,
-                                                   int row0, int extent, int head, int batch, int lane) {
-  constexpr int kBlk = C::kD / 64;  // 128-byte column blocks
+                                                   int x0, int row0, int extent, int head, int batch, int lane) {
+  constexpr int kBlk = kCols / 64;  // 128-byte column blocks
 #pragma unroll
   for (int blk = 0; blk < kBlk; ++blk) {
     uint32_t rr[2][32];
@@ -810,7 +814,7 @@ __device__ __forceinline__ void bwd_store_tile_tma(uint32_t tacc, float mul, uin
   __syncwarp();
   if (lane == 0 && row0 < extent) {
 #pragma unroll
-    for (int blk = 0; blk < kBlk; ++blk) tma_store_4d(map, slot + blk * (32 * 128), blk * 64, row0, head, batch);
+    for (int blk = 0; blk < kBlk; ++blk) tma_store_4d(map, slot + blk * (32 * 128), x0 + blk * 64, row0, head, batch);
     tma_store_commit();
   }
 }
@@ -1235,8 +1239,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             constexpr int kSlot = (C::kD / 64) * 32 * 128;
             const int row0 = k0 + 32 * (warp & 3);
             bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc0, C::kDrop ? p.drop_scale : 1.0f,
-                                  sQ + (warp & 3) * kSlot, &tmDV, row0, p.kL, kvh, b, lane);
-            bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc1, p.scale, sDO + (warp & 3) * kSlot, &tmDK, row0,
+                                  sQ + (warp & 3) * kSlot, &tmDV, 0, row0, p.kL, kvh, b, lane);
+            bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc1, p.scale, sDO + (warp & 3) * kSlot, &tmDK, 0, row0,
                                   p.kL, kvh, b, lane);
             if (lane == 0) tma_store_wait0();
           }
@@ -1597,7 +1601,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             bwd_store_row<C>(tmem + lane_addr + C::kColAcc0, p.scale, dqp, store);
           } else {  // staged in the K ring (every load of it consumed)
             constexpr int kSlot = (C::kD / 64) * 32 * 128;
-            bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc0, p.scale, sK + (warp & 3) * kSlot, &tmDQ,
+            bwd_store_tile_tma<C>(tmem + lane_addr + C::kColAcc0, p.scale, sK + (warp & 3) * kSlot, &tmDQ, 0,
                                   q0 + 32 * (warp & 3), p.qL, h, b, lane);
             if (lane == 0) tma_store_wait0();
           }

@@ -33,11 +33,12 @@ bool encode_rows(CUtensorMap* m, const void* ptr, int B, int H, int rows, int D,
 
 template <class C>
 int launch_role(const CUtensorMap& r0, const CUtensorMap& r1, const CUtensorMap& t0, const CUtensorMap& t1,
-                const CUtensorMap& t2, const BwdParams& p, long long grid, cudaStream_t stream, const char* what) {
+                const CUtensorMap& t2, const CUtensorMap& out, const BwdParams& p, long long grid, cudaStream_t stream,
+                const char* what) {
   static std::atomic<unsigned long long> cfg{0};
   if (int rc = bwd_impl::set_smem_once<C>((const void*)fa_bwd_tf32_kernel<C>, C::kSmem, cfg)) return rc;
   if (grid <= 0) return 0;
-  fa_bwd_tf32_kernel<C><<<(unsigned)grid, C::kThreads, C::kSmem, stream>>>(r0, r1, t0, t1, t2, p);
+  fa_bwd_tf32_kernel<C><<<(unsigned)grid, C::kThreads, C::kSmem, stream>>>(r0, r1, t0, t1, t2, out, p);
   return check(what);
 }
 
@@ -100,6 +101,11 @@ int launch_tf32_d(const BwdLaunchArgs& a) {
       !encode_vt(&mdot, dot, a.B, a.Hq, (int)l.qt_row, kD, l.qt_row) ||
       !encode_vt(&mkt, kt, a.B, a.Hkv, (int)l.kt_row, kD, l.kt_row))
     return 4;
+  // the gradients as 32-row, 128-byte boxes for the epilogues' TMA stores
+  CUtensorMap odq, odk, odv;
+  if (!encode_rows(&odq, a.dq, a.B, a.Hq, a.qL, kD, 32) || !encode_rows(&odk, a.dk, a.B, a.Hkv, a.kL, kD, 32) ||
+      !encode_rows(&odv, a.dv, a.B, a.Hkv, a.kL, kD, 32))
+    return 4;
 
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -128,9 +134,9 @@ int launch_tf32_d(const BwdLaunchArgs& a) {
     return 2;
   }
   // 4. dV (K resident; Q, dO^T streamed), dK (K, V; Q, dO, Q^T), dQ (Q, dO; K, V, K^T).
-  if (int rc = launch_role<CV>(k128, k128, q64, q64, mdot, p, n_kv, a.stream, "dV")) return rc;
-  if (int rc = launch_role<CK>(k128, v128, q64, do64, mqt, p, n_kv, a.stream, "dK")) return rc;
-  return launch_role<CQ>(q128, do128, k64, v64, mkt, p, n_q, a.stream, "dQ");
+  if (int rc = launch_role<CV>(k128, k128, q64, q64, mdot, odv, p, n_kv, a.stream, "dV")) return rc;
+  if (int rc = launch_role<CK>(k128, v128, q64, do64, mqt, odk, p, n_kv, a.stream, "dK")) return rc;
+  return launch_role<CQ>(q128, do128, k64, v64, mkt, odq, p, n_q, a.stream, "dQ");
 }
 
 }  // namespace

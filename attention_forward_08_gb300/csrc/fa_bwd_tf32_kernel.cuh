@@ -64,6 +64,8 @@ struct BwdT32Cfg {
   static_assert(kD == 64 || kD == 128, "fp32 backward head dims: 64 or 128");
   static_assert(kStages >= 1 && kSmem <= 232448, "shared memory overflow");
   static_assert(kColAcc + kD <= 512, "TMEM overflow");
+  // The epilogue stages the 128-row output tile in the streamed rings (idle by then).
+  static_assert(kOffLD - kOffT0 >= kRows * kD * 4, "epilogue staging space");
 };
 
 struct BwdT32Ctrl {
@@ -112,13 +114,51 @@ __device__ __forceinline__ void t32_store64(uint32_t taddr, const float (&x)[64]
   }
 }
 
+// The epilogue through TMA stores: this warp's 32 rows (its TMEM lanes) of
+// the kD-column fp32 accumulator, times `mul`, staged as kD / 32 boxes of 32
+// rows x 128 bytes (32 floats) with the 128-byte swizzle (row r's 16-byte piece
+// k at r * 128 + (k ^ (r & 7)) * 16) in `slot` -- the streamed rings, idle once
+// every MMA has finished; 1024-byte aligned -- then stored by lane 0 at rows
+// row0 .. row0 + 31 of (head, batch), clipped past the extent.  One TMEM load
+// wait per 64 columns.
+template <class C>
+__device__ __forceinline__ void t32_store_tile_tma(uint32_t tacc, float mul, uint8_t* slot, const CUtensorMap* map,
+                                                   int row0, int extent, int head, int batch, int lane) {
+#pragma unroll
+  for (int hh = 0; hh < C::kD / 64; ++hh) {
+    uint32_t rr[2][32];
+    tmem_ld32(tacc + hh * 64, rr[0]);
+    tmem_ld32(tacc + hh * 64 + 32, rr[1]);
+    tmem_wait_ld();
+    reg_fence(rr[0]);
+    reg_fence(rr[1]);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint8_t* box = slot + (2 * hh + q) * (32 * 128);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)  // piece k: columns 4k .. 4k + 3 of the box
+        *reinterpret_cast<float4*>(box + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+            make_float4(__uint_as_float(rr[q][4 * k]) * mul, __uint_as_float(rr[q][4 * k + 1]) * mul,
+                        __uint_as_float(rr[q][4 * k + 2]) * mul, __uint_as_float(rr[q][4 * k + 3]) * mul);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < extent) {
+#pragma unroll
+    for (int bx = 0; bx < C::kD / 32; ++bx) tma_store_4d(map, slot + bx * (32 * 128), bx * 32, row0, head, batch);
+    tma_store_commit();
+  }
+}
+
 // Grid: dV, dK -- one CTA per (128-key tile, kvh, b); dQ -- one CTA per
 // (128-row query tile, h, b).  Causal: heavy tiles first; else head-major.
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_bwd_tf32_kernel(const __grid_constant__ CUtensorMap tmR0, const __grid_constant__ CUtensorMap tmR1,
                        const __grid_constant__ CUtensorMap tmT0, const __grid_constant__ CUtensorMap tmT1,
-                       const __grid_constant__ CUtensorMap tmT2, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmT2, const __grid_constant__ CUtensorMap tmOut,
+                       const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sR0 = smem;
@@ -466,20 +506,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         ok = warp_wait(&ctl->done, 0, abort_flag, p.status, p.timeout_cycles);
         if (ok) {
           tc_fence_after();
-#pragma unroll
-          for (int cc = 0; cc < C::kD / 32; ++cc) {
-            uint32_t rr[32];
-            tmem_ld32(tmem + lane_addr + C::kColAcc + cc * 32, rr);
-            tmem_wait_ld();
-            reg_fence(rr);
-            if (store) {
-              float4* o4 = reinterpret_cast<float4*>(out + cc * 32);
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                o4[u] = make_float4(__uint_as_float(rr[4 * u]) * mul, __uint_as_float(rr[4 * u + 1]) * mul,
-                                    __uint_as_float(rr[4 * u + 2]) * mul, __uint_as_float(rr[4 * u + 3]) * mul);
-            }
-          }
+          // staged in the streamed rings (every load of them consumed)
+          constexpr int kSlot = (C::kD / 32) * 32 * 128;
+          t32_store_tile_tma<C>(tmem + lane_addr + C::kColAcc, mul, smem + C::kOffT0 + (warp & 3) * kSlot, &tmOut,
+                                r0 + 32 * (warp & 3), n_out, rh, b, lane);
+          if (lane == 0) tma_store_wait0();
         }
       }
     }
