@@ -25,6 +25,10 @@ SMALL = [
     S("bf16_d128_plain", 1, 2, 2, 384, 384, 128, "bf16"),
     S("bf16_d128_causal_gqa", 1, 4, 2, 512, 512, 128, "bf16", causal=True),
     S("bf16_d128_causal_ragged", 2, 2, 1, 333, 333, 128, "bf16", causal=True),
+    # 16-bit O token-major ([qL, H * D]): the two-tile plans store O through a tensor map with
+    # the caller's strides (head stride D, row stride H * D), rows past qL clipped
+    S("bf16_d128_tokenmajor_causal_ragged", 1, 3, 3, 300, 300, 128, "bf16", causal=True, layout="dit"),
+    S("f16_d64_tokenmajor_gqa", 1, 4, 2, 260, 260, 64, "f16", layout="dit"),
     S("bf16_d64_causal_ragged", 2, 2, 2, 300, 300, 64, "bf16", causal=True),
     S("bf16_d64_plain_long_kv", 1, 2, 2, 200, 700, 64, "bf16"),
     S("bf16_d256_additive_ragged", 1, 2, 2, 200, 200, 256, "bf16", mask_kind=W.MASK_ADDITIVE),
