@@ -128,9 +128,13 @@ struct BwdCfg {
   static constexpr int kThreads = 256;
   // TMEM columns: S (or S^T) 0..127, dP (or dP^T) 128..255, then the accumulators.
   static constexpr int kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + kD;
-  // dQ kernel: a second dP buffer after dQ, so dP_{j+1} need not wait for dQ_j
-  // to read dS_j.
-  static constexpr int kColDP2 = 384;
+  // dQ kernel: the tile's Q and dO rows as 16-bit pairs after dQ (the A
+  // operands of S and dP, so those MMAs read only K_j or V_j from shared
+  // memory), then, where TMEM has room (D = 64), a second dP buffer, so
+  // dP_{j+1} need not wait for dQ_j to read dS_j.
+  static constexpr int kColQT = kColAcc0 + kD, kColDOT = kColQT + kD / 2;
+  static constexpr bool kDP2 = kColDOT + kD / 2 + 128 <= 512;
+  static constexpr int kColDP2 = kDP2 ? kColDOT + kD / 2 : kColDP;
   static constexpr uint32_t kTmemCols = 512;
   // dK/dV kernel shared memory: K, V, then Q and dO rings, then L2 and D slots.
   static constexpr uint32_t kKVOffQ = 2 * kTileBytes;
@@ -152,7 +156,7 @@ struct BwdCfg {
   static_assert(kD == 64 || kD == 128, "backward head dims: 64 or 128");
   static_assert(kKVSmem <= 232448 && kQSmem <= 232448, "shared memory overflow");
   static_assert(kColAcc1 + kD <= 512, "TMEM overflow");
-  static_assert(kColAcc0 + kD <= kColDP2 && kColDP2 + 128 <= 512, "dQ kernel TMEM overflow");
+  static_assert(kColDOT + kD / 2 <= 512 && (!kDP2 || kColDP2 + 128 <= 512), "dQ kernel TMEM overflow");
   // The epilogues stage their gradients in rings the finished MMAs no longer read.
   static_assert(kStages * kTileBytes >= kTile * kD * 2 && kQKStages * kTileBytes >= kTile * kD * 2,
                 "epilogue staging space");
@@ -172,6 +176,7 @@ struct BwdQCtrl {
   // dp_full / ds_ready per dP buffer: a phase of buffer b can only complete
   // after its previous phase was waited for, so parity waits cannot skip one.
   uint64_t s_full, s_free, dp_full[2], ds_ready[2], done, drain;
+  uint64_t qt_ready;  // Q and dO copied into TMEM
   uint32_t tmem_base;
   int abort;
 };
@@ -302,6 +307,38 @@ __device__ __forceinline__ void bwd_mma_tmem_a(uint32_t dst, uint32_t a_tmem, ui
 #pragma unroll
   for (int kk = 1; kk < C::kTile / C::kKStep; ++kk)
     mma_ts_lh<false, 1>(dst, a_tmem + kk * 8, b_lo + ((kk * C::kKStep * 128) >> 4), b_hi, idesc, 1u);
+}
+
+// S-like product with A in TMEM: dst = A[128 x kD] (16-bit pairs in TMEM) *
+// B[128 x kD]^T, B a K-major tile of 128-byte swizzled rows.
+template <class C>
+__device__ __forceinline__ void bwd_mma_tmem_kmajor(uint32_t dst, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                    uint32_t idesc) {
+  constexpr int kCol = (C::kTile * 128) >> 4;
+  mma_ts_lh<false, 0>(dst, a_tmem, b_lo, b_hi, idesc, 0u);
+#pragma unroll
+  for (int kk = 1; kk < C::kD / C::kKStep; ++kk)
+    mma_ts_lh<false, 1>(dst, a_tmem + kk * 8, b_lo + (kk / 4) * kCol + (kk % 4) * 2, b_hi, idesc, 1u);
+}
+
+// Row r of a K-major tile (128-byte swizzled 64-column blocks, 128 rows
+// each) into this lane's TMEM columns as 16-bit pairs: the layout of an MMA's
+// A operand in TMEM (column c holds elements 2c and 2c + 1).
+template <class C>
+__device__ __forceinline__ void bwd_row_to_tmem(const uint8_t* tile, int r, uint32_t taddr) {
+#pragma unroll
+  for (int c = 0; c < C::kNChunk; ++c) {
+    uint32_t w[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + c * (C::kTile * 128) + r * 128 + ((k ^ (r & 7)) << 4));
+      w[4 * k] = v.x;
+      w[4 * k + 1] = v.y;
+      w[4 * k + 2] = v.z;
+      w[4 * k + 3] = v.w;
+    }
+    tmem_st32(taddr + c * 32, w);
+  }
 }
 
 // Read 64 fp32 TMEM columns of this lane.
@@ -1316,6 +1353,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       mbar_init(&ctl->dp_full[d], 1);
       mbar_init(&ctl->ds_ready[d], 4);
     }
+    mbar_init(&ctl->qt_ready, 4);  // one arrival per elementwise warp
     mbar_init(&ctl->done, 1);
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -1382,20 +1420,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (lane == 0 && n_blk > 0) {
       constexpr uint32_t idS = make_idesc_fmt(C::kFmt, 128, 128, false, false);
       constexpr uint32_t idAcc = make_idesc_fmt(C::kFmt, 128, C::kD, false, true);
-      const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dO = make_sdesc_sw128(smem_u32(sDO), 16, 1024);
       const uint64_t dKk = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dVk = make_sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dKmn = make_sdesc_sw128(smem_u32(sK), C::kTile * 128, 1024);
-      const uint32_t hi = (uint32_t)(dQ >> 32), hi_mn = (uint32_t)(dKmn >> 32);
+      const uint32_t hi = (uint32_t)(dKk >> 32), hi_mn = (uint32_t)(dKmn >> 32);
       const uint32_t slot = C::kTileBytes >> 4;
-      auto issue_s = [&](int s) { bwd_mma_kmajor<C>(tmem + C::kColS, (uint32_t)dQ, hi, (uint32_t)dKk + s * slot, hi, idS); };
-      // dP_j goes to buffer j % 2 (kColDP or kColDP2)
-      auto dp_col = [](int j) { return (uint32_t)((j & 1) ? C::kColDP2 : C::kColDP); };
-      auto issue_dp = [&](int s, int j) {
-        bwd_mma_kmajor<C>(tmem + dp_col(j), (uint32_t)dO, hi, (uint32_t)dVk + s * slot, hi, idS);
+      // S = Q K_j^T and dP = dO V_j^T with Q and dO in TMEM
+      auto issue_s = [&](int s) {
+        bwd_mma_tmem_kmajor<C>(tmem + C::kColS, tmem + C::kColQT, (uint32_t)dKk + s * slot, hi, idS);
       };
-      bool ok = wait_bounded(&ctl->q_full, 0, abort_flag, p.status, p.timeout_cycles);
+      // dP_j goes to buffer j % 2 (kColDP or kColDP2) where there are two
+      auto dp_col = [](int j) { return (uint32_t)((C::kDP2 && (j & 1)) ? C::kColDP2 : C::kColDP); };
+      auto issue_dp = [&](int s, int j) {
+        bwd_mma_tmem_kmajor<C>(tmem + dp_col(j), tmem + C::kColDOT, (uint32_t)dVk + s * slot, hi, idS);
+      };
+      bool ok = wait_bounded(&ctl->qt_ready, 0, abort_flag, p.status, p.timeout_cycles);
       if (ok) ok = wait_bounded(&ctl->k_full[0], 0, abort_flag, p.status, p.timeout_cycles);
       if (ok) {
         tc_fence_after();
@@ -1409,8 +1448,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mma_commit(&ctl->dp_full[0]);
         mma_commit(&ctl->v_empty[0]);
       }
-      // Tensor-core order per block: S_{j+1}, dP_{j+1}, dQ_j.  dP_{j+1} overwrites
-      // the buffer of dS_{j-1}, which dQ_{j-1} (issued before it) has read.
+      // Tensor-core order per block: S_{j+1}, dP_{j+1}, dQ_j with two dP
+      // buffers (dP_{j+1} overwrites the buffer of dS_{j-1}, which dQ_{j-1},
+      // issued before it, has read); S_{j+1}, dQ_j, dP_{j+1} with one.
       for (int j = 0; j < n_blk && ok; ++j) {
         const int s = j % C::kQKStages;  // K slot of block j
         const int sk1 = (j + 1) % C::kQKStages, uk1 = (j + 1) / C::kQKStages;
@@ -1418,26 +1458,39 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const bool more = j + 1 < n_blk;
         ok = wait_bounded(&ctl->s_free, j & 1, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
+        auto next_dp = [&]() {
+          ok = wait_bounded(&ctl->v_full[sv1], uv1 & 1, abort_flag, p.status, p.timeout_cycles);
+          if (!ok) return;
+          tc_fence_after();
+          issue_dp(sv1, j + 1);
+          mma_commit(&ctl->dp_full[C::kDP2 ? (j + 1) & 1 : 0]);
+          mma_commit(&ctl->v_empty[sv1]);
+        };
         if (more) {
           ok = wait_bounded(&ctl->k_full[sk1], uk1 & 1, abort_flag, p.status, p.timeout_cycles);
           if (!ok) break;
           tc_fence_after();
           issue_s(sk1);
           mma_commit(&ctl->s_full);
-          ok = wait_bounded(&ctl->v_full[sv1], uv1 & 1, abort_flag, p.status, p.timeout_cycles);
-          if (!ok) break;
-          tc_fence_after();
-          issue_dp(sv1, j + 1);
-          mma_commit(&ctl->dp_full[(j + 1) & 1]);
-          mma_commit(&ctl->v_empty[sv1]);
+          if constexpr (C::kDP2) {
+            next_dp();
+            if (!ok) break;
+          }
         }
-        ok = wait_bounded(&ctl->ds_ready[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
+        const int x = C::kDP2 ? j & 1 : 0, par = C::kDP2 ? (j >> 1) & 1 : j & 1;
+        ok = wait_bounded(&ctl->ds_ready[x], par, abort_flag, p.status, p.timeout_cycles);
         if (!ok) break;
         tc_fence_after();
         // dQ += dS K_j (dS: bf16 pairs over dP_j's columns; K_j read MN-major)
         bwd_mma_tmem_a<C>(tmem + C::kColAcc0, tmem + dp_col(j), (uint32_t)dKmn + s * slot, hi_mn, idAcc,
                           j > 0 ? 1u : 0u);
         mma_commit(&ctl->k_empty[s]);
+        if constexpr (!C::kDP2) {
+          if (more) {
+            next_dp();
+            if (!ok) break;
+          }
+        }
       }
       if (ok) mma_commit(&ctl->done);
       mma_commit(&ctl->drain);
@@ -1481,6 +1534,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
     }
     bool ok = true;
+    if (n_blk > 0) {  // this row of Q and of dO into TMEM, once the tiles have landed
+      ok = warp_wait(&ctl->q_full, 0, abort_flag, p.status, p.timeout_cycles);
+      if (ok) {
+        bwd_row_to_tmem<C>(sQ, tl, tmem + lane_addr + C::kColQT);
+        bwd_row_to_tmem<C>(sDO, tl, tmem + lane_addr + C::kColDOT);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->qt_ready);
+      }
+    }
     for (int j = 0; j < n_blk && ok; ++j) {
       const int kbase = (jb0 + j) * C::kTile;
       // Dropout: this row's keep bits of block j (bit x of word q: key
@@ -1562,11 +1626,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
       }
-      ok = warp_wait(&ctl->dp_full[j & 1], (j >> 1) & 1, abort_flag, p.status, p.timeout_cycles);
+      const int x = C::kDP2 ? j & 1 : 0, par = C::kDP2 ? (j >> 1) & 1 : j & 1;
+      ok = warp_wait(&ctl->dp_full[x], par, abort_flag, p.status, p.timeout_cycles);
       if (!ok) break;
       tc_fence_after();
+      const uint32_t tdp = x ? tDP2 : tDP;
       if constexpr (C::kDrop) {
-        const uint32_t tdp = (j & 1) ? tDP2 : tDP;
         auto dsub = [&](int) { return di; };
         auto l2c = [&](int) { return l2; };
         auto kword = [&](int cc) { return kw[cc]; };
@@ -1575,15 +1640,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         else
           bwd_ds_pass_drop<C, false, false>(tdp, pr, dsub, l2c, 0.0f, kword, p.drop_scale);
       } else if (C::kCap && p.softcap_on) {
-        bwd_ds_pass_softcap<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; }, [&](int) { return l2; },
-                               p.softcap_inv);
+        bwd_ds_pass_softcap<C>(tdp, pr, [&](int) { return di; }, [&](int) { return l2; }, p.softcap_inv);
       } else {
-        bwd_ds_pass<C>((j & 1) ? tDP2 : tDP, pr, [&](int) { return di; });
+        bwd_ds_pass<C>(tdp, pr, [&](int) { return di; });
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->ds_ready[j & 1]);
+      if (lane == 0) mbar_arrive(&ctl->ds_ready[x]);
     }
     if (ok) {
       const bool store = i < p.qL;
