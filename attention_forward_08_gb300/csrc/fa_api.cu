@@ -37,6 +37,7 @@ int g_num_sms[kMaxDevices] = {0};
 long long g_timeout_cycles = 0;  // 0: not yet initialised
 int g_max_ctas = 0;              // 0: one CTA per SM
 int g_q_tiles = 0;               // 0: choose per call; 1 or 2: Q tiles per CTA for bf16/fp16 D <= 128
+int g_kv_splits = 0;             // 0: choose per call; >= 1: key ranges per query tile (1: no split-KV)
 EncodeTiledFn g_encode = nullptr;
 bool g_encode_tried = false;
 
@@ -220,6 +221,51 @@ long long pre_workspace_bytes(const fa_fwd_args* a) {
   const long long vt_row = (a->kL + 3) / 4 * 4;
   return align256((long long)a->B * a->H_q * a->qL * a->D * 4) + align256((long long)a->B * a->H_kv * a->kL * a->D * 4) +
          align256((long long)a->B * a->H_kv * a->D * vt_row * 4);
+}
+
+// The plan choice for bf16 / fp16 I/O at D <= 128 without window, softcap,
+// offset or dropout: one Q tile per CTA when the two-tile work units cannot
+// occupy every SM (`sms`: the CTAs the launch may start), or as
+// fa_set_q_tiles says.
+bool one_tile_plan(const fa_fwd_args* a, int sms) {
+  const bool feat = a->dropout_p != 0.0f || a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f;
+  if (feat || a->dtype == FA_DTYPE_F32 || a->D > 128) return false;
+  int policy;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    policy = g_q_tiles;
+  }
+  const long long units2 = (long long)((a->qL + 255) / 256) * a->B * a->H_q;
+  return policy == 1 || (policy == 0 && units2 < sms);
+}
+
+// Key ranges per query tile (split-KV; 1: none) for the one-tile plans
+// without a mask: automatically when their units leave more than half of the
+// SMs idle, as many ranges as fill the SMs with at least 4 key blocks each
+// (at most 64); fa_set_kv_splits overrides the count.
+int kv_splits_for(const fa_fwd_args* a, int sms) {
+  if (sms <= 0 || a->mask_kind != FA_MASK_NONE || !one_tile_plan(a, sms)) return 1;
+  int forced;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    forced = g_kv_splits;
+  }
+  const long long units1 = (long long)((a->qL + 127) / 128) * a->B * a->H_q;
+  const long long n_kb = (a->kL + 127) / 128;
+  long long s = 1;
+  if (forced >= 1)
+    s = forced;
+  else if (units1 * 2 <= sms)
+    s = std::min<long long>(sms / units1, n_kb / 4);
+  return (int)std::max<long long>(1, std::min<long long>(std::min<long long>(s, n_kb), 64));
+}
+
+// Workspace of split-KV with `splits` ranges: the partial O (fp32, D per row)
+// and logsumexp of every (range, row).
+long long split_rows(const fa_fwd_args* a, int splits) { return (long long)splits * a->B * a->H_q * a->qL; }
+long long split_workspace_bytes(const fa_fwd_args* a, int splits) {
+  if (splits <= 1) return 0;
+  return align256(split_rows(a, splits) * a->D * 4) + align256(split_rows(a, splits) * 4);
 }
 
 }  // namespace
@@ -411,17 +457,25 @@ int fa_fwd_ex(const fa_fwd_args* a) {
   const bool drop = a->dropout_p != 0.0f;
   const bool feat = drop || a->window != 0 || a->q_offset != 0 || a->softcap != 0.0f;
   // bf16 / fp16 at D <= 128 (no window, softcap or offset): one Q tile per CTA
-  // when the two-tile work units cannot occupy every SM.
-  bool one_tile = false;
-  if (!feat && a->dtype != FA_DTYPE_F32 && a->D <= 128) {
-    int policy;
-    {
-      std::lock_guard<std::mutex> lk(g_mu);
-      policy = g_q_tiles;
+  // when the two-tile work units cannot occupy every SM; with a workspace,
+  // split-KV when even those leave most SMs idle.
+  const int sms = la.max_ctas > 0 ? std::min(la.max_ctas, la.num_sms) : la.num_sms;
+  const bool one_tile = one_tile_plan(a, sms);
+  la.kv_splits = 1;
+  la.part_o = nullptr;
+  la.part_lse = nullptr;
+  const int splits = one_tile ? kv_splits_for(a, sms) : 1;
+  if (splits > 1 && a->workspace) {
+    const long long need = split_workspace_bytes(a, splits);
+    if (a->workspace_bytes < need) {
+      set_error("workspace of %lld bytes is smaller than the %lld this call needs (fa_fwd_workspace_bytes)",
+                a->workspace_bytes, need);
+      return FA_ERR_INVALID_ARGUMENT;
     }
-    const long long units2 = (long long)((a->qL + 255) / 256) * a->B * a->H_q;
-    const int sms = la.max_ctas > 0 ? std::min(la.max_ctas, la.num_sms) : la.num_sms;
-    one_tile = policy == 1 || (policy == 0 && units2 < sms);
+    la.kv_splits = splits;
+    la.part_o = static_cast<float*>(a->workspace);
+    la.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) +
+                                           align256(split_rows(a, splits) * a->D * 4));
   }
   if (a->workspace && pre_bytes > 0) {
     uint8_t* ws = static_cast<uint8_t*>(a->workspace);
@@ -483,7 +537,22 @@ long long fa_fwd_workspace_bytes(const fa_fwd_args* a) {
   using namespace fa;
   g_err[0] = '\0';
   if (validate(a) != FA_OK) return -1;
-  return pre_workspace_bytes(a);
+  const long long pre = pre_workspace_bytes(a);
+  if (pre > 0) return pre;
+  // Split-KV depends on the device's SM count; without a device no plan needs scratch.
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || device_setup(dev) != FA_OK) {
+    cudaGetLastError();
+    g_err[0] = '\0';
+    return 0;
+  }
+  int max_ctas;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    max_ctas = g_max_ctas;
+  }
+  const int sms = max_ctas > 0 ? std::min(max_ctas, g_num_sms[dev]) : g_num_sms[dev];
+  return split_workspace_bytes(a, kv_splits_for(a, sms));
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q, int H_kv, int qL,
@@ -565,6 +634,11 @@ void fa_set_timeout_cycles(long long cycles) {
 void fa_set_q_tiles(int n) {
   std::lock_guard<std::mutex> lk(fa::g_mu);
   fa::g_q_tiles = (n == 1 || n == 2) ? n : 0;
+}
+
+void fa_set_kv_splits(int n) {
+  std::lock_guard<std::mutex> lk(fa::g_mu);
+  fa::g_kv_splits = n >= 1 ? n : 0;
 }
 
 void fa_set_max_ctas(int n) {
@@ -749,6 +823,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
                    causal, 0, 0, 0.0f, 0.0f, 0ull, 0ull, dtype, stream);
 }
 
-int fa_version(void) { return 110; }
+int fa_version(void) { return 111; }
 
 }  // extern "C"

@@ -128,6 +128,9 @@ struct Cfg {
   // tile, each taking 64 of a block's 128 keys for all 128 rows, so every SM
   // sub-partition runs two softmax warps (one alone leaves its latency bare).
   static constexpr bool kSplitRows = kNQT == 1 && !kTf32 && !kDrop;
+  // Split-KV: the one-Q-tile 16-bit plans without features may cut a tile's
+  // key blocks into ranges (FaParams::kv_splits), each its own work unit.
+  static constexpr bool kSplitKV = kNQT == 1 && !kTf32 && !kFeat && !kDrop;
   static constexpr int kCvtWarps = kHelpers ? (kExtraHelpers ? 6 : 2) : 1;
   static constexpr int kCvtThreads = 32 * kCvtWarps;
   static constexpr int kThreads = 128 * (1 + kNQT) + (kExtraHelpers || kSplitRows ? 128 : 0);
@@ -611,15 +614,17 @@ __device__ __forceinline__ void p_pass_dropout(const float (&s)[C::kBN], float s
 // head, or (head pairs) the same rows of two heads that share a K/V head.
 struct Unit {
   int b, h, kvh, q0, N;
+  int ks;            // key range (split-KV; 0 otherwise)
   int th[2], tr[2];  // head and first row of Q tile t
   int j0;       // first KV tile of the unit (the tiles share one K/V stream from j0 to N)
   int nblk[2];  // one past each Q tile's last KV tile (0: the tile has no rows)
 };
 
-// The unit's first KV tile: a compile-time 0 without a sliding window.
+// The unit's first KV tile: a compile-time 0 without a sliding window or
+// key ranges.
 template <class C>
 __device__ __forceinline__ int unit_j0(const Unit& w) {
-  if constexpr (C::kFeat)
+  if constexpr (C::kFeat || C::kSplitKV)
     return w.j0;
   else
     return 0;
@@ -633,9 +638,18 @@ __device__ __forceinline__ Unit decode_unit(const FaParams& p, int u) {
   // visit the same K/V blocks and finish together (a causal row pair would
   // leave the second tile one block alone at the end of every unit).
   Unit w;
-  const int per_q = p.B * p.hq_units;
+  // Split-KV: the key ranges of a query block come next to each other in the
+  // order, between the query block and the (batch, head) units.
+  const int per_bh = p.B * p.hq_units;
+  const int splits = C::kSplitKV ? p.kv_splits : 1;
+  const int per_q = per_bh * splits;
   const int qb_rev = u / per_q;
-  const int rem = u - qb_rev * per_q;
+  int rem = u - qb_rev * per_q;
+  w.ks = 0;
+  if constexpr (C::kSplitKV) {
+    w.ks = rem / per_bh;
+    rem -= w.ks * per_bh;
+  }
   const int qb = p.causal ? (p.n_qblocks - 1 - qb_rev) : qb_rev;
   w.b = rem / p.hq_units;
   const int hu = rem - w.b * p.hq_units;
@@ -652,6 +666,15 @@ __device__ __forceinline__ Unit decode_unit(const FaParams& p, int u) {
   // Tile 0's rows come first (or equal), so its window starts first; tile 1
   // masks the (at most one) leading block it cannot see.
   w.j0 = tile_kv_begin<C>(p, w.tr[0], w.nblk[0]);
+  if constexpr (C::kSplitKV) {
+    if (splits > 1) {  // key blocks [j0, nblk) of range ks; an empty range is a unit without work
+      const int jb = w.ks * p.kv_chunk;
+      const int je = min(w.nblk[0], jb + p.kv_chunk);
+      w.j0 = jb;
+      w.nblk[0] = je > jb ? je : 0;
+      w.N = w.nblk[0];
+    }
+  }
   return w;
 }
 
@@ -729,9 +752,9 @@ __device__ __forceinline__ void tf32_helpers(uint8_t* sQ, uint8_t* sK, uint8_t* 
 // value into a column of the OTHER half, which that half reads before
 // overwriting it with its P; the row sums meet the same way in the epilogue.
 //
-// Sync supplies the schedule and the hand-offs: next(r, b, h, r0, j0, nb) (the
-// r-th unit: batch, head, this CTA's first row, key blocks [j0, nb); false when
-// done), wait_s / wait_m / wait_o (bounded waits on S landed, the mask tile
+// Sync supplies the schedule and the hand-offs: next(r, b, h, r0, j0, nb, ks)
+// (the r-th unit: batch, head, this CTA's first row, key blocks [j0, nb), key
+// range ks; false when done), wait_s / wait_m / wait_o (bounded waits on S landed, the mask tile
 // landed, P V landed) and the arrivals s_free / m_free / p_ready / o_free.
 template <class C, class Sync>
 __device__ __forceinline__ void softmax_split_rows(Sync& sy, uint8_t* sM, uint32_t tmem, const FaParams& p, int warp,
@@ -751,8 +774,8 @@ __device__ __forceinline__ void softmax_split_rows(Sync& sy, uint8_t* sM, uint32
   int blocks_seen = 0, masks_seen = 0;
   bool ok = true;
   for (int r = 0; ok; ++r) {
-    int b, h, r0, j0, nb;
-    if (!sy.next(r, b, h, r0, j0, nb)) break;
+    int b, h, r0, j0, nb, ks;
+    if (!sy.next(r, b, h, r0, j0, nb, ks)) break;
     if (nb == 0) continue;
     const int row = r0 + tl;
     float m_run = -INFINITY;  // running max of the whole row, base 2 (scaled)
@@ -873,6 +896,10 @@ __device__ __forceinline__ void softmax_split_rows(Sync& sy, uint8_t* sM, uint32
     uint8_t* orow = static_cast<uint8_t*>(p.o) +
                     ((long long)b * p.o_sb + (long long)h * p.o_sh + (long long)(store ? row : 0) * p.o_ss) * C::kEsz +
                     g * kHalfD * C::kEsz;
+    // Split-KV: this range's normalised O (fp32) and logsumexp go to the
+    // partial buffers, row ((ks * B + b) * H_q + h) * qL + row.
+    const bool part = C::kSplitKV && p.kv_splits > 1;
+    const long long prow = (((long long)ks * p.B + b) * p.Hq + h) * p.qL + (store ? row : 0);
     constexpr int kBatch = kHalfD / 32 < 4 ? kHalfD / 32 : 4;
 #pragma unroll
     for (int c0 = 0; c0 < kHalfD / 32; c0 += kBatch) {
@@ -887,7 +914,19 @@ __device__ __forceinline__ void softmax_split_rows(Sync& sy, uint8_t* sM, uint32
         __syncwarp();
         if (lane == 0) sy.o_free();
       }
-      if (store) {
+      if (store && part) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          uint4* dst = reinterpret_cast<uint4*>(p.part_o + prow * C::kD + g * kHalfD + (c0 + i) * 32);
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4) {
+            float a0, a1, a2, a3;
+            fmul2(a0, a1, __uint_as_float(rb[i][4 * u4]), __uint_as_float(rb[i][4 * u4 + 1]), inv_l, inv_l);
+            fmul2(a2, a3, __uint_as_float(rb[i][4 * u4 + 2]), __uint_as_float(rb[i][4 * u4 + 3]), inv_l, inv_l);
+            dst[u4] = make_uint4(__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3));
+          }
+        }
+      } else if (store) {
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
           uint4* dst = reinterpret_cast<uint4*>(orow + (c0 + i) * 64);
@@ -908,7 +947,10 @@ __device__ __forceinline__ void softmax_split_rows(Sync& sy, uint8_t* sM, uint32
     }
     if (store && g == 0) {
       const float lse = (l_run > 0.0f) ? (m_run + lg2(l_run)) * kLn2 : -INFINITY;
-      p.lse[((long long)b * p.Hq + h) * p.qL + row] = lse;
+      if (part)
+        p.part_lse[prow] = lse;
+      else
+        p.lse[((long long)b * p.Hq + h) * p.qL + row] = lse;
     }
   }
 }
@@ -920,7 +962,7 @@ struct LocalSync {
   const FaParams& p;
   volatile int* abort;
   int num_units;
-  __device__ bool next(int r, int& b, int& h, int& r0, int& j0, int& nb) {
+  __device__ bool next(int r, int& b, int& h, int& r0, int& j0, int& nb, int& ks) {
     const int u = unit_of(r, num_units);
     if (u < 0) return false;
     const Unit w = decode_unit<C>(p, u);
@@ -929,6 +971,7 @@ struct LocalSync {
     r0 = w.tr[0];
     j0 = unit_j0<C>(w);
     nb = w.nblk[0];
+    ks = w.ks;
     return true;
   }
   __device__ bool wait_s(uint32_t par) { return warp_wait(&ctl->s_full[0], par, abort, p.status, p.timeout_cycles); }
@@ -939,6 +982,57 @@ struct LocalSync {
   __device__ void p_ready() { mbar_arrive(&ctl->p_ready[0]); }
   __device__ void o_free() { mbar_arrive(&ctl->o_free[0]); }
 };
+
+// Split-KV combine pass: for each row, over the key ranges that ran a unit
+// for the row's query tile (a range starting past the tile's last key block
+// ran none), O = sum_s w_s O_s / sum_s w_s with w_s = exp(lse_s - max_s lse_s)
+// and L = max_s lse_s + log(sum_s w_s) -- the softmax of the union of the
+// ranges, since each O_s is its range's normalised output and lse_s its
+// logsumexp.  A row none of whose ranges saw a key keeps O = 0, L = -inf.
+// D / 8 threads per row, 8 columns each.
+template <class C>
+__global__ void __launch_bounds__(256) fa_splitkv_combine_kernel(const FaParams p) {
+  constexpr int kT = C::kD / 8;
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long plane = (long long)p.B * p.Hq * p.qL;  // rows of one range
+  if (t >= plane * kT) return;
+  const long long row = t / kT;  // ((b * H_q + h) * qL + i)
+  const int c8 = (int)(t - row * kT);
+  const long long bh = row / p.qL;
+  const int i = (int)(row - bh * p.qL);
+  const int b = (int)(bh / p.Hq), h = (int)(bh - (long long)b * p.Hq);
+  const int last = min((i / C::kBM) * C::kBM + C::kBM, p.qL) - 1;
+  const int kv_end = p.causal ? min(p.kL, last + 1) : p.kL;
+  const int nb = (kv_end + C::kBN - 1) / C::kBN;  // the tile's key blocks
+  float m = -INFINITY;
+  for (int s = 0; s < p.kv_splits && s * p.kv_chunk < nb; ++s) m = fmaxf(m, p.part_lse[s * plane + row]);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+  float sum = 0.0f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < p.kv_splits && s * p.kv_chunk < nb; ++s) {
+      const float w = expf(p.part_lse[s * plane + row] - m);  // 0 for a range without keys for the row
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + (s * plane + row) * C::kD + c8 * 8);
+      const float4 x0 = src[0], x1 = src[1];
+      sum += w;
+      acc[0] = fmaf(w, x0.x, acc[0]);
+      acc[1] = fmaf(w, x0.y, acc[1]);
+      acc[2] = fmaf(w, x0.z, acc[2]);
+      acc[3] = fmaf(w, x0.w, acc[3]);
+      acc[4] = fmaf(w, x1.x, acc[4]);
+      acc[5] = fmaf(w, x1.y, acc[5]);
+      acc[6] = fmaf(w, x1.z, acc[6]);
+      acc[7] = fmaf(w, x1.w, acc[7]);
+    }
+  }
+  const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
+  uint8_t* dst = static_cast<uint8_t*>(p.o) +
+                 ((long long)b * p.o_sb + (long long)h * p.o_sh + (long long)i * p.o_ss + c8 * 8) * C::kEsz;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(pack16x2<C>(acc[0] * inv, acc[1] * inv), pack16x2<C>(acc[2] * inv, acc[3] * inv),
+                                              pack16x2<C>(acc[4] * inv, acc[5] * inv), pack16x2<C>(acc[6] * inv, acc[7] * inv));
+  if (c8 == 0) p.lse[row] = sum > 0.0f ? m + logf(sum) : -INFINITY;
+}
 
 // Persistent forward kernel: each CTA walks its units; every role carries its
 // barrier phase counters from one unit to the next, so the next unit's Q and
@@ -961,7 +1055,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_units = p.n_qblocks * p.B * p.hq_units;
+  const int num_units = p.n_qblocks * p.B * p.hq_units * p.kv_splits;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -1197,6 +1291,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const int u = unit_of(r, num_units);
         if (u < 0) break;
         const Unit w = decode_unit<C>(p, u);
+        if (w.N == 0) continue;  // an empty key range (split-KV): the producer loads nothing for it
 #pragma unroll
         for (int t = 0; t < C::kNQT; ++t) {
           if (t < t_begin || t >= t_end || !ok || w.nblk[t] == 0) continue;

@@ -34,6 +34,11 @@ struct LaunchArgs {
   long long timeout_cycles;
   int num_sms;
   int max_ctas;  // 0: one CTA per SM
+  // Split-KV (plans with Cfg::kSplitKV): key ranges per query tile (1: off)
+  // and the partial buffers in the caller's workspace.
+  int kv_splits;
+  float* part_o;
+  float* part_lse;
 };
 
 // cuTensorMapEncodeTiled, resolved from the driver at run time (the library
@@ -199,6 +204,10 @@ void setup_params(const LaunchArgs& a, CUtensorMap& tm, FaParams& p) {
   p.lse = a.lse;
   p.status = a.status;
   p.timeout_cycles = a.timeout_cycles;
+  p.kv_splits = (C::kSplitKV && a.kv_splits > 1) ? a.kv_splits : 1;
+  p.kv_chunk = ((a.kL + C::kBN - 1) / C::kBN + p.kv_splits - 1) / p.kv_splits;
+  p.part_o = p.kv_splits > 1 ? a.part_o : nullptr;
+  p.part_lse = p.kv_splits > 1 ? a.part_lse : nullptr;
 }
 
 template <class C>
@@ -245,7 +254,7 @@ int launch_fa_fwd(const LaunchArgs& a) {
   }
   // Persistent grid: one CTA per SM (or fewer when capped), each walking its
   // share of the (query block, batch, head) units.
-  const long long units = (long long)p.n_qblocks * a.B * p.hq_units;
+  const long long units = (long long)p.n_qblocks * a.B * p.hq_units * p.kv_splits;
   if (units <= 0 || units > 0x7fffffffLL) {
     set_error("%lld work units are out of range", units);
     return 2;
@@ -258,6 +267,17 @@ int launch_fa_fwd(const LaunchArgs& a) {
   if (e != cudaSuccess) {
     set_error("kernel launch failed: %s", cudaGetErrorString(e));
     return 4;
+  }
+  if constexpr (C::kSplitKV) {
+    if (p.kv_splits > 1) {  // merge the key ranges into O and L
+      const long long threads = (long long)a.B * a.Hq * a.qL * (C::kD / 8);
+      fa_splitkv_combine_kernel<C><<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) {
+        set_error("split-KV combine launch failed: %s", cudaGetErrorString(e));
+        return 4;
+      }
+    }
   }
   return 0;
 }

@@ -41,6 +41,15 @@ struct FaParams {
   void* o;                              // output, I/O dtype
   long long o_sb, o_sh, o_ss;           // O element strides: batch, head, query row
   float* lse;                           // [B, Hq, qL] fp32, natural log
+  // Split-KV (one-Q-tile 16-bit plans without features): the key blocks of
+  // each (query tile, head) are cut into kv_splits ranges of kv_chunk blocks,
+  // one work unit each; a unit writes its range's normalised O in fp32 and
+  // its logsumexp to part_o / part_lse instead of O and L, and a combine pass
+  // merges the ranges.  kv_splits = 1: off.
+  int kv_splits;
+  int kv_chunk;
+  float* part_o;                        // [kv_splits, B * Hq, qL, D]
+  float* part_lse;                      // [kv_splits, B * Hq, qL]
   unsigned int* status;                 // device status word (kStatus* bits)
   long long timeout_cycles;             // bound on every wait, in SM clock cycles
 };

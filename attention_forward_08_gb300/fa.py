@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED
                 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 EXPORTED = ("fa_fwd", "fa_fwd_ex", "fa_fwd_workspace_bytes", "fa_last_error", "fa_sync_status",
-            "fa_set_timeout_cycles", "fa_set_max_ctas", "fa_set_q_tiles", "fa_bwd_workspace_bytes",
+            "fa_set_timeout_cycles", "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_kv_splits", "fa_bwd_workspace_bytes",
             "fa_bwd_ex_workspace_bytes", "fa_bwd", "fa_bwd_ex", "fa_bwd_full", "fa_bwd_full_workspace_bytes",
             "fa_bwd_noalloc", "fa_version")
 
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH):
     lib.fa_set_max_ctas.argtypes = [ctypes.c_int]
     lib.fa_set_q_tiles.restype = None
     lib.fa_set_q_tiles.argtypes = [ctypes.c_int]
+    lib.fa_set_kv_splits.restype = None
+    lib.fa_set_kv_splits.argtypes = [ctypes.c_int]
     lib.fa_version.restype = ctypes.c_int
     lib.fa_version.argtypes = []
     lib.fa_bwd_workspace_bytes.restype = ctypes.c_longlong
@@ -168,6 +170,11 @@ def fa_set_max_ctas(n: int) -> None:
 
 def fa_set_q_tiles(n: int) -> None:
     load_library().fa_set_q_tiles(int(n))
+
+
+def fa_set_kv_splits(n: int) -> None:
+    """``fa_set_kv_splits`` of include/fa.h: key ranges per query tile for split-KV (0: automatic)."""
+    load_library().fa_set_kv_splits(int(n))
 
 
 def fa_version() -> int:

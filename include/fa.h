@@ -135,7 +135,10 @@ int fa_fwd_ex(const fa_fwd_args* args);
  * fa_fwd_workspace_bytes -- device scratch that lets fa_fwd_ex run the faster
  * plan for these arguments (all fields filled as for the call), or 0 when no
  * plan needs one; -1 (with the message set) when the arguments are invalid.
- * Today: fp32 I/O (TF32) without window, softcap, offset or dropout and with
+ * Split-KV (fa_set_kv_splits; it depends on the current device's SM count and
+ * fa_set_max_ctas, so ask again after changing either): 4 * S * B*H_q*qL * D
+ * bytes of partial O and 4 * S * B*H_q*qL of partial logsumexp, each rounded
+ * up to 256, for S key ranges.  Also: fp32 I/O (TF32) without window, softcap, offset or dropout and with
  * kL >= 1024, where the library rounds Q and K to tf32 and transposes V once
  * into the workspace (one extra launch) instead of per tile inside the kernel:
  * 4 * (B*H_q*qL*D + B*H_kv*kL*D + B*H_kv*D*ceil4(kL)) bytes, each part rounded
@@ -182,6 +185,23 @@ void fa_set_max_ctas(int n);
  * any other value restores the automatic one.  Results do not depend on it.
  */
 void fa_set_q_tiles(int n);
+
+/*
+ * fa_set_kv_splits -- split-KV for the one-Q-tile plans (bf16 / fp16 I/O,
+ * D <= 128, no mask, window, softcap, offset or dropout): each 128-row query
+ * tile's key blocks are cut into n ranges, each its own work unit, which
+ * writes its range's normalised O (fp32) and logsumexp to the workspace; a
+ * second launch merges the ranges (O = sum_s w_s O_s / sum_s w_s, w_s =
+ * exp(L_s - max L), L = max L + log sum_s w_s: the same softmax, rounded
+ * once to the I/O type).  It applies only when fa_fwd_ex gets a workspace of
+ * fa_fwd_workspace_bytes; without one the call runs unsplit.  n >= 1 forces
+ * n ranges (at most one per key block, at most 64; 1: off); any other value
+ * restores the automatic choice: split when the one-tile units would leave
+ * more than half of the SMs idle (few, long query tiles: decoding-like
+ * shapes), into as many ranges as fill the SMs with at least 4 key blocks
+ * each.  Results agree with the unsplit plan to rounding.
+ */
+void fa_set_kv_splits(int n);
 
 /*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
@@ -348,7 +368,7 @@ long long fa_bwd_full_workspace_bytes(const fa_bwd_args* args);
  * FA_DTYPE_F16; 1.06: fa_fwd_args.workspace, fa_fwd_workspace_bytes; 1.07:
  * fa_bwd_ex; 1.08: fa_bwd_ex takes the forward's dropout arguments,
  * fa_bwd_ex_workspace_bytes; 1.09: fa_bwd_args, fa_bwd_full with masks;
- * 1.10: the backward at D = 256). */
+ * 1.10: the backward at D = 256; 1.11: fa_set_kv_splits). */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -33,7 +33,7 @@ def test_header_declares_the_abi():
          "fa_bwd_ex_workspace_bytes", "fa_bwd_full", "fa_bwd_full_workspace_bytes", "fa_bwd_noalloc",
          "fa_last_error",
          "fa_sync_status",
-         "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_timeout_cycles", "fa_version"])
+         "fa_set_kv_splits", "fa_set_max_ctas", "fa_set_q_tiles", "fa_set_timeout_cycles", "fa_version"])
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -65,7 +65,7 @@ def test_args_struct_matches_header(tmp_path, cname, pyname):
 
 
 def test_version(fa):
-    assert fa.fa_version() == 110
+    assert fa.fa_version() == 111
 
 
 P = 0x10000  # a 16-byte aligned stand-in address: validation never dereferences it

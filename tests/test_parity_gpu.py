@@ -116,6 +116,36 @@ def test_fp32_both_plans(w, workspace):
     _run_small(w, qkv=(q, k, v), mask=m, workspace=workspace)
 
 
+# Split-KV (the one-Q-tile 16-bit plans without mask or features): each query
+# tile's key blocks cut into ranges, one work unit each, the partial O and L
+# merged by a second launch.  Forced counts that leave ranges empty (early
+# causal tiles, kL past the causal limit) or exceed the key blocks, and the
+# automatic count on a decoding-like shape (few query tiles, long kL); both
+# head dims and 16-bit types, ragged qL and kL, GQA.
+SPLIT_KV = [
+    (S("splitkv_bf16_d128_gqa", 1, 4, 1, 130, 3000, 128, "bf16", seed=101), 5),
+    (S("splitkv_f16_d64_auto", 2, 2, 2, 64, 5000, 64, "f16", seed=102), 0),
+    (S("splitkv_bf16_d128_causal", 1, 2, 1, 1000, 1000, 128, "bf16", causal=True, seed=103), 3),
+    (S("splitkv_bf16_d64_beyond_blocks", 1, 2, 2, 100, 300, 64, "bf16", seed=104), 64),
+    (S("splitkv_f16_d128_causal_kl_longer", 1, 4, 2, 200, 2500, 128, "f16", causal=True, seed=105), 4),
+]
+
+
+@pytest.mark.parametrize("w,splits", SPLIT_KV, ids=[w.name for w, _ in SPLIT_KV])
+def test_split_kv(w, splits):
+    import attention_forward_08_gb300 as fa
+    fa.fa_set_kv_splits(splits)
+    try:
+        q, k, v, m = W.make_inputs(w)
+        qd = q.cuda()
+        args = fa.make_args(qd, k.cuda(), v.cuda(), torch.empty_like(qd),
+                            torch.empty((w.B, w.H_q, w.qL), device="cuda"), scale=w.sm_scale, causal=w.causal)
+        assert fa.fa_fwd_workspace_bytes(args) > 0  # the split plan applies
+        _run_small(w, qkv=(q, k, v), mask=m)
+    finally:
+        fa.fa_set_kv_splits(0)
+
+
 # Sliding window, softcap and query offset on every kernel plan (two Q tiles,
 # one Q tile, TF32, masks).  Softcaps of 1.5-4 against N(0,1) inputs with a
 # raised scale make the cap bend most scores.
