@@ -128,9 +128,10 @@ struct Cfg {
   // tile, each taking 64 of a block's 128 keys for all 128 rows, so every SM
   // sub-partition runs two softmax warps (one alone leaves its latency bare).
   static constexpr bool kSplitRows = kNQT == 1 && !kTf32 && !kDrop;
-  // Split-KV: the one-Q-tile 16-bit plans without features may cut a tile's
-  // key blocks into ranges (FaParams::kv_splits), each its own work unit.
-  static constexpr bool kSplitKV = kNQT == 1 && !kTf32 && !kFeat && !kDrop;
+  // Split-KV: the one-Q-tile 16-bit plans at D <= 128 without features may
+  // cut a tile's key blocks into ranges (FaParams::kv_splits), each its own
+  // work unit.
+  static constexpr bool kSplitKV = kNQT == 1 && !kTf32 && !kFeat && !kDrop && kD <= 128;
   static constexpr int kCvtWarps = kHelpers ? (kExtraHelpers ? 6 : 2) : 1;
   static constexpr int kCvtThreads = 32 * kCvtWarps;
   static constexpr int kThreads = 128 * (1 + kNQT) + (kExtraHelpers || kSplitRows ? 128 : 0);
