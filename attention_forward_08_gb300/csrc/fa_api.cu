@@ -239,12 +239,12 @@ bool one_tile_plan(const fa_fwd_args* a, int sms) {
   return policy == 1 || (policy == 0 && units2 < sms);
 }
 
-// Key ranges per query tile (split-KV; 1: none) for the one-tile plans
-// without a mask: automatically when their units leave more than half of the
-// SMs idle, as many ranges as fill the SMs with at least 4 key blocks each
-// (at most 64); fa_set_kv_splits overrides the count.
+// Key ranges per query tile (split-KV; 1: none) for the one-tile plans:
+// automatically when their units leave more than half of the SMs idle, as
+// many ranges as fill the SMs with at least 4 key blocks each (at most 64);
+// fa_set_kv_splits overrides the count.
 int kv_splits_for(const fa_fwd_args* a, int sms) {
-  if (sms <= 0 || a->mask_kind != FA_MASK_NONE || !one_tile_plan(a, sms)) return 1;
+  if (sms <= 0 || !one_tile_plan(a, sms)) return 1;
   int forced;
   {
     std::lock_guard<std::mutex> lk(g_mu);

@@ -188,7 +188,7 @@ void fa_set_q_tiles(int n);
 
 /*
  * fa_set_kv_splits -- split-KV for the one-Q-tile plans (bf16 / fp16 I/O,
- * D <= 128, no mask, window, softcap, offset or dropout): each 128-row query
+ * D <= 128, masks allowed; no window, softcap, offset or dropout): each 128-row query
  * tile's key blocks are cut into n ranges, each its own work unit, which
  * writes its range's normalised O (fp32) and logsumexp to the workspace; a
  * second launch merges the ranges (O = sum_s w_s O_s / sum_s w_s, w_s =

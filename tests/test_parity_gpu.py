@@ -116,18 +116,20 @@ def test_fp32_both_plans(w, workspace):
     _run_small(w, qkv=(q, k, v), mask=m, workspace=workspace)
 
 
-# Split-KV (the one-Q-tile 16-bit plans without mask or features): each query
-# tile's key blocks cut into ranges, one work unit each, the partial O and L
-# merged by a second launch.  Forced counts that leave ranges empty (early
-# causal tiles, kL past the causal limit) or exceed the key blocks, and the
-# automatic count on a decoding-like shape (few query tiles, long kL); both
-# head dims and 16-bit types, ragged qL and kL, GQA.
+# Split-KV (the one-Q-tile 16-bit plans without features): each query tile's
+# key blocks cut into ranges, one work unit each, the partial O and L merged
+# by a second launch.  Forced counts that leave ranges empty (early causal
+# tiles, kL past the causal limit) or exceed the key blocks, and the automatic
+# count on decoding-like shapes (few query tiles, long kL); both head dims and
+# 16-bit types, ragged qL and kL, GQA, bool and additive masks.
 SPLIT_KV = [
     (S("splitkv_bf16_d128_gqa", 1, 4, 1, 130, 3000, 128, "bf16", seed=101), 5),
     (S("splitkv_f16_d64_auto", 2, 2, 2, 64, 5000, 64, "f16", seed=102), 0),
     (S("splitkv_bf16_d128_causal", 1, 2, 1, 1000, 1000, 128, "bf16", causal=True, seed=103), 3),
     (S("splitkv_bf16_d64_beyond_blocks", 1, 2, 2, 100, 300, 64, "bf16", seed=104), 64),
     (S("splitkv_f16_d128_causal_kl_longer", 1, 4, 2, 200, 2500, 128, "f16", causal=True, seed=105), 4),
+    (S("splitkv_bf16_d128_bool_mask", 1, 2, 2, 130, 2000, 128, "bf16", mask_kind=W.MASK_BOOL, seed=106), 0),
+    (S("splitkv_f16_d64_additive_ragged", 1, 2, 1, 300, 1801, 64, "f16", mask_kind=W.MASK_ADDITIVE, seed=107), 5),
 ]
 
 
@@ -138,8 +140,10 @@ def test_split_kv(w, splits):
     try:
         q, k, v, m = W.make_inputs(w)
         qd = q.cuda()
+        md = None if m is None else m.cuda()
         args = fa.make_args(qd, k.cuda(), v.cuda(), torch.empty_like(qd),
-                            torch.empty((w.B, w.H_q, w.qL), device="cuda"), scale=w.sm_scale, causal=w.causal)
+                            torch.empty((w.B, w.H_q, w.qL), device="cuda"), scale=w.sm_scale, causal=w.causal,
+                            mask=md, mask_kind=None if md is None else w.mask_kind)
         assert fa.fa_fwd_workspace_bytes(args) > 0  # the split plan applies
         _run_small(w, qkv=(q, k, v), mask=m)
     finally:
